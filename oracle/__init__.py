@@ -1,0 +1,13 @@
+"""CPU oracle (test infrastructure only).
+
+The oracle is the plain fp64 statement of the denoise step used to check the
+CUDA library.  Only tests/, the package smoke check and the benchmark's
+CPU-baseline leg may import it; the product path must never depend on it.
+"""
+from .bd_oracle import (MASK, block_mask, block_attention, current_block_attention,
+                        confidence, commit, denoise_step, decode_block,
+                        paged_read, append_block)
+
+__all__ = ["MASK", "block_mask", "block_attention", "current_block_attention",
+           "confidence", "commit", "denoise_step", "decode_block",
+           "paged_read", "append_block"]

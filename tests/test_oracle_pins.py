@@ -1,0 +1,282 @@
+"""Pins of the CPU oracle to facts fixed outside it.
+
+Each test ties one oracle function to something other than itself: a library
+routine on a special case the block mask reduces to, a closed form, an
+invariant the pages state, or a hand-worked example (tests/golden/).
+Sources: "Rethinking Document OCR as Inverse Rendering via Diffusion Decoding"
+(paper.rainbus.top summary), method steps 3-4 and the novelty paragraph;
+"MinerU-Diffusion reads documents with diffusion decoding instead of left to
+right", section "The idea: OCR as inverse rendering".
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+from scipy.special import logsumexp
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _sdpa(q, k, v, mask=None, causal=False):
+    """torch's fp64 CPU scaled_dot_product_attention on [S, H, D] inputs."""
+    group = q.shape[1] // k.shape[1]
+    qt = torch.from_numpy(q).permute(1, 0, 2)
+    kt = torch.from_numpy(k).repeat_interleave(group, dim=1).permute(1, 0, 2)
+    vt = torch.from_numpy(v).repeat_interleave(group, dim=1).permute(1, 0, 2)
+    m = None if mask is None else torch.from_numpy(mask)
+    o = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=m, is_causal=causal)
+    return o.permute(1, 0, 2).numpy()
+
+
+def _qkv(rng, S, Hq, Hkv, D):
+    return (rng.standard_normal((S, Hq, D)), rng.standard_normal((S, Hkv, D)),
+            rng.standard_normal((S, Hkv, D)))
+
+
+# --- attention ------------------------------------------------------------
+def test_block_size_one_is_causal_attention():
+    # one token per block: the mask is lower-triangular, i.e. AR decoding
+    rng = np.random.default_rng(1)
+    q, k, v = _qkv(rng, 13, 4, 2, 8)
+    got = oracle.block_attention(q, k, v, np.arange(13), np.arange(13))
+    np.testing.assert_allclose(got, _sdpa(q, k, v, causal=True), rtol=1e-12, atol=1e-12)
+
+
+def test_single_block_is_full_bidirectional_attention():
+    rng = np.random.default_rng(2)
+    q, k, v = _qkv(rng, 11, 6, 3, 5)
+    got = oracle.block_attention(q, k, v, np.zeros(11, int), np.arange(11))
+    np.testing.assert_allclose(got, _sdpa(q, k, v), rtol=1e-12, atol=1e-12)
+
+
+def test_prefix_and_blocks_match_boundary_mask():
+    # mask built a second way: i sees j iff j < end of i's block
+    rng = np.random.default_rng(3)
+    P, L, nb = 5, 3, 3
+    S = P + L * nb
+    q, k, v = _qkv(rng, S, 4, 1, 6)
+    block_id = np.array([0] * P + [1 + (j - P) // L for j in range(P, S)])
+    end = np.array([P if i < P else P + L * ((i - P) // L + 1) for i in range(S)])
+    mask = np.arange(S)[None, :] < end[:, None]
+    got = oracle.block_attention(q, k, v, block_id, np.arange(S))
+    np.testing.assert_allclose(got, _sdpa(q, k, v, mask=mask), rtol=1e-12, atol=1e-12)
+
+
+def test_zero_query_averages_exactly_the_visible_values():
+    # q = 0 makes the softmax uniform over the visible keys, so each output is
+    # the mean of v over the visible set; v_j = 2^j identifies that set.
+    P, L, nb = 3, 2, 3
+    S = P + L * nb
+    block_id = np.array([0] * P + [1 + (j - P) // L for j in range(P, S)])
+    q = np.zeros((S, 1, 1))
+    k = np.random.default_rng(4).standard_normal((S, 1, 1))
+    v = (2.0 ** np.arange(S)).reshape(S, 1, 1)
+    got = oracle.block_attention(q, k, v, block_id, np.arange(S))[:, 0, 0]
+    for i in range(S):
+        last = P - 1 if i < P else P + L * ((i - P) // L + 1) - 1
+        visible = 2.0 ** np.arange(last + 1)
+        assert got[i] == pytest.approx(visible.mean(), rel=1e-14)
+
+
+def test_future_blocks_do_not_change_outputs():
+    rng = np.random.default_rng(5)
+    P, L, nb = 4, 4, 3
+    S = P + L * nb
+    q, k, v = _qkv(rng, S, 4, 2, 8)
+    block_id = np.array([0] * P + [1 + (j - P) // L for j in range(P, S)])
+    rows = np.arange(P + L, P + 2 * L)                      # block 2
+    ref = oracle.block_attention(q, k, v, block_id, rows)
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    fut = slice(P + 2 * L, S)                               # block 3
+    q2[fut] = rng.standard_normal(q2[fut].shape) * 50
+    k2[fut] = rng.standard_normal(k2[fut].shape) * 50
+    v2[fut] = rng.standard_normal(v2[fut].shape) * 50
+    got = oracle.block_attention(q2, k2, v2, block_id, rows)
+    assert np.array_equal(got, ref)
+
+
+def test_current_block_attention_is_block_attention_over_cache():
+    rng = np.random.default_rng(6)
+    C, L = 7, 4
+    q, k, v = _qkv(rng, C + L, 4, 2, 8)
+    got = oracle.current_block_attention(q[C:], k[:C], v[:C], k[C:], v[C:])
+    block_id = np.array([0] * C + [1] * L)
+    mask = block_id[None, :] <= block_id[:, None]
+    ref = _sdpa(q, k, v, mask=mask)[C:]
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+# --- confidence -----------------------------------------------------------
+def test_two_word_vocab_closed_form():
+    x = np.array([-7.0, -0.3, 0.0, 0.25, 4.0])
+    h = x[:, None]
+    W = np.array([[0.0], [1.0]])
+    c = oracle.confidence(h, W)
+    np.testing.assert_allclose(c["p_max"], 1.0 / (1.0 + np.exp(-np.abs(x))), rtol=1e-15)
+    assert c["argmax"].tolist() == [0, 0, 0, 1, 1]      # x = 0 ties -> lowest id
+
+
+def test_confidence_matches_logsumexp():
+    rng = np.random.default_rng(7)
+    h = rng.standard_normal((9, 16))
+    W = rng.standard_normal((300, 16)) * 0.7
+    c = oracle.confidence(h, W, row_chunk=4)
+    l = h @ W.T
+    np.testing.assert_allclose(c["p_max"], np.exp(l.max(1) - logsumexp(l, axis=1)), rtol=1e-12)
+    assert np.array_equal(c["argmax"], l.argmax(1))
+    srt = np.sort(l, axis=1)
+    np.testing.assert_allclose(c["top2_logit_gap"], srt[:, -1] - srt[:, -2], rtol=1e-12)
+
+
+def test_argmax_ties_take_lowest_id():
+    rng = np.random.default_rng(8)
+    W = rng.standard_normal((50, 8))
+    W[31] = W[12]                                           # exact duplicate rows
+    h = 20.0 * W[12][None, :]
+    c = oracle.confidence(h, W)
+    assert c["argmax"][0] == 12
+    assert c["top2_logit_gap"][0] == 0.0
+
+
+def test_uniform_logits_give_one_over_v():
+    c = oracle.confidence(np.zeros((2, 4)), np.ones((37, 4)))
+    np.testing.assert_allclose(c["p_max"], 1.0 / 37, rtol=1e-15)
+    assert c["argmax"].tolist() == [0, 0]
+
+
+def test_strong_planted_row_is_recovered():
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    w = wl.WORKLOADS["tiny_fp32"]
+    W = wl.lm_head(w)
+    h, t = wl.planted_hidden(w, W, 0, steps=1, a_max=1e-9)   # noise only
+    h_big, _ = wl.planted_hidden(w, W, 0, steps=1)
+    # replace the amplitude by a large one: a * W[t]/|W[t]| + noise, a = 200
+    dirs = W[t[0]].astype(np.float64)
+    dirs /= np.linalg.norm(dirs, axis=1, keepdims=True)
+    hp = h[0, 0].astype(np.float64) + 200.0 * dirs
+    c = oracle.confidence(hp, W)
+    assert np.array_equal(c["argmax"], t[0])
+    assert (c["p_max"] > 0.99).all()
+
+
+# --- commit ---------------------------------------------------------------
+def test_golden_hand_worked_commit():
+    with open(os.path.join(HERE, "golden", "tiny_commit_v2.json")) as f:
+        g = json.load(f)
+    W = np.array(g["W"])
+    h = np.array(g["h_steps"])
+    tokens, steps, trace = oracle.decode_block(h, W, g["threshold"])
+    assert steps.tolist() == g["expected_steps"]
+    assert [t.tolist() for t in trace] == g["expected_tokens_after_step"]
+    _, p_max, *_ = oracle.denoise_step(np.full((1, 4), -1), h[0], W, g["threshold"])
+    np.testing.assert_allclose(p_max[0], g["expected_p_max_step0"], rtol=1e-14)
+
+
+def _random_step_inputs(rng, B=3, L=8, V=20, H=6, scale=3.0):
+    return rng.standard_normal((L, B, L, H)) * scale, rng.standard_normal((V, H))
+
+
+def test_threshold_zero_commits_everything_in_one_step():
+    rng = np.random.default_rng(9)
+    h, W = _random_step_inputs(rng)
+    tokens, steps, trace = oracle.decode_block(h, W, 0.0)
+    assert steps.tolist() == [1, 1, 1] and len(trace) == 1
+    assert (tokens >= 0).all()
+
+
+def test_threshold_above_one_commits_exactly_one_per_step():
+    rng = np.random.default_rng(10)
+    h, W = _random_step_inputs(rng)
+    tokens, steps, trace = oracle.decode_block(h, W, 1.5)
+    assert steps.tolist() == [8, 8, 8]
+    prev = np.full((3, 8), -1)
+    for t in trace:
+        assert ((t != -1).sum(1) - (prev != -1).sum(1)).tolist() == [1, 1, 1]
+        prev = t
+
+
+def test_commit_rule_properties_random():
+    # the rule is characterised by: commits only masked positions; commits
+    # every masked position with p >= T; if none reaches T, commits exactly the
+    # most confident one (lowest position on ties); leaves the rest unchanged.
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        B, L = 2, int(rng.integers(1, 7))
+        tokens = np.where(rng.random((B, L)) < 0.6, -1, rng.integers(0, 9, (B, L)))
+        p = np.round(rng.random((B, L)), 1)                  # many exact ties
+        a = rng.integers(0, 9, (B, L))
+        T = float(rng.choice([0.0, 0.3, 0.5, 0.9, 1.01]))
+        new, chosen = oracle.commit(tokens, p, a, T)
+        for b in range(B):
+            masked = tokens[b] == -1
+            assert not chosen[b][~masked].any()
+            assert np.array_equal(new[b][~masked], tokens[b][~masked])
+            assert np.array_equal(new[b][chosen[b]], a[b][chosen[b]])
+            assert np.array_equal(new[b][masked & ~chosen[b]], tokens[b][masked & ~chosen[b]])
+            hi = masked & (p[b] >= T)
+            if hi.any():
+                assert np.array_equal(chosen[b], hi)
+            elif masked.any():
+                assert chosen[b].sum() == 1
+                i = int(np.nonzero(chosen[b])[0][0])
+                best = p[b][masked].max()
+                assert p[b, i] == best
+                assert i == int(np.nonzero(masked & (p[b] == best))[0][0])
+            else:
+                assert not chosen[b].any()
+
+
+def test_decode_invariants():
+    rng = np.random.default_rng(12)
+    h, W = _random_step_inputs(rng, scale=1.2)
+    tokens, steps, trace = oracle.decode_block(h, W, 0.6)
+    assert ((steps >= 1) & (steps <= 8)).all()
+    for a, b in zip(trace[:-1], trace[1:]):
+        done = a != -1
+        assert np.array_equal(a[done], b[done])             # never revised
+        assert (b != -1).sum() > (a != -1).sum()             # progress each step
+
+
+def test_literal_planted_spec_never_reaches_half():
+    # a ~ U(0,12), W ~ N(0,0.02): correct-token logit <= 12*0.02*sqrt(H) ~ 5.4
+    # at H=512 against V-1 noise logits, so p_max stays far below 0.5 and
+    # every step commits exactly one position through the fallback.
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    w = wl.WORKLOADS["tiny_fp32"]
+    W = wl.lm_head(w)
+    h, _ = wl.planted_hidden(w, W, 0)
+    tokens, steps, trace = oracle.decode_block(h, W, 0.5)
+    assert steps.tolist() == [32]
+
+
+# --- paged cache ----------------------------------------------------------
+def test_paged_append_then_read_is_concatenation():
+    rng = np.random.default_rng(13)
+    B, L, Hkv, D, ps = 2, 5, 2, 3, 4
+    ctx = np.array([6, 8])                                   # seq 0 straddles a page
+    npg = 8
+    table = rng.permutation(npg).reshape(B, npg // B)
+    pool = rng.standard_normal((npg, Hkv, ps, D))
+    before = [oracle.paged_read(pool, table[b], ctx[b], ps) for b in range(B)]
+    blk = rng.standard_normal((B, L, Hkv, D))
+    pool2, ctx2 = oracle.append_block(pool, table, ctx, blk, [True, True], ps)
+    assert ctx2.tolist() == [11, 13]
+    for b in range(B):
+        got = oracle.paged_read(pool2, table[b], ctx2[b], ps)
+        assert np.array_equal(got, np.concatenate([before[b], blk[b]]))
+    pool3, ctx3 = oracle.append_block(pool, table, ctx, blk, [False, True], ps)
+    assert ctx3.tolist() == [6, 13]
+    assert np.array_equal(oracle.paged_read(pool3, table[0], 8, ps)[:6], before[0])
+
+
+def test_paged_read_follows_page_table():
+    ps = 2
+    pool = np.arange(4 * 1 * ps * 1, dtype=float).reshape(4, 1, ps, 1)
+    got = oracle.paged_read(pool, [3, 0], 4, ps)[:, 0, 0]
+    assert got.tolist() == [6.0, 7.0, 0.0, 1.0]
