@@ -1,0 +1,409 @@
+"""Benchmark: committed tokens/sec of the block-diffusion denoise loop.
+
+Workload (one GPU): SDAR-1.7B-shaped decoder layer in bf16, batch 1, prefix
+4096 (visual + prompt tokens) in a paged KV cache (64-token pages, randomly
+permuted), one block of L'=32 masked tokens, LM head 151936 x 2048 ~ N(0,0.02),
+planted hidden states h = a W[t]/|W[t]| + N(0,1) with a ~ U(0,12) redrawn per
+step, threshold T = 0.95.
+
+One bench step = one full pass of the hot path over the block: denoise steps
+(block attention + LM head/confidence/commit) until no position is masked,
+then the append of the block's K/V.  value = committed tokens / second.
+
+Arms:
+  default            the CUDA library (libbd.so) through its C ABI
+  --impl reference   the CPU oracle on the host cores (rank 0 only), the same
+                     metric on a bounded sample of the same workload
+Under torchrun with N > 1 GPUs every rank decodes its own replica of the
+workload (no collective on the data path); timing takes the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "committed tokens/sec per denoise loop"
+UNIT = "tokens/s"
+WORKLOAD = "sdar_b1"
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--check-every", type=int, default=8)
+    return ap.parse_args()
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _inputs(w, seed=0):
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    W = wl.lm_head(w, seed)
+    plen = wl.prefix_lengths(w, seed)
+    kv = [wl.prefix_kv(w, b, int(plen[b]), seed) for b in range(w.batch)]
+    q, kb, vb = wl.block_qkv(w, 0, seed)
+    h, _ = wl.planted_hidden(w, W, 0, seed)
+    return W, plen, kv, q, kb, vb, h
+
+
+def _config(w, extra=None):
+    c = {"workload": f"{w.name}: SDAR-1.7B-shaped layer, batch {w.batch}, prefix {w.prefix}, "
+                     f"block {w.block_len}, Hq {w.num_q_heads}/Hkv {w.num_kv_heads}, "
+                     f"D {w.head_dim}, LM head {w.vocab}x{w.hidden}, T={w.threshold}, "
+                     f"planted a~U(0,{w.a_max:g})",
+         "batch": w.batch, "prefix": w.prefix, "block_len": w.block_len,
+         "vocab": w.vocab, "hidden": w.hidden, "threshold": w.threshold,
+         "paged_kv": "64-token pages, permuted page table",
+         "l2": "inputs larger than L2: the 622 MB LM head is streamed every denoise step "
+               "(evicting the 17 MB KV cache between steps)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg
+# ---------------------------------------------------------------------------
+def oracle_block(w, W64, kv, q, kb, vb, h, step_lo=0, step_hi=None, tokens=None):
+    """Run denoise steps [step_lo, step_hi) of the block on the CPU oracle.
+
+    Every step runs the oracle's block attention (all sequences), confidence,
+    commit; the append runs when the block finishes.  Returns
+    (tokens, committed count, denoise steps run)."""
+    import oracle
+    B, L = w.batch, w.block_len
+    tokens = np.full((B, L), -1, np.int64) if tokens is None else tokens
+    committed, s = 0, step_lo
+    step_hi = L if step_hi is None else step_hi
+    while (tokens == -1).any() and s < step_hi:
+        for b in range(B):
+            oracle.current_block_attention(q[b], kv[b][0], kv[b][1], kb[b], vb[b])
+        new, *_ = oracle.denoise_step(tokens, h[s].astype(np.float64), W64, w.threshold)
+        committed += int((new != tokens).sum())
+        tokens = new
+        s += 1
+    if not (tokens == -1).any():
+        ps = 64
+        for b in range(B):
+            n = kv[b][0].shape[0]
+            table = np.arange((n + L + ps - 1) // ps)
+            pool = np.zeros((len(table), w.num_kv_heads, ps, w.head_dim))
+            oracle.append_block(pool, table[None], [n], kb[b:b + 1], [True], ps)
+    return tokens, committed, s - step_lo
+
+
+def cpu_baseline(w, W, kv, q, kb, vb, h, budget_s=25.0):
+    """Time the oracle on a bounded sample: whole blocks while the budget lasts."""
+    W64 = W.astype(np.float64)
+    t0 = time.perf_counter()
+    tokens_done, blocks, steps = 0, 0, 0
+    while True:
+        _, c, s = oracle_block(w, W64, kv, q, kb, vb, h)
+        tokens_done += c
+        steps += s
+        blocks += 1
+        if time.perf_counter() - t0 > budget_s / 2 or blocks >= 4:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": tokens_done / dt, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+            "sample": f"{blocks} full block(s) of {w.name} ({steps} denoise steps, "
+                      f"{tokens_done} committed tokens) in {dt:.1f} s, numpy fp64"}
+
+
+def run_reference(a):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    w = wl.WORKLOADS[WORKLOAD]
+    W, plen, kv, q, kb, vb, h = _inputs(w)
+    W64 = W.astype(np.float64)
+    chunk = 8                       # one reference step = 8 denoise steps of the block
+    state = {"tokens": None, "s": 0}
+
+    def ref_step():
+        if state["tokens"] is None or not (state["tokens"] == -1).any():
+            state["tokens"], state["s"] = None, 0
+        tok, c, n = oracle_block(w, W64, kv, q, kb, vb, h, state["s"], state["s"] + chunk,
+                                 state["tokens"])
+        state["tokens"], state["s"] = tok, state["s"] + n
+        return c
+
+    for _ in range(a.warmup):
+        ref_step()
+    t0 = time.perf_counter()
+    committed = sum(ref_step() for _ in range(a.steps))
+    dt = time.perf_counter() - t0
+    value = committed / dt
+    sample = (f"each step = {chunk} denoise steps of one {w.name} block on the fp64 oracle "
+              f"(attention, full-logit confidence, commit, append at block end)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt * 1e3 / a.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+# ---------------------------------------------------------------------------
+# CUDA leg
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def run_cuda(a):
+    import torch
+    rank, world, local = _dist()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the CUDA arm has no CPU fallback)")
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from block_diffusion_decoding_denoise_gb300 import bd, build
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    from block_diffusion_decoding_denoise_gb300.engine import DenoiseEngine, PagedCache
+    if not os.path.exists(bd.LIB_PATH):
+        build.build()
+    bd.load()
+
+    w = wl.WORKLOADS[WORKLOAD]
+    W, plen, kv, q, kb, vb, h = _inputs(w)
+    table, npg = wl.page_tables(w, plen + w.block_len)
+    cache = PagedCache(npg, w.num_kv_heads, w.head_dim, torch.bfloat16, table)
+    for b in range(w.batch):
+        cache.load_prefix(b, torch.from_numpy(kv[b][0]), torch.from_numpy(kv[b][1]))
+    Wd = torch.from_numpy(W).to("cuda", torch.bfloat16)
+    qd = torch.from_numpy(q).to("cuda", torch.bfloat16)
+    kbd = torch.from_numpy(kb).to("cuda", torch.bfloat16)
+    vbd = torch.from_numpy(vb).to("cuda", torch.bfloat16)
+    hd = torch.from_numpy(h).to("cuda", torch.bfloat16)
+    max_ctx = int(plen.max()) + w.block_len
+    eng = DenoiseEngine(Wd, cache, plen, batch=w.batch, block_len=w.block_len,
+                        num_q_heads=w.num_q_heads, threshold=w.threshold, max_ctx=max_ctx)
+    ctx0 = eng.ctx_len.clone()
+    stream = torch.cuda.current_stream()
+
+    # per-call events around bd_confidence_commit (the dominant call)
+    conf_events = []
+    orig_step = eng.step
+
+    def timed_step(hh, qq, kk, vv, ncom=None, layer=0):
+        bd.bd_block_attention(eng.caches[layer].kv, eng.ctx_len, eng.tokens, qq, kk, vv,
+                              eng.attn_out, eng.attn_ws, eng.max_ctx, dev_status=eng.dev_status)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        bd.bd_confidence_commit(hh, eng.W, eng.T, eng.tokens, eng.p_max, eng.argmax,
+                                eng.n_committed[0] if ncom is None else ncom, eng.n_masked,
+                                eng.conf_ws, dev_status=eng.dev_status)
+        e1.record(stream)
+        conf_events.append((e0, e1))
+
+    def block():
+        eng.ctx_len.copy_(ctx0)
+        return eng.decode_block(hd, qd, kbd, vbd, check_every=a.check_every)
+
+    for _ in range(max(3, a.warmup)):
+        block()
+    torch.cuda.synchronize()
+    eng.check_status()
+
+    # timed region (device-resident inputs)
+    eng.step = timed_step
+    steps_issued = 0
+    l0 = bd.bd_kernel_launches()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(a.steps):
+            steps_issued += block()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = bd.bd_kernel_launches() - l0
+    ms = t0.elapsed_time(t1)
+    eng.step = orig_step
+    eng.check_status()
+    committed_per_block = int((eng.tokens != -1).sum().item())
+    tokens_total = committed_per_block * a.steps
+    steps_per_seq = eng.steps_per_sequence()
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = tokens_total * world / (ms / 1e3)
+
+    # roofline of the dominant call: bd_confidence_commit
+    conf_ms = [e0.elapsed_time(e1) for e0, e1 in conf_events]
+    # algorithmic bytes per call: W once, plus the masked rows of h (read) and
+    # the per-position outputs; masked rows per step follow the commit trace
+    masked_rows = []
+    rem = w.batch * w.block_len
+    nc = eng.n_committed.cpu().numpy()
+    for s in range(nc.shape[0]):
+        if rem <= 0:
+            break
+        masked_rows.append(rem)
+        rem -= int(nc[s].sum())
+    calls_per_block = len(conf_events) // a.steps
+    rows_per_call = [masked_rows[i % calls_per_block] if i % calls_per_block < len(masked_rows)
+                     else 0 for i in range(len(conf_events))]
+    bytes_w = w.vocab * w.hidden * 2
+    alg = [bytes_w + r * w.hidden * 2 + w.batch * w.block_len * 12 for r in rows_per_call]
+    peak, peak_kind = _peaks()
+    active = [(b, t) for b, t, r in zip(alg, conf_ms, rows_per_call) if r > 0]
+    achieved = sum(b for b, _ in active) / (sum(t for _, t in active) / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": None,
+                "kernel": "bd_confidence_commit (masked-row compaction + LM head with online "
+                          "max/sum-exp/argmax + commit)",
+                "peak_source": f"{peak_kind} hbm_gbs"}
+
+    # end to end: host buffers, copies inside the timed region
+    h_host = torch.from_numpy(h).to(torch.bfloat16).pin_memory()
+    q_host = torch.from_numpy(q).to(torch.bfloat16).pin_memory()
+    k_host = torch.from_numpy(kb).to(torch.bfloat16).pin_memory()
+    v_host = torch.from_numpy(vb).to(torch.bfloat16).pin_memory()
+    tok_host = torch.empty(w.batch, w.block_len, dtype=torch.int32).pin_memory()
+    h_in = torch.empty_like(hd)
+    q_in, k_in, v_in = torch.empty_like(qd), torch.empty_like(kbd), torch.empty_like(vbd)
+    h2d = sum(t.numel() * t.element_size() for t in (h_host, q_host, k_host, v_host))
+    d2h = tok_host.numel() * tok_host.element_size()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(a.steps):
+        h_in.copy_(h_host, non_blocking=True)
+        q_in.copy_(q_host, non_blocking=True)
+        k_in.copy_(k_host, non_blocking=True)
+        v_in.copy_(v_host, non_blocking=True)
+        eng.ctx_len.copy_(ctx0)
+        eng.decode_block(h_in, q_in, k_in, v_in, check_every=a.check_every)
+        tok_host.copy_(eng.tokens, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e = {"value": committed_per_block * a.steps * world / (e2e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        return
+    cpu = None
+    if not a.no_cpu_baseline:
+        cpu = cpu_baseline(w, W, kv, q, kb, vb, h)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": max(3, a.warmup), "ms_per_step": ms / a.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": _config(w, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                              "denoise_steps_per_block": [int(x) for x in steps_per_seq],
+                              "denoise_steps_issued": steps_issued // a.steps,
+                              "check_every": a.check_every}),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(launches), "clocks": clk.summary(),
+        "conf_call_us_mean": 1e3 * statistics.mean(conf_ms) if conf_ms else None,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    a = _args()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_cuda(a)
+
+
+if __name__ == "__main__":
+    main()

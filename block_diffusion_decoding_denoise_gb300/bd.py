@@ -1,0 +1,182 @@
+"""ctypes binding of libbd.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of its own: it checks that tensors live on the GPU with the right
+dtype and layout, passes their device pointers and the current CUDA stream,
+and raises BDError on a non-OK status.  Torch is used for device memory and
+streams only.  There is no CPU fallback: if libbd.so has not been built the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import c_float, c_int32, c_size_t, c_void_p
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libbd.so")
+
+BD_F32, BD_BF16 = 0, 1
+BD_MASK = -1
+BD_PAGE_SIZE = 64
+STATUS = {0: "BD_OK", 1: "BD_ERR_INVALID_ARG", 2: "BD_ERR_UNSUPPORTED", 3: "BD_ERR_CUDA",
+          4: "BD_ERR_DEVICE_CHECK", 5: "BD_ERR_TIMEOUT", 6: "BD_ERR_WORKSPACE"}
+
+# every symbol include/bd.h declares
+EXPORTS = ("bd_block_attention_workspace", "bd_block_attention",
+           "bd_confidence_commit_workspace", "bd_confidence_commit",
+           "bd_append_block_kv", "bd_status_string", "bd_version", "bd_kernel_launches")
+
+
+class BDError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+        self.status = status
+
+
+class PagedKV(ctypes.Structure):
+    """Mirror of bd_paged_kv."""
+    _fields_ = [("dtype", c_int32), ("num_pages", c_int32), ("page_size", c_int32),
+                ("num_kv_heads", c_int32), ("head_dim", c_int32),
+                ("max_pages_per_seq", c_int32), ("k_pool", c_void_p),
+                ("v_pool", c_void_p), ("page_table", c_void_p)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libbd.so once; raise if it is missing (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is not built; run "
+                               "`python -m block_diffusion_decoding_denoise_gb300.build`")
+        lib = ctypes.CDLL(path)
+        P = ctypes.POINTER(PagedKV)
+        sig = {
+            "bd_block_attention_workspace": (c_size_t, [c_int32] * 6),
+            "bd_block_attention": (c_int32, [P, c_void_p, c_void_p, c_int32, c_int32, c_int32,
+                                             c_int32, c_void_p, c_void_p, c_void_p, c_float,
+                                             c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
+            "bd_confidence_commit_workspace": (c_size_t, [c_int32] * 5),
+            "bd_confidence_commit": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_int32,
+                                               c_void_p, c_void_p, c_float, c_void_p, c_void_p,
+                                               c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                               c_void_p, c_void_p]),
+            "bd_append_block_kv": (c_int32, [P, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                             c_void_p, c_void_p, c_void_p]),
+            "bd_status_string": (ctypes.c_char_p, [c_int32]),
+            "bd_version": (c_int32, []),
+            "bd_kernel_launches": (ctypes.c_uint64, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return BD_F32
+    if t.dtype == torch.bfloat16:
+        return BD_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise BDError(fn, status)
+
+
+def paged_kv(k_pool: torch.Tensor, v_pool: torch.Tensor, page_table: torch.Tensor) -> PagedKV:
+    """bd_paged_kv for pools [num_pages, Hkv, 64, D] and a [B, max_pages] int32 table."""
+    if k_pool.shape != v_pool.shape or k_pool.dim() != 4 or k_pool.dtype != v_pool.dtype:
+        raise ValueError("k_pool and v_pool must both be [num_pages, Hkv, page_size, D]")
+    if page_table.dim() != 2:
+        raise ValueError("page_table must be [batch, max_pages_per_seq]")
+    return PagedKV(_dtype_code(k_pool), k_pool.shape[0], k_pool.shape[2], k_pool.shape[1],
+                   k_pool.shape[3], page_table.shape[1], _ptr(k_pool, name="k_pool"),
+                   _ptr(v_pool, name="v_pool"), _ptr(page_table, torch.int32, "page_table"))
+
+
+def bd_block_attention_workspace(batch, block_len, num_q_heads, num_kv_heads, head_dim,
+                                 max_ctx) -> int:
+    return int(load().bd_block_attention_workspace(batch, block_len, num_q_heads, num_kv_heads,
+                                                   head_dim, max_ctx))
+
+
+def bd_block_attention(kv: PagedKV, ctx_len, tokens, q, k_blk, v_blk, out, ws, max_ctx,
+                       softmax_scale=None, dev_status=None, stream=None):
+    B, L, Hq, D = q.shape
+    scale = D ** -0.5 if softmax_scale is None else softmax_scale
+    st = load().bd_block_attention(
+        ctypes.byref(kv), _ptr(ctx_len, torch.int32, "ctx_len"),
+        _ptr(tokens, torch.int32, "tokens"), B, L, Hq, max_ctx, _ptr(q, name="q"),
+        _ptr(k_blk, name="k_blk"), _ptr(v_blk, name="v_blk"), scale, _ptr(out, name="out"),
+        _ptr(ws, name="ws") if ws is not None and ws.numel() else None,
+        0 if ws is None else ws.numel() * ws.element_size(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("bd_block_attention", st)
+
+
+def bd_confidence_commit_workspace(dtype_code, batch, block_len, hidden, vocab) -> int:
+    return int(load().bd_confidence_commit_workspace(dtype_code, batch, block_len, hidden, vocab))
+
+
+def bd_confidence_commit(hidden_states, lm_head, threshold, tokens, p_max, argmax,
+                         n_committed, n_masked, ws, dev_status=None, stream=None):
+    B, L, H = hidden_states.shape
+    V = lm_head.shape[0]
+    if lm_head.shape[1] != H or lm_head.dtype != hidden_states.dtype:
+        raise ValueError("lm_head must be [vocab, hidden] with the hidden states' dtype")
+    st = load().bd_confidence_commit(
+        _dtype_code(hidden_states), B, L, H, V, _ptr(hidden_states, name="hidden_states"),
+        _ptr(lm_head, name="lm_head"), float(threshold), _ptr(tokens, torch.int32, "tokens"),
+        _ptr(p_max, torch.float32, "p_max"), _ptr(argmax, torch.int32, "argmax"),
+        _ptr(n_committed, torch.int32, "n_committed"), _ptr(n_masked, torch.int32, "n_masked"),
+        _ptr(ws, name="ws"), ws.numel() * ws.element_size(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("bd_confidence_commit", st)
+
+
+def bd_append_block_kv(kv: PagedKV, k_blk, v_blk, ctx_len, n_masked=None, dev_status=None,
+                       stream=None):
+    B, L = k_blk.shape[0], k_blk.shape[1]
+    st = load().bd_append_block_kv(
+        ctypes.byref(kv), B, L, _ptr(k_blk, name="k_blk"), _ptr(v_blk, name="v_blk"),
+        _ptr(ctx_len, torch.int32, "ctx_len"), _ptr(n_masked, torch.int32, "n_masked"),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("bd_append_block_kv", st)
+
+
+def bd_status_string(status: int) -> str:
+    return load().bd_status_string(status).decode()
+
+
+def bd_version() -> int:
+    return int(load().bd_version())
+
+
+def bd_kernel_launches() -> int:
+    return int(load().bd_kernel_launches())

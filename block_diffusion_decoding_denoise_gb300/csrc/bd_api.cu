@@ -1,0 +1,203 @@
+// Host entry points of libbd: block attention dispatch, KV append, status.
+#include <math.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "bd_attention.cuh"
+#include "bd_common.cuh"
+
+namespace bd {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+static int num_sms() {
+  static int cached = 0;
+  if (cached == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      cached = n;
+    else
+      return 148;
+  }
+  return cached;
+}
+
+// KV split: enough CTAs to cover every SM about twice, page-aligned slices.
+static void choose_split(int batch, int hkv, int block_len, int max_ctx, int *num_splits,
+                         int *split_keys) {
+  const int nkeys = max_ctx + block_len;
+  const int max_splits = std::max(1, (nkeys + BD_PAGE_SIZE - 1) / BD_PAGE_SIZE);
+  const int want = std::max(1, (2 * num_sms() + batch * hkv - 1) / (batch * hkv));
+  int s = std::min(want, max_splits);
+  int keys = (nkeys + s - 1) / s;
+  keys = (keys + BD_PAGE_SIZE - 1) / BD_PAGE_SIZE * BD_PAGE_SIZE;
+  *split_keys = keys;
+  *num_splits = (nkeys + keys - 1) / keys;
+}
+
+static bool attn_shape_ok(int32_t batch, int32_t block_len, int32_t hq, int32_t hkv, int32_t d,
+                          int32_t max_ctx) {
+  if (batch < 1 || block_len < 1 || block_len > 32 || hq < 1 || hkv < 1 || hq % hkv) return false;
+  if (d != 64 && d != 128) return false;
+  if (block_len * (hq / hkv) > 128) return false;
+  if (max_ctx < 0 || (int64_t)max_ctx + block_len > (1 << 30)) return false;
+  return true;
+}
+
+static size_t attn_ws_bytes(int batch, int block_len, int hq, int hkv, int d, int max_ctx,
+                            int *num_splits, int *split_keys, size_t *off_ml) {
+  choose_split(batch, hkv, block_len, max_ctx, num_splits, split_keys);
+  if (*num_splits == 1) {
+    *off_ml = 0;
+    return 0;
+  }
+  const size_t rows = (size_t)batch * hkv * (*num_splits) * block_len * (hq / hkv);
+  *off_ml = align_up(rows * d * sizeof(float), 256);
+  return *off_ml + align_up(rows * 2 * sizeof(float), 256);
+}
+
+// ---------------------------------------------------------------------------
+// append: one CTA per sequence, 16-byte vector copies
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) append_kv_kernel(bd_paged_kv kv, int block_len,
+                                                        size_t elem_bytes, const char *k_blk,
+                                                        const char *v_blk, int32_t *ctx_len,
+                                                        const int32_t *n_masked,
+                                                        int32_t *dev_status) {
+  const int b = blockIdx.x;
+  if (n_masked && n_masked[b] != 0) return;
+  const int ctx = ctx_len[b];
+  const size_t row_bytes = (size_t)kv.head_dim * elem_bytes;           // one head, one token
+  const int vec_per_row = (int)(row_bytes / 16);
+  const int total = block_len * kv.num_kv_heads * vec_per_row;
+  if (ctx < 0 || ctx + block_len > kv.max_pages_per_seq * kv.page_size) {
+    if (threadIdx.x == 0) flag_error(dev_status, BD_ERR_DEVICE_CHECK);
+    return;
+  }
+  for (int e = threadIdx.x; e < total; e += blockDim.x) {
+    const int c = e % vec_per_row;
+    const int g = (e / vec_per_row) % kv.num_kv_heads;
+    const int i = e / (vec_per_row * kv.num_kv_heads);
+    const int pos = ctx + i;
+    const int pg = kv.page_table[(size_t)b * kv.max_pages_per_seq + pos / kv.page_size];
+    if (pg < 0 || pg >= kv.num_pages) {
+      flag_error(dev_status, BD_ERR_DEVICE_CHECK);
+      continue;
+    }
+    const size_t src = ((((size_t)b * block_len + i) * kv.num_kv_heads + g) * row_bytes) + c * 16;
+    const size_t dst = ((((size_t)pg * kv.num_kv_heads + g) * kv.page_size + pos % kv.page_size) *
+                        row_bytes) + c * 16;
+    *reinterpret_cast<int4 *>(static_cast<char *>(kv.k_pool) + dst) =
+        *reinterpret_cast<const int4 *>(k_blk + src);
+    *reinterpret_cast<int4 *>(static_cast<char *>(kv.v_pool) + dst) =
+        *reinterpret_cast<const int4 *>(v_blk + src);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) ctx_len[b] = ctx + block_len;
+}
+
+static bool kv_ok(const bd_paged_kv *kv) {
+  if (!kv || !kv->k_pool || !kv->v_pool || !kv->page_table) return false;
+  if (kv->dtype != BD_F32 && kv->dtype != BD_BF16) return false;
+  if (kv->page_size != BD_PAGE_SIZE || kv->num_pages < 1 || kv->num_kv_heads < 1) return false;
+  if (kv->max_pages_per_seq < 1) return false;
+  if (kv->head_dim != 64 && kv->head_dim != 128) return false;
+  if ((reinterpret_cast<uintptr_t>(kv->k_pool) | reinterpret_cast<uintptr_t>(kv->v_pool)) & 15)
+    return false;
+  return true;
+}
+
+}  // namespace bd
+
+using namespace bd;
+
+BD_API size_t bd_block_attention_workspace(int32_t batch, int32_t block_len, int32_t num_q_heads,
+                                           int32_t num_kv_heads, int32_t head_dim,
+                                           int32_t max_ctx) {
+  if (!attn_shape_ok(batch, block_len, num_q_heads, num_kv_heads, head_dim, max_ctx)) return 0;
+  int ns, sk;
+  size_t off_ml;
+  return attn_ws_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim, max_ctx, &ns, &sk,
+                       &off_ml);
+}
+
+BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_len,
+                                    const int32_t *tokens, int32_t batch, int32_t block_len,
+                                    int32_t num_q_heads, int32_t max_ctx, const void *q,
+                                    const void *k_blk, const void *v_blk, float softmax_scale,
+                                    void *out, void *ws, size_t ws_bytes, int32_t *dev_status,
+                                    void *stream) {
+  if (!kv_ok(kv) || !ctx_len || !q || !k_blk || !v_blk || !out) return BD_ERR_INVALID_ARG;
+  if (!attn_shape_ok(batch, block_len, num_q_heads, kv->num_kv_heads, kv->head_dim, max_ctx))
+    return BD_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || isinf(softmax_scale)) return BD_ERR_INVALID_ARG;
+  AttnParams p{};
+  p.dtype = kv->dtype;
+  p.batch = batch;
+  p.block_len = block_len;
+  p.hq = num_q_heads;
+  p.hkv = kv->num_kv_heads;
+  p.head_dim = kv->head_dim;
+  p.num_pages = kv->num_pages;
+  p.page_size = kv->page_size;
+  p.max_pages = kv->max_pages_per_seq;
+  p.max_ctx = max_ctx;
+  p.scale = softmax_scale;
+  p.q = q;
+  p.k_blk = k_blk;
+  p.v_blk = v_blk;
+  p.k_pool = kv->k_pool;
+  p.v_pool = kv->v_pool;
+  p.page_table = kv->page_table;
+  p.ctx_len = ctx_len;
+  p.tokens = tokens;
+  p.out = out;
+  p.dev_status = dev_status;
+  size_t off_ml;
+  const size_t need = attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx,
+                                    &p.num_splits, &p.split_keys, &off_ml);
+  if (need > 0) {
+    if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return BD_ERR_WORKSPACE;
+    p.part_o = static_cast<float *>(ws);
+    p.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + off_ml);
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bd_status s = attention_tc(p, st);
+  if (s != BD_ERR_UNSUPPORTED) return s;
+  return attention_simt(p, st);
+}
+
+BD_API bd_status bd_append_block_kv(const bd_paged_kv *kv, int32_t batch, int32_t block_len,
+                                    const void *k_blk, const void *v_blk, int32_t *ctx_len,
+                                    const int32_t *n_masked, int32_t *dev_status, void *stream) {
+  if (!kv_ok(kv) || !k_blk || !v_blk || !ctx_len) return BD_ERR_INVALID_ARG;
+  if (batch < 1 || block_len < 1 || block_len > 1024) return BD_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_blk) | reinterpret_cast<uintptr_t>(v_blk)) & 15)
+    return BD_ERR_INVALID_ARG;
+  const size_t elem = kv->dtype == BD_BF16 ? 2 : 4;
+  append_kv_kernel<<<batch, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      *kv, block_len, elem, static_cast<const char *>(k_blk), static_cast<const char *>(v_blk),
+      ctx_len, n_masked, dev_status);
+  count_launches(1);
+  return launch_status();
+}
+
+BD_API const char *bd_status_string(bd_status s) {
+  switch (s) {
+    case BD_OK: return "BD_OK";
+    case BD_ERR_INVALID_ARG: return "BD_ERR_INVALID_ARG";
+    case BD_ERR_UNSUPPORTED: return "BD_ERR_UNSUPPORTED";
+    case BD_ERR_CUDA: return "BD_ERR_CUDA";
+    case BD_ERR_DEVICE_CHECK: return "BD_ERR_DEVICE_CHECK";
+    case BD_ERR_TIMEOUT: return "BD_ERR_TIMEOUT";
+    case BD_ERR_WORKSPACE: return "BD_ERR_WORKSPACE";
+  }
+  return "BD_ERR_UNKNOWN";
+}
+
+BD_API int32_t bd_version(void) { return 100; }
+
+BD_API uint64_t bd_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -1,0 +1,230 @@
+// Block attention over a paged KV cache: split-KV online softmax.
+//
+// "Rethinking Document OCR as Inverse Rendering via Diffusion Decoding"
+// (paper.rainbus.top summary), method step 3: a token of the current block
+// attends fully to its own block, causally to all earlier blocks and the
+// prefix, and never to later blocks.  At decode time the cache holds exactly
+// the prefix and the earlier blocks, so the rule becomes "all cached keys plus
+// all block keys".
+//
+// This file holds the generic SIMT path (fp32 or bf16 storage, fp32 math);
+// it is the fp32 path of the library.  Grid: (split, kv head, sequence).  A
+// CTA owns the R = block_len * (Hq/Hkv) query rows of one KV head and one
+// page-aligned slice of the keys; warps own 8 rows each; lanes own one key of
+// a 32-key tile for Q.K and 1/32 of head_dim for P.V.  Split partials
+// (unnormalised O, running max m, running sum l) are merged by
+// attn_combine_kernel.
+#include <math.h>
+
+#include "bd_attention.cuh"
+#include "bd_common.cuh"
+
+namespace bd {
+
+constexpr int kTileKeys = 32;
+constexpr int kRowsPerWarp = 8;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(512) attn_splitkv_simt_kernel(AttnParams p) {
+  extern __shared__ float smem[];
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int group = p.hq / p.hkv;
+  const int R = p.block_len * group;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nthreads = blockDim.x;
+
+  if (p.tokens) {  // skip sequences whose block is fully committed
+    int any = 0;
+    for (int i = 0; i < p.block_len; ++i) any |= (p.tokens[b * p.block_len + i] == BD_MASK);
+    if (!any) return;
+  }
+  const int ctx = p.ctx_len[b];
+  if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) {
+    if (split == 0 && g == 0 && threadIdx.x == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+    return;
+  }
+  const int nkeys = ctx + p.block_len;
+  const int kbeg = split * p.split_keys;
+  const int kend = min(nkeys, kbeg + p.split_keys);
+
+  float *Qs = smem;                            // [R][D]
+  float *Ks = Qs + R * D;                      // [32][D+1]
+  float *Vs = Ks + kTileKeys * (D + 1);        // [32][D]
+  const T *q = static_cast<const T *>(p.q);
+  for (int idx = threadIdx.x; idx < R * D; idx += nthreads) {
+    const int r = idx / D, d = idx % D;
+    const int i = r / group, h = g * group + r % group;
+    Qs[idx] = to_f32(q[(((size_t)b * p.block_len + i) * p.hq + h) * D + d]) * p.scale;
+  }
+
+  constexpr int DPL = D / 32;                  // head_dim elements per lane
+  float acc[kRowsPerWarp][DPL];
+  float mrow[kRowsPerWarp], lrow[kRowsPerWarp];
+#pragma unroll
+  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+    mrow[rr] = -INFINITY;
+    lrow[rr] = 0.f;
+#pragma unroll
+    for (int t = 0; t < DPL; ++t) acc[rr][t] = 0.f;
+  }
+
+  const T *kpool = static_cast<const T *>(p.k_pool);
+  const T *vpool = static_cast<const T *>(p.v_pool);
+  const T *kblk = static_cast<const T *>(p.k_blk);
+  const T *vblk = static_cast<const T *>(p.v_blk);
+
+  for (int k0 = kbeg; k0 < kend; k0 += kTileKeys) {
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < kTileKeys * D; idx += nthreads) {
+      const int j = idx / D, d = idx % D;
+      const int pos = k0 + j;
+      float kv = 0.f, vv = 0.f;
+      if (pos < kend) {
+        if (pos < ctx) {
+          const int pg = p.page_table[(size_t)b * p.max_pages + pos / p.page_size];
+          if (pg >= 0 && pg < p.num_pages) {
+            const size_t off = (((size_t)pg * p.hkv + g) * p.page_size + pos % p.page_size) * D + d;
+            kv = to_f32(kpool[off]);
+            vv = to_f32(vpool[off]);
+          } else if (d == 0) {
+            flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+          }
+        } else {
+          const size_t off = (((size_t)b * p.block_len + (pos - ctx)) * p.hkv + g) * D + d;
+          kv = to_f32(kblk[off]);
+          vv = to_f32(vblk[off]);
+        }
+      }
+      Ks[j * (D + 1) + d] = kv;
+      Vs[j * D + d] = vv;
+    }
+    __syncthreads();
+    const bool valid = (k0 + lane) < kend;
+#pragma unroll
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+      const int r = warp * kRowsPerWarp + rr;
+      if (r >= R) break;
+      const float *qr = Qs + r * D;
+      const float *kr = Ks + lane * (D + 1);
+      float s = 0.f;
+#pragma unroll 8
+      for (int d = 0; d < D; ++d) s = fmaf(qr[d], kr[d], s);
+      s = valid ? s : -INFINITY;
+      float mt = s;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+      const float mnew = fmaxf(mrow[rr], mt);
+      const float corr = __expf(mrow[rr] - mnew);   // exp(-inf) = 0 on the first tile
+      const float pj = valid ? __expf(s - mnew) : 0.f;
+      float ps = pj;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+      lrow[rr] = lrow[rr] * corr + ps;
+      mrow[rr] = mnew;
+#pragma unroll
+      for (int t = 0; t < DPL; ++t) acc[rr][t] *= corr;
+      for (int j = 0; j < kTileKeys; ++j) {
+        const float pjj = __shfl_sync(0xffffffffu, pj, j);
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) acc[rr][t] = fmaf(pjj, Vs[j * D + lane + 32 * t], acc[rr][t]);
+      }
+    }
+  }
+
+  // write: final output when there is one split, else the partial
+#pragma unroll
+  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+    const int r = warp * kRowsPerWarp + rr;
+    if (r >= R) break;
+    const int i = r / group, h = g * group + r % group;
+    if (p.num_splits == 1) {
+      T *out = static_cast<T *>(p.out);
+      const float inv = lrow[rr] > 0.f ? 1.f / lrow[rr] : 0.f;
+#pragma unroll
+      for (int t = 0; t < DPL; ++t)
+        out[(((size_t)b * p.block_len + i) * p.hq + h) * D + lane + 32 * t] =
+            from_f32<T>(acc[rr][t] * inv);
+    } else {
+      const size_t prow = (((size_t)b * p.hkv + g) * p.num_splits + split) * R + r;
+#pragma unroll
+      for (int t = 0; t < DPL; ++t) p.part_o[prow * D + lane + 32 * t] = acc[rr][t];
+      if (lane == 0) {
+        p.part_ml[prow * 2 + 0] = mrow[rr];
+        p.part_ml[prow * 2 + 1] = lrow[rr];
+      }
+    }
+  }
+}
+
+// Merge split partials: O = sum_s O_s exp(m_s - m) / sum_s l_s exp(m_s - m).
+template <typename T, int D>
+__global__ void attn_combine_kernel(AttnParams p) {
+  const int group = p.hq / p.hkv;
+  const int R = p.block_len * group;
+  const size_t total = (size_t)p.batch * p.hkv * R * D;
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const int d = e % D;
+    const int r = (e / D) % R;
+    const int g = (e / ((size_t)D * R)) % p.hkv;
+    const int b = e / ((size_t)D * R * p.hkv);
+    if (p.tokens) {
+      int any = 0;
+      for (int i = 0; i < p.block_len; ++i) any |= (p.tokens[b * p.block_len + i] == BD_MASK);
+      if (!any) continue;
+    }
+    const int ctx = p.ctx_len[b];
+    if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) continue;
+    const int nkeys = ctx + p.block_len;
+    const int used = (nkeys + p.split_keys - 1) / p.split_keys;   // splits that saw keys
+    const size_t base = (((size_t)b * p.hkv + g) * p.num_splits) * R + r;
+    float m = -INFINITY;
+    for (int s = 0; s < used; ++s) m = fmaxf(m, p.part_ml[(base + (size_t)s * R) * 2]);
+    float l = 0.f, o = 0.f;
+    for (int s = 0; s < used; ++s) {
+      const size_t pr = base + (size_t)s * R;
+      const float w = __expf(p.part_ml[pr * 2] - m);
+      l += p.part_ml[pr * 2 + 1] * w;
+      o += p.part_o[pr * D + d] * w;
+    }
+    const int i = r / group, h = g * group + r % group;
+    T *out = static_cast<T *>(p.out);
+    out[(((size_t)b * p.block_len + i) * p.hq + h) * D + d] = from_f32<T>(l > 0.f ? o / l : 0.f);
+  }
+}
+
+template <typename T, int D>
+static bd_status launch_simt(const AttnParams &p, cudaStream_t st) {
+  const int R = p.block_len * (p.hq / p.hkv);
+  const int warps = (R + kRowsPerWarp - 1) / kRowsPerWarp;
+  const size_t smem = sizeof(float) * ((size_t)R * D + kTileKeys * (D + 1) + kTileKeys * D);
+  auto kern = attn_splitkv_simt_kernel<T, D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return BD_ERR_CUDA;
+  dim3 grid(p.num_splits, p.hkv, p.batch);
+  kern<<<grid, warps * 32, smem, st>>>(p);
+  count_launches(1);
+  if (cudaGetLastError() != cudaSuccess) return BD_ERR_CUDA;
+  if (p.num_splits > 1) {
+    const size_t total = (size_t)p.batch * p.hkv * R * D;
+    const int blocks = (int)std::min<size_t>((total + 255) / 256, 4096);
+    attn_combine_kernel<T, D><<<blocks, 256, 0, st>>>(p);
+    count_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return BD_ERR_CUDA;
+  }
+  return BD_OK;
+}
+
+bd_status attention_simt(const AttnParams &p, cudaStream_t st) {
+  if (p.dtype == BD_F32) {
+    if (p.head_dim == 64) return launch_simt<float, 64>(p, st);
+    if (p.head_dim == 128) return launch_simt<float, 128>(p, st);
+  } else {
+    if (p.head_dim == 64) return launch_simt<__nv_bfloat16, 64>(p, st);
+    if (p.head_dim == 128) return launch_simt<__nv_bfloat16, 128>(p, st);
+  }
+  return BD_ERR_UNSUPPORTED;
+}
+
+}  // namespace bd

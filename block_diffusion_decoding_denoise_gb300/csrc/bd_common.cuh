@@ -1,0 +1,59 @@
+// Shared device/host helpers of libbd (CUDA, sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/bd.h"
+
+#define BD_API extern "C" __attribute__((visibility("default")))
+
+namespace bd {
+
+// First device-side error wins; the caller's status word starts at 0.
+__device__ __forceinline__ void flag_error(int32_t *dev_status, int32_t code) {
+  if (dev_status) atomicCAS(dev_status, 0, code);
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Online-softmax state of one row: running max m, running sum s of
+// exp(l - m), and the lowest index attaining m.
+struct MaxSumArg {
+  float m;
+  float s;
+  int32_t idx;
+};
+
+// Merge b into a.  Deterministic: on equal maxima the lower index wins and
+// both sums are kept.
+__device__ __forceinline__ MaxSumArg merge(MaxSumArg a, MaxSumArg b) {
+  if (b.m > a.m || (b.m == a.m && b.idx < a.idx)) {
+    MaxSumArg t = a;
+    a = b;
+    b = t;
+  }
+  // a.m >= b.m now
+  if (b.s > 0.f) a.s += b.s * __expf(b.m - a.m);
+  return a;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Launch counter behind bd_kernel_launches(); every host entry point adds
+// the number of kernels it launched.
+void count_launches(int n);
+
+inline bd_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
+
+}  // namespace bd

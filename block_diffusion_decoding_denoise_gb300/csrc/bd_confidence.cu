@@ -1,0 +1,317 @@
+// Vocabulary projection, confidence and threshold commit of one denoise step.
+//
+// "Rethinking Document OCR as Inverse Rendering via Diffusion Decoding"
+// (paper.rainbus.top summary), method step 4 (a token is confirmed once its
+// prediction confidence passes T = 0.95, otherwise it is denoised again) and
+// step 6 (greedy settings: top-k 0, temperature 1, top-p 1).  Confidence is
+// the largest softmax probability, p_max = 1 / sum_v exp(l_v - max l); the
+// token is the lowest id attaining max l.  When no masked position reaches T,
+// the most confident masked position is confirmed (lowest position on ties).
+//
+// Pipeline (one stream, no host synchronisation):
+//   conf_prep_kernel     compact the still-masked positions into a row list
+//   lmhead_*             per (producer, row) online max / sum-exp / argmax of
+//                        h . W^T over a slice of the vocabulary; logits stay
+//                        on chip (SIMT path here, tcgen05 path in
+//                        bd_lmhead_tc.cu)
+//   conf_commit_kernel   one warp per sequence: merge the partial states,
+//                        p_max, argmax, ballot over p_max >= T, fallback, write
+#include <math.h>
+
+#include <algorithm>
+
+#include "bd_confidence.cuh"
+
+namespace bd {
+
+// ---------------------------------------------------------------------------
+// masked-row compaction: one CTA, block-wide exclusive scan
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) conf_prep_kernel(const int32_t *tokens, int n,
+                                                         ConfWorkspace ws) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int pos = base + threadIdx.x;
+    const int m = (pos < n && tokens[pos] == BD_MASK) ? 1 : 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, m);
+    const int before_in_warp = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) warp_sums[warp] = __popc(bal);
+    __syncthreads();
+    int before = carry;
+    for (int w = 0; w < warp; ++w) before += warp_sums[w];
+    const int k = before + before_in_warp;
+    if (pos < n) {
+      ws.row_of[pos] = m ? k : -1;
+      if (m) ws.rows[k] = pos;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += warp_sums[w];
+      carry += tot;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *ws.count = carry;
+}
+
+// ---------------------------------------------------------------------------
+// SIMT LM head: 64 rows x 64 vocab tiles, 4x4 per thread, fp32 FMA
+// ---------------------------------------------------------------------------
+constexpr int kSimtRows = 64, kSimtVocab = 64, kSimtK = 16;
+constexpr int kSimtChunk = 512;  // vocab entries per CTA (-> one partial per chunk)
+
+template <typename T>
+__global__ void __launch_bounds__(256) lmhead_simt_kernel(ConfParams p) {
+  __shared__ float As[kSimtK][kSimtRows + 4];
+  __shared__ float Bs[kSimtK][kSimtVocab + 4];
+  __shared__ MaxSumArg state[kSimtRows];
+  const int count = *p.ws.count;
+  const int r0 = blockIdx.y * kSimtRows;
+  if (r0 >= count) return;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int v_lo = blockIdx.x * kSimtChunk;
+  const int v_hi = min(p.vocab, v_lo + kSimtChunk);
+  const T *h = static_cast<const T *>(p.h);
+  const T *w = static_cast<const T *>(p.w);
+  const int H = p.hidden;
+  if (threadIdx.x < kSimtRows) state[threadIdx.x] = MaxSumArg{-INFINITY, 0.f, 0x7fffffff};
+
+  for (int v0 = v_lo; v0 < v_hi; v0 += kSimtVocab) {
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+    for (int k0 = 0; k0 < H; k0 += kSimtK) {
+      __syncthreads();
+      for (int e = threadIdx.x; e < kSimtK * kSimtRows; e += blockDim.x) {
+        const int rr = e / kSimtK, kk = e % kSimtK;
+        const int r = r0 + rr;
+        As[kk][rr] = r < count ? to_f32(h[(size_t)p.ws.rows[r] * H + k0 + kk]) : 0.f;
+        const int v = v0 + rr;
+        Bs[kk][rr] = v < v_hi ? to_f32(w[(size_t)v * H + k0 + kk]) : 0.f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int kk = 0; kk < kSimtK; ++kk) {
+        float a[4], bv[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          a[t] = As[kk][ty * 4 + t];
+          bv[t] = Bs[kk][tx * 4 + t];
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+          for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(a[x], bv[y], acc[x][y]);
+      }
+    }
+    // epilogue: reduce each row over this tile's 64 vocab entries
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      MaxSumArg st{-INFINITY, 0.f, 0x7fffffff};
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int v = v0 + tx * 4 + y;
+        if (v < v_hi && acc[x][y] > st.m) {
+          st.m = acc[x][y];
+          st.idx = v;
+        }
+      }
+      if (st.idx != 0x7fffffff) {
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const int v = v0 + tx * 4 + y;
+          if (v < v_hi) st.s += __expf(acc[x][y] - st.m);
+        }
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        MaxSumArg other;
+        other.m = __shfl_xor_sync(0xffffffffu, st.m, o);
+        other.s = __shfl_xor_sync(0xffffffffu, st.s, o);
+        other.idx = __shfl_xor_sync(0xffffffffu, st.idx, o);
+        st = merge(st, other);
+      }
+      if (tx == 0) state[ty * 4 + x] = merge(state[ty * 4 + x], st);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < kSimtRows) {
+    const int r = r0 + threadIdx.x;
+    if (r < count) p.ws.partial[(size_t)blockIdx.x * (p.batch * p.block_len) + r] = state[threadIdx.x];
+  }
+}
+
+bd_status lmhead_simt(const ConfParams &p, cudaStream_t st) {
+  const int nrows = p.batch * p.block_len;
+  dim3 grid((p.vocab + kSimtChunk - 1) / kSimtChunk, (nrows + kSimtRows - 1) / kSimtRows);
+  if (p.dtype == BD_F32)
+    lmhead_simt_kernel<float><<<grid, 256, 0, st>>>(p);
+  else
+    lmhead_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+  count_launches(1);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// commit: one warp per sequence
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(32) conf_commit_kernel(ConfParams p) {
+  const int b = blockIdx.x, lane = threadIdx.x;
+  const int L = p.block_len;
+  const int pos = b * L + lane;
+  const bool in = lane < L;
+  const int tok = in ? p.tokens[pos] : 0;
+  const bool masked = in && tok == BD_MASK;
+  float pm = -1.f;
+  int am = -1;
+  if (masked) {
+    const int k = p.ws.row_of[pos];
+    const size_t stride = (size_t)p.batch * L;
+    MaxSumArg st{-INFINITY, 0.f, 0x7fffffff};
+    for (int c = 0; c < p.ws.num_partials; ++c) st = merge(st, p.ws.partial[c * stride + k]);
+    if (st.idx < 0 || st.idx >= p.vocab || !(st.s >= 1.f)) {
+      flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+      pm = 0.f;
+      am = 0;
+    } else {
+      pm = 1.f / st.s;
+      am = st.idx;
+    }
+  }
+  const unsigned mmask = __ballot_sync(0xffffffffu, masked);
+  unsigned sel = __ballot_sync(0xffffffffu, masked && pm >= p.threshold);
+  if (sel == 0u && mmask != 0u) {
+    // fallback: the most confident masked position, lowest position on ties
+    float best = masked ? pm : -INFINITY;
+    int who = masked ? lane : 32;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int ow = __shfl_xor_sync(0xffffffffu, who, o);
+      if (ob > best || (ob == best && ow < who)) {
+        best = ob;
+        who = ow;
+      }
+    }
+    sel = 1u << who;
+  }
+  if (in) {
+    p.p_max[pos] = pm;
+    p.argmax[pos] = am;
+    if ((sel >> lane) & 1u) p.tokens[pos] = am;
+  }
+  if (lane == 0) {
+    p.n_committed[b] = __popc(sel);
+    p.n_masked[b] = __popc(mmask) - __popc(sel);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+int conf_num_partials(bd_dtype dtype, int batch, int block_len, int hidden, int vocab) {
+  ConfParams probe{};
+  probe.dtype = dtype;
+  probe.batch = batch;
+  probe.block_len = block_len;
+  probe.hidden = hidden;
+  probe.vocab = vocab;
+  if (lmhead_tc_supported(probe)) return lmhead_tc_num_partials(vocab);
+  return (vocab + kSimtChunk - 1) / kSimtChunk;
+}
+
+static size_t carve(const ConfParams &p, char *base, ConfWorkspace *ws) {
+  const size_t n = (size_t)p.batch * p.block_len;
+  const int np = conf_num_partials(p.dtype, p.batch, p.block_len, p.hidden, p.vocab);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char *ptr = base ? base + off : nullptr;
+    off = align_up(off + bytes, 256);
+    return ptr;
+  };
+  char *rows = take(n * 4), *row_of = take(n * 4), *count = take(4);
+  char *part = take((size_t)np * n * sizeof(MaxSumArg));
+  if (ws) {
+    ws->rows = reinterpret_cast<int32_t *>(rows);
+    ws->row_of = reinterpret_cast<int32_t *>(row_of);
+    ws->count = reinterpret_cast<int32_t *>(count);
+    ws->partial = reinterpret_cast<MaxSumArg *>(part);
+    ws->num_partials = np;
+  }
+  return off;
+}
+
+static bool conf_args_ok(bd_dtype dtype, int32_t batch, int32_t block_len, int32_t hidden,
+                         int32_t vocab) {
+  if (dtype != BD_F32 && dtype != BD_BF16) return false;
+  if (batch < 1 || block_len < 1 || block_len > 32 || hidden < 1 || vocab < 1) return false;
+  if (dtype == BD_BF16 && hidden % 64 != 0) return false;
+  if (dtype == BD_F32 && hidden % 16 != 0) return false;
+  if ((int64_t)batch * block_len > (1 << 20)) return false;
+  return true;
+}
+
+}  // namespace bd
+
+using namespace bd;
+
+BD_API size_t bd_confidence_commit_workspace(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                             int32_t hidden, int32_t vocab) {
+  if (!conf_args_ok(dtype, batch, block_len, hidden, vocab)) return 0;
+  ConfParams p{};
+  p.dtype = dtype;
+  p.batch = batch;
+  p.block_len = block_len;
+  p.hidden = hidden;
+  p.vocab = vocab;
+  return carve(p, nullptr, nullptr);
+}
+
+BD_API bd_status bd_confidence_commit(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                      int32_t hidden, int32_t vocab, const void *hidden_states,
+                                      const void *lm_head, float threshold, int32_t *tokens,
+                                      float *p_max, int32_t *argmax, int32_t *n_committed,
+                                      int32_t *n_masked, void *ws, size_t ws_bytes,
+                                      int32_t *dev_status, void *stream) {
+  if (!conf_args_ok(dtype, batch, block_len, hidden, vocab)) return BD_ERR_INVALID_ARG;
+  if (!hidden_states || !lm_head || !tokens || !p_max || !argmax || !n_committed || !n_masked)
+    return BD_ERR_INVALID_ARG;
+  if (isnan(threshold)) return BD_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(hidden_states) | reinterpret_cast<uintptr_t>(lm_head)) & 15)
+    return BD_ERR_INVALID_ARG;
+  ConfParams p{};
+  p.dtype = dtype;
+  p.batch = batch;
+  p.block_len = block_len;
+  p.hidden = hidden;
+  p.vocab = vocab;
+  p.h = hidden_states;
+  p.w = lm_head;
+  p.threshold = threshold;
+  p.tokens = tokens;
+  p.p_max = p_max;
+  p.argmax = argmax;
+  p.n_committed = n_committed;
+  p.n_masked = n_masked;
+  p.dev_status = dev_status;
+  const size_t need = carve(p, nullptr, nullptr);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return BD_ERR_WORKSPACE;
+  carve(p, static_cast<char *>(ws), &p.ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  conf_prep_kernel<<<1, 1024, 0, st>>>(tokens, batch * block_len, p.ws);
+  count_launches(1);
+  if (cudaGetLastError() != cudaSuccess) return BD_ERR_CUDA;
+  const bd_status s = lmhead_tc_supported(p) ? lmhead_tc(p, st) : lmhead_simt(p, st);
+  if (s != BD_OK) return s;
+  conf_commit_kernel<<<batch, 32, 0, st>>>(p);
+  count_launches(1);
+  return launch_status();
+}

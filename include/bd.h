@@ -1,0 +1,178 @@
+/*
+ * bd.h -- C ABI of the block-diffusion denoise-step library (libbd.so).
+ *
+ * One denoise step of block-wise masked-diffusion decoding, as described in
+ * "MinerU-Diffusion: Rethinking Document OCR as Inverse Rendering via
+ * Diffusion Decoding" (paper.rainbus.top summary), method steps 2-4:
+ *   the output is split into blocks of L' tokens decoded in order; in every
+ *   denoise step the current block attends bidirectionally to itself and
+ *   causally to every earlier block and the visual/prompt prefix (kept in a
+ *   KV cache, novelty paragraph: "KV-cache reuse"), never to later blocks;
+ *   each still-masked position whose prediction confidence reaches the
+ *   threshold T (0.95) is confirmed, the others are denoised again.
+ *
+ * Conventions shared by every call:
+ *   - All pointers to tensors are DEVICE pointers unless stated otherwise.
+ *     The caller owns every buffer, workspace and stream; the library never
+ *     allocates, frees or synchronises.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream).  Host-side argument checks run first;
+ *     on failure the call returns a non-OK status and launches nothing.
+ *   - Kernels that meet a bad value in device memory (a page id outside the
+ *     pool, a context longer than the page table covers, a token id outside
+ *     the vocabulary) skip the offending access and write BD_ERR_DEVICE_CHECK
+ *     into *dev_status (first error wins; 0 means OK).  dev_status is a
+ *     device int32 the caller zeroes and reads when it chooses.  No device
+ *     code traps or asserts.
+ *   - Element types: BD_F32 (float) or BD_BF16 (bfloat16, accumulation in
+ *     fp32).  All tensors of one call share the dtype.
+ *   - Token state: int32, BD_MASK (-1) marks a still-masked position
+ *     ("yellow" in the pages' Fig. 1); any other value is a confirmed token.
+ */
+#ifndef BD_H
+#define BD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BD_MASK (-1)
+#define BD_PAGE_SIZE 64
+
+typedef enum {
+  BD_OK = 0,
+  BD_ERR_INVALID_ARG = 1,  /* host-side check failed, nothing launched      */
+  BD_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim)     */
+  BD_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed          */
+  BD_ERR_DEVICE_CHECK = 4, /* device-side bounds check (via *dev_status)    */
+  BD_ERR_TIMEOUT = 5,      /* a bounded device wait gave up (via dev_status)*/
+  BD_ERR_WORKSPACE = 6     /* workspace pointer/size too small or misaligned*/
+} bd_status;
+
+typedef enum { BD_F32 = 0, BD_BF16 = 1 } bd_dtype;
+
+/*
+ * Paged KV cache of ONE attention layer.
+ *   k_pool, v_pool: [num_pages][num_kv_heads][page_size][head_dim], dtype.
+ *   page_table:     [batch][max_pages_per_seq] int32 physical page ids; token
+ *                   position p of sequence b lives in page
+ *                   page_table[b][p / page_size], slot p % page_size.
+ * page_size must be BD_PAGE_SIZE.  The pool base pointers must be 16-byte
+ * aligned.  The struct itself is read on the host only (it may live on the
+ * caller's stack).
+ */
+typedef struct {
+  bd_dtype dtype;
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t max_pages_per_seq;
+  void *k_pool;
+  void *v_pool;
+  const int32_t *page_table;
+} bd_paged_kv;
+
+/* ------------------------------------------------------------------------
+ * bd_block_attention -- block attention of the current block (method step 3,
+ * "block-attention diffusion decoding"; also the training figure's mask in
+ * "MinerU-Diffusion reads documents with diffusion decoding instead of left
+ * to right", section "The idea").
+ *
+ * For sequence b, query position i < block_len and query head h (KV head
+ * g = h / (num_q_heads / num_kv_heads)):
+ *   keys   = cache tokens [0, ctx_len[b]) of head g   (prefix + earlier blocks)
+ *            followed by the block's own block_len keys k_blk[b, :, g]
+ *   out[b,i,h] = softmax_j(softmax_scale * q[b,i,h] . key_j) @ value_j
+ * Every block position attends to every block position (masked or not); no
+ * later block exists at decode time, so no further mask applies.
+ *
+ *   ctx_len   [batch] int32, device: cached tokens per sequence (<= max_ctx and
+ *             <= max_pages_per_seq * page_size, checked on the device).
+ *   tokens    [batch][block_len] int32 or NULL.  When given, a sequence with
+ *             no BD_MASK position is skipped (its out rows are not written).
+ *   q         [batch][block_len][num_q_heads][head_dim]
+ *   k_blk,v_blk [batch][block_len][num_kv_heads][head_dim]
+ *   out       [batch][block_len][num_q_heads][head_dim], dtype
+ *   max_ctx   host-side upper bound on ctx_len (sizes the KV split).
+ *   ws        device workspace of at least bd_block_attention_workspace() bytes,
+ *             256-byte aligned; its contents need no initialisation.
+ * Limits: head_dim 64 or 128; block_len 1..32; num_q_heads % num_kv_heads == 0;
+ *         block_len * (num_q_heads / num_kv_heads) <= 128.
+ * ------------------------------------------------------------------------ */
+size_t bd_block_attention_workspace(int32_t batch, int32_t block_len, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t max_ctx);
+
+bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_len,
+                             const int32_t *tokens, int32_t batch, int32_t block_len,
+                             int32_t num_q_heads, int32_t max_ctx, const void *q,
+                             const void *k_blk, const void *v_blk, float softmax_scale,
+                             void *out, void *ws, size_t ws_bytes, int32_t *dev_status,
+                             void *stream);
+
+/* ------------------------------------------------------------------------
+ * bd_confidence_commit -- vocabulary projection, confidence and threshold
+ * commit for one denoise step (method steps 4 and 6).
+ *
+ * For every still-masked position (b, i) (tokens[b][i] == BD_MASK):
+ *   logits_v  = hidden_states[b,i,:] . lm_head[v,:]      (v < vocab)
+ *   p_max     = max_v softmax(logits)_v = 1 / sum_v exp(logits_v - max logits)
+ *   argmax    = lowest v attaining max logits
+ * Full logits never leave the chip.  Then, per sequence b:
+ *   S = { masked i : p_max[b,i] >= threshold }; if S is empty and a position is
+ *   masked, S = { the masked i with the largest p_max, lowest i on ties };
+ *   tokens[b,i] = argmax[b,i] for i in S.  Confirmed tokens are never changed.
+ *
+ *   hidden_states [batch][block_len][hidden], lm_head [vocab][hidden], dtype.
+ *   tokens     [batch][block_len] int32, in/out.
+ *   p_max      [batch][block_len] float out (-1 at positions not masked on entry)
+ *   argmax     [batch][block_len] int32 out (-1 likewise)
+ *   n_committed[batch] int32 out: positions confirmed in this step
+ *   n_masked   [batch] int32 out: positions still masked after this step
+ *   ws         device workspace of at least bd_confidence_commit_workspace()
+ *              bytes, 256-byte aligned; no initialisation needed.
+ * Limits: block_len 1..32; hidden % 64 == 0 (bf16) or % 16 == 0 (f32);
+ *         1 <= vocab < 2^31; threshold not NaN.
+ * ------------------------------------------------------------------------ */
+size_t bd_confidence_commit_workspace(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                      int32_t hidden, int32_t vocab);
+
+bd_status bd_confidence_commit(bd_dtype dtype, int32_t batch, int32_t block_len,
+                               int32_t hidden, int32_t vocab, const void *hidden_states,
+                               const void *lm_head, float threshold, int32_t *tokens,
+                               float *p_max, int32_t *argmax, int32_t *n_committed,
+                               int32_t *n_masked, void *ws, size_t ws_bytes,
+                               int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * bd_append_block_kv -- append a finished block's K/V to the paged cache
+ * (novelty paragraph: block-causal structure lets earlier blocks' K/V be
+ * reused).  For every sequence b with n_masked[b] == 0 (NULL = all):
+ *   cache position ctx_len[b] + i  <-  k_blk[b, i], v_blk[b, i]  (i < block_len)
+ *   ctx_len[b] += block_len
+ * Call it once per finished block.  The block may straddle two pages.
+ *   k_blk, v_blk [batch][block_len][num_kv_heads][head_dim], dtype.
+ *   ctx_len [batch] int32 device, in/out.
+ * ------------------------------------------------------------------------ */
+bd_status bd_append_block_kv(const bd_paged_kv *kv, int32_t batch, int32_t block_len,
+                             const void *k_blk, const void *v_blk, int32_t *ctx_len,
+                             const int32_t *n_masked, int32_t *dev_status, void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *bd_status_string(bd_status status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int32_t bd_version(void);
+
+/* Diagnostic: number of kernels this process has launched through the
+ * library so far (all devices, all threads).  Reading it never synchronises. */
+uint64_t bd_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BD_H */

@@ -138,9 +138,9 @@ def confidence(h, W, row_chunk: int = 64):
         p_max[r0:r0 + row_chunk] = p.max(axis=1)
         argmax[r0:r0 + row_chunk] = np.argmax(l, axis=1)       # first = lowest id
         if l.shape[1] > 1:
-            top2 = np.sort(l, axis=1)[:, -2:]
+            top2 = np.partition(l, -2, axis=1)[:, -2:]          # two largest, ascending
             lgap[r0:r0 + row_chunk] = top2[:, 1] - top2[:, 0]
-            ptop2 = np.sort(p, axis=1)[:, -2:]
+            ptop2 = np.partition(p, -2, axis=1)[:, -2:]
             pmarg[r0:r0 + row_chunk] = ptop2[:, 1] - ptop2[:, 0]
         else:
             lgap[r0:r0 + row_chunk] = np.inf

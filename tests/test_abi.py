@@ -1,0 +1,68 @@
+"""The C ABI: libbd.so builds, loads without a GPU and exports every symbol
+that include/bd.h declares; host-side argument checks answer without
+launching anything (so they run on a machine with no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_diffusion_decoding_denoise_gb300 import bd, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return bd.load()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "bd.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bd_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("bd_block_attention", "bd_confidence_commit", "bd_append_block_kv",
+              "bd_status_string"):
+        assert n in names
+    assert sorted(bd.EXPORTS) == names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert bd.bd_status_string(0) == "BD_OK"
+    assert bd.bd_status_string(4) == "BD_ERR_DEVICE_CHECK"
+    assert bd.bd_status_string(99) == "BD_ERR_UNKNOWN"
+    assert bd.bd_version() >= 100
+
+
+def test_workspace_queries_reject_bad_shapes(lib):
+    assert bd.bd_confidence_commit_workspace(bd.BD_BF16, 1, 32, 2048, 151936) > 0
+    assert bd.bd_confidence_commit_workspace(bd.BD_BF16, 1, 33, 2048, 151936) == 0
+    assert bd.bd_confidence_commit_workspace(bd.BD_BF16, 1, 32, 100, 151936) == 0
+    assert bd.bd_confidence_commit_workspace(7, 1, 32, 2048, 151936) == 0
+    assert bd.bd_block_attention_workspace(1, 32, 16, 8, 96, 4096) == 0
+    assert bd.bd_block_attention_workspace(1, 32, 16, 5, 128, 4096) == 0
+    assert bd.bd_block_attention_workspace(1, 32, 16, 8, 128, -1) == 0
+
+
+def test_null_arguments_are_rejected_before_any_launch(lib):
+    f = lib.bd_confidence_commit
+    st = f(1, 1, 32, 2048, 1000, None, None, 0.9, None, None, None, None, None, None, 0,
+           None, None)
+    assert st == 1
+    st = lib.bd_block_attention(None, None, None, 1, 32, 16, 100, None, None, None, 0.1,
+                                None, None, 0, None, None)
+    assert st == 1
+    kv = bd.PagedKV(1, 4, 64, 8, 128, 4, None, None, None)
+    st = lib.bd_append_block_kv(ctypes.byref(kv), 1, 32, None, None, None, None, None, None)
+    assert st == 1
