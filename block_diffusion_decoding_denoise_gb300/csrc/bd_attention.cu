@@ -193,6 +193,8 @@ __global__ void attn_combine_kernel(AttnParams p) {
   }
 }
 
+bd_status attention_combine(const AttnParams &p, cudaStream_t st);
+
 template <typename T, int D>
 static bd_status launch_simt(const AttnParams &p, cudaStream_t st) {
   const int R = p.block_len * (p.hq / p.hkv);
@@ -206,14 +208,24 @@ static bd_status launch_simt(const AttnParams &p, cudaStream_t st) {
   kern<<<grid, warps * 32, smem, st>>>(p);
   count_launches(1);
   if (cudaGetLastError() != cudaSuccess) return BD_ERR_CUDA;
-  if (p.num_splits > 1) {
-    const size_t total = (size_t)p.batch * p.hkv * R * D;
-    const int blocks = (int)std::min<size_t>((total + 255) / 256, 4096);
-    attn_combine_kernel<T, D><<<blocks, 256, 0, st>>>(p);
-    count_launches(1);
-    if (cudaGetLastError() != cudaSuccess) return BD_ERR_CUDA;
-  }
-  return BD_OK;
+  return p.num_splits > 1 ? attention_combine(p, st) : BD_OK;
+}
+
+template <typename T, int D>
+static bd_status launch_combine(const AttnParams &p, cudaStream_t st) {
+  const int R = p.block_len * (p.hq / p.hkv);
+  const size_t total = (size_t)p.batch * p.hkv * R * D;
+  const int blocks = (int)std::min<size_t>((total + 255) / 256, 4096);
+  attn_combine_kernel<T, D><<<blocks, 256, 0, st>>>(p);
+  count_launches(1);
+  return launch_status();
+}
+
+bd_status attention_combine(const AttnParams &p, cudaStream_t st) {
+  if (p.dtype == BD_F32)
+    return p.head_dim == 64 ? launch_combine<float, 64>(p, st) : launch_combine<float, 128>(p, st);
+  return p.head_dim == 64 ? launch_combine<__nv_bfloat16, 64>(p, st)
+                          : launch_combine<__nv_bfloat16, 128>(p, st);
 }
 
 bd_status attention_simt(const AttnParams &p, cudaStream_t st) {

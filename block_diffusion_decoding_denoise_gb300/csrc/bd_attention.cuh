@@ -25,5 +25,6 @@ struct AttnParams {
 
 bd_status attention_simt(const AttnParams &p, cudaStream_t st);
 bd_status attention_tc(const AttnParams &p, cudaStream_t st);
+bd_status attention_combine(const AttnParams &p, cudaStream_t st);
 
 }  // namespace bd

@@ -1,6 +1,7 @@
 // Shared device/host helpers of libbd (CUDA, sm_103a).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -51,6 +52,19 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Launch counter behind bd_kernel_launches(); every host entry point adds
 // the number of kernels it launched.
 void count_launches(int n);
+
+// Device facts of the current device (cached per device; zeros when no GPU).
+struct DevInfo {
+  int sms = 0;
+  int major = 0;
+};
+DevInfo dev_info();
+
+// TMA tensor maps over bf16 tensors with a 128-byte swizzle.  dims[0] is the
+// innermost (contiguous) extent; strides_bytes[i] is the stride of dim i+1.
+bool tma_available();
+bool tma_encode_bf16(CUtensorMap *m, int rank, const void *base, const uint64_t *dims,
+                     const uint64_t *strides_bytes, const uint32_t *box);
 
 inline bd_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? BD_OK : BD_ERR_CUDA;

@@ -25,16 +25,24 @@
 namespace bd {
 
 // ---------------------------------------------------------------------------
-// masked-row compaction: one CTA, block-wide exclusive scan
+// masked-row compaction (+ optional gather of the masked rows of h into a
+// contiguous buffer).  Every CTA scans all positions (a block-wide exclusive
+// scan, B*L' <= a few thousand); CTA 0 publishes the row list, and CTA c
+// copies the rows whose compact index k satisfies k % gridDim.x == c.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) conf_prep_kernel(const int32_t *tokens, int n,
-                                                         ConfWorkspace ws) {
+                                                         ConfWorkspace ws, const char *src,
+                                                         int row_bytes) {
   __shared__ int warp_sums[32];
   __shared__ int carry;
+  __shared__ int list_n;
+  __shared__ int2 list[1024];
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
   for (int base = 0; base < n; base += blockDim.x) {
+    if (threadIdx.x == 0) list_n = 0;
     const int pos = base + threadIdx.x;
     const int m = (pos < n && tokens[pos] == BD_MASK) ? 1 : 0;
     const unsigned bal = __ballot_sync(0xffffffffu, m);
@@ -44,19 +52,29 @@ __global__ void __launch_bounds__(1024) conf_prep_kernel(const int32_t *tokens, 
     int before = carry;
     for (int w = 0; w < warp; ++w) before += warp_sums[w];
     const int k = before + before_in_warp;
-    if (pos < n) {
+    if (blockIdx.x == 0 && pos < n) {
       ws.row_of[pos] = m ? k : -1;
       if (m) ws.rows[k] = pos;
     }
+    if (src && m && (k % gridDim.x) == blockIdx.x) list[atomicAdd(&list_n, 1)] = make_int2(k, pos);
     __syncthreads();
+    if (src) {  // copy this CTA's rows of the chunk, one warp per row, 16 bytes per lane
+      const int vecs = row_bytes / 16;
+      for (int e = warp; e < list_n; e += nwarps) {
+        const int2 kp = list[e];
+        const int4 *from = reinterpret_cast<const int4 *>(src + (size_t)kp.y * row_bytes);
+        int4 *to = reinterpret_cast<int4 *>(ws.hc + (size_t)kp.x * row_bytes);
+        for (int v = lane; v < vecs; v += 32) to[v] = from[v];
+      }
+    }
     if (threadIdx.x == 0) {
       int tot = 0;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += warp_sums[w];
+      for (int w = 0; w < nwarps; ++w) tot += warp_sums[w];
       carry += tot;
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) *ws.count = carry;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ws.count = carry;
 }
 
 // ---------------------------------------------------------------------------
@@ -160,31 +178,52 @@ bd_status lmhead_simt(const ConfParams &p, cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------------------
-// commit: one warp per sequence
+// commit: one CTA per sequence; warp i merges the partial states of position
+// i (lanes stride over the producers), warp 0 then takes the decision
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(32) conf_commit_kernel(ConfParams p) {
-  const int b = blockIdx.x, lane = threadIdx.x;
+__global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
+  __shared__ float s_pm[32];
+  __shared__ int s_am[32];
+  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = p.block_len;
-  const int pos = b * L + lane;
-  const bool in = lane < L;
-  const int tok = in ? p.tokens[pos] : 0;
-  const bool masked = in && tok == BD_MASK;
-  float pm = -1.f;
-  int am = -1;
-  if (masked) {
-    const int k = p.ws.row_of[pos];
-    const size_t stride = (size_t)p.batch * L;
-    MaxSumArg st{-INFINITY, 0.f, 0x7fffffff};
-    for (int c = 0; c < p.ws.num_partials; ++c) st = merge(st, p.ws.partial[c * stride + k]);
-    if (st.idx < 0 || st.idx >= p.vocab || !(st.s >= 1.f)) {
-      flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
-      pm = 0.f;
-      am = 0;
-    } else {
-      pm = 1.f / st.s;
-      am = st.idx;
+  if (warp < L) {
+    const int pos = b * L + warp;
+    float pm = -1.f;
+    int am = -1;
+    if (p.tokens[pos] == BD_MASK) {
+      const int k = p.ws.row_of[pos];
+      const size_t stride = (size_t)p.batch * L;
+      MaxSumArg st{-INFINITY, 0.f, 0x7fffffff};
+      for (int c = lane; c < p.ws.num_partials; c += 32) st = merge(st, p.ws.partial[c * stride + k]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        MaxSumArg other;
+        other.m = __shfl_xor_sync(0xffffffffu, st.m, o);
+        other.s = __shfl_xor_sync(0xffffffffu, st.s, o);
+        other.idx = __shfl_xor_sync(0xffffffffu, st.idx, o);
+        st = merge(st, other);
+      }
+      if (st.idx < 0 || st.idx >= p.vocab || !(st.s >= 1.f)) {
+        if (lane == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+        pm = 0.f;
+        am = 0;
+      } else {
+        pm = 1.f / st.s;
+        am = st.idx;
+      }
+    }
+    if (lane == 0) {
+      s_pm[warp] = pm;
+      s_am[warp] = am;
     }
   }
+  __syncthreads();
+  if (warp != 0) return;
+  const int pos = b * L + lane;
+  const bool in = lane < L;
+  const bool masked = in && p.tokens[pos] == BD_MASK;
+  const float pm = in ? s_pm[lane] : -1.f;
+  const int am = in ? s_am[lane] : -1;
   const unsigned mmask = __ballot_sync(0xffffffffu, masked);
   unsigned sel = __ballot_sync(0xffffffffu, masked && pm >= p.threshold);
   if (sel == 0u && mmask != 0u) {
@@ -238,12 +277,14 @@ static size_t carve(const ConfParams &p, char *base, ConfWorkspace *ws) {
   };
   char *rows = take(n * 4), *row_of = take(n * 4), *count = take(4);
   char *part = take((size_t)np * n * sizeof(MaxSumArg));
+  char *hc = p.dtype == BD_BF16 ? take(n * (size_t)p.hidden * 2) : nullptr;
   if (ws) {
     ws->rows = reinterpret_cast<int32_t *>(rows);
     ws->row_of = reinterpret_cast<int32_t *>(row_of);
     ws->count = reinterpret_cast<int32_t *>(count);
     ws->partial = reinterpret_cast<MaxSumArg *>(part);
     ws->num_partials = np;
+    ws->hc = hc;
   }
   return off;
 }
@@ -306,12 +347,19 @@ BD_API bd_status bd_confidence_commit(bd_dtype dtype, int32_t batch, int32_t blo
   carve(p, static_cast<char *>(ws), &p.ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  conf_prep_kernel<<<1, 1024, 0, st>>>(tokens, batch * block_len, p.ws);
+  const bool tc = lmhead_tc_supported(p);
+  const int nrows = batch * block_len;
+  // the tensor-core path reads the masked rows from a contiguous copy
+  const int prep_ctas = tc ? std::max(1, std::min(std::max(dev_info().sms, 1), (nrows + 7) / 8)) : 1;
+  conf_prep_kernel<<<prep_ctas, 1024, 0, st>>>(tokens, nrows, p.ws,
+                                               tc ? static_cast<const char *>(hidden_states)
+                                                  : nullptr,
+                                               hidden * 2);
   count_launches(1);
   if (cudaGetLastError() != cudaSuccess) return BD_ERR_CUDA;
-  const bd_status s = lmhead_tc_supported(p) ? lmhead_tc(p, st) : lmhead_simt(p, st);
+  const bd_status s = tc ? lmhead_tc(p, st) : lmhead_simt(p, st);
   if (s != BD_OK) return s;
-  conf_commit_kernel<<<batch, 32, 0, st>>>(p);
+  conf_commit_kernel<<<batch, 32 * block_len, 0, st>>>(p);
   count_launches(1);
   return launch_status();
 }

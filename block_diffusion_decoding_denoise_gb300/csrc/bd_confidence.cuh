@@ -14,10 +14,12 @@ namespace bd {
 //   row_of   [B*L] int32   position -> compact row (-1 if not masked)
 //   count    [1]   int32   number of masked rows
 //   partial  [P][B*L] MaxSumArg   one online-softmax state per producer and row
+//   hc       [B*L][H] bf16        masked rows of h, compacted (bf16 only)
 struct ConfWorkspace {
   int32_t *rows, *row_of, *count;
   MaxSumArg *partial;
   int num_partials;
+  char *hc;
 };
 
 struct ConfParams {

@@ -1,8 +1,372 @@
-// Tensor-core LM head (placeholder until the tcgen05 kernel lands).
+// LM head + online-softmax confidence on the 5th-generation tensor cores.
+//
+// Computes, for every still-masked row r of the step (the compact row list
+// written by conf_prep_kernel) and every vocabulary entry v,
+//     l[r, v] = h[row r] . W[v]            (bf16 x bf16 -> fp32, tcgen05.mma)
+// and reduces each row to the online-softmax state (max l, sum exp(l - max),
+// lowest argmax) over the vocabulary slice this CTA owns, without writing a
+// logit to memory ("Rethinking Document OCR as Inverse Rendering via
+// Diffusion Decoding", paper.rainbus.top summary, method step 4: confidence of
+// each masked prediction).
+//
+// Orientation ("swap AB"): the vocabulary is the MMA's M dimension (tiles of
+// 128 entries of W, A operand) and the masked rows are N (up to 128 per pass,
+// B operand), so a step with only a handful of masked rows still fills the
+// 128-lane tensor-core tile and the kernel streams W at HBM speed.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over vocabulary tiles
+// vt = blockIdx.x + i * gridDim.x):
+//   warp 0     TMA producer: per 64-wide K chunk, one 128x64 box of W and
+//              16x64 boxes of the compacted masked rows of h (conf_prep_kernel
+//              gathers them) into a ring of smem stages (128-byte swizzle),
+//              completion on the stage's "full" mbarrier
+//   warp 1     TMEM allocator and MMA issuer (one thread): 4 x (M128,N,K16)
+//              per stage into one of two TMEM accumulators; tcgen05.commit
+//              frees the stage and, after the last K chunk, hands the
+//              accumulator to the epilogue
+//   warps 2-5  epilogue: tcgen05.ld 32 lanes x 16 columns, per column a warp
+//              max / argmax (ballot) / sum-exp, a 4-warp merge through smem,
+//              and a running state per row kept in registers
+// Each CTA writes one partial state per row; conf_commit_kernel merges them.
+// Every mbarrier wait is bounded (1 s); on expiry the kernel records
+// BD_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
+#include <math.h>
+
+#include <algorithm>
+
 #include "bd_confidence.cuh"
+#include "bd_sm100.cuh"
 
 namespace bd {
-bool lmhead_tc_supported(const ConfParams &) { return false; }
-int lmhead_tc_num_partials(int) { return 0; }
-bd_status lmhead_tc(const ConfParams &, cudaStream_t) { return BD_ERR_UNSUPPORTED; }
+
+using namespace sm100;
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kTileV = 128;                 // vocabulary entries per tile (MMA M)
+constexpr int kKChunk = 64;                 // K elements per stage (128 bytes of bf16)
+constexpr int kMaxN = 128;                  // masked rows per pass (MMA N)
+constexpr int kBoxRows = 16;                // rows of the compact h copy per TMA box
+constexpr int kABytes = kTileV * 128;       // 16 KB of W per stage
+constexpr int kMaxStages = 12;
+constexpr uint32_t kTmemCols = 2 * kMaxN;   // two accumulators
+constexpr int kSmemLimit = 227 * 1024;
+
+struct Ctrl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  volatile int32_t abort;
+  MaxSumArg red[2][4][kMaxN];
+};
+
+struct LmTcArgs {
+  ConfParams p;
+  int stages;
+  int stage_bytes;
+  int num_tiles;
+};
+
+__device__ __forceinline__ bool barrier_or(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                     const __grid_constant__ CUtensorMap tmap_h, const LmTcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + (size_t)a.stages * a.stage_bytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ConfParams &p = a.p;
+
+  const int count = *p.ws.count;
+  if (count <= 0) return;                   // nothing masked: uniform early exit
+  const int npass = (count + kMaxN - 1) / kMaxN;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int my_tiles = (a.num_tiles - cta + G - 1) / G;
+  const int KC = p.hidden / kKChunk;
+  const int S = a.stages;
+  const size_t stride = (size_t)p.batch * p.block_len;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&ctrl->full[s]), 1);
+      mbar_init(smem_u32(&ctrl->empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&ctrl->tfull[i]), 1);
+      mbar_init(smem_u32(&ctrl->tempty[i]), 4);
+    }
+    mbar_init(smem_u32(&ctrl->mma_done), 1);
+    ctrl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_w);
+    tma_prefetch_desc(&tmap_h);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctrl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctrl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0;
+    bool stop = false;
+    for (int pass = 0; pass < npass && !stop; ++pass) {
+      const int r0 = pass * kMaxN;
+      const int n = min(kMaxN, count - r0);
+      const int npad = (n + 15) & ~15;
+      const uint32_t tx = kABytes + npad * 128;
+      for (int t = 0; t < my_tiles && !stop; ++t) {
+        const int vt = cta + t * G;
+        for (int kc = 0; kc < KC; ++kc, ++it) {
+          const uint32_t s = it % S, round = it / S;
+          uint8_t *st = smem + (size_t)s * a.stage_bytes;
+          int ok = 1;
+          if (lane == 0) {
+            if (ctrl->abort) ok = 0;
+            else if (round > 0 && !mbar_wait(smem_u32(&ctrl->empty[s]), (round - 1) & 1)) {
+              ok = 0;
+              ctrl->abort = 1;
+              flag_error(p.dev_status, BD_ERR_TIMEOUT);
+            }
+            if (ok) {
+              const uint32_t bar = smem_u32(&ctrl->full[s]);
+              mbar_arrive_expect_tx(bar, tx);
+              tma_load_2d(smem_u32(st), &tmap_w, kc * kKChunk, vt * kTileV, bar);
+              for (int r = 0; r < npad; r += kBoxRows)
+                tma_load_2d(smem_u32(st + kABytes + r * 128), &tmap_h, kc * kKChunk, r0 + r, bar);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            stop = true;
+            break;
+          }
+        }
+      }
+    }
+    // on an abort, wait (bounded) for the copies this warp may still have in flight
+    if (stop && lane == 0) {
+      const uint32_t first = it > (uint32_t)S ? it - S : 0;
+      for (uint32_t i = first; i < it; ++i)
+        mbar_wait(smem_u32(&ctrl->full[i % S]), (i / S) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, tg = 0;
+      bool stop = false;
+      for (int pass = 0; pass < npass && !stop; ++pass) {
+        const int n = min(kMaxN, count - pass * kMaxN);
+        const int npad = (n + 15) & ~15;
+        const uint32_t idesc = idesc_bf16_f32(kTileV, npad);
+        for (int t = 0; t < my_tiles && !stop; ++t, ++tg) {
+          const uint32_t acc = tg & 1, use = tg >> 1;
+          if (ctrl->abort ||
+              (use > 0 && !mbar_wait(smem_u32(&ctrl->tempty[acc]), (use - 1) & 1))) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + acc * kMaxN;
+          for (int kc = 0; kc < KC; ++kc, ++it) {
+            const uint32_t s = it % S, round = it / S;
+            if (ctrl->abort || !mbar_wait(smem_u32(&ctrl->full[s]), round & 1)) {
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(smem + (size_t)s * a.stage_bytes);
+            const uint32_t b_base = a_base + kABytes;
+#pragma unroll
+            for (int k = 0; k < kKChunk / 16; ++k)
+              mma_bf16(d, sw128_kmajor_desc(a_base + k * 32), sw128_kmajor_desc(b_base + k * 32),
+                       idesc, (kc | k) != 0);
+            mma_commit(smem_u32(&ctrl->empty[s]));
+          }
+          if (stop) break;
+          mma_commit(smem_u32(&ctrl->tfull[acc]));
+        }
+      }
+      if (stop) {
+        ctrl->abort = 1;
+        flag_error(p.dev_status, BD_ERR_TIMEOUT);
+      }
+      // every MMA this thread issued has completed once mma_done fires
+      mma_commit(smem_u32(&ctrl->mma_done));
+      mbar_wait(smem_u32(&ctrl->mma_done), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;                 // slot of this warp in the merge buffer
+    const int q = warp & 3;                  // TMEM sub-partition this warp may read
+    const int tid_e = threadIdx.x - 64;      // 0..127: row of the pass owned in merges
+    uint32_t tg = 0;
+    bool stop = false;
+    for (int pass = 0; pass < npass && !stop; ++pass) {
+      const int r0 = pass * kMaxN;
+      const int n = min(kMaxN, count - r0);
+      const int npad = (n + 15) & ~15;
+      MaxSumArg run{-INFINITY, 0.f, 0x7fffffff};
+      for (int t = 0; t < my_tiles; ++t, ++tg) {
+        const int vt = cta + t * G;
+        const uint32_t acc = tg & 1, use = tg >> 1;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(smem_u32(&ctrl->tfull[acc]), use & 1) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) {
+          tc_fence_after();
+          const int vbase = vt * kTileV + 32 * q;
+          const bool valid = vbase + lane < p.vocab;
+          MaxSumArg held[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) held[j] = MaxSumArg{-INFINITY, 0.f, 0x7fffffff};
+          for (int c0 = 0; c0 < npad; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(tmem + ((uint32_t)(32 * q) << 16) + acc * kMaxN + c0, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float x = valid ? __uint_as_float(r[j]) : -INFINITY;
+              const float m = warp_max(x);
+              const unsigned bal = __ballot_sync(0xffffffffu, valid && x == m);
+              MaxSumArg res{-INFINITY, 0.f, 0x7fffffff};
+              if (bal) {
+                res.m = m;
+                res.s = warp_sum(valid ? __expf(x - m) : 0.f);
+                res.idx = vbase + __ffs(bal) - 1;
+              }
+              const int c = c0 + j;
+              if (lane == (c & 31)) {
+                const int slot = c >> 5;
+                if (slot == 0) held[0] = res;
+                else if (slot == 1) held[1] = res;
+                else if (slot == 2) held[2] = res;
+                else held[3] = res;
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctrl->tempty[acc]));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = lane + 32 * j;
+            if (c < npad) ctrl->red[tg & 1][ew][c] = held[j];
+          }
+        } else {
+          ctrl->abort = 1;
+          if (lane == 0) flag_error(p.dev_status, BD_ERR_TIMEOUT);
+        }
+        if (barrier_or(1, 128, !ok || ctrl->abort)) {
+          stop = true;
+          break;
+        }
+        if (tid_e < npad) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) run = merge(run, ctrl->red[tg & 1][w][tid_e]);
+        }
+      }
+      if (!stop && tid_e < n) p.ws.partial[(size_t)cta * stride + r0 + tid_e] = run;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// 2-D bf16 tensor map over a row-major [outer][inner] matrix, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_in,
+              uint32_t box_out) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint64_t strides[1] = {inner * 2};
+  const uint32_t box[2] = {box_in, box_out};
+  return tma_encode_bf16(m, 2, base, dims, strides, box);
+}
+
+int num_tiles(int vocab) { return (vocab + kTileV - 1) / kTileV; }
+
+void plan(const ConfParams &p, int *stages, int *stage_bytes, size_t *smem) {
+  const int rows = p.batch * p.block_len;
+  const int nmax = std::min(kMaxN, (rows + 15) & ~15);
+  *stage_bytes = (kABytes + nmax * 128 + 1023) & ~1023;
+  const int avail = kSmemLimit - (int)sizeof(Ctrl) - 1024;
+  *stages = std::max(2, std::min(kMaxStages, avail / *stage_bytes));
+  *smem = (size_t)(*stages) * (*stage_bytes) + sizeof(Ctrl) + 1024;
+}
+
+}  // namespace
+
+bool lmhead_tc_supported(const ConfParams &p) {
+  if (p.dtype != BD_BF16 || p.hidden % kKChunk != 0 || p.hidden < kKChunk) return false;
+  if ((int64_t)p.batch * p.block_len > (1 << 20)) return false;
+  const DevInfo d = dev_info();
+  if (d.major < 10 || d.sms <= 0) return false;
+  return tma_available();
+}
+
+int lmhead_tc_num_partials(int vocab) {
+  const DevInfo d = dev_info();
+  return std::max(1, std::min(d.sms, num_tiles(vocab)));
+}
+
+bd_status lmhead_tc(const ConfParams &p, cudaStream_t st) {
+  LmTcArgs a;
+  a.p = p;
+  a.num_tiles = num_tiles(p.vocab);
+  size_t smem;
+  plan(p, &a.stages, &a.stage_bytes, &smem);
+  if (smem > (size_t)kSmemLimit) return BD_ERR_UNSUPPORTED;
+  CUtensorMap mw, mh;
+  if (!make_map(&mw, p.w, p.hidden, p.vocab, kKChunk, kTileV)) return BD_ERR_CUDA;
+  if (!make_map(&mh, p.ws.hc, p.hidden, (uint64_t)p.batch * p.block_len, kKChunk, kBoxRows))
+    return BD_ERR_CUDA;
+  if (cudaFuncSetAttribute(lmhead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return BD_ERR_CUDA;
+  const int grid = p.ws.num_partials;
+  if (grid < 1 || grid > a.num_tiles) return BD_ERR_INVALID_ARG;
+  lmhead_tc_kernel<<<grid, kThreads, smem, st>>>(mw, mh, a);
+  count_launches(1);
+  return launch_status();
+}
+
 }  // namespace bd

@@ -165,6 +165,14 @@ def test_decode_threshold_extremes(T, steps):
     assert st.steps_gpu.tolist() == [steps] * w.batch
 
 
+def test_decode_more_rows_than_one_pass():
+    # 5 x 32 = 160 masked rows: the LM head takes two passes of at most 128 rows
+    w = SMALL_BF16.with_(batch=5)
+    W = wl.lm_head(w)
+    h, _ = wl.planted_hidden(w, W, 0, a_max=30.0)
+    lockstep_block(w, W, h, 0.9)
+
+
 def test_decode_partially_committed_entry_state():
     w = SMALL_BF16
     W = wl.lm_head(w)
