@@ -45,6 +45,9 @@ def _args():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--check-every", type=int, default=8)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload name (the headline line uses sdar_b1)")
     return ap.parse_args()
 
 
@@ -251,7 +254,7 @@ def run_cuda(a):
         build.build()
     bd.load()
 
-    w = wl.WORKLOADS[WORKLOAD]
+    w = wl.WORKLOADS[a.workload]
     W, plen, kv, q, kb, vb, h = _inputs(w)
     table, npg = wl.page_tables(w, plen + w.block_len)
     cache = PagedCache(npg, w.num_kv_heads, w.head_dim, torch.bfloat16, table)
@@ -272,17 +275,20 @@ def run_cuda(a):
     conf_events = []
     orig_step = eng.step
 
+    attn_events = []
+
     def timed_step(hh, qq, kk, vv, ncom=None, layer=0):
+        ea = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ea[0].record(stream)
         bd.bd_block_attention(eng.caches[layer].kv, eng.ctx_len, eng.tokens, qq, kk, vv,
                               eng.attn_out, eng.attn_ws, eng.max_ctx, dev_status=eng.dev_status)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        ea[1].record(stream)
         bd.bd_confidence_commit(hh, eng.W, eng.T, eng.tokens, eng.p_max, eng.argmax,
                                 eng.n_committed[0] if ncom is None else ncom, eng.n_masked,
                                 eng.conf_ws, dev_status=eng.dev_status)
-        e1.record(stream)
-        conf_events.append((e0, e1))
+        ea[2].record(stream)
+        attn_events.append((ea[0], ea[1]))
+        conf_events.append((ea[1], ea[2]))
 
     def block():
         eng.ctx_len.copy_(ctx0)
@@ -348,8 +354,47 @@ def run_cuda(a):
                 "kernel": "bd_confidence_commit (masked-row compaction + LM head with online "
                           "max/sum-exp/argmax + commit)",
                 "peak_source": f"{peak_kind} hbm_gbs"}
+    # block attention: K/V of cache + block once per KV head, Q read, O written
+    attn_ms = [e0.elapsed_time(e1) for e0, e1 in attn_events]
+    ctx_tot = int(plen.sum())
+    attn_bytes = (2 * (ctx_tot + w.batch * w.block_len) * w.num_kv_heads * w.head_dim * 2
+                  + 2 * w.batch * w.block_len * w.num_q_heads * w.head_dim * 2)
+    act = [t for t, r in zip(attn_ms, rows_per_call) if r > 0]
+    attn_gbs = attn_bytes * len(act) / (sum(act) / 1e3) / 1e9 if act else None
+    roofline_attn = {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": attn_gbs / peak if attn_gbs else None,
+                     "bytes_per_call": attn_bytes,
+                     "us_per_call": 1e3 * statistics.mean(act) if act else None}
 
-    # end to end: host buffers, copies inside the timed region
+    e2e = None
+    if not a.no_e2e:
+        e2e = _e2e(a, eng, w, h, q, kb, vb, hd, qd, kbd, vbd, ctx0, stream, committed_per_block,
+                   world)
+    if rank != 0:
+        return
+    cpu = None
+    if not a.no_cpu_baseline:
+        cpu = cpu_baseline(w, W, kv, q, kb, vb, h)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": max(3, a.warmup), "ms_per_step": ms / a.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": _config(w, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                              "denoise_steps_per_block": [int(x) for x in steps_per_seq],
+                              "denoise_steps_issued": steps_issued // a.steps,
+                              "check_every": a.check_every}),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(launches), "clocks": clk.summary(),
+        "conf_call_us_mean": 1e3 * statistics.mean(conf_ms) if conf_ms else None,
+        "roofline_attention": roofline_attn,
+    }
+    print(json.dumps(line))
+
+
+def _e2e(a, eng, w, h, q, kb, vb, hd, qd, kbd, vbd, ctx0, stream, committed_per_block, world):
+    """Same metric through the public API with host buffers: every block copies its
+    inputs from pinned host memory and reads the committed tokens back."""
+    import torch
     h_host = torch.from_numpy(h).to(torch.bfloat16).pin_memory()
     q_host = torch.from_numpy(q).to(torch.bfloat16).pin_memory()
     k_host = torch.from_numpy(kb).to(torch.bfloat16).pin_memory()
@@ -374,27 +419,8 @@ def run_cuda(a):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    e2e = {"value": committed_per_block * a.steps * world / (e2e_ms / 1e3), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-
-    if rank != 0:
-        return
-    cpu = None
-    if not a.no_cpu_baseline:
-        cpu = cpu_baseline(w, W, kv, q, kb, vb, h)
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
-        "warmup": max(3, a.warmup), "ms_per_step": ms / a.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": _config(w, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                              "denoise_steps_per_block": [int(x) for x in steps_per_seq],
-                              "denoise_steps_issued": steps_issued // a.steps,
-                              "check_every": a.check_every}),
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": int(launches), "clocks": clk.summary(),
-        "conf_call_us_mean": 1e3 * statistics.mean(conf_ms) if conf_ms else None,
-    }
-    print(json.dumps(line))
+    return {"value": committed_per_block * a.steps * world / (e2e_ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
 def main():

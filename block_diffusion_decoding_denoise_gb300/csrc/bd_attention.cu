@@ -157,40 +157,47 @@ __global__ void __launch_bounds__(512) attn_splitkv_simt_kernel(AttnParams p) {
 }
 
 // Merge split partials: O = sum_s O_s exp(m_s - m) / sum_s l_s exp(m_s - m).
+// One warp per (sequence, KV head, query row); lanes own D/32 output columns.
 template <typename T, int D>
-__global__ void attn_combine_kernel(AttnParams p) {
+__global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p) {
+  constexpr int DPL = D / 32;
   const int group = p.hq / p.hkv;
   const int R = p.block_len * group;
-  const size_t total = (size_t)p.batch * p.hkv * R * D;
-  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-       e += (size_t)gridDim.x * blockDim.x) {
-    const int d = e % D;
-    const int r = (e / D) % R;
-    const int g = (e / ((size_t)D * R)) % p.hkv;
-    const int b = e / ((size_t)D * R * p.hkv);
-    if (p.tokens) {
-      int any = 0;
-      for (int i = 0; i < p.block_len; ++i) any |= (p.tokens[b * p.block_len + i] == BD_MASK);
-      if (!any) continue;
-    }
-    const int ctx = p.ctx_len[b];
-    if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) continue;
-    const int nkeys = ctx + p.block_len;
-    const int used = (nkeys + p.split_keys - 1) / p.split_keys;   // splits that saw keys
-    const size_t base = (((size_t)b * p.hkv + g) * p.num_splits) * R + r;
-    float m = -INFINITY;
-    for (int s = 0; s < used; ++s) m = fmaxf(m, p.part_ml[(base + (size_t)s * R) * 2]);
-    float l = 0.f, o = 0.f;
-    for (int s = 0; s < used; ++s) {
-      const size_t pr = base + (size_t)s * R;
-      const float w = __expf(p.part_ml[pr * 2] - m);
-      l += p.part_ml[pr * 2 + 1] * w;
-      o += p.part_o[pr * D + d] * w;
-    }
-    const int i = r / group, h = g * group + r % group;
-    T *out = static_cast<T *>(p.out);
-    out[(((size_t)b * p.block_len + i) * p.hq + h) * D + d] = from_f32<T>(l > 0.f ? o / l : 0.f);
+  const int wid = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= p.batch * p.hkv * R) return;
+  const int r = wid % R, g = (wid / R) % p.hkv, b = wid / (R * p.hkv);
+  if (p.tokens) {
+    int any = 0;
+    for (int i = 0; i < p.block_len; ++i) any |= (p.tokens[b * p.block_len + i] == BD_MASK);
+    if (!any) return;
   }
+  const int ctx = p.ctx_len[b];
+  if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) return;
+  const int used = (ctx + p.block_len + p.split_keys - 1) / p.split_keys;  // splits with keys
+  const size_t base = (((size_t)b * p.hkv + g) * p.num_splits) * R + r;
+  float m = -INFINITY;
+  for (int s = lane; s < used; s += 32) m = fmaxf(m, __ldcg(&p.part_ml[(base + (size_t)s * R) * 2]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float l = 0.f, acc[DPL];
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
+#pragma unroll 4
+  for (int s = 0; s < used; ++s) {
+    const size_t pr = base + (size_t)s * R;
+    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + pr * 2));
+    const float w = __expf(ml.x - m);
+    l = fmaf(ml.y, w, l);
+    const float *src = p.part_o + pr * D + lane * DPL;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) acc[j] = fmaf(__ldcg(src + j), w, acc[j]);
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const int i = r / group, h = g * group + r % group;
+  T *out = static_cast<T *>(p.out) + (((size_t)b * p.block_len + i) * p.hq + h) * D + lane * DPL;
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) out[j] = from_f32<T>(acc[j] * inv);
 }
 
 bd_status attention_combine(const AttnParams &p, cudaStream_t st);
@@ -214,8 +221,8 @@ static bd_status launch_simt(const AttnParams &p, cudaStream_t st) {
 template <typename T, int D>
 static bd_status launch_combine(const AttnParams &p, cudaStream_t st) {
   const int R = p.block_len * (p.hq / p.hkv);
-  const size_t total = (size_t)p.batch * p.hkv * R * D;
-  const int blocks = (int)std::min<size_t>((total + 255) / 256, 4096);
+  const size_t warps = (size_t)p.batch * p.hkv * R;
+  const int blocks = (int)((warps + 7) / 8);
   attn_combine_kernel<T, D><<<blocks, 256, 0, st>>>(p);
   count_launches(1);
   return launch_status();
