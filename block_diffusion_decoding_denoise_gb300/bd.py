@@ -27,7 +27,8 @@ STATUS = {0: "BD_OK", 1: "BD_ERR_INVALID_ARG", 2: "BD_ERR_UNSUPPORTED", 3: "BD_E
 # every symbol include/bd.h declares
 EXPORTS = ("bd_block_attention_workspace", "bd_block_attention",
            "bd_confidence_commit_workspace", "bd_confidence_commit",
-           "bd_append_block_kv", "bd_status_string", "bd_version", "bd_kernel_launches")
+           "bd_append_block_kv", "bd_status_string", "bd_version", "bd_kernel_launches",
+           "bd_confidence_commit_noalloc")
 
 
 class BDError(RuntimeError):
@@ -71,6 +72,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "bd_status_string": (ctypes.c_char_p, [c_int32]),
             "bd_version": (c_int32, []),
             "bd_kernel_launches": (ctypes.c_uint64, []),
+            "bd_confidence_commit_noalloc": (c_int32, [c_int32, c_int32, c_int32, c_int32,
+                                                       c_int32, c_void_p, c_void_p, c_float,
+                                                       c_void_p, c_void_p, c_void_p, c_void_p,
+                                                       c_void_p, c_void_p, c_void_p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -158,6 +163,23 @@ def bd_confidence_commit(hidden_states, lm_head, threshold, tokens, p_max, argma
         _ptr(ws, name="ws"), ws.numel() * ws.element_size(),
         _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check("bd_confidence_commit", st)
+
+
+def bd_confidence_commit_noalloc(hidden_states, lm_head, threshold, tokens, p_max, argmax,
+                                 n_committed, n_masked, dev_status=None, stream=None):
+    """bd_confidence_commit with the library's fixed device scratch array in
+    place of a caller workspace, for callers that cannot allocate (see bd.h)."""
+    B, L, H = hidden_states.shape
+    V = lm_head.shape[0]
+    if lm_head.shape[1] != H or lm_head.dtype != hidden_states.dtype:
+        raise ValueError("lm_head must be [vocab, hidden] with the hidden states' dtype")
+    st = load().bd_confidence_commit_noalloc(
+        _dtype_code(hidden_states), B, L, H, V, _ptr(hidden_states, name="hidden_states"),
+        _ptr(lm_head, name="lm_head"), float(threshold), _ptr(tokens, torch.int32, "tokens"),
+        _ptr(p_max, torch.float32, "p_max"), _ptr(argmax, torch.int32, "argmax"),
+        _ptr(n_committed, torch.int32, "n_committed"), _ptr(n_masked, torch.int32, "n_masked"),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("bd_confidence_commit_noalloc", st)
 
 
 def bd_append_block_kv(kv: PagedKV, k_blk, v_blk, ctx_len, n_masked=None, dev_status=None,

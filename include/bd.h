@@ -148,6 +148,31 @@ bd_status bd_confidence_commit(bd_dtype dtype, int32_t batch, int32_t block_len,
                                int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * bd_confidence_commit_noalloc -- bd_confidence_commit without a caller
+ * workspace.  The paper has no counterpart to this call: it exists for
+ * callers that cannot allocate device memory when they run a step (code
+ * recorded into a CUDA graph, serving runtimes that forbid allocation while a
+ * request is in flight, plugins with no access to their host's allocator).
+ *
+ * Same arguments, results and limits as bd_confidence_commit, minus ws and
+ * ws_bytes.  The scratch space comes from one 8 MiB array in device memory
+ * that the library reserves on every GPU that loads it, for the life of the
+ * process.  Shapes whose bd_confidence_commit_workspace() exceeds 8 MiB are
+ * rejected with BD_ERR_WORKSPACE before any launch (at hidden 2048 and vocab
+ * 151936 on a 152-SM GPU this allows batch * block_len up to about 1400).
+ * The first call on a device looks up the array's address while that device
+ * is current; make that first call before any stream capture starts.  All
+ * calls on a device share the array and leave its contents behind: nothing in
+ * it needs to start at zero, but calls whose executions overlap on the GPU
+ * (unordered streams) race on it.  It allocates and frees nothing.
+ * ------------------------------------------------------------------------ */
+bd_status bd_confidence_commit_noalloc(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                       int32_t hidden, int32_t vocab, const void *hidden_states,
+                                       const void *lm_head, float threshold, int32_t *tokens,
+                                       float *p_max, int32_t *argmax, int32_t *n_committed,
+                                       int32_t *n_masked, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
  * bd_append_block_kv -- append a finished block's K/V to the paged cache
  * (novelty paragraph: block-causal structure lets earlier blocks' K/V be
  * reused).  For every sequence b with n_masked[b] == 0 (NULL = all):
