@@ -46,6 +46,8 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--check-every", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="launch every kernel from the host instead of replaying CUDA graphs")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="workload name (the headline line uses sdar_b1)")
     return ap.parse_args()
@@ -271,38 +273,61 @@ def run_cuda(a):
     ctx0 = eng.ctx_len.clone()
     stream = torch.cuda.current_stream()
 
-    # per-call events around bd_confidence_commit (the dominant call)
-    conf_events = []
+    # per-call CUDA events around both calls of every denoise step.  With CUDA
+    # graphs the events are captured as event-record nodes, so every replay
+    # re-records them; they are read after each chunk (the engine syncs there).
+    use_graphs = not a.no_graphs
+    ev_kw = {"enable_timing": True}
+    if use_graphs:
+        try:
+            torch.cuda.Event(enable_timing=True, external=True)
+            ev_kw["external"] = True
+        except TypeError:
+            use_graphs = False           # this torch cannot time inside a graph
     orig_step = eng.step
-
-    attn_events = []
+    step_events = {}
+    attn_ms, conf_ms, rows_seen = [], [], []
+    stride = eng.n_committed.stride(0) * eng.n_committed.element_size()
 
     def timed_step(hh, qq, kk, vv, ncom=None, layer=0):
-        ea = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        ea[0].record(stream)
+        s = (ncom.data_ptr() - eng.n_committed.data_ptr()) // stride
+        ea = [torch.cuda.Event(**ev_kw) for _ in range(3)]
+        ea[0].record(torch.cuda.current_stream())
         bd.bd_block_attention(eng.caches[layer].kv, eng.ctx_len, eng.tokens, qq, kk, vv,
                               eng.attn_out, eng.attn_ws, eng.max_ctx, dev_status=eng.dev_status)
-        ea[1].record(stream)
-        bd.bd_confidence_commit(hh, eng.W, eng.T, eng.tokens, eng.p_max, eng.argmax,
-                                eng.n_committed[0] if ncom is None else ncom, eng.n_masked,
-                                eng.conf_ws, dev_status=eng.dev_status)
-        ea[2].record(stream)
-        attn_events.append((ea[0], ea[1]))
-        conf_events.append((ea[1], ea[2]))
+        ea[1].record(torch.cuda.current_stream())
+        bd.bd_confidence_commit(hh, eng.W, eng.T, eng.tokens, eng.p_max, eng.argmax, ncom,
+                                eng.n_masked, eng.conf_ws, dev_status=eng.dev_status)
+        ea[2].record(torch.cuda.current_stream())
+        step_events[s] = ea
+
+    recording = [False]
+
+    def on_chunk(s0, s1):
+        if recording[0]:
+            for s in range(s0, s1):
+                ea = step_events[s]
+                attn_ms.append(ea[0].elapsed_time(ea[1]))
+                conf_ms.append(ea[1].elapsed_time(ea[2]))
+                rows_seen.append(s)
+
+    eng.step = timed_step
 
     def block():
         eng.ctx_len.copy_(ctx0)
-        return eng.decode_block(hd, qd, kbd, vbd, check_every=a.check_every)
+        return eng.decode_block(hd, qd, kbd, vbd, check_every=a.check_every, graphs=use_graphs,
+                                on_chunk=on_chunk)
 
-    for _ in range(max(3, a.warmup)):
+    for _ in range(max(3, a.warmup)):     # the first block captures the graphs
         block()
     torch.cuda.synchronize()
     eng.check_status()
 
     # timed region (device-resident inputs)
-    eng.step = timed_step
     steps_issued = 0
+    recording[0] = True
     l0 = bd.bd_kernel_launches()
+    g0 = eng.graph_kernel_launches
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -316,9 +341,9 @@ def run_cuda(a):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    launches = bd.bd_kernel_launches() - l0
+    recording[0] = False
+    launches = (bd.bd_kernel_launches() - l0) + (eng.graph_kernel_launches - g0)
     ms = t0.elapsed_time(t1)
-    eng.step = orig_step
     eng.check_status()
     committed_per_block = int((eng.tokens != -1).sum().item())
     tokens_total = committed_per_block * a.steps
@@ -330,20 +355,15 @@ def run_cuda(a):
     value = tokens_total * world / (ms / 1e3)
 
     # roofline of the dominant call: bd_confidence_commit
-    conf_ms = [e0.elapsed_time(e1) for e0, e1 in conf_events]
     # algorithmic bytes per call: W once, plus the masked rows of h (read) and
     # the per-position outputs; masked rows per step follow the commit trace
     masked_rows = []
     rem = w.batch * w.block_len
     nc = eng.n_committed.cpu().numpy()
     for s in range(nc.shape[0]):
-        if rem <= 0:
-            break
-        masked_rows.append(rem)
+        masked_rows.append(max(rem, 0))
         rem -= int(nc[s].sum())
-    calls_per_block = len(conf_events) // a.steps
-    rows_per_call = [masked_rows[i % calls_per_block] if i % calls_per_block < len(masked_rows)
-                     else 0 for i in range(len(conf_events))]
+    rows_per_call = [masked_rows[s] for s in rows_seen]
     bytes_w = w.vocab * w.hidden * 2
     alg = [bytes_w + r * w.hidden * 2 + w.batch * w.block_len * 12 for r in rows_per_call]
     peak, peak_kind = _peaks()
@@ -355,7 +375,6 @@ def run_cuda(a):
                           "max/sum-exp/argmax + commit)",
                 "peak_source": f"{peak_kind} hbm_gbs"}
     # block attention: K/V of cache + block once per KV head, Q read, O written
-    attn_ms = [e0.elapsed_time(e1) for e0, e1 in attn_events]
     ctx_tot = int(plen.sum())
     attn_bytes = (2 * (ctx_tot + w.batch * w.block_len) * w.num_kv_heads * w.head_dim * 2
                   + 2 * w.batch * w.block_len * w.num_q_heads * w.head_dim * 2)
@@ -368,8 +387,9 @@ def run_cuda(a):
 
     e2e = None
     if not a.no_e2e:
+        eng.step = orig_step
         e2e = _e2e(a, eng, w, h, q, kb, vb, hd, qd, kbd, vbd, ctx0, stream, committed_per_block,
-                   world)
+                   world, use_graphs)
     if rank != 0:
         return
     cpu = None
@@ -382,7 +402,7 @@ def run_cuda(a):
         "config": _config(w, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                               "denoise_steps_per_block": [int(x) for x in steps_per_seq],
                               "denoise_steps_issued": steps_issued // a.steps,
-                              "check_every": a.check_every}),
+                              "check_every": a.check_every, "cuda_graphs": use_graphs}),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches), "clocks": clk.summary(),
         "conf_call_us_mean": 1e3 * statistics.mean(conf_ms) if conf_ms else None,
@@ -391,7 +411,8 @@ def run_cuda(a):
     print(json.dumps(line))
 
 
-def _e2e(a, eng, w, h, q, kb, vb, hd, qd, kbd, vbd, ctx0, stream, committed_per_block, world):
+def _e2e(a, eng, w, h, q, kb, vb, hd, qd, kbd, vbd, ctx0, stream, committed_per_block, world,
+         use_graphs):
     """Same metric through the public API with host buffers: every block copies its
     inputs from pinned host memory and reads the committed tokens back."""
     import torch
@@ -404,18 +425,22 @@ def _e2e(a, eng, w, h, q, kb, vb, hd, qd, kbd, vbd, ctx0, stream, committed_per_
     q_in, k_in, v_in = torch.empty_like(qd), torch.empty_like(kbd), torch.empty_like(vbd)
     h2d = sum(t.numel() * t.element_size() for t in (h_host, q_host, k_host, v_host))
     d2h = tok_host.numel() * tok_host.element_size()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(a.steps):
+    def one():
         h_in.copy_(h_host, non_blocking=True)
         q_in.copy_(q_host, non_blocking=True)
         k_in.copy_(k_host, non_blocking=True)
         v_in.copy_(v_host, non_blocking=True)
         eng.ctx_len.copy_(ctx0)
-        eng.decode_block(h_in, q_in, k_in, v_in, check_every=a.check_every)
+        eng.decode_block(h_in, q_in, k_in, v_in, check_every=a.check_every, graphs=use_graphs)
         tok_host.copy_(eng.tokens, non_blocking=True)
+
+    one()                                  # captures the graphs over these buffers
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(a.steps):
+        one()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)

@@ -25,13 +25,24 @@ static int num_sms() {
   return cached;
 }
 
-// KV split: enough CTAs to cover every SM about twice, page-aligned slices.
+// KV split (page-aligned slices of the keys).  Small problems (at most about
+// 8 pages per SM in all) get one work item per SM, so every SM streams a few
+// pages at once; larger ones get about four items per SM, each at least 8
+// pages long, so the persistent kernel balances ragged sequences.
 static void choose_split(int batch, int hkv, int block_len, int max_ctx, int *num_splits,
                          int *split_keys) {
+  const int sms = num_sms();
   const int nkeys = max_ctx + block_len;
-  const int max_splits = std::max(1, (nkeys + BD_PAGE_SIZE - 1) / BD_PAGE_SIZE);
-  const int want = std::max(1, (2 * num_sms() + batch * hkv - 1) / (batch * hkv));
-  int s = std::min(want, max_splits);
+  const int heads = batch * hkv;
+  const long long pages = (long long)heads * ((nkeys + BD_PAGE_SIZE - 1) / BD_PAGE_SIZE);
+  int s;
+  if (pages <= 8LL * sms) {
+    s = std::max(1, (sms + heads - 1) / heads);
+  } else {
+    s = std::max(1, (4 * sms + heads - 1) / heads);
+    s = std::min(s, std::max(1, nkeys / (8 * BD_PAGE_SIZE)));
+  }
+  s = std::min(s, std::max(1, (nkeys + BD_PAGE_SIZE - 1) / BD_PAGE_SIZE));
   int keys = (nkeys + s - 1) / s;
   keys = (keys + BD_PAGE_SIZE - 1) / BD_PAGE_SIZE * BD_PAGE_SIZE;
   *split_keys = keys;
@@ -68,6 +79,8 @@ __global__ void __launch_bounds__(256) append_kv_kernel(bd_paged_kv kv, int bloc
                                                         const int32_t *n_masked,
                                                         int32_t *dev_status) {
   const int b = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();
   if (n_masked && n_masked[b] != 0) return;
   const int ctx = ctx_len[b];
   const size_t row_bytes = (size_t)kv.head_dim * elem_bytes;           // one head, one token
@@ -178,11 +191,13 @@ BD_API bd_status bd_append_block_kv(const bd_paged_kv *kv, int32_t batch, int32_
   if ((reinterpret_cast<uintptr_t>(k_blk) | reinterpret_cast<uintptr_t>(v_blk)) & 15)
     return BD_ERR_INVALID_ARG;
   const size_t elem = kv->dtype == BD_BF16 ? 2 : 4;
-  append_kv_kernel<<<batch, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      *kv, block_len, elem, static_cast<const char *>(k_blk), static_cast<const char *>(v_blk),
-      ctx_len, n_masked, dev_status);
+  const cudaError_t e = launch_pdl(append_kv_kernel, dim3(batch), dim3(256), 0,
+                                   static_cast<cudaStream_t>(stream), *kv, block_len, elem,
+                                   static_cast<const char *>(k_blk),
+                                   static_cast<const char *>(v_blk), ctx_len, n_masked,
+                                   dev_status);
   count_launches(1);
-  return launch_status();
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
 
 BD_API const char *bd_status_string(bd_status s) {

@@ -32,12 +32,11 @@ __global__ void __launch_bounds__(512) attn_splitkv_simt_kernel(AttnParams p) {
   const int R = p.block_len * group;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nthreads = blockDim.x;
+  pdl_trigger();
+  pdl_wait();
 
-  if (p.tokens) {  // skip sequences whose block is fully committed
-    int any = 0;
-    for (int i = 0; i < p.block_len; ++i) any |= (p.tokens[b * p.block_len + i] == BD_MASK);
-    if (!any) return;
-  }
+  // skip sequences whose block is fully committed
+  if (p.tokens && !block_has_mask(p.tokens + (size_t)b * p.block_len, p.block_len)) return;
   const int ctx = p.ctx_len[b];
   if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) {
     if (split == 0 && g == 0 && threadIdx.x == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
@@ -165,13 +164,11 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p) {
   const int R = p.block_len * group;
   const int wid = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
   if (wid >= p.batch * p.hkv * R) return;
   const int r = wid % R, g = (wid / R) % p.hkv, b = wid / (R * p.hkv);
-  if (p.tokens) {
-    int any = 0;
-    for (int i = 0; i < p.block_len; ++i) any |= (p.tokens[b * p.block_len + i] == BD_MASK);
-    if (!any) return;
-  }
+  if (p.tokens && !block_has_mask(p.tokens + (size_t)b * p.block_len, p.block_len)) return;
   const int ctx = p.ctx_len[b];
   if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) return;
   const int used = (ctx + p.block_len + p.split_keys - 1) / p.split_keys;  // splits with keys
@@ -212,9 +209,9 @@ static bd_status launch_simt(const AttnParams &p, cudaStream_t st) {
       cudaSuccess)
     return BD_ERR_CUDA;
   dim3 grid(p.num_splits, p.hkv, p.batch);
-  kern<<<grid, warps * 32, smem, st>>>(p);
+  const cudaError_t e = launch_pdl(kern, grid, dim3(warps * 32), smem, st, p);
   count_launches(1);
-  if (cudaGetLastError() != cudaSuccess) return BD_ERR_CUDA;
+  if (e != cudaSuccess) return BD_ERR_CUDA;
   return p.num_splits > 1 ? attention_combine(p, st) : BD_OK;
 }
 
@@ -223,9 +220,9 @@ static bd_status launch_combine(const AttnParams &p, cudaStream_t st) {
   const int R = p.block_len * (p.hq / p.hkv);
   const size_t warps = (size_t)p.batch * p.hkv * R;
   const int blocks = (int)((warps + 7) / 8);
-  attn_combine_kernel<T, D><<<blocks, 256, 0, st>>>(p);
+  const cudaError_t e = launch_pdl(attn_combine_kernel<T, D>, dim3(blocks), dim3(256), 0, st, p);
   count_launches(1);
-  return launch_status();
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
 
 bd_status attention_combine(const AttnParams &p, cudaStream_t st) {

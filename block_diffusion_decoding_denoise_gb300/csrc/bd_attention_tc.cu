@@ -21,6 +21,8 @@
 // warp-level MMA has ample throughput.
 #include <math.h>
 
+#include <algorithm>
+
 #include "bd_attention.cuh"
 #include "bd_common.cuh"
 #include "bd_sm100.cuh"
@@ -81,271 +83,403 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)((chunk >> 3) * kHalfBytes + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-template <int D>
-__global__ void __launch_bounds__(256) attn_tc_kernel(const __grid_constant__ CUtensorMap mk_pool,
-                                                      const __grid_constant__ CUtensorMap mv_pool,
-                                                      const __grid_constant__ CUtensorMap mk_blk,
-                                                      const __grid_constant__ CUtensorMap mv_blk,
-                                                      const AttnParams p) {
+// Per-stage description written by the producer before it arms the stage.
+struct TileMeta {
+  int item;   // work item = (sequence, KV head, split)
+  int lo, hi; // valid key rows [lo, hi) of the tile
+  int flags;  // kFirst | kLast | kSkip | kEnd
+};
+constexpr int kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8;
+constexpr int kMaxStages = 12;
+
+// Persistent, warp-specialised block attention.
+//   warp 0        producer: walks this CTA's work items (item = blockIdx.x +
+//                 i * gridDim.x over (sequence, KV head, split)), and for each
+//                 tile (one cached page, or the block's own keys) arms a ring
+//                 stage with the tile's TMA loads and a TileMeta record
+//   warps 1..NW   consumers: warp w owns query rows [16(w-1), 16w) of the
+//                 item; it runs Q K^T, the online softmax and P V on each
+//                 stage, releases the stage, and writes the item's output (or
+//                 its split partial) after the item's last tile
+// A sentinel stage (kEnd) tells the consumers that the producer is done.
+template <int D, int RG, int KH>
+__global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap mk_pool,
+                   const __grid_constant__ CUtensorMap mv_pool,
+                   const __grid_constant__ CUtensorMap mk_blk,
+                   const __grid_constant__ CUtensorMap mv_blk, const AttnParams p, int S) {
   constexpr int NH = D / 64;                  // 64-column halves per row
   constexpr int TILE = NH * kHalfBytes;       // one K (or V) tile
   constexpr int KSTEPS = D / 16;
   constexpr int DN = D / 8;                   // 8-wide output column tiles
+  constexpr int NW = RG * KH;                 // consumer warps
+  constexpr size_t kXchgBytes = KH == 2 ? (size_t)RG * (4 * DN + 4) * 32 * 4 : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *bufk[2] = {smem, smem + 2 * TILE};
-  uint8_t *bufv[2] = {smem + TILE, smem + 3 * TILE};
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + 4 * TILE);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * 2 * TILE + kXchgBytes);
+  uint64_t *empty = full + kMaxStages;
+  TileMeta *meta = reinterpret_cast<TileMeta *>(empty + kMaxStages);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(meta + kMaxStages);
 
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int group = p.hq / p.hkv;
   const int R = p.block_len * group;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = p.block_len;
-
-  if (p.tokens) {
-    int any = 0;
-    for (int i = 0; i < L; ++i) any |= (p.tokens[b * L + i] == BD_MASK);
-    if (!any) return;
-  }
-  const int ctx = p.ctx_len[b];
-  if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) {
-    if (split == 0 && g == 0 && threadIdx.x == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
-    return;
-  }
-  const int kbeg = split * p.split_keys;
-  const int kend = min(ctx + L, kbeg + p.split_keys);
-  if (kbeg >= kend) return;                   // this split holds no key of this sequence
-  const int p_first = kbeg / kPageRows;
-  const int p_end = kbeg < ctx ? (min(kend, ctx) + kPageRows - 1) / kPageRows : p_first;
-  const int npg = p_end - p_first;
-  const int ntiles = npg + (kend > ctx ? 1 : 0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nitems = p.batch * p.hkv * p.num_splits;
 
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&full[0]), 1);
-    mbar_init(smem_u32(&full[1]), 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), NW);
+    }
+    *abort_flag = 0;
     fence_barrier_init();
   }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mk_pool);
+    tma_prefetch_desc(&mv_pool);
+    tma_prefetch_desc(&mk_blk);
+    tma_prefetch_desc(&mv_blk);
+  }
   __syncthreads();
+  pdl_trigger();
+  pdl_wait();
 
-  // page id of tile u (-1 for the block tile, -2 for a page id outside the pool)
-  auto tile_page = [&](int u) -> int {
-    if (u >= npg) return -1;
-    const int pg = p.page_table[(size_t)b * p.max_pages + p_first + u];
-    return (pg >= 0 && pg < p.num_pages) ? pg : -2;
-  };
-  auto issue = [&](int u) {
-    const int buf = u & 1;
-    const uint32_t bar = smem_u32(&full[buf]);
-    const int pg = tile_page(u);
-    fence_proxy_async();
-    if (pg >= 0) {
-      mbar_arrive_expect_tx(bar, 2 * TILE);
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        tma_load_4d(smem_u32(bufk[buf] + h * kHalfBytes), &mk_pool, 64 * h, 0, g, pg, bar);
-        tma_load_4d(smem_u32(bufv[buf] + h * kHalfBytes), &mv_pool, 64 * h, 0, g, pg, bar);
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0;
+    bool stop = false;
+    // arm stage `it` (waiting for it to be free); false on timeout or abort
+    auto acquire = [&](uint32_t &s_out) -> bool {
+      const uint32_t s = it % S, round = it / S;
+      int ok = 1;
+      if (lane == 0) {
+        if (*abort_flag) ok = 0;
+        else if (round > 0 && !mbar_wait(smem_u32(&empty[s]), (round - 1) & 1)) {
+          ok = 0;
+          *abort_flag = 1;
+          flag_error(p.dev_status, BD_ERR_TIMEOUT);
+        }
       }
-    } else if (pg == -1) {
-      mbar_arrive_expect_tx(bar, 2 * NH * L * 128);
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        tma_load_4d(smem_u32(bufk[buf] + h * kHalfBytes), &mk_blk, 64 * h, g, 0, b, bar);
-        tma_load_4d(smem_u32(bufv[buf] + h * kHalfBytes), &mv_blk, 64 * h, g, 0, b, bar);
+      s_out = s;
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
+    for (int item = blockIdx.x; item < nitems && !stop; item += gridDim.x) {
+      const int split = item % p.num_splits;
+      const int g = (item / p.num_splits) % p.hkv;
+      const int b = item / (p.num_splits * p.hkv);
+      if (p.tokens && !block_has_mask(p.tokens + (size_t)b * L, L)) continue;
+      const int ctx = p.ctx_len[b];
+      if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) {
+        if (split == 0 && g == 0 && lane == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+        continue;
       }
-    } else {
-      flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
-      mbar_arrive(bar);                       // nothing to load; the tile is skipped
-    }
-  };
-  if (threadIdx.x == 0) issue(0);
-
-  // Q fragments of this warp's 16 rows (A operand, row-major 16x16 per k-step)
-  const int gid = lane >> 2, tig = lane & 3;
-  uint32_t qa[KSTEPS][4];
-  {
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
-    const int r_lo = warp * 16 + gid, r_hi = r_lo + 8;
-    const __nv_bfloat16 *q_lo = nullptr, *q_hi = nullptr;
-    if (r_lo < R) q_lo = q + (((size_t)b * L + r_lo / group) * p.hq + g * group + r_lo % group) * D;
-    if (r_hi < R) q_hi = q + (((size_t)b * L + r_hi / group) * p.hq + g * group + r_hi % group) * D;
+      const int kbeg = split * p.split_keys;
+      const int kend = min(ctx + L, kbeg + p.split_keys);
+      if (kbeg >= kend) continue;              // no key of this sequence in this split
+      const int p_first = kbeg / kPageRows;
+      const int p_end = kbeg < ctx ? (min(kend, ctx) + kPageRows - 1) / kPageRows : p_first;
+      const int npg = p_end - p_first;
+      const int ntiles = npg + (kend > ctx ? 1 : 0);
+      for (int u = 0; u < ntiles; ++u, ++it) {
+        uint32_t s;
+        if (!acquire(s)) {
+          stop = true;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t bar = smem_u32(&full[s]);
+          uint8_t *bk = smem + (size_t)s * 2 * TILE, *bv = bk + TILE;
+          TileMeta m;
+          m.item = item;
+          m.flags = (u == 0 ? kFirst : 0) | (u == ntiles - 1 ? kLast : 0);
+          if (u < npg) {
+            const int pg = p.page_table[(size_t)b * p.max_pages + p_first + u];
+            m.lo = 0;
+            m.hi = min(kPageRows, ctx - (p_first + u) * kPageRows);
+            if (pg >= 0 && pg < p.num_pages) {
+              meta[s] = m;
+              fence_proxy_async();
+              mbar_arrive_expect_tx(bar, 2 * TILE);
 #pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
-      const int c = kk * 16 + tig * 2;
-      qa[kk][0] = q_lo ? *reinterpret_cast<const uint32_t *>(q_lo + c) : 0u;
-      qa[kk][1] = q_hi ? *reinterpret_cast<const uint32_t *>(q_hi + c) : 0u;
-      qa[kk][2] = q_lo ? *reinterpret_cast<const uint32_t *>(q_lo + c + 8) : 0u;
-      qa[kk][3] = q_hi ? *reinterpret_cast<const uint32_t *>(q_hi + c + 8) : 0u;
-    }
-  }
-
-  const float sl2 = p.scale * 1.4426950408889634f;   // softmax scale in base 2
-  float o[DN][4];
+              for (int h = 0; h < NH; ++h) {
+                tma_load_4d(smem_u32(bk + h * kHalfBytes), &mk_pool, 64 * h, 0, g, pg, bar);
+                tma_load_4d(smem_u32(bv + h * kHalfBytes), &mv_pool, 64 * h, 0, g, pg, bar);
+              }
+            } else {
+              flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+              m.flags |= kSkip;
+              meta[s] = m;
+              mbar_arrive(bar);
+            }
+          } else {
+            m.lo = max(kbeg, ctx) - ctx;
+            m.hi = kend - ctx;
+            meta[s] = m;
+            fence_proxy_async();
+            mbar_arrive_expect_tx(bar, 2 * NH * L * 128);
 #pragma unroll
-  for (int j = 0; j < DN; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  bool aborted = false;
-  int u_stop = 0;
-
-  for (int u = 0; u < ntiles; ++u) {
-    if (threadIdx.x == 0 && u + 1 < ntiles) issue(u + 1);
-    const int buf = u & 1;
-    const bool ok = mbar_wait(smem_u32(&full[buf]), (u >> 1) & 1);
-    if (__syncthreads_or(!ok)) {
-      if (threadIdx.x == 0) flag_error(p.dev_status, BD_ERR_TIMEOUT);
-      aborted = true;
-      u_stop = u;
-      break;
-    }
-    const int pg = tile_page(u);
-    if (pg == -2) {                            // corrupt page id: skip the tile
-      __syncthreads();
-      continue;
-    }
-    // valid key rows [lo, hi) of this tile
-    int lo = 0, hi;
-    if (pg >= 0) {
-      hi = min(kPageRows, ctx - (p_first + u) * kPageRows);
-    } else {
-      lo = max(kbeg, ctx) - ctx;
-      hi = kend - ctx;
-    }
-    const uint32_t kbase = smem_u32(bufk[buf]);
-    const uint32_t vbase = smem_u32(bufv[buf]);
-    const int hi16 = (hi + 15) & ~15;
-    if (hi & 15) {                             // rows past the valid ones feed P = 0: make them finite
-      for (int e = threadIdx.x; e < (hi16 - hi) * NH * 8; e += blockDim.x) {
-        const int row = hi + e / (NH * 8), chunk = e % (NH * 8);
-        *reinterpret_cast<int4 *>(bufv[buf] + swz(row, chunk)) = make_int4(0, 0, 0, 0);
+            for (int h = 0; h < NH; ++h) {
+              tma_load_4d(smem_u32(bk + h * kHalfBytes), &mk_blk, 64 * h, g, 0, b, bar);
+              tma_load_4d(smem_u32(bv + h * kHalfBytes), &mv_blk, 64 * h, g, 0, b, bar);
+            }
+          }
+        }
+        __syncwarp();
       }
-      __syncthreads();
     }
-
-    // S = Q K^T for this warp's 16 rows x 64 keys
-    float s[8][4];
+    // sentinel: tells the consumers there is no more work
+    if (!stop) {
+      uint32_t s;
+      if (acquire(s)) {
+        if (lane == 0) {
+          meta[s] = TileMeta{-1, 0, 0, kEnd};
+          mbar_arrive(smem_u32(&full[s]));
+        }
+        ++it;
+      } else {
+        stop = true;
+      }
+    }
+    if (stop && lane == 0) {                   // drain copies that may still be in flight
+      const uint32_t first = it > (uint32_t)S ? it - S : 0;
+      for (uint32_t i = first; i < it; ++i) mbar_wait(smem_u32(&full[i % S]), (i / S) & 1);
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    // warp cw owns rows [16 rg, 16 rg + 16) and, when KH == 2, one half of the
+    // keys of every tile; the two key halves of a row group merge at item end
+    const int cw = warp - 1;
+    const int rg = cw % RG, kh = cw / RG;
+    constexpr int KJ = 8 / KH;                 // 8-key column tiles per warp
+    const int key0 = kh * 8 * KJ;              // first key of this warp within a tile
+    const int gid = lane >> 2, tig = lane & 3;
+    const float sl2 = p.scale * 1.4426950408889634f;   // softmax scale in base 2
+    float *xchg = reinterpret_cast<float *>(smem + (size_t)S * 2 * TILE);   // key-half exchange
+    uint32_t qa[KSTEPS][4];
+    float o[DN][4];
+    float m_run[2], l_run[2];
+    int b = 0, g = 0, split = 0;
+    for (uint32_t it = 0;; ++it) {
+      const uint32_t s = it % S;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(smem_u32(&full[s]), (it / S) & 1) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          flag_error(p.dev_status, BD_ERR_TIMEOUT);
+        }
+        break;
+      }
+      TileMeta m;
+      {
+        const volatile int *mv = reinterpret_cast<const volatile int *>(&meta[s]);
+        m.item = mv[0];
+        m.lo = mv[1];
+        m.hi = mv[2];
+        m.flags = mv[3];
+      }
+      if (m.flags & kEnd) break;
+      if (m.flags & kFirst) {
+        split = m.item % p.num_splits;
+        g = (m.item / p.num_splits) % p.hkv;
+        b = m.item / (p.num_splits * p.hkv);
+        const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+        const int r_lo = rg * 16 + gid, r_hi = r_lo + 8;
+        const __nv_bfloat16 *q_lo = nullptr, *q_hi = nullptr;
+        if (r_lo < R)
+          q_lo = q + (((size_t)b * L + r_lo / group) * p.hq + g * group + r_lo % group) * D;
+        if (r_hi < R)
+          q_hi = q + (((size_t)b * L + r_hi / group) * p.hq + g * group + r_hi % group) * D;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+          const int c = kk * 16 + tig * 2;
+          qa[kk][0] = q_lo ? *reinterpret_cast<const uint32_t *>(q_lo + c) : 0u;
+          qa[kk][1] = q_hi ? *reinterpret_cast<const uint32_t *>(q_hi + c) : 0u;
+          qa[kk][2] = q_lo ? *reinterpret_cast<const uint32_t *>(q_lo + c + 8) : 0u;
+          qa[kk][3] = q_hi ? *reinterpret_cast<const uint32_t *>(q_hi + c + 8) : 0u;
+        }
 #pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
+        for (int j = 0; j < DN; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
+      }
+      // this warp's valid keys of the tile: [max(lo, key0), min(hi, key0 + 8 KJ))
+      const int lo = m.lo, hi = m.hi;
+      const int w_lo = max(lo, key0), w_hi = min(hi, key0 + 8 * KJ);
+      if (!(m.flags & kSkip) && w_lo < w_hi) {
+        uint8_t *bk = smem + (size_t)s * 2 * TILE, *bv = bk + TILE;
+        const uint32_t kbase = smem_u32(bk), vbase = smem_u32(bv);
+        const int hi16 = (w_hi + 15) & ~15;
+        const bool zeroed = (w_hi & 15) != 0;
+        if (zeroed) {                          // rows past the valid ones feed P = 0: make them finite
+          for (int e = lane; e < (hi16 - w_hi) * NH * 8; e += 32) {
+            const int row = w_hi + e / (NH * 8), chunk = e % (NH * 8);
+            *reinterpret_cast<int4 *>(bv + swz(row, chunk)) = make_int4(0, 0, 0, 0);
+          }
+          __syncwarp();
+        }
+        // S = Q K^T for this warp's 16 rows x 8 KJ keys
+        float sc[KJ][4];
 #pragma unroll
-      for (int jp = 0; jp < 4; ++jp) {
-        if (16 * jp < hi) {
-          const int key = 16 * jp + (lane & 7) + ((lane >> 4) << 3);
-          const int chunk = 2 * kk + ((lane >> 3) & 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kbase + swz(key, chunk), b0, b1, b2, b3);
-          mma_16816(s[2 * jp], qa[kk], b0, b1);
-          mma_16816(s[2 * jp + 1], qa[kk], b2, b3);
+        for (int j = 0; j < KJ; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+#pragma unroll
+          for (int jp = 0; jp < KJ / 2; ++jp) {
+            if (key0 + 16 * jp < w_hi) {
+              const int key = key0 + 16 * jp + (lane & 7) + ((lane >> 4) << 3);
+              const int chunk = 2 * kk + ((lane >> 3) & 1);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(kbase + swz(key, chunk), b0, b1, b2, b3);
+              mma_16816(sc[2 * jp], qa[kk], b0, b1);
+              mma_16816(sc[2 * jp + 1], qa[kk], b2, b3);
+            }
+          }
+        }
+        float mt[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int j = 0; j < KJ; ++j) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int key = key0 + 8 * j + tig * 2 + (e & 1);
+            if (key < w_lo || key >= w_hi) sc[j][e] = -INFINITY;
+            mt[e >> 1] = fmaxf(mt[e >> 1], sc[j][e]);
+          }
+        }
+        float corr[2], mneg[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], 1));
+          mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], 2));
+          const float mnew = fmaxf(m_run[i], mt[i]);
+          corr[i] = exp2f((m_run[i] - mnew) * sl2);
+          m_run[i] = mnew;
+          mneg[i] = -mnew * sl2;
+          l_run[i] *= corr[i];
+        }
+#pragma unroll
+        for (int j = 0; j < DN; ++j) {
+          o[j][0] *= corr[0];
+          o[j][1] *= corr[0];
+          o[j][2] *= corr[1];
+          o[j][3] *= corr[1];
+        }
+#pragma unroll
+        for (int j = 0; j < KJ; ++j) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sc[j][e] = exp2f(fmaf(sc[j][e], sl2, mneg[e >> 1]));
+            l_run[e >> 1] += sc[j][e];
+          }
+        }
+        uint32_t pa[KJ / 2][4];
+#pragma unroll
+        for (int kk = 0; kk < KJ / 2; ++kk) {
+          pa[kk][0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
+          pa[kk][1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
+          pa[kk][2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+          pa[kk][3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+        }
+#pragma unroll
+        for (int kk = 0; kk < KJ / 2; ++kk) {
+          if (key0 + 16 * kk < hi16) {
+#pragma unroll
+            for (int dp = 0; dp < DN / 2; ++dp) {
+              const int key = key0 + 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
+              const int chunk = 2 * dp + (lane >> 4);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4_t(vbase + swz(key, chunk), b0, b1, b2, b3);
+              mma_16816(o[2 * dp], pa[kk], b0, b1);
+              mma_16816(o[2 * dp + 1], pa[kk], b2, b3);
+            }
+          }
+        }
+        if (zeroed) fence_proxy_async();       // our generic writes precede the next TMA fill
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+      if (m.flags & kLast) {
+        if (KH == 2) {
+          // merge the two key halves of the row group: half 1 hands over, half 0 writes
+          constexpr int F = 4 * DN + 4;        // floats per lane: o[DN][4] + m[2], l[2]
+          float *xw = xchg + (size_t)rg * F * 32;
+          if (kh == 1) {
+#pragma unroll
+            for (int j = 0; j < DN; ++j)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) xw[(j * 4 + e) * 32 + lane] = o[j][e];
+            xw[(4 * DN + 0) * 32 + lane] = m_run[0];
+            xw[(4 * DN + 1) * 32 + lane] = m_run[1];
+            xw[(4 * DN + 2) * 32 + lane] = l_run[0];
+            xw[(4 * DN + 3) * 32 + lane] = l_run[1];
+          }
+          named_barrier(1 + rg, 64);
+          if (kh == 0) {
+            float w0[2], w1[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const float mo = xw[(4 * DN + i) * 32 + lane];
+              const float mnew = fmaxf(m_run[i], mo);
+              w0[i] = m_run[i] == -INFINITY ? 0.f : exp2f((m_run[i] - mnew) * sl2);
+              w1[i] = mo == -INFINITY ? 0.f : exp2f((mo - mnew) * sl2);
+              l_run[i] = l_run[i] * w0[i] + xw[(4 * DN + 2 + i) * 32 + lane] * w1[i];
+              m_run[i] = mnew;
+            }
+#pragma unroll
+            for (int j = 0; j < DN; ++j)
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                o[j][e] = o[j][e] * w0[e >> 1] + xw[(j * 4 + e) * 32 + lane] * w1[e >> 1];
+          }
+          named_barrier(1 + rg, 64);           // exchange slot free for the next item
+        }
+        if (kh == 0) {
+          float lsum[2];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            lsum[i] = l_run[i] + __shfl_xor_sync(0xffffffffu, l_run[i], 1);
+            lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], 2);
+          }
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int r = rg * 16 + gid + 8 * i;
+            if (r >= R) continue;
+            const int qi = r / group, h = g * group + r % group;
+            if (p.num_splits == 1) {
+              const float inv = lsum[i] > 0.f ? 1.f / lsum[i] : 0.f;
+              __nv_bfloat16 *out =
+                  static_cast<__nv_bfloat16 *>(p.out) + (((size_t)b * L + qi) * p.hq + h) * D;
+#pragma unroll
+              for (int j = 0; j < DN; ++j)
+                *reinterpret_cast<uint32_t *>(out + 8 * j + tig * 2) =
+                    pack_bf16(o[j][2 * i] * inv, o[j][2 * i + 1] * inv);
+            } else {
+              const size_t prow = (((size_t)b * p.hkv + g) * p.num_splits + split) * R + r;
+#pragma unroll
+              for (int j = 0; j < DN; ++j)
+                *reinterpret_cast<float2 *>(p.part_o + prow * D + 8 * j + tig * 2) =
+                    make_float2(o[j][2 * i], o[j][2 * i + 1]);
+              if (tig == 0) {
+                p.part_ml[prow * 2 + 0] = m_run[i] * p.scale;   // natural-log units
+                p.part_ml[prow * 2 + 1] = lsum[i];
+              }
+            }
+          }
         }
       }
     }
-    // mask, online softmax (rows gid and gid + 8 of the warp)
-    float mt[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = 8 * j + tig * 2 + (e & 1);
-        if (key < lo || key >= hi) s[j][e] = -INFINITY;
-        mt[e >> 1] = fmaxf(mt[e >> 1], s[j][e]);
-      }
-    }
-    float corr[2], mneg[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], 1));
-      mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], 2));
-      const float mnew = fmaxf(m_run[i], mt[i]);
-      corr[i] = exp2f((m_run[i] - mnew) * sl2);
-      m_run[i] = mnew;
-      mneg[i] = -mnew * sl2;
-      l_run[i] *= corr[i];
-    }
-#pragma unroll
-    for (int j = 0; j < DN; ++j) {
-      o[j][0] *= corr[0];
-      o[j][1] *= corr[0];
-      o[j][2] *= corr[1];
-      o[j][3] *= corr[1];
-    }
-    uint32_t pa[4][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        s[j][e] = exp2f(fmaf(s[j][e], sl2, mneg[e >> 1]));
-        l_run[e >> 1] += s[j][e];
-      }
-    }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      pa[kk][0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-      pa[kk][1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-      pa[kk][2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      pa[kk][3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-    }
-    // O += P V
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      if (16 * kk < hi16) {
-#pragma unroll
-        for (int dp = 0; dp < DN / 2; ++dp) {
-          const int key = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
-          const int chunk = 2 * dp + (lane >> 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vbase + swz(key, chunk), b0, b1, b2, b3);
-          mma_16816(o[2 * dp], pa[kk], b0, b1);
-          mma_16816(o[2 * dp + 1], pa[kk], b2, b3);
-        }
-      }
-    }
-    __syncthreads();                           // buffer free for the load two tiles ahead
   }
-
-  if (aborted) {
-    // wait (bounded) for copies still in flight before the CTA's smem goes away
-    if (threadIdx.x == 0)
-      for (int v = u_stop; v < ntiles && v < u_stop + 2; ++v)
-        mbar_wait(smem_u32(&full[v & 1]), (v >> 1) & 1);
-    return;
-  }
-
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 1);
-    l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 2);
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int r = warp * 16 + gid + 8 * i;
-    if (r >= R) continue;
-    const int qi = r / group, h = g * group + r % group;
-    if (p.num_splits == 1) {
-      const float inv = l_run[i] > 0.f ? 1.f / l_run[i] : 0.f;
-      __nv_bfloat16 *out =
-          static_cast<__nv_bfloat16 *>(p.out) + (((size_t)b * L + qi) * p.hq + h) * D;
-#pragma unroll
-      for (int j = 0; j < DN; ++j)
-        *reinterpret_cast<uint32_t *>(out + 8 * j + tig * 2) =
-            pack_bf16(o[j][2 * i] * inv, o[j][2 * i + 1] * inv);
-    } else {
-      const size_t prow = (((size_t)b * p.hkv + g) * p.num_splits + split) * R + r;
-#pragma unroll
-      for (int j = 0; j < DN; ++j)
-        *reinterpret_cast<float2 *>(p.part_o + prow * D + 8 * j + tig * 2) =
-            make_float2(o[j][2 * i], o[j][2 * i + 1]);
-      if (tig == 0) {
-        p.part_ml[prow * 2 + 0] = m_run[i] * p.scale;   // natural-log units, like the SIMT path
-        p.part_ml[prow * 2 + 1] = l_run[i];
-      }
-    }
-  }
+  __syncthreads();
 }
 
-template <int D>
+template <int D, int RG, int KH>
 bd_status launch(const AttnParams &p, cudaStream_t st) {
+  constexpr int NW = RG * KH;
+  constexpr size_t kXchgBytes = KH == 2 ? (size_t)RG * (4 * (D / 8) + 4) * 32 * 4 : 0;
   constexpr int NH = D / 64;
+  constexpr int TILE = NH * kHalfBytes;
   const uint64_t eb = 2;
   CUtensorMap mkp, mvp, mkb, mvb;
   const uint64_t pdims[4] = {(uint64_t)D, (uint64_t)p.page_size, (uint64_t)p.hkv,
@@ -363,17 +497,20 @@ bd_status launch(const AttnParams &p, cudaStream_t st) {
       !tma_encode_bf16(&mkb, 4, p.k_blk, bdims, bstr, bbox) ||
       !tma_encode_bf16(&mvb, 4, p.v_blk, bdims, bstr, bbox))
     return BD_ERR_CUDA;
-  const int R = p.block_len * (p.hq / p.hkv);
-  const int warps = (R + 15) / 16;
-  const size_t smem = 4 * (size_t)NH * kHalfBytes + 64 + 1024;
-  auto kern = attn_tc_kernel<D>;
+  const size_t ctrl = kMaxStages * (2 * sizeof(uint64_t) + sizeof(TileMeta)) + 16;
+  const int S = (int)std::min<size_t>(kMaxStages,
+                                      (200 * 1024 - ctrl - kXchgBytes) / (2 * TILE));
+  const size_t smem = (size_t)S * 2 * TILE + kXchgBytes + ctrl + 1024;
+  auto kern = attn_tc_kernel<D, RG, KH>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return BD_ERR_CUDA;
-  dim3 grid(p.num_splits, p.hkv, p.batch);
-  kern<<<grid, warps * 32, smem, st>>>(mkp, mvp, mkb, mvb, p);
+  const int nitems = p.batch * p.hkv * p.num_splits;
+  const int grid = std::max(1, std::min(nitems, std::max(dev_info().sms, 1)));
+  const cudaError_t e =
+      launch_pdl(kern, dim3(grid), dim3((NW + 1) * 32), smem, st, mkp, mvp, mkb, mvb, p, S);
   count_launches(1);
-  return launch_status();
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
 
 }  // namespace
@@ -385,7 +522,13 @@ bd_status attention_tc(const AttnParams &p, cudaStream_t st) {
   if ((reinterpret_cast<uintptr_t>(p.q) & 3) != 0) return BD_ERR_UNSUPPORTED;
   const DevInfo d = dev_info();
   if (d.major < 10 || !tma_available()) return BD_ERR_UNSUPPORTED;
-  const bd_status s = p.head_dim == 64 ? launch<64>(p, st) : launch<128>(p, st);
+  const int R = p.block_len * (p.hq / p.hkv);
+  bd_status s;
+  // up to 64 rows: 4 row groups x 2 key halves; up to 128 rows: 8 row groups
+  if (p.head_dim == 64)
+    s = R <= 64 ? launch<64, 4, 2>(p, st) : launch<64, 8, 1>(p, st);
+  else
+    s = R <= 64 ? launch<128, 4, 2>(p, st) : launch<128, 8, 1>(p, st);
   if (s != BD_OK || p.num_splits == 1) return s;
   return attention_combine(p, st);
 }

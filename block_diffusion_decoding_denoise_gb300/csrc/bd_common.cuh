@@ -17,6 +17,40 @@ __device__ __forceinline__ void flag_error(int32_t *dev_status, int32_t code) {
   if (dev_status) atomicCAS(dev_status, 0, code);
 }
 
+// Programmatic dependent launch: every kernel of the library is launched so
+// that it may start while the previous kernel on the stream drains.  A kernel
+// calls pdl_wait() before it touches global memory that earlier stream work
+// writes or reads, and pdl_trigger() once its own dependents may be scheduled.
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Whether any of the block_len (<= 32) tokens is still masked; one load per
+// lane, so the answer costs one memory latency.  Call with the full warp.
+__device__ __forceinline__ bool block_has_mask(const int32_t *tokens, int block_len) {
+  const int lane = threadIdx.x & 31;
+  const bool m = lane < block_len && tokens[lane] == BD_MASK;
+  return __any_sync(0xffffffffu, m);
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 

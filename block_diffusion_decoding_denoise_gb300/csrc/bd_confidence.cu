@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(1024) conf_prep_kernel(const int32_t *tokens, 
   __shared__ int carry;
   __shared__ int list_n;
   __shared__ int2 list[1024];
+  pdl_trigger();
+  pdl_wait();
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -74,7 +76,10 @@ __global__ void __launch_bounds__(1024) conf_prep_kernel(const int32_t *tokens, 
     }
     __syncthreads();
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) *ws.count = carry;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *ws.count = carry;
+    *ws.ticket = 0;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -88,6 +93,8 @@ __global__ void __launch_bounds__(256) lmhead_simt_kernel(ConfParams p) {
   __shared__ float As[kSimtK][kSimtRows + 4];
   __shared__ float Bs[kSimtK][kSimtVocab + 4];
   __shared__ MaxSumArg state[kSimtRows];
+  pdl_trigger();
+  pdl_wait();
   const int count = *p.ws.count;
   const int r0 = blockIdx.y * kSimtRows;
   if (r0 >= count) return;
@@ -169,12 +176,11 @@ __global__ void __launch_bounds__(256) lmhead_simt_kernel(ConfParams p) {
 bd_status lmhead_simt(const ConfParams &p, cudaStream_t st) {
   const int nrows = p.batch * p.block_len;
   dim3 grid((p.vocab + kSimtChunk - 1) / kSimtChunk, (nrows + kSimtRows - 1) / kSimtRows);
-  if (p.dtype == BD_F32)
-    lmhead_simt_kernel<float><<<grid, 256, 0, st>>>(p);
-  else
-    lmhead_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+  const cudaError_t e =
+      p.dtype == BD_F32 ? launch_pdl(lmhead_simt_kernel<float>, grid, dim3(256), 0, st, p)
+                        : launch_pdl(lmhead_simt_kernel<__nv_bfloat16>, grid, dim3(256), 0, st, p);
   count_launches(1);
-  return launch_status();
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------------------
@@ -186,6 +192,8 @@ __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
   __shared__ int s_am[32];
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = p.block_len;
+  pdl_trigger();
+  pdl_wait();
   if (warp < L) {
     const int pos = b * L + warp;
     float pm = -1.f;
@@ -203,14 +211,7 @@ __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
         other.idx = __shfl_xor_sync(0xffffffffu, st.idx, o);
         st = merge(st, other);
       }
-      if (st.idx < 0 || st.idx >= p.vocab || !(st.s >= 1.f)) {
-        if (lane == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
-        pm = 0.f;
-        am = 0;
-      } else {
-        pm = 1.f / st.s;
-        am = st.idx;
-      }
+      if (lane == 0) finalize_row(p, st, pm, am);
     }
     if (lane == 0) {
       s_pm[warp] = pm;
@@ -219,37 +220,8 @@ __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
   }
   __syncthreads();
   if (warp != 0) return;
-  const int pos = b * L + lane;
-  const bool in = lane < L;
-  const bool masked = in && p.tokens[pos] == BD_MASK;
-  const float pm = in ? s_pm[lane] : -1.f;
-  const int am = in ? s_am[lane] : -1;
-  const unsigned mmask = __ballot_sync(0xffffffffu, masked);
-  unsigned sel = __ballot_sync(0xffffffffu, masked && pm >= p.threshold);
-  if (sel == 0u && mmask != 0u) {
-    // fallback: the most confident masked position, lowest position on ties
-    float best = masked ? pm : -INFINITY;
-    int who = masked ? lane : 32;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-      const int ow = __shfl_xor_sync(0xffffffffu, who, o);
-      if (ob > best || (ob == best && ow < who)) {
-        best = ob;
-        who = ow;
-      }
-    }
-    sel = 1u << who;
-  }
-  if (in) {
-    p.p_max[pos] = pm;
-    p.argmax[pos] = am;
-    if ((sel >> lane) & 1u) p.tokens[pos] = am;
-  }
-  if (lane == 0) {
-    p.n_committed[b] = __popc(sel);
-    p.n_masked[b] = __popc(mmask) - __popc(sel);
-  }
+  const bool masked = lane < L && p.tokens[b * L + lane] == BD_MASK;
+  commit_sequence_warp(p, b, masked, masked ? s_pm[lane] : -1.f, masked ? s_am[lane] : -1);
 }
 
 // ---------------------------------------------------------------------------
@@ -278,6 +250,7 @@ static size_t carve(const ConfParams &p, char *base, ConfWorkspace *ws) {
   char *rows = take(n * 4), *row_of = take(n * 4), *count = take(4);
   char *part = take((size_t)np * n * sizeof(MaxSumArg));
   char *hc = p.dtype == BD_BF16 ? take(n * (size_t)p.hidden * 2) : nullptr;
+  char *ticket = take(4);
   if (ws) {
     ws->rows = reinterpret_cast<int32_t *>(rows);
     ws->row_of = reinterpret_cast<int32_t *>(row_of);
@@ -285,6 +258,7 @@ static size_t carve(const ConfParams &p, char *base, ConfWorkspace *ws) {
     ws->partial = reinterpret_cast<MaxSumArg *>(part);
     ws->num_partials = np;
     ws->hc = hc;
+    ws->ticket = reinterpret_cast<int32_t *>(ticket);
   }
   return off;
 }
@@ -351,15 +325,16 @@ BD_API bd_status bd_confidence_commit(bd_dtype dtype, int32_t batch, int32_t blo
   const int nrows = batch * block_len;
   // the tensor-core path reads the masked rows from a contiguous copy
   const int prep_ctas = tc ? std::max(1, std::min(std::max(dev_info().sms, 1), (nrows + 7) / 8)) : 1;
-  conf_prep_kernel<<<prep_ctas, 1024, 0, st>>>(tokens, nrows, p.ws,
-                                               tc ? static_cast<const char *>(hidden_states)
-                                                  : nullptr,
-                                               hidden * 2);
+  const int32_t *tok_in = tokens;
+  const char *src = tc ? static_cast<const char *>(hidden_states) : nullptr;
+  cudaError_t e = launch_pdl(conf_prep_kernel, dim3(prep_ctas), dim3(1024), 0, st, tok_in, nrows,
+                             p.ws, src, hidden * 2);
   count_launches(1);
-  if (cudaGetLastError() != cudaSuccess) return BD_ERR_CUDA;
-  const bd_status s = tc ? lmhead_tc(p, st) : lmhead_simt(p, st);
-  if (s != BD_OK) return s;
-  conf_commit_kernel<<<batch, 32 * block_len, 0, st>>>(p);
+  if (e != cudaSuccess) return BD_ERR_CUDA;
+  const bool fuse = tc && nrows <= kFuseMaxRows;
+  const bd_status s = tc ? lmhead_tc(p, st, fuse) : lmhead_simt(p, st);
+  if (s != BD_OK || fuse) return s;
+  e = launch_pdl(conf_commit_kernel, dim3(batch), dim3(32 * block_len), 0, st, p);
   count_launches(1);
-  return launch_status();
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }

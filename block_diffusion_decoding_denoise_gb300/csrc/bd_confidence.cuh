@@ -15,11 +15,13 @@ namespace bd {
 //   count    [1]   int32   number of masked rows
 //   partial  [P][B*L] MaxSumArg   one online-softmax state per producer and row
 //   hc       [B*L][H] bf16        masked rows of h, compacted (bf16 only)
+//   ticket   [1]   int32   CTAs of the LM head that finished (zeroed by the prep kernel)
 struct ConfWorkspace {
   int32_t *rows, *row_of, *count;
   MaxSumArg *partial;
   int num_partials;
   char *hc;
+  int32_t *ticket;
 };
 
 struct ConfParams {
@@ -34,12 +36,66 @@ struct ConfParams {
   ConfWorkspace ws;
 };
 
+// Batches up to this many positions (B * L') have the commit fused into the
+// tensor-core LM head (its last CTA merges the partials and decides).
+constexpr int kFuseMaxRows = 64;
+
+// p_max and argmax of a row from its merged online-softmax state.
+__device__ __forceinline__ void finalize_row(const ConfParams &p, const MaxSumArg &st, float &pm,
+                                             int &am) {
+  if (st.idx < 0 || st.idx >= p.vocab || !(st.s >= 1.f)) {
+    flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+    pm = 0.f;
+    am = 0;
+  } else {
+    pm = 1.f / st.s;
+    am = st.idx;
+  }
+}
+
+// Commit decision of sequence b by one warp; lane i (< block_len) holds
+// position i's masked flag and, when masked, its p_max and argmax.
+//   S = { masked i : p_max_i >= T }; if S is empty and a position is masked,
+//   S = { the masked i with the largest p_max, lowest i on ties }.
+__device__ __forceinline__ void commit_sequence_warp(const ConfParams &p, int b, bool masked,
+                                                     float pm, int am) {
+  const int lane = threadIdx.x & 31;
+  const int L = p.block_len;
+  const int pos = b * L + lane;
+  const bool in = lane < L;
+  const unsigned mmask = __ballot_sync(0xffffffffu, masked);
+  unsigned sel = __ballot_sync(0xffffffffu, masked && pm >= p.threshold);
+  if (sel == 0u && mmask != 0u) {
+    float best = masked ? pm : -INFINITY;
+    int who = masked ? lane : 32;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int ow = __shfl_xor_sync(0xffffffffu, who, o);
+      if (ob > best || (ob == best && ow < who)) {
+        best = ob;
+        who = ow;
+      }
+    }
+    sel = 1u << who;
+  }
+  if (in) {
+    p.p_max[pos] = masked ? pm : -1.f;
+    p.argmax[pos] = masked ? am : -1;
+    if ((sel >> lane) & 1u) p.tokens[pos] = am;
+  }
+  if (lane == 0) {
+    p.n_committed[b] = __popc(sel);
+    p.n_masked[b] = __popc(mmask) - __popc(sel);
+  }
+}
+
 // Number of partial states the LM-head kernel of `dtype` produces per row.
 int conf_num_partials(bd_dtype dtype, int batch, int block_len, int hidden, int vocab);
 
 bd_status lmhead_simt(const ConfParams &p, cudaStream_t st);
 bool lmhead_tc_supported(const ConfParams &p);
 int lmhead_tc_num_partials(int vocab);
-bd_status lmhead_tc(const ConfParams &p, cudaStream_t st);
+bd_status lmhead_tc(const ConfParams &p, cudaStream_t st, bool fuse_commit);
 
 }  // namespace bd

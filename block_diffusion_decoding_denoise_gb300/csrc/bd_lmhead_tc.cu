@@ -24,9 +24,10 @@
 //              per stage into one of two TMEM accumulators; tcgen05.commit
 //              frees the stage and, after the last K chunk, hands the
 //              accumulator to the epilogue
-//   warps 2-5  epilogue: tcgen05.ld 32 lanes x 16 columns, per column a warp
-//              max / argmax (ballot) / sum-exp, a 4-warp merge through smem,
-//              and a running state per row kept in registers
+//   warps 2-5  epilogue: tcgen05.ld 32 lanes x 16 columns; a transposing
+//              butterfly over the 32 lanes reduces the 16 columns to one
+//              (max, sum-exp, argmax) each; a 4-warp merge through smem; a
+//              running state per row kept in registers
 // Each CTA writes one partial state per row; conf_commit_kernel merges them.
 // Every mbarrier wait is bounded (1 s); on expiry the kernel records
 // BD_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
@@ -46,11 +47,11 @@ namespace {
 constexpr int kThreads = 192;
 constexpr int kTileV = 128;                 // vocabulary entries per tile (MMA M)
 constexpr int kKChunk = 64;                 // K elements per stage (128 bytes of bf16)
-constexpr int kMaxN = 128;                  // masked rows per pass (MMA N)
+constexpr int kMaxN = 256;                  // masked rows per pass (MMA N)
 constexpr int kBoxRows = 16;                // rows of the compact h copy per TMA box
 constexpr int kABytes = kTileV * 128;       // 16 KB of W per stage
 constexpr int kMaxStages = 12;
-constexpr uint32_t kTmemCols = 2 * kMaxN;   // two accumulators
+constexpr uint32_t kTmemCols = 2 * kMaxN;   // two accumulators (all 512 columns)
 constexpr int kSmemLimit = 227 * 1024;
 
 struct Ctrl {
@@ -61,6 +62,7 @@ struct Ctrl {
   uint64_t mma_done;
   uint32_t tmem_base;
   volatile int32_t abort;
+  int32_t last_cta;
   MaxSumArg red[2][4][kMaxN];
 };
 
@@ -69,6 +71,7 @@ struct LmTcArgs {
   int stages;
   int stage_bytes;
   int num_tiles;
+  int fuse_commit;   // the last CTA merges the partials and commits
 };
 
 __device__ __forceinline__ bool barrier_or(uint32_t id, uint32_t nthreads, bool pred) {
@@ -84,16 +87,87 @@ __device__ __forceinline__ bool barrier_or(uint32_t id, uint32_t nthreads, bool 
   return r != 0;
 }
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
+// Merge the online-softmax state (bm, bs, bi) into (m, s, i): larger max
+// wins, equal maxima keep the lower index, sums are rescaled to the new max.
+__device__ __forceinline__ void merge_into(float &m, float &s, int &i, float bm, float bs,
+                                           int bi) {
+  const bool take = bm > m || (bm == m && bi < i);
+  const float hi_m = take ? bm : m, lo_m = take ? m : bm;
+  const float hi_s = take ? bs : s, lo_s = take ? s : bs;
+  s = hi_s + (lo_s > 0.f ? lo_s * __expf(lo_m - hi_m) : 0.f);
+  m = hi_m;
+  i = take ? bi : i;
 }
 
-__device__ __forceinline__ float warp_sum(float x) {
+// One butterfly round over lanes (lane, lane ^ off): a lane keeps K of its 2K
+// states (the lower half when its `off` bit is clear) and merges in the
+// partner's copy of the same K columns.
+template <int K>
+__device__ __forceinline__ void bfly_round(float (&m)[16], float (&s)[16], int (&id)[16], int off,
+                                           int lane) {
+  const bool upper = (lane & off) != 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
+  for (int k = 0; k < K; ++k) {
+    const float send_m = upper ? m[k] : m[K + k];
+    const float send_s = upper ? s[k] : s[K + k];
+    const int send_i = upper ? id[k] : id[K + k];
+    float km = upper ? m[K + k] : m[k];
+    float ks = upper ? s[K + k] : s[k];
+    int ki = upper ? id[K + k] : id[k];
+    const float rm = __shfl_xor_sync(0xffffffffu, send_m, off);
+    const float rs = __shfl_xor_sync(0xffffffffu, send_s, off);
+    const int ri = __shfl_xor_sync(0xffffffffu, send_i, off);
+    merge_into(km, ks, ki, rm, rs, ri);
+    m[k] = km;
+    s[k] = ks;
+    id[k] = ki;
+  }
+}
+
+// Merge the G per-CTA partial states of each masked row (several threads per
+// row, then a merge through smem) and take every sequence's commit decision
+// (one warp per sequence).  Runs in one CTA after all others finished.
+__device__ __noinline__ void fused_commit(const ConfParams &p, int count, uint8_t *smem, int G) {
+  float *pm_s = reinterpret_cast<float *>(smem);
+  int *am_s = reinterpret_cast<int *>(pm_s + kFuseMaxRows);
+  MaxSumArg *red = reinterpret_cast<MaxSumArg *>(am_s + kFuseMaxRows);
+  const int t = threadIdx.x, T = blockDim.x;
+  const size_t stride = (size_t)p.batch * p.block_len;
+  for (int r0 = 0; r0 < count; r0 += T) {
+    const int nr = min(T, count - r0);
+    const int nsub = T / nr;
+    MaxSumArg st{-INFINITY, 0.f, 0x7fffffff};
+    if (t < nr * nsub) {
+      const int row = r0 + t % nr;
+#pragma unroll 4
+      for (int c = t / nr; c < G; c += nsub) {
+        const MaxSumArg *src = p.ws.partial + (size_t)c * stride + row;
+        MaxSumArg v;
+        v.m = __ldcg(&src->m);
+        v.s = __ldcg(&src->s);
+        v.idx = __ldcg(&src->idx);
+        st = merge(st, v);
+      }
+    }
+    red[t] = st;
+    __syncthreads();
+    if (t < nr) {
+      for (int j = 1; j < nsub; ++j) st = merge(st, red[t + j * nr]);
+      float pm;
+      int am;
+      finalize_row(p, st, pm, am);
+      pm_s[r0 + t] = pm;
+      am_s[r0 + t] = am;
+    }
+    __syncthreads();
+  }
+  const int warp = t >> 5, lane = t & 31, nwarps = T >> 5;
+  for (int b = warp; b < p.batch; b += nwarps) {
+    const int pos = b * p.block_len + lane;
+    const bool masked = lane < p.block_len && p.tokens[pos] == BD_MASK;
+    const int k = masked ? p.ws.row_of[pos] : 0;
+    commit_sequence_warp(p, b, masked, masked ? pm_s[k] : -1.f, masked ? am_s[k] : -1);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -106,9 +180,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ConfParams &p = a.p;
 
-  const int count = *p.ws.count;
-  if (count <= 0) return;                   // nothing masked: uniform early exit
-  const int npass = (count + kMaxN - 1) / kMaxN;
   const int G = gridDim.x, cta = blockIdx.x;
   const int my_tiles = (a.num_tiles - cta + G - 1) / G;
   const int KC = p.hidden / kKChunk;
@@ -140,9 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
+  // set-up above overlaps the previous kernel; the row list is read after it
+  pdl_trigger();
+  pdl_wait();
+  const int count = *p.ws.count;
+  const int npass = count > 0 ? (count + kMaxN - 1) / kMaxN : 0;   // 0: nothing masked
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    const uint64_t w_policy = l2_policy_evict_first();   // W is read once per step
     uint32_t it = 0;
     bool stop = false;
     for (int pass = 0; pass < npass && !stop; ++pass) {
@@ -166,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
               const uint32_t bar = smem_u32(&ctrl->full[s]);
               mbar_arrive_expect_tx(bar, tx);
-              tma_load_2d(smem_u32(st), &tmap_w, kc * kKChunk, vt * kTileV, bar);
+              tma_load_2d_hint(smem_u32(st), &tmap_w, kc * kKChunk, vt * kTileV, bar, w_policy);
               for (int r = 0; r < npad; r += kBoxRows)
                 tma_load_2d(smem_u32(st + kABytes + r * 128), &tmap_h, kc * kKChunk, r0 + r, bar);
             }
@@ -234,14 +311,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;                 // slot of this warp in the merge buffer
     const int q = warp & 3;                  // TMEM sub-partition this warp may read
-    const int tid_e = threadIdx.x - 64;      // 0..127: row of the pass owned in merges
+    const int tid_e = threadIdx.x - 64;      // 0..127: rows tid_e, tid_e + 128 of the pass
     uint32_t tg = 0;
     bool stop = false;
     for (int pass = 0; pass < npass && !stop; ++pass) {
       const int r0 = pass * kMaxN;
       const int n = min(kMaxN, count - r0);
       const int npad = (n + 15) & ~15;
-      MaxSumArg run{-INFINITY, 0.f, 0x7fffffff};
+      MaxSumArg run{-INFINITY, 0.f, 0x7fffffff}, run2{-INFINITY, 0.f, 0x7fffffff};
       for (int t = 0; t < my_tiles; ++t, ++tg) {
         const int vt = cta + t * G;
         const uint32_t acc = tg & 1, use = tg >> 1;
@@ -252,42 +329,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const int vbase = vt * kTileV + 32 * q;
           const bool valid = vbase + lane < p.vocab;
-          MaxSumArg held[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) held[j] = MaxSumArg{-INFINITY, 0.f, 0x7fffffff};
           for (int c0 = 0; c0 < npad; c0 += 16) {
             uint32_t r[16];
             tmem_ld_32x32b_x16(tmem + ((uint32_t)(32 * q) << 16) + acc * kMaxN + c0, r);
             tmem_ld_wait();
+            // 16 columns x 32 vocabulary lanes -> one (max, sum-exp, argmax) per
+            // column, by a transposing butterfly: each round halves the columns a
+            // lane keeps and merges the partner's copy of them
+            float m[16], sx[16];
+            int id[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float x = valid ? __uint_as_float(r[j]) : -INFINITY;
-              const float m = warp_max(x);
-              const unsigned bal = __ballot_sync(0xffffffffu, valid && x == m);
-              MaxSumArg res{-INFINITY, 0.f, 0x7fffffff};
-              if (bal) {
-                res.m = m;
-                res.s = warp_sum(valid ? __expf(x - m) : 0.f);
-                res.idx = vbase + __ffs(bal) - 1;
-              }
-              const int c = c0 + j;
-              if (lane == (c & 31)) {
-                const int slot = c >> 5;
-                if (slot == 0) held[0] = res;
-                else if (slot == 1) held[1] = res;
-                else if (slot == 2) held[2] = res;
-                else held[3] = res;
-              }
+              m[j] = valid ? __uint_as_float(r[j]) : -INFINITY;
+              sx[j] = valid ? 1.f : 0.f;
+              id[j] = valid ? vbase + lane : 0x7fffffff;
             }
+            bfly_round<8>(m, sx, id, 16, lane);
+            bfly_round<4>(m, sx, id, 8, lane);
+            bfly_round<2>(m, sx, id, 4, lane);
+            bfly_round<1>(m, sx, id, 2, lane);
+            {
+              const float om = __shfl_xor_sync(0xffffffffu, m[0], 1);
+              const float os = __shfl_xor_sync(0xffffffffu, sx[0], 1);
+              const int oi = __shfl_xor_sync(0xffffffffu, id[0], 1);
+              merge_into(m[0], sx[0], id[0], om, os, oi);
+            }
+            // lanes 2k and 2k+1 now hold column c0 + k of the 32 lanes' reduction
+            if ((lane & 1) == 0)
+              ctrl->red[tg & 1][ew][c0 + (lane >> 1)] = MaxSumArg{m[0], sx[0], id[0]};
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&ctrl->tempty[acc]));
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int c = lane + 32 * j;
-            if (c < npad) ctrl->red[tg & 1][ew][c] = held[j];
-          }
         } else {
           ctrl->abort = 1;
           if (lane == 0) flag_error(p.dev_status, BD_ERR_TIMEOUT);
@@ -300,8 +373,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int w = 0; w < 4; ++w) run = merge(run, ctrl->red[tg & 1][w][tid_e]);
         }
+        if (tid_e + 128 < npad) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) run2 = merge(run2, ctrl->red[tg & 1][w][tid_e + 128]);
+        }
       }
       if (!stop && tid_e < n) p.ws.partial[(size_t)cta * stride + r0 + tid_e] = run;
+      if (!stop && tid_e + 128 < n) p.ws.partial[(size_t)cta * stride + r0 + tid_e + 128] = run2;
     }
   }
 
@@ -310,6 +388,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  if (a.fuse_commit) {
+    // last CTA to finish: merge every CTA's partial state per row and commit
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) ctrl->last_cta = atomicAdd(p.ws.ticket, 1) == G - 1;
+    __syncthreads();
+    if (ctrl->last_cta) {
+      __threadfence();
+      fused_commit(p, count, smem, G);
+    }
   }
 }
 
@@ -348,9 +437,10 @@ int lmhead_tc_num_partials(int vocab) {
   return std::max(1, std::min(d.sms, num_tiles(vocab)));
 }
 
-bd_status lmhead_tc(const ConfParams &p, cudaStream_t st) {
+bd_status lmhead_tc(const ConfParams &p, cudaStream_t st, bool fuse_commit) {
   LmTcArgs a;
   a.p = p;
+  a.fuse_commit = fuse_commit ? 1 : 0;
   a.num_tiles = num_tiles(p.vocab);
   size_t smem;
   plan(p, &a.stages, &a.stage_bytes, &smem);
@@ -364,9 +454,9 @@ bd_status lmhead_tc(const ConfParams &p, cudaStream_t st) {
     return BD_ERR_CUDA;
   const int grid = p.ws.num_partials;
   if (grid < 1 || grid > a.num_tiles) return BD_ERR_INVALID_ARG;
-  lmhead_tc_kernel<<<grid, kThreads, smem, st>>>(mw, mh, a);
+  const cudaError_t e = launch_pdl(lmhead_tc_kernel, dim3(grid), dim3(kThreads), smem, st, mw, mh, a);
   count_launches(1);
-  return launch_status();
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
 
 }  // namespace bd

@@ -90,6 +90,8 @@ class DenoiseEngine:
         self.attn_ws = torch.empty(max(aws, 1), dtype=torch.uint8, device=dev)
         self.conf_ws = torch.empty(cws, dtype=torch.uint8, device=dev)
         self._host_masked = torch.empty(batch, dtype=torch.int32, pin_memory=True)
+        self._graphs = {}
+        self.graph_kernel_launches = 0   # kernels launched by graph replays
 
     # -- one denoise step ---------------------------------------------------
     def step(self, h, q, k_blk, v_blk, n_committed_out=None, layer: int = 0):
@@ -101,25 +103,53 @@ class DenoiseEngine:
                                 else n_committed_out, self.n_masked, self.conf_ws,
                                 dev_status=self.dev_status)
 
+    # -- CUDA graphs of step chunks -----------------------------------------
+    def _chunk_graph(self, h_steps, q, k_blk, v_blk, s0: int, s1: int):
+        """Graph of denoise steps [s0, s1) over these input buffers (captured once).
+
+        Replaying it issues exactly the launches of the eager loop, with no
+        host work per kernel."""
+        key = (h_steps.data_ptr(), q.data_ptr(), k_blk.data_ptr(), v_blk.data_ptr(), s0, s1,
+               self.step)
+        entry = self._graphs.get(key)
+        if entry is None:
+            g = torch.cuda.CUDAGraph()
+            n0 = bd.bd_kernel_launches()
+            with torch.cuda.graph(g):
+                for s in range(s0, s1):
+                    self.step(h_steps[s], q, k_blk, v_blk, self.n_committed[s])
+            entry = (g, bd.bd_kernel_launches() - n0)
+            self._graphs[key] = entry
+        return entry
+
     # -- one block ----------------------------------------------------------
-    def decode_block(self, h_steps, q, k_blk, v_blk, check_every: int = 8):
+    def decode_block(self, h_steps, q, k_blk, v_blk, check_every: int = 8,
+                     graphs: bool = False, on_chunk=None):
         """Denoise the current block to completion and append its K/V.
 
         h_steps [S, B, L, H] (S >= block_len) holds each step's hidden
-        states.  Returns the number of denoise steps issued; per-sequence step
-        counts are available from `steps_per_sequence()`.
+        states.  Steps run in chunks of `check_every` (replayed CUDA graphs
+        when `graphs`); after each chunk the host reads the masked count and
+        `on_chunk(s0, s1)` is called.  Returns the number of denoise steps
+        issued; per-sequence step counts come from `steps_per_sequence()`.
         """
         self.tokens.fill_(MASK)
         self.n_committed.zero_()
         s = 0
         while True:
-            for _ in range(check_every):
-                if s >= self.L:
-                    break
-                self.step(h_steps[s], q, k_blk, v_blk, self.n_committed[s])
-                s += 1
+            s1 = min(self.L, s + check_every)
+            if graphs:
+                g, n_kernels = self._chunk_graph(h_steps, q, k_blk, v_blk, s, s1)
+                g.replay()
+                self.graph_kernel_launches += n_kernels
+            else:
+                for t in range(s, s1):
+                    self.step(h_steps[t], q, k_blk, v_blk, self.n_committed[t])
             self._host_masked.copy_(self.n_masked, non_blocking=True)
             torch.cuda.current_stream().synchronize()
+            if on_chunk is not None:
+                on_chunk(s, s1)
+            s = s1
             if int(self._host_masked.sum()) == 0 or s >= self.L:
                 break
         bd.bd_append_block_kv(self.caches[0].kv, k_blk, v_blk, self.ctx_len, self.n_masked,

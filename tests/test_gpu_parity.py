@@ -60,6 +60,23 @@ def test_attention_fp32_d128_gqa4():
     _attn_check(w, plen=[200, 64])
 
 
+def test_attention_bf16_gqa4_128_rows():
+    # 32 positions x 4 query heads per KV head = 128 rows: eight row groups per tile
+    w = SMALL_BF16.with_(name="gqa4", num_q_heads=16, num_kv_heads=4, batch=2)
+    _attn_check(w, plen=[333, 64])
+
+
+def test_attention_bf16_head_dim_64():
+    w = SMALL_BF16.with_(name="d64", head_dim=64, num_q_heads=8, num_kv_heads=2, batch=2)
+    _attn_check(w, plen=[190, 0])
+
+
+def test_attention_bf16_long_ragged_batch():
+    # enough pages for the multi-item-per-CTA split (several items per SM)
+    w = SMALL_BF16.with_(name="ragged", batch=6, prefix=3000, prefix_min=100)
+    _attn_check(w, plen=[3000, 100, 2049, 64, 1, 2900], rows_of=[0, 1, 2, 3, 4, 5])
+
+
 def test_attention_block_len_one_is_causal_step():
     # block size 1: the query sees the cache and itself, i.e. one AR step
     w = wl.WORKLOADS["tiny_fp32"].with_(name="ar", block_len=1, batch=2)
@@ -171,6 +188,14 @@ def test_decode_more_rows_than_one_pass():
     W = wl.lm_head(w)
     h, _ = wl.planted_hidden(w, W, 0, a_max=30.0)
     lockstep_block(w, W, h, 0.9)
+
+
+def test_decode_unfused_commit_three_passes():
+    # 9 x 32 = 288 positions: above the fused-commit limit, two LM-head passes
+    w = SMALL_BF16.with_(batch=9)
+    W = wl.lm_head(w)
+    h, _ = wl.planted_hidden(w, W, 0, a_max=30.0)
+    lockstep_block(w, W, h, 0.9, check_oracle_full=False)
 
 
 def test_decode_partially_committed_entry_state():
@@ -287,3 +312,37 @@ def test_host_validation_rejects_bad_arguments():
     assert bd.bd_block_attention_workspace(1, 32, 16, 8, 96, 100) == 0   # head_dim 96
     assert bd.bd_confidence_commit_workspace(bd.BD_BF16, 1, 33, 2048, 10) == 0
     assert (tok == -1).all()                          # nothing ran
+
+
+# --- full-size batched serving workload, sampled against the oracle -------------
+def test_serving_b64_full_size_sampled():
+    """64 sequences with ragged prefixes (2048..12288) in a permuted paged cache and
+    the 151936 x 2048 LM head: attention checked on sampled sequences, the first
+    denoise step's confidence checked on two whole sequences, and the commit rule
+    checked on every sequence."""
+    w = wl.WORKLOADS["serving_b64"]
+    s = make_cache(w, 0)
+    q, kb, vb = wl.block_qkv(w, 0)
+    got = gpu_attention(s, q, kb, vb)
+    for b in (0, 17, 63):
+        ref = oracle_attention(s, b, q, kb, vb)
+        assert np.abs(got[b] - ref).max() <= 2e-2
+    W = wl.lm_head(w)
+    h, _ = wl.planted_hidden(w, W, 0, steps=1)
+    run = ConfRunner(w, W, w.threshold)
+    tok, p, a, nc, nm = run.step(dev(h[0], w.dtype))
+    # every sequence: exactly one commit (nothing reaches 0.95 under this recipe),
+    # at a position whose GPU p_max is the largest, with the GPU argmax
+    assert (nc == 1).all() and (nm == 31).all()
+    for b in range(w.batch):
+        i = int(np.nonzero(tok[b] != -1)[0][0])
+        assert p[b, i] == p[b].max() and tok[b, i] == a[b, i]
+    # two whole sequences against fp64 logits
+    for b in (5, 40):
+        c = oracle.confidence(h[0, b].astype(np.float64), W.astype(np.float64))
+        assert np.abs(p[b] - c["p_max"]).max() <= 2e-2
+        exempt = c["top2_prob_margin"] < 1e-3
+        assert (a[b][~exempt] == c["argmax"][~exempt]).all()
+        best = c["p_max"].max()
+        i = int(np.nonzero(tok[b] != -1)[0][0])
+        assert best - c["p_max"][i] < 1e-3        # same position up to the near-tie exemption
