@@ -46,6 +46,11 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--check-every", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", default=None,
+                    help="comma-separated thresholds: run the multi-block threshold sweep")
+    ap.add_argument("--blocks", type=int, default=0, help="blocks per sweep decode")
+    ap.add_argument("--a-max", type=float, default=None,
+                    help="planted amplitude bound (the workload's own by default)")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every kernel from the host instead of replaying CUDA graphs")
     ap.add_argument("--workload", default=WORKLOAD,
@@ -448,10 +453,75 @@ def _e2e(a, eng, w, h, q, kb, vb, hd, qd, kbd, vbd, ctx0, stream, committed_per_
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
+def run_sweep(a):
+    """Threshold sweep: full multi-block decodes (each finished block's K/V is
+    appended before the next block) at every T, one JSON line per T with the
+    denoise steps per block and committed tokens/s.  Not the headline line."""
+    import torch
+    from block_diffusion_decoding_denoise_gb300 import bd, build
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    from block_diffusion_decoding_denoise_gb300.engine import DenoiseEngine, PagedCache
+    if not os.path.exists(bd.LIB_PATH):
+        build.build()
+    bd.load()
+    w = wl.WORKLOADS[a.workload]
+    nblk = a.blocks or w.num_blocks
+    a_max = w.a_max if a.a_max is None else a.a_max
+    W = wl.lm_head(w)
+    Wd = torch.from_numpy(W).to("cuda", torch.bfloat16)
+    plen = wl.prefix_lengths(w)
+    cap = plen + nblk * w.block_len
+    table, npg = wl.page_tables(w, cap)
+    blocks = []
+    for blk in range(nblk):
+        q, kb, vb = wl.block_qkv(w, blk)
+        h, _ = wl.planted_hidden(w, W, blk, a_max=a_max)
+        blocks.append(tuple(torch.from_numpy(x).to("cuda", torch.bfloat16) for x in (h, q, kb, vb)))
+    kvs = [wl.prefix_kv(w, b, int(plen[b])) for b in range(w.batch)]
+    for T in [float(x) for x in a.sweep.split(",")]:
+        cache = PagedCache(npg, w.num_kv_heads, w.head_dim, torch.bfloat16, table)
+        for b in range(w.batch):
+            cache.load_prefix(b, torch.from_numpy(kvs[b][0]), torch.from_numpy(kvs[b][1]))
+        eng = DenoiseEngine(Wd, cache, plen, batch=w.batch, block_len=w.block_len,
+                            num_q_heads=w.num_q_heads, threshold=T, max_ctx=int(cap.max()))
+        ctx0 = eng.ctx_len.clone()
+        for _ in range(2):                      # warm-up decodes (capture the graphs)
+            eng.ctx_len.copy_(ctx0)
+            for (h, q, kb, vb) in blocks:
+                eng.decode_block(h, q, kb, vb, check_every=a.check_every,
+                                 graphs=not a.no_graphs)
+        torch.cuda.synchronize()
+        eng.ctx_len.copy_(ctx0)
+        steps = []
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for (h, q, kb, vb) in blocks:
+            eng.decode_block(h, q, kb, vb, check_every=a.check_every, graphs=not a.no_graphs)
+            steps.append(eng.steps_per_sequence())
+        e1.record()
+        torch.cuda.synchronize()
+        eng.check_status()
+        ms = e0.elapsed_time(e1)
+        tokens = w.batch * w.block_len * nblk
+        st = np.array(steps)
+        print(json.dumps({
+            "sweep": True, "metric": METRIC, "unit": UNIT, "threshold": T,
+            "value": tokens / (ms / 1e3), "ms": ms, "blocks": nblk,
+            "denoise_steps_per_block_mean": float(st.mean()),
+            "denoise_steps_per_block_min": int(st.min()),
+            "denoise_steps_per_block_max": int(st.max()),
+            "config": _config(w, {"a_max": a_max, "blocks": nblk,
+                                  "prefix_after": int(eng.ctx_len.max().item())})}),
+              flush=True)
+
+
 def main():
     a = _args()
     if a.impl == "reference":
         run_reference(a)
+    elif a.sweep:
+        run_sweep(a)
     else:
         run_cuda(a)
 

@@ -76,10 +76,7 @@ __global__ void __launch_bounds__(1024) conf_prep_kernel(const int32_t *tokens, 
     }
     __syncthreads();
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    *ws.count = carry;
-    *ws.ticket = 0;
-  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ws.count = carry;
 }
 
 // ---------------------------------------------------------------------------
@@ -250,7 +247,6 @@ static size_t carve(const ConfParams &p, char *base, ConfWorkspace *ws) {
   char *rows = take(n * 4), *row_of = take(n * 4), *count = take(4);
   char *part = take((size_t)np * n * sizeof(MaxSumArg));
   char *hc = p.dtype == BD_BF16 ? take(n * (size_t)p.hidden * 2) : nullptr;
-  char *ticket = take(4);
   if (ws) {
     ws->rows = reinterpret_cast<int32_t *>(rows);
     ws->row_of = reinterpret_cast<int32_t *>(row_of);
@@ -258,7 +254,6 @@ static size_t carve(const ConfParams &p, char *base, ConfWorkspace *ws) {
     ws->partial = reinterpret_cast<MaxSumArg *>(part);
     ws->num_partials = np;
     ws->hc = hc;
-    ws->ticket = reinterpret_cast<int32_t *>(ticket);
   }
   return off;
 }
@@ -331,9 +326,8 @@ BD_API bd_status bd_confidence_commit(bd_dtype dtype, int32_t batch, int32_t blo
                              p.ws, src, hidden * 2);
   count_launches(1);
   if (e != cudaSuccess) return BD_ERR_CUDA;
-  const bool fuse = tc && nrows <= kFuseMaxRows;
-  const bd_status s = tc ? lmhead_tc(p, st, fuse) : lmhead_simt(p, st);
-  if (s != BD_OK || fuse) return s;
+  const bd_status s = tc ? lmhead_tc(p, st) : lmhead_simt(p, st);
+  if (s != BD_OK) return s;
   e = launch_pdl(conf_commit_kernel, dim3(batch), dim3(32 * block_len), 0, st, p);
   count_launches(1);
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;

@@ -15,13 +15,11 @@ namespace bd {
 //   count    [1]   int32   number of masked rows
 //   partial  [P][B*L] MaxSumArg   one online-softmax state per producer and row
 //   hc       [B*L][H] bf16        masked rows of h, compacted (bf16 only)
-//   ticket   [1]   int32   CTAs of the LM head that finished (zeroed by the prep kernel)
 struct ConfWorkspace {
   int32_t *rows, *row_of, *count;
   MaxSumArg *partial;
   int num_partials;
   char *hc;
-  int32_t *ticket;
 };
 
 struct ConfParams {
@@ -35,10 +33,6 @@ struct ConfParams {
   int32_t *dev_status;
   ConfWorkspace ws;
 };
-
-// Batches up to this many positions (B * L') have the commit fused into the
-// tensor-core LM head (its last CTA merges the partials and decides).
-constexpr int kFuseMaxRows = 64;
 
 // p_max and argmax of a row from its merged online-softmax state.
 __device__ __forceinline__ void finalize_row(const ConfParams &p, const MaxSumArg &st, float &pm,
@@ -96,6 +90,6 @@ int conf_num_partials(bd_dtype dtype, int batch, int block_len, int hidden, int 
 bd_status lmhead_simt(const ConfParams &p, cudaStream_t st);
 bool lmhead_tc_supported(const ConfParams &p);
 int lmhead_tc_num_partials(int vocab);
-bd_status lmhead_tc(const ConfParams &p, cudaStream_t st, bool fuse_commit);
+bd_status lmhead_tc(const ConfParams &p, cudaStream_t st);
 
 }  // namespace bd

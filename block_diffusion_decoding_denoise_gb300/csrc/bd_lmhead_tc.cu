@@ -28,7 +28,8 @@
 //              butterfly over the 32 lanes reduces the 16 columns to one
 //              (max, sum-exp, argmax) each; a 4-warp merge through smem; a
 //              running state per row kept in registers
-// Each CTA writes one partial state per row; conf_commit_kernel merges them.
+// Each CTA writes one partial state per row; conf_commit_kernel (launched
+// right behind, with programmatic dependent launch) merges them and commits.
 // Every mbarrier wait is bounded (1 s); on expiry the kernel records
 // BD_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
 #include <math.h>
@@ -62,7 +63,6 @@ struct Ctrl {
   uint64_t mma_done;
   uint32_t tmem_base;
   volatile int32_t abort;
-  int32_t last_cta;
   MaxSumArg red[2][4][kMaxN];
 };
 
@@ -71,7 +71,6 @@ struct LmTcArgs {
   int stages;
   int stage_bytes;
   int num_tiles;
-  int fuse_commit;   // the last CTA merges the partials and commits
 };
 
 __device__ __forceinline__ bool barrier_or(uint32_t id, uint32_t nthreads, bool pred) {
@@ -121,52 +120,6 @@ __device__ __forceinline__ void bfly_round(float (&m)[16], float (&s)[16], int (
     m[k] = km;
     s[k] = ks;
     id[k] = ki;
-  }
-}
-
-// Merge the G per-CTA partial states of each masked row (several threads per
-// row, then a merge through smem) and take every sequence's commit decision
-// (one warp per sequence).  Runs in one CTA after all others finished.
-__device__ __noinline__ void fused_commit(const ConfParams &p, int count, uint8_t *smem, int G) {
-  float *pm_s = reinterpret_cast<float *>(smem);
-  int *am_s = reinterpret_cast<int *>(pm_s + kFuseMaxRows);
-  MaxSumArg *red = reinterpret_cast<MaxSumArg *>(am_s + kFuseMaxRows);
-  const int t = threadIdx.x, T = blockDim.x;
-  const size_t stride = (size_t)p.batch * p.block_len;
-  for (int r0 = 0; r0 < count; r0 += T) {
-    const int nr = min(T, count - r0);
-    const int nsub = T / nr;
-    MaxSumArg st{-INFINITY, 0.f, 0x7fffffff};
-    if (t < nr * nsub) {
-      const int row = r0 + t % nr;
-#pragma unroll 4
-      for (int c = t / nr; c < G; c += nsub) {
-        const MaxSumArg *src = p.ws.partial + (size_t)c * stride + row;
-        MaxSumArg v;
-        v.m = __ldcg(&src->m);
-        v.s = __ldcg(&src->s);
-        v.idx = __ldcg(&src->idx);
-        st = merge(st, v);
-      }
-    }
-    red[t] = st;
-    __syncthreads();
-    if (t < nr) {
-      for (int j = 1; j < nsub; ++j) st = merge(st, red[t + j * nr]);
-      float pm;
-      int am;
-      finalize_row(p, st, pm, am);
-      pm_s[r0 + t] = pm;
-      am_s[r0 + t] = am;
-    }
-    __syncthreads();
-  }
-  const int warp = t >> 5, lane = t & 31, nwarps = T >> 5;
-  for (int b = warp; b < p.batch; b += nwarps) {
-    const int pos = b * p.block_len + lane;
-    const bool masked = lane < p.block_len && p.tokens[pos] == BD_MASK;
-    const int k = masked ? p.ws.row_of[pos] : 0;
-    commit_sequence_warp(p, b, masked, masked ? pm_s[k] : -1.f, masked ? am_s[k] : -1);
   }
 }
 
@@ -389,17 +342,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (a.fuse_commit) {
-    // last CTA to finish: merge every CTA's partial state per row and commit
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) ctrl->last_cta = atomicAdd(p.ws.ticket, 1) == G - 1;
-    __syncthreads();
-    if (ctrl->last_cta) {
-      __threadfence();
-      fused_commit(p, count, smem, G);
-    }
-  }
 }
 
 // 2-D bf16 tensor map over a row-major [outer][inner] matrix, 128-byte swizzle.
@@ -437,10 +379,9 @@ int lmhead_tc_num_partials(int vocab) {
   return std::max(1, std::min(d.sms, num_tiles(vocab)));
 }
 
-bd_status lmhead_tc(const ConfParams &p, cudaStream_t st, bool fuse_commit) {
+bd_status lmhead_tc(const ConfParams &p, cudaStream_t st) {
   LmTcArgs a;
   a.p = p;
-  a.fuse_commit = fuse_commit ? 1 : 0;
   a.num_tiles = num_tiles(p.vocab);
   size_t smem;
   plan(p, &a.stages, &a.stage_bytes, &smem);

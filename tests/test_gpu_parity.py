@@ -190,8 +190,8 @@ def test_decode_more_rows_than_one_pass():
     lockstep_block(w, W, h, 0.9)
 
 
-def test_decode_unfused_commit_three_passes():
-    # 9 x 32 = 288 positions: above the fused-commit limit, two LM-head passes
+def test_decode_two_lmhead_passes():
+    # 9 x 32 = 288 masked positions: two LM-head passes of up to 256 rows
     w = SMALL_BF16.with_(batch=9)
     W = wl.lm_head(w)
     h, _ = wl.planted_hidden(w, W, 0, a_max=30.0)
