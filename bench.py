@@ -33,6 +33,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "committed tokens/sec per denoise loop"
+# DRAM bytes (read + write) of one lmhead_tc_kernel launch at this workload (24
+# masked rows), from an ncu capture of the current kernel:
+# dram__bytes_read.sum 622.60 MB + dram__bytes_write.sum 3.16 MB.
+LMHEAD_TRAFFIC_BYTES = 622_600_960 + 3_159_296
 UNIT = "tokens/s"
 WORKLOAD = "sdar_b1"
 
@@ -375,7 +379,8 @@ def run_cuda(a):
     active = [(b, t) for b, t, r in zip(alg, conf_ms, rows_per_call) if r > 0]
     achieved = sum(b for b, _ in active) / (sum(t for _, t in active) / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak,
+                "traffic": LMHEAD_TRAFFIC_BYTES if a.workload == WORKLOAD else None,
                 "kernel": "bd_confidence_commit (masked-row compaction + LM head with online "
                           "max/sum-exp/argmax + commit)",
                 "peak_source": f"{peak_kind} hbm_gbs"}

@@ -1,5 +1,7 @@
 // Host entry points of libbd: block attention dispatch, KV append, status.
 #include <math.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <algorithm>
 #include <atomic>
@@ -178,8 +180,22 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
     p.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + off_ml);
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bd_status s = attention_tc(p, st);
-  if (s != BD_ERR_UNSUPPORTED) return s;
+  // Kernel choice: the persistent mma.sync kernel for bf16 (measured faster
+  // than the tcgen05 kernel at every batch size so far), SIMT for fp32.
+  // BD_ATTENTION (tc5 | mma | simt) forces one kernel, for testing and
+  // measurement.
+  const char *env = getenv("BD_ATTENTION");
+  const bool force5 = env && !strcmp(env, "tc5");
+  const bool force_simt = env && !strcmp(env, "simt");
+  if (force5 && attention_tc5_supported(p)) {
+    const bd_status s = attention_tc5(p, st);
+    if (s != BD_OK || p.num_splits == 1) return s;
+    return attention_combine(p, st);
+  }
+  if (!force_simt) {
+    const bd_status s = attention_tc(p, st);
+    if (s != BD_ERR_UNSUPPORTED) return s;
+  }
   return attention_simt(p, st);
 }
 

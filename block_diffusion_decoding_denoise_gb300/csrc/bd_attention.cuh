@@ -26,5 +26,7 @@ struct AttnParams {
 bd_status attention_simt(const AttnParams &p, cudaStream_t st);
 bd_status attention_tc(const AttnParams &p, cudaStream_t st);
 bd_status attention_combine(const AttnParams &p, cudaStream_t st);
+bool attention_tc5_supported(const AttnParams &p);
+bd_status attention_tc5(const AttnParams &p, cudaStream_t st);
 
 }  // namespace bd

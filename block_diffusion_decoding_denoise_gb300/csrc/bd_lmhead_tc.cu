@@ -63,7 +63,6 @@ struct Ctrl {
   uint64_t mma_done;
   uint32_t tmem_base;
   volatile int32_t abort;
-  MaxSumArg red[2][4][kMaxN];
 };
 
 struct LmTcArgs {
@@ -71,6 +70,9 @@ struct LmTcArgs {
   int stages;
   int stage_bytes;
   int num_tiles;
+  int nmax;       // masked rows per pass this launch can hold (multiple of 16)
+  int red_off;    // smem offsets of the merge buffer and Ctrl
+  int ctrl_off;
 };
 
 __device__ __forceinline__ bool barrier_or(uint32_t id, uint32_t nthreads, bool pred) {
@@ -129,7 +131,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + (size_t)a.stages * a.stage_bytes);
+  Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + a.ctrl_off);
+  MaxSumArg *red = reinterpret_cast<MaxSumArg *>(smem + a.red_off);   // [2][4][nmax]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ConfParams &p = a.p;
 
@@ -309,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // lanes 2k and 2k+1 now hold column c0 + k of the 32 lanes' reduction
             if ((lane & 1) == 0)
-              ctrl->red[tg & 1][ew][c0 + (lane >> 1)] = MaxSumArg{m[0], sx[0], id[0]};
+              red[((tg & 1) * 4 + ew) * a.nmax + c0 + (lane >> 1)] = MaxSumArg{m[0], sx[0], id[0]};
           }
           tc_fence_before();
           __syncwarp();
@@ -324,11 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (tid_e < npad) {
 #pragma unroll
-          for (int w = 0; w < 4; ++w) run = merge(run, ctrl->red[tg & 1][w][tid_e]);
+          for (int w = 0; w < 4; ++w) run = merge(run, red[((tg & 1) * 4 + w) * a.nmax + tid_e]);
         }
         if (tid_e + 128 < npad) {
 #pragma unroll
-          for (int w = 0; w < 4; ++w) run2 = merge(run2, ctrl->red[tg & 1][w][tid_e + 128]);
+          for (int w = 0; w < 4; ++w)
+            run2 = merge(run2, red[((tg & 1) * 4 + w) * a.nmax + tid_e + 128]);
         }
       }
       if (!stop && tid_e < n) p.ws.partial[(size_t)cta * stride + r0 + tid_e] = run;
@@ -355,13 +359,17 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, 
 
 int num_tiles(int vocab) { return (vocab + kTileV - 1) / kTileV; }
 
-void plan(const ConfParams &p, int *stages, int *stage_bytes, size_t *smem) {
+void plan(const ConfParams &p, LmTcArgs &a, size_t *smem) {
   const int rows = p.batch * p.block_len;
   const int nmax = std::min(kMaxN, (rows + 15) & ~15);
-  *stage_bytes = (kABytes + nmax * 128 + 1023) & ~1023;
-  const int avail = kSmemLimit - (int)sizeof(Ctrl) - 1024;
-  *stages = std::max(2, std::min(kMaxStages, avail / *stage_bytes));
-  *smem = (size_t)(*stages) * (*stage_bytes) + sizeof(Ctrl) + 1024;
+  a.nmax = nmax;
+  a.stage_bytes = (kABytes + nmax * 128 + 1023) & ~1023;
+  const int red = (2 * 4 * nmax * (int)sizeof(MaxSumArg) + 1023) & ~1023;
+  const int fixed = red + (int)sizeof(Ctrl) + 1024;
+  a.stages = std::max(2, std::min(kMaxStages, (kSmemLimit - fixed) / a.stage_bytes));
+  a.red_off = a.stages * a.stage_bytes;
+  a.ctrl_off = a.red_off + red;
+  *smem = (size_t)a.ctrl_off + sizeof(Ctrl) + 1024;
 }
 
 }  // namespace
@@ -384,7 +392,7 @@ bd_status lmhead_tc(const ConfParams &p, cudaStream_t st) {
   a.p = p;
   a.num_tiles = num_tiles(p.vocab);
   size_t smem;
-  plan(p, &a.stages, &a.stage_bytes, &smem);
+  plan(p, a, &smem);
   if (smem > (size_t)kSmemLimit) return BD_ERR_UNSUPPORTED;
   CUtensorMap mw, mh;
   if (!make_map(&mw, p.w, p.hidden, p.vocab, kKChunk, kTileV)) return BD_ERR_CUDA;
