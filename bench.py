@@ -53,6 +53,9 @@ def _args():
     ap.add_argument("--sweep", default=None,
                     help="comma-separated thresholds: run the multi-block threshold sweep")
     ap.add_argument("--blocks", type=int, default=0, help="blocks per sweep decode")
+    ap.add_argument("--ar-compare", action="store_true",
+                    help="block diffusion vs token-by-token decoding on the same shapes")
+    ap.add_argument("--ar-threshold", type=float, default=0.95)
     ap.add_argument("--a-max", type=float, default=None,
                     help="planted amplitude bound (the workload's own by default)")
     ap.add_argument("--no-graphs", action="store_true",
@@ -521,12 +524,87 @@ def run_sweep(a):
               flush=True)
 
 
+def _decode_tokens_per_s(w, W, Wd, a_max, T, ntok, check_every, graphs):
+    """Decode ntok tokens per sequence in blocks of w.block_len (appending each
+    finished block), twice; returns (tokens/s of the second pass, mean denoise
+    steps per block)."""
+    import torch
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    from block_diffusion_decoding_denoise_gb300.engine import DenoiseEngine, PagedCache
+    nblk = ntok // w.block_len
+    plen = wl.prefix_lengths(w)
+    cap = plen + ntok
+    table, npg = wl.page_tables(w, cap)
+    cache = PagedCache(npg, w.num_kv_heads, w.head_dim, torch.bfloat16, table)
+    for b in range(w.batch):
+        k, v = wl.prefix_kv(w, b, int(plen[b]))
+        cache.load_prefix(b, torch.from_numpy(k), torch.from_numpy(v))
+    blocks = []
+    for blk in range(nblk):
+        q, kb, vb = wl.block_qkv(w, blk)
+        h, _ = wl.planted_hidden(w, W, blk, a_max=a_max)
+        blocks.append(tuple(torch.from_numpy(x).to("cuda", torch.bfloat16) for x in (h, q, kb, vb)))
+    eng = DenoiseEngine(Wd, cache, plen, batch=w.batch, block_len=w.block_len,
+                        num_q_heads=w.num_q_heads, threshold=T, max_ctx=int(cap.max()))
+    ctx0 = eng.ctx_len.clone()
+    ms = steps = 0.0
+    for rep in range(2):
+        eng.ctx_len.copy_(ctx0)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        tot = 0
+        for (h, q, kb, vb) in blocks:
+            eng.decode_block(h, q, kb, vb, check_every=min(check_every, w.block_len),
+                             graphs=graphs)
+            tot += float(eng.steps_per_sequence().mean())
+        e1.record()
+        torch.cuda.synchronize()
+        eng.check_status()
+        ms, steps = e0.elapsed_time(e1), tot / nblk
+    return w.batch * ntok / (ms / 1e3), steps
+
+
+def run_ar_compare(a):
+    """Block diffusion (blocks of 32) against token-by-token decoding (blocks of
+    1, i.e. causal AR decoding on the same kernels) on the same shapes: the
+    synthetic counterpart of the pages' decoding-speedup comparison."""
+    import torch
+    from block_diffusion_decoding_denoise_gb300 import bd, build
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    if not os.path.exists(bd.LIB_PATH):
+        build.build()
+    bd.load()
+    w = wl.WORKLOADS[a.workload]
+    a_max = w.a_max if a.a_max is None else a.a_max
+    T = float(a.ar_threshold)
+    W = wl.lm_head(w)
+    Wd = torch.from_numpy(W).to("cuda", torch.bfloat16)
+    ntok = 32 * max(1, a.blocks or 1)
+    res = {}
+    for L in (w.block_len, 1):
+        wb = w.with_(block_len=L)
+        res[L] = _decode_tokens_per_s(wb, W, Wd, a_max, T, ntok, a.check_every,
+                                      not a.no_graphs)
+    print(json.dumps({
+        "ar_compare": True, "metric": METRIC, "unit": UNIT, "threshold": T, "a_max": a_max,
+        "tokens_per_sequence": ntok,
+        "block_diffusion": {"block_len": w.block_len, "value": res[w.block_len][0],
+                            "denoise_steps_per_block": res[w.block_len][1]},
+        "autoregressive": {"block_len": 1, "value": res[1][0]},
+        "speedup": res[w.block_len][0] / res[1][0],
+        "config": _config(w, {"a_max": a_max})}))
+
+
 def main():
     a = _args()
     if a.impl == "reference":
         run_reference(a)
     elif a.sweep:
         run_sweep(a)
+    elif a.ar_compare:
+        run_ar_compare(a)
     else:
         run_cuda(a)
 

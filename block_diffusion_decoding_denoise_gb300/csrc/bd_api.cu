@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 #include "bd_attention.cuh"
 #include "bd_common.cuh"
@@ -13,6 +14,31 @@ namespace bd {
 
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+__global__ void append_kv_kernel(bd_paged_kv kv, int block_len, size_t elem_bytes,
+                                 const char *k_blk, const char *v_blk, int32_t *ctx_len,
+                                 const int32_t *n_masked, int32_t *dev_status);
+
+bool preload_all() {
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return true;
+  const bool ok = preload_kernel(append_kv_kernel, false) && preload_attention_simt() &&
+                  preload_attention_tc() && preload_attention_tc5() && preload_confidence() &&
+                  preload_lmhead_tc();
+  if (!ok) {
+    cudaGetLastError();
+    return false;
+  }
+  done[dev] = true;
+  return true;
+}
 
 static int num_sms() {
   static int cached = 0;
@@ -133,6 +159,7 @@ BD_API size_t bd_block_attention_workspace(int32_t batch, int32_t block_len, int
                                            int32_t num_kv_heads, int32_t head_dim,
                                            int32_t max_ctx) {
   if (!attn_shape_ok(batch, block_len, num_q_heads, num_kv_heads, head_dim, max_ctx)) return 0;
+  preload_all();
   int ns, sk;
   size_t off_ml;
   return attn_ws_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim, max_ctx, &ns, &sk,
@@ -149,6 +176,7 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
   if (!attn_shape_ok(batch, block_len, num_q_heads, kv->num_kv_heads, kv->head_dim, max_ctx))
     return BD_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || isinf(softmax_scale)) return BD_ERR_INVALID_ARG;
+  if (!preload_all()) return BD_ERR_CUDA;
   AttnParams p{};
   p.dtype = kv->dtype;
   p.batch = batch;
@@ -206,6 +234,7 @@ BD_API bd_status bd_append_block_kv(const bd_paged_kv *kv, int32_t batch, int32_
   if (batch < 1 || block_len < 1 || block_len > 1024) return BD_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(k_blk) | reinterpret_cast<uintptr_t>(v_blk)) & 15)
     return BD_ERR_INVALID_ARG;
+  if (!preload_all()) return BD_ERR_CUDA;
   const size_t elem = kv->dtype == BD_BF16 ? 2 : 4;
   const cudaError_t e = launch_pdl(append_kv_kernel, dim3(batch), dim3(256), 0,
                                    static_cast<cudaStream_t>(stream), *kv, block_len, elem,

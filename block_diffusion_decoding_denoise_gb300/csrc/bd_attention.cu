@@ -205,9 +205,6 @@ static bd_status launch_simt(const AttnParams &p, cudaStream_t st) {
   const int warps = (R + kRowsPerWarp - 1) / kRowsPerWarp;
   const size_t smem = sizeof(float) * ((size_t)R * D + kTileKeys * (D + 1) + kTileKeys * D);
   auto kern = attn_splitkv_simt_kernel<T, D>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return BD_ERR_CUDA;
   dim3 grid(p.num_splits, p.hkv, p.batch);
   const cudaError_t e = launch_pdl(kern, grid, dim3(warps * 32), smem, st, p);
   count_launches(1);
@@ -230,6 +227,17 @@ bd_status attention_combine(const AttnParams &p, cudaStream_t st) {
     return p.head_dim == 64 ? launch_combine<float, 64>(p, st) : launch_combine<float, 128>(p, st);
   return p.head_dim == 64 ? launch_combine<__nv_bfloat16, 64>(p, st)
                           : launch_combine<__nv_bfloat16, 128>(p, st);
+}
+
+bool preload_attention_simt() {
+  return preload_kernel(attn_splitkv_simt_kernel<float, 64>, true) &&
+         preload_kernel(attn_splitkv_simt_kernel<float, 128>, true) &&
+         preload_kernel(attn_splitkv_simt_kernel<__nv_bfloat16, 64>, true) &&
+         preload_kernel(attn_splitkv_simt_kernel<__nv_bfloat16, 128>, true) &&
+         preload_kernel(attn_combine_kernel<float, 64>, false) &&
+         preload_kernel(attn_combine_kernel<float, 128>, false) &&
+         preload_kernel(attn_combine_kernel<__nv_bfloat16, 64>, false) &&
+         preload_kernel(attn_combine_kernel<__nv_bfloat16, 128>, false);
 }
 
 bd_status attention_simt(const AttnParams &p, cudaStream_t st) {

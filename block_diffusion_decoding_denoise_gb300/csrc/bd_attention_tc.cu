@@ -502,9 +502,6 @@ bd_status launch(const AttnParams &p, cudaStream_t st) {
                                       (200 * 1024 - ctrl - kXchgBytes) / (2 * TILE));
   const size_t smem = (size_t)S * 2 * TILE + kXchgBytes + ctrl + 1024;
   auto kern = attn_tc_kernel<D, RG, KH>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return BD_ERR_CUDA;
   const int nitems = p.batch * p.hkv * p.num_splits;
   const int grid = std::max(1, std::min(nitems, std::max(dev_info().sms, 1)));
   const cudaError_t e =
@@ -514,6 +511,13 @@ bd_status launch(const AttnParams &p, cudaStream_t st) {
 }
 
 }  // namespace
+
+bool preload_attention_tc() {
+  return preload_kernel(attn_tc_kernel<64, 4, 2>, true) &&
+         preload_kernel(attn_tc_kernel<64, 8, 1>, true) &&
+         preload_kernel(attn_tc_kernel<128, 4, 2>, true) &&
+         preload_kernel(attn_tc_kernel<128, 8, 1>, true);
+}
 
 bd_status attention_tc(const AttnParams &p, cudaStream_t st) {
   if (p.dtype != BD_BF16 || (p.head_dim != 64 && p.head_dim != 128)) return BD_ERR_UNSUPPORTED;

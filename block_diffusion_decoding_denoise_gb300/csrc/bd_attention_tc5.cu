@@ -557,6 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+bool preload_attention_tc5() { return preload_kernel(attn_tc5_kernel, true); }
+
 bool attention_tc5_supported(const AttnParams &p) {
   if (p.dtype != BD_BF16 || p.head_dim != D || p.page_size != kPage) return false;
   const int R = p.block_len * (p.hq / p.hkv);
@@ -592,9 +594,6 @@ bd_status attention_tc5(const AttnParams &p, cudaStream_t st) {
       !tma_encode_bf16(&mq, 4, p.q, qdims, qstr, qbox))
     return BD_ERR_CUDA;
   const size_t smem = sizeof(Smem) + 1024;
-  if (cudaFuncSetAttribute(attn_tc5_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
-    return BD_ERR_CUDA;
   const int nitems = p.batch * p.hkv * p.num_splits;
   const int grid = std::max(1, std::min(nitems, std::max(dev_info().sms, 1)));
   const cudaError_t e = launch_pdl(attn_tc5_kernel, dim3(grid), dim3(kThreads), smem, st, mkp,

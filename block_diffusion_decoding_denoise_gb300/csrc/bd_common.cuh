@@ -100,6 +100,32 @@ bool tma_available();
 bool tma_encode_bf16(CUtensorMap *m, int rank, const void *base, const uint64_t *dims,
                      const uint64_t *strides_bytes, const uint32_t *box);
 
+// Load a kernel's module and allow it the largest dynamic shared memory the
+// device offers.  Done once per device before first use (kernel modules load
+// lazily, and a first load inside a CUDA-graph capture is not allowed).
+template <typename... KArgs>
+inline bool preload_kernel(void (*kernel)(KArgs...), bool dyn_smem) {
+  if (dyn_smem) {
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+      return false;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) ==
+           cudaSuccess;
+  }
+  cudaFuncAttributes attr;
+  return cudaFuncGetAttributes(&attr, kernel) == cudaSuccess;
+}
+
+// Preload every kernel of the library on the current device (idempotent).
+bool preload_all();
+bool preload_attention_simt();
+bool preload_attention_tc();
+bool preload_attention_tc5();
+bool preload_confidence();
+bool preload_lmhead_tc();
+
 inline bd_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }

@@ -235,6 +235,12 @@ int conf_num_partials(bd_dtype dtype, int batch, int block_len, int hidden, int 
   return (vocab + kSimtChunk - 1) / kSimtChunk;
 }
 
+bool preload_confidence() {
+  return preload_kernel(conf_prep_kernel, false) && preload_kernel(conf_commit_kernel, false) &&
+         preload_kernel(lmhead_simt_kernel<float>, false) &&
+         preload_kernel(lmhead_simt_kernel<__nv_bfloat16>, false);
+}
+
 static size_t carve(const ConfParams &p, char *base, ConfWorkspace *ws) {
   const size_t n = (size_t)p.batch * p.block_len;
   const int np = conf_num_partials(p.dtype, p.batch, p.block_len, p.hidden, p.vocab);
@@ -275,6 +281,7 @@ using namespace bd;
 BD_API size_t bd_confidence_commit_workspace(bd_dtype dtype, int32_t batch, int32_t block_len,
                                              int32_t hidden, int32_t vocab) {
   if (!conf_args_ok(dtype, batch, block_len, hidden, vocab)) return 0;
+  preload_all();
   ConfParams p{};
   p.dtype = dtype;
   p.batch = batch;
@@ -293,6 +300,7 @@ BD_API bd_status bd_confidence_commit(bd_dtype dtype, int32_t batch, int32_t blo
   if (!conf_args_ok(dtype, batch, block_len, hidden, vocab)) return BD_ERR_INVALID_ARG;
   if (!hidden_states || !lm_head || !tokens || !p_max || !argmax || !n_committed || !n_masked)
     return BD_ERR_INVALID_ARG;
+  if (!preload_all()) return BD_ERR_CUDA;
   if (isnan(threshold)) return BD_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(hidden_states) | reinterpret_cast<uintptr_t>(lm_head)) & 15)
     return BD_ERR_INVALID_ARG;

@@ -374,6 +374,8 @@ void plan(const ConfParams &p, LmTcArgs &a, size_t *smem) {
 
 }  // namespace
 
+bool preload_lmhead_tc() { return preload_kernel(lmhead_tc_kernel, true); }
+
 bool lmhead_tc_supported(const ConfParams &p) {
   if (p.dtype != BD_BF16 || p.hidden % kKChunk != 0 || p.hidden < kKChunk) return false;
   if ((int64_t)p.batch * p.block_len > (1 << 20)) return false;
@@ -397,9 +399,6 @@ bd_status lmhead_tc(const ConfParams &p, cudaStream_t st) {
   CUtensorMap mw, mh;
   if (!make_map(&mw, p.w, p.hidden, p.vocab, kKChunk, kTileV)) return BD_ERR_CUDA;
   if (!make_map(&mh, p.ws.hc, p.hidden, (uint64_t)p.batch * p.block_len, kKChunk, kBoxRows))
-    return BD_ERR_CUDA;
-  if (cudaFuncSetAttribute(lmhead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
     return BD_ERR_CUDA;
   const int grid = p.ws.num_partials;
   if (grid < 1 || grid > a.num_tiles) return BD_ERR_INVALID_ARG;
