@@ -229,6 +229,119 @@ def decode_block(h_steps, W, threshold, tokens0=None):
 
 
 # ---------------------------------------------------------------------------
+# (3b) Sampling reading of the inference settings           [RS] step 6
+# ---------------------------------------------------------------------------
+# The summary's settings "top-k=0, temperature=1.0, top-p=1.0" are read by
+# default as greedy decoding (R4).  Read as sampling instead, they mean: draw
+# the token from softmax(l / temperature) with no top-k and no nucleus
+# truncation.  The draw uses the Gumbel-max identity: argmax_v (l_v / t + G_v)
+# with G_v = -ln(-ln U_v) and U_v uniform on (0, 1) is distributed as
+# softmax(l / t).  The confidence of the drawn token is its probability.
+# U comes from a counter-based generator so that the GPU and this oracle draw
+# the same numbers: Philox-4x64 with 10 rounds (Salmon, Moraes, Dror and Shaw,
+# "Parallel random numbers: as easy as 1, 2, 3", SC'11) under the key
+# (seed, 0), at counter (v // 4, position, offset, 0); word v % 4 of the output
+# gives U = ((word >> 40) + 1/2) / 2^24, exactly representable in fp32.
+# `offset` is the caller's step counter, so every denoise step draws afresh.
+
+_M64 = (1 << 64) - 1
+PHILOX_M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)   # round multipliers
+PHILOX_W = (0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B)   # Weyl key increments
+
+
+def _mulhilo64(a, m):
+    """High and low 64-bit halves of the 128-bit product a * m (a uint64 array)."""
+    a = np.asarray(a, dtype=np.uint64)
+    lo32 = np.uint64(0xFFFFFFFF)
+    s32 = np.uint64(32)
+    a0, a1 = a & lo32, a >> s32
+    m0, m1 = np.uint64(m & 0xFFFFFFFF), np.uint64(m >> 32)
+    p00, p01, p10, p11 = a0 * m0, a0 * m1, a1 * m0, a1 * m1
+    mid = (p00 >> s32) + (p01 & lo32) + (p10 & lo32)
+    hi = p11 + (p01 >> s32) + (p10 >> s32) + (mid >> s32)
+    lo = (mid << s32) | (p00 & lo32)
+    return hi, lo
+
+
+def philox4x64_10(counter, key):
+    """Philox-4x64-10 of a counter (4 uint64 arrays) under a key (2 ints).
+
+    One round: (h0, l0) = M0 * c0, (h1, l1) = M1 * c2 (128-bit products);
+    c <- (h1 ^ c1 ^ k0, l1, h0 ^ c3 ^ k1, l0); the key grows by (W0, W1)
+    before every round but the first."""
+    c0, c1, c2, c3 = (np.asarray(c, dtype=np.uint64) for c in counter)
+    k0, k1 = int(key[0]) & _M64, int(key[1]) & _M64
+    for r in range(10):
+        if r > 0:
+            k0 = (k0 + PHILOX_W[0]) & _M64
+            k1 = (k1 + PHILOX_W[1]) & _M64
+        h0, l0 = _mulhilo64(c0, PHILOX_M[0])
+        h1, l1 = _mulhilo64(c2, PHILOX_M[1])
+        c0, c1, c2, c3 = h1 ^ c1 ^ np.uint64(k0), l1, h0 ^ c3 ^ np.uint64(k1), l0
+    return c0, c1, c2, c3
+
+
+def uniform01(v, pos, seed, offset=0):
+    """U[v, pos] in (0, 1) for vocabulary entry v at position id pos."""
+    v, pos = np.broadcast_arrays(np.asarray(v, dtype=np.int64), np.asarray(pos, dtype=np.int64))
+    zero = np.zeros(v.shape, dtype=np.uint64)
+    words = philox4x64_10((v >> 2, pos, zero + np.uint64(int(offset) & _M64), zero), (seed, 0))
+    w = np.choose(v & 3, words)
+    return ((w >> np.uint64(40)).astype(np.float64) + 0.5) / float(1 << 24)
+
+
+def sample_confidence(h, W, pos, seed, temperature, offset=0, row_chunk: int = 16):
+    """Gumbel-max draw from softmax(h W^T / temperature) for each row of h.
+
+    pos[m] is the position id of row m (b * L' + i).  Returns dict:
+      token   = argmax_v (z_v + G_v), z = l / temperature (lowest v on ties)
+      p_sel   = softmax(z)[token]
+      key_gap = gap between the two largest z_v + G_v (exemption of near ties)
+    """
+    h = np.asarray(h, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    pos = np.asarray(pos, dtype=np.int64)
+    M, V = h.shape[0], W.shape[0]
+    token = np.empty(M, dtype=np.int64)
+    p_sel = np.empty(M)
+    gap = np.empty(M)
+    vs = np.arange(V)
+    for r0 in range(0, M, row_chunk):
+        z = (h[r0:r0 + row_chunk] @ W.T) / float(temperature)          # [m, V]
+        g = -np.log(-np.log(uniform01(vs[None, :], pos[r0:r0 + row_chunk, None], seed, offset)))
+        key = z + g
+        t = np.argmax(key, axis=1)
+        zmax = z.max(axis=1)
+        lse = zmax + np.log(np.exp(z - zmax[:, None]).sum(axis=1))
+        token[r0:r0 + row_chunk] = t
+        p_sel[r0:r0 + row_chunk] = np.exp(z[np.arange(len(t)), t] - lse)
+        if V > 1:
+            top2 = np.partition(key, -2, axis=1)[:, -2:]
+            gap[r0:r0 + row_chunk] = top2[:, 1] - top2[:, 0]
+        else:
+            gap[r0:r0 + row_chunk] = np.inf
+    return {"token": token, "p_sel": p_sel, "key_gap": gap}
+
+
+def denoise_step_sampled(tokens, h, W, threshold, temperature, seed, offset=0):
+    """denoise_step with the sampling reading: each masked position draws its
+    token (sample_confidence, position id b * L' + i) and its confidence is the
+    drawn token's probability; the commit rule is unchanged."""
+    tokens = np.asarray(tokens)
+    B, L = tokens.shape
+    bi, ii = np.nonzero(tokens == MASK)
+    conf = np.full((B, L), -1.0)
+    tok = np.full((B, L), -1, dtype=np.int64)
+    res = None
+    if len(bi):
+        res = sample_confidence(np.asarray(h)[bi, ii], W, bi * L + ii, seed, temperature, offset)
+        conf[bi, ii] = res["p_sel"]
+        tok[bi, ii] = res["token"]
+    new, chosen = commit(tokens, conf, tok, threshold)
+    return new, conf, tok, chosen, res, (bi, ii)
+
+
+# ---------------------------------------------------------------------------
 # (4) Paged KV cache: reading and appending          [RS] novelty (KV reuse)
 # ---------------------------------------------------------------------------
 def paged_read(pool, page_row, length, page_size):

@@ -280,3 +280,74 @@ def test_paged_read_follows_page_table():
     pool = np.arange(4 * 1 * ps * 1, dtype=float).reshape(4, 1, ps, 1)
     got = oracle.paged_read(pool, [3, 0], 4, ps)[:, 0, 0]
     assert got.tolist() == [6.0, 7.0, 0.0, 1.0]
+
+
+# --- sampling reading (temperature sampling, no truncation) ---------------------
+def test_philox_matches_numpy_bit_generator():
+    # numpy's Philox bit generator is Philox-4x64-10; it advances its counter
+    # by one before producing each block of four words.
+    cases = [([0, 0, 0, 0], [0, 0]), ([5, 7, 11, 13], [123, 456]),
+             ([2**64 - 2, 2**64 - 1, 3, 2**63], [2**64 - 1, 2**63 + 5])]
+    for ctr, key in cases:
+        bg = np.random.Philox(counter=np.array(ctr, dtype=np.uint64),
+                              key=np.array(key, dtype=np.uint64))
+        ref = bg.random_raw(4)
+        got = oracle.philox4x64_10([np.uint64(ctr[0] + 1)] + [np.uint64(c) for c in ctr[1:]], key)
+        assert [int(w) for w in got] == [int(w) for w in ref]
+
+
+def test_philox_uniforms_are_uniform_and_decorrelated():
+    from scipy import stats
+    v = np.arange(200000)
+    u0 = oracle.uniform01(v, 0, 12345)
+    u1 = oracle.uniform01(v, 1, 12345)          # next position id
+    u2 = oracle.uniform01(v, 0, 12345, offset=1)  # next step
+    assert ((u0 > 0) & (u0 < 1)).all()
+    for u in (u0, u1, u2):
+        assert stats.kstest(u, "uniform").pvalue > 1e-3
+    assert abs(np.corrcoef(u0, u1)[0, 1]) < 0.01
+    assert abs(np.corrcoef(u0, u2)[0, 1]) < 0.01
+    assert abs(np.corrcoef(u0[:-1], u0[1:])[0, 1]) < 0.01   # words of one counter
+    assert not np.array_equal(u0, oracle.uniform01(v, 0, 12346))
+    assert np.array_equal(u0, oracle.uniform01(v, 0, 12345))
+    # the 24-bit grid: U * 2^24 - 1/2 is an integer
+    k = u0 * (1 << 24) - 0.5
+    assert np.array_equal(k, np.floor(k))
+
+
+@pytest.mark.parametrize("temperature", [1.0, 0.5, 2.0])
+def test_gumbel_max_draws_follow_softmax(temperature):
+    # one row per draw: same logits, different position ids -> independent draws
+    from scipy import stats
+    l = np.array([0.3, -1.2, 2.0, 0.0, 0.7])
+    W = np.diag(l)                                  # h = ones -> logits = l
+    n = 20000
+    h = np.ones((n, 5))
+    res = oracle.sample_confidence(h, W, np.arange(n), seed=7, temperature=temperature,
+                                   row_chunk=4096)
+    p = np.exp(l / temperature - logsumexp(l / temperature))
+    counts = np.bincount(res["token"], minlength=5)
+    chi = stats.chisquare(counts, n * p)
+    assert chi.pvalue > 1e-4, (counts, n * p)
+    np.testing.assert_allclose(res["p_sel"], p[res["token"]], rtol=1e-12)
+
+
+def test_tiny_temperature_draw_is_the_argmax():
+    rng = np.random.default_rng(21)
+    h = rng.standard_normal((50, 8))
+    W = rng.standard_normal((40, 8))
+    res = oracle.sample_confidence(h, W, np.arange(50), seed=3, temperature=1e-4)
+    assert np.array_equal(res["token"], (h @ W.T).argmax(axis=1))
+
+
+def test_sampled_step_uses_the_commit_rule():
+    rng = np.random.default_rng(22)
+    h = rng.standard_normal((2, 6, 4)) * 3
+    W = rng.standard_normal((9, 4))
+    tokens = np.full((2, 6), -1)
+    tokens[0, 2] = 4
+    new, conf, tok, chosen, res, (bi, ii) = oracle.denoise_step_sampled(tokens, h, W, 0.5, 1.0, 5)
+    assert conf[0, 2] == -1 and tok[0, 2] == -1 and new[0, 2] == 4
+    exp_new, _ = oracle.commit(tokens, conf, tok, 0.5)
+    assert np.array_equal(new, exp_new)
+    assert (new[chosen] == tok[chosen]).all()
