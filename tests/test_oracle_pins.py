@@ -300,18 +300,19 @@ def test_philox_uniforms_are_uniform_and_decorrelated():
     from scipy import stats
     v = np.arange(200000)
     u0 = oracle.uniform01(v, 0, 12345)
-    u1 = oracle.uniform01(v, 1, 12345)          # next position id
+    u1 = oracle.uniform01(v, 1, 12345)          # next position id (other word)
     u2 = oracle.uniform01(v, 0, 12345, offset=1)  # next step
+    u4 = oracle.uniform01(v, 4, 12345)          # next counter along positions
     assert ((u0 > 0) & (u0 < 1)).all()
-    for u in (u0, u1, u2):
+    for u in (u0, u1, u2, u4):
         assert stats.kstest(u, "uniform").pvalue > 1e-3
-    assert abs(np.corrcoef(u0, u1)[0, 1]) < 0.01
-    assert abs(np.corrcoef(u0, u2)[0, 1]) < 0.01
-    assert abs(np.corrcoef(u0[:-1], u0[1:])[0, 1]) < 0.01   # words of one counter
+    for u in (u1, u2, u4):
+        assert abs(np.corrcoef(u0, u)[0, 1]) < 0.01
+    assert abs(np.corrcoef(u0[:-1], u0[1:])[0, 1]) < 0.01   # neighbouring counters
     assert not np.array_equal(u0, oracle.uniform01(v, 0, 12346))
     assert np.array_equal(u0, oracle.uniform01(v, 0, 12345))
-    # the 24-bit grid: U * 2^24 - 1/2 is an integer
-    k = u0 * (1 << 24) - 0.5
+    # the 23-bit grid: U * 2^23 - 1/2 is an integer
+    k = u0 * (1 << 23) - 0.5
     assert np.array_equal(k, np.floor(k))
 
 
