@@ -240,9 +240,11 @@ def decode_block(h_steps, W, threshold, tokens0=None):
 # U comes from a counter-based generator so that the GPU and this oracle draw
 # the same numbers: Philox-4x64 with 10 rounds (Salmon, Moraes, Dror and Shaw,
 # "Parallel random numbers: as easy as 1, 2, 3", SC'11) under the key
-# (seed, 0), at counter (v, position // 4, offset, 0); word position % 4 of the
-# output gives U = ((word >> 41) + 1/2) / 2^23, exactly representable in fp32.
-# `offset` is the caller's step counter, so every denoise step draws afresh.
+# (seed, 0), at counter (v, position // 8, offset, 0).  The block's four 64-bit
+# words hold eight 23-bit fields: position p takes word (p // 2) % 4, bits
+# 41..63 when p is even and bits 9..31 when p is odd, and U = (field + 1/2) /
+# 2^23, exactly representable in fp32.  `offset` is the caller's step counter,
+# so every denoise step draws afresh.
 
 _M64 = (1 << 64) - 1
 PHILOX_M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)   # round multipliers
@@ -285,9 +287,10 @@ def uniform01(v, pos, seed, offset=0):
     """U[v, pos] in (0, 1) for vocabulary entry v at position id pos."""
     v, pos = np.broadcast_arrays(np.asarray(v, dtype=np.int64), np.asarray(pos, dtype=np.int64))
     zero = np.zeros(v.shape, dtype=np.uint64)
-    words = philox4x64_10((v, pos >> 2, zero + np.uint64(int(offset) & _M64), zero), (seed, 0))
-    w = np.choose(pos & 3, words)
-    return ((w >> np.uint64(41)).astype(np.float64) + 0.5) / float(1 << 23)
+    words = philox4x64_10((v, pos >> 3, zero + np.uint64(int(offset) & _M64), zero), (seed, 0))
+    w = np.choose((pos >> 1) & 3, words)
+    field = np.where((pos & 1) == 0, w >> np.uint64(41), (w >> np.uint64(9)) & np.uint64(0x7FFFFF))
+    return (field.astype(np.float64) + 0.5) / float(1 << 23)
 
 
 def sample_confidence(h, W, pos, seed, temperature, offset=0, row_chunk: int = 16):

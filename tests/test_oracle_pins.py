@@ -300,14 +300,18 @@ def test_philox_uniforms_are_uniform_and_decorrelated():
     from scipy import stats
     v = np.arange(200000)
     u0 = oracle.uniform01(v, 0, 12345)
-    u1 = oracle.uniform01(v, 1, 12345)          # next position id (other word)
+    u1 = oracle.uniform01(v, 1, 12345)          # other half of the same 64-bit word
     u2 = oracle.uniform01(v, 0, 12345, offset=1)  # next step
-    u4 = oracle.uniform01(v, 4, 12345)          # next counter along positions
+    u4 = oracle.uniform01(v, 8, 12345)          # next counter along positions
     assert ((u0 > 0) & (u0 < 1)).all()
-    for u in (u0, u1, u2, u4):
+    u3 = oracle.uniform01(v, 3, 12345)          # another word of the same block
+    for u in (u0, u1, u2, u3, u4):
         assert stats.kstest(u, "uniform").pvalue > 1e-3
-    for u in (u1, u2, u4):
+    for u in (u1, u2, u3, u4):
         assert abs(np.corrcoef(u0, u)[0, 1]) < 0.01
+    # the eight positions of one block use eight distinct fields of its words
+    block = np.stack([oracle.uniform01(v[:1000], p, 12345) for p in range(8)])
+    assert len({tuple(r) for r in block}) == 8
     assert abs(np.corrcoef(u0[:-1], u0[1:])[0, 1]) < 0.01   # neighbouring counters
     assert not np.array_equal(u0, oracle.uniform01(v, 0, 12346))
     assert np.array_equal(u0, oracle.uniform01(v, 0, 12345))
