@@ -7,9 +7,11 @@ CPU-baseline leg may import it; the product path must never depend on it.
 from .bd_oracle import (MASK, block_mask, block_attention, current_block_attention,
                         confidence, commit, denoise_step, decode_block,
                         paged_read, append_block, philox4x64_10, uniform01,
-                        sample_confidence, denoise_step_sampled)
+                        sample_confidence, denoise_step_sampled, round_bf16, rms_norm,
+                        embed, decoder_layer, decoder_forward)
 
 __all__ = ["MASK", "block_mask", "block_attention", "current_block_attention",
            "confidence", "commit", "denoise_step", "decode_block",
            "paged_read", "append_block", "philox4x64_10", "uniform01",
-           "sample_confidence", "denoise_step_sampled"]
+           "sample_confidence", "denoise_step_sampled", "round_bf16", "rms_norm",
+           "embed", "decoder_layer", "decoder_forward"]

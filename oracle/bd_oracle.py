@@ -378,3 +378,85 @@ def append_block(pool, page_table, ctx_len, blk, done, page_size):
             pool[page_table[b][p // page_size], :, p % page_size, :] = blk[b, i]
         ctx[b] += L
     return pool, ctx
+
+
+# ---------------------------------------------------------------------------
+# (5) Decoder layer stack                     [RS] reproduction paragraph
+# ---------------------------------------------------------------------------
+# The summary names the decoder (initialised from SDAR-1.7B-Chat-b32) but
+# gives none of its internals.  The plainest reading that the rest supports
+# (R10-R13 of the design notes):
+#   x0      = E[token] for a confirmed position, e_mask for a masked one
+#   layer l: xn = bf16(rms_norm(x));  [q | k | v] = bf16(xn Wqkv_l^T)
+#            a  = bf16(block attention of q over layer l's cache and the
+#                 block's own k, v)
+#            x  = x + a Wo_l^T
+# with rms_norm(x) = x / sqrt(mean(x^2) + eps), no learned gain, and no MLP.
+# Activations are stored in bf16 between kernels (xn, q, k, v, a); the
+# residual stream x is kept at full precision.  bf16() below rounds to the
+# nearest bf16 value (ties to even), written out on the fp32 bit pattern.
+
+def round_bf16(x):
+    """Nearest bfloat16 value of x (via fp32, ties to even), returned as fp64."""
+    f = np.asarray(x, dtype=np.float32)
+    bits = f.view(np.uint32).astype(np.uint64)
+    lsb = (bits >> np.uint64(16)) & np.uint64(1)
+    bits = (bits + np.uint64(0x7FFF) + lsb) & np.uint64(0xFFFF0000)
+    out = bits.astype(np.uint32).view(np.float32).astype(np.float64)
+    return np.where(np.isnan(f), np.nan, out)
+
+
+def rms_norm(x, eps=1e-6):
+    """x / sqrt(mean(x^2) + eps) along the last axis (no gain)."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps)
+
+
+def embed(tokens, E, e_mask):
+    """Input rows of the decoder: E[token] where confirmed, e_mask where masked.
+
+    tokens [..., L'] int; E [V, H]; e_mask [H].  Returns [..., L', H] fp64."""
+    tokens = np.asarray(tokens)
+    E = np.asarray(E, dtype=np.float64)
+    out = np.empty(tokens.shape + (E.shape[1],))
+    masked = tokens == MASK
+    out[masked] = np.asarray(e_mask, dtype=np.float64)
+    out[~masked] = E[tokens[~masked]]
+    return out
+
+
+def decoder_layer(x, wqkv, wo, k_cache, v_cache, num_q_heads, num_kv_heads, eps=1e-6):
+    """One layer for one sequence's block.
+
+    x [L', H] (fp64 residual stream); wqkv [(Hq + 2 Hkv) D, H]; wo [H, Hq D];
+    k_cache, v_cache [C, Hkv, D] (this layer's cached tokens).  Returns
+    (new x, k_blk, v_blk) where k_blk, v_blk [L', Hkv, D] are the block's
+    keys and values of this layer (bf16 values, what a finished block appends).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    L = x.shape[0]
+    Hq, Hkv = num_q_heads, num_kv_heads
+    D = np.asarray(wo).shape[1] // Hq
+    xn = round_bf16(rms_norm(x, eps))
+    qkv = round_bf16(xn @ np.asarray(wqkv, dtype=np.float64).T)
+    q = qkv[:, :Hq * D].reshape(L, Hq, D)
+    k = qkv[:, Hq * D:(Hq + Hkv) * D].reshape(L, Hkv, D)
+    v = qkv[:, (Hq + Hkv) * D:].reshape(L, Hkv, D)
+    a = round_bf16(current_block_attention(q, k_cache, v_cache, k, v))
+    x = x + a.reshape(L, Hq * D) @ np.asarray(wo, dtype=np.float64).T
+    return x, k, v
+
+
+def decoder_forward(tokens, E, e_mask, layers, caches, num_q_heads, num_kv_heads, eps=1e-6):
+    """The layer stack over one sequence's current block.
+
+    tokens [L']; layers = [(wqkv, wo), ...]; caches = [(k_cache, v_cache), ...]
+    per layer.  Returns (x after the last layer [L', H], [k_blk per layer],
+    [v_blk per layer])."""
+    x = embed(tokens, E, e_mask)
+    ks, vs = [], []
+    for (wqkv, wo), (kc, vc) in zip(layers, caches):
+        x, k, v = decoder_layer(x, wqkv, wo, kc, vc, num_q_heads, num_kv_heads, eps)
+        ks.append(k)
+        vs.append(v)
+    return x, ks, vs

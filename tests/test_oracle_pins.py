@@ -356,3 +356,120 @@ def test_sampled_step_uses_the_commit_rule():
     exp_new, _ = oracle.commit(tokens, conf, tok, 0.5)
     assert np.array_equal(new, exp_new)
     assert (new[chosen] == tok[chosen]).all()
+
+
+# --- decoder layer stack (reading R10-R13) -------------------------------------
+def test_round_bf16_matches_torch_conversion():
+    rng = np.random.default_rng(31)
+    x = np.concatenate([rng.standard_normal(5000) * 10.0 ** rng.integers(-6, 6, 5000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.01171875, -3.0e38, 1e-40, np.inf,
+                         -np.inf]])
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_bf16(x)
+    assert np.array_equal(got, ref)
+    assert np.isnan(oracle.round_bf16([np.nan])).all()
+
+
+def test_rms_norm_closed_forms():
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((7, 64)) * 3.0
+    eps = 1e-6
+    y = oracle.rms_norm(x, eps)
+    ms = (x * x).mean(axis=1)
+    np.testing.assert_allclose((y * y).mean(axis=1), ms / (ms + eps), rtol=1e-13)
+    np.testing.assert_allclose(y / x, np.broadcast_to(1 / np.sqrt(ms + eps)[:, None], x.shape),
+                               rtol=1e-13)
+    c = np.full((1, 16), -0.5)
+    np.testing.assert_allclose(oracle.rms_norm(c, eps), -1 / np.sqrt(1 + eps / 0.25), rtol=1e-14)
+    if hasattr(F, "rms_norm"):
+        ref = F.rms_norm(torch.from_numpy(x), (64,), eps=eps).numpy()
+        np.testing.assert_allclose(y, ref, rtol=1e-12)
+
+
+def test_embed_picks_rows_and_mask_row():
+    E = np.arange(12.0).reshape(4, 3)
+    e_mask = np.array([-1.0, -2.0, -3.0])
+    got = oracle.embed(np.array([[2, -1, 0], [-1, -1, 3]]), E, e_mask)
+    assert got.tolist() == [[[6, 7, 8], [-1, -2, -3], [0, 1, 2]],
+                            [[-1, -2, -3], [-1, -2, -3], [9, 10, 11]]]
+
+
+def _layer_inputs(rng, L=5, C=7, Hq=4, Hkv=2, D=8, H=24):
+    x = rng.standard_normal((L, H))
+    wqkv = rng.standard_normal(((Hq + 2 * Hkv) * D, H)) * 0.3
+    wo = rng.standard_normal((H, Hq * D)) * 0.3
+    kc = oracle.round_bf16(rng.standard_normal((C, Hkv, D)))
+    vc = oracle.round_bf16(rng.standard_normal((C, Hkv, D)))
+    return x, wqkv, wo, kc, vc
+
+
+def test_decoder_layer_with_zero_output_projection_keeps_x():
+    rng = np.random.default_rng(33)
+    x, wqkv, wo, kc, vc = _layer_inputs(rng)
+    x2, k, v = oracle.decoder_layer(x, wqkv, np.zeros_like(wo), kc, vc, 4, 2)
+    assert np.array_equal(x2, x)
+    xn = oracle.round_bf16(oracle.rms_norm(x))
+    np.testing.assert_allclose(k.reshape(5, -1), oracle.round_bf16(xn @ wqkv[32:48].T), rtol=0)
+    np.testing.assert_allclose(v.reshape(5, -1), oracle.round_bf16(xn @ wqkv[48:64].T), rtol=0)
+
+
+def test_decoder_layer_uniform_attention_closed_form():
+    # zero query weights make every softmax uniform: each query head h then
+    # averages the values of KV head h // 2 over the cache and the block, and
+    # Wo = [I | 0] copies head outputs into the first Hq*D features of x
+    rng = np.random.default_rng(34)
+    L, C, Hq, Hkv, D = 5, 7, 4, 2, 8
+    H = Hq * D + 3
+    x, wqkv, _, kc, vc = _layer_inputs(rng, L, C, Hq, Hkv, D, H)
+    wqkv[:Hq * D] = 0.0
+    wo = np.zeros((H, Hq * D))
+    wo[:Hq * D] = np.eye(Hq * D)
+    x2, k, v = oracle.decoder_layer(x, wqkv, wo, kc, vc, Hq, Hkv)
+    vall = np.concatenate([vc, v])                          # [C + L, Hkv, D]
+    mean = vall.mean(axis=0)                                # [Hkv, D]
+    heads = oracle.round_bf16(np.stack([mean[h // 2] for h in range(Hq)]))  # [Hq, D]
+    expect = x.copy()
+    expect[:, :Hq * D] += heads.reshape(1, -1)
+    np.testing.assert_allclose(x2, expect, rtol=1e-13, atol=1e-13)
+
+
+def test_decoder_layer_matches_torch_composition():
+    rng = np.random.default_rng(35)
+    L, C, Hq, Hkv, D, H = 6, 9, 4, 2, 8, 40
+    x, wqkv, wo, kc, vc = _layer_inputs(rng, L, C, Hq, Hkv, D, H)
+
+    def bf(t):
+        return t.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+
+    xt = torch.from_numpy(x)
+    xn = bf(xt / torch.sqrt((xt * xt).mean(-1, keepdim=True) + 1e-6))
+    qkv = bf(F.linear(xn, torch.from_numpy(wqkv)))
+    q, k, v = qkv.split([Hq * D, Hkv * D, Hkv * D], dim=-1)
+    kall = torch.cat([torch.from_numpy(kc).reshape(C, -1), k]).reshape(C + L, Hkv, D)
+    vall = torch.cat([torch.from_numpy(vc).reshape(C, -1), v]).reshape(C + L, Hkv, D)
+    qh = q.reshape(L, Hq, D).permute(1, 0, 2)
+    kh = kall.repeat_interleave(Hq // Hkv, dim=1).permute(1, 0, 2)
+    vh = vall.repeat_interleave(Hq // Hkv, dim=1).permute(1, 0, 2)
+    a = F.scaled_dot_product_attention(qh, kh, vh).permute(1, 0, 2).reshape(L, Hq * D)
+    ref = xt + F.linear(bf(a), torch.from_numpy(wo))
+    x2, k2, v2 = oracle.decoder_layer(x, wqkv, wo, kc, vc, Hq, Hkv)
+    np.testing.assert_allclose(x2, ref.numpy(), rtol=1e-9, atol=1e-9)
+    assert np.array_equal(k2.reshape(L, -1), k.numpy())
+
+
+def test_decoder_forward_composes_layers():
+    rng = np.random.default_rng(36)
+    V, H, Hq, Hkv, D, L, C = 11, 16, 2, 1, 8, 4, 3
+    E = rng.standard_normal((V, H))
+    e_mask = rng.standard_normal(H)
+    tokens = np.array([3, -1, 10, -1])
+    layers = [(rng.standard_normal(((Hq + 2 * Hkv) * D, H)) * 0.2,
+               rng.standard_normal((H, Hq * D)) * 0.2) for _ in range(3)]
+    caches = [(rng.standard_normal((C, Hkv, D)), rng.standard_normal((C, Hkv, D)))
+              for _ in range(3)]
+    x, ks, vs = oracle.decoder_forward(tokens, E, e_mask, layers, caches, Hq, Hkv)
+    y = oracle.embed(tokens, E, e_mask)
+    for (wqkv, wo), (kc, vc), k, v in zip(layers, caches, ks, vs):
+        y, k1, v1 = oracle.decoder_layer(y, wqkv, wo, kc, vc, Hq, Hkv)
+        assert np.array_equal(k1, k) and np.array_equal(v1, v)
+    assert np.array_equal(x, y)
