@@ -58,6 +58,8 @@ def _args():
     ap.add_argument("--ar-threshold", type=float, default=0.95)
     ap.add_argument("--a-max", type=float, default=None,
                     help="planted amplitude bound (the workload's own by default)")
+    ap.add_argument("--temperature", type=float, default=None,
+                    help="decode with sampled tokens (bd_sample_commit) at this temperature")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every kernel from the host instead of replaying CUDA graphs")
     ap.add_argument("--workload", default=WORKLOAD,
@@ -90,7 +92,8 @@ def _inputs(w, seed=0):
 
 
 def _config(w, extra=None):
-    c = {"workload": f"{w.name}: SDAR-1.7B-shaped layer, batch {w.batch}, prefix {w.prefix}, "
+    shape = "layer" if w.num_layers == 1 else f"{w.num_layers}-layer decoder"
+    c = {"workload": f"{w.name}: SDAR-1.7B-shaped {shape}, batch {w.batch}, prefix {w.prefix}, "
                      f"block {w.block_len}, Hq {w.num_q_heads}/Hkv {w.num_kv_heads}, "
                      f"D {w.head_dim}, LM head {w.vocab}x{w.hidden}, T={w.threshold}, "
                      f"planted a~U(0,{w.a_max:g})",
@@ -158,7 +161,9 @@ def run_reference(a):
     if rank != 0:
         return
     from block_diffusion_decoding_denoise_gb300 import workload as wl
-    w = wl.WORKLOADS[WORKLOAD]
+    w = wl.WORKLOADS[a.workload]
+    if a.a_max is not None:
+        w = w.with_(a_max=a.a_max)
     W, plen, kv, q, kb, vb, h = _inputs(w)
     W64 = W.astype(np.float64)
     chunk = 8                       # one reference step = 8 denoise steps of the block
@@ -269,6 +274,8 @@ def run_cuda(a):
     bd.load()
 
     w = wl.WORKLOADS[a.workload]
+    if a.a_max is not None:
+        w = w.with_(a_max=a.a_max)
     W, plen, kv, q, kb, vb, h = _inputs(w)
     table, npg = wl.page_tables(w, plen + w.block_len)
     cache = PagedCache(npg, w.num_kv_heads, w.head_dim, torch.bfloat16, table)
@@ -281,7 +288,8 @@ def run_cuda(a):
     hd = torch.from_numpy(h).to("cuda", torch.bfloat16)
     max_ctx = int(plen.max()) + w.block_len
     eng = DenoiseEngine(Wd, cache, plen, batch=w.batch, block_len=w.block_len,
-                        num_q_heads=w.num_q_heads, threshold=w.threshold, max_ctx=max_ctx)
+                        num_q_heads=w.num_q_heads, threshold=w.threshold, max_ctx=max_ctx,
+                        temperature=a.temperature, seed=1)
     ctx0 = eng.ctx_len.clone()
     stream = torch.cuda.current_stream()
 
@@ -308,8 +316,7 @@ def run_cuda(a):
         bd.bd_block_attention(eng.caches[layer].kv, eng.ctx_len, eng.tokens, qq, kk, vv,
                               eng.attn_out, eng.attn_ws, eng.max_ctx, dev_status=eng.dev_status)
         ea[1].record(torch.cuda.current_stream())
-        bd.bd_confidence_commit(hh, eng.W, eng.T, eng.tokens, eng.p_max, eng.argmax, ncom,
-                                eng.n_masked, eng.conf_ws, dev_status=eng.dev_status)
+        eng.commit(hh, ncom)
         ea[2].record(torch.cuda.current_stream())
         step_events[s] = ea
 
@@ -415,7 +422,9 @@ def run_cuda(a):
         "config": _config(w, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                               "denoise_steps_per_block": [int(x) for x in steps_per_seq],
                               "denoise_steps_issued": steps_issued // a.steps,
-                              "check_every": a.check_every, "cuda_graphs": use_graphs}),
+                              "check_every": a.check_every, "cuda_graphs": use_graphs,
+                              "decoding": ("greedy" if a.temperature is None
+                                           else f"sampled, temperature {a.temperature}")}),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches), "clocks": clk.summary(),
         "conf_call_us_mean": 1e3 * statistics.mean(conf_ms) if conf_ms else None,
@@ -547,6 +556,8 @@ def _decode_tokens_per_s(w, W, Wd, a_max, T, ntok, check_every, graphs):
     eng = DenoiseEngine(Wd, cache, plen, batch=w.batch, block_len=w.block_len,
                         num_q_heads=w.num_q_heads, threshold=T, max_ctx=int(cap.max()))
     ctx0 = eng.ctx_len.clone()
+    if w.block_len == 1:
+        return _ar_tokens_per_s(eng, blocks, ctx0, w.batch * ntok, graphs), 1.0
     ms = steps = 0.0
     for rep in range(2):
         eng.ctx_len.copy_(ctx0)
@@ -564,6 +575,46 @@ def _decode_tokens_per_s(w, W, Wd, a_max, T, ntok, check_every, graphs):
         eng.check_status()
         ms, steps = e0.elapsed_time(e1), tot / nblk
     return w.batch * ntok / (ms / 1e3), steps
+
+
+def _ar_tokens_per_s(eng, blocks, ctx0, ntok_total, graphs):
+    """Token-by-token decoding: with one position per block every step
+    commits it, so the loop needs no host check at all.  Each token is
+    reset-mask + attention + confidence/commit + append; with `graphs` the
+    whole token sequence is one CUDA graph.  Returns tokens/s of the second
+    pass."""
+    import torch
+    from block_diffusion_decoding_denoise_gb300 import bd
+
+    def one_pass():
+        for (h, q, kb, vb) in blocks:
+            eng.tokens.fill_(bd.BD_MASK)
+            eng.step(h[0], q, kb, vb, eng.n_committed[0])
+            bd.bd_append_block_kv(eng.caches[0].kv, kb, vb, eng.ctx_len, eng.n_masked,
+                                  eng.dev_status)
+
+    g = None
+    if graphs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            one_pass()
+    ms = 0.0
+    for rep in range(2):
+        eng.ctx_len.copy_(ctx0)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        if g is not None:
+            g.replay()
+        else:
+            one_pass()
+        e1.record()
+        torch.cuda.synchronize()
+        eng.check_status()
+        ms = e0.elapsed_time(e1)
+    assert int((eng.ctx_len - ctx0).min().item()) == len(blocks)   # every token appended
+    return ntok_total / (ms / 1e3)
 
 
 def run_ar_compare(a):
@@ -597,6 +648,248 @@ def run_ar_compare(a):
         "config": _config(w, {"a_max": a_max})}))
 
 
+# ---------------------------------------------------------------------------
+# decoder workload (28-layer stack, successive blocks)
+# ---------------------------------------------------------------------------
+def _decoder_inputs(w, plen, seed=0, keep_seq=None):
+    """Per-layer prefix K/V generator: yields (layer, b, k, v); the caller loads
+    them.  Sequences of a layer are drawn in parallel threads."""
+    import concurrent.futures as cf
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    with cf.ThreadPoolExecutor(min(w.batch, _cores())) as ex:
+        for l in range(w.num_layers):
+            futs = [ex.submit(wl.prefix_kv, w, b, int(plen[b]), seed, l) for b in range(w.batch)]
+            for b, f in enumerate(futs):
+                k, v = f.result()
+                yield l, b, k, v
+
+
+def _decoder_oracle_sample(w, W, E, em, lw, host_kv, h_blk, budget_s):
+    """The oracle's denoise steps for sequence 0 of the first block: the
+    28-layer stack over the current tokens, then confidence and commit."""
+    import oracle
+    W64 = W.astype(np.float64)
+    tokens = np.full((1, w.block_len), -1, np.int64)
+    t0 = time.perf_counter()
+    steps = committed = 0
+    while True:
+        oracle.decoder_forward(tokens[0], E, em, lw, host_kv, w.num_q_heads, w.num_kv_heads)
+        new, *_ = oracle.denoise_step(tokens, h_blk[steps][:1].astype(np.float64), W64,
+                                      w.threshold)
+        committed += int((new != tokens).sum())
+        tokens = new
+        steps += 1
+        if time.perf_counter() - t0 > budget_s or steps >= w.block_len:
+            break
+    dt = time.perf_counter() - t0
+    return committed / dt, steps, committed, dt
+
+
+def run_decoder(a):
+    """The long-context workload: a 28-layer decoder stack in front of every
+    denoise step's commit, successive blocks of one decode (each finished
+    block is run through the stack once more and its K/V appended to every
+    layer before the next block)."""
+    import torch
+    rank, world, local = _dist()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the CUDA arm has no CPU fallback)")
+    torch.cuda.set_device(local)
+    from block_diffusion_decoding_denoise_gb300 import bd, build
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    from block_diffusion_decoding_denoise_gb300.engine import (DecoderStack, DenoiseEngine,
+                                                               PagedCache)
+    if not os.path.exists(bd.LIB_PATH):
+        build.build()
+    bd.load()
+    w = wl.WORKLOADS[a.workload]
+    if a.a_max is not None:
+        w = w.with_(a_max=a.a_max)
+    L, nb = w.block_len, w.num_blocks
+    plen = wl.prefix_lengths(w)
+    cap = plen + nb * L
+    table, npg = wl.page_tables(w, cap)
+    bf = torch.bfloat16
+    caches = [PagedCache(npg, w.num_kv_heads, w.head_dim, bf, table) for _ in range(w.num_layers)]
+    keep = [] if rank == 0 and not a.no_cpu_baseline else None
+    t_gen = time.perf_counter()
+    for l, b, k, v in _decoder_inputs(w, plen):
+        caches[l].load_prefix(b, torch.from_numpy(k), torch.from_numpy(v))
+        if keep is not None and b == 0:
+            keep.append((k, v))
+    W = wl.lm_head(w)
+    E = wl.embed_table(w)
+    em = wl.mask_embedding(w)
+    lw = [wl.layer_weights(w, l) for l in range(w.num_layers)]
+    dev = lambda x: torch.from_numpy(x).to("cuda", bf)
+    ctx = torch.from_numpy(plen.astype(np.int32)).cuda()
+    max_ctx = int(cap.max())
+    stack = DecoderStack(dev(E), dev(em), [(dev(x), dev(y)) for x, y in lw], caches, ctx,
+                         batch=w.batch, block_len=L, num_q_heads=w.num_q_heads, max_ctx=max_ctx)
+    eng = DenoiseEngine(dev(W), caches, plen, batch=w.batch, block_len=L,
+                        num_q_heads=w.num_q_heads, threshold=w.threshold, max_ctx=max_ctx,
+                        temperature=a.temperature, seed=1, decoder=stack)
+    h_host = [wl.planted_hidden(w, W, blk)[0] for blk in range(nb)]
+    h_dev = [dev(h) for h in h_host]
+    h_cur = torch.empty_like(h_dev[0])
+    dummy = torch.empty(1, dtype=bf, device="cuda")
+    gen_s = time.perf_counter() - t_gen
+    ctx0 = ctx.clone()
+    use_graphs = not a.no_graphs
+    ev_kw = {"enable_timing": True}
+    if use_graphs:
+        try:
+            torch.cuda.Event(enable_timing=True, external=True)
+            ev_kw["external"] = True
+        except TypeError:
+            use_graphs = False
+
+    # per-layer attention events inside every denoise step (captured into the
+    # step graphs as event nodes, read after each chunk)
+    orig_forward = stack.forward
+    events = {}
+    attn_ms = []
+    stride = eng.n_committed.stride(0) * eng.n_committed.element_size()
+    cur_step = [None]
+
+    def timed_forward(tokens, attn_tokens=None):
+        if attn_tokens is None:
+            return orig_forward(tokens, None)
+        s = cur_step[0]
+        evs = []
+        stack_attn = bd.bd_block_attention
+
+        def attn_wrap(*args, **kw):
+            e0, e1 = torch.cuda.Event(**ev_kw), torch.cuda.Event(**ev_kw)
+            e0.record(torch.cuda.current_stream())
+            stack_attn(*args, **kw)
+            e1.record(torch.cuda.current_stream())
+            evs.append((e0, e1))
+        bd.bd_block_attention = attn_wrap
+        try:
+            orig_forward(tokens, attn_tokens)
+        finally:
+            bd.bd_block_attention = stack_attn
+        events[s] = evs
+
+    orig_step = eng.step
+
+    def step(hh, qq, kk, vv, ncom=None, layer=0):
+        cur_step[0] = (ncom.data_ptr() - eng.n_committed.data_ptr()) // stride
+        orig_step(hh, qq, kk, vv, ncom, layer)
+
+    recording = [False]
+
+    def on_chunk(s0, s1):
+        if recording[0]:
+            for s in range(s0, s1):
+                for e0, e1 in events.get(s, ()):
+                    attn_ms.append(e0.elapsed_time(e1))
+
+    stack.forward = timed_forward
+    eng.step = step
+    blk_ctr = [0]
+
+    def block():
+        blk = blk_ctr[0] % nb
+        if blk == 0:
+            ctx.copy_(ctx0)
+        blk_ctr[0] += 1
+        h_cur.copy_(h_dev[blk])
+        return eng.decode_block(h_cur, dummy, dummy, dummy, check_every=a.check_every,
+                                graphs=use_graphs, on_chunk=on_chunk)
+
+    warm = max(3, a.warmup)
+    for _ in range(warm):
+        block()
+    torch.cuda.synchronize()
+    eng.check_status()
+    ctx_at = ctx.clone()
+    recording[0] = True
+    steps_issued = committed = 0
+    l0 = bd.bd_kernel_launches()
+    g0 = eng.graph_kernel_launches
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(a.steps):
+            steps_issued += block()
+            committed += w.batch * L
+        t1.record()
+        torch.cuda.synchronize()
+    recording[0] = False
+    ms = t0.elapsed_time(t1)
+    eng.check_status()
+    launches = (bd.bd_kernel_launches() - l0) + (eng.graph_kernel_launches - g0)
+    value = committed / (ms / 1e3)
+    # attention roofline: K/V of the cache + block once per KV head, Q read, O written;
+    # the context grows by one block per step, so use the mean context of the timed blocks
+    ctx_mean = float(ctx_at.float().mean().item()) + L * (a.steps - 1) / 2.0
+    attn_bytes = (2 * w.batch * (ctx_mean + L) * w.num_kv_heads * w.head_dim * 2
+                  + 2 * w.batch * L * w.num_q_heads * w.head_dim * 2)
+    peak, peak_kind = _peaks()
+    attn_us = 1e3 * statistics.mean(attn_ms) if attn_ms else None
+    achieved = attn_bytes / (attn_us / 1e6) / 1e9 if attn_us else None
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak if achieved else None, "traffic": None,
+                "kernel": "bd_block_attention (per layer, 28 per denoise step)",
+                "bytes_per_call": attn_bytes, "us_per_call": attn_us,
+                "peak_source": f"{peak_kind} hbm_gbs"}
+    stack.forward = orig_forward
+    eng.step = orig_step
+
+    # e2e: the same blocks through the public API, planted h copied from pinned
+    # host memory per block and the committed tokens read back
+    e2e = None
+    if not a.no_e2e:
+        hp = [torch.from_numpy(h).to(bf).pin_memory() for h in h_host]
+        tok_host = torch.empty(w.batch, L, dtype=torch.int32).pin_memory()
+        ctx.copy_(ctx0)
+        blk_ctr[0] = 0
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for j in range(a.steps):
+            blk = j % nb
+            if blk == 0:
+                ctx.copy_(ctx0)
+            h_cur.copy_(hp[blk], non_blocking=True)
+            eng.decode_block(h_cur, dummy, dummy, dummy, check_every=a.check_every,
+                             graphs=use_graphs)
+            tok_host.copy_(eng.tokens, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        e2e = {"value": committed / (e0.elapsed_time(e1) / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": hp[0].numel() * hp[0].element_size(),
+               "d2h_bytes_per_step": tok_host.numel() * 4}
+    if rank != 0:
+        return
+    cpu = None
+    if keep is not None:
+        v, st, c, dt = _decoder_oracle_sample(w, W, E, em, lw, keep, h_host[0], 20.0)
+        cpu = {"value": v, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+               "sample": f"sequence 0 of block 0: {st} denoise step(s) of the {w.num_layers}-"
+                         f"layer stack + commit ({c} committed tokens) in {dt:.1f} s, numpy fp64"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": a.steps,
+        "warmup": warm, "ms_per_step": ms / a.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": _config(w, {"parallelism": "single GPU", "layers": w.num_layers,
+                              "blocks_timed": a.steps,
+                              "denoise_steps_issued": steps_issued // a.steps,
+                              "check_every": a.check_every, "cuda_graphs": use_graphs,
+                              "input_generation_s": gen_s,
+                              "l2": "inputs larger than L2: 15.5 GB of per-layer KV cache",
+                              "decoding": ("greedy" if a.temperature is None
+                                           else f"sampled, temperature {a.temperature}")}),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(launches), "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+
+
 def main():
     a = _args()
     if a.impl == "reference":
@@ -606,7 +899,11 @@ def main():
     elif a.ar_compare:
         run_ar_compare(a)
     else:
-        run_cuda(a)
+        from block_diffusion_decoding_denoise_gb300 import workload as wl
+        if wl.WORKLOADS[a.workload].num_layers > 1:
+            run_decoder(a)
+        else:
+            run_cuda(a)
 
 
 if __name__ == "__main__":

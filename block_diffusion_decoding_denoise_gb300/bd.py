@@ -28,7 +28,10 @@ STATUS = {0: "BD_OK", 1: "BD_ERR_INVALID_ARG", 2: "BD_ERR_UNSUPPORTED", 3: "BD_E
 EXPORTS = ("bd_block_attention_workspace", "bd_block_attention",
            "bd_confidence_commit_workspace", "bd_confidence_commit",
            "bd_append_block_kv", "bd_status_string", "bd_version", "bd_kernel_launches",
-           "bd_confidence_commit_noalloc")
+           "bd_confidence_commit_noalloc", "bd_sample_commit_workspace", "bd_sample_commit",
+           "bd_embed_rmsnorm", "bd_qkv_projection_workspace", "bd_qkv_projection",
+           "bd_out_projection_workspace", "bd_out_projection_residual",
+           "bd_append_block_kv_layers")
 
 
 class BDError(RuntimeError):
@@ -76,6 +79,26 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                                        c_int32, c_void_p, c_void_p, c_float,
                                                        c_void_p, c_void_p, c_void_p, c_void_p,
                                                        c_void_p, c_void_p, c_void_p]),
+            "bd_sample_commit_workspace": (c_size_t, [c_int32] * 5),
+            "bd_sample_commit": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_int32,
+                                           c_void_p, c_void_p, c_float, c_float, ctypes.c_uint64,
+                                           c_void_p, c_void_p, c_void_p, c_void_p,
+                                           c_void_p, c_void_p, c_void_p, c_size_t, c_void_p,
+                                           c_void_p]),
+            "bd_embed_rmsnorm": (c_int32, [c_int32, c_int32, c_int32, c_void_p, c_void_p,
+                                           c_void_p, c_float, c_void_p, c_void_p, c_void_p,
+                                           c_void_p]),
+            "bd_qkv_projection_workspace": (c_size_t, [c_int32] * 5),
+            "bd_qkv_projection": (c_int32, [c_int32] * 5 + [c_void_p] * 6 +
+                                  [c_size_t, c_void_p, c_void_p]),
+            "bd_out_projection_workspace": (c_size_t, [c_int32] * 3),
+            "bd_out_projection_residual": (c_int32, [c_int32] * 3 + [c_void_p, c_void_p, c_float,
+                                                                    c_void_p, c_void_p, c_void_p,
+                                                                    c_size_t, c_void_p,
+                                                                    c_void_p]),
+            "bd_append_block_kv_layers": (c_int32, [P, c_int32, c_int32, c_int32, c_void_p,
+                                                    c_void_p, c_void_p, c_void_p, c_void_p,
+                                                    c_void_p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -182,6 +205,30 @@ def bd_confidence_commit_noalloc(hidden_states, lm_head, threshold, tokens, p_ma
     _check("bd_confidence_commit_noalloc", st)
 
 
+def bd_sample_commit_workspace(dtype_code, batch, block_len, hidden, vocab) -> int:
+    return int(load().bd_sample_commit_workspace(dtype_code, batch, block_len, hidden, vocab))
+
+
+def bd_sample_commit(hidden_states, lm_head, threshold, temperature, seed, offset, tokens,
+                     p_sel, sampled, n_committed, n_masked, ws, dev_status=None, stream=None):
+    """`offset` is a one-element int64 CUDA tensor: the draw counter the call
+    reads and advances by one (see bd.h)."""
+    B, L, H = hidden_states.shape
+    V = lm_head.shape[0]
+    if lm_head.shape[1] != H or lm_head.dtype != hidden_states.dtype:
+        raise ValueError("lm_head must be [vocab, hidden] with the hidden states' dtype")
+    st = load().bd_sample_commit(
+        _dtype_code(hidden_states), B, L, H, V, _ptr(hidden_states, name="hidden_states"),
+        _ptr(lm_head, name="lm_head"), float(threshold), float(temperature),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(offset, torch.int64, "offset"),
+        _ptr(tokens, torch.int32, "tokens"), _ptr(p_sel, torch.float32, "p_sel"),
+        _ptr(sampled, torch.int32, "sampled"), _ptr(n_committed, torch.int32, "n_committed"),
+        _ptr(n_masked, torch.int32, "n_masked"), _ptr(ws, name="ws"),
+        ws.numel() * ws.element_size(), _ptr(dev_status, torch.int32, "dev_status"),
+        _stream(stream))
+    _check("bd_sample_commit", st)
+
+
 def bd_append_block_kv(kv: PagedKV, k_blk, v_blk, ctx_len, n_masked=None, dev_status=None,
                        stream=None):
     B, L = k_blk.shape[0], k_blk.shape[1]
@@ -202,3 +249,62 @@ def bd_version() -> int:
 
 def bd_kernel_launches() -> int:
     return int(load().bd_kernel_launches())
+
+
+# --- decoder layer stack --------------------------------------------------------
+def bd_embed_rmsnorm(tokens, embed, mask_embed, x, xn, eps=1e-6, dev_status=None, stream=None):
+    rows = tokens.numel()
+    V, H = embed.shape
+    st = load().bd_embed_rmsnorm(
+        rows, H, V, _ptr(tokens, torch.int32, "tokens"), _ptr(embed, torch.bfloat16, "embed"),
+        _ptr(mask_embed, torch.bfloat16, "mask_embed"), float(eps),
+        _ptr(x, torch.float32, "x"), _ptr(xn, torch.bfloat16, "xn"),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("bd_embed_rmsnorm", st)
+
+
+def bd_qkv_projection_workspace(rows, hidden, num_q_heads, num_kv_heads, head_dim) -> int:
+    return int(load().bd_qkv_projection_workspace(rows, hidden, num_q_heads, num_kv_heads,
+                                                  head_dim))
+
+
+def bd_qkv_projection(xn, w_qkv, q, k, v, ws, dev_status=None, stream=None):
+    rows, H = xn.shape[0] * (xn.shape[1] if xn.dim() == 3 else 1), xn.shape[-1]
+    Hq, D = q.shape[-2], q.shape[-1]
+    Hkv = k.shape[-2]
+    st = load().bd_qkv_projection(
+        rows, H, Hq, Hkv, D, _ptr(xn, torch.bfloat16, "xn"), _ptr(w_qkv, torch.bfloat16, "w_qkv"),
+        _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"),
+        _ptr(ws, name="ws"), ws.numel() * ws.element_size(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("bd_qkv_projection", st)
+
+
+def bd_out_projection_workspace(rows, in_features, hidden) -> int:
+    return int(load().bd_out_projection_workspace(rows, in_features, hidden))
+
+
+def bd_out_projection_residual(attn, w_o, x, xn, ws, eps=1e-6, dev_status=None, stream=None):
+    H, Fin = w_o.shape
+    rows = x.numel() // H
+    st = load().bd_out_projection_residual(
+        rows, Fin, H, _ptr(attn, torch.bfloat16, "attn"), _ptr(w_o, torch.bfloat16, "w_o"),
+        float(eps), _ptr(x, torch.float32, "x"), _ptr(xn, torch.bfloat16, "xn"),
+        _ptr(ws, name="ws"), ws.numel() * ws.element_size(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("bd_out_projection_residual", st)
+
+
+def bd_append_block_kv_layers(kvs, k_blk, v_blk, ctx_len, n_masked=None, dev_status=None,
+                              stream=None):
+    """kvs: list of PagedKV (one per layer, shared page table); k_blk/v_blk
+    [layers, B, L', Hkv, D]."""
+    arr = (PagedKV * len(kvs))(*kvs)
+    L_, B, L = k_blk.shape[0], k_blk.shape[1], k_blk.shape[2]
+    if L_ != len(kvs):
+        raise ValueError("k_blk must hold one block per layer")
+    st = load().bd_append_block_kv_layers(
+        arr, len(kvs), B, L, _ptr(k_blk, name="k_blk"), _ptr(v_blk, name="v_blk"),
+        _ptr(ctx_len, torch.int32, "ctx_len"), _ptr(n_masked, torch.int32, "n_masked"),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("bd_append_block_kv_layers", st)

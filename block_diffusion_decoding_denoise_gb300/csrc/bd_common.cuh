@@ -81,6 +81,96 @@ __device__ __forceinline__ MaxSumArg merge(MaxSumArg a, MaxSumArg b) {
   return a;
 }
 
+// State of one row under temperature sampling (Gumbel-max): the online
+// softmax of z = l / temperature (max m, sum s of exp(z - m)) and the best
+// perturbed key z + G seen so far (key kb, its z zb and its index idx).
+struct SampleState {
+  float m;
+  float s;
+  float kb;
+  float zb;
+  int32_t idx;
+};
+
+// Merge two sampling states: sums rescaled to the larger max; the larger key
+// wins, equal keys keep the lower index.
+__device__ __forceinline__ void merge_sample_into(float &m, float &s, float &kb, float &zb,
+                                                  int &i, float bm, float bs, float bkb,
+                                                  float bzb, int bi) {
+  const float mm = fmaxf(m, bm);
+  s = (s > 0.f ? s * __expf(m - mm) : 0.f) + (bs > 0.f ? bs * __expf(bm - mm) : 0.f);
+  m = mm;
+  const bool take = bkb > kb || (bkb == kb && bi < i);
+  kb = take ? bkb : kb;
+  zb = take ? bzb : zb;
+  i = take ? bi : i;
+}
+
+__device__ __forceinline__ SampleState merge(SampleState a, const SampleState &b) {
+  merge_sample_into(a.m, a.s, a.kb, a.zb, a.idx, b.m, b.s, b.kb, b.zb, b.idx);
+  return a;
+}
+
+// Philox-4x64 with 10 rounds (Salmon, Moraes, Dror and Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC'11): a round multiplies c0 and c2 by the
+// two round constants into 128-bit products and mixes the halves with c1, c3
+// and the key; the key steps by the two Weyl constants between rounds.
+__device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t c1, uint64_t c2, uint64_t c3,
+                                              uint64_t k0, uint64_t k1, uint64_t (&out)[4]) {
+  constexpr uint64_t kM0 = 0xD2E7470EE14C6C93ull, kM1 = 0xCA5A826395121157ull;
+  constexpr uint64_t kW0 = 0x9E3779B97F4A7C15ull, kW1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += kW0;
+      k1 += kW1;
+    }
+    const uint64_t h0 = __umul64hi(kM0, c0), l0 = kM0 * c0;
+    const uint64_t h1 = __umul64hi(kM1, c2), l1 = kM1 * c2;
+    c0 = h1 ^ c1 ^ k0;
+    c1 = l1;
+    c2 = h0 ^ c3 ^ k1;
+    c3 = l0;
+  }
+  out[0] = c0;
+  out[1] = c1;
+  out[2] = c2;
+  out[3] = c3;
+}
+
+// The 23-bit field of position id pos in its Philox block (the block serves
+// the eight positions 8k..8k+7): word (pos / 2) % 4, bits 41..63 for even pos
+// and bits 9..31 for odd pos.
+__device__ __forceinline__ uint32_t philox_field(const uint64_t (&w)[4], int pos) {
+  const int k = (pos >> 1) & 3;
+  const uint64_t word = k == 0 ? w[0] : k == 1 ? w[1] : k == 2 ? w[2] : w[3];
+  return (pos & 1) ? static_cast<uint32_t>(word >> 9) & 0x7FFFFFu
+                   : static_cast<uint32_t>(word >> 41);
+}
+
+// Gumbel noise G = -ln(-ln U) of U = (field + 1/2) / 2^23, a value fp32 holds
+// exactly.  x = -ln U comes from the Taylor series of -ln(1 - d), d = 1 - U,
+// while d < 2^-6 (four terms, relative error below 2^-26), which keeps x
+// accurate near U = 1 where G is largest; elsewhere from the fast logarithm
+// (absolute error about 2^-21 near U = 1/2, so relative error below 1e-4 of x
+// and below 1e-4 in G).
+__device__ __forceinline__ float gumbel_of_field(uint32_t field) {
+  const float u = (static_cast<float>(field) + 0.5f) * 1.1920928955078125e-07f;   // 2^-23
+  const float d = (static_cast<float>(0x7FFFFFu - field) + 0.5f) * 1.1920928955078125e-07f;
+  const float series = d * (1.f + d * (0.5f + d * (0.33333334f + d * 0.25f)));
+  const float x = d < 0.015625f ? series : -__logf(u);
+  return -__logf(x);
+}
+
+// Gumbel noise of vocabulary entry v at position id pos: Philox block at
+// counter (v, pos / 8, draw, 0) under key (seed, 0).
+__device__ __forceinline__ float gumbel_at(int v, int pos, uint64_t seed, uint64_t draw) {
+  uint64_t w[4];
+  philox4x64_10(static_cast<uint64_t>(v), static_cast<uint64_t>(pos >> 3), draw, 0ull, seed, 0ull,
+                w);
+  return gumbel_of_field(philox_field(w, pos));
+}
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Launch counter behind bd_kernel_launches(); every host entry point adds
@@ -125,6 +215,7 @@ bool preload_attention_tc();
 bool preload_attention_tc5();
 bool preload_confidence();
 bool preload_lmhead_tc();
+bool preload_decoder();
 
 inline bd_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? BD_OK : BD_ERR_CUDA;

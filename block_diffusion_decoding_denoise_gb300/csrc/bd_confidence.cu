@@ -16,6 +16,11 @@
 //                        bd_lmhead_tc.cu)
 //   conf_commit_kernel   one warp per sequence: merge the partial states,
 //                        p_max, argmax, ballot over p_max >= T, fallback, write
+//
+// bd_sample_commit runs the same pipeline in sampling mode: each masked
+// position draws its token from softmax(l / temperature) by the Gumbel-max
+// rule, its confidence is the drawn token's probability, and the commit rule
+// is unchanged (the sampling reading of step 6's settings).
 #include <math.h>
 
 #include <algorithm>
@@ -85,23 +90,56 @@ __global__ void __launch_bounds__(1024) conf_prep_kernel(const int32_t *tokens, 
 constexpr int kSimtRows = 64, kSimtVocab = 64, kSimtK = 16;
 constexpr int kSimtChunk = 512;  // vocab entries per CTA (-> one partial per chunk)
 
-template <typename T>
+__device__ __forceinline__ MaxSumArg shfl_xor_state(const MaxSumArg &a, int o) {
+  MaxSumArg b;
+  b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+  b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+  b.idx = __shfl_xor_sync(0xffffffffu, a.idx, o);
+  return b;
+}
+
+__device__ __forceinline__ SampleState shfl_xor_state(const SampleState &a, int o) {
+  SampleState b;
+  b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+  b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+  b.kb = __shfl_xor_sync(0xffffffffu, a.kb, o);
+  b.zb = __shfl_xor_sync(0xffffffffu, a.zb, o);
+  b.idx = __shfl_xor_sync(0xffffffffu, a.idx, o);
+  return b;
+}
+
+__device__ __forceinline__ void set_empty(MaxSumArg &a) { a = MaxSumArg{-INFINITY, 0.f, 0x7fffffff}; }
+__device__ __forceinline__ void set_empty(SampleState &a) {
+  a = SampleState{-INFINITY, 0.f, -INFINITY, -INFINITY, 0x7fffffff};
+}
+
+template <bool kSample> struct ConfState { using type = MaxSumArg; };
+template <> struct ConfState<true> { using type = SampleState; };
+
+template <typename T, bool kSample>
 __global__ void __launch_bounds__(256) lmhead_simt_kernel(ConfParams p) {
+  using St = typename ConfState<kSample>::type;
   __shared__ float As[kSimtK][kSimtRows + 4];
   __shared__ float Bs[kSimtK][kSimtVocab + 4];
-  __shared__ MaxSumArg state[kSimtRows];
+  __shared__ St state[kSimtRows];
+  __shared__ int spos[kSimtRows];
   pdl_trigger();
   pdl_wait();
   const int count = *p.ws.count;
   const int r0 = blockIdx.y * kSimtRows;
   if (r0 >= count) return;
+  uint64_t draw = 0;                       // the step's draw counter (sampling)
+  if constexpr (kSample) draw = *p.offset;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int v_lo = blockIdx.x * kSimtChunk;
   const int v_hi = min(p.vocab, v_lo + kSimtChunk);
   const T *h = static_cast<const T *>(p.h);
   const T *w = static_cast<const T *>(p.w);
   const int H = p.hidden;
-  if (threadIdx.x < kSimtRows) state[threadIdx.x] = MaxSumArg{-INFINITY, 0.f, 0x7fffffff};
+  if (threadIdx.x < kSimtRows) {
+    set_empty(state[threadIdx.x]);
+    spos[threadIdx.x] = r0 + threadIdx.x < count ? p.ws.rows[r0 + threadIdx.x] : 0;
+  }
 
   for (int v0 = v_lo; v0 < v_hi; v0 += kSimtVocab) {
     float acc[4][4];
@@ -136,46 +174,61 @@ __global__ void __launch_bounds__(256) lmhead_simt_kernel(ConfParams p) {
     // epilogue: reduce each row over this tile's 64 vocab entries
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
-      MaxSumArg st{-INFINITY, 0.f, 0x7fffffff};
-#pragma unroll
-      for (int y = 0; y < 4; ++y) {
-        const int v = v0 + tx * 4 + y;
-        if (v < v_hi && acc[x][y] > st.m) {
-          st.m = acc[x][y];
-          st.idx = v;
-        }
-      }
-      if (st.idx != 0x7fffffff) {
+      St st;
+      set_empty(st);
+      if constexpr (kSample) {
+        const int pos = spos[ty * 4 + x];
 #pragma unroll
         for (int y = 0; y < 4; ++y) {
           const int v = v0 + tx * 4 + y;
-          if (v < v_hi) st.s += __expf(acc[x][y] - st.m);
+          if (v < v_hi) {
+            const float z = acc[x][y] * p.inv_temp;
+            const float key = z + gumbel_at(v, pos, p.seed, draw);
+            st = merge(st, SampleState{z, 1.f, key, z, v});
+          }
+        }
+      } else {
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const int v = v0 + tx * 4 + y;
+          if (v < v_hi && acc[x][y] > st.m) {
+            st.m = acc[x][y];
+            st.idx = v;
+          }
+        }
+        if (st.idx != 0x7fffffff) {
+#pragma unroll
+          for (int y = 0; y < 4; ++y) {
+            const int v = v0 + tx * 4 + y;
+            if (v < v_hi) st.s += __expf(acc[x][y] - st.m);
+          }
         }
       }
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {
-        MaxSumArg other;
-        other.m = __shfl_xor_sync(0xffffffffu, st.m, o);
-        other.s = __shfl_xor_sync(0xffffffffu, st.s, o);
-        other.idx = __shfl_xor_sync(0xffffffffu, st.idx, o);
-        st = merge(st, other);
-      }
+      for (int o = 8; o > 0; o >>= 1) st = merge(st, shfl_xor_state(st, o));
       if (tx == 0) state[ty * 4 + x] = merge(state[ty * 4 + x], st);
     }
   }
   __syncthreads();
   if (threadIdx.x < kSimtRows) {
     const int r = r0 + threadIdx.x;
-    if (r < count) p.ws.partial[(size_t)blockIdx.x * (p.batch * p.block_len) + r] = state[threadIdx.x];
+    St *part;
+    if constexpr (kSample) part = p.ws.spartial;
+    else part = p.ws.partial;
+    if (r < count) part[(size_t)blockIdx.x * (p.batch * p.block_len) + r] = state[threadIdx.x];
   }
+}
+
+template <bool kSample> static cudaError_t launch_simt(const ConfParams &p, dim3 grid, cudaStream_t st) {
+  return p.dtype == BD_F32
+             ? launch_pdl(lmhead_simt_kernel<float, kSample>, grid, dim3(256), 0, st, p)
+             : launch_pdl(lmhead_simt_kernel<__nv_bfloat16, kSample>, grid, dim3(256), 0, st, p);
 }
 
 bd_status lmhead_simt(const ConfParams &p, cudaStream_t st) {
   const int nrows = p.batch * p.block_len;
   dim3 grid((p.vocab + kSimtChunk - 1) / kSimtChunk, (nrows + kSimtRows - 1) / kSimtRows);
-  const cudaError_t e =
-      p.dtype == BD_F32 ? launch_pdl(lmhead_simt_kernel<float>, grid, dim3(256), 0, st, p)
-                        : launch_pdl(lmhead_simt_kernel<__nv_bfloat16>, grid, dim3(256), 0, st, p);
+  const cudaError_t e = p.sample ? launch_simt<true>(p, grid, st) : launch_simt<false>(p, grid, st);
   count_launches(1);
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
@@ -184,13 +237,19 @@ bd_status lmhead_simt(const ConfParams &p, cudaStream_t st) {
 // commit: one CTA per sequence; warp i merges the partial states of position
 // i (lanes stride over the producers), warp 0 then takes the decision
 // ---------------------------------------------------------------------------
+template <bool kSample>
 __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
+  using St = typename ConfState<kSample>::type;
   __shared__ float s_pm[32];
   __shared__ int s_am[32];
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = p.block_len;
   pdl_trigger();
   pdl_wait();
+  // the LM-head kernel has read the draw counter (it completed before this
+  // kernel passed the wait); advance it for the next call on the stream
+  if constexpr (kSample)
+    if (b == 0 && threadIdx.x == 0) *p.offset += 1;
   if (warp < L) {
     const int pos = b * L + warp;
     float pm = -1.f;
@@ -198,17 +257,18 @@ __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
     if (p.tokens[pos] == BD_MASK) {
       const int k = p.ws.row_of[pos];
       const size_t stride = (size_t)p.batch * L;
-      MaxSumArg st{-INFINITY, 0.f, 0x7fffffff};
-      for (int c = lane; c < p.ws.num_partials; c += 32) st = merge(st, p.ws.partial[c * stride + k]);
+      St st;
+      set_empty(st);
+      const St *part;
+      if constexpr (kSample) part = p.ws.spartial;
+      else part = p.ws.partial;
+      for (int c = lane; c < p.ws.num_partials; c += 32) st = merge(st, part[c * stride + k]);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        MaxSumArg other;
-        other.m = __shfl_xor_sync(0xffffffffu, st.m, o);
-        other.s = __shfl_xor_sync(0xffffffffu, st.s, o);
-        other.idx = __shfl_xor_sync(0xffffffffu, st.idx, o);
-        st = merge(st, other);
+      for (int o = 16; o > 0; o >>= 1) st = merge(st, shfl_xor_state(st, o));
+      if (lane == 0) {
+        if constexpr (kSample) finalize_sample_row(p, st, pm, am);
+        else finalize_row(p, st, pm, am);
       }
-      if (lane == 0) finalize_row(p, st, pm, am);
     }
     if (lane == 0) {
       s_pm[warp] = pm;
@@ -236,9 +296,13 @@ int conf_num_partials(bd_dtype dtype, int batch, int block_len, int hidden, int 
 }
 
 bool preload_confidence() {
-  return preload_kernel(conf_prep_kernel, false) && preload_kernel(conf_commit_kernel, false) &&
-         preload_kernel(lmhead_simt_kernel<float>, false) &&
-         preload_kernel(lmhead_simt_kernel<__nv_bfloat16>, false);
+  return preload_kernel(conf_prep_kernel, false) &&
+         preload_kernel(conf_commit_kernel<false>, false) &&
+         preload_kernel(conf_commit_kernel<true>, false) &&
+         preload_kernel(lmhead_simt_kernel<float, false>, false) &&
+         preload_kernel(lmhead_simt_kernel<__nv_bfloat16, false>, false) &&
+         preload_kernel(lmhead_simt_kernel<float, true>, false) &&
+         preload_kernel(lmhead_simt_kernel<__nv_bfloat16, true>, false);
 }
 
 static size_t carve(const ConfParams &p, char *base, ConfWorkspace *ws) {
@@ -251,13 +315,14 @@ static size_t carve(const ConfParams &p, char *base, ConfWorkspace *ws) {
     return ptr;
   };
   char *rows = take(n * 4), *row_of = take(n * 4), *count = take(4);
-  char *part = take((size_t)np * n * sizeof(MaxSumArg));
+  char *part = take((size_t)np * n * (p.sample ? sizeof(SampleState) : sizeof(MaxSumArg)));
   char *hc = p.dtype == BD_BF16 ? take(n * (size_t)p.hidden * 2) : nullptr;
   if (ws) {
     ws->rows = reinterpret_cast<int32_t *>(rows);
     ws->row_of = reinterpret_cast<int32_t *>(row_of);
     ws->count = reinterpret_cast<int32_t *>(count);
     ws->partial = reinterpret_cast<MaxSumArg *>(part);
+    ws->spartial = reinterpret_cast<SampleState *>(part);
     ws->num_partials = np;
     ws->hc = hc;
   }
@@ -274,12 +339,8 @@ static bool conf_args_ok(bd_dtype dtype, int32_t batch, int32_t block_len, int32
   return true;
 }
 
-}  // namespace bd
-
-using namespace bd;
-
-BD_API size_t bd_confidence_commit_workspace(bd_dtype dtype, int32_t batch, int32_t block_len,
-                                             int32_t hidden, int32_t vocab) {
+static size_t conf_workspace(bd_dtype dtype, int32_t batch, int32_t block_len, int32_t hidden,
+                             int32_t vocab, bool sample) {
   if (!conf_args_ok(dtype, batch, block_len, hidden, vocab)) return 0;
   preload_all();
   ConfParams p{};
@@ -288,7 +349,56 @@ BD_API size_t bd_confidence_commit_workspace(bd_dtype dtype, int32_t batch, int3
   p.block_len = block_len;
   p.hidden = hidden;
   p.vocab = vocab;
+  p.sample = sample ? 1 : 0;
   return carve(p, nullptr, nullptr);
+}
+
+// Shared body of bd_confidence_commit and bd_sample_commit: argument checks,
+// workspace carve, then prep -> LM head -> commit on one stream.
+static bd_status conf_run(ConfParams &p, const void *hidden_states, const void *lm_head,
+                          void *ws, size_t ws_bytes, void *stream) {
+  if (!conf_args_ok(p.dtype, p.batch, p.block_len, p.hidden, p.vocab)) return BD_ERR_INVALID_ARG;
+  if (!hidden_states || !lm_head || !p.tokens || !p.p_max || !p.argmax || !p.n_committed ||
+      !p.n_masked)
+    return BD_ERR_INVALID_ARG;
+  if (!preload_all()) return BD_ERR_CUDA;
+  if (isnan(p.threshold)) return BD_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(hidden_states) | reinterpret_cast<uintptr_t>(lm_head)) & 15)
+    return BD_ERR_INVALID_ARG;
+  p.h = hidden_states;
+  p.w = lm_head;
+  const size_t need = carve(p, nullptr, nullptr);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return BD_ERR_WORKSPACE;
+  carve(p, static_cast<char *>(ws), &p.ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  const bool tc = lmhead_tc_supported(p);
+  const int nrows = p.batch * p.block_len;
+  // the tensor-core path reads the masked rows from a contiguous copy
+  const int prep_ctas = tc ? std::max(1, std::min(std::max(dev_info().sms, 1), (nrows + 7) / 8)) : 1;
+  const int32_t *tok_in = p.tokens;
+  const char *src = tc ? static_cast<const char *>(hidden_states) : nullptr;
+  cudaError_t e = launch_pdl(conf_prep_kernel, dim3(prep_ctas), dim3(1024), 0, st, tok_in, nrows,
+                             p.ws, src, p.hidden * 2);
+  count_launches(1);
+  if (e != cudaSuccess) return BD_ERR_CUDA;
+  const bd_status s = tc ? lmhead_tc(p, st) : lmhead_simt(p, st);
+  if (s != BD_OK) return s;
+  e = p.sample ? launch_pdl(conf_commit_kernel<true>, dim3(p.batch), dim3(32 * p.block_len), 0,
+                            st, p)
+               : launch_pdl(conf_commit_kernel<false>, dim3(p.batch), dim3(32 * p.block_len), 0,
+                            st, p);
+  count_launches(1);
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
+
+}  // namespace bd
+
+using namespace bd;
+
+BD_API size_t bd_confidence_commit_workspace(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                             int32_t hidden, int32_t vocab) {
+  return conf_workspace(dtype, batch, block_len, hidden, vocab, false);
 }
 
 BD_API bd_status bd_confidence_commit(bd_dtype dtype, int32_t batch, int32_t block_len,
@@ -297,21 +407,12 @@ BD_API bd_status bd_confidence_commit(bd_dtype dtype, int32_t batch, int32_t blo
                                       float *p_max, int32_t *argmax, int32_t *n_committed,
                                       int32_t *n_masked, void *ws, size_t ws_bytes,
                                       int32_t *dev_status, void *stream) {
-  if (!conf_args_ok(dtype, batch, block_len, hidden, vocab)) return BD_ERR_INVALID_ARG;
-  if (!hidden_states || !lm_head || !tokens || !p_max || !argmax || !n_committed || !n_masked)
-    return BD_ERR_INVALID_ARG;
-  if (!preload_all()) return BD_ERR_CUDA;
-  if (isnan(threshold)) return BD_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(hidden_states) | reinterpret_cast<uintptr_t>(lm_head)) & 15)
-    return BD_ERR_INVALID_ARG;
   ConfParams p{};
   p.dtype = dtype;
   p.batch = batch;
   p.block_len = block_len;
   p.hidden = hidden;
   p.vocab = vocab;
-  p.h = hidden_states;
-  p.w = lm_head;
   p.threshold = threshold;
   p.tokens = tokens;
   p.p_max = p_max;
@@ -319,24 +420,38 @@ BD_API bd_status bd_confidence_commit(bd_dtype dtype, int32_t batch, int32_t blo
   p.n_committed = n_committed;
   p.n_masked = n_masked;
   p.dev_status = dev_status;
-  const size_t need = carve(p, nullptr, nullptr);
-  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return BD_ERR_WORKSPACE;
-  carve(p, static_cast<char *>(ws), &p.ws);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return conf_run(p, hidden_states, lm_head, ws, ws_bytes, stream);
+}
 
-  const bool tc = lmhead_tc_supported(p);
-  const int nrows = batch * block_len;
-  // the tensor-core path reads the masked rows from a contiguous copy
-  const int prep_ctas = tc ? std::max(1, std::min(std::max(dev_info().sms, 1), (nrows + 7) / 8)) : 1;
-  const int32_t *tok_in = tokens;
-  const char *src = tc ? static_cast<const char *>(hidden_states) : nullptr;
-  cudaError_t e = launch_pdl(conf_prep_kernel, dim3(prep_ctas), dim3(1024), 0, st, tok_in, nrows,
-                             p.ws, src, hidden * 2);
-  count_launches(1);
-  if (e != cudaSuccess) return BD_ERR_CUDA;
-  const bd_status s = tc ? lmhead_tc(p, st) : lmhead_simt(p, st);
-  if (s != BD_OK) return s;
-  e = launch_pdl(conf_commit_kernel, dim3(batch), dim3(32 * block_len), 0, st, p);
-  count_launches(1);
-  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+BD_API size_t bd_sample_commit_workspace(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                         int32_t hidden, int32_t vocab) {
+  return conf_workspace(dtype, batch, block_len, hidden, vocab, true);
+}
+
+BD_API bd_status bd_sample_commit(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                  int32_t hidden, int32_t vocab, const void *hidden_states,
+                                  const void *lm_head, float threshold, float temperature,
+                                  uint64_t seed, uint64_t *offset, int32_t *tokens, float *p_sel,
+                                  int32_t *sampled, int32_t *n_committed, int32_t *n_masked,
+                                  void *ws, size_t ws_bytes, int32_t *dev_status, void *stream) {
+  if (!(temperature >= 1e-6f) || !(temperature <= 1e6f)) return BD_ERR_INVALID_ARG;
+  if (!offset || (reinterpret_cast<uintptr_t>(offset) & 7)) return BD_ERR_INVALID_ARG;
+  ConfParams p{};
+  p.dtype = dtype;
+  p.batch = batch;
+  p.block_len = block_len;
+  p.hidden = hidden;
+  p.vocab = vocab;
+  p.threshold = threshold;
+  p.tokens = tokens;
+  p.p_max = p_sel;
+  p.argmax = sampled;
+  p.n_committed = n_committed;
+  p.n_masked = n_masked;
+  p.dev_status = dev_status;
+  p.sample = 1;
+  p.inv_temp = 1.0f / temperature;
+  p.seed = seed;
+  p.offset = offset;
+  return conf_run(p, hidden_states, lm_head, ws, ws_bytes, stream);
 }

@@ -14,10 +14,12 @@ namespace bd {
 //   row_of   [B*L] int32   position -> compact row (-1 if not masked)
 //   count    [1]   int32   number of masked rows
 //   partial  [P][B*L] MaxSumArg   one online-softmax state per producer and row
+//                                 (SampleState when sampling)
 //   hc       [B*L][H] bf16        masked rows of h, compacted (bf16 only)
 struct ConfWorkspace {
   int32_t *rows, *row_of, *count;
   MaxSumArg *partial;
+  SampleState *spartial;  // the same memory, typed for the sampling mode
   int num_partials;
   char *hc;
 };
@@ -28,11 +30,32 @@ struct ConfParams {
   const void *h, *w;
   float threshold;
   int32_t *tokens;
-  float *p_max;
-  int32_t *argmax, *n_committed, *n_masked;
+  float *p_max;                 // greedy: p_max; sampling: probability of the draw
+  int32_t *argmax, *n_committed, *n_masked;   // argmax: greedy argmax or the draw
   int32_t *dev_status;
+  // sampling mode (bd_sample_commit): z = l * inv_temp, draw by Gumbel-max;
+  // *offset is the device-side draw counter (read by the LM-head kernel,
+  // advanced by one by the commit kernel)
+  int sample;
+  float inv_temp;
+  uint64_t seed;
+  uint64_t *offset;
   ConfWorkspace ws;
 };
+
+// Confidence and token of a row from its merged sampling state: the drawn
+// token and its probability exp(z_token - m) / s.
+__device__ __forceinline__ void finalize_sample_row(const ConfParams &p, const SampleState &st,
+                                                    float &pm, int &am) {
+  if (st.idx < 0 || st.idx >= p.vocab || !(st.s >= 1.f) || !(st.zb <= st.m)) {
+    flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+    pm = 0.f;
+    am = 0;
+  } else {
+    pm = __expf(st.zb - st.m) / st.s;
+    am = st.idx;
+  }
+}
 
 // p_max and argmax of a row from its merged online-softmax state.
 __device__ __forceinline__ void finalize_row(const ConfParams &p, const MaxSumArg &st, float &pm,

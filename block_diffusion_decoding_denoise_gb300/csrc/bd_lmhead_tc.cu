@@ -14,7 +14,7 @@
 // B operand), so a step with only a handful of masked rows still fills the
 // 128-lane tensor-core tile and the kernel streams W at HBM speed.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over vocabulary tiles
+// Warp roles (320 threads, one CTA per SM, persistent over vocabulary tiles
 // vt = blockIdx.x + i * gridDim.x):
 //   warp 0     TMA producer: per 64-wide K chunk, one 128x64 box of W and
 //              16x64 boxes of the compacted masked rows of h (conf_prep_kernel
@@ -24,10 +24,16 @@
 //              per stage into one of two TMEM accumulators; tcgen05.commit
 //              frees the stage and, after the last K chunk, hands the
 //              accumulator to the epilogue
-//   warps 2-5  epilogue: tcgen05.ld 32 lanes x 16 columns; a transposing
+//   warps 2-9  epilogue, two warps per TMEM lane quarter taking alternate
+//              16-column chunks: tcgen05.ld 32 lanes x 16 columns; a transposing
 //              butterfly over the 32 lanes reduces the 16 columns to one
 //              (max, sum-exp, argmax) each; a 4-warp merge through smem; a
 //              running state per row kept in registers
+// Sampling mode (kSample, bd_sample_commit): the epilogue scales the logits
+// by 1 / temperature, adds per-entry Gumbel noise from the counter-based
+// generator (one Philox block per vocabulary entry and group of eight
+// positions, shared by consecutive masked rows of the same group) and keeps
+// the online softmax of z together with the best perturbed key.
 // Each CTA writes one partial state per row; conf_commit_kernel (launched
 // right behind, with programmatic dependent launch) merges them and commits.
 // Every mbarrier wait is bounded (1 s); on expiry the kernel records
@@ -45,11 +51,14 @@ using namespace sm100;
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;               // epilogue warps: two per TMEM lane quarter
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTileV = 128;                 // vocabulary entries per tile (MMA M)
 constexpr int kKChunk = 64;                 // K elements per stage (128 bytes of bf16)
 constexpr int kMaxN = 256;                  // masked rows per pass (MMA N)
-constexpr int kBoxRows = 16;                // rows of the compact h copy per TMA box
+constexpr int kBoxRows = 16;                // rows of the compact h copy per small TMA box
+constexpr int kBigBoxRows = 64;             // ... per large box (whole 64-row groups)
 constexpr int kABytes = kTileV * 128;       // 16 KB of W per stage
 constexpr int kMaxStages = 12;
 constexpr uint32_t kTmemCols = 2 * kMaxN;   // two accumulators (all 512 columns)
@@ -71,7 +80,9 @@ struct LmTcArgs {
   int stage_bytes;
   int num_tiles;
   int nmax;       // masked rows per pass this launch can hold (multiple of 16)
-  int red_off;    // smem offsets of the merge buffer and Ctrl
+  int big_boxes;  // 1: tmap_h64 (64-row boxes) is valid
+  int red_off;    // smem offsets of the merge buffer, the row positions
+  int pos_off;    // (sampling only) and Ctrl
   int ctrl_off;
 };
 
@@ -125,14 +136,131 @@ __device__ __forceinline__ void bfly_round(float (&m)[16], float (&s)[16], int (
   }
 }
 
+// bfly_round for sampling states (online softmax of z plus the best key).
+template <int K>
+__device__ __forceinline__ void bfly_round_s(float (&m)[16], float (&s)[16], float (&kb)[16],
+                                             float (&zb)[16], int (&id)[16], int off, int lane) {
+  const bool upper = (lane & off) != 0;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const float send_m = upper ? m[k] : m[K + k];
+    const float send_s = upper ? s[k] : s[K + k];
+    const float send_kb = upper ? kb[k] : kb[K + k];
+    const float send_zb = upper ? zb[k] : zb[K + k];
+    const int send_i = upper ? id[k] : id[K + k];
+    float km = upper ? m[K + k] : m[k];
+    float ks = upper ? s[K + k] : s[k];
+    float kkb = upper ? kb[K + k] : kb[k];
+    float kzb = upper ? zb[K + k] : zb[k];
+    int ki = upper ? id[K + k] : id[k];
+    const float rm = __shfl_xor_sync(0xffffffffu, send_m, off);
+    const float rs = __shfl_xor_sync(0xffffffffu, send_s, off);
+    const float rkb = __shfl_xor_sync(0xffffffffu, send_kb, off);
+    const float rzb = __shfl_xor_sync(0xffffffffu, send_zb, off);
+    const int ri = __shfl_xor_sync(0xffffffffu, send_i, off);
+    merge_sample_into(km, ks, kkb, kzb, ki, rm, rs, rkb, rzb, ri);
+    m[k] = km;
+    s[k] = ks;
+    kb[k] = kkb;
+    zb[k] = kzb;
+    id[k] = ki;
+  }
+}
+
+// 16 accumulator columns (rows c0..c0+15 of the pass) x 32 vocabulary lanes
+// -> one greedy state per column, written to red[c0 .. c0+15].
+__device__ __forceinline__ void reduce_chunk(const uint32_t (&r)[16], int vbase, bool valid,
+                                             int lane, MaxSumArg *red) {
+  // a transposing butterfly: each round halves the columns a lane keeps and
+  // merges the partner's copy of them
+  float m[16], sx[16];
+  int id[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    m[j] = valid ? __uint_as_float(r[j]) : -INFINITY;
+    sx[j] = valid ? 1.f : 0.f;
+    id[j] = valid ? vbase + lane : 0x7fffffff;
+  }
+  bfly_round<8>(m, sx, id, 16, lane);
+  bfly_round<4>(m, sx, id, 8, lane);
+  bfly_round<2>(m, sx, id, 4, lane);
+  bfly_round<1>(m, sx, id, 2, lane);
+  {
+    const float om = __shfl_xor_sync(0xffffffffu, m[0], 1);
+    const float os = __shfl_xor_sync(0xffffffffu, sx[0], 1);
+    const int oi = __shfl_xor_sync(0xffffffffu, id[0], 1);
+    merge_into(m[0], sx[0], id[0], om, os, oi);
+  }
+  // lanes 2k and 2k+1 now hold column k of the 32 lanes' reduction
+  if ((lane & 1) == 0) red[lane >> 1] = MaxSumArg{m[0], sx[0], id[0]};
+}
+
+// Sampling variant: z = l * inv_temp, key = z + Gumbel(v, pos).  pos[j] is
+// the position id of column j; consecutive columns of one group of eight
+// positions reuse one Philox block (the group test is uniform across the warp).
+__device__ __forceinline__ void reduce_chunk(const uint32_t (&r)[16], int vbase, bool valid,
+                                             int lane, SampleState *red, const int *pos,
+                                             float inv_temp, uint64_t seed, uint64_t offset) {
+  float m[16], sx[16], kb[16], zb[16];
+  int id[16];
+  const int v = vbase + lane;
+  uint64_t w[4] = {0ull, 0ull, 0ull, 0ull};
+  int prev_g = -1;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int pj = pos[j];
+    const int g = pj >> 3;
+    if (g != prev_g) {
+      philox4x64_10(static_cast<uint64_t>(v), static_cast<uint64_t>(g), offset, 0ull, seed, 0ull,
+                    w);
+      prev_g = g;
+    }
+    const float z = __uint_as_float(r[j]) * inv_temp;
+    const float key = z + gumbel_of_field(philox_field(w, pj));
+    m[j] = valid ? z : -INFINITY;
+    sx[j] = valid ? 1.f : 0.f;
+    kb[j] = valid ? key : -INFINITY;
+    zb[j] = valid ? z : -INFINITY;
+    id[j] = valid ? v : 0x7fffffff;
+  }
+  bfly_round_s<8>(m, sx, kb, zb, id, 16, lane);
+  bfly_round_s<4>(m, sx, kb, zb, id, 8, lane);
+  bfly_round_s<2>(m, sx, kb, zb, id, 4, lane);
+  bfly_round_s<1>(m, sx, kb, zb, id, 2, lane);
+  {
+    const float om = __shfl_xor_sync(0xffffffffu, m[0], 1);
+    const float os = __shfl_xor_sync(0xffffffffu, sx[0], 1);
+    const float okb = __shfl_xor_sync(0xffffffffu, kb[0], 1);
+    const float ozb = __shfl_xor_sync(0xffffffffu, zb[0], 1);
+    const int oi = __shfl_xor_sync(0xffffffffu, id[0], 1);
+    merge_sample_into(m[0], sx[0], kb[0], zb[0], id[0], om, os, okb, ozb, oi);
+  }
+  if ((lane & 1) == 0) red[lane >> 1] = SampleState{m[0], sx[0], kb[0], zb[0], id[0]};
+}
+
+template <bool kSample> struct StateOf { using type = MaxSumArg; };
+template <> struct StateOf<true> { using type = SampleState; };
+
+template <typename St> __device__ __forceinline__ St empty_state();
+template <> __device__ __forceinline__ MaxSumArg empty_state<MaxSumArg>() {
+  return MaxSumArg{-INFINITY, 0.f, 0x7fffffff};
+}
+template <> __device__ __forceinline__ SampleState empty_state<SampleState>() {
+  return SampleState{-INFINITY, 0.f, -INFINITY, -INFINITY, 0x7fffffff};
+}
+
+template <bool kSample>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                     const __grid_constant__ CUtensorMap tmap_h, const LmTcArgs a) {
+                     const __grid_constant__ CUtensorMap tmap_h,
+                     const __grid_constant__ CUtensorMap tmap_h64, const LmTcArgs a) {
+  using St = typename StateOf<kSample>::type;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + a.ctrl_off);
-  MaxSumArg *red = reinterpret_cast<MaxSumArg *>(smem + a.red_off);   // [2][4][nmax]
+  St *red = reinterpret_cast<St *>(smem + a.red_off);   // [2][4][nmax]
+  int *spos = reinterpret_cast<int *>(smem + a.pos_off);  // [nmax], sampling only
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ConfParams &p = a.p;
 
@@ -149,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctrl->tfull[i]), 1);
-      mbar_init(smem_u32(&ctrl->tempty[i]), 4);
+      mbar_init(smem_u32(&ctrl->tempty[i]), kEpiWarps);
     }
     mbar_init(smem_u32(&ctrl->mma_done), 1);
     ctrl->abort = 0;
@@ -158,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_w);
     tma_prefetch_desc(&tmap_h);
+    if (a.big_boxes) tma_prefetch_desc(&tmap_h64);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctrl->tmem_base), kTmemCols);
@@ -200,7 +329,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t bar = smem_u32(&ctrl->full[s]);
               mbar_arrive_expect_tx(bar, tx);
               tma_load_2d_hint(smem_u32(st), &tmap_w, kc * kKChunk, vt * kTileV, bar, w_policy);
-              for (int r = 0; r < npad; r += kBoxRows)
+              // whole 64-row groups in one box each (fewer, larger copies), the
+              // rest of the pass in 16-row boxes
+              int r = 0;
+              if (a.big_boxes)
+                for (; r + kBigBoxRows <= npad; r += kBigBoxRows)
+                  tma_load_2d(smem_u32(st + kABytes + r * 128), &tmap_h64, kc * kKChunk, r0 + r,
+                              bar);
+              for (; r < npad; r += kBoxRows)
                 tma_load_2d(smem_u32(st + kABytes + r * 128), &tmap_h, kc * kKChunk, r0 + r, bar);
             }
           }
@@ -265,16 +401,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;                 // slot of this warp in the merge buffer
-    const int q = warp & 3;                  // TMEM sub-partition this warp may read
-    const int tid_e = threadIdx.x - 64;      // 0..127: rows tid_e, tid_e + 128 of the pass
+    const int ew = warp - 2;                 // 0..7
+    const int q = warp & 3;                  // TMEM lane quarter this warp may read
+    const int slot = ew & 3;                 // merge-buffer slot (one per lane quarter)
+    const int half = ew >> 2;                // the two warps of a quarter split the chunks
+    const int tid_e = threadIdx.x - 64;      // 0..255: row tid_e of the pass
+    uint64_t draw = 0;                       // the step's draw counter (sampling)
+    if constexpr (kSample) draw = *p.offset;
     uint32_t tg = 0;
     bool stop = false;
     for (int pass = 0; pass < npass && !stop; ++pass) {
       const int r0 = pass * kMaxN;
       const int n = min(kMaxN, count - r0);
       const int npad = (n + 15) & ~15;
-      MaxSumArg run{-INFINITY, 0.f, 0x7fffffff}, run2{-INFINITY, 0.f, 0x7fffffff};
+      St run = empty_state<St>();
+      if constexpr (kSample) {
+        // position ids of this pass's rows (the previous pass's readers have
+        // all passed the per-tile barrier below)
+        for (int i = tid_e; i < npad; i += kEpiThreads) spos[i] = i < n ? p.ws.rows[r0 + i] : 0;
+        named_barrier(2, kEpiThreads);
+      }
       for (int t = 0; t < my_tiles; ++t, ++tg) {
         const int vt = cta + t * G;
         const uint32_t acc = tg & 1, use = tg >> 1;
@@ -285,34 +431,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const int vbase = vt * kTileV + 32 * q;
           const bool valid = vbase + lane < p.vocab;
-          for (int c0 = 0; c0 < npad; c0 += 16) {
+          for (int c0 = 16 * half; c0 < npad; c0 += 32) {
             uint32_t r[16];
             tmem_ld_32x32b_x16(tmem + ((uint32_t)(32 * q) << 16) + acc * kMaxN + c0, r);
             tmem_ld_wait();
-            // 16 columns x 32 vocabulary lanes -> one (max, sum-exp, argmax) per
-            // column, by a transposing butterfly: each round halves the columns a
-            // lane keeps and merges the partner's copy of them
-            float m[16], sx[16];
-            int id[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              m[j] = valid ? __uint_as_float(r[j]) : -INFINITY;
-              sx[j] = valid ? 1.f : 0.f;
-              id[j] = valid ? vbase + lane : 0x7fffffff;
-            }
-            bfly_round<8>(m, sx, id, 16, lane);
-            bfly_round<4>(m, sx, id, 8, lane);
-            bfly_round<2>(m, sx, id, 4, lane);
-            bfly_round<1>(m, sx, id, 2, lane);
-            {
-              const float om = __shfl_xor_sync(0xffffffffu, m[0], 1);
-              const float os = __shfl_xor_sync(0xffffffffu, sx[0], 1);
-              const int oi = __shfl_xor_sync(0xffffffffu, id[0], 1);
-              merge_into(m[0], sx[0], id[0], om, os, oi);
-            }
-            // lanes 2k and 2k+1 now hold column c0 + k of the 32 lanes' reduction
-            if ((lane & 1) == 0)
-              red[((tg & 1) * 4 + ew) * a.nmax + c0 + (lane >> 1)] = MaxSumArg{m[0], sx[0], id[0]};
+            St *dst = red + ((tg & 1) * 4 + slot) * a.nmax + c0;
+            if constexpr (kSample)
+              reduce_chunk(r, vbase, valid, lane, dst, spos + c0, p.inv_temp, p.seed, draw);
+            else
+              reduce_chunk(r, vbase, valid, lane, dst);
           }
           tc_fence_before();
           __syncwarp();
@@ -321,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ctrl->abort = 1;
           if (lane == 0) flag_error(p.dev_status, BD_ERR_TIMEOUT);
         }
-        if (barrier_or(1, 128, !ok || ctrl->abort)) {
+        if (barrier_or(1, kEpiThreads, !ok || ctrl->abort)) {
           stop = true;
           break;
         }
@@ -329,14 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int w = 0; w < 4; ++w) run = merge(run, red[((tg & 1) * 4 + w) * a.nmax + tid_e]);
         }
-        if (tid_e + 128 < npad) {
-#pragma unroll
-          for (int w = 0; w < 4; ++w)
-            run2 = merge(run2, red[((tg & 1) * 4 + w) * a.nmax + tid_e + 128]);
-        }
       }
-      if (!stop && tid_e < n) p.ws.partial[(size_t)cta * stride + r0 + tid_e] = run;
-      if (!stop && tid_e + 128 < n) p.ws.partial[(size_t)cta * stride + r0 + tid_e + 128] = run2;
+      St *part;
+      if constexpr (kSample) part = p.ws.spartial;
+      else part = p.ws.partial;
+      if (!stop && tid_e < n) part[(size_t)cta * stride + r0 + tid_e] = run;
     }
   }
 
@@ -364,17 +488,22 @@ void plan(const ConfParams &p, LmTcArgs &a, size_t *smem) {
   const int nmax = std::min(kMaxN, (rows + 15) & ~15);
   a.nmax = nmax;
   a.stage_bytes = (kABytes + nmax * 128 + 1023) & ~1023;
-  const int red = (2 * 4 * nmax * (int)sizeof(MaxSumArg) + 1023) & ~1023;
-  const int fixed = red + (int)sizeof(Ctrl) + 1024;
+  const int state = p.sample ? (int)sizeof(SampleState) : (int)sizeof(MaxSumArg);
+  const int red = (2 * 4 * nmax * state + 1023) & ~1023;
+  const int pos = p.sample ? ((nmax * 4 + 127) & ~127) : 0;
+  const int fixed = red + pos + (int)sizeof(Ctrl) + 1024;
   a.stages = std::max(2, std::min(kMaxStages, (kSmemLimit - fixed) / a.stage_bytes));
   a.red_off = a.stages * a.stage_bytes;
-  a.ctrl_off = a.red_off + red;
+  a.pos_off = a.red_off + red;
+  a.ctrl_off = a.pos_off + pos;
   *smem = (size_t)a.ctrl_off + sizeof(Ctrl) + 1024;
 }
 
 }  // namespace
 
-bool preload_lmhead_tc() { return preload_kernel(lmhead_tc_kernel, true); }
+bool preload_lmhead_tc() {
+  return preload_kernel(lmhead_tc_kernel<false>, true) && preload_kernel(lmhead_tc_kernel<true>, true);
+}
 
 bool lmhead_tc_supported(const ConfParams &p) {
   if (p.dtype != BD_BF16 || p.hidden % kKChunk != 0 || p.hidden < kKChunk) return false;
@@ -396,13 +525,24 @@ bd_status lmhead_tc(const ConfParams &p, cudaStream_t st) {
   size_t smem;
   plan(p, a, &smem);
   if (smem > (size_t)kSmemLimit) return BD_ERR_UNSUPPORTED;
-  CUtensorMap mw, mh;
+  CUtensorMap mw, mh, mh64;
+  const uint64_t rows = (uint64_t)p.batch * p.block_len;
   if (!make_map(&mw, p.w, p.hidden, p.vocab, kKChunk, kTileV)) return BD_ERR_CUDA;
-  if (!make_map(&mh, p.ws.hc, p.hidden, (uint64_t)p.batch * p.block_len, kKChunk, kBoxRows))
-    return BD_ERR_CUDA;
+  if (!make_map(&mh, p.ws.hc, p.hidden, rows, kKChunk, kBoxRows)) return BD_ERR_CUDA;
+  // the large-box map only when a whole 64-row group can exist
+  a.big_boxes = rows >= (uint64_t)kBigBoxRows ? 1 : 0;
+  if (a.big_boxes) {
+    if (!make_map(&mh64, p.ws.hc, p.hidden, rows, kKChunk, kBigBoxRows)) return BD_ERR_CUDA;
+  } else {
+    mh64 = mh;
+  }
   const int grid = p.ws.num_partials;
   if (grid < 1 || grid > a.num_tiles) return BD_ERR_INVALID_ARG;
-  const cudaError_t e = launch_pdl(lmhead_tc_kernel, dim3(grid), dim3(kThreads), smem, st, mw, mh, a);
+  const cudaError_t e =
+      p.sample
+          ? launch_pdl(lmhead_tc_kernel<true>, dim3(grid), dim3(kThreads), smem, st, mw, mh, mh64, a)
+          : launch_pdl(lmhead_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, st, mw, mh, mh64,
+                       a);
   count_launches(1);
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }

@@ -61,7 +61,17 @@ class DenoiseEngine:
     """One batch of sequences decoding blocks of `block_len` tokens."""
 
     def __init__(self, lm_head: torch.Tensor, caches, ctx_len, *, batch: int, block_len: int,
-                 num_q_heads: int, threshold: float, max_ctx: int):
+                 num_q_heads: int, threshold: float, max_ctx: int,
+                 temperature: float | None = None, seed: int = 0, decoder=None):
+        """`temperature` None: greedy confidence (bd_confidence_commit); a
+        number: sampled tokens (bd_sample_commit) with key `seed` and a device
+        draw counter that every step advances, also under graph replay.
+        `decoder` (a DecoderStack sharing this engine's ctx_len): every step
+        runs the layer stack over the current tokens (its attention replaces
+        the single-layer attention call), and a finished block is run through
+        the stack once more with its committed tokens to produce the K/V that
+        every layer appends."""
+        self.decoder = decoder
         self.W = lm_head
         self.caches = caches if isinstance(caches, (list, tuple)) else [caches]
         self.B, self.L, self.Hq = batch, block_len, num_q_heads
@@ -72,7 +82,8 @@ class DenoiseEngine:
         self.Hkv, self.D = c0.k.shape[1], c0.k.shape[3]
         self.dtype = lm_head.dtype
         self.V, self.H = lm_head.shape
-        self.ctx_len = torch.as_tensor(np.asarray(ctx_len, np.int32)).to(dev)
+        self.ctx_len = (decoder.ctx_len if decoder is not None
+                        else torch.as_tensor(np.asarray(ctx_len, np.int32)).to(dev))
         self.tokens = torch.full((batch, block_len), MASK, dtype=torch.int32, device=dev)
         self.p_max = torch.empty(batch, block_len, dtype=torch.float32, device=dev)
         self.argmax = torch.empty(batch, block_len, dtype=torch.int32, device=dev)
@@ -84,7 +95,12 @@ class DenoiseEngine:
         code = bd.BD_BF16 if self.dtype == torch.bfloat16 else bd.BD_F32
         aws = bd.bd_block_attention_workspace(batch, block_len, num_q_heads, self.Hkv, self.D,
                                               self.max_ctx)
-        cws = bd.bd_confidence_commit_workspace(code, batch, block_len, self.H, self.V)
+        self.temperature = None if temperature is None else float(temperature)
+        self.seed = int(seed)
+        self.draw_counter = torch.zeros(1, dtype=torch.int64, device=dev)
+        query = (bd.bd_confidence_commit_workspace if self.temperature is None
+                 else bd.bd_sample_commit_workspace)
+        cws = query(code, batch, block_len, self.H, self.V)
         if cws == 0:
             raise ValueError("unsupported confidence-commit shape")
         self.attn_ws = torch.empty(max(aws, 1), dtype=torch.uint8, device=dev)
@@ -95,12 +111,33 @@ class DenoiseEngine:
 
     # -- one denoise step ---------------------------------------------------
     def step(self, h, q, k_blk, v_blk, n_committed_out=None, layer: int = 0):
-        bd.bd_block_attention(self.caches[layer].kv, self.ctx_len, self.tokens, q, k_blk, v_blk,
-                              self.attn_out, self.attn_ws, self.max_ctx,
-                              dev_status=self.dev_status)
-        bd.bd_confidence_commit(h, self.W, self.T, self.tokens, self.p_max, self.argmax,
-                                self.n_committed[0] if n_committed_out is None
-                                else n_committed_out, self.n_masked, self.conf_ws,
+        if self.decoder is not None:
+            self.decoder.forward(self.tokens, attn_tokens=self.tokens)
+        else:
+            bd.bd_block_attention(self.caches[layer].kv, self.ctx_len, self.tokens, q, k_blk,
+                                  v_blk, self.attn_out, self.attn_ws, self.max_ctx,
+                                  dev_status=self.dev_status)
+        self.commit(h, self.n_committed[0] if n_committed_out is None else n_committed_out)
+
+    def append_block(self, k_blk, v_blk):
+        """Append the finished block's K/V (every layer's, with a decoder)."""
+        if self.decoder is not None:
+            self.decoder.forward(self.tokens)
+            self.decoder.append(self.n_masked)
+        else:
+            bd.bd_append_block_kv(self.caches[0].kv, k_blk, v_blk, self.ctx_len, self.n_masked,
+                                  self.dev_status)
+
+    def commit(self, h, n_committed_out):
+        """The confidence/commit call of one step (greedy or sampled)."""
+        if self.temperature is None:
+            bd.bd_confidence_commit(h, self.W, self.T, self.tokens, self.p_max, self.argmax,
+                                    n_committed_out, self.n_masked, self.conf_ws,
+                                    dev_status=self.dev_status)
+        else:
+            bd.bd_sample_commit(h, self.W, self.T, self.temperature, self.seed,
+                                self.draw_counter, self.tokens, self.p_max, self.argmax,
+                                n_committed_out, self.n_masked, self.conf_ws,
                                 dev_status=self.dev_status)
 
     # -- CUDA graphs of step chunks -----------------------------------------
@@ -152,8 +189,7 @@ class DenoiseEngine:
             s = s1
             if int(self._host_masked.sum()) == 0 or s >= self.L:
                 break
-        bd.bd_append_block_kv(self.caches[0].kv, k_blk, v_blk, self.ctx_len, self.n_masked,
-                              self.dev_status)
+        self.append_block(k_blk, v_blk)
         return s
 
     def steps_per_sequence(self) -> np.ndarray:
@@ -162,5 +198,77 @@ class DenoiseEngine:
 
     def check_status(self):
         st = int(self.dev_status.item())
+        if st == 0 and self.decoder is not None:
+            st = int(self.decoder.dev_status.item())
         if st != 0:
             raise bd.BDError("device check", st)
+
+
+class DecoderStack:
+    """The layer stack that feeds the block attention in the long-context
+    workload: embedding + RMSNorm, then per layer QKV projection, block
+    attention over that layer's paged cache and output projection with the
+    residual add (bd_embed_rmsnorm, bd_qkv_projection, bd_block_attention,
+    bd_out_projection_residual).  All layers share one page table and one
+    ctx_len; a finished block's K/V of every layer is appended by one
+    bd_append_block_kv_layers call."""
+
+    def __init__(self, embed: torch.Tensor, mask_embed: torch.Tensor, layers, caches, ctx_len,
+                 *, batch: int, block_len: int, num_q_heads: int, max_ctx: int,
+                 eps: float = 1e-6):
+        self.E, self.e_mask = embed, mask_embed
+        self.layers = list(layers)                 # [(wqkv, wo)] bf16 on the device
+        self.caches = list(caches)                 # [PagedCache] sharing one page table
+        assert len(self.layers) == len(self.caches)
+        self.ctx_len = ctx_len
+        self.B, self.L, self.Hq = batch, block_len, num_q_heads
+        c0 = self.caches[0]
+        self.Hkv, self.D = c0.k.shape[1], c0.k.shape[3]
+        self.H = embed.shape[1]
+        self.max_ctx, self.eps = int(max_ctx), float(eps)
+        dev = embed.device
+        rows = batch * block_len
+        nl = len(self.layers)
+        self.x = torch.empty(rows, self.H, dtype=torch.float32, device=dev)
+        self.xn = torch.empty(rows, self.H, dtype=torch.bfloat16, device=dev)
+        self.q = torch.empty(batch, block_len, num_q_heads, self.D, dtype=torch.bfloat16,
+                             device=dev)
+        self.k = torch.empty(nl, batch, block_len, self.Hkv, self.D, dtype=torch.bfloat16,
+                             device=dev)
+        self.v = torch.empty_like(self.k)
+        self.attn = torch.empty_like(self.q)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        qws = bd.bd_qkv_projection_workspace(rows, self.H, num_q_heads, self.Hkv, self.D)
+        ows = bd.bd_out_projection_workspace(rows, num_q_heads * self.D, self.H)
+        aws = bd.bd_block_attention_workspace(batch, block_len, num_q_heads, self.Hkv, self.D,
+                                              self.max_ctx)
+        if qws == 0 or ows == 0:
+            raise ValueError("unsupported decoder shape")
+        self.ws = torch.empty(max(qws, ows, 1), dtype=torch.uint8, device=dev)
+        self.attn_ws = torch.empty(max(aws, 1), dtype=torch.uint8, device=dev)
+        # every layer addresses its pool through one shared page table
+        for c in self.caches[1:]:
+            if not np.array_equal(c.page_table_np, c0.page_table_np):
+                raise ValueError("decoder layers must share one page table")
+        self.kvs = [bd.paged_kv(c.k, c.v, c0.page_table) for c in self.caches]
+
+    def forward(self, tokens, attn_tokens=None):
+        """Run the stack over the block whose state is `tokens` [B, L'].
+        `attn_tokens` (or None) lets the attention skip finished sequences.
+        Leaves x (after the last layer) and every layer's block K/V in
+        self.x, self.k, self.v."""
+        bd.bd_embed_rmsnorm(tokens, self.E, self.e_mask, self.x, self.xn, self.eps,
+                            self.dev_status)
+        for l, (wqkv, wo) in enumerate(self.layers):
+            bd.bd_qkv_projection(self.xn, wqkv, self.q, self.k[l], self.v[l], self.ws,
+                                 self.dev_status)
+            bd.bd_block_attention(self.kvs[l], self.ctx_len, attn_tokens, self.q, self.k[l],
+                                  self.v[l], self.attn, self.attn_ws, self.max_ctx,
+                                  dev_status=self.dev_status)
+            bd.bd_out_projection_residual(self.attn, wo, self.x, self.xn, self.ws, self.eps,
+                                          self.dev_status)
+
+    def append(self, n_masked=None):
+        """Append the block K/V of the last forward to every layer's cache."""
+        bd.bd_append_block_kv_layers(self.kvs, self.k, self.v, self.ctx_len, n_masked,
+                                     self.dev_status)

@@ -42,6 +42,7 @@ PAGE_SIZE = 64
 # stream ids (fixed forever: changing one changes every stored expectation)
 S_Q, S_KBLK, S_VBLK, S_KPRE, S_VPRE, S_W = 1, 2, 3, 4, 5, 6
 S_TGT, S_AMP, S_NOISE, S_PERM, S_PLEN = 7, 8, 9, 10, 11
+S_EMB, S_EMASK, S_WQKV, S_WO = 12, 13, 14, 15
 
 
 @dataclasses.dataclass(frozen=True)
@@ -204,3 +205,26 @@ def page_tables(w: Workload, ctx_capacity: np.ndarray, seed: int = 0):
         table[b, :n] = perm[off:off + n]
         off += n
     return table, num_pages
+
+
+# --- decoder-layer inputs (the 28-layer long-context workload) -----------------
+def embed_table(w: Workload, seed: int = 0) -> np.ndarray:
+    """Token embedding E [V, H], N(0,1), in storage precision."""
+    return to_storage(normal_f32((w.vocab, w.hidden), seed, w.wid, S_EMB), w.dtype)
+
+
+def mask_embedding(w: Workload, seed: int = 0) -> np.ndarray:
+    """Embedding row of the mask token [H], N(0,1), in storage precision."""
+    return to_storage(normal_f32((w.hidden,), seed, w.wid, S_EMASK), w.dtype)
+
+
+def layer_weights(w: Workload, layer: int, seed: int = 0):
+    """Projection weights of one decoder layer, N(0, w_std^2), storage precision:
+    wqkv [(Hq + 2 Hkv) D, H] (rows: q heads, then k heads, then v heads) and
+    wo [H, Hq D]."""
+    nqkv = (w.num_q_heads + 2 * w.num_kv_heads) * w.head_dim
+    wqkv = normal_f32((nqkv, w.hidden), seed, w.wid, S_WQKV, layer, std=w.w_std)
+    wo = normal_f32((w.hidden, w.num_q_heads * w.head_dim), seed, w.wid, S_WO, layer,
+                    std=w.w_std)
+    return to_storage(wqkv, w.dtype), to_storage(wo, w.dtype)
+

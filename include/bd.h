@@ -173,6 +173,44 @@ bd_status bd_confidence_commit_noalloc(bd_dtype dtype, int32_t batch, int32_t bl
                                        int32_t *n_masked, int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * bd_sample_commit -- bd_confidence_commit under the sampling reading of the
+ * inference settings (method step 6 lists top-k 0, temperature 1.0, top-p
+ * 1.0; read as sampling, each masked position draws its token from
+ * softmax(logits / temperature) with no top-k or nucleus truncation).
+ *
+ * For every still-masked position (b, i), with pos = b * block_len + i:
+ *   z_v      = (hidden_states[b,i,:] . lm_head[v,:]) / temperature
+ *   U_v      = ((word >> 41) + 1/2) / 2^23, word = word (pos % 4) of
+ *              Philox-4x64-10 (Salmon et al., SC'11) at counter
+ *              (v, pos / 4, n, 0) under key (seed, 0)
+ *   sampled  = lowest v attaining max_v (z_v - ln(-ln U_v))   (Gumbel-max)
+ *   p_sel    = softmax(z)[sampled]
+ * then the commit rule of bd_confidence_commit with p_sel as the confidence
+ * and sampled as the token.
+ *
+ *   offset     DEVICE pointer to a uint64 draw counter n (8-byte aligned),
+ *              owned by the caller.  The call draws with the value it finds
+ *              there (in stream order) and adds 1 to it, so consecutive
+ *              steps on a stream, including replays of a captured CUDA
+ *              graph, draw fresh noise.  Equal (seed, n, inputs) give equal
+ *              results.
+ *   p_sel      [batch][block_len] float out (-1 at positions not masked on entry)
+ *   sampled    [batch][block_len] int32 out (-1 likewise)
+ *   other arguments, workspace rules and limits as bd_confidence_commit, with
+ *   bd_sample_commit_workspace() in place of its workspace query;
+ *   1e-6 <= temperature <= 1e6 and offset non-NULL, else BD_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------ */
+size_t bd_sample_commit_workspace(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                  int32_t hidden, int32_t vocab);
+
+bd_status bd_sample_commit(bd_dtype dtype, int32_t batch, int32_t block_len, int32_t hidden,
+                           int32_t vocab, const void *hidden_states, const void *lm_head,
+                           float threshold, float temperature, uint64_t seed, uint64_t *offset,
+                           int32_t *tokens, float *p_sel, int32_t *sampled,
+                           int32_t *n_committed, int32_t *n_masked, void *ws, size_t ws_bytes,
+                           int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
  * bd_append_block_kv -- append a finished block's K/V to the paged cache
  * (novelty paragraph: block-causal structure lets earlier blocks' K/V be
  * reused).  For every sequence b with n_masked[b] == 0 (NULL = all):
@@ -185,6 +223,70 @@ bd_status bd_confidence_commit_noalloc(bd_dtype dtype, int32_t batch, int32_t bl
 bd_status bd_append_block_kv(const bd_paged_kv *kv, int32_t batch, int32_t block_len,
                              const void *k_blk, const void *v_blk, int32_t *ctx_len,
                              const int32_t *n_masked, int32_t *dev_status, void *stream);
+
+/* ========================================================================
+ * Decoder layer stack (the long-context workload's 28-layer decoder).
+ *
+ * "Rethinking Document OCR as Inverse Rendering via Diffusion Decoding"
+ * (paper.rainbus.top summary), reproduction paragraph: the diffusion decoder
+ * is initialised from SDAR-1.7B-Chat-b32 (hidden 2048, 16 query / 8 KV heads
+ * of 128).  The pages give no layer internals; these calls compute the
+ * plainest reading, one layer being
+ *   xn = bf16(x / sqrt(mean(x^2) + eps))      (RMSNorm, no gain)
+ *   [q | k | v] = bf16(xn Wqkv^T)             (bd_qkv_projection)
+ *   a = bf16(block attention)                 (bd_block_attention)
+ *   x = x + a Wo^T; next xn                   (bd_out_projection_residual)
+ * with no MLP.  x (the residual stream) is fp32 [rows][hidden]; every other
+ * activation is bf16.  rows = batch * block_len, row r = b * block_len + i.
+ * Weights are bf16, row-major [out_features][in_features].  These calls need
+ * a GPU with tcgen05 (sm_100 family) and return BD_ERR_UNSUPPORTED elsewhere.
+ * ======================================================================== */
+
+/* bd_embed_rmsnorm -- decoder input: x[r] = E[tokens[r]] for a confirmed
+ * position, mask_embed for tokens[r] == BD_MASK; xn[r] = RMSNorm(x[r]).
+ *   tokens [rows] int32; embed [vocab][hidden] bf16; mask_embed [hidden] bf16;
+ *   x [rows][hidden] float out; xn [rows][hidden] bf16 out.
+ * A token outside [0, vocab) sets BD_ERR_DEVICE_CHECK and uses mask_embed.
+ * Limits: hidden % 4 == 0, hidden <= 4096; pointers 16-byte aligned. */
+bd_status bd_embed_rmsnorm(int32_t rows, int32_t hidden, int32_t vocab, const int32_t *tokens,
+                           const void *embed, const void *mask_embed, float eps, float *x,
+                           void *xn, int32_t *dev_status, void *stream);
+
+/* bd_qkv_projection -- [q | k | v] = bf16(xn Wqkv^T).
+ *   xn [rows][hidden] bf16; w_qkv [(Hq + 2 Hkv) D][hidden] bf16 (rows: the
+ *   query heads, then the key heads, then the value heads);
+ *   q [rows][Hq][D], k and v [rows][Hkv][D] bf16 out.
+ *   ws: at least bd_qkv_projection_workspace() bytes, 256-byte aligned.
+ * Limits: hidden % 64 == 0; (Hq + 2 Hkv) D % 128 == 0. */
+size_t bd_qkv_projection_workspace(int32_t rows, int32_t hidden, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim);
+bd_status bd_qkv_projection(int32_t rows, int32_t hidden, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, const void *xn,
+                            const void *w_qkv, void *q, void *k, void *v, void *ws,
+                            size_t ws_bytes, int32_t *dev_status, void *stream);
+
+/* bd_out_projection_residual -- x += attn Wo^T, then xn = RMSNorm(x) (the
+ * next layer's input).
+ *   attn [rows][in_features] bf16; w_o [hidden][in_features] bf16;
+ *   x [rows][hidden] float in/out; xn [rows][hidden] bf16 out.
+ *   ws: at least bd_out_projection_workspace() bytes, 256-byte aligned.
+ * Limits: in_features % 64 == 0; hidden % 128 == 0, hidden <= 4096. */
+size_t bd_out_projection_workspace(int32_t rows, int32_t in_features, int32_t hidden);
+bd_status bd_out_projection_residual(int32_t rows, int32_t in_features, int32_t hidden,
+                                     const void *attn, const void *w_o, float eps, float *x,
+                                     void *xn, void *ws, size_t ws_bytes, int32_t *dev_status,
+                                     void *stream);
+
+/* bd_append_block_kv_layers -- bd_append_block_kv for num_layers layers that
+ * share one page table and one ctx_len (kv: host array of num_layers structs
+ * with equal dtype, geometry and page_table; only the pools differ).
+ *   k_blk, v_blk [num_layers][batch][block_len][num_kv_heads][head_dim].
+ * Every done sequence's block goes to positions ctx_len[b] .. + block_len - 1
+ * of every layer, then ctx_len[b] += block_len once.  num_layers <= 64. */
+bd_status bd_append_block_kv_layers(const bd_paged_kv *kv, int32_t num_layers, int32_t batch,
+                                    int32_t block_len, const void *k_blk, const void *v_blk,
+                                    int32_t *ctx_len, const int32_t *n_masked,
+                                    int32_t *dev_status, void *stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *bd_status_string(bd_status status);

@@ -193,3 +193,103 @@ def lockstep_block(w: wl.Workload, W: np.ndarray, h_steps: np.ndarray, threshold
             assert np.array_equal(o_tok, tokens)
             assert np.array_equal(o_steps, steps_gpu)
     return stats
+
+
+class SampleRunner:
+    """Runs bd_sample_commit step by step on device buffers."""
+
+    def __init__(self, w: wl.Workload, W: np.ndarray, threshold: float, temperature: float,
+                 seed: int):
+        self.w, self.T, self.temp, self.seed = w, threshold, temperature, seed
+        self.W = dev(W, w.dtype)
+        B, L = w.batch, w.block_len
+        code = bd.BD_F32 if w.dtype == "f32" else bd.BD_BF16
+        n = bd.bd_sample_commit_workspace(code, B, L, w.hidden, w.vocab)
+        assert n > 0
+        self.ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        self.tokens = torch.full((B, L), -1, dtype=torch.int32, device="cuda")
+        self.p_sel = torch.empty(B, L, dtype=torch.float32, device="cuda")
+        self.sampled = torch.empty(B, L, dtype=torch.int32, device="cuda")
+        self.ncom = torch.empty(B, dtype=torch.int32, device="cuda")
+        self.nmask = torch.empty(B, dtype=torch.int32, device="cuda")
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.offset = torch.zeros(1, dtype=torch.int64, device="cuda")
+
+    def set_tokens(self, tokens: np.ndarray):
+        self.tokens.copy_(torch.from_numpy(tokens.astype(np.int32)))
+
+    def step(self, h_dev, offset: int | None = None):
+        """One call; `offset` sets the device draw counter first (None: keep it)."""
+        if offset is not None:
+            self.offset.fill_(offset)
+        before = int(self.offset.item())
+        bd.bd_sample_commit(h_dev, self.W, self.T, self.temp, self.seed, self.offset,
+                            self.tokens, self.p_sel, self.sampled, self.ncom, self.nmask,
+                            self.ws, dev_status=self.status)
+        torch.cuda.synchronize()
+        assert int(self.status.item()) == 0, bd.STATUS.get(int(self.status.item()))
+        assert int(self.offset.item()) == before + 1      # the call advanced the counter
+        return (self.tokens.cpu().numpy().astype(np.int64), self.p_sel.cpu().numpy(),
+                self.sampled.cpu().numpy().astype(np.int64), self.ncom.cpu().numpy(),
+                self.nmask.cpu().numpy())
+
+
+def lockstep_sampled_block(w: wl.Workload, W: np.ndarray, h_steps: np.ndarray, threshold: float,
+                           temperature: float, seed: int, tokens0: np.ndarray | None = None,
+                           max_steps: int | None = None):
+    """Sampled denoising of one block (offset = step index) on the GPU, every
+    step compared with the oracle's sampled step on the same token state.
+
+    Exemptions: a drawn token may differ where the oracle's two best
+    perturbed keys are within 1e-3; a commit decision may differ there, where
+    |p_sel - T| < 1e-3, or where the fallback's two best candidates are
+    within 1e-3.  The comparison then continues from the GPU's tokens."""
+    B, L = w.batch, w.block_len
+    tol = tol_for(w.dtype)
+    run = SampleRunner(w, W, threshold, temperature, seed)
+    tokens = np.full((B, L), -1, np.int64) if tokens0 is None else tokens0.astype(np.int64)
+    run.set_tokens(tokens)
+    Wd = W.astype(np.float64)
+    stats = StepStats(np.zeros(B, np.int64), None, None, None)
+    s = 0
+    while (tokens == -1).any() and (max_steps is None or s < max_steps):
+        assert s < h_steps.shape[0], "block did not finish"
+        active = (tokens == -1).any(axis=1)
+        g_tok, g_p, g_s, g_nc, g_nm = run.step(dev(h_steps[s], w.dtype), offset=s)
+        exp_tok, o_p, o_s, chosen, res, (bi, ii) = oracle.denoise_step_sampled(
+            tokens, h_steps[s].astype(np.float64), Wd, threshold, temperature, seed, s)
+        stats.rows_checked += len(bi)
+        unmasked = tokens != -1
+        assert (g_p[unmasked] == -1).all() and (g_s[unmasked] == -1).all()
+        key_exempt = res["key_gap"] < EXEMPT
+        same = g_s[bi, ii] == o_s[bi, ii]
+        bad = ~same & ~key_exempt
+        stats.argmax_mismatch_nonexempt += int(bad.sum())
+        assert not bad.any(), f"sampled token mismatch at non-exempt rows, step {s}"
+        err = np.abs(g_p[bi, ii] - o_p[bi, ii])[same]
+        if err.size:
+            stats.max_pmax_err = max(stats.max_pmax_err, float(err.max()))
+            assert err.max() <= tol, f"p_sel error {err.max()} > {tol} at step {s}"
+        exempt_pos = np.zeros((B, L), bool)
+        exempt_pos[bi, ii] = key_exempt | (np.abs(o_p[bi, ii] - threshold) < EXEMPT)
+        for b in range(B):
+            mb = tokens[b] == -1
+            if mb.any() and not (o_p[b][mb] >= threshold).any() and mb.sum() > 1:
+                ps = np.sort(o_p[b][mb])
+                if ps[-1] - ps[-2] < EXEMPT:
+                    exempt_pos[b] |= mb & (o_p[b] > ps[-1] - EXEMPT)
+        diff = g_tok != exp_tok
+        stats.exempt_positions += int((diff & exempt_pos).sum())
+        bad = diff & ~exempt_pos
+        stats.commit_mismatch_nonexempt += int(bad.sum())
+        assert not bad.any(), f"commit mismatch at non-exempt positions, step {s}: {np.argwhere(bad)}"
+        if diff.any():
+            stats.lockstep_adoptions += 1
+        assert np.array_equal(g_nc, (g_tok != tokens).sum(axis=1))
+        assert np.array_equal(g_nm, (g_tok == -1).sum(axis=1))
+        assert ((g_nc >= 1) | ~active).all()
+        stats.steps_gpu += active
+        tokens = g_tok
+        s += 1
+    stats.final_gpu = tokens
+    return stats

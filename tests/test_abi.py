@@ -66,3 +66,17 @@ def test_null_arguments_are_rejected_before_any_launch(lib):
     kv = bd.PagedKV(1, 4, 64, 8, 128, 4, None, None, None)
     st = lib.bd_append_block_kv(ctypes.byref(kv), 1, 32, None, None, None, None, None, None)
     assert st == 1
+
+
+def test_sample_commit_checks_arguments_on_the_host(lib):
+    assert bd.bd_sample_commit_workspace(bd.BD_BF16, 1, 32, 2048, 151936) >= \
+        bd.bd_confidence_commit_workspace(bd.BD_BF16, 1, 32, 2048, 151936)
+    assert bd.bd_sample_commit_workspace(bd.BD_BF16, 1, 33, 2048, 151936) == 0
+    f = lib.bd_sample_commit
+    for temp in (0.0, -1.0, float("nan"), float("inf")):
+        st = f(1, 1, 32, 2048, 1000, None, None, 0.9, temp, 1, None, None, None, None, None,
+               None, None, 0, None, None)
+        assert st == 1
+    st = f(1, 1, 32, 2048, 1000, None, None, 0.9, 1.0, 1, None, None, None, None, None, None,
+           None, 0, None, None)
+    assert st == 1

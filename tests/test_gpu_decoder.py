@@ -1,0 +1,189 @@
+"""GPU parity of the decoder layer stack (embedding + RMSNorm, QKV projection,
+block attention, output projection with the residual add, per-layer append)
+against the oracle's decoder_forward.
+
+Tolerances: bf16 activations (xn, q, k, v) may differ from the oracle by one
+bf16 rounding step (the GPU accumulates in fp32, the oracle in fp64, and a
+value near a rounding boundary can land on either side) plus the fp32
+accumulation error of a K-term dot product: |d| <= 2^-7 |ref| +
+2^-18 sum_k |x_k w_k| + 1e-6.  The fp32 residual stream after a layer stack is
+held to max-abs 2e-2 (the bf16 tolerance of the target statement); the
+observed error is printed.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_diffusion_decoding_denoise_gb300 import bd
+from block_diffusion_decoding_denoise_gb300 import workload as wl
+from block_diffusion_decoding_denoise_gb300.engine import DecoderStack, PagedCache
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_diffusion_decoding_denoise_gb300 import build
+    build.build()
+    bd.load()
+
+
+def _bf(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to("cuda", torch.bfloat16)
+
+
+def _close_bf16(got, ref, absdot=None):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    tol = 2.0 ** -7 * np.abs(ref) + 1e-6
+    if absdot is not None:
+        tol = tol + 2.0 ** -18 * absdot
+    err = np.abs(got - ref)
+    bad = err > tol
+    assert not bad.any(), (f"{bad.sum()} of {bad.size} values off by more than one bf16 step; "
+                           f"worst {err[bad].max():.3e} at |ref| {np.abs(ref[bad]).max():.3e}")
+
+
+def test_embed_rmsnorm_matches_oracle():
+    rng = np.random.default_rng(41)
+    V, H, rows = 300, 2048, 70
+    E = wl.round_bf16(rng.standard_normal((V, H)).astype(np.float32))
+    em = wl.round_bf16(rng.standard_normal(H).astype(np.float32))
+    tok = rng.integers(0, V, rows).astype(np.int32)
+    tok[::3] = -1
+    x = torch.empty(rows, H, device="cuda")
+    xn = torch.empty(rows, H, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.bd_embed_rmsnorm(torch.from_numpy(tok).cuda(), _bf(E), _bf(em), x, xn, 1e-6, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = oracle.embed(tok, E, em)
+    assert np.array_equal(x.cpu().numpy(), ref.astype(np.float32))
+    _close_bf16(xn.float().cpu().numpy(), oracle.round_bf16(oracle.rms_norm(ref)))
+
+
+@pytest.mark.parametrize("rows,H,Hq,Hkv,D", [(256, 2048, 16, 8, 128), (300, 2048, 16, 8, 128),
+                                             (5, 128, 2, 1, 64), (40, 512, 8, 2, 64)])
+def test_qkv_projection_matches_oracle(rows, H, Hq, Hkv, D):
+    rng = np.random.default_rng(42)
+    xn = wl.round_bf16(rng.standard_normal((rows, H)).astype(np.float32))
+    F = (Hq + 2 * Hkv) * D
+    w = wl.round_bf16((rng.standard_normal((F, H)) * 0.02).astype(np.float32))
+    q = torch.empty(rows, Hq, D, dtype=torch.bfloat16, device="cuda")
+    k = torch.empty(rows, Hkv, D, dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    ws = torch.empty(bd.bd_qkv_projection_workspace(rows, H, Hq, Hkv, D), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.bd_qkv_projection(_bf(xn), _bf(w), q, k, v, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = oracle.round_bf16(xn.astype(np.float64) @ w.astype(np.float64).T)
+    absdot = np.abs(xn.astype(np.float64)) @ np.abs(w.astype(np.float64)).T
+    got = np.concatenate([t.float().cpu().numpy().reshape(rows, -1) for t in (q, k, v)], axis=1)
+    _close_bf16(got, ref, absdot)
+
+
+@pytest.mark.parametrize("rows,Fin,H", [(256, 2048, 2048), (100, 2048, 2048), (33, 256, 384)])
+def test_out_projection_residual_matches_oracle(rows, Fin, H):
+    rng = np.random.default_rng(43)
+    a = wl.round_bf16(rng.standard_normal((rows, Fin)).astype(np.float32))
+    w = wl.round_bf16((rng.standard_normal((H, Fin)) * 0.02).astype(np.float32))
+    x0 = rng.standard_normal((rows, H)).astype(np.float32)
+    x = torch.from_numpy(x0).cuda()
+    xn = torch.empty(rows, H, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(bd.bd_out_projection_workspace(rows, Fin, H), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.bd_out_projection_residual(_bf(a), _bf(w), x, xn, ws, 1e-6, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = x0.astype(np.float64) + a.astype(np.float64) @ w.astype(np.float64).T
+    got = x.cpu().numpy()
+    assert np.abs(got - ref).max() <= 1e-4 * max(1.0, np.abs(ref).max())
+    _close_bf16(xn.float().cpu().numpy(), oracle.round_bf16(oracle.rms_norm(got)))
+
+
+def _stack_setup(w, plen, seed=0):
+    """Device copies of a workload's decoder inputs plus a per-layer paged cache."""
+    cap = np.asarray(plen) + w.block_len
+    table, npg = wl.page_tables(w, cap, seed)
+    caches, host = [], []
+    for l in range(w.num_layers):
+        c = PagedCache(max(npg, 1), w.num_kv_heads, w.head_dim, torch.bfloat16, table)
+        kv = []
+        for b in range(w.batch):
+            k, v = wl.prefix_kv(w, b, int(plen[b]), seed, layer=l)
+            c.load_prefix(b, torch.from_numpy(k), torch.from_numpy(v))
+            kv.append((k, v))
+        caches.append(c)
+        host.append(kv)
+    E = wl.embed_table(w, seed)
+    em = wl.mask_embedding(w, seed)
+    lw = [wl.layer_weights(w, l, seed) for l in range(w.num_layers)]
+    ctx = torch.from_numpy(np.asarray(plen, np.int32)).cuda()
+    stack = DecoderStack(_bf(E), _bf(em), [(_bf(a), _bf(b)) for a, b in lw], caches, ctx,
+                         batch=w.batch, block_len=w.block_len, num_q_heads=w.num_q_heads,
+                         max_ctx=int(cap.max()))
+    return stack, E, em, lw, host
+
+
+DEC = wl.WORKLOADS["longctx_b8"].with_(name="dec_small", batch=3, vocab=1000, num_layers=3,
+                                       prefix=300, prefix_min=0)
+
+
+def test_decoder_stack_matches_oracle():
+    w = DEC
+    plen = [0, 77, 300]
+    stack, E, em, lw, host = _stack_setup(w, plen)
+    rng = np.random.default_rng(44)
+    tok = rng.integers(0, w.vocab, (w.batch, w.block_len)).astype(np.int32)
+    tok[rng.random(tok.shape) < 0.6] = -1
+    stack.forward(torch.from_numpy(tok).cuda())
+    torch.cuda.synchronize()
+    assert int(stack.dev_status.item()) == 0
+    x = stack.x.cpu().numpy().reshape(w.batch, w.block_len, -1)
+    ks = stack.k.float().cpu().numpy()
+    worst = mean = scale = 0.0
+    for b in range(w.batch):
+        caches = [(host[l][b][0], host[l][b][1]) for l in range(w.num_layers)]
+        rx, rk, rv = oracle.decoder_forward(tok[b], E, em, lw, caches, w.num_q_heads,
+                                            w.num_kv_heads)
+        err = float(np.abs(x[b] - rx).max())
+        worst = max(worst, err)
+        mean += float(np.abs(x[b] - rx).mean()) / w.batch
+        scale = max(scale, float(np.abs(rx).max()))
+        assert err <= 2e-2, f"sequence {b}: residual stream error {err}"
+        assert np.abs(ks[0, b] - rk[0]).max() <= 2e-2
+    print(f"\ndecoder stack: max |dx| {worst:.2e}, mean |dx| {mean:.2e}, max |x| {scale:.2f}")
+
+
+def test_decoder_append_all_layers():
+    w = DEC.with_(num_layers=2)
+    plen = [5, 64, 130]
+    stack, E, em, lw, host = _stack_setup(w, plen)
+    tok = np.arange(w.batch * w.block_len, dtype=np.int32).reshape(w.batch, w.block_len) % w.vocab
+    stack.forward(torch.from_numpy(tok).cuda())
+    n_masked = torch.tensor([0, 3, 0], dtype=torch.int32, device="cuda")   # sequence 1 not done
+    stack.append(n_masked)
+    torch.cuda.synchronize()
+    assert int(stack.dev_status.item()) == 0
+    assert stack.ctx_len.cpu().tolist() == [5 + 32, 64, 130 + 32]
+    kb, vb = stack.k.cpu(), stack.v.cpu()
+    for l in range(w.num_layers):
+        c = stack.caches[l]
+        pool_k = c.k.cpu().float().numpy()
+        pool_v = c.v.cpu().float().numpy()
+        for b in range(w.batch):
+            n = int(stack.ctx_len[b].item())
+            got_k = oracle.paged_read(pool_k, c.page_table_np[b], n, bd.BD_PAGE_SIZE)
+            got_v = oracle.paged_read(pool_v, c.page_table_np[b], n, bd.BD_PAGE_SIZE)
+            exp_k = host[l][b][0]
+            exp_v = host[l][b][1]
+            if b != 1:
+                exp_k = np.concatenate([exp_k, kb[l, b].float().numpy()])
+                exp_v = np.concatenate([exp_v, vb[l, b].float().numpy()])
+            assert np.array_equal(got_k, exp_k) and np.array_equal(got_v, exp_v)
