@@ -64,6 +64,11 @@ def _args():
                     help="launch every kernel from the host instead of replaying CUDA graphs")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="workload name (the headline line uses sdar_b1)")
+    ap.add_argument("--kernel", default=None, choices=["lmhead", "attention"],
+                    help="time one call alone (per-call us, GB/s, TFLOP/s) instead of decoding")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="--kernel lmhead: masked rows of the call (default: all of the workload's)")
+    ap.add_argument("--iters", type=int, default=20, help="--kernel: timed calls")
     return ap.parse_args()
 
 
@@ -890,8 +895,101 @@ def run_decoder(a):
     print(json.dumps(line))
 
 
+def run_kernel(a):
+    """One library call timed alone: the LM head + confidence/commit call at a
+    given number of masked rows, or the block attention at a workload's prefix
+    lengths.  Inputs are seeded synthetic tensors of the workload's shapes;
+    a 256 MB buffer is rewritten between calls so no call starts with the
+    previous call's data in L2."""
+    import torch
+    from block_diffusion_decoding_denoise_gb300 import bd, build
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    from block_diffusion_decoding_denoise_gb300.engine import PagedCache
+    if not os.path.exists(bd.LIB_PATH):
+        build.build()
+    bd.load()
+    w = wl.WORKLOADS[a.workload]
+    g = torch.Generator(device="cuda").manual_seed(0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L, H, V = w.block_len, w.hidden, w.vocab
+    if a.kernel == "lmhead":
+        rows = a.rows or w.batch * L
+        B = (rows + L - 1) // L
+        W = torch.from_numpy(wl.lm_head(w)).to("cuda", torch.bfloat16)
+        h = torch.randn(B, L, H, device="cuda", generator=g).to(torch.bfloat16)
+        ws = torch.empty(bd.bd_confidence_commit_workspace(bd.BD_BF16, B, L, H, V),
+                         dtype=torch.uint8, device="cuda")
+        tok = torch.empty(B, L, dtype=torch.int32, device="cuda")
+        pm = torch.empty(B, L, device="cuda")
+        am = torch.empty_like(tok)
+        nc = torch.empty(B, dtype=torch.int32, device="cuda")
+        nm = torch.empty_like(nc)
+
+        def call():
+            tok.fill_(7)
+            tok.view(-1)[:rows] = -1
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            bd.bd_confidence_commit(h, W, w.threshold, tok, pm, am, nc, nm, ws, dev_status=st)
+            e1.record()
+            return e0, e1
+        flops = 2.0 * rows * H * V
+        byts = V * H * 2 + rows * H * 2
+        what = f"bd_confidence_commit, {rows} masked rows, LM head {V}x{H}"
+    else:
+        plen = wl.prefix_lengths(w)
+        table, npg = wl.page_tables(w, plen + L)
+        cache = PagedCache(npg, w.num_kv_heads, w.head_dim, torch.bfloat16, table)
+        cache.k.normal_(generator=g)
+        cache.v.normal_(generator=g)
+        ctx = torch.from_numpy(plen.astype(np.int32)).cuda()
+        q = torch.randn(w.batch, L, w.num_q_heads, w.head_dim, device="cuda",
+                        generator=g).to(torch.bfloat16)
+        kb = torch.randn(w.batch, L, w.num_kv_heads, w.head_dim, device="cuda",
+                         generator=g).to(torch.bfloat16)
+        vb = torch.randn(kb.shape, device="cuda", generator=g).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        mc = int(plen.max()) + L
+        ws = torch.empty(max(1, bd.bd_block_attention_workspace(
+            w.batch, L, w.num_q_heads, w.num_kv_heads, w.head_dim, mc)), dtype=torch.uint8,
+            device="cuda")
+
+        def call():
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            bd.bd_block_attention(cache.kv, ctx, None, q, kb, vb, out, ws, mc, dev_status=st)
+            e1.record()
+            return e0, e1
+        nk = int(plen.sum()) + w.batch * L
+        byts = 2 * nk * w.num_kv_heads * w.head_dim * 2 + 2 * w.batch * L * w.num_q_heads * w.head_dim * 2
+        flops = 4.0 * nk * L * w.num_q_heads * w.head_dim
+        what = f"bd_block_attention, {w.name} prefixes (sum {int(plen.sum())}, max {int(plen.max())})"
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(a.iters):
+        e0, e1 = call()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    if int(st.item()) != 0:
+        raise SystemExit(f"device status {bd.STATUS.get(int(st.item()))}")
+    us = statistics.median(ts)
+    peak, kind = _peaks()
+    print(json.dumps({"kernel": a.kernel, "call": what, "us_median": us, "us_min": min(ts),
+                      "gb_s": byts / us / 1e3, "hbm_frac": byts / us / 1e3 / peak,
+                      "tflop_s": flops / us / 1e6, "iters": a.iters,
+                      "peak_source": f"{kind} hbm_gbs"}))
+
+
 def main():
     a = _args()
+    if a.kernel:
+        run_kernel(a)
+        return
     if a.impl == "reference":
         run_reference(a)
     elif a.sweep:

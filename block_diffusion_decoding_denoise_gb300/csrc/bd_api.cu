@@ -53,25 +53,36 @@ static int num_sms() {
   return cached;
 }
 
-// KV split (page-aligned slices of the keys).  Small problems (at most about
-// 8 pages per SM in all) get one work item per SM, so every SM streams a few
-// pages at once; larger ones get about four items per SM, each at least 8
-// pages long, so the persistent kernel balances ragged sequences.
+// KV split of the fp32 and tcgen05 kernels (page-aligned slices of the keys).
+// Small problems (at most about 8 pages per SM in all) get one work item per
+// SM, so every SM streams a few pages at once; larger ones get about four
+// items per SM, each at least 8 pages long.  (The bf16 mma.sync kernel
+// partitions the tiles itself, see attn_plan_kernel.)
+// At most about 8 pages per SM in all.
+static bool attn_small(int batch, int hkv, int block_len, int max_ctx) {
+  const long long pages =
+      (long long)batch * hkv * ((max_ctx + block_len + BD_PAGE_SIZE - 1) / BD_PAGE_SIZE);
+  return pages <= 8LL * num_sms();
+}
+
 static void choose_split(int batch, int hkv, int block_len, int max_ctx, int *num_splits,
                          int *split_keys) {
   const int sms = num_sms();
   const int nkeys = max_ctx + block_len;
   const int heads = batch * hkv;
   const long long pages = (long long)heads * ((nkeys + BD_PAGE_SIZE - 1) / BD_PAGE_SIZE);
-  int s;
+  int keys;
   if (pages <= 8LL * sms) {
-    s = std::max(1, (sms + heads - 1) / heads);
+    // small problem: about one item per SM
+    int s = std::max(1, (sms + heads - 1) / heads);
+    s = std::min(s, std::max(1, (nkeys + BD_PAGE_SIZE - 1) / BD_PAGE_SIZE));
+    keys = (nkeys + s - 1) / s;
   } else {
-    s = std::max(1, (4 * sms + heads - 1) / heads);
+    // large problem: about four items per SM, each at least 8 pages long
+    int s = std::max(1, (4 * sms + heads - 1) / heads);
     s = std::min(s, std::max(1, nkeys / (8 * BD_PAGE_SIZE)));
+    keys = (nkeys + s - 1) / s;
   }
-  s = std::min(s, std::max(1, (nkeys + BD_PAGE_SIZE - 1) / BD_PAGE_SIZE));
-  int keys = (nkeys + s - 1) / s;
   keys = (keys + BD_PAGE_SIZE - 1) / BD_PAGE_SIZE * BD_PAGE_SIZE;
   *split_keys = keys;
   *num_splits = (nkeys + keys - 1) / keys;
@@ -84,6 +95,16 @@ static bool attn_shape_ok(int32_t batch, int32_t block_len, int32_t hq, int32_t 
   if (block_len * (hq / hkv) > 128) return false;
   if (max_ctx < 0 || (int64_t)max_ctx + block_len > (1 << 30)) return false;
   return true;
+}
+
+// Workspace of the tile-range partition (bf16 mma.sync kernel): the plan,
+// then partial O and (m, l) for batch * hkv + grid slots.
+static size_t attn_sk_bytes(int batch, int block_len, int hq, int hkv, int d, int grid,
+                            size_t *off_o, size_t *off_ml) {
+  const size_t rows = ((size_t)batch * hkv + grid) * block_len * (hq / hkv);
+  *off_o = align_up((2 * (size_t)batch + 1) * sizeof(int), 256);
+  *off_ml = *off_o + align_up(rows * d * sizeof(float), 256);
+  return *off_ml + align_up(rows * 2 * sizeof(float), 256);
 }
 
 static size_t attn_ws_bytes(int batch, int block_len, int hq, int hkv, int d, int max_ctx,
@@ -161,9 +182,11 @@ BD_API size_t bd_block_attention_workspace(int32_t batch, int32_t block_len, int
   if (!attn_shape_ok(batch, block_len, num_q_heads, num_kv_heads, head_dim, max_ctx)) return 0;
   preload_all();
   int ns, sk;
-  size_t off_ml;
-  return attn_ws_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim, max_ctx, &ns, &sk,
-                       &off_ml);
+  size_t off_ml, so, sm;
+  return std::max(attn_ws_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim, max_ctx,
+                                &ns, &sk, &off_ml),
+                  attn_sk_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim, num_sms(),
+                                &so, &sm));
 }
 
 BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_len,
@@ -199,13 +222,27 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
   p.tokens = tokens;
   p.out = out;
   p.dev_status = dev_status;
-  size_t off_ml;
-  const size_t need = attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx,
-                                    &p.num_splits, &p.split_keys, &off_ml);
-  if (need > 0) {
-    if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return BD_ERR_WORKSPACE;
-    p.part_o = static_cast<float *>(ws);
-    p.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + off_ml);
+  size_t off_ml, sk_o, sk_ml;
+  p.grid = num_sms();
+  const size_t need = std::max(
+      attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx, &p.num_splits,
+                    &p.split_keys, &off_ml),
+      attn_sk_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, p.grid, &sk_o, &sk_ml));
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return BD_ERR_WORKSPACE;
+  // the split partials and the partition's buffers share the workspace (one
+  // scheme runs per call)
+  p.part_o = static_cast<float *>(ws);
+  p.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + off_ml);
+  if (attn_small(batch, p.hkv, block_len, max_ctx)) {
+    // fixed splits: the mma.sync kernel writes its partials where the
+    // split combine reads them
+    p.plan = nullptr;
+    p.sk_o = p.part_o;
+    p.sk_ml = p.part_ml;
+  } else {
+    p.plan = static_cast<int *>(ws);
+    p.sk_o = reinterpret_cast<float *>(static_cast<char *>(ws) + sk_o);
+    p.sk_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + sk_ml);
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // Kernel choice: the persistent mma.sync kernel for bf16 (measured faster

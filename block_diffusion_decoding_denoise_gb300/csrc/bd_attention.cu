@@ -197,7 +197,76 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p) {
   for (int j = 0; j < DPL; ++j) out[j] = from_f32<T>(acc[j] * inv);
 }
 
+// Merge the pieces of every segment cut by the tile-range partition of the
+// bf16 mma.sync kernel; same arithmetic as attn_combine_kernel, slots
+// segment + CTA for the CTAs between those holding the segment's first and
+// last tiles (skipping CTAs with an empty range).  A segment inside one CTA
+// was written by that CTA directly.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) attn_combine_sk_kernel(AttnParams p) {
+  constexpr int DPL = D / 32;
+  const int group = p.hq / p.hkv;
+  const int R = p.block_len * group;
+  const int wid = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
+  if (wid >= p.batch * p.hkv * R) return;
+  const int r = wid % R, g = (wid / R) % p.hkv, b = wid / (R * p.hkv);
+  const int total = p.plan[2 * p.batch];
+  const int tiles = p.plan[2 * b + 1];
+  if (tiles <= 0 || total <= 0) return;
+  const long long seg0 = (long long)p.plan[2 * b] + (long long)g * tiles;
+  const int c0 = sk_cta_of(seg0, total, p.grid), c1 = sk_cta_of(seg0 + tiles - 1, total, p.grid);
+  if (c0 == c1) return;
+  // CTAs c0..c1 hold the segment's pieces, except those whose tile range is
+  // empty (when there are more CTAs than tiles)
+  const size_t seg = (size_t)b * p.hkv + g;
+  auto holds = [&](int c) {
+    return ((long long)c * total) / p.grid < ((long long)(c + 1) * total) / p.grid;
+  };
+  float m = -INFINITY;
+  for (int c = c0 + lane; c <= c1; c += 32)
+    if (holds(c)) m = fmaxf(m, __ldcg(&p.sk_ml[((seg + c) * R + r) * 2]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float l = 0.f, acc[DPL];
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
+  for (int c = c0; c <= c1; ++c) {
+    if (!holds(c)) continue;
+    const size_t pr = (seg + c) * R + r;
+    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.sk_ml + pr * 2));
+    const float w = __expf(ml.x - m);
+    l = fmaf(ml.y, w, l);
+    const float *src = p.sk_o + pr * D + lane * DPL;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) acc[j] = fmaf(__ldcg(src + j), w, acc[j]);
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const int i = r / group, h = g * group + r % group;
+  T *out = static_cast<T *>(p.out) + (((size_t)b * p.block_len + i) * p.hq + h) * D + lane * DPL;
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) out[j] = from_f32<T>(acc[j] * inv);
+}
+
 bd_status attention_combine(const AttnParams &p, cudaStream_t st);
+
+template <typename T, int D>
+static bd_status launch_combine_sk(const AttnParams &p, cudaStream_t st) {
+  const int R = p.block_len * (p.hq / p.hkv);
+  const size_t warps = (size_t)p.batch * p.hkv * R;
+  const int blocks = (int)((warps + 7) / 8);
+  const cudaError_t e =
+      launch_pdl(attn_combine_sk_kernel<T, D>, dim3(blocks), dim3(256), 0, st, p);
+  count_launches(1);
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
+
+bd_status attention_combine_sk(const AttnParams &p, cudaStream_t st) {
+  return p.head_dim == 64 ? launch_combine_sk<__nv_bfloat16, 64>(p, st)
+                          : launch_combine_sk<__nv_bfloat16, 128>(p, st);
+}
 
 template <typename T, int D>
 static bd_status launch_simt(const AttnParams &p, cudaStream_t st) {
@@ -237,7 +306,9 @@ bool preload_attention_simt() {
          preload_kernel(attn_combine_kernel<float, 64>, false) &&
          preload_kernel(attn_combine_kernel<float, 128>, false) &&
          preload_kernel(attn_combine_kernel<__nv_bfloat16, 64>, false) &&
-         preload_kernel(attn_combine_kernel<__nv_bfloat16, 128>, false);
+         preload_kernel(attn_combine_kernel<__nv_bfloat16, 128>, false) &&
+         preload_kernel(attn_combine_sk_kernel<__nv_bfloat16, 64>, false) &&
+         preload_kernel(attn_combine_sk_kernel<__nv_bfloat16, 128>, false);
 }
 
 bd_status attention_simt(const AttnParams &p, cudaStream_t st) {

@@ -1,11 +1,21 @@
 // bf16 block attention on the tensor cores, K/V pages streamed by TMA.
 //
-// Same contract and split as attention_simt (see bd_attention.cu): CTA =
-// (KV split, KV head g, sequence b) over the R = block_len * (Hq/Hkv) query
-// rows that read KV head g, key positions [split * split_keys, ...) of
-// [cache | block] ("Rethinking Document OCR as Inverse Rendering via Diffusion
+// Same contract as attention_simt (see bd_attention.cu): the R = block_len *
+// (Hq/Hkv) query rows that read KV head g attend to the keys of [cache |
+// block] ("Rethinking Document OCR as Inverse Rendering via Diffusion
 // Decoding", paper.rainbus.top summary, method step 3: bidirectional inside
 // the block, causal to every earlier block and the prefix).
+//
+// Work partition (large problems): the keys of (sequence b, KV head g) form
+// a segment of tiles (one per cached 64-token page, then one for the block's
+// own keys); attn_plan_kernel lays the segments end to end and every CTA
+// takes an equal contiguous range of tiles, so ragged batches cost no
+// balance.  Small problems (a few pages per SM) skip the plan launch and deal
+// fixed KV splits round-robin instead, which starts streaming sooner.  A segment
+// inside one CTA's range is written as the final output; a segment cut by
+// range boundaries leaves one partial per piece (slot = segment + CTA, which
+// is unique because pieces are ordered along the tile line) for
+// attn_combine_sk_kernel.
 //
 // The cached keys arrive one 64-token page at a time: a 4-D TMA map over the
 // pool [page][Hkv][64][D] fetches the page's [64][D] slab of head g (two
@@ -72,6 +82,14 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// 2^x by the SFU's approximation (relative error about 2^-22; exact 0 for
+// -inf), which is ample for probabilities that are rounded to bf16 next.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
@@ -85,22 +103,83 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 // Per-stage description written by the producer before it arms the stage.
 struct TileMeta {
-  int item;   // work item = (sequence, KV head, split)
+  int item;   // segment = sequence * Hkv + KV head
   int lo, hi; // valid key rows [lo, hi) of the tile
   int flags;  // kFirst | kLast | kSkip | kEnd
+  int slot;   // partial slot of this piece, -1 when the piece is the whole segment
 };
+
+// Tile plan: tiles_b = ceil(ctx_b / 64) + 1 (0 for a sequence with no masked
+// position or an invalid context) and base_b = Hkv * sum_{b' < b} tiles_b';
+// plan[2b] = base_b, plan[2b + 1] = tiles_b, plan[2 batch] = the total T.
+// One CTA; a block-wide scan per 1024 sequences.
+__global__ void __launch_bounds__(1024) attn_plan_kernel(AttnParams p) {
+  __shared__ int warp_sum[32];
+  __shared__ int carry;
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int b0 = 0; b0 < p.batch; b0 += blockDim.x) {
+    const int b = b0 + threadIdx.x;
+    int tiles = 0;
+    if (b < p.batch) {
+      bool active = true;
+      if (p.tokens) {
+        active = false;
+        const int32_t *t = p.tokens + (size_t)b * p.block_len;
+        for (int i = 0; i < p.block_len; ++i) active |= t[i] == BD_MASK;
+      }
+      const int ctx = p.ctx_len[b];
+      if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) {
+        if (active) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+        active = false;
+      }
+      tiles = active ? (ctx + kPageRows - 1) / kPageRows + 1 : 0;
+    }
+    const int v = tiles * p.hkv;
+    int inc = v;                                 // inclusive scan inside the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += u;
+    }
+    if (lane == 31) warp_sum[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < (int)(blockDim.x >> 5) ? warp_sum[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += u;
+      }
+      warp_sum[lane] = w;                        // inclusive over warps
+    }
+    __syncthreads();
+    const int excl = carry + (warp > 0 ? warp_sum[warp - 1] : 0) + inc - v;
+    if (b < p.batch) {
+      p.plan[2 * b] = excl;
+      p.plan[2 * b + 1] = tiles;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) carry += warp_sum[31];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.plan[2 * p.batch] = carry;
+}
 constexpr int kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8;
 constexpr int kMaxStages = 12;
 
 // Persistent, warp-specialised block attention.
-//   warp 0        producer: walks this CTA's work items (item = blockIdx.x +
-//                 i * gridDim.x over (sequence, KV head, split)), and for each
-//                 tile (one cached page, or the block's own keys) arms a ring
-//                 stage with the tile's TMA loads and a TileMeta record
-//   warps 1..NW   consumers: warp w owns query rows [16(w-1), 16w) of the
-//                 item; it runs Q K^T, the online softmax and P V on each
-//                 stage, releases the stage, and writes the item's output (or
-//                 its split partial) after the item's last tile
+//   warp 0        producer: walks this CTA's tile range of the plan, and for
+//                 each tile (one cached page, or the block's own keys) arms a
+//                 ring stage with the tile's TMA loads and a TileMeta record
+//   warps 1..NW   consumers: a row group of 16 query rows (and, with KH = 2,
+//                 one half of every tile's keys) per warp; Q K^T, the online
+//                 softmax and P V on each stage, release of the stage, and
+//                 after a piece's last tile the output (whole segment) or the
+//                 piece's partial
 // A sentinel stage (kEnd) tells the consumers that the producer is done.
 template <int D, int RG, int KH>
 __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
@@ -126,7 +205,6 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
   const int R = p.block_len * group;
   const int L = p.block_len;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nitems = p.batch * p.hkv * p.num_splits;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -165,68 +243,118 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
       s_out = s;
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
-    for (int item = blockIdx.x; item < nitems && !stop; item += gridDim.x) {
-      const int split = item % p.num_splits;
-      const int g = (item / p.num_splits) % p.hkv;
-      const int b = item / (p.num_splits * p.hkv);
-      if (p.tokens && !block_has_mask(p.tokens + (size_t)b * L, L)) continue;
-      const int ctx = p.ctx_len[b];
-      if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) {
-        if (split == 0 && g == 0 && lane == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
-        continue;
-      }
-      const int kbeg = split * p.split_keys;
-      const int kend = min(ctx + L, kbeg + p.split_keys);
-      if (kbeg >= kend) continue;              // no key of this sequence in this split
-      const int p_first = kbeg / kPageRows;
-      const int p_end = kbeg < ctx ? (min(kend, ctx) + kPageRows - 1) / kPageRows : p_first;
-      const int npg = p_end - p_first;
-      const int ntiles = npg + (kend > ctx ? 1 : 0);
-      for (int u = 0; u < ntiles; ++u, ++it) {
-        uint32_t s;
-        if (!acquire(s)) {
-          stop = true;
-          break;
-        }
-        if (lane == 0) {
-          const uint32_t bar = smem_u32(&full[s]);
-          uint8_t *bk = smem + (size_t)s * 2 * TILE, *bv = bk + TILE;
-          TileMeta m;
-          m.item = item;
-          m.flags = (u == 0 ? kFirst : 0) | (u == ntiles - 1 ? kLast : 0);
-          if (u < npg) {
-            const int pg = p.page_table[(size_t)b * p.max_pages + p_first + u];
-            m.lo = 0;
-            m.hi = min(kPageRows, ctx - (p_first + u) * kPageRows);
-            if (pg >= 0 && pg < p.num_pages) {
-              meta[s] = m;
-              fence_proxy_async();
-              mbar_arrive_expect_tx(bar, 2 * TILE);
-#pragma unroll
-              for (int h = 0; h < NH; ++h) {
-                tma_load_4d(smem_u32(bk + h * kHalfBytes), &mk_pool, 64 * h, 0, g, pg, bar);
-                tma_load_4d(smem_u32(bv + h * kHalfBytes), &mv_pool, 64 * h, 0, g, pg, bar);
-              }
-            } else {
-              flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
-              m.flags |= kSkip;
-              meta[s] = m;
-              mbar_arrive(bar);
-            }
-          } else {
-            m.lo = max(kbeg, ctx) - ctx;
-            m.hi = kend - ctx;
+    // Arm one tile of segment (b, g): the cached page u (keys [64u, 64u + 64)
+    // of the sequence, valid up to ctx) or, for u == npg, the block's own keys
+    // [klo, khi) (relative to ctx).  Lane 0 issues; returns false on abort.
+    auto arm = [&](int b, int g, int u, int npg, int ctx, int klo, int khi, int seg, int slot,
+                   int flags) -> bool {
+      uint32_t s;
+      if (!acquire(s)) return false;
+      if (lane == 0) {
+        const uint32_t bar = smem_u32(&full[s]);
+        uint8_t *bk = smem + (size_t)s * 2 * TILE, *bv = bk + TILE;
+        TileMeta m;
+        m.item = seg;
+        m.slot = slot;
+        m.flags = flags;
+        if (u < npg) {
+          const int pg = p.page_table[(size_t)b * p.max_pages + u];
+          m.lo = 0;
+          m.hi = min(kPageRows, ctx - u * kPageRows);
+          if (pg >= 0 && pg < p.num_pages) {
             meta[s] = m;
             fence_proxy_async();
-            mbar_arrive_expect_tx(bar, 2 * NH * L * 128);
+            mbar_arrive_expect_tx(bar, 2 * TILE);
 #pragma unroll
             for (int h = 0; h < NH; ++h) {
-              tma_load_4d(smem_u32(bk + h * kHalfBytes), &mk_blk, 64 * h, g, 0, b, bar);
-              tma_load_4d(smem_u32(bv + h * kHalfBytes), &mv_blk, 64 * h, g, 0, b, bar);
+              tma_load_4d(smem_u32(bk + h * kHalfBytes), &mk_pool, 64 * h, 0, g, pg, bar);
+              tma_load_4d(smem_u32(bv + h * kHalfBytes), &mv_pool, 64 * h, 0, g, pg, bar);
             }
+          } else {
+            flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+            m.flags |= kSkip;
+            meta[s] = m;
+            mbar_arrive(bar);
+          }
+        } else {
+          m.lo = klo;
+          m.hi = khi;
+          meta[s] = m;
+          fence_proxy_async();
+          mbar_arrive_expect_tx(bar, 2 * NH * L * 128);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            tma_load_4d(smem_u32(bk + h * kHalfBytes), &mk_blk, 64 * h, g, 0, b, bar);
+            tma_load_4d(smem_u32(bv + h * kHalfBytes), &mv_blk, 64 * h, g, 0, b, bar);
           }
         }
-        __syncwarp();
+      }
+      __syncwarp();
+      ++it;
+      return true;
+    };
+    if (p.plan) {
+      // tile-range partition: this CTA's tiles [t_begin, t_end) of the plan's T
+      const int T = p.plan[2 * p.batch];
+      const int c = blockIdx.x, G = gridDim.x;
+      const int t_begin = (int)(((long long)c * T) / G);
+      const int t_end = (int)(((long long)(c + 1) * T) / G);
+      int b = 0;
+      {                                          // last sequence with base <= t_begin
+        int lo = 0, hi = p.batch - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (p.plan[2 * mid] <= t_begin) lo = mid;
+          else hi = mid - 1;
+        }
+        b = lo;
+      }
+      for (int t = t_begin; t < t_end && !stop;) {
+        while (b < p.batch - 1 && t >= p.plan[2 * b] + p.hkv * p.plan[2 * b + 1]) ++b;
+        const int base = p.plan[2 * b], tiles = p.plan[2 * b + 1];
+        if (tiles <= 0 || t < base || t >= base + p.hkv * tiles) {   // inconsistent plan
+          if (lane == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+          break;
+        }
+        const int g = (t - base) / tiles, u0 = (t - base) % tiles;
+        const int seg0 = base + g * tiles;
+        const int u1 = min(seg0 + tiles, t_end) - seg0;
+        const int seg = b * p.hkv + g;
+        const int slot = (u0 == 0 && u1 == tiles) ? -1 : seg + c;
+        const int ctx = p.ctx_len[b];
+        for (int u = u0; u < u1 && !stop; ++u)
+          stop = !arm(b, g, u, tiles - 1, ctx, 0, L, seg, slot,
+                      (u == u0 ? kFirst : 0) | (u == u1 - 1 ? kLast : 0));
+        t = seg0 + u1;
+      }
+    } else {
+      // KV splits (small problems): items (sequence, KV head, split) dealt
+      // round-robin; split s covers keys [s * split_keys, (s + 1) * split_keys)
+      const int nitems = p.batch * p.hkv * p.num_splits;
+      for (int item = blockIdx.x; item < nitems && !stop; item += gridDim.x) {
+        const int split = item % p.num_splits;
+        const int g = (item / p.num_splits) % p.hkv;
+        const int b = item / (p.num_splits * p.hkv);
+        if (p.tokens && !block_has_mask(p.tokens + (size_t)b * L, L)) continue;
+        const int ctx = p.ctx_len[b];
+        if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) {
+          if (split == 0 && g == 0 && lane == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+          continue;
+        }
+        const int kbeg = split * p.split_keys;
+        const int kend = min(ctx + L, kbeg + p.split_keys);
+        if (kbeg >= kend) continue;              // no key of this sequence in this split
+        const int p_first = kbeg / kPageRows;
+        const int npg = (ctx + kPageRows - 1) / kPageRows;
+        const int p_end = kbeg < ctx ? (min(kend, ctx) + kPageRows - 1) / kPageRows : p_first;
+        const int ntiles = (p_end - p_first) + (kend > ctx ? 1 : 0);
+        const int seg = b * p.hkv + g;
+        const int slot = p.num_splits == 1 ? -1 : seg * p.num_splits + split;
+        for (int k = 0; k < ntiles && !stop; ++k) {
+          const int u = p_first + k < p_end ? p_first + k : npg;
+          stop = !arm(b, g, u, npg, ctx, max(kbeg, ctx) - ctx, kend - ctx, seg, slot,
+                      (k == 0 ? kFirst : 0) | (k == ntiles - 1 ? kLast : 0));
+        }
       }
     }
     // sentinel: tells the consumers there is no more work
@@ -234,7 +362,7 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
       uint32_t s;
       if (acquire(s)) {
         if (lane == 0) {
-          meta[s] = TileMeta{-1, 0, 0, kEnd};
+          meta[s] = TileMeta{-1, 0, 0, kEnd, -1};
           mbar_arrive(smem_u32(&full[s]));
         }
         ++it;
@@ -260,7 +388,7 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
     uint32_t qa[KSTEPS][4];
     float o[DN][4];
     float m_run[2], l_run[2];
-    int b = 0, g = 0, split = 0;
+    int b = 0, g = 0;
     for (uint32_t it = 0;; ++it) {
       const uint32_t s = it % S;
       int ok = 1;
@@ -279,12 +407,12 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
         m.lo = mv[1];
         m.hi = mv[2];
         m.flags = mv[3];
+        m.slot = mv[4];
       }
       if (m.flags & kEnd) break;
       if (m.flags & kFirst) {
-        split = m.item % p.num_splits;
-        g = (m.item / p.num_splits) % p.hkv;
-        b = m.item / (p.num_splits * p.hkv);
+        g = m.item % p.hkv;
+        b = m.item / p.hkv;
         const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
         const int r_lo = rg * 16 + gid, r_hi = r_lo + 8;
         const __nv_bfloat16 *q_lo = nullptr, *q_hi = nullptr;
@@ -339,38 +467,46 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
           }
         }
         float mt[2] = {-INFINITY, -INFINITY};
+        if (w_lo != key0 || w_hi != key0 + 8 * KJ) {   // partial tile: mask the invalid keys
 #pragma unroll
-        for (int j = 0; j < KJ; ++j) {
+          for (int j = 0; j < KJ; ++j)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int key = key0 + 8 * j + tig * 2 + (e & 1);
-            if (key < w_lo || key >= w_hi) sc[j][e] = -INFINITY;
-            mt[e >> 1] = fmaxf(mt[e >> 1], sc[j][e]);
-          }
+            for (int e = 0; e < 4; ++e) {
+              const int key = key0 + 8 * j + tig * 2 + (e & 1);
+              if (key < w_lo || key >= w_hi) sc[j][e] = -INFINITY;
+            }
         }
+#pragma unroll
+        for (int j = 0; j < KJ; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) mt[e >> 1] = fmaxf(mt[e >> 1], sc[j][e]);
         float corr[2], mneg[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], 1));
           mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], 2));
           const float mnew = fmaxf(m_run[i], mt[i]);
-          corr[i] = exp2f((m_run[i] - mnew) * sl2);
+          corr[i] = fast_exp2((m_run[i] - mnew) * sl2);
           m_run[i] = mnew;
           mneg[i] = -mnew * sl2;
           l_run[i] *= corr[i];
         }
+        // rescale only when some running max of the warp moved (a factor of
+        // exactly 1 changes nothing, and after the first tiles most do not move)
+        if (!__all_sync(0xffffffffu, corr[0] == 1.f && corr[1] == 1.f)) {
 #pragma unroll
-        for (int j = 0; j < DN; ++j) {
-          o[j][0] *= corr[0];
-          o[j][1] *= corr[0];
-          o[j][2] *= corr[1];
-          o[j][3] *= corr[1];
+          for (int j = 0; j < DN; ++j) {
+            o[j][0] *= corr[0];
+            o[j][1] *= corr[0];
+            o[j][2] *= corr[1];
+            o[j][3] *= corr[1];
+          }
         }
 #pragma unroll
         for (int j = 0; j < KJ; ++j) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            sc[j][e] = exp2f(fmaf(sc[j][e], sl2, mneg[e >> 1]));
+            sc[j][e] = fast_exp2(fmaf(sc[j][e], sl2, mneg[e >> 1]));
             l_run[e >> 1] += sc[j][e];
           }
         }
@@ -447,7 +583,7 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
             const int r = rg * 16 + gid + 8 * i;
             if (r >= R) continue;
             const int qi = r / group, h = g * group + r % group;
-            if (p.num_splits == 1) {
+            if (m.slot < 0) {
               const float inv = lsum[i] > 0.f ? 1.f / lsum[i] : 0.f;
               __nv_bfloat16 *out =
                   static_cast<__nv_bfloat16 *>(p.out) + (((size_t)b * L + qi) * p.hq + h) * D;
@@ -456,14 +592,14 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
                 *reinterpret_cast<uint32_t *>(out + 8 * j + tig * 2) =
                     pack_bf16(o[j][2 * i] * inv, o[j][2 * i + 1] * inv);
             } else {
-              const size_t prow = (((size_t)b * p.hkv + g) * p.num_splits + split) * R + r;
+              const size_t prow = (size_t)m.slot * R + r;
 #pragma unroll
               for (int j = 0; j < DN; ++j)
-                *reinterpret_cast<float2 *>(p.part_o + prow * D + 8 * j + tig * 2) =
+                *reinterpret_cast<float2 *>(p.sk_o + prow * D + 8 * j + tig * 2) =
                     make_float2(o[j][2 * i], o[j][2 * i + 1]);
               if (tig == 0) {
-                p.part_ml[prow * 2 + 0] = m_run[i] * p.scale;   // natural-log units
-                p.part_ml[prow * 2 + 1] = lsum[i];
+                p.sk_ml[prow * 2 + 0] = m_run[i] * p.scale;     // natural-log units
+                p.sk_ml[prow * 2 + 1] = lsum[i];
               }
             }
           }
@@ -502,8 +638,14 @@ bd_status launch(const AttnParams &p, cudaStream_t st) {
                                       (200 * 1024 - ctrl - kXchgBytes) / (2 * TILE));
   const size_t smem = (size_t)S * 2 * TILE + kXchgBytes + ctrl + 1024;
   auto kern = attn_tc_kernel<D, RG, KH>;
-  const int nitems = p.batch * p.hkv * p.num_splits;
-  const int grid = std::max(1, std::min(nitems, std::max(dev_info().sms, 1)));
+  int grid = p.grid;
+  if (p.plan) {
+    const cudaError_t e = launch_pdl(attn_plan_kernel, dim3(1), dim3(1024), 0, st, p);
+    count_launches(1);
+    if (e != cudaSuccess) return BD_ERR_CUDA;
+  } else {
+    grid = std::max(1, std::min(p.batch * p.hkv * p.num_splits, p.grid));
+  }
   const cudaError_t e =
       launch_pdl(kern, dim3(grid), dim3((NW + 1) * 32), smem, st, mkp, mvp, mkb, mvb, p, S);
   count_launches(1);
@@ -513,7 +655,7 @@ bd_status launch(const AttnParams &p, cudaStream_t st) {
 }  // namespace
 
 bool preload_attention_tc() {
-  return preload_kernel(attn_tc_kernel<64, 4, 2>, true) &&
+  return preload_kernel(attn_plan_kernel, false) && preload_kernel(attn_tc_kernel<64, 4, 2>, true) &&
          preload_kernel(attn_tc_kernel<64, 8, 1>, true) &&
          preload_kernel(attn_tc_kernel<128, 4, 2>, true) &&
          preload_kernel(attn_tc_kernel<128, 8, 1>, true);
@@ -524,6 +666,10 @@ bd_status attention_tc(const AttnParams &p, cudaStream_t st) {
   if (p.page_size != kPageRows || p.block_len > 32) return BD_ERR_UNSUPPORTED;
   if (p.block_len * (p.hq / p.hkv) > 128) return BD_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(p.q) & 3) != 0) return BD_ERR_UNSUPPORTED;
+  if (p.grid < 1 || ((p.plan || p.num_splits > 1) && (!p.sk_o || !p.sk_ml)))
+    return BD_ERR_UNSUPPORTED;
+  if (p.plan && (long long)p.batch * p.hkv * (p.max_pages + 1) >= (1LL << 30))
+    return BD_ERR_UNSUPPORTED;
   const DevInfo d = dev_info();
   if (d.major < 10 || !tma_available()) return BD_ERR_UNSUPPORTED;
   const int R = p.block_len * (p.hq / p.hkv);
@@ -533,8 +679,9 @@ bd_status attention_tc(const AttnParams &p, cudaStream_t st) {
     s = R <= 64 ? launch<64, 4, 2>(p, st) : launch<64, 8, 1>(p, st);
   else
     s = R <= 64 ? launch<128, 4, 2>(p, st) : launch<128, 8, 1>(p, st);
-  if (s != BD_OK || p.num_splits == 1) return s;
-  return attention_combine(p, st);
+  if (s != BD_OK) return s;
+  if (p.plan) return attention_combine_sk(p, st);
+  return p.num_splits > 1 ? attention_combine(p, st) : BD_OK;
 }
 
 }  // namespace bd
