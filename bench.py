@@ -64,7 +64,7 @@ def _args():
                     help="launch every kernel from the host instead of replaying CUDA graphs")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="workload name (the headline line uses sdar_b1)")
-    ap.add_argument("--kernel", default=None, choices=["lmhead", "attention"],
+    ap.add_argument("--kernel", default=None, choices=["lmhead", "attention", "proj"],
                     help="time one call alone (per-call us, GB/s, TFLOP/s) instead of decoding")
     ap.add_argument("--rows", type=int, default=None,
                     help="--kernel lmhead: masked rows of the call (default: all of the workload's)")
@@ -938,6 +938,35 @@ def run_kernel(a):
         flops = 2.0 * rows * H * V
         byts = V * H * 2 + rows * H * 2
         what = f"bd_confidence_commit, {rows} masked rows, LM head {V}x{H}"
+    elif a.kernel == "proj":
+        # the decoder's QKV projection and output projection + residual + RMSNorm
+        # of one layer over the workload's block rows
+        rows = a.rows or w.batch * L
+        Fq = (w.num_q_heads + 2 * w.num_kv_heads) * w.head_dim
+        Fi = w.num_q_heads * w.head_dim
+        wqkv, wo = (torch.from_numpy(x).to("cuda", torch.bfloat16) for x in wl.layer_weights(w, 0))
+        xn = torch.randn(rows, H, device="cuda", generator=g).to(torch.bfloat16)
+        att = torch.randn(rows, Fi, device="cuda", generator=g).to(torch.bfloat16)
+        x = torch.randn(rows, H, device="cuda", generator=g)
+        q = torch.empty(rows, w.num_q_heads, w.head_dim, dtype=torch.bfloat16, device="cuda")
+        k = torch.empty(rows, w.num_kv_heads, w.head_dim, dtype=torch.bfloat16, device="cuda")
+        v = torch.empty_like(k)
+        ws = torch.empty(max(bd.bd_qkv_projection_workspace(rows, H, w.num_q_heads,
+                                                            w.num_kv_heads, w.head_dim),
+                             bd.bd_out_projection_workspace(rows, Fi, H)),
+                         dtype=torch.uint8, device="cuda")
+
+        def call():
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            bd.bd_qkv_projection(xn, wqkv, q, k, v, ws, dev_status=st)
+            bd.bd_out_projection_residual(att, wo, x, xn, ws, dev_status=st)
+            e1.record()
+            return e0, e1
+        flops = 2.0 * rows * H * (Fq + Fi)
+        byts = (Fq + H) * H * 2 + rows * (H + Fi) * 2 + rows * (Fq + H) * 2 + rows * H * 8
+        what = f"bd_qkv_projection + bd_out_projection_residual, {rows} rows, {Fq}x{H} + {H}x{Fi}"
     else:
         plen = wl.prefix_lengths(w)
         table, npg = wl.page_tables(w, plen + L)
