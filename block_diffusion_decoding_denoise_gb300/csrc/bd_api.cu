@@ -31,7 +31,7 @@ bool preload_all() {
   if (done[dev]) return true;
   const bool ok = preload_kernel(append_kv_kernel, false) && preload_attention_simt() &&
                   preload_attention_tc() && preload_attention_tc5() && preload_confidence() &&
-                  preload_lmhead_tc() && preload_decoder();
+                  preload_lmhead_tc() && preload_decoder() && preload_attention_pair();
   if (!ok) {
     cudaGetLastError();
     return false;
@@ -101,7 +101,9 @@ static bool attn_shape_ok(int32_t batch, int32_t block_len, int32_t hq, int32_t 
 // then partial O and (m, l) for batch * hkv + grid slots.
 static size_t attn_sk_bytes(int batch, int block_len, int hq, int hkv, int d, int grid,
                             size_t *off_o, size_t *off_ml) {
-  const size_t rows = ((size_t)batch * hkv + grid) * block_len * (hq / hkv);
+  // slots: batch * hkv + grid of R rows (one KV head per segment); the
+  // head-pair kernel needs batch * hkv / 2 + grid slots of 2R rows, fewer
+  const size_t rows = ((size_t)batch * hkv + 2 * (size_t)grid) * block_len * (hq / hkv);
   *off_o = align_up((2 * (size_t)batch + 1) * sizeof(int), 256);
   *off_ml = *off_o + align_up(rows * d * sizeof(float), 256);
   return *off_ml + align_up(rows * 2 * sizeof(float), 256);
@@ -224,6 +226,7 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
   p.dev_status = dev_status;
   size_t off_ml, sk_o, sk_ml;
   p.grid = num_sms();
+  p.seg_heads = 1;
   const size_t need = std::max(
       attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx, &p.num_splits,
                     &p.split_keys, &off_ml),
@@ -233,7 +236,14 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
   // scheme runs per call)
   p.part_o = static_cast<float *>(ws);
   p.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + off_ml);
-  if (attn_small(batch, p.hkv, block_len, max_ctx)) {
+  // Kernel choice: BD_ATTENTION (pair | tc5 | mma | simt) forces one kernel,
+  // for testing and measurement; the head-pair kernel always partitions tiles
+  const char *env = getenv("BD_ATTENTION");
+  const bool force5 = env && !strcmp(env, "tc5");
+  const bool force_simt = env && !strcmp(env, "simt");
+  const bool force_pair = env && !strcmp(env, "pair");
+  const bool force_mma = env && !strcmp(env, "mma");
+  if (attn_small(batch, p.hkv, block_len, max_ctx) && !force_pair) {
     // fixed splits: the mma.sync kernel writes its partials where the
     // split combine reads them
     p.plan = nullptr;
@@ -245,13 +255,14 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
     p.sk_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + sk_ml);
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // Kernel choice: the persistent mma.sync kernel for bf16 (measured faster
-  // than the tcgen05 kernel at every batch size so far), SIMT for fp32.
-  // BD_ATTENTION (tc5 | mma | simt) forces one kernel, for testing and
-  // measurement.
-  const char *env = getenv("BD_ATTENTION");
-  const bool force5 = env && !strcmp(env, "tc5");
-  const bool force_simt = env && !strcmp(env, "simt");
+  // Default: for bf16 at head_dim 128 and 64 query rows per KV head (the SDAR
+  // shapes), the tcgen05 head-pair kernel on large problems and the mma.sync
+  // kernel with fixed splits on small ones (a few pages per SM, where its
+  // shorter start wins); the mma.sync kernel for other bf16 shapes; SIMT for
+  // fp32.
+  if ((force_pair || (!force5 && !force_simt && !force_mma)) && p.plan &&
+      attention_pair_supported(p))
+    return attention_pair(p, st);
   if (force5 && attention_tc5_supported(p)) {
     const bd_status s = attention_tc5(p, st);
     if (s != BD_OK || p.num_splits == 1) return s;

@@ -213,21 +213,24 @@ __global__ void __launch_bounds__(256) attn_combine_sk_kernel(AttnParams p) {
   pdl_wait();
   if (wid >= p.batch * p.hkv * R) return;
   const int r = wid % R, g = (wid / R) % p.hkv, b = wid / (R * p.hkv);
+  const int HS = p.seg_heads;                  // KV heads per segment
   const int total = p.plan[2 * p.batch];
   const int tiles = p.plan[2 * b + 1];
   if (tiles <= 0 || total <= 0) return;
-  const long long seg0 = (long long)p.plan[2 * b] + (long long)g * tiles;
+  const long long seg0 = (long long)p.plan[2 * b] + (long long)(g / HS) * tiles;
   const int c0 = sk_cta_of(seg0, total, p.grid), c1 = sk_cta_of(seg0 + tiles - 1, total, p.grid);
   if (c0 == c1) return;
   // CTAs c0..c1 hold the segment's pieces, except those whose tile range is
-  // empty (when there are more CTAs than tiles)
-  const size_t seg = (size_t)b * p.hkv + g;
+  // empty (when there are more CTAs than tiles); a slot holds HS * R rows
+  const size_t seg = (size_t)b * (p.hkv / HS) + g / HS;
+  const size_t srows = (size_t)HS * R;
+  const size_t rin = (size_t)(g % HS) * R + r;
   auto holds = [&](int c) {
     return ((long long)c * total) / p.grid < ((long long)(c + 1) * total) / p.grid;
   };
   float m = -INFINITY;
   for (int c = c0 + lane; c <= c1; c += 32)
-    if (holds(c)) m = fmaxf(m, __ldcg(&p.sk_ml[((seg + c) * R + r) * 2]));
+    if (holds(c)) m = fmaxf(m, __ldcg(&p.sk_ml[((seg + c) * srows + rin) * 2]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float l = 0.f, acc[DPL];
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(256) attn_combine_sk_kernel(AttnParams p) {
   for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
   for (int c = c0; c <= c1; ++c) {
     if (!holds(c)) continue;
-    const size_t pr = (seg + c) * R + r;
+    const size_t pr = (seg + c) * srows + rin;
     const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.sk_ml + pr * 2));
     const float w = __expf(ml.x - m);
     l = fmaf(ml.y, w, l);

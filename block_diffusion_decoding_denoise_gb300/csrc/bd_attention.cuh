@@ -27,6 +27,7 @@ struct AttnParams {
   // [c T / grid, (c+1) T / grid) of the concatenated segments; a piece of
   // segment s computed by CTA c writes partial slot s + c
   int grid;
+  int seg_heads;   // KV heads per segment: 1 (mma.sync kernel) or 2 (head-pair kernel)
   int *plan;       // [2 batch + 1]: base_b, tiles_b per sequence, then T
   float *sk_o;     // [batch * hkv + grid][R][head_dim]
   float *sk_ml;    // [batch * hkv + grid][R][2]
@@ -42,6 +43,9 @@ bd_status attention_tc(const AttnParams &p, cudaStream_t st);
 bd_status attention_combine(const AttnParams &p, cudaStream_t st);
 bd_status attention_combine_sk(const AttnParams &p, cudaStream_t st);
 bool attention_tc5_supported(const AttnParams &p);
+bool attention_pair_supported(const AttnParams &p);
+bd_status attention_pair(const AttnParams &p, cudaStream_t st);
+cudaError_t attention_plan_launch(const AttnParams &p, cudaStream_t st);
 bd_status attention_tc5(const AttnParams &p, cudaStream_t st);
 
 }  // namespace bd

@@ -1,0 +1,648 @@
+// bf16 block attention on the 5th-generation tensor cores, two KV heads per
+// tile so that the MMA's M dimension is 128 query rows.
+//
+// Same contract as the other attention kernels: the R = block_len * (Hq/Hkv)
+// query rows of KV head g attend to head g's keys of [cache | block]
+// ("Rethinking Document OCR as Inverse Rendering via Diffusion Decoding",
+// paper.rainbus.top summary, method step 3).  Used for head_dim 128 and
+// R = 64, the SDAR shapes (32-token blocks, two query heads per KV head).
+//
+// A tile is one 64-token page (or the block's own keys) of the KV heads
+// 2p and 2p + 1.  Rows 0..63 of every operand belong to head 2p, rows
+// 64..127 to head 2p + 1:
+//   MMA1  S[row][key]  = Q[row][:] . K[key][:]     M = 128 rows, N = 128 keys, K = D
+//   softmax (one thread per query row, no shuffles): the row's 64 keys of its
+//         own head, running max kept in base-2 units and moved only when a new
+//         maximum exceeds it by more than 8 (then O's row is rescaled in
+//         TMEM), P = exp2(s - m) as bf16 written to TMEM (the thread's own
+//         lane); the other head's 64 keys of P stay zero
+//   MMA2  O[row][d]   += P[row][key] . V[key][d]    M = 128, N = D, K = 128 keys
+//         (P read from TMEM, V from shared memory MN-major); O stays in TMEM
+//         for the whole piece
+// The off-diagonal halves of MMA1 and MMA2 are wasted work; the tensor pipe
+// has several times the throughput this HBM-bound loop needs.
+//
+// Work partition: the tile-range plan of attn_plan_kernel over (sequence,
+// KV-head pair) segments; a segment inside one CTA's range is written as the
+// final output, a cut one leaves a partial per piece in slot segment + CTA
+// (merged by attn_combine_sk_kernel).
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0     TMA producer: Q of each piece, K and V of each tile (three stages)
+//   warp 1     TMEM allocator and MMA issuer: MMA1 of tile t, then MMA2 of
+//              tile t - 1 (the softmax of t overlaps MMA2 of t - 1)
+//   warps 2-5  softmax, O rescale and the output of each piece
+// Every wait is bounded; on expiry the kernel records BD_ERR_TIMEOUT, stops
+// issuing, waits (bounded) for its copies and MMAs, frees TMEM and returns.
+#include <math.h>
+
+#include <algorithm>
+
+#include "bd_attention.cuh"
+#include "bd_common.cuh"
+#include "bd_sm100.cuh"
+
+namespace bd {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int D = 128;
+constexpr int kRows = 128;                  // 2 heads x 64 query rows
+constexpr int kPage = 64;
+constexpr int kHalf = 128 * 128;            // 128 rows x 64 columns of bf16: 16 KB
+constexpr int kHeadOff = 64 * 128;          // rows of the second head: +8 KB
+constexpr int kThreads = 192;
+constexpr int kStages = 3;
+constexpr uint32_t kTmemCols = 512;         // S x2 (128 cols each), O (128), P x2 (64 each)
+constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = 384;             // P buffer b at kColP + 64 b: 128 keys as bf16 pairs
+constexpr float kLazy = 8.f;                // max moves only beyond 2^8
+constexpr int kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8;
+
+struct Meta {
+  int item, lo, hi, flags, slot;
+};
+
+struct Smem {
+  uint8_t q[2][kHalf];                      // two 64-column halves of D
+  uint8_t k[kStages][2][kHalf];             // [stage][half]
+  uint8_t v[kStages][2][kHalf];
+  Meta meta[kStages];
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t q_full, q_empty;
+  uint64_t s_full[2], s_empty[2], p_full[2];
+  uint64_t o_done, o_empty;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// MN-major operand in the 128-byte-swizzled layout a TMA load of [key][64 d]
+// boxes writes: 128-byte rows of 64 consecutive d for one key, 8-key groups
+// 1024 B apart, the next 64 d one half (16 KB) further.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(kHalf >> 4) << 16;        // leading byte offset: next 64 along N (d)
+  d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset: next 8 along K (keys)
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulator; A is M
+// rows (one per TMEM lane) of K bf16 values packed two per 32-bit column.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_pair_kernel(const __grid_constant__ CUtensorMap mk_pool,
+                     const __grid_constant__ CUtensorMap mv_pool,
+                     const __grid_constant__ CUtensorMap mk_blk,
+                     const __grid_constant__ CUtensorMap mv_blk,
+                     const __grid_constant__ CUtensorMap mq, const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int group = p.hq / p.hkv;
+  const int L = p.block_len;
+  const int npairs = p.hkv / 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sm.kv_full[s]), 1);
+      mbar_init(smem_u32(&sm.kv_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&sm.s_full[s]), 1);
+      mbar_init(smem_u32(&sm.s_empty[s]), 4);
+      mbar_init(smem_u32(&sm.p_full[s]), 4);
+    }
+    mbar_init(smem_u32(&sm.q_full), 1);
+    mbar_init(smem_u32(&sm.q_empty), 1);
+    mbar_init(smem_u32(&sm.o_done), 1);
+    mbar_init(smem_u32(&sm.o_empty), 4);
+    mbar_init(smem_u32(&sm.mma_done), 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mk_pool);
+    tma_prefetch_desc(&mv_pool);
+    tma_prefetch_desc(&mk_blk);
+    tma_prefetch_desc(&mv_blk);
+    tma_prefetch_desc(&mq);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  // finite contents everywhere a masked key can reach MMA2 (P = 0 times a V
+  // row that no TMA load has written yet must not be 0 * NaN)
+  {
+    int4 *z = reinterpret_cast<int4 *>(&sm.k[0][0][0]);
+    const int n = (int)((sizeof(sm.k) + sizeof(sm.v)) / sizeof(int4));
+    for (int i = threadIdx.x; i < n; i += blockDim.x) z[i] = make_int4(0, 0, 0, 0);
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  pdl_trigger();
+  pdl_wait();
+
+  auto fail = [&]() {
+    sm.abort_flag = 1;
+    flag_error(p.dev_status, BD_ERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0, pc = 0;
+    bool stop = false;
+    if (lane == 0) {
+      const int T = p.plan[2 * p.batch];
+      const int c = blockIdx.x, G = gridDim.x;
+      const int t_begin = (int)(((long long)c * T) / G);
+      const int t_end = (int)(((long long)(c + 1) * T) / G);
+      int b = 0;
+      {                                        // last sequence with base <= t_begin
+        int lo = 0, hi = p.batch - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (p.plan[2 * mid] <= t_begin) lo = mid;
+          else hi = mid - 1;
+        }
+        b = lo;
+      }
+      for (int t = t_begin; t < t_end && !stop;) {
+        while (b < p.batch - 1 && t >= p.plan[2 * b] + npairs * p.plan[2 * b + 1]) ++b;
+        const int base = p.plan[2 * b], tiles = p.plan[2 * b + 1];
+        if (tiles <= 0 || t < base || t >= base + npairs * tiles) {
+          flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+          break;
+        }
+        const int hp = (t - base) / tiles, u0 = (t - base) % tiles;
+        const int seg0 = base + hp * tiles;
+        const int u1 = min(seg0 + tiles, t_end) - seg0;
+        const int seg = b * npairs + hp;
+        const int slot = (u0 == 0 && u1 == tiles) ? -1 : seg + c;
+        const int ctx = p.ctx_len[b];
+        const int npg = tiles - 1;
+        // Q of both heads: rows i * group + j of head 2hp, then of head 2hp + 1
+        if (pc > 0 && !mbar_wait(smem_u32(&sm.q_empty), (pc - 1) & 1)) {
+          fail();
+          stop = true;
+          break;
+        }
+        {
+          const uint32_t bar = smem_u32(&sm.q_full);
+          mbar_arrive_expect_tx(bar, 2 * 2 * L * group * 128);
+          for (int hs = 0; hs < 2; ++hs)
+            for (int h = 0; h < 2; ++h)
+              tma_load_4d(smem_u32(sm.q[h] + hs * kHeadOff), &mq, 64 * h,
+                          (2 * hp + hs) * group, 0, b, bar);
+        }
+        ++pc;
+        for (int u = u0; u < u1; ++u, ++it) {
+          const uint32_t s = it % kStages, round = it / kStages;
+          if (sm.abort_flag) {
+            stop = true;
+            break;
+          }
+          if (round > 0 && !mbar_wait(smem_u32(&sm.kv_empty[s]), (round - 1) & 1)) {
+            fail();
+            stop = true;
+            break;
+          }
+          const uint32_t bar = smem_u32(&sm.kv_full[s]);
+          Meta m;
+          m.item = seg;
+          m.slot = slot;
+          m.lo = 0;
+          m.flags = (u == u0 ? kFirst : 0) | (u == u1 - 1 ? kLast : 0);
+          if (u < npg) {
+            const int pg = p.page_table[(size_t)b * p.max_pages + u];
+            m.hi = min(kPage, ctx - u * kPage);
+            if (pg >= 0 && pg < p.num_pages) {
+              sm.meta[s] = m;
+              fence_proxy_async();
+              mbar_arrive_expect_tx(bar, 2 * 2 * 2 * kPage * 128);
+              for (int hs = 0; hs < 2; ++hs)
+                for (int h = 0; h < 2; ++h) {
+                  tma_load_4d(smem_u32(sm.k[s][h] + hs * kHeadOff), &mk_pool, 64 * h, 0,
+                              2 * hp + hs, pg, bar);
+                  tma_load_4d(smem_u32(sm.v[s][h] + hs * kHeadOff), &mv_pool, 64 * h, 0,
+                              2 * hp + hs, pg, bar);
+                }
+            } else {
+              flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+              m.flags |= kSkip;
+              m.hi = 0;
+              sm.meta[s] = m;
+              mbar_arrive(bar);
+            }
+          } else {
+            m.hi = L;
+            sm.meta[s] = m;
+            fence_proxy_async();
+            mbar_arrive_expect_tx(bar, 2 * 2 * 2 * L * 128);
+            for (int hs = 0; hs < 2; ++hs)
+              for (int h = 0; h < 2; ++h) {
+                tma_load_4d(smem_u32(sm.k[s][h] + hs * kHeadOff), &mk_blk, 64 * h,
+                            2 * hp + hs, 0, b, bar);
+                tma_load_4d(smem_u32(sm.v[s][h] + hs * kHeadOff), &mv_blk, 64 * h,
+                            2 * hp + hs, 0, b, bar);
+              }
+          }
+        }
+        t = seg0 + u1;
+      }
+      if (!stop) {                             // sentinel stage: no more work
+        const uint32_t s = it % kStages, round = it / kStages;
+        if (round > 0 && !mbar_wait(smem_u32(&sm.kv_empty[s]), (round - 1) & 1)) {
+          fail();
+        } else {
+          sm.meta[s] = Meta{-1, 0, 0, kEnd, -1};
+          mbar_arrive(smem_u32(&sm.kv_full[s]));
+          ++it;
+        }
+      }
+      if (sm.abort_flag) {                     // wait (bounded) for copies in flight
+        const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0;
+        for (uint32_t i = first; i < it; ++i)
+          mbar_wait(smem_u32(&sm.kv_full[i % kStages]), (i / kStages) & 1);
+        if (pc > 0) mbar_wait(smem_u32(&sm.q_full), (pc - 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc1 = idesc_bf16_f32(kRows, kRows);
+      const uint32_t idesc2 = idesc_bf16_f32(kRows, D) | (1u << 16);   // B (V) MN-major
+      uint32_t pc = 0;                         // pieces whose Q was consumed
+      // pending MMA2: tile index, its meta, whether it starts a piece, piece index
+      bool have_prev = false, prev_first = false, prev_skip = false, o_init = false;
+      uint32_t prev_t = 0, prev_piece = 0;
+      auto mma2 = [&](uint32_t tp, bool first, bool skip, uint32_t piece) -> bool {
+        if (!mbar_wait(smem_u32(&sm.p_full[tp & 1]), (tp >> 1) & 1)) return false;
+        if (first) {
+          if (piece > 0 && !mbar_wait(smem_u32(&sm.o_empty), (piece - 1) & 1)) return false;
+          o_init = false;
+        }
+        tc_fence_after();
+        if (!skip) {
+          const uint32_t pt = tmem + kColP + 64 * (tp & 1);
+          const uint32_t vb = smem_u32(sm.v[tp % kStages][0]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)           // 16 keys = 8 TMEM columns per step
+            mma_bf16_ts(tmem + kColO, pt + 8 * j, sw128_mnmajor_desc(vb + j * 2048), idesc2,
+                        (o_init || j > 0) ? 1u : 0u);
+          o_init = true;
+        }
+        mma_commit(smem_u32(&sm.kv_empty[tp % kStages]));
+        mma_commit(smem_u32(&sm.o_done));
+        return true;
+      };
+      bool ok = true;
+      for (uint32_t t = 0; ok; ++t) {
+        const uint32_t st = t % kStages, s = t & 1;   // K/V stage, S buffer
+        if (sm.abort_flag || !mbar_wait(smem_u32(&sm.kv_full[st]), (t / kStages) & 1)) {
+          ok = false;
+          break;
+        }
+        const volatile int *mv = reinterpret_cast<const volatile int *>(&sm.meta[st]);
+        const int flags = mv[3];
+        if (flags & kEnd) {
+          if (have_prev && !mma2(prev_t, prev_first, prev_skip, prev_piece)) ok = false;
+          mma_commit(smem_u32(&sm.s_full[s]));   // tells the softmax warps to stop
+          break;
+        }
+        const bool first = (flags & kFirst) != 0, skip = (flags & kSkip) != 0;
+        if (first && !mbar_wait(smem_u32(&sm.q_full), pc & 1)) {
+          ok = false;
+          break;
+        }
+        if (t >= 2 && !mbar_wait(smem_u32(&sm.s_empty[s]), ((t >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (!skip) {
+          const uint32_t qa = smem_u32(sm.q[0]);
+          const uint32_t kb = smem_u32(sm.k[st][0]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            mma_bf16(tmem + s * 128, sw128_kmajor_desc(qa + (j >> 2) * kHalf + (j & 3) * 32),
+                     sw128_kmajor_desc(kb + (j >> 2) * kHalf + (j & 3) * 32), idesc1,
+                     j > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&sm.s_full[s]));
+        const uint32_t piece = first ? pc : (pc > 0 ? pc - 1 : 0);
+        if (flags & kLast) {
+          mma_commit(smem_u32(&sm.q_empty));     // Q free once this MMA1 is done
+        }
+        if (first) ++pc;
+        if (have_prev && !mma2(prev_t, prev_first, prev_skip, prev_piece)) {
+          ok = false;
+          break;
+        }
+        have_prev = true;
+        prev_t = t;
+        prev_first = first;
+        prev_skip = skip;
+        prev_piece = piece;
+      }
+      if (!ok) fail();
+      // every MMA issued above has completed once mma_done fires
+      mma_commit(smem_u32(&sm.mma_done));
+      mbar_wait(smem_u32(&sm.mma_done), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int q = warp & 3;                    // TMEM lane quarter of this warp
+    const int row = 32 * q + lane;             // query row of the tile (0..127)
+    const int hs = row >> 6;                   // which head of the pair
+    const int rr = row & 63;                   // row within its head: i * group + j
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+    const float sl2 = p.scale * 1.4426950408889634f;
+    float m2 = -INFINITY, l = 0.f;
+    uint32_t o_seen = 0;                       // o_done phases consumed
+    {                                          // the other head's keys of P stay zero
+      uint32_t z[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) z[j] = 0u;
+#pragma unroll
+      for (int b2 = 0; b2 < 2; ++b2)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tmem_st_32x32b_x16(lane_base + kColP + 64 * b2 + 32 * (1 - hs) + 16 * c, z);
+      tmem_st_wait();
+    }
+    bool ok = true;
+    auto wait_o = [&](uint32_t tile) -> bool {   // MMA2 of `tile` has completed
+      int w = 1;
+      if (lane == 0) w = mbar_wait(smem_u32(&sm.o_done), tile & 1) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, w, 0) != 0;
+    };
+    for (uint32_t t = 0;; ++t) {
+      const uint32_t s = t & 1;
+      int w = 1;
+      if (lane == 0) w = mbar_wait(smem_u32(&sm.s_full[s]), (t >> 1) & 1) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, w, 0)) {
+        ok = false;
+        break;
+      }
+      Meta m;
+      {
+        const volatile int *mv = reinterpret_cast<const volatile int *>(&sm.meta[t % kStages]);
+        m.item = mv[0];
+        m.lo = mv[1];
+        m.hi = mv[2];
+        m.flags = mv[3];
+        m.slot = mv[4];
+      }
+      if (m.flags & kEnd) break;
+      if (m.flags & kFirst) {
+        m2 = -INFINITY;
+        l = 0.f;
+      }
+      tc_fence_after();
+      // this row's 64 scores (its own head's keys of the tile)
+      float sc[64];
+      {
+        uint32_t r[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld_32x32b_x16(lane_base + s * 128 + hs * 64 + c * 16, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) sc[c * 16 + j] = __uint_as_float(r[j]) * sl2;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.s_empty[s]));
+      const int hi = (m.flags & kSkip) ? 0 : m.hi;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        if (j < hi) mt = fmaxf(mt, sc[j]);
+      float factor = 1.f;
+      if (mt > m2) {
+        if (m2 == -INFINITY) {
+          m2 = mt;                             // first keys of the piece: O not yet written
+        } else if (mt > m2 + kLazy) {
+          factor = fast_exp2(m2 - mt);
+          l *= factor;
+          m2 = mt;
+        }
+      }
+      // P row as bf16 pairs (its own head's 64 keys = 32 TMEM columns)
+      uint32_t pw[32];
+      {
+        float sum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int j0 = 2 * e, j1 = j0 + 1;
+          const float p0 = j0 < hi ? fast_exp2(sc[j0] - m2) : 0.f;
+          const float p1 = j1 < hi ? fast_exp2(sc[j1] - m2) : 0.f;
+          sum += p0 + p1;
+          pw[e] = pack_bf16(p0, p1);
+        }
+        l += sum;
+      }
+      // MMA2 of the previous tile has to be complete before O is rescaled and
+      // before this tile's P overwrites the buffer MMA2 of tile t - 2 read
+      if (t >= 1 && o_seen < t) {
+        if (!wait_o(t - 1)) {
+          ok = false;
+          break;
+        }
+        o_seen = t;
+      }
+      tc_fence_after();
+      {
+        uint32_t h16[16];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) h16[j] = pw[16 * c + j];
+          tmem_st_32x32b_x16(lane_base + kColP + 64 * s + 32 * hs + 16 * c, h16);
+        }
+      }
+      if (__any_sync(0xffffffffu, factor != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(lane_base + kColO + c * 16, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * factor);
+          tmem_st_32x32b_x16(lane_base + kColO + c * 16, r);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[s]));
+      if (m.flags & kLast) {
+        if (!wait_o(t)) {
+          ok = false;
+          break;
+        }
+        o_seen = t + 1;
+        tc_fence_after();
+        const int b = m.item / npairs, hp = m.item % npairs;
+        const int g = 2 * hp + hs;
+        const int qi = rr / group, h = g * group + rr % group;
+        if (m.slot < 0) {
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          __nv_bfloat16 *out =
+              static_cast<__nv_bfloat16 *>(p.out) + (((size_t)b * L + qi) * p.hq + h) * D;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(lane_base + kColO + c * 16, r);
+            tmem_ld_wait();
+            uint32_t w8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              w8[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+            *reinterpret_cast<uint4 *>(out + c * 16) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+            *reinterpret_cast<uint4 *>(out + c * 16 + 8) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+          }
+        } else {
+          const size_t prow = (size_t)m.slot * kRows + row;
+          float *po = p.sk_o + prow * D;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(lane_base + kColO + c * 16, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<uint4 *>(po + c * 16 + 4 * e) =
+                  make_uint4(r[4 * e], r[4 * e + 1], r[4 * e + 2], r[4 * e + 3]);
+          }
+          p.sk_ml[prow * 2 + 0] = m2 * 0.6931471805599453f;   // natural-log units
+          p.sk_ml[prow * 2 + 1] = l;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.o_empty));
+      }
+    }
+    if (!ok && lane == 0) fail();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool preload_attention_pair() { return preload_kernel(attn_pair_kernel, true); }
+
+bool attention_pair_supported(const AttnParams &p) {
+  if (p.dtype != BD_BF16 || p.head_dim != D || p.page_size != kPage) return false;
+  if (p.hkv % 2 != 0 || p.hq % p.hkv != 0) return false;
+  if (p.block_len * (p.hq / p.hkv) != 64) return false;
+  if (!p.plan || !p.sk_o || !p.sk_ml || p.grid < 1) return false;
+  if ((long long)p.batch * (p.hkv / 2) * (p.max_pages + 1) >= (1LL << 30)) return false;
+  const DevInfo d = dev_info();
+  return d.major >= 10 && tma_available();
+}
+
+bd_status attention_pair(const AttnParams &p0, cudaStream_t st) {
+  if (!attention_pair_supported(p0)) return BD_ERR_UNSUPPORTED;
+  AttnParams p = p0;
+  p.seg_heads = 2;
+  const uint64_t eb = 2;
+  const int group = p.hq / p.hkv;
+  CUtensorMap mkp, mvp, mkb, mvb, mq;
+  const uint64_t pdims[4] = {(uint64_t)D, (uint64_t)p.page_size, (uint64_t)p.hkv,
+                             (uint64_t)p.num_pages};
+  const uint64_t pstr[3] = {D * eb, (uint64_t)p.page_size * D * eb,
+                            (uint64_t)p.hkv * p.page_size * D * eb};
+  const uint32_t pbox[4] = {64, (uint32_t)p.page_size, 1, 1};
+  const uint64_t bdims[4] = {(uint64_t)D, (uint64_t)p.hkv, (uint64_t)p.block_len,
+                             (uint64_t)p.batch};
+  const uint64_t bstr[3] = {D * eb, (uint64_t)p.hkv * D * eb,
+                            (uint64_t)p.block_len * p.hkv * D * eb};
+  const uint32_t bbox[4] = {64, 1, (uint32_t)p.block_len, 1};
+  const uint64_t qdims[4] = {(uint64_t)D, (uint64_t)p.hq, (uint64_t)p.block_len,
+                             (uint64_t)p.batch};
+  const uint64_t qstr[3] = {D * eb, (uint64_t)p.hq * D * eb,
+                            (uint64_t)p.block_len * p.hq * D * eb};
+  const uint32_t qbox[4] = {64, (uint32_t)group, (uint32_t)p.block_len, 1};
+  if (!tma_encode_bf16(&mkp, 4, p.k_pool, pdims, pstr, pbox) ||
+      !tma_encode_bf16(&mvp, 4, p.v_pool, pdims, pstr, pbox) ||
+      !tma_encode_bf16(&mkb, 4, p.k_blk, bdims, bstr, bbox) ||
+      !tma_encode_bf16(&mvb, 4, p.v_blk, bdims, bstr, bbox) ||
+      !tma_encode_bf16(&mq, 4, p.q, qdims, qstr, qbox))
+    return BD_ERR_CUDA;
+  const size_t smem = sizeof(Smem) + 1024;
+  cudaError_t e = attention_plan_launch(p, st);
+  if (e != cudaSuccess) return BD_ERR_CUDA;
+  e = launch_pdl(attn_pair_kernel, dim3(p.grid), dim3(kThreads), smem, st, mkp, mvp, mkb, mvb, mq,
+                 p);
+  count_launches(1);
+  if (e != cudaSuccess) return BD_ERR_CUDA;
+  return attention_combine_sk(p, st);
+}
+
+}  // namespace bd

@@ -110,7 +110,8 @@ struct TileMeta {
 };
 
 // Tile plan: tiles_b = ceil(ctx_b / 64) + 1 (0 for a sequence with no masked
-// position or an invalid context) and base_b = Hkv * sum_{b' < b} tiles_b';
+// position or an invalid context) and base_b = (Hkv / seg_heads) *
+// sum_{b' < b} tiles_b' (segments of one or two KV heads);
 // plan[2b] = base_b, plan[2b + 1] = tiles_b, plan[2 batch] = the total T.
 // One CTA; a block-wide scan per 1024 sequences.
 __global__ void __launch_bounds__(1024) attn_plan_kernel(AttnParams p) {
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(1024) attn_plan_kernel(AttnParams p) {
       }
       tiles = active ? (ctx + kPageRows - 1) / kPageRows + 1 : 0;
     }
-    const int v = tiles * p.hkv;
+    const int v = tiles * (p.hkv / p.seg_heads);
     int inc = v;                                 // inclusive scan inside the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -640,9 +641,7 @@ bd_status launch(const AttnParams &p, cudaStream_t st) {
   auto kern = attn_tc_kernel<D, RG, KH>;
   int grid = p.grid;
   if (p.plan) {
-    const cudaError_t e = launch_pdl(attn_plan_kernel, dim3(1), dim3(1024), 0, st, p);
-    count_launches(1);
-    if (e != cudaSuccess) return BD_ERR_CUDA;
+    if (attention_plan_launch(p, st) != cudaSuccess) return BD_ERR_CUDA;
   } else {
     grid = std::max(1, std::min(p.batch * p.hkv * p.num_splits, p.grid));
   }
@@ -653,6 +652,12 @@ bd_status launch(const AttnParams &p, cudaStream_t st) {
 }
 
 }  // namespace
+
+cudaError_t attention_plan_launch(const AttnParams &p, cudaStream_t st) {
+  const cudaError_t e = launch_pdl(attn_plan_kernel, dim3(1), dim3(1024), 0, st, p);
+  count_launches(1);
+  return e;
+}
 
 bool preload_attention_tc() {
   return preload_kernel(attn_plan_kernel, false) && preload_kernel(attn_tc_kernel<64, 4, 2>, true) &&

@@ -216,6 +216,7 @@ bool preload_attention_tc5();
 bool preload_confidence();
 bool preload_lmhead_tc();
 bool preload_decoder();
+bool preload_attention_pair();
 
 inline bd_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? BD_OK : BD_ERR_CUDA;

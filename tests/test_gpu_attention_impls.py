@@ -1,8 +1,10 @@
 """Each attention kernel of the library against the oracle on the same cases.
 
-bd_block_attention runs the mma.sync kernel for bf16 and the SIMT kernel for
-fp32; the tcgen05 kernel is selectable.  BD_ATTENTION forces one kernel so
-that each is checked on small, ragged and full-size inputs.
+bd_block_attention runs the tcgen05 head-pair kernel for large bf16 problems
+at the SDAR shapes, the mma.sync kernel for the other bf16 cases and the SIMT
+kernel for fp32; each (and the older per-head tcgen05 kernel) is selectable.  BD_ATTENTION forces one kernel so that each is checked on small,
+ragged and full-size inputs (a kernel that does not support a shape falls
+back to the default one).
 """
 import os
 
@@ -30,7 +32,7 @@ def _lib():
     bd.load()
 
 
-@pytest.fixture(params=["tc5", "mma", "simt"])
+@pytest.fixture(params=["pair", "tc5", "mma", "simt"])
 def impl(request):
     old = os.environ.get("BD_ATTENTION")
     os.environ["BD_ATTENTION"] = request.param
@@ -69,3 +71,15 @@ def test_sdar_b1(impl):
 def test_block_len_8(impl):
     # 8 positions x 2 heads = 16 query rows per KV head
     _check(SMALL.with_(block_len=8), [130, 5, 64], impl)
+
+
+def test_serving_shapes_sampled(impl):
+    # 64 ragged sequences (2048..12288 cached tokens): many pieces per segment
+    # and segments inside one CTA's range; three sequences checked
+    w = wl.WORKLOADS["serving_b64"]
+    s = make_cache(w, 0)
+    q, kb, vb = wl.block_qkv(w, 0)
+    got = gpu_attention(s, q, kb, vb)
+    for b in (0, 31, 63):
+        err = float(np.abs(got[b] - oracle_attention(s, b, q, kb, vb)).max())
+        assert err <= 2e-2, f"{impl}: sequence {b} max-abs error {err}"
