@@ -80,3 +80,27 @@ def test_sample_commit_checks_arguments_on_the_host(lib):
     st = f(1, 1, 32, 2048, 1000, None, None, 0.9, 1.0, 1, None, None, None, None, None, None,
            None, 0, None, None)
     assert st == 1
+
+
+def test_decoder_calls_check_arguments_on_the_host(lib):
+    # shapes the projection kernels cannot take return a zero workspace
+    assert bd.bd_qkv_projection_workspace(256, 2048, 16, 8, 128) > 0
+    assert bd.bd_qkv_projection_workspace(256, 2000, 16, 8, 128) == 0      # hidden % 64
+    assert bd.bd_qkv_projection_workspace(256, 2048, 16, 8, 3) == 0        # features % 128
+    assert bd.bd_out_projection_workspace(256, 2048, 2048) > 0
+    assert bd.bd_out_projection_workspace(0, 2048, 2048) == 0
+    # null pointers and bad sizes are rejected before any launch
+    assert lib.bd_embed_rmsnorm(4, 2048, 100, None, None, None, 1e-6, None, None, None,
+                                None) == 1
+    assert lib.bd_embed_rmsnorm(4, 6000, 100, None, None, None, 1e-6, None, None, None,
+                                None) == 1
+    assert lib.bd_qkv_projection(256, 2048, 16, 8, 128, None, None, None, None, None, None, 0,
+                                 None, None) == 1
+    assert lib.bd_out_projection_residual(256, 2048, 2048, None, None, 1e-6, None, None, None,
+                                          0, None, None) == 1
+    kv = (bd.PagedKV * 2)(bd.PagedKV(1, 4, 64, 8, 128, 4, None, None, None),
+                          bd.PagedKV(1, 4, 64, 8, 128, 4, None, None, None))
+    assert lib.bd_append_block_kv_layers(kv, 2, 1, 32, None, None, None, None, None,
+                                         None) == 1
+    assert lib.bd_append_block_kv_layers(kv, 65, 1, 32, None, None, None, None, None,
+                                         None) == 1

@@ -187,3 +187,48 @@ def test_decoder_append_all_layers():
                 exp_k = np.concatenate([exp_k, kb[l, b].float().numpy()])
                 exp_v = np.concatenate([exp_v, vb[l, b].float().numpy()])
             assert np.array_equal(got_k, exp_k) and np.array_equal(got_v, exp_v)
+
+
+@pytest.mark.slow
+def test_longctx_full_size_sampled_sequence():
+    """The 28-layer long-context workload at full size (8 sequences, 16384
+    cached tokens per layer): one stack pass over a partly masked block,
+    sequence 3 checked against the oracle through all 28 layers (its final
+    residual stream and layer 27's block K/V)."""
+    w = wl.WORKLOADS["longctx_b8"]
+    plen = wl.prefix_lengths(w)
+    cap = plen + w.block_len
+    table, npg = wl.page_tables(w, cap)
+    caches, keep = [], []
+    for l in range(w.num_layers):
+        c = PagedCache(npg, w.num_kv_heads, w.head_dim, torch.bfloat16, table)
+        for b in range(w.batch):
+            k, v = wl.prefix_kv(w, b, int(plen[b]), 0, layer=l)
+            c.load_prefix(b, torch.from_numpy(k), torch.from_numpy(v))
+            if b == 3:
+                keep.append((k, v))
+        caches.append(c)
+    E = wl.embed_table(w)
+    em = wl.mask_embedding(w)
+    lw = [wl.layer_weights(w, l) for l in range(w.num_layers)]
+    ctx = torch.from_numpy(plen.astype(np.int32)).cuda()
+    stack = DecoderStack(_bf(E), _bf(em), [(_bf(a), _bf(b)) for a, b in lw], caches, ctx,
+                         batch=w.batch, block_len=w.block_len, num_q_heads=w.num_q_heads,
+                         max_ctx=int(cap.max()))
+    rng = np.random.default_rng(45)
+    tok = rng.integers(0, w.vocab, (w.batch, w.block_len)).astype(np.int32)
+    tok[rng.random(tok.shape) < 0.5] = -1
+    stack.forward(torch.from_numpy(tok).cuda())
+    torch.cuda.synchronize()
+    assert int(stack.dev_status.item()) == 0
+    x = stack.x.cpu().numpy().reshape(w.batch, w.block_len, -1)[3]
+    k27 = stack.k[27, 3].float().cpu().numpy()
+    rx, rk, _ = oracle.decoder_forward(tok[3], E, em, lw, keep, w.num_q_heads, w.num_kv_heads)
+    scale = float(np.abs(rx).max())
+    err = float(np.abs(x - rx).max())
+    print(f"\nlongctx 28 layers: max |dx| {err:.3e}, max |x| {scale:.2f}, "
+          f"mean |dx| {float(np.abs(x - rx).mean()):.2e}")
+    # 28 layers of bf16 activations: the residual stream is held to 2e-2 of its
+    # largest magnitude, layer 27's K to max-abs 2e-2 per element scale
+    assert err <= 2e-2 * max(1.0, scale)
+    assert float(np.abs(k27 - rk[27]).max()) <= 2e-2 * max(1.0, float(np.abs(rk[27]).max()))
