@@ -336,21 +336,24 @@ def run_cuda(a):
                 conf_ms.append(ea[1].elapsed_time(ea[2]))
                 rows_seen.append(s)
 
-    eng.step = timed_step
-
     def block():
         eng.ctx_len.copy_(ctx0)
         return eng.decode_block(hd, qd, kbd, vbd, check_every=a.check_every, graphs=use_graphs,
                                 on_chunk=on_chunk)
 
-    for _ in range(max(3, a.warmup)):     # the first block captures the graphs
-        block()
+    # warm-up of both variants (the first block of each captures its graphs):
+    # the plain step, timed for `value`, and the step with per-call events,
+    # run afterwards for the per-call rooflines (the event nodes cost a few
+    # percent of throughput, so they stay out of the timed region)
+    for variant in (timed_step, orig_step):
+        eng.step = variant
+        for _ in range(max(3, a.warmup)):
+            block()
     torch.cuda.synchronize()
     eng.check_status()
 
     # timed region (device-resident inputs)
     steps_issued = 0
-    recording[0] = True
     l0 = bd.bd_kernel_launches()
     g0 = eng.graph_kernel_launches
     if world > 1:
@@ -366,13 +369,22 @@ def run_cuda(a):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    recording[0] = False
     launches = (bd.bd_kernel_launches() - l0) + (eng.graph_kernel_launches - g0)
     ms = t0.elapsed_time(t1)
     eng.check_status()
     committed_per_block = int((eng.tokens != -1).sum().item())
     tokens_total = committed_per_block * a.steps
     steps_per_seq = eng.steps_per_sequence()
+
+    # per-call durations: the same blocks again with CUDA events around each call
+    eng.step = timed_step
+    recording[0] = True
+    for _ in range(min(a.steps, 20)):
+        block()
+    torch.cuda.synchronize()
+    recording[0] = False
+    eng.step = orig_step
+    eng.check_status()
     if world > 1:
         t = torch.tensor([ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -413,7 +425,6 @@ def run_cuda(a):
 
     e2e = None
     if not a.no_e2e:
-        eng.step = orig_step
         e2e = _e2e(a, eng, w, h, q, kb, vb, hd, qd, kbd, vbd, ctx0, stream, committed_per_block,
                    world, use_graphs)
     if rank != 0:
@@ -430,7 +441,10 @@ def run_cuda(a):
                               "denoise_steps_issued": steps_issued // a.steps,
                               "check_every": a.check_every, "cuda_graphs": use_graphs,
                               "decoding": ("greedy" if a.temperature is None
-                                           else f"sampled, temperature {a.temperature}")}),
+                                           else f"sampled, temperature {a.temperature}"),
+                              "per_call_timing": f"CUDA events around every call in "
+                                                 f"{min(a.steps, 20)} further blocks after the "
+                                                 f"timed region (event nodes slow the graphs)"}),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches), "clocks": clk.summary(),
         "conf_call_us_mean": 1e3 * statistics.mean(conf_ms) if conf_ms else None,

@@ -65,11 +65,12 @@ static bool attn_small(int batch, int hkv, int block_len, int max_ctx) {
   return pages <= 8LL * num_sms();
 }
 
-static void choose_split(int batch, int hkv, int block_len, int max_ctx, int *num_splits,
+// `heads` counts the segments that are split: KV heads of all sequences, or
+// head pairs for the head-pair kernel.
+static void choose_split(int heads, int block_len, int max_ctx, int *num_splits,
                          int *split_keys) {
   const int sms = num_sms();
   const int nkeys = max_ctx + block_len;
-  const int heads = batch * hkv;
   const long long pages = (long long)heads * ((nkeys + BD_PAGE_SIZE - 1) / BD_PAGE_SIZE);
   int keys;
   if (pages <= 8LL * sms) {
@@ -109,9 +110,11 @@ static size_t attn_sk_bytes(int batch, int block_len, int hq, int hkv, int d, in
   return *off_ml + align_up(rows * 2 * sizeof(float), 256);
 }
 
+// Workspace of the fixed KV splits: partial O and (m, l) per (segment, split,
+// query row); a segment is `seg_heads` KV heads of one sequence.
 static size_t attn_ws_bytes(int batch, int block_len, int hq, int hkv, int d, int max_ctx,
-                            int *num_splits, int *split_keys, size_t *off_ml) {
-  choose_split(batch, hkv, block_len, max_ctx, num_splits, split_keys);
+                            int seg_heads, int *num_splits, int *split_keys, size_t *off_ml) {
+  choose_split(batch * (hkv / seg_heads), block_len, max_ctx, num_splits, split_keys);
   if (*num_splits == 1) {
     *off_ml = 0;
     return 0;
@@ -185,10 +188,14 @@ BD_API size_t bd_block_attention_workspace(int32_t batch, int32_t block_len, int
   preload_all();
   int ns, sk;
   size_t off_ml, so, sm;
-  return std::max(attn_ws_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim, max_ctx,
-                                &ns, &sk, &off_ml),
-                  attn_sk_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim, num_sms(),
-                                &so, &sm));
+  size_t need = std::max(attn_ws_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim,
+                                       max_ctx, 1, &ns, &sk, &off_ml),
+                         attn_sk_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim,
+                                       num_sms(), &so, &sm));
+  if (num_kv_heads % 2 == 0)
+    need = std::max(need, attn_ws_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim,
+                                        max_ctx, 2, &ns, &sk, &off_ml));
+  return need;
 }
 
 BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_len,
@@ -227,23 +234,28 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
   size_t off_ml, sk_o, sk_ml;
   p.grid = num_sms();
   p.seg_heads = 1;
+  // Kernel choice: BD_ATTENTION (pair | pair_plan | tc5 | mma | simt) forces
+  // one kernel, for testing and measurement; pair_plan runs the head-pair
+  // kernel with the tile-range partition even on small problems
+  const char *env = getenv("BD_ATTENTION");
+  const bool force5 = env && !strcmp(env, "tc5");
+  const bool force_simt = env && !strcmp(env, "simt");
+  const bool force_pair_plan = env && !strcmp(env, "pair_plan");
+  const bool force_pair = (env && !strcmp(env, "pair")) || force_pair_plan;
+  const bool force_mma = env && !strcmp(env, "mma");
+  const bool small = attn_small(batch, p.hkv, block_len, max_ctx) && !force_pair_plan;
+  // fixed splits of the head-pair kernel: split per head pair
+  const bool pair_split = small && force_pair && p.hkv % 2 == 0;
   const size_t need = std::max(
-      attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx, &p.num_splits,
-                    &p.split_keys, &off_ml),
+      attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx,
+                    pair_split ? 2 : 1, &p.num_splits, &p.split_keys, &off_ml),
       attn_sk_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, p.grid, &sk_o, &sk_ml));
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return BD_ERR_WORKSPACE;
   // the split partials and the partition's buffers share the workspace (one
   // scheme runs per call)
   p.part_o = static_cast<float *>(ws);
   p.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + off_ml);
-  // Kernel choice: BD_ATTENTION (pair | tc5 | mma | simt) forces one kernel,
-  // for testing and measurement; the head-pair kernel always partitions tiles
-  const char *env = getenv("BD_ATTENTION");
-  const bool force5 = env && !strcmp(env, "tc5");
-  const bool force_simt = env && !strcmp(env, "simt");
-  const bool force_pair = env && !strcmp(env, "pair");
-  const bool force_mma = env && !strcmp(env, "mma");
-  if (attn_small(batch, p.hkv, block_len, max_ctx) && !force_pair) {
+  if (small) {
     // fixed splits: the mma.sync kernel writes its partials where the
     // split combine reads them
     p.plan = nullptr;
@@ -260,9 +272,16 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
   // kernel with fixed splits on small ones (a few pages per SM, where its
   // shorter start wins); the mma.sync kernel for other bf16 shapes; SIMT for
   // fp32.
-  if ((force_pair || (!force5 && !force_simt && !force_mma)) && p.plan &&
-      attention_pair_supported(p))
-    return attention_pair(p, st);
+  if (pair_split || ((force_pair || (!force5 && !force_simt && !force_mma)) && p.plan)) {
+    if (attention_pair_supported(p)) return attention_pair(p, st);
+    if (pair_split) {            // shape not supported: the default kernel, default splits
+      if (ws_bytes < attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx, 1,
+                                   &p.num_splits, &p.split_keys, &off_ml))
+        return BD_ERR_WORKSPACE;
+      p.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + off_ml);
+      p.sk_ml = p.part_ml;
+    }
+  }
   if (force5 && attention_tc5_supported(p)) {
     const bd_status s = attention_tc5(p, st);
     if (s != BD_OK || p.num_splits == 1) return s;

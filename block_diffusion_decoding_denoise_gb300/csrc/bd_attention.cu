@@ -172,9 +172,14 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p) {
   const int ctx = p.ctx_len[b];
   if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) return;
   const int used = (ctx + p.block_len + p.split_keys - 1) / p.split_keys;  // splits with keys
-  const size_t base = (((size_t)b * p.hkv + g) * p.num_splits) * R + r;
+  // partials [segment][split][seg_heads * R rows]; a segment is one KV head, or
+  // a pair of them for the head-pair kernel
+  const int HS = p.seg_heads > 0 ? p.seg_heads : 1;
+  const size_t seg = (size_t)b * (p.hkv / HS) + g / HS;
+  const size_t srows = (size_t)HS * R;
+  const size_t base = seg * p.num_splits * srows + (size_t)(g % HS) * R + r;
   float m = -INFINITY;
-  for (int s = lane; s < used; s += 32) m = fmaxf(m, __ldcg(&p.part_ml[(base + (size_t)s * R) * 2]));
+  for (int s = lane; s < used; s += 32) m = fmaxf(m, __ldcg(&p.part_ml[(base + (size_t)s * srows) * 2]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float l = 0.f, acc[DPL];
@@ -182,7 +187,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p) {
   for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
 #pragma unroll 4
   for (int s = 0; s < used; ++s) {
-    const size_t pr = base + (size_t)s * R;
+    const size_t pr = base + (size_t)s * srows;
     const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + pr * 2));
     const float w = __expf(ml.x - m);
     l = fmaf(ml.y, w, l);

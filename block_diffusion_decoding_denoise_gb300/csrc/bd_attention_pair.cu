@@ -210,39 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0, pc = 0;
     bool stop = false;
     if (lane == 0) {
-      const int T = p.plan[2 * p.batch];
-      const int c = blockIdx.x, G = gridDim.x;
-      const int t_begin = (int)(((long long)c * T) / G);
-      const int t_end = (int)(((long long)(c + 1) * T) / G);
-      int b = 0;
-      {                                        // last sequence with base <= t_begin
-        int lo = 0, hi = p.batch - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (p.plan[2 * mid] <= t_begin) lo = mid;
-          else hi = mid - 1;
-        }
-        b = lo;
-      }
-      for (int t = t_begin; t < t_end && !stop;) {
-        while (b < p.batch - 1 && t >= p.plan[2 * b] + npairs * p.plan[2 * b + 1]) ++b;
-        const int base = p.plan[2 * b], tiles = p.plan[2 * b + 1];
-        if (tiles <= 0 || t < base || t >= base + npairs * tiles) {
-          flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
-          break;
-        }
-        const int hp = (t - base) / tiles, u0 = (t - base) % tiles;
-        const int seg0 = base + hp * tiles;
-        const int u1 = min(seg0 + tiles, t_end) - seg0;
-        const int seg = b * npairs + hp;
-        const int slot = (u0 == 0 && u1 == tiles) ? -1 : seg + c;
-        const int ctx = p.ctx_len[b];
-        const int npg = tiles - 1;
-        // Q of both heads: rows i * group + j of head 2hp, then of head 2hp + 1
+      // one piece: Q of the head pair, then tiles u in [u_first, u_last) of
+      // sequence b (u < npg: cached page u; u == npg: the block's own keys
+      // [blo, bhi)); false once stopped
+      auto emit = [&](int b, int hp, int ctx, int npg, int u_first, int u_last, int blo,
+                      int bhi, int seg, int slot) -> bool {
         if (pc > 0 && !mbar_wait(smem_u32(&sm.q_empty), (pc - 1) & 1)) {
           fail();
-          stop = true;
-          break;
+          return false;
         }
         {
           const uint32_t bar = smem_u32(&sm.q_full);
@@ -253,23 +228,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                           (2 * hp + hs) * group, 0, b, bar);
         }
         ++pc;
-        for (int u = u0; u < u1; ++u, ++it) {
+        for (int u = u_first; u < u_last; ++u, ++it) {
           const uint32_t s = it % kStages, round = it / kStages;
-          if (sm.abort_flag) {
-            stop = true;
-            break;
-          }
+          if (sm.abort_flag) return false;
           if (round > 0 && !mbar_wait(smem_u32(&sm.kv_empty[s]), (round - 1) & 1)) {
             fail();
-            stop = true;
-            break;
+            return false;
           }
           const uint32_t bar = smem_u32(&sm.kv_full[s]);
           Meta m;
           m.item = seg;
           m.slot = slot;
           m.lo = 0;
-          m.flags = (u == u0 ? kFirst : 0) | (u == u1 - 1 ? kLast : 0);
+          m.flags = (u == u_first ? kFirst : 0) | (u == u_last - 1 ? kLast : 0);
           if (u < npg) {
             const int pg = p.page_table[(size_t)b * p.max_pages + u];
             m.hi = min(kPage, ctx - u * kPage);
@@ -292,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive(bar);
             }
           } else {
-            m.hi = L;
+            m.lo = blo;
+            m.hi = bhi;
             sm.meta[s] = m;
             fence_proxy_async();
             mbar_arrive_expect_tx(bar, 2 * 2 * 2 * L * 128);
@@ -305,7 +277,69 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
           }
         }
-        t = seg0 + u1;
+        return true;
+      };
+      if (p.plan) {
+        // tile-range partition: this CTA's tiles [t_begin, t_end) of the plan's T
+        const int T = p.plan[2 * p.batch];
+        const int c = blockIdx.x, G = gridDim.x;
+        const int t_begin = (int)(((long long)c * T) / G);
+        const int t_end = (int)(((long long)(c + 1) * T) / G);
+        int b = 0;
+        {                                      // last sequence with base <= t_begin
+          int lo = 0, hi = p.batch - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.plan[2 * mid] <= t_begin) lo = mid;
+            else hi = mid - 1;
+          }
+          b = lo;
+        }
+        for (int t = t_begin; t < t_end && !stop;) {
+          while (b < p.batch - 1 && t >= p.plan[2 * b] + npairs * p.plan[2 * b + 1]) ++b;
+          const int base = p.plan[2 * b], tiles = p.plan[2 * b + 1];
+          if (tiles <= 0 || t < base || t >= base + npairs * tiles) {
+            flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+            break;
+          }
+          const int hp = (t - base) / tiles, u0 = (t - base) % tiles;
+          const int seg0 = base + hp * tiles;
+          const int u1 = min(seg0 + tiles, t_end) - seg0;
+          const int seg = b * npairs + hp;
+          const int slot = (u0 == 0 && u1 == tiles) ? -1 : seg + c;
+          stop = !emit(b, hp, p.ctx_len[b], tiles - 1, u0, u1, 0, L, seg, slot);
+          t = seg0 + u1;
+        }
+      } else {
+        // fixed KV splits (small problems): items (sequence, head pair, split)
+        // dealt round-robin; split s covers keys [s * split_keys, + split_keys)
+        const int nitems = p.batch * npairs * p.num_splits;
+        for (int item = blockIdx.x; item < nitems && !stop; item += gridDim.x) {
+          const int split = item % p.num_splits;
+          const int hp = (item / p.num_splits) % npairs;
+          const int b = item / (p.num_splits * npairs);
+          if (p.tokens) {
+            bool masked = false;
+            for (int i = 0; i < L; ++i) masked |= p.tokens[(size_t)b * L + i] == BD_MASK;
+            if (!masked) continue;
+          }
+          const int ctx = p.ctx_len[b];
+          if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) {
+            if (split == 0 && hp == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+            continue;
+          }
+          const int kbeg = split * p.split_keys;
+          const int kend = min(ctx + L, kbeg + p.split_keys);
+          if (kbeg >= kend) continue;            // no key of this sequence in this split
+          const int npg = (ctx + kPage - 1) / kPage;
+          const int p_first = kbeg / kPage;
+          const int p_end = kbeg < ctx ? (min(kend, ctx) + kPage - 1) / kPage : p_first;
+          const int u_last = kend > ctx ? npg + 1 : p_end;   // the block tile follows page npg - 1
+          const int seg = b * npairs + hp;
+          const int slot = p.num_splits == 1 ? -1 : seg * p.num_splits + split;
+          stop = !emit(b, hp, ctx, npg, p_first, u_last, max(kbeg, ctx) - ctx, kend - ctx, seg,
+                       slot);
+        }
       }
       if (!stop) {                             // sentinel stage: no more work
         const uint32_t s = it % kStages, round = it / kStages;
@@ -472,11 +506,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.s_empty[s]));
-      const int hi = (m.flags & kSkip) ? 0 : m.hi;
+      const int lo = m.lo, hi = (m.flags & kSkip) ? 0 : m.hi;
       float mt = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 64; ++j)
-        if (j < hi) mt = fmaxf(mt, sc[j]);
+        if (j >= lo && j < hi) mt = fmaxf(mt, sc[j]);
       float factor = 1.f;
       if (mt > m2) {
         if (m2 == -INFINITY) {
@@ -494,8 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int j0 = 2 * e, j1 = j0 + 1;
-          const float p0 = j0 < hi ? fast_exp2(sc[j0] - m2) : 0.f;
-          const float p1 = j1 < hi ? fast_exp2(sc[j1] - m2) : 0.f;
+          const float p0 = (j0 >= lo && j0 < hi) ? fast_exp2(sc[j0] - m2) : 0.f;
+          const float p1 = (j1 >= lo && j1 < hi) ? fast_exp2(sc[j1] - m2) : 0.f;
           sum += p0 + p1;
           pw[e] = pack_bf16(p0, p1);
         }
@@ -601,7 +635,7 @@ bool attention_pair_supported(const AttnParams &p) {
   if (p.dtype != BD_BF16 || p.head_dim != D || p.page_size != kPage) return false;
   if (p.hkv % 2 != 0 || p.hq % p.hkv != 0) return false;
   if (p.block_len * (p.hq / p.hkv) != 64) return false;
-  if (!p.plan || !p.sk_o || !p.sk_ml || p.grid < 1) return false;
+  if (p.grid < 1 || ((p.plan || p.num_splits > 1) && (!p.sk_o || !p.sk_ml))) return false;
   if ((long long)p.batch * (p.hkv / 2) * (p.max_pages + 1) >= (1LL << 30)) return false;
   const DevInfo d = dev_info();
   return d.major >= 10 && tma_available();
@@ -636,13 +670,18 @@ bd_status attention_pair(const AttnParams &p0, cudaStream_t st) {
       !tma_encode_bf16(&mq, 4, p.q, qdims, qstr, qbox))
     return BD_ERR_CUDA;
   const size_t smem = sizeof(Smem) + 1024;
-  cudaError_t e = attention_plan_launch(p, st);
-  if (e != cudaSuccess) return BD_ERR_CUDA;
-  e = launch_pdl(attn_pair_kernel, dim3(p.grid), dim3(kThreads), smem, st, mkp, mvp, mkb, mvb, mq,
-                 p);
+  int grid = p.grid;
+  if (p.plan) {
+    if (attention_plan_launch(p, st) != cudaSuccess) return BD_ERR_CUDA;
+  } else {
+    grid = std::max(1, std::min(p.batch * (p.hkv / 2) * p.num_splits, p.grid));
+  }
+  const cudaError_t e =
+      launch_pdl(attn_pair_kernel, dim3(grid), dim3(kThreads), smem, st, mkp, mvp, mkb, mvb, mq, p);
   count_launches(1);
   if (e != cudaSuccess) return BD_ERR_CUDA;
-  return attention_combine_sk(p, st);
+  if (p.plan) return attention_combine_sk(p, st);
+  return p.num_splits > 1 ? attention_combine(p, st) : BD_OK;
 }
 
 }  // namespace bd
