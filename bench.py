@@ -53,6 +53,9 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--sweep", default=None,
                     help="comma-separated thresholds: run the multi-block threshold sweep")
+    ap.add_argument("--regions", default=None,
+                    help="region thresholds by block position, e.g. 0.99:8,0.7:16,0.9:8 "
+                         "(T:positions, summing to the block length): one more sweep line")
     ap.add_argument("--blocks", type=int, default=0, help="blocks per sweep decode")
     ap.add_argument("--ar-compare", action="store_true",
                     help="block diffusion vs token-by-token decoding on the same shapes")
@@ -515,7 +518,17 @@ def run_sweep(a):
         h, _ = wl.planted_hidden(w, W, blk, a_max=a_max)
         blocks.append(tuple(torch.from_numpy(x).to("cuda", torch.bfloat16) for x in (h, q, kb, vb)))
     kvs = [wl.prefix_kv(w, b, int(plen[b])) for b in range(w.batch)]
-    for T in [float(x) for x in a.sweep.split(",")]:
+    entries = [({"threshold": float(x)}, float(x)) for x in a.sweep.split(",")] if a.sweep else []
+    if a.regions:
+        row = []
+        for part in a.regions.split(","):
+            t, n = part.split(":")
+            row += [float(t)] * int(n)
+        if len(row) != w.block_len:
+            raise SystemExit(f"--regions covers {len(row)} positions, the block has {w.block_len}")
+        entries.append(({"region_thresholds": a.regions},
+                         np.tile(np.asarray(row, np.float32), (w.batch, 1))))
+    for label, T in entries:
         cache = PagedCache(npg, w.num_kv_heads, w.head_dim, torch.bfloat16, table)
         for b in range(w.batch):
             cache.load_prefix(b, torch.from_numpy(kvs[b][0]), torch.from_numpy(kvs[b][1]))
@@ -543,7 +556,7 @@ def run_sweep(a):
         tokens = w.batch * w.block_len * nblk
         st = np.array(steps)
         print(json.dumps({
-            "sweep": True, "metric": METRIC, "unit": UNIT, "threshold": T,
+            "sweep": True, "metric": METRIC, "unit": UNIT, **label,
             "value": tokens / (ms / 1e3), "ms": ms, "blocks": nblk,
             "denoise_steps_per_block_mean": float(st.mean()),
             "denoise_steps_per_block_min": int(st.min()),
@@ -1036,7 +1049,7 @@ def main():
         return
     if a.impl == "reference":
         run_reference(a)
-    elif a.sweep:
+    elif a.sweep or a.regions:
         run_sweep(a)
     elif a.ar_compare:
         run_ar_compare(a)

@@ -31,7 +31,7 @@ EXPORTS = ("bd_block_attention_workspace", "bd_block_attention",
            "bd_confidence_commit_noalloc", "bd_sample_commit_workspace", "bd_sample_commit",
            "bd_embed_rmsnorm", "bd_qkv_projection_workspace", "bd_qkv_projection",
            "bd_out_projection_workspace", "bd_out_projection_residual",
-           "bd_append_block_kv_layers")
+           "bd_append_block_kv_layers", "bd_confidence_commit_regions")
 
 
 class BDError(RuntimeError):
@@ -70,6 +70,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                                c_void_p, c_void_p, c_float, c_void_p, c_void_p,
                                                c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
                                                c_void_p, c_void_p]),
+            "bd_confidence_commit_regions": (c_int32, [c_int32, c_int32, c_int32, c_int32,
+                                                       c_int32, c_void_p, c_void_p, c_void_p,
+                                                       c_void_p, c_void_p, c_void_p, c_void_p,
+                                                       c_void_p, c_void_p, c_size_t, c_void_p,
+                                                       c_void_p]),
             "bd_append_block_kv": (c_int32, [P, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p]),
             "bd_status_string": (ctypes.c_char_p, [c_int32]),
@@ -186,6 +191,27 @@ def bd_confidence_commit(hidden_states, lm_head, threshold, tokens, p_max, argma
         _ptr(ws, name="ws"), ws.numel() * ws.element_size(),
         _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check("bd_confidence_commit", st)
+
+
+def bd_confidence_commit_regions(hidden_states, lm_head, thresholds, tokens, p_max, argmax,
+                                 n_committed, n_masked, ws, dev_status=None, stream=None):
+    """bd_confidence_commit with a per-position threshold array
+    `thresholds` [B, L'] float32 on the device (region thresholds)."""
+    B, L, H = hidden_states.shape
+    V = lm_head.shape[0]
+    if lm_head.shape[1] != H or lm_head.dtype != hidden_states.dtype:
+        raise ValueError("lm_head must be [vocab, hidden] with the hidden states' dtype")
+    if tuple(thresholds.shape) != (B, L):
+        raise ValueError("thresholds must be [batch, block_len]")
+    st = load().bd_confidence_commit_regions(
+        _dtype_code(hidden_states), B, L, H, V, _ptr(hidden_states, name="hidden_states"),
+        _ptr(lm_head, name="lm_head"), _ptr(thresholds, torch.float32, "thresholds"),
+        _ptr(tokens, torch.int32, "tokens"),
+        _ptr(p_max, torch.float32, "p_max"), _ptr(argmax, torch.int32, "argmax"),
+        _ptr(n_committed, torch.int32, "n_committed"), _ptr(n_masked, torch.int32, "n_masked"),
+        _ptr(ws, name="ws"), ws.numel() * ws.element_size(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("bd_confidence_commit_regions", st)
 
 
 def bd_confidence_commit_noalloc(hidden_states, lm_head, threshold, tokens, p_max, argmax,

@@ -423,6 +423,32 @@ BD_API bd_status bd_confidence_commit(bd_dtype dtype, int32_t batch, int32_t blo
   return conf_run(p, hidden_states, lm_head, ws, ws_bytes, stream);
 }
 
+BD_API bd_status bd_confidence_commit_regions(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                              int32_t hidden, int32_t vocab,
+                                              const void *hidden_states, const void *lm_head,
+                                              const float *thresholds, int32_t *tokens,
+                                              float *p_max, int32_t *argmax,
+                                              int32_t *n_committed, int32_t *n_masked, void *ws,
+                                              size_t ws_bytes, int32_t *dev_status,
+                                              void *stream) {
+  if (!thresholds || (reinterpret_cast<uintptr_t>(thresholds) & 3)) return BD_ERR_INVALID_ARG;
+  ConfParams p{};
+  p.dtype = dtype;
+  p.batch = batch;
+  p.block_len = block_len;
+  p.hidden = hidden;
+  p.vocab = vocab;
+  p.threshold = 0.f;
+  p.thresholds = thresholds;
+  p.tokens = tokens;
+  p.p_max = p_max;
+  p.argmax = argmax;
+  p.n_committed = n_committed;
+  p.n_masked = n_masked;
+  p.dev_status = dev_status;
+  return conf_run(p, hidden_states, lm_head, ws, ws_bytes, stream);
+}
+
 BD_API size_t bd_sample_commit_workspace(bd_dtype dtype, int32_t batch, int32_t block_len,
                                          int32_t hidden, int32_t vocab) {
   return conf_workspace(dtype, batch, block_len, hidden, vocab, true);

@@ -29,6 +29,7 @@ struct ConfParams {
   int batch, block_len, hidden, vocab;
   const void *h, *w;
   float threshold;
+  const float *thresholds;      // per-position thresholds [batch][block_len], or null: threshold
   int32_t *tokens;
   float *p_max;                 // greedy: p_max; sampling: probability of the draw
   int32_t *argmax, *n_committed, *n_masked;   // argmax: greedy argmax or the draw
@@ -72,8 +73,10 @@ __device__ __forceinline__ void finalize_row(const ConfParams &p, const MaxSumAr
 
 // Commit decision of sequence b by one warp; lane i (< block_len) holds
 // position i's masked flag and, when masked, its p_max and argmax.
-//   S = { masked i : p_max_i >= T }; if S is empty and a position is masked,
+//   S = { masked i : p_max_i >= T_i }; if S is empty and a position is masked,
 //   S = { the masked i with the largest p_max, lowest i on ties }.
+// T_i is the scalar threshold, or position i's entry of the per-position
+// array (region thresholds); a NaN entry never qualifies.
 __device__ __forceinline__ void commit_sequence_warp(const ConfParams &p, int b, bool masked,
                                                      float pm, int am) {
   const int lane = threadIdx.x & 31;
@@ -81,7 +84,8 @@ __device__ __forceinline__ void commit_sequence_warp(const ConfParams &p, int b,
   const int pos = b * L + lane;
   const bool in = lane < L;
   const unsigned mmask = __ballot_sync(0xffffffffu, masked);
-  unsigned sel = __ballot_sync(0xffffffffu, masked && pm >= p.threshold);
+  const float thr = (p.thresholds && in) ? p.thresholds[pos] : p.threshold;
+  unsigned sel = __ballot_sync(0xffffffffu, masked && pm >= thr);
   if (sel == 0u && mmask != 0u) {
     float best = masked ? pm : -INFINITY;
     int who = masked ? lane : 32;

@@ -63,7 +63,10 @@ class DenoiseEngine:
     def __init__(self, lm_head: torch.Tensor, caches, ctx_len, *, batch: int, block_len: int,
                  num_q_heads: int, threshold: float, max_ctx: int,
                  temperature: float | None = None, seed: int = 0, decoder=None):
-        """`temperature` None: greedy confidence (bd_confidence_commit); a
+        """`threshold`: one number, or a [batch, block_len] array of
+        per-position thresholds (region thresholds, greedy only:
+        bd_confidence_commit_regions).
+        `temperature` None: greedy confidence (bd_confidence_commit); a
         number: sampled tokens (bd_sample_commit) with key `seed` and a device
         draw counter that every step advances, also under graph replay.
         `decoder` (a DecoderStack sharing this engine's ctx_len): every step
@@ -75,9 +78,19 @@ class DenoiseEngine:
         self.W = lm_head
         self.caches = caches if isinstance(caches, (list, tuple)) else [caches]
         self.B, self.L, self.Hq = batch, block_len, num_q_heads
-        self.T = float(threshold)
-        self.max_ctx = int(max_ctx)
         dev = lm_head.device
+        self.thresholds = None
+        if np.ndim(threshold) == 0:
+            self.T = float(threshold)
+        else:
+            if temperature is not None:
+                raise ValueError("per-position thresholds are a greedy-commit option")
+            thr = np.asarray(threshold, np.float32)
+            if thr.shape != (batch, block_len):
+                raise ValueError("per-position thresholds must be [batch, block_len]")
+            self.T = None
+            self.thresholds = torch.as_tensor(thr).to(dev)
+        self.max_ctx = int(max_ctx)
         c0 = self.caches[0]
         self.Hkv, self.D = c0.k.shape[1], c0.k.shape[3]
         self.dtype = lm_head.dtype
@@ -130,7 +143,11 @@ class DenoiseEngine:
 
     def commit(self, h, n_committed_out):
         """The confidence/commit call of one step (greedy or sampled)."""
-        if self.temperature is None:
+        if self.thresholds is not None:
+            bd.bd_confidence_commit_regions(h, self.W, self.thresholds, self.tokens, self.p_max,
+                                            self.argmax, n_committed_out, self.n_masked,
+                                            self.conf_ws, dev_status=self.dev_status)
+        elif self.temperature is None:
             bd.bd_confidence_commit(h, self.W, self.T, self.tokens, self.p_max, self.argmax,
                                     n_committed_out, self.n_masked, self.conf_ws,
                                     dev_status=self.dev_status)

@@ -148,6 +148,28 @@ bd_status bd_confidence_commit(bd_dtype dtype, int32_t batch, int32_t block_len,
                                int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * bd_confidence_commit_regions -- bd_confidence_commit with one threshold per
+ * block position.  The pages suggest, as future work, thresholds that adapt
+ * to the region of the page being decoded (text, table, formula); here a
+ * region is any set of positions the caller gives the same value.
+ *
+ *   thresholds [batch][block_len] float, DEVICE pointer, 4-byte aligned, read
+ *              in stream order: position (b, i) qualifies when masked and
+ *              p_max[b,i] >= thresholds[b,i] (a NaN entry never qualifies);
+ *              if no masked position of b qualifies, the single most
+ *              confident one is committed, as in bd_confidence_commit.
+ *   all other arguments, results, workspace (bd_confidence_commit_workspace)
+ *   and limits as bd_confidence_commit; thresholds NULL or misaligned:
+ *   BD_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------ */
+bd_status bd_confidence_commit_regions(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                       int32_t hidden, int32_t vocab, const void *hidden_states,
+                                       const void *lm_head, const float *thresholds,
+                                       int32_t *tokens, float *p_max, int32_t *argmax,
+                                       int32_t *n_committed, int32_t *n_masked, void *ws,
+                                       size_t ws_bytes, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
  * bd_confidence_commit_noalloc -- bd_confidence_commit without a caller
  * workspace.  The paper has no counterpart to this call: it exists for
  * callers that cannot allocate device memory when they run a step (code
@@ -180,9 +202,10 @@ bd_status bd_confidence_commit_noalloc(bd_dtype dtype, int32_t batch, int32_t bl
  *
  * For every still-masked position (b, i), with pos = b * block_len + i:
  *   z_v      = (hidden_states[b,i,:] . lm_head[v,:]) / temperature
- *   U_v      = ((word >> 41) + 1/2) / 2^23, word = word (pos % 4) of
- *              Philox-4x64-10 (Salmon et al., SC'11) at counter
- *              (v, pos / 4, n, 0) under key (seed, 0)
+ *   U_v      = (f + 1/2) / 2^23, f = a 23-bit field of word ((pos / 2) % 4)
+ *              of Philox-4x64-10 (Salmon et al., SC'11) at counter
+ *              (v, pos / 8, n, 0) under key (seed, 0): bits 63..41 of the
+ *              word for even pos, bits 31..9 for odd pos
  *   sampled  = lowest v attaining max_v (z_v - ln(-ln U_v))   (Gumbel-max)
  *   p_sel    = softmax(z)[sampled]
  * then the commit rule of bd_confidence_commit with p_sel as the confidence

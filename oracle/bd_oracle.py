@@ -157,8 +157,11 @@ def commit(tokens, p_max, argmax, threshold):
 
     tokens [B, L'] int (MASK = -1 marks still-masked positions); p_max and
     argmax [B, L'] hold the step's confidence for the masked positions (other
-    entries are ignored).  For each sequence:
-        S = { i masked : p_max[i] >= T }                        (R1)
+    entries are ignored).  `threshold` is one number T, or a [B, L'] array of
+    per-position thresholds T[b, i] (region thresholds: the summary's
+    weaknesses paragraph proposes local thresholds that follow the region of
+    the page; the scalar is the constant array).  For each sequence:
+        S = { i masked : p_max[i] >= T[b, i] }                  (R1)
         if S is empty and some position is masked:
             S = { the masked i with the largest p_max, lowest i on ties }  (R2)
         tokens[i] = argmax[i] for i in S; other tokens unchanged   (R5)
@@ -166,10 +169,11 @@ def commit(tokens, p_max, argmax, threshold):
     """
     tokens = np.array(tokens, dtype=np.int64, copy=True)
     B, L = tokens.shape
+    T = np.broadcast_to(np.asarray(threshold, dtype=np.float64), (B, L))
     chosen = np.zeros((B, L), dtype=bool)
     for b in range(B):
         masked = [i for i in range(L) if tokens[b, i] == MASK]
-        sel = [i for i in masked if p_max[b, i] >= threshold]
+        sel = [i for i in masked if p_max[b, i] >= T[b, i]]
         if not sel and masked:
             best = masked[0]
             for i in masked[1:]:

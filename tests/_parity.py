@@ -100,10 +100,15 @@ class StepStats:
 class ConfRunner:
     """Runs bd_confidence_commit step by step on device buffers."""
 
-    def __init__(self, w: wl.Workload, W: np.ndarray, threshold: float):
+    def __init__(self, w: wl.Workload, W: np.ndarray, threshold):
+        """`threshold`: a number (bd_confidence_commit) or a [B, L'] array of
+        per-position thresholds (bd_confidence_commit_regions)."""
         self.w, self.T = w, threshold
         self.W = dev(W, w.dtype)
         B, L = w.batch, w.block_len
+        self.T_dev = None
+        if np.ndim(threshold) > 0:
+            self.T_dev = torch.from_numpy(np.asarray(threshold, np.float32).copy()).cuda()
         code = bd.BD_F32 if w.dtype == "f32" else bd.BD_BF16
         n = bd.bd_confidence_commit_workspace(code, B, L, w.hidden, w.vocab)
         assert n > 0
@@ -119,8 +124,13 @@ class ConfRunner:
         self.tokens.copy_(torch.from_numpy(tokens.astype(np.int32)))
 
     def step(self, h_dev):
-        bd.bd_confidence_commit(h_dev, self.W, self.T, self.tokens, self.p_max, self.argmax,
-                                self.ncom, self.nmask, self.ws, dev_status=self.status)
+        if self.T_dev is not None:
+            bd.bd_confidence_commit_regions(h_dev, self.W, self.T_dev, self.tokens, self.p_max,
+                                            self.argmax, self.ncom, self.nmask, self.ws,
+                                            dev_status=self.status)
+        else:
+            bd.bd_confidence_commit(h_dev, self.W, self.T, self.tokens, self.p_max, self.argmax,
+                                    self.ncom, self.nmask, self.ws, dev_status=self.status)
         torch.cuda.synchronize()
         assert int(self.status.item()) == 0, bd.STATUS.get(int(self.status.item()))
         return (self.tokens.cpu().numpy().astype(np.int64), self.p_max.cpu().numpy(),
@@ -128,10 +138,12 @@ class ConfRunner:
                 self.nmask.cpu().numpy())
 
 
-def lockstep_block(w: wl.Workload, W: np.ndarray, h_steps: np.ndarray, threshold: float,
+def lockstep_block(w: wl.Workload, W: np.ndarray, h_steps: np.ndarray, threshold,
                    tokens0: np.ndarray | None = None, check_oracle_full: bool = True):
-    """Denoise one block on the GPU and compare every step with the oracle."""
+    """Denoise one block on the GPU and compare every step with the oracle.
+    `threshold` is a number or a [B, L'] array of per-position thresholds."""
     B, L = w.batch, w.block_len
+    T = np.broadcast_to(np.asarray(threshold, np.float64), (B, L))
     tol = tol_for(w.dtype)
     run = ConfRunner(w, W, threshold)
     tokens = np.full((B, L), -1, np.int64) if tokens0 is None else tokens0.astype(np.int64)
@@ -155,7 +167,7 @@ def lockstep_block(w: wl.Workload, W: np.ndarray, h_steps: np.ndarray, threshold
         unmasked = tokens != -1
         assert (g_p[unmasked] == -1).all() and (g_a[unmasked] == -1).all()
         margin = conf["top2_prob_margin"]
-        near_t = np.abs(conf["p_max"] - threshold) < EXEMPT
+        near_t = np.abs(conf["p_max"] - T[bi, ii]) < EXEMPT
         am_exempt = margin < EXEMPT
         bad_am = (g_a[bi, ii] != o_a[bi, ii]) & ~am_exempt
         stats.argmax_mismatch_nonexempt += int(bad_am.sum())
@@ -165,7 +177,7 @@ def lockstep_block(w: wl.Workload, W: np.ndarray, h_steps: np.ndarray, threshold
         exempt_pos[bi, ii] = am_exempt | near_t
         for b in range(B):                                   # fallback near-ties
             mb = tokens[b] == -1
-            if mb.any() and not (o_p[b][mb] >= threshold).any() and mb.sum() > 1:
+            if mb.any() and not (o_p[b][mb] >= T[b][mb]).any() and mb.sum() > 1:
                 ps = np.sort(o_p[b][mb])
                 if ps[-1] - ps[-2] < EXEMPT:
                     exempt_pos[b] |= mb & (o_p[b] > ps[-1] - EXEMPT)
@@ -274,7 +286,7 @@ def lockstep_sampled_block(w: wl.Workload, W: np.ndarray, h_steps: np.ndarray, t
         exempt_pos[bi, ii] = key_exempt | (np.abs(o_p[bi, ii] - threshold) < EXEMPT)
         for b in range(B):
             mb = tokens[b] == -1
-            if mb.any() and not (o_p[b][mb] >= threshold).any() and mb.sum() > 1:
+            if mb.any() and not (o_p[b][mb] >= T[b][mb]).any() and mb.sum() > 1:
                 ps = np.sort(o_p[b][mb])
                 if ps[-1] - ps[-2] < EXEMPT:
                     exempt_pos[b] |= mb & (o_p[b] > ps[-1] - EXEMPT)

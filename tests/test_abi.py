@@ -82,6 +82,17 @@ def test_sample_commit_checks_arguments_on_the_host(lib):
     assert st == 1
 
 
+def test_region_commit_checks_arguments_on_the_host(lib):
+    f = lib.bd_confidence_commit_regions
+    for thr in (None, 2, 4096 + 1):                      # missing or not 4-byte aligned
+        st = f(1, 1, 32, 2048, 1000, None, None, thr, None, None, None, None, None, None, 0,
+               None, None)
+        assert st == 1
+    st = f(1, 1, 33, 2048, 1000, None, None, 4096, None, None, None, None, None, None, 0,
+           None, None)                                   # block_len above 32
+    assert st == 1
+
+
 def test_decoder_calls_check_arguments_on_the_host(lib):
     # shapes the projection kernels cannot take return a zero workspace
     assert bd.bd_qkv_projection_workspace(256, 2048, 16, 8, 128) > 0

@@ -182,6 +182,36 @@ def test_decode_threshold_extremes(T, steps):
     assert st.steps_gpu.tolist() == [steps] * w.batch
 
 
+def test_decode_region_thresholds():
+    # per-position thresholds (bd_confidence_commit_regions): three regions per
+    # sequence at different offsets, one sequence with a NaN region (never
+    # qualifies), under a plant strong enough for every threshold to matter
+    w = SMALL_BF16
+    W = wl.lm_head(w)
+    h, _ = wl.planted_hidden(w, W, 0, a_max=30.0)
+    B, L = w.batch, w.block_len
+    T = np.empty((B, L))
+    for b in range(B):
+        i = (np.arange(L) + 7 * b) % L
+        T[b] = np.where(i < 8, 0.99, np.where(i < 24, 0.7, 0.9))
+    T[-1, :5] = np.nan
+    st = lockstep_block(w, W, h, T)
+    assert st.rows_checked > 0
+
+
+def test_decode_region_thresholds_closed_form():
+    # T = 0 on region A, T = 2 elsewhere: step 1 commits exactly A, then one
+    # position per step through the fallback, so steps = 1 + (L' - |A|)
+    w = SMALL_BF16
+    W = wl.lm_head(w)
+    h, _ = wl.planted_hidden(w, W, 0)
+    B, L = w.batch, w.block_len
+    sizes = [(5 * b + 3) % L for b in range(B)]
+    T = np.stack([np.where(np.arange(L) < n, 0.0, 2.0) for n in sizes])
+    st = lockstep_block(w, W, h, T)
+    assert st.steps_gpu.tolist() == [1 + L - n if n else L for n in sizes]
+
+
 def test_decode_more_rows_than_one_pass():
     # 5 x 32 = 160 masked rows: the LM head takes two passes of at most 128 rows
     w = SMALL_BF16.with_(batch=5)

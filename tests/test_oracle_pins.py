@@ -232,6 +232,49 @@ def test_commit_rule_properties_random():
                 assert not chosen[b].any()
 
 
+def test_region_thresholds_step_count_closed_form():
+    # region A (T = 0): every masked position qualifies, so step 1 commits all
+    # of A and nothing else; region B (T = 2 > any probability): its positions
+    # only ever go through the fallback, one per step.  Steps = 1 + |B|.
+    rng = np.random.default_rng(21)
+    h, W = _random_step_inputs(rng)
+    B, L = 3, 8
+    regions = [np.arange(L) < 3, np.arange(L) % 2 == 0, np.arange(L) >= 7]
+    T = np.stack([np.where(a, 0.0, 2.0) for a in regions])
+    tokens, steps, trace = oracle.decode_block(h, W, T)
+    assert steps.tolist() == [1 + int((~a).sum()) for a in regions]
+    for b, a in enumerate(regions):
+        assert np.array_equal(trace[0][b] != -1, a)
+        for k in range(1, int(steps[b])):          # while the sequence is active
+            assert (trace[k][b] != -1).sum() - (trace[k - 1][b] != -1).sum() == 1
+
+
+def test_region_thresholds_match_scalar_per_region():
+    # per-position thresholds: a position's decision uses only its own T.  A
+    # sequence whose positions all share one value must decode exactly as the
+    # scalar rule with that value, whatever the other sequences use.
+    rng = np.random.default_rng(22)
+    h, W = _random_step_inputs(rng, scale=1.5)
+    T = np.array([[0.3] * 8, [0.6] * 8, [0.9] * 8])
+    tok_r, steps_r, _ = oracle.decode_block(h, W, T)
+    for b, t in enumerate((0.3, 0.6, 0.9)):
+        tok_s, steps_s, _ = oracle.decode_block(h[:, b:b + 1], W, t)
+        assert np.array_equal(tok_r[b], tok_s[0]) and steps_r[b] == steps_s[0]
+
+
+def test_region_threshold_nan_never_qualifies():
+    # NaN compares false: a NaN region commits only through the fallback,
+    # exactly like T above one
+    rng = np.random.default_rng(23)
+    h, W = _random_step_inputs(rng)
+    T_nan = np.where(np.arange(8) < 4, 0.0, np.nan)[None].repeat(3, 0)
+    T_big = np.where(np.arange(8) < 4, 0.0, 1.5)[None].repeat(3, 0)
+    a = oracle.decode_block(h, W, T_nan)
+    b = oracle.decode_block(h, W, T_big)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert a[1].tolist() == [5, 5, 5]
+
+
 def test_decode_invariants():
     rng = np.random.default_rng(12)
     h, W = _random_step_inputs(rng, scale=1.2)
