@@ -330,10 +330,88 @@ def sample_confidence(h, W, pos, seed, temperature, offset=0, row_chunk: int = 1
     return {"token": token, "p_sel": p_sel, "key_gap": gap}
 
 
-def denoise_step_sampled(tokens, h, W, threshold, temperature, seed, offset=0):
+# Truncated sampling: the other settings of step 6, top-k and top-p, applied
+# in the order samplers usually apply them (temperature, then top-k, then
+# top-p on what top-k kept, renormalised).  Each leaves a value threshold:
+#   top-k (k > 0, k < V): theta_k = the k-th largest z (entries equal to it
+#       are all kept, so ties at the boundary never split);
+#   top-p (0 < p < 1): over the kept entries sorted by z descending with
+#       masses w = exp(z - max z), the first one at which the running mass
+#       reaches p * (total kept mass); theta_p = its z (its ties kept).
+# The kept set is {v : z_v >= max(theta_k, theta_p)}; the token is the
+# Gumbel-max draw restricted to it (same noise G_v as above) and its
+# confidence is its probability under the renormalised kept distribution.
+# k = 0 and p = 1 keep everything, which is sample_confidence again.
+def truncation_threshold(z, top_k=0, top_p=1.0):
+    """Value threshold theta of one row z (fp64): entries with z >= theta are
+    kept.  Also returns the top-p mass margin: min(target - mass before the
+    boundary group, mass through it - target) / kept mass (inf without top-p)."""
+    z = np.asarray(z, dtype=np.float64)
+    zs = np.sort(z)[::-1]
+    theta = -np.inf
+    if 0 < top_k < len(z):
+        theta = zs[top_k - 1]
+    margin = np.inf
+    if top_p < 1.0:
+        kept = zs[zs >= theta]
+        w = np.exp(kept - kept[0])
+        cum = np.cumsum(w)
+        target = top_p * cum[-1]
+        j = int(np.searchsorted(cum, target, side="left"))
+        j = min(j, len(kept) - 1)
+        first = int(np.searchsorted(-kept, -kept[j], side="left"))   # start of j's tie group
+        last = int(np.searchsorted(-kept, -kept[j], side="right")) - 1
+        before = cum[first - 1] if first > 0 else 0.0
+        margin = min(target - before, cum[last] - target) / cum[-1]
+        theta = max(theta, kept[j])
+    return theta, margin
+
+
+def sample_confidence_truncated(h, W, pos, seed, temperature, top_k=0, top_p=1.0, offset=0,
+                                row_chunk: int = 16):
+    """Top-k / top-p truncated Gumbel-max draw for each row of h.
+
+    Returns dict: token, p_sel (probability under the renormalised kept
+    distribution), key_gap (gap between the two largest perturbed keys among
+    the kept entries), theta, p_margin (truncation_threshold's margin) and
+    band_mass (kept-mass share of the entries within 1e-3 of theta, the ones
+    whose membership a small change of z could flip)."""
+    h = np.asarray(h, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    pos = np.asarray(pos, dtype=np.int64)
+    M, V = h.shape[0], W.shape[0]
+    out = {k: np.empty(M) for k in ("p_sel", "key_gap", "theta", "p_margin", "band_mass")}
+    out["token"] = np.empty(M, dtype=np.int64)
+    vs = np.arange(V)
+    for r0 in range(0, M, row_chunk):
+        z = (h[r0:r0 + row_chunk] @ W.T) / float(temperature)
+        g = -np.log(-np.log(uniform01(vs[None, :], pos[r0:r0 + row_chunk, None], seed, offset)))
+        for j in range(z.shape[0]):
+            r = r0 + j
+            theta, margin = truncation_threshold(z[j], top_k, top_p)
+            keep = z[j] >= theta
+            key = np.where(keep, z[j] + g[j], -np.inf)
+            t = int(np.argmax(key))
+            m = z[j][keep].max()
+            w = np.where(keep, np.exp(z[j] - m), 0.0)
+            out["token"][r] = t
+            out["p_sel"][r] = w[t] / w.sum()
+            kk = np.sort(key[keep])
+            out["key_gap"][r] = kk[-1] - kk[-2] if len(kk) > 1 else np.inf
+            out["theta"][r] = theta
+            out["p_margin"][r] = margin
+            band = np.abs(z[j] - theta) < 1e-3
+            out["band_mass"][r] = (np.exp(z[j][band] - m).sum() / w.sum()
+                                   if np.isfinite(theta) else 0.0)
+    return out
+
+
+def denoise_step_sampled(tokens, h, W, threshold, temperature, seed, offset=0, top_k=0,
+                         top_p=1.0):
     """denoise_step with the sampling reading: each masked position draws its
-    token (sample_confidence, position id b * L' + i) and its confidence is the
-    drawn token's probability; the commit rule is unchanged."""
+    token (sample_confidence, or sample_confidence_truncated when top_k > 0 or
+    top_p < 1; position id b * L' + i) and its confidence is the drawn token's
+    probability; the commit rule is unchanged."""
     tokens = np.asarray(tokens)
     B, L = tokens.shape
     bi, ii = np.nonzero(tokens == MASK)
@@ -341,7 +419,12 @@ def denoise_step_sampled(tokens, h, W, threshold, temperature, seed, offset=0):
     tok = np.full((B, L), -1, dtype=np.int64)
     res = None
     if len(bi):
-        res = sample_confidence(np.asarray(h)[bi, ii], W, bi * L + ii, seed, temperature, offset)
+        if top_k > 0 or top_p < 1.0:
+            res = sample_confidence_truncated(np.asarray(h)[bi, ii], W, bi * L + ii, seed,
+                                              temperature, top_k, top_p, offset)
+        else:
+            res = sample_confidence(np.asarray(h)[bi, ii], W, bi * L + ii, seed, temperature,
+                                    offset)
         conf[bi, ii] = res["p_sel"]
         tok[bi, ii] = res["token"]
     new, chosen = commit(tokens, conf, tok, threshold)

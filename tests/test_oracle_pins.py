@@ -388,6 +388,78 @@ def test_tiny_temperature_draw_is_the_argmax():
     assert np.array_equal(res["token"], (h @ W.T).argmax(axis=1))
 
 
+def _logits_as_hw(z):
+    # h = z, W = I: h W^T = z exactly
+    z = np.atleast_2d(np.asarray(z, dtype=np.float64))
+    return z, np.eye(z.shape[1])
+
+
+def test_truncation_threshold_closed_forms():
+    # ties at the top-k boundary are all kept
+    th, _ = oracle.truncation_threshold([3.0, 1.0, 3.0, 3.0, 0.0], top_k=2)
+    assert th == 3.0
+    # top-p over probabilities (0.4, 0.25, 0.2, 0.1, 0.05): running mass 0.4,
+    # 0.65, 0.85 -> p = 0.7 keeps the top three
+    p = np.array([0.4, 0.25, 0.2, 0.1, 0.05])
+    z = np.log(p)
+    th, margin = oracle.truncation_threshold(z, top_p=0.7)
+    assert np.isclose(th, np.log(0.2)) and np.isclose(margin, 0.05)
+    # p exactly at a running-mass value keeps that entry and nothing below it
+    th, _ = oracle.truncation_threshold(z, top_p=0.65 - 1e-12)
+    assert np.isclose(th, np.log(0.25))
+    # order: top-k first, then top-p on the renormalised remainder.  With
+    # probabilities (0.5, 0.3, 0.15, 0.05), k = 2 leaves (0.625, 0.375), and
+    # p = 0.6 then keeps only the first; top-p first would have kept two
+    z = np.log([0.5, 0.3, 0.15, 0.05])
+    th, _ = oracle.truncation_threshold(z, top_k=2, top_p=0.6)
+    assert np.isclose(th, np.log(0.5))
+    # no truncation
+    assert oracle.truncation_threshold(z)[0] == -np.inf
+    assert oracle.truncation_threshold(z, top_k=4)[0] == -np.inf
+
+
+def test_truncated_draw_degenerate_cases():
+    rng = np.random.default_rng(31)
+    h = rng.standard_normal((6, 5))
+    W = rng.standard_normal((40, 5))
+    pos = np.arange(6)
+    z = h @ W.T
+    for kw in ({"top_k": 1}, {"top_p": 1e-12}):
+        r = oracle.sample_confidence_truncated(h, W, pos, seed=5, temperature=1.0, **kw)
+        assert np.array_equal(r["token"], z.argmax(1))       # only the argmax is kept
+        assert np.allclose(r["p_sel"], 1.0)
+    # no truncation is the untruncated sampler
+    a = oracle.sample_confidence_truncated(h, W, pos, seed=5, temperature=0.8)
+    b = oracle.sample_confidence(h, W, pos, seed=5, temperature=0.8)
+    assert np.array_equal(a["token"], b["token"])
+    np.testing.assert_allclose(a["p_sel"], b["p_sel"], rtol=1e-12)
+
+
+@pytest.mark.parametrize("kw,kept", [({"top_k": 3}, [0, 1, 2]),
+                                     ({"top_p": 0.7}, [0, 1, 2]),
+                                     ({"top_k": 4, "top_p": 0.5}, [0, 1])])
+def test_truncated_draws_follow_the_renormalised_distribution(kw, kept):
+    # chi-square of 8000 draws (offsets 0..7999) against the kept entries'
+    # renormalised probabilities; nothing outside the kept set is ever drawn
+    p = np.array([0.4, 0.25, 0.2, 0.1, 0.05])
+    h, W = _logits_as_hw(np.log(p))
+    n = 8000
+    toks, psel = [], []
+    for off in range(n):
+        r = oracle.sample_confidence_truncated(h, W, [3], seed=11, temperature=1.0,
+                                               offset=off, **kw)
+        toks.append(int(r["token"][0]))
+        psel.append(float(r["p_sel"][0]))
+    toks = np.array(toks)
+    assert set(np.unique(toks)) <= set(kept)
+    q = p[kept] / p[kept].sum()
+    counts = np.array([(toks == k).sum() for k in kept])
+    chi2 = float((((counts - n * q) ** 2) / (n * q)).sum())
+    assert chi2 < 20.0, (chi2, counts)                        # df <= 2: p < 5e-5
+    for k in kept:                                            # confidence = q of the token
+        assert np.allclose(np.array(psel)[toks == k], q[kept.index(k)])
+
+
 def test_sampled_step_uses_the_commit_rule():
     rng = np.random.default_rng(22)
     h = rng.standard_normal((2, 6, 4)) * 3
