@@ -64,6 +64,10 @@ def _args():
                     help="planted amplitude bound (the workload's own by default)")
     ap.add_argument("--temperature", type=float, default=None,
                     help="decode with sampled tokens (bd_sample_commit) at this temperature")
+    ap.add_argument("--top-k", type=int, default=0,
+                    help="with --temperature: keep the k most likely tokens (0: all)")
+    ap.add_argument("--top-p", type=float, default=1.0,
+                    help="with --temperature: nucleus truncation at this mass (1: none)")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every kernel from the host instead of replaying CUDA graphs")
     ap.add_argument("--workload", default=WORKLOAD,
@@ -298,7 +302,7 @@ def run_cuda(a):
     max_ctx = int(plen.max()) + w.block_len
     eng = DenoiseEngine(Wd, cache, plen, batch=w.batch, block_len=w.block_len,
                         num_q_heads=w.num_q_heads, threshold=w.threshold, max_ctx=max_ctx,
-                        temperature=a.temperature, seed=1)
+                        temperature=a.temperature, seed=1, top_k=a.top_k, top_p=a.top_p)
     ctx0 = eng.ctx_len.clone()
     stream = torch.cuda.current_stream()
 
@@ -443,8 +447,7 @@ def run_cuda(a):
                               "denoise_steps_per_block": [int(x) for x in steps_per_seq],
                               "denoise_steps_issued": steps_issued // a.steps,
                               "check_every": a.check_every, "cuda_graphs": use_graphs,
-                              "decoding": ("greedy" if a.temperature is None
-                                           else f"sampled, temperature {a.temperature}"),
+                              "decoding": _decoding(a),
                               "per_call_timing": f"CUDA events around every call in "
                                                  f"{min(a.steps, 20)} further blocks after the "
                                                  f"timed region (event nodes slow the graphs)"}),
@@ -491,6 +494,17 @@ def _e2e(a, eng, w, h, q, kb, vb, hd, qd, kbd, vbd, ctx0, stream, committed_per_
     e2e_ms = e0.elapsed_time(e1)
     return {"value": committed_per_block * a.steps * world / (e2e_ms / 1e3), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def _decoding(a):
+    if a.temperature is None:
+        return "greedy"
+    d = f"sampled, temperature {a.temperature}"
+    if a.top_k > 0:
+        d += f", top-k {a.top_k}"
+    if a.top_p < 1.0:
+        d += f", top-p {a.top_p}"
+    return d
 
 
 def run_sweep(a):
@@ -761,7 +775,8 @@ def run_decoder(a):
                          batch=w.batch, block_len=L, num_q_heads=w.num_q_heads, max_ctx=max_ctx)
     eng = DenoiseEngine(dev(W), caches, plen, batch=w.batch, block_len=L,
                         num_q_heads=w.num_q_heads, threshold=w.threshold, max_ctx=max_ctx,
-                        temperature=a.temperature, seed=1, decoder=stack)
+                        temperature=a.temperature, seed=1, decoder=stack,
+                        top_k=a.top_k, top_p=a.top_p)
     h_host = [wl.planted_hidden(w, W, blk)[0] for blk in range(nb)]
     h_dev = [dev(h) for h in h_host]
     h_cur = torch.empty_like(h_dev[0])
@@ -915,8 +930,7 @@ def run_decoder(a):
                               "check_every": a.check_every, "cuda_graphs": use_graphs,
                               "input_generation_s": gen_s,
                               "l2": "inputs larger than L2: 15.5 GB of per-layer KV cache",
-                              "decoding": ("greedy" if a.temperature is None
-                                           else f"sampled, temperature {a.temperature}")}),
+                              "decoding": _decoding(a)}),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches), "clocks": clk.summary(),
     }

@@ -31,7 +31,8 @@ EXPORTS = ("bd_block_attention_workspace", "bd_block_attention",
            "bd_confidence_commit_noalloc", "bd_sample_commit_workspace", "bd_sample_commit",
            "bd_embed_rmsnorm", "bd_qkv_projection_workspace", "bd_qkv_projection",
            "bd_out_projection_workspace", "bd_out_projection_residual",
-           "bd_append_block_kv_layers", "bd_confidence_commit_regions")
+           "bd_append_block_kv_layers", "bd_confidence_commit_regions",
+           "bd_sample_commit_truncated_workspace", "bd_sample_commit_truncated")
 
 
 class BDError(RuntimeError):
@@ -90,6 +91,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                            c_void_p, c_void_p, c_void_p, c_void_p,
                                            c_void_p, c_void_p, c_void_p, c_size_t, c_void_p,
                                            c_void_p]),
+            "bd_sample_commit_truncated_workspace": (c_size_t, [c_int32] * 5),
+            "bd_sample_commit_truncated": (c_int32, [c_int32, c_int32, c_int32, c_int32, c_int32,
+                                                     c_void_p, c_void_p, c_float, c_float,
+                                                     c_int32, c_float, ctypes.c_uint64,
+                                                     c_void_p, c_void_p, c_void_p, c_void_p,
+                                                     c_void_p, c_void_p, c_void_p, c_size_t,
+                                                     c_void_p, c_void_p]),
             "bd_embed_rmsnorm": (c_int32, [c_int32, c_int32, c_int32, c_void_p, c_void_p,
                                            c_void_p, c_float, c_void_p, c_void_p, c_void_p,
                                            c_void_p]),
@@ -253,6 +261,31 @@ def bd_sample_commit(hidden_states, lm_head, threshold, temperature, seed, offse
         ws.numel() * ws.element_size(), _ptr(dev_status, torch.int32, "dev_status"),
         _stream(stream))
     _check("bd_sample_commit", st)
+
+
+def bd_sample_commit_truncated_workspace(dtype_code, batch, block_len, hidden, vocab) -> int:
+    return int(load().bd_sample_commit_truncated_workspace(dtype_code, batch, block_len, hidden,
+                                                           vocab))
+
+
+def bd_sample_commit_truncated(hidden_states, lm_head, threshold, temperature, top_k, top_p,
+                               seed, offset, tokens, p_sel, sampled, n_committed, n_masked, ws,
+                               dev_status=None, stream=None):
+    """bd_sample_commit with top-k / top-p truncation (see bd.h)."""
+    B, L, H = hidden_states.shape
+    V = lm_head.shape[0]
+    if lm_head.shape[1] != H or lm_head.dtype != hidden_states.dtype:
+        raise ValueError("lm_head must be [vocab, hidden] with the hidden states' dtype")
+    st = load().bd_sample_commit_truncated(
+        _dtype_code(hidden_states), B, L, H, V, _ptr(hidden_states, name="hidden_states"),
+        _ptr(lm_head, name="lm_head"), float(threshold), float(temperature), int(top_k),
+        float(top_p), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(offset, torch.int64, "offset"),
+        _ptr(tokens, torch.int32, "tokens"), _ptr(p_sel, torch.float32, "p_sel"),
+        _ptr(sampled, torch.int32, "sampled"), _ptr(n_committed, torch.int32, "n_committed"),
+        _ptr(n_masked, torch.int32, "n_masked"), _ptr(ws, name="ws"),
+        ws.numel() * ws.element_size(), _ptr(dev_status, torch.int32, "dev_status"),
+        _stream(stream))
+    _check("bd_sample_commit_truncated", st)
 
 
 def bd_append_block_kv(kv: PagedKV, k_blk, v_blk, ctx_len, n_masked=None, dev_status=None,

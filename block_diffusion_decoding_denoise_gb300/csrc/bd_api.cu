@@ -31,7 +31,8 @@ bool preload_all() {
   if (done[dev]) return true;
   const bool ok = preload_kernel(append_kv_kernel, false) && preload_attention_simt() &&
                   preload_attention_tc() && preload_attention_tc5() && preload_confidence() &&
-                  preload_lmhead_tc() && preload_decoder() && preload_attention_pair();
+                  preload_lmhead_tc() && preload_decoder() && preload_attention_pair() &&
+                  preload_truncated();
   if (!ok) {
     cudaGetLastError();
     return false;

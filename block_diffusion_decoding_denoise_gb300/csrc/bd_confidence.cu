@@ -353,10 +353,19 @@ static size_t conf_workspace(bd_dtype dtype, int32_t batch, int32_t block_len, i
   return carve(p, nullptr, nullptr);
 }
 
-// Shared body of bd_confidence_commit and bd_sample_commit: argument checks,
-// workspace carve, then prep -> LM head -> commit on one stream.
+// Truncation of a sampled call: logits buffer after the carved workspace.
+struct TruncArgs {
+  int top_k;
+  float top_p;
+  float *logits;
+};
+
+// Shared body of bd_confidence_commit, bd_sample_commit and
+// bd_sample_commit_truncated: argument checks, workspace carve, then
+// prep -> LM head (or logits + truncated selection) -> commit on one stream.
 static bd_status conf_run(ConfParams &p, const void *hidden_states, const void *lm_head,
-                          void *ws, size_t ws_bytes, void *stream) {
+                          void *ws, size_t ws_bytes, void *stream,
+                          const TruncArgs *trunc_in = nullptr) {
   if (!conf_args_ok(p.dtype, p.batch, p.block_len, p.hidden, p.vocab)) return BD_ERR_INVALID_ARG;
   if (!hidden_states || !lm_head || !p.tokens || !p.p_max || !p.argmax || !p.n_committed ||
       !p.n_masked)
@@ -367,14 +376,23 @@ static bd_status conf_run(ConfParams &p, const void *hidden_states, const void *
     return BD_ERR_INVALID_ARG;
   p.h = hidden_states;
   p.w = lm_head;
-  const size_t need = carve(p, nullptr, nullptr);
+  const size_t carved = carve(p, nullptr, nullptr);
+  const size_t need =
+      carved + (trunc_in ? align_up((size_t)p.batch * p.block_len * p.vocab * 4, 256) : 0);
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return BD_ERR_WORKSPACE;
   carve(p, static_cast<char *>(ws), &p.ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TruncArgs tr{};
+  const TruncArgs *trunc = nullptr;
+  if (trunc_in) {
+    tr = *trunc_in;
+    tr.logits = reinterpret_cast<float *>(static_cast<char *>(ws) + carved);
+    trunc = &tr;
+  }
 
-  const bool tc = lmhead_tc_supported(p);
+  // the tensor-core paths read the masked rows from a contiguous copy
+  const bool tc = trunc ? p.dtype == BD_BF16 : lmhead_tc_supported(p);
   const int nrows = p.batch * p.block_len;
-  // the tensor-core path reads the masked rows from a contiguous copy
   const int prep_ctas = tc ? std::max(1, std::min(std::max(dev_info().sms, 1), (nrows + 7) / 8)) : 1;
   const int32_t *tok_in = p.tokens;
   const char *src = tc ? static_cast<const char *>(hidden_states) : nullptr;
@@ -382,7 +400,13 @@ static bd_status conf_run(ConfParams &p, const void *hidden_states, const void *
                              p.ws, src, p.hidden * 2);
   count_launches(1);
   if (e != cudaSuccess) return BD_ERR_CUDA;
-  const bd_status s = tc ? lmhead_tc(p, st) : lmhead_simt(p, st);
+  bd_status s;
+  if (trunc) {
+    s = trunc_logits_and_select(p, trunc->logits, trunc->top_k, trunc->top_p, st);
+    p.ws.num_partials = 1;                    // one sampling state per row
+  } else {
+    s = tc ? lmhead_tc(p, st) : lmhead_simt(p, st);
+  }
   if (s != BD_OK) return s;
   e = p.sample ? launch_pdl(conf_commit_kernel<true>, dim3(p.batch), dim3(32 * p.block_len), 0,
                             st, p)
@@ -447,6 +471,46 @@ BD_API bd_status bd_confidence_commit_regions(bd_dtype dtype, int32_t batch, int
   p.n_masked = n_masked;
   p.dev_status = dev_status;
   return conf_run(p, hidden_states, lm_head, ws, ws_bytes, stream);
+}
+
+BD_API size_t bd_sample_commit_truncated_workspace(bd_dtype dtype, int32_t batch,
+                                                   int32_t block_len, int32_t hidden,
+                                                   int32_t vocab) {
+  const size_t base = conf_workspace(dtype, batch, block_len, hidden, vocab, true);
+  return base ? base + align_up((size_t)batch * block_len * vocab * 4, 256) : 0;
+}
+
+BD_API bd_status bd_sample_commit_truncated(
+    bd_dtype dtype, int32_t batch, int32_t block_len, int32_t hidden, int32_t vocab,
+    const void *hidden_states, const void *lm_head, float threshold, float temperature,
+    int32_t top_k, float top_p, uint64_t seed, uint64_t *offset, int32_t *tokens, float *p_sel,
+    int32_t *sampled, int32_t *n_committed, int32_t *n_masked, void *ws, size_t ws_bytes,
+    int32_t *dev_status, void *stream) {
+  if (!(temperature >= 1e-6f) || !(temperature <= 1e6f)) return BD_ERR_INVALID_ARG;
+  if (!offset || (reinterpret_cast<uintptr_t>(offset) & 7)) return BD_ERR_INVALID_ARG;
+  if (top_k < 0 || !(top_p > 0.f) || !(top_p <= 1.f)) return BD_ERR_INVALID_ARG;
+  ConfParams p{};
+  p.dtype = dtype;
+  p.batch = batch;
+  p.block_len = block_len;
+  p.hidden = hidden;
+  p.vocab = vocab;
+  p.threshold = threshold;
+  p.tokens = tokens;
+  p.p_max = p_sel;
+  p.argmax = sampled;
+  p.n_committed = n_committed;
+  p.n_masked = n_masked;
+  p.dev_status = dev_status;
+  p.sample = 1;
+  p.inv_temp = 1.0f / temperature;
+  p.seed = seed;
+  p.offset = offset;
+  if ((top_k == 0 || top_k >= vocab) && top_p == 1.f)   // nothing truncated: the fused path
+    return conf_run(p, hidden_states, lm_head, ws, ws_bytes, stream);
+  if (vocab > 65535 * 256) return BD_ERR_UNSUPPORTED;
+  TruncArgs tr{top_k, top_p, nullptr};
+  return conf_run(p, hidden_states, lm_head, ws, ws_bytes, stream, &tr);
 }
 
 BD_API size_t bd_sample_commit_workspace(bd_dtype dtype, int32_t batch, int32_t block_len,

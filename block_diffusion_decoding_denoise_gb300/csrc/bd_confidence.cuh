@@ -119,4 +119,14 @@ bool lmhead_tc_supported(const ConfParams &p);
 int lmhead_tc_num_partials(int vocab);
 bd_status lmhead_tc(const ConfParams &p, cudaStream_t st);
 
+// Truncated sampling (bd_sample_commit_truncated): logits of the masked rows
+// into `logits` ([batch * block_len][vocab] fp32, rows < *ws.count written),
+// then one sampling state per row into ws.spartial[row] (a single partial).
+bd_status trunc_logits_and_select(const ConfParams &p, float *logits, int top_k, float top_p,
+                                  cudaStream_t st);
+// tcgen05 projection of x [rows_max][K] (bf16) against w [V][K] (bf16) into
+// out [rows_max][V] fp32 for rows < *dev_rows.
+bd_status logits_tc(int rows_max, int K, int V, const void *x, const void *w, float *out,
+                    const int32_t *dev_rows, int32_t *dev_status, cudaStream_t st);
+
 }  // namespace bd

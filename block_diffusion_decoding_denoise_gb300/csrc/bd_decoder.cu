@@ -211,6 +211,7 @@ struct ProjCtrl {
 
 struct ProjArgs {
   int rows, K, F;       // partial[s][r][f] = sum over split s's K range of x[r][k] * w[f][k]
+  const int32_t *dev_rows;  // if set: only rows < min(rows, *dev_rows) are computed
   int splits, kper;     // K range of one split (a multiple of kPK)
   int box_rows;         // rows per TMA box of x (the pass width, rounded up to 16)
   int stages, stage_bytes, ctrl_off;
@@ -228,8 +229,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ft = blockIdx.x, sp = blockIdx.y, pass = blockIdx.z;
   const int r0 = pass * kPMaxN;
-  const int n = min(kPMaxN, a.rows - r0);
-  const int npad = (n + 15) & ~15;
   const int KC = a.kper / kPK;
   const int k0 = sp * a.kper;
   const int S = a.stages;
@@ -257,9 +256,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
   pdl_trigger();
-  pdl_wait();   // x is written by the previous kernel on the stream
+  pdl_wait();   // x (and the row count) are written by the previous kernel on the stream
+  const int rows = a.dev_rows ? min(a.rows, max(0, *a.dev_rows)) : a.rows;
+  const int n = min(kPMaxN, rows - r0);     // rows of this pass; none: nothing to do
+  const int npad = (n + 15) & ~15;
 
-  if (warp == 0) {
+  if (n <= 0) {
+    // pass beyond the row count
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int kc = 0;
@@ -316,6 +320,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (ok && !ctrl->abort) {
       tc_fence_after();
       const int f = ft * kPTileF + 32 * q + lane;
+      const bool fin = f < a.F;               // the last tile may run past F
       float *out = a.partial + (size_t)sp * a.rows * a.F + f;
       for (int c0 = 0; c0 < npad; c0 += 16) {
         uint32_t r[16];
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int row = r0 + c0 + j;
-          if (row < a.rows) out[(size_t)row * a.F] = __uint_as_float(r[j]);
+          if (row < rows && fin) out[(size_t)row * a.F] = __uint_as_float(r[j]);
         }
       }
     }
@@ -346,12 +351,12 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, 
   return tma_encode_bf16(m, 2, base, dims, strides, box);
 }
 
-void proj_plan(int rows, int K, int F, ProjArgs &a, size_t *smem) {
+void proj_plan(int rows, int K, int F, ProjArgs &a, size_t *smem, bool split_k = true) {
   const int sms = std::max(1, dev_info().sms);
-  const int ftiles = F / kPTileF;
+  const int ftiles = (F + kPTileF - 1) / kPTileF;
   const int passes = (rows + kPMaxN - 1) / kPMaxN;
   const int kchunks = K / kPK;
-  const int want = std::max(1, sms / std::max(1, ftiles * passes));
+  const int want = split_k ? std::max(1, sms / std::max(1, ftiles * passes)) : 1;
   int splits = 1;
   for (int s = std::min(want, kchunks); s >= 1; --s)
     if (kchunks % s == 0) {
@@ -361,6 +366,7 @@ void proj_plan(int rows, int K, int F, ProjArgs &a, size_t *smem) {
   a.rows = rows;
   a.K = K;
   a.F = F;
+  a.dev_rows = nullptr;
   a.splits = splits;
   a.kper = K / splits;
   a.box_rows = std::min(kPMaxN, (rows + 15) & ~15);
@@ -402,6 +408,31 @@ bd_status proj_launch(int rows, int K, int F, const void *x, const void *w, void
   *splits = a.splits;
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
+
+}  // namespace
+
+// Logits of the masked rows for truncated sampling: out[r][v] = x[r] . w[v]
+// (fp32) for r < *dev_rows (at most rows_max), v < V; one K pass, no split.
+bd_status logits_tc(int rows_max, int K, int V, const void *x, const void *w, float *out,
+                    const int32_t *dev_rows, int32_t *dev_status, cudaStream_t st) {
+  if (rows_max < 1 || K < kPK || K % kPK || V < 1) return BD_ERR_UNSUPPORTED;
+  ProjArgs a;
+  size_t smem;
+  proj_plan(rows_max, K, V, a, &smem, false);
+  if (smem > (size_t)kPSmemLimit) return BD_ERR_UNSUPPORTED;
+  a.partial = out;
+  a.dev_rows = dev_rows;
+  a.dev_status = dev_status;
+  CUtensorMap mw, mx;
+  if (!make_map(&mw, w, K, V, kPK, kPTileF)) return BD_ERR_CUDA;
+  if (!make_map(&mx, x, K, rows_max, kPK, a.box_rows)) return BD_ERR_CUDA;
+  const dim3 grid((V + kPTileF - 1) / kPTileF, 1, (rows_max + kPMaxN - 1) / kPMaxN);
+  const cudaError_t e = launch_pdl(proj_tc_kernel, grid, dim3(kPThreads), smem, st, mw, mx, a);
+  count_launches(1);
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
+
+namespace {
 
 bool tc_ready() {
   const DevInfo d = dev_info();

@@ -62,13 +62,16 @@ class DenoiseEngine:
 
     def __init__(self, lm_head: torch.Tensor, caches, ctx_len, *, batch: int, block_len: int,
                  num_q_heads: int, threshold: float, max_ctx: int,
-                 temperature: float | None = None, seed: int = 0, decoder=None):
+                 temperature: float | None = None, seed: int = 0, decoder=None,
+                 top_k: int = 0, top_p: float = 1.0):
         """`threshold`: one number, or a [batch, block_len] array of
         per-position thresholds (region thresholds, greedy only:
         bd_confidence_commit_regions).
         `temperature` None: greedy confidence (bd_confidence_commit); a
         number: sampled tokens (bd_sample_commit) with key `seed` and a device
-        draw counter that every step advances, also under graph replay.
+        draw counter that every step advances, also under graph replay;
+        `top_k` > 0 or `top_p` < 1 truncate the sampled distribution
+        (bd_sample_commit_truncated).
         `decoder` (a DecoderStack sharing this engine's ctx_len): every step
         runs the layer stack over the current tokens (its attention replaces
         the single-layer attention call), and a finished block is run through
@@ -111,7 +114,12 @@ class DenoiseEngine:
         self.temperature = None if temperature is None else float(temperature)
         self.seed = int(seed)
         self.draw_counter = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.top_k, self.top_p = int(top_k), float(top_p)
+        self.truncated = self.top_k > 0 or self.top_p < 1.0
+        if self.truncated and self.temperature is None:
+            raise ValueError("top-k / top-p truncation needs a sampling temperature")
         query = (bd.bd_confidence_commit_workspace if self.temperature is None
+                 else bd.bd_sample_commit_truncated_workspace if self.truncated
                  else bd.bd_sample_commit_workspace)
         cws = query(code, batch, block_len, self.H, self.V)
         if cws == 0:
@@ -151,6 +159,12 @@ class DenoiseEngine:
             bd.bd_confidence_commit(h, self.W, self.T, self.tokens, self.p_max, self.argmax,
                                     n_committed_out, self.n_masked, self.conf_ws,
                                     dev_status=self.dev_status)
+        elif self.truncated:
+            bd.bd_sample_commit_truncated(h, self.W, self.T, self.temperature, self.top_k,
+                                          self.top_p, self.seed, self.draw_counter, self.tokens,
+                                          self.p_max, self.argmax, n_committed_out,
+                                          self.n_masked, self.conf_ws,
+                                          dev_status=self.dev_status)
         else:
             bd.bd_sample_commit(h, self.W, self.T, self.temperature, self.seed,
                                 self.draw_counter, self.tokens, self.p_max, self.argmax,

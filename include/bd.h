@@ -234,6 +234,46 @@ bd_status bd_sample_commit(bd_dtype dtype, int32_t batch, int32_t block_len, int
                            int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * bd_sample_commit_truncated -- bd_sample_commit with the other two settings
+ * of method step 6 switched on: top-k and top-p (nucleus) truncation, applied
+ * in that order to z = logits / temperature.
+ *
+ * Per masked position (b, i), pos = b * block_len + i:
+ *   theta_k  = the top_k-th largest z_v            (top_k > 0 and < vocab)
+ *   theta_p  = over the entries with z >= theta_k, sorted by z descending with
+ *              masses exp(z - max z): the z of the first entry at which the
+ *              running mass reaches top_p * (their total mass)  (top_p < 1)
+ *   kept     = { v : z_v >= max(theta_k, theta_p) }  (boundary ties kept)
+ *   sampled  = lowest v in kept attaining max (z_v - ln(-ln U_v)), U_v as in
+ *              bd_sample_commit (same counter, key and draw counter)
+ *   p_sel    = exp(z_sampled) / sum_{v in kept} exp(z_v)
+ * then the commit rule with p_sel as the confidence.  The boundary search is
+ * exact in the GPU's fp32 z; the masses it accumulates are exp(z - max z)
+ * rounded down to multiples of 2^-40.
+ *
+ *   top_k      >= 0; 0 (or >= vocab) disables it.
+ *   top_p      in (0, 1]; 1 disables it.  With both disabled this is
+ *              bd_sample_commit.
+ *   ws         at least bd_sample_commit_truncated_workspace() bytes: the
+ *              truncation needs each masked row's full distribution, so the
+ *              fp32 logits of the masked rows (batch * block_len * vocab * 4
+ *              bytes) pass through the workspace.
+ *   other arguments, results and limits as bd_sample_commit; top_k < 0 or
+ *   top_p outside (0, 1] (or NaN): BD_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------ */
+size_t bd_sample_commit_truncated_workspace(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                            int32_t hidden, int32_t vocab);
+
+bd_status bd_sample_commit_truncated(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                     int32_t hidden, int32_t vocab, const void *hidden_states,
+                                     const void *lm_head, float threshold, float temperature,
+                                     int32_t top_k, float top_p, uint64_t seed,
+                                     uint64_t *offset, int32_t *tokens, float *p_sel,
+                                     int32_t *sampled, int32_t *n_committed, int32_t *n_masked,
+                                     void *ws, size_t ws_bytes, int32_t *dev_status,
+                                     void *stream);
+
+/* ------------------------------------------------------------------------
  * bd_append_block_kv -- append a finished block's K/V to the paged cache
  * (novelty paragraph: block-causal structure lets earlier blocks' K/V be
  * reused).  For every sequence b with n_masked[b] == 0 (NULL = all):

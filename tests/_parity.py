@@ -211,12 +211,17 @@ class SampleRunner:
     """Runs bd_sample_commit step by step on device buffers."""
 
     def __init__(self, w: wl.Workload, W: np.ndarray, threshold: float, temperature: float,
-                 seed: int):
+                 seed: int, top_k: int = 0, top_p: float = 1.0):
+        """top_k > 0 or top_p < 1: bd_sample_commit_truncated."""
         self.w, self.T, self.temp, self.seed = w, threshold, temperature, seed
+        self.top_k, self.top_p = top_k, top_p
+        self.truncated = top_k > 0 or top_p < 1.0
         self.W = dev(W, w.dtype)
         B, L = w.batch, w.block_len
         code = bd.BD_F32 if w.dtype == "f32" else bd.BD_BF16
-        n = bd.bd_sample_commit_workspace(code, B, L, w.hidden, w.vocab)
+        query = (bd.bd_sample_commit_truncated_workspace if self.truncated
+                 else bd.bd_sample_commit_workspace)
+        n = query(code, B, L, w.hidden, w.vocab)
         assert n > 0
         self.ws = torch.empty(n, dtype=torch.uint8, device="cuda")
         self.tokens = torch.full((B, L), -1, dtype=torch.int32, device="cuda")
@@ -235,9 +240,15 @@ class SampleRunner:
         if offset is not None:
             self.offset.fill_(offset)
         before = int(self.offset.item())
-        bd.bd_sample_commit(h_dev, self.W, self.T, self.temp, self.seed, self.offset,
-                            self.tokens, self.p_sel, self.sampled, self.ncom, self.nmask,
-                            self.ws, dev_status=self.status)
+        if self.truncated:
+            bd.bd_sample_commit_truncated(h_dev, self.W, self.T, self.temp, self.top_k,
+                                          self.top_p, self.seed, self.offset, self.tokens,
+                                          self.p_sel, self.sampled, self.ncom, self.nmask,
+                                          self.ws, dev_status=self.status)
+        else:
+            bd.bd_sample_commit(h_dev, self.W, self.T, self.temp, self.seed, self.offset,
+                                self.tokens, self.p_sel, self.sampled, self.ncom, self.nmask,
+                                self.ws, dev_status=self.status)
         torch.cuda.synchronize()
         assert int(self.status.item()) == 0, bd.STATUS.get(int(self.status.item()))
         assert int(self.offset.item()) == before + 1      # the call advanced the counter
@@ -248,17 +259,24 @@ class SampleRunner:
 
 def lockstep_sampled_block(w: wl.Workload, W: np.ndarray, h_steps: np.ndarray, threshold: float,
                            temperature: float, seed: int, tokens0: np.ndarray | None = None,
-                           max_steps: int | None = None):
+                           max_steps: int | None = None, top_k: int = 0, top_p: float = 1.0):
     """Sampled denoising of one block (offset = step index) on the GPU, every
     step compared with the oracle's sampled step on the same token state.
 
     Exemptions: a drawn token may differ where the oracle's two best
     perturbed keys are within 1e-3; a commit decision may differ there, where
     |p_sel - T| < 1e-3, or where the fallback's two best candidates are
-    within 1e-3.  The comparison then continues from the GPU's tokens."""
+    within 1e-3.  With truncation, also where either drawn token lies within
+    1e-3 of the oracle's threshold theta (its membership of the kept set can
+    flip with the GPU's fp32 logits), and the row's p_sel where the entries
+    within 1e-3 of theta hold 1e-3 of the kept mass or more, or where the
+    top-p running mass passes p within 1e-3.  The comparison then continues
+    from the GPU's tokens."""
     B, L = w.batch, w.block_len
+    T = np.broadcast_to(np.asarray(threshold, np.float64), (B, L))
     tol = tol_for(w.dtype)
-    run = SampleRunner(w, W, threshold, temperature, seed)
+    truncated = top_k > 0 or top_p < 1.0
+    run = SampleRunner(w, W, threshold, temperature, seed, top_k, top_p)
     tokens = np.full((B, L), -1, np.int64) if tokens0 is None else tokens0.astype(np.int64)
     run.set_tokens(tokens)
     Wd = W.astype(np.float64)
@@ -269,21 +287,31 @@ def lockstep_sampled_block(w: wl.Workload, W: np.ndarray, h_steps: np.ndarray, t
         active = (tokens == -1).any(axis=1)
         g_tok, g_p, g_s, g_nc, g_nm = run.step(dev(h_steps[s], w.dtype), offset=s)
         exp_tok, o_p, o_s, chosen, res, (bi, ii) = oracle.denoise_step_sampled(
-            tokens, h_steps[s].astype(np.float64), Wd, threshold, temperature, seed, s)
+            tokens, h_steps[s].astype(np.float64), Wd, threshold, temperature, seed, s,
+            top_k=top_k, top_p=top_p)
         stats.rows_checked += len(bi)
         unmasked = tokens != -1
         assert (g_p[unmasked] == -1).all() and (g_s[unmasked] == -1).all()
         key_exempt = res["key_gap"] < EXEMPT
+        p_exempt = np.zeros(len(bi), bool)
+        if truncated:
+            hr = h_steps[s][bi, ii].astype(np.float64)
+            z_g = (hr * Wd[g_s[bi, ii]]).sum(axis=1) / temperature
+            z_o = (hr * Wd[o_s[bi, ii]]).sum(axis=1) / temperature
+            th = res["theta"]
+            band_tok = (np.abs(z_g - th) < EXEMPT) | (np.abs(z_o - th) < EXEMPT)
+            p_exempt = (res["band_mass"] >= EXEMPT) | (res["p_margin"] < EXEMPT)
+            key_exempt = key_exempt | band_tok | p_exempt
         same = g_s[bi, ii] == o_s[bi, ii]
         bad = ~same & ~key_exempt
         stats.argmax_mismatch_nonexempt += int(bad.sum())
         assert not bad.any(), f"sampled token mismatch at non-exempt rows, step {s}"
-        err = np.abs(g_p[bi, ii] - o_p[bi, ii])[same]
+        err = np.abs(g_p[bi, ii] - o_p[bi, ii])[same & ~p_exempt]
         if err.size:
             stats.max_pmax_err = max(stats.max_pmax_err, float(err.max()))
             assert err.max() <= tol, f"p_sel error {err.max()} > {tol} at step {s}"
         exempt_pos = np.zeros((B, L), bool)
-        exempt_pos[bi, ii] = key_exempt | (np.abs(o_p[bi, ii] - threshold) < EXEMPT)
+        exempt_pos[bi, ii] = key_exempt | (np.abs(o_p[bi, ii] - T[bi, ii]) < EXEMPT)
         for b in range(B):
             mb = tokens[b] == -1
             if mb.any() and not (o_p[b][mb] >= T[b][mb]).any() and mb.sum() > 1:

@@ -93,6 +93,20 @@ def test_region_commit_checks_arguments_on_the_host(lib):
     assert st == 1
 
 
+def test_truncated_sample_commit_checks_arguments_on_the_host(lib):
+    assert bd.bd_sample_commit_truncated_workspace(bd.BD_BF16, 1, 32, 2048, 151936) >= \
+        bd.bd_sample_commit_workspace(bd.BD_BF16, 1, 32, 2048, 151936) + 32 * 151936 * 4
+    assert bd.bd_sample_commit_truncated_workspace(bd.BD_BF16, 1, 33, 2048, 151936) == 0
+    f = lib.bd_sample_commit_truncated
+    for k, p in ((-1, 0.9), (5, 0.0), (5, 1.5), (5, float("nan")), (5, -0.5)):
+        st = f(1, 1, 32, 2048, 1000, None, None, 0.9, 1.0, k, p, 1, 4096, None, None, None,
+               None, None, None, 0, None, None)
+        assert st == 1
+    st = f(1, 1, 32, 2048, 1000, None, None, 0.9, 1.0, 5, 0.9, 1, None, None, None, None,
+           None, None, None, 0, None, None)              # no draw counter
+    assert st == 1
+
+
 def test_decoder_calls_check_arguments_on_the_host(lib):
     # shapes the projection kernels cannot take return a zero workspace
     assert bd.bd_qkv_projection_workspace(256, 2048, 16, 8, 128) > 0

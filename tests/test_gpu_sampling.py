@@ -1,7 +1,7 @@
 """GPU parity of the sampling reading (bd_sample_commit) against the oracle.
 
 The oracle draws with the same counter-based generator (Philox-4x64-10 at
-counter (v, position / 4, offset, 0)), so sampled tokens are compared token by
+counter (v, position / 8, offset, 0)), so sampled tokens are compared token by
 token; see tests/_parity.py for the exemption rule.  A chi-square test checks
 the GPU's draws against softmax directly, independent of the oracle.
 """
@@ -49,7 +49,7 @@ def test_sampled_block_bf16_ragged_vocab(temperature):
 
 def test_sampled_sparse_masked_positions():
     # masked positions scattered over position groups: the kernel's Philox
-    # blocks are shared only by rows of one group of four positions
+    # blocks are shared only by rows of one group of eight positions
     w = SMALL_BF16
     W = wl.lm_head(w)
     h, _ = wl.planted_hidden(w, W, 0, a_max=30.0)
