@@ -9,11 +9,11 @@ from .bd_oracle import (MASK, block_mask, block_attention, current_block_attenti
                         paged_read, append_block, philox4x64_10, uniform01,
                         sample_confidence, denoise_step_sampled, round_bf16, rms_norm,
                         embed, decoder_layer, decoder_forward, truncation_threshold,
-                        sample_confidence_truncated)
+                        sample_confidence_truncated, silu, mlp_residual)
 
 __all__ = ["MASK", "block_mask", "block_attention", "current_block_attention",
            "confidence", "commit", "denoise_step", "decode_block",
            "paged_read", "append_block", "philox4x64_10", "uniform01",
            "sample_confidence", "denoise_step_sampled", "round_bf16", "rms_norm",
            "embed", "decoder_layer", "decoder_forward", "truncation_threshold",
-           "sample_confidence_truncated"]
+           "sample_confidence_truncated", "silu", "mlp_residual"]

@@ -512,13 +512,35 @@ def embed(tokens, E, e_mask):
     return out
 
 
-def decoder_layer(x, wqkv, wo, k_cache, v_cache, num_q_heads, num_kv_heads, eps=1e-6):
+def silu(g):
+    """g * sigmoid(g)."""
+    return g / (1.0 + np.exp(-g))
+
+
+def mlp_residual(x, w_gate_up, w_down, eps=1e-6):
+    """Optional gated MLP after the attention residual (SwiGLU, the MLP of the
+    Qwen3 family that SDAR derives from; the pages give no layer internals):
+        xn = bf16(RMSNorm(x)); [g | u] = xn W_gu^T (gate rows first)
+        a  = bf16(silu(g) * u);  x <- x + a W_down^T
+    x [L', H] fp64; w_gate_up [2 I, H]; w_down [H, I]."""
+    x = np.asarray(x, dtype=np.float64)
+    Wgu = np.asarray(w_gate_up, dtype=np.float64)
+    I = Wgu.shape[0] // 2
+    xn = round_bf16(rms_norm(x, eps))
+    gu = xn @ Wgu.T
+    a = round_bf16(silu(gu[:, :I]) * gu[:, I:])
+    return x + a @ np.asarray(w_down, dtype=np.float64).T
+
+
+def decoder_layer(x, wqkv, wo, k_cache, v_cache, num_q_heads, num_kv_heads, eps=1e-6,
+                  w_gate_up=None, w_down=None):
     """One layer for one sequence's block.
 
     x [L', H] (fp64 residual stream); wqkv [(Hq + 2 Hkv) D, H]; wo [H, Hq D];
-    k_cache, v_cache [C, Hkv, D] (this layer's cached tokens).  Returns
-    (new x, k_blk, v_blk) where k_blk, v_blk [L', Hkv, D] are the block's
-    keys and values of this layer (bf16 values, what a finished block appends).
+    k_cache, v_cache [C, Hkv, D] (this layer's cached tokens); optionally the
+    MLP weights (mlp_residual).  Returns (new x, k_blk, v_blk) where k_blk,
+    v_blk [L', Hkv, D] are the block's keys and values of this layer (bf16
+    values, what a finished block appends).
     """
     x = np.asarray(x, dtype=np.float64)
     L = x.shape[0]
@@ -531,19 +553,22 @@ def decoder_layer(x, wqkv, wo, k_cache, v_cache, num_q_heads, num_kv_heads, eps=
     v = qkv[:, (Hq + Hkv) * D:].reshape(L, Hkv, D)
     a = round_bf16(current_block_attention(q, k_cache, v_cache, k, v))
     x = x + a.reshape(L, Hq * D) @ np.asarray(wo, dtype=np.float64).T
+    if w_gate_up is not None:
+        x = mlp_residual(x, w_gate_up, w_down, eps)
     return x, k, v
 
 
 def decoder_forward(tokens, E, e_mask, layers, caches, num_q_heads, num_kv_heads, eps=1e-6):
     """The layer stack over one sequence's current block.
 
-    tokens [L']; layers = [(wqkv, wo), ...]; caches = [(k_cache, v_cache), ...]
-    per layer.  Returns (x after the last layer [L', H], [k_blk per layer],
-    [v_blk per layer])."""
+    tokens [L']; layers = [(wqkv, wo), ...] or [(wqkv, wo, w_gate_up, w_down),
+    ...] with the MLP; caches = [(k_cache, v_cache), ...] per layer.  Returns
+    (x after the last layer [L', H], [k_blk per layer], [v_blk per layer])."""
     x = embed(tokens, E, e_mask)
     ks, vs = [], []
-    for (wqkv, wo), (kc, vc) in zip(layers, caches):
-        x, k, v = decoder_layer(x, wqkv, wo, kc, vc, num_q_heads, num_kv_heads, eps)
+    for lw, (kc, vc) in zip(layers, caches):
+        x, k, v = decoder_layer(x, lw[0], lw[1], kc, vc, num_q_heads, num_kv_heads, eps,
+                                *lw[2:4])
         ks.append(k)
         vs.append(v)
     return x, ks, vs

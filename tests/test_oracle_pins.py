@@ -572,6 +572,45 @@ def test_decoder_layer_matches_torch_composition():
     assert np.array_equal(k2.reshape(L, -1), k.numpy())
 
 
+def test_silu_closed_forms():
+    g = np.array([0.0, 1.0, -1.0, 30.0, -30.0])
+    s = oracle.silu(g)
+    assert s[0] == 0.0
+    np.testing.assert_allclose(s[1], 1.0 / (1.0 + np.exp(-1.0)), rtol=1e-15)
+    np.testing.assert_allclose(s[1] - s[2], 1.0, rtol=1e-15)   # silu(g) - silu(-g) = g
+    np.testing.assert_allclose(s[3], 30.0, rtol=1e-12)
+    assert abs(s[4]) < 1e-11
+
+
+def test_mlp_zero_gate_or_down_is_identity_and_torch_composition():
+    rng = np.random.default_rng(37)
+    L, H, I = 5, 24, 40
+    x = rng.standard_normal((L, H))
+    wgu = rng.standard_normal((2 * I, H)) * 0.3
+    wd = rng.standard_normal((H, I)) * 0.3
+    # silu(0) = 0: a zero gate makes the MLP add nothing, whatever the up rows
+    z = wgu.copy()
+    z[:I] = 0.0
+    assert np.array_equal(oracle.mlp_residual(x, z, wd), x)
+    assert np.array_equal(oracle.mlp_residual(x, wgu, np.zeros_like(wd)), x)
+    # torch: F.silu, F.linear, with the bf16 roundings at the same points
+
+    def bf(t):
+        return t.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+
+    xt = torch.from_numpy(x)
+    xn = bf(F.rms_norm(xt, (H,), eps=1e-6))
+    g, u = F.linear(xn, torch.from_numpy(wgu)).split([I, I], dim=-1)
+    ref = xt + F.linear(bf(F.silu(g) * u), torch.from_numpy(wd))
+    np.testing.assert_allclose(oracle.mlp_residual(x, wgu, wd), ref.numpy(), rtol=1e-9,
+                               atol=1e-9)
+    # in the layer: after the attention residual
+    _, wqkv, wo, kc, vc = _layer_inputs(rng, L, 7, 4, 2, 8, H)
+    xa, k, v = oracle.decoder_layer(x, wqkv, wo, kc, vc, 4, 2)
+    xm, k2, v2 = oracle.decoder_layer(x, wqkv, wo, kc, vc, 4, 2, 1e-6, wgu, wd)
+    assert np.array_equal(xm, oracle.mlp_residual(xa, wgu, wd)) and np.array_equal(k, k2)
+
+
 def test_decoder_forward_composes_layers():
     rng = np.random.default_rng(36)
     V, H, Hq, Hkv, D, L, C = 11, 16, 2, 1, 8, 4, 3
