@@ -57,6 +57,9 @@ def _args():
                     help="region thresholds by block position, e.g. 0.99:8,0.7:16,0.9:8 "
                          "(T:positions, summing to the block length): one more sweep line")
     ap.add_argument("--blocks", type=int, default=0, help="blocks per sweep decode")
+    ap.add_argument("--mlp", action="store_true",
+                    help="longctx_b8: add the gated MLP (SwiGLU, intermediate 6144) to every "
+                         "decoder layer")
     ap.add_argument("--ar-compare", action="store_true",
                     help="block diffusion vs token-by-token decoding on the same shapes")
     ap.add_argument("--ar-threshold", type=float, default=0.95)
@@ -768,10 +771,12 @@ def run_decoder(a):
     E = wl.embed_table(w)
     em = wl.mask_embedding(w)
     lw = [wl.layer_weights(w, l) for l in range(w.num_layers)]
+    if a.mlp:
+        lw = [t + wl.mlp_weights(w, l) for l, t in enumerate(lw)]
     dev = lambda x: torch.from_numpy(x).to("cuda", bf)
     ctx = torch.from_numpy(plen.astype(np.int32)).cuda()
     max_ctx = int(cap.max())
-    stack = DecoderStack(dev(E), dev(em), [(dev(x), dev(y)) for x, y in lw], caches, ctx,
+    stack = DecoderStack(dev(E), dev(em), [tuple(dev(x) for x in t) for t in lw], caches, ctx,
                          batch=w.batch, block_len=L, num_q_heads=w.num_q_heads, max_ctx=max_ctx)
     eng = DenoiseEngine(dev(W), caches, plen, batch=w.batch, block_len=L,
                         num_q_heads=w.num_q_heads, threshold=w.threshold, max_ctx=max_ctx,
@@ -925,6 +930,8 @@ def run_decoder(a):
         "warmup": warm, "ms_per_step": ms / a.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": _config(w, {"parallelism": "single GPU", "layers": w.num_layers,
+                              "mlp": (f"SwiGLU, intermediate {wl.MLP_INTER}" if a.mlp
+                                      else "none (the plainest reading)"),
                               "blocks_timed": a.steps,
                               "denoise_steps_issued": steps_issued // a.steps,
                               "check_every": a.check_every, "cuda_graphs": use_graphs,

@@ -32,7 +32,8 @@ EXPORTS = ("bd_block_attention_workspace", "bd_block_attention",
            "bd_embed_rmsnorm", "bd_qkv_projection_workspace", "bd_qkv_projection",
            "bd_out_projection_workspace", "bd_out_projection_residual",
            "bd_append_block_kv_layers", "bd_confidence_commit_regions",
-           "bd_sample_commit_truncated_workspace", "bd_sample_commit_truncated")
+           "bd_sample_commit_truncated_workspace", "bd_sample_commit_truncated",
+           "bd_mlp_workspace", "bd_mlp_residual")
 
 
 class BDError(RuntimeError):
@@ -98,6 +99,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                                      c_void_p, c_void_p, c_void_p, c_void_p,
                                                      c_void_p, c_void_p, c_void_p, c_size_t,
                                                      c_void_p, c_void_p]),
+            "bd_mlp_workspace": (c_size_t, [c_int32] * 3),
+            "bd_mlp_residual": (c_int32, [c_int32] * 3 + [c_void_p, c_void_p, c_void_p, c_float,
+                                                         c_void_p, c_void_p, c_void_p, c_size_t,
+                                                         c_void_p, c_void_p]),
             "bd_embed_rmsnorm": (c_int32, [c_int32, c_int32, c_int32, c_void_p, c_void_p,
                                            c_void_p, c_float, c_void_p, c_void_p, c_void_p,
                                            c_void_p]),
@@ -352,6 +357,28 @@ def bd_out_projection_residual(attn, w_o, x, xn, ws, eps=1e-6, dev_status=None, 
         _ptr(ws, name="ws"), ws.numel() * ws.element_size(),
         _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check("bd_out_projection_residual", st)
+
+
+def bd_mlp_workspace(rows, hidden, inter) -> int:
+    return int(load().bd_mlp_workspace(rows, hidden, inter))
+
+
+def bd_mlp_residual(xn, w_gate_up, w_down, x, xn_out, ws, eps=1e-6, dev_status=None,
+                    stream=None):
+    """x += bf16(silu(g) * u) w_down^T with [g | u] = xn w_gate_up^T, then
+    xn_out = bf16(RMSNorm(x)) (see bd.h)."""
+    H = w_down.shape[0]
+    inter = w_down.shape[1]
+    if tuple(w_gate_up.shape) != (2 * inter, H):
+        raise ValueError("w_gate_up must be [2 * inter, hidden]")
+    rows = x.numel() // H
+    st = load().bd_mlp_residual(
+        rows, H, inter, _ptr(xn, torch.bfloat16, "xn"),
+        _ptr(w_gate_up, torch.bfloat16, "w_gate_up"), _ptr(w_down, torch.bfloat16, "w_down"),
+        float(eps), _ptr(x, torch.float32, "x"), _ptr(xn_out, torch.bfloat16, "xn_out"),
+        _ptr(ws, name="ws"), ws.numel() * ws.element_size(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("bd_mlp_residual", st)
 
 
 def bd_append_block_kv_layers(kvs, k_blk, v_blk, ctx_len, n_masked=None, dev_status=None,

@@ -9,7 +9,9 @@
 //   per layer: xn = bf16(x / sqrt(mean(x^2) + eps))     (no gain)
 //              [q | k | v] = bf16(xn Wqkv^T)
 //              a = bf16(block attention of q over the layer's cache + k, v)
-//              x = x + a Wo^T                           (no MLP)
+//              x = x + a Wo^T
+//   optional MLP:  xn = bf16(RMSNorm(x)); [g | u] = xn Wgu^T
+//                  x = x + bf16(silu(g) * u) Wdown^T      (SwiGLU, Qwen3 family)
 // x is kept in fp32; everything stored between kernels except x is bf16.
 //
 // Kernels:
@@ -24,6 +26,10 @@
 //   qkv_finish_kernel  sum of the partials -> bf16 q, k, v
 //   out_finish_kernel  one CTA per row: x += sum of the partials, then the
 //                      next layer's xn
+//   swiglu_finish_kernel  (optional MLP, bd_mlp_residual) act = bf16(silu(g) * u)
+//                      from the partials of the gate/up projection; the down
+//                      projection then goes through proj_tc_kernel and
+//                      out_finish_kernel like the output projection
 //   append_layers_kernel / ctx_bump_kernel: a finished block's K/V of every
 //                      layer into the per-layer caches, then ctx += L' once
 // Every mbarrier wait is bounded (1 s); on expiry the kernel records
@@ -187,6 +193,36 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const float *partial, i
   else if (f < fq + fk) dst = k + (size_t)row * fk + (f - fq);
   else dst = v + (size_t)row * fk + (f - fq - fk);
   store_bf16x4(dst, acc);
+}
+
+// act = bf16(silu(g) * u) from the split partials of [g | u] (gate rows
+// first); one thread per 4 features of the intermediate.
+__global__ void __launch_bounds__(256) swiglu_finish_kernel(const float *partial, int splits,
+                                                            int rows, int inter,
+                                                            __nv_bfloat16 *act) {
+  pdl_trigger();
+  pdl_wait();
+  const size_t e = 4 * ((size_t)blockIdx.x * blockDim.x + threadIdx.x);
+  if (e >= (size_t)rows * inter) return;
+  const int row = (int)(e / inter), j = (int)(e % inter);
+  const size_t F = 2 * (size_t)inter;
+  float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+  for (int s = 0; s < splits; ++s) {
+    const float *base = partial + ((size_t)s * rows + row) * F;
+    const float4 pg = *reinterpret_cast<const float4 *>(base + j);
+    const float4 pu = *reinterpret_cast<const float4 *>(base + inter + j);
+    g.x += pg.x;
+    g.y += pg.y;
+    g.z += pg.z;
+    g.w += pg.w;
+    u.x += pu.x;
+    u.y += pu.y;
+    u.z += pu.z;
+    u.w += pu.w;
+  }
+  const auto silu = [](float x) { return x / (1.f + __expf(-x)); };
+  store_bf16x4(act + (size_t)row * inter + j,
+               make_float4(silu(g.x) * u.x, silu(g.y) * u.y, silu(g.z) * u.z, silu(g.w) * u.w));
 }
 
 // ---------------------------------------------------------------------------
@@ -522,7 +558,8 @@ bool kv_layer_ok(const bd_paged_kv &kv, const bd_paged_kv &ref) {
 bool preload_decoder() {
   return preload_kernel(embed_norm_kernel, false) && preload_kernel(out_finish_kernel, false) &&
          preload_kernel(qkv_finish_kernel, false) && preload_kernel(proj_tc_kernel, true) &&
-         preload_kernel(append_layers_kernel, false) && preload_kernel(ctx_bump_kernel, false);
+         preload_kernel(append_layers_kernel, false) && preload_kernel(ctx_bump_kernel, false) &&
+         preload_kernel(swiglu_finish_kernel, false);
 }
 
 }  // namespace bd
@@ -616,6 +653,62 @@ BD_API bd_status bd_out_projection_residual(int32_t rows, int32_t in_features, i
   const cudaError_t e = launch_pdl(out_finish_kernel, dim3(rows), dim3(kRowThreads), 0, st,
                                    static_cast<const float *>(ws), splits, (int)rows, (int)hidden,
                                    eps, x, static_cast<__nv_bfloat16 *>(xn));
+  count_launches(1);
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
+
+// Workspace of bd_mlp_residual: the activation, then the partials of the
+// larger of its two projections (they run one after the other).
+static size_t mlp_ws(int rows, int hidden, int inter, size_t *act_bytes) {
+  *act_bytes = align_up((size_t)rows * inter * 2, 256);
+  return *act_bytes + std::max(proj_ws_bytes(rows, hidden, 2 * inter),
+                               proj_ws_bytes(rows, inter, hidden));
+}
+
+static bool mlp_shape_ok(int rows, int hidden, int inter) {
+  return inter >= 64 && inter % 64 == 0 && inter <= (1 << 15) &&
+         proj_shape_ok(rows, hidden, 2 * inter) && proj_shape_ok(rows, inter, hidden) &&
+         hidden <= 4 * kMaxVec * kRowThreads;
+}
+
+BD_API size_t bd_mlp_workspace(int32_t rows, int32_t hidden, int32_t inter) {
+  if (!mlp_shape_ok(rows, hidden, inter)) return 0;
+  preload_all();
+  size_t act;
+  return mlp_ws(rows, hidden, inter, &act);
+}
+
+BD_API bd_status bd_mlp_residual(int32_t rows, int32_t hidden, int32_t inter, const void *xn,
+                                 const void *w_gate_up, const void *w_down, float eps, float *x,
+                                 void *xn_out, void *ws, size_t ws_bytes, int32_t *dev_status,
+                                 void *stream) {
+  if (!mlp_shape_ok(rows, hidden, inter)) return BD_ERR_INVALID_ARG;
+  if (!xn || !w_gate_up || !w_down || !x || !xn_out || !(eps >= 0.f) || isinf(eps))
+    return BD_ERR_INVALID_ARG;
+  if (!aligned16(xn) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(x) ||
+      !aligned16(xn_out))
+    return BD_ERR_INVALID_ARG;
+  if (!preload_all()) return BD_ERR_CUDA;
+  if (!tc_ready()) return BD_ERR_UNSUPPORTED;
+  size_t act_bytes;
+  const size_t need = mlp_ws(rows, hidden, inter, &act_bytes);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return BD_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  __nv_bfloat16 *act = static_cast<__nv_bfloat16 *>(ws);
+  float *part = reinterpret_cast<float *>(static_cast<char *>(ws) + act_bytes);
+  int splits = 0;
+  bd_status s = proj_launch(rows, hidden, 2 * inter, xn, w_gate_up, part, dev_status, st, &splits);
+  if (s != BD_OK) return s;
+  const size_t quads = (size_t)rows * inter / 4;
+  cudaError_t e = launch_pdl(swiglu_finish_kernel, dim3((unsigned)((quads + 255) / 256)),
+                             dim3(256), 0, st, (const float *)part, splits, (int)rows,
+                             (int)inter, act);
+  count_launches(1);
+  if (e != cudaSuccess) return BD_ERR_CUDA;
+  s = proj_launch(rows, inter, hidden, act, w_down, part, dev_status, st, &splits);
+  if (s != BD_OK) return s;
+  e = launch_pdl(out_finish_kernel, dim3(rows), dim3(kRowThreads), 0, st, (const float *)part,
+                 splits, (int)rows, (int)hidden, eps, x, static_cast<__nv_bfloat16 *>(xn_out));
   count_launches(1);
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }

@@ -240,15 +240,16 @@ class DecoderStack:
     workload: embedding + RMSNorm, then per layer QKV projection, block
     attention over that layer's paged cache and output projection with the
     residual add (bd_embed_rmsnorm, bd_qkv_projection, bd_block_attention,
-    bd_out_projection_residual).  All layers share one page table and one
-    ctx_len; a finished block's K/V of every layer is appended by one
-    bd_append_block_kv_layers call."""
+    bd_out_projection_residual), and the gated MLP (bd_mlp_residual) for
+    layers given as (wqkv, wo, w_gate_up, w_down).  All layers share one page
+    table and one ctx_len; a finished block's K/V of every layer is appended
+    by one bd_append_block_kv_layers call."""
 
     def __init__(self, embed: torch.Tensor, mask_embed: torch.Tensor, layers, caches, ctx_len,
                  *, batch: int, block_len: int, num_q_heads: int, max_ctx: int,
                  eps: float = 1e-6):
         self.E, self.e_mask = embed, mask_embed
-        self.layers = list(layers)                 # [(wqkv, wo)] bf16 on the device
+        self.layers = list(layers)                 # [(wqkv, wo[, w_gate_up, w_down])] bf16
         self.caches = list(caches)                 # [PagedCache] sharing one page table
         assert len(self.layers) == len(self.caches)
         self.ctx_len = ctx_len
@@ -275,7 +276,13 @@ class DecoderStack:
                                               self.max_ctx)
         if qws == 0 or ows == 0:
             raise ValueError("unsupported decoder shape")
-        self.ws = torch.empty(max(qws, ows, 1), dtype=torch.uint8, device=dev)
+        mws = 0
+        for lw in self.layers:
+            if len(lw) > 2:
+                mws = max(mws, bd.bd_mlp_workspace(rows, self.H, lw[3].shape[1]))
+                if mws == 0:
+                    raise ValueError("unsupported MLP shape")
+        self.ws = torch.empty(max(qws, ows, mws, 1), dtype=torch.uint8, device=dev)
         self.attn_ws = torch.empty(max(aws, 1), dtype=torch.uint8, device=dev)
         # every layer addresses its pool through one shared page table
         for c in self.caches[1:]:
@@ -290,7 +297,8 @@ class DecoderStack:
         self.x, self.k, self.v."""
         bd.bd_embed_rmsnorm(tokens, self.E, self.e_mask, self.x, self.xn, self.eps,
                             self.dev_status)
-        for l, (wqkv, wo) in enumerate(self.layers):
+        for l, lw in enumerate(self.layers):
+            wqkv, wo = lw[0], lw[1]
             bd.bd_qkv_projection(self.xn, wqkv, self.q, self.k[l], self.v[l], self.ws,
                                  self.dev_status)
             bd.bd_block_attention(self.kvs[l], self.ctx_len, attn_tokens, self.q, self.k[l],
@@ -298,6 +306,9 @@ class DecoderStack:
                                   dev_status=self.dev_status)
             bd.bd_out_projection_residual(self.attn, wo, self.x, self.xn, self.ws, self.eps,
                                           self.dev_status)
+            if len(lw) > 2:
+                bd.bd_mlp_residual(self.xn, lw[2], lw[3], self.x, self.xn, self.ws, self.eps,
+                                   self.dev_status)
 
     def append(self, n_masked=None):
         """Append the block K/V of the last forward to every layer's cache."""

@@ -43,6 +43,8 @@ PAGE_SIZE = 64
 S_Q, S_KBLK, S_VBLK, S_KPRE, S_VPRE, S_W = 1, 2, 3, 4, 5, 6
 S_TGT, S_AMP, S_NOISE, S_PERM, S_PLEN = 7, 8, 9, 10, 11
 S_EMB, S_EMASK, S_WQKV, S_WO = 12, 13, 14, 15
+S_WGU, S_WDOWN = 16, 17
+MLP_INTER = 6144          # SDAR-1.7B (Qwen3-1.7B family) intermediate size
 
 
 @dataclasses.dataclass(frozen=True)
@@ -227,4 +229,13 @@ def layer_weights(w: Workload, layer: int, seed: int = 0):
     wo = normal_f32((w.hidden, w.num_q_heads * w.head_dim), seed, w.wid, S_WO, layer,
                     std=w.w_std)
     return to_storage(wqkv, w.dtype), to_storage(wo, w.dtype)
+
+
+def mlp_weights(w: Workload, layer: int, inter: int = MLP_INTER, seed: int = 0):
+    """Weights of the optional gated MLP of one layer, N(0, w_std^2), storage
+    precision: w_gate_up [2 inter, H] (gate rows, then up rows) and
+    w_down [H, inter]."""
+    wgu = normal_f32((2 * inter, w.hidden), seed, w.wid, S_WGU, layer, std=w.w_std)
+    wd = normal_f32((w.hidden, inter), seed, w.wid, S_WDOWN, layer, std=w.w_std)
+    return to_storage(wgu, w.dtype), to_storage(wd, w.dtype)
 

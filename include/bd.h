@@ -340,6 +340,26 @@ bd_status bd_out_projection_residual(int32_t rows, int32_t in_features, int32_t 
                                      void *xn, void *ws, size_t ws_bytes, int32_t *dev_status,
                                      void *stream);
 
+/* bd_mlp_residual -- optional gated MLP of a decoder layer, after the
+ * attention residual.  The pages give no layer internals; the decoder starts
+ * from SDAR-1.7B-Chat (reproduction paragraph), a Qwen3-family model, whose
+ * MLP is SwiGLU:
+ *   [g | u] = xn w_gate_up^T     (xn = bf16(RMSNorm(x)), as
+ *                                 bd_out_projection_residual leaves it)
+ *   a       = bf16(silu(g) * u), silu(g) = g / (1 + exp(-g))
+ *   x      += a w_down^T         (fp32), then xn_out = bf16(RMSNorm(x))
+ *   xn [rows][hidden] bf16 in; xn_out [rows][hidden] bf16 out (may be xn);
+ *   w_gate_up [2 inter][hidden] bf16, gate rows first; w_down [hidden][inter]
+ *   bf16; x [rows][hidden] float in/out.
+ *   ws: at least bd_mlp_workspace() bytes, 256-byte aligned.
+ * Limits: inter % 64 == 0, 64 <= inter <= 32768; hidden % 128 == 0,
+ *         hidden <= 4096; pointers 16-byte aligned. */
+size_t bd_mlp_workspace(int32_t rows, int32_t hidden, int32_t inter);
+bd_status bd_mlp_residual(int32_t rows, int32_t hidden, int32_t inter, const void *xn,
+                          const void *w_gate_up, const void *w_down, float eps, float *x,
+                          void *xn_out, void *ws, size_t ws_bytes, int32_t *dev_status,
+                          void *stream);
+
 /* bd_append_block_kv_layers -- bd_append_block_kv for num_layers layers that
  * share one page table and one ctx_len (kv: host array of num_layers structs
  * with equal dtype, geometry and page_table; only the pools differ).

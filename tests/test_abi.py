@@ -107,6 +107,18 @@ def test_truncated_sample_commit_checks_arguments_on_the_host(lib):
     assert st == 1
 
 
+def test_mlp_call_checks_arguments_on_the_host(lib):
+    assert bd.bd_mlp_workspace(32, 2048, 6144) > 32 * 6144 * 2
+    for rows, H, inter in ((0, 2048, 6144), (32, 2000, 6144), (32, 2048, 100), (32, 8192, 64)):
+        assert bd.bd_mlp_workspace(rows, H, inter) == 0
+    st = lib.bd_mlp_residual(32, 2048, 6144, None, None, None, 1e-6, None, None, None, 0, None,
+                             None)
+    assert st == 1
+    st = lib.bd_mlp_residual(32, 2048, 6144, 4096, 4096, 4096, -1.0, 4096, 4096, 4096, 1 << 30,
+                             None, None)                 # negative eps
+    assert st == 1
+
+
 def test_decoder_calls_check_arguments_on_the_host(lib):
     # shapes the projection kernels cannot take return a zero workspace
     assert bd.bd_qkv_projection_workspace(256, 2048, 16, 8, 128) > 0

@@ -7,8 +7,9 @@ bf16 rounding step (the GPU accumulates in fp32, the oracle in fp64, and a
 value near a rounding boundary can land on either side) plus the fp32
 accumulation error of a K-term dot product: |d| <= 2^-7 |ref| +
 2^-18 sum_k |x_k w_k| + 1e-6.  The fp32 residual stream after a layer stack is
-held to max-abs 2e-2 (the bf16 tolerance of the target statement); the
-observed error is printed.
+held to max-abs 2e-2 (the bf16 tolerance of the target statement), or to two
+bf16 steps at the stream's largest magnitude where that is larger (with the
+MLP the stream grows past 4); the observed error is printed.
 """
 import numpy as np
 import pytest
@@ -107,8 +108,36 @@ def test_out_projection_residual_matches_oracle(rows, Fin, H):
     _close_bf16(xn.float().cpu().numpy(), oracle.round_bf16(oracle.rms_norm(got)))
 
 
-def _stack_setup(w, plen, seed=0):
-    """Device copies of a workload's decoder inputs plus a per-layer paged cache."""
+@pytest.mark.parametrize("rows,H,inter", [(256, 2048, 6144), (300, 2048, 6144), (5, 256, 512),
+                                          (40, 384, 64)])
+def test_mlp_residual_matches_oracle(rows, H, inter):
+    rng = np.random.default_rng(45)
+    x0 = rng.standard_normal((rows, H)).astype(np.float32)
+    xn = wl.round_bf16(oracle.rms_norm(x0.astype(np.float64)).astype(np.float32))
+    wgu = wl.round_bf16((rng.standard_normal((2 * inter, H)) * 0.02).astype(np.float32))
+    wd = wl.round_bf16((rng.standard_normal((H, inter)) * 0.02).astype(np.float32))
+    x = torch.from_numpy(x0).cuda()
+    xn_d = _bf(xn)
+    ws = torch.empty(bd.bd_mlp_workspace(rows, H, inter), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.bd_mlp_residual(xn_d, _bf(wgu), _bf(wd), x, xn_d, ws, 1e-6, st)   # xn updated in place
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = oracle.mlp_residual(x0.astype(np.float64), wgu, wd)
+    # the activation a may differ by one bf16 step per entry (fp32 vs fp64
+    # pre-activations near a rounding boundary): |dx| <= 2^-8 sum_j |a_j w_j|
+    gu = xn.astype(np.float64) @ wgu.astype(np.float64).T
+    a = oracle.round_bf16(oracle.silu(gu[:, :inter]) * gu[:, inter:])
+    bound = 2.0 ** -8 * (np.abs(a) @ np.abs(wd.astype(np.float64)).T) + 1e-5
+    got = x.cpu().numpy()
+    err = np.abs(got - ref)
+    assert (err <= bound).all(), f"max excess {(err - bound).max():.3e}"
+    _close_bf16(xn_d.float().cpu().numpy(), oracle.round_bf16(oracle.rms_norm(got)))
+
+
+def _stack_setup(w, plen, seed=0, mlp_inter=0):
+    """Device copies of a workload's decoder inputs plus a per-layer paged cache
+    (with the gated MLP of that intermediate size when mlp_inter > 0)."""
     cap = np.asarray(plen) + w.block_len
     table, npg = wl.page_tables(w, cap, seed)
     caches, host = [], []
@@ -124,8 +153,10 @@ def _stack_setup(w, plen, seed=0):
     E = wl.embed_table(w, seed)
     em = wl.mask_embedding(w, seed)
     lw = [wl.layer_weights(w, l, seed) for l in range(w.num_layers)]
+    if mlp_inter:
+        lw = [t + wl.mlp_weights(w, l, mlp_inter, seed) for l, t in enumerate(lw)]
     ctx = torch.from_numpy(np.asarray(plen, np.int32)).cuda()
-    stack = DecoderStack(_bf(E), _bf(em), [(_bf(a), _bf(b)) for a, b in lw], caches, ctx,
+    stack = DecoderStack(_bf(E), _bf(em), [tuple(_bf(a) for a in t) for t in lw], caches, ctx,
                          batch=w.batch, block_len=w.block_len, num_q_heads=w.num_q_heads,
                          max_ctx=int(cap.max()))
     return stack, E, em, lw, host
@@ -135,10 +166,11 @@ DEC = wl.WORKLOADS["longctx_b8"].with_(name="dec_small", batch=3, vocab=1000, nu
                                        prefix=300, prefix_min=0)
 
 
-def test_decoder_stack_matches_oracle():
+@pytest.mark.parametrize("mlp_inter", [0, wl.MLP_INTER])
+def test_decoder_stack_matches_oracle(mlp_inter):
     w = DEC
     plen = [0, 77, 300]
-    stack, E, em, lw, host = _stack_setup(w, plen)
+    stack, E, em, lw, host = _stack_setup(w, plen, mlp_inter=mlp_inter)
     rng = np.random.default_rng(44)
     tok = rng.integers(0, w.vocab, (w.batch, w.block_len)).astype(np.int32)
     tok[rng.random(tok.shape) < 0.6] = -1
@@ -156,7 +188,13 @@ def test_decoder_stack_matches_oracle():
         worst = max(worst, err)
         mean += float(np.abs(x[b] - rx).mean()) / w.batch
         scale = max(scale, float(np.abs(rx).max()))
-        assert err <= 2e-2, f"sequence {b}: residual stream error {err}"
+        # activations are stored in bf16 between kernels, so a value near a
+        # rounding boundary may land one bf16 step apart and carry that step
+        # through later layers: 2e-2, or two bf16 steps at the stream's
+        # largest magnitude when that is larger; the mean must stay far below
+        tol = max(2e-2, 2.0 ** -7 * float(np.abs(rx).max()))
+        assert err <= tol, f"sequence {b}: residual stream error {err} > {tol}"
+        assert np.abs(x[b] - rx).mean() <= 1e-3 * float(np.abs(rx).max())
         assert np.abs(ks[0, b] - rk[0]).max() <= 2e-2
     print(f"\ndecoder stack: max |dx| {worst:.2e}, mean |dx| {mean:.2e}, max |x| {scale:.2f}")
 
