@@ -197,12 +197,15 @@ template <typename... KArgs>
 inline bool preload_kernel(void (*kernel)(KArgs...), bool dyn_smem) {
   if (dyn_smem) {
     int dev = 0, optin = 0;
+    cudaFuncAttributes attr;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-            cudaSuccess)
+            cudaSuccess ||
+        cudaFuncGetAttributes(&attr, kernel) != cudaSuccess)
       return false;
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) ==
-           cudaSuccess;
+    // the opt-in limit covers static and dynamic shared memory together
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin - (int)attr.sharedSizeBytes) == cudaSuccess;
   }
   cudaFuncAttributes attr;
   return cudaFuncGetAttributes(&attr, kernel) == cudaSuccess;

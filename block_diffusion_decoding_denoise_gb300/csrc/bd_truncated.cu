@@ -28,7 +28,14 @@
 //   trunc_select_kernel  one CTA per masked row: max and the top-k digits,
 //                        the top-p digits, then the restricted Gumbel-max draw
 //                        and the kept mass; writes one sampling state per row
-//                        for conf_commit_kernel
+//                        for conf_commit_kernel.  With top-k, once the first
+//                        digit is known, every entry at or above the boundary
+//                        digit (at most 4096) is copied to shared memory and
+//                        the remaining passes run there: two passes over the
+//                        row instead of up to seven.  Row passes load eight
+//                        values per thread before using them and count into
+//                        per-warp private histograms (no contention between
+//                        warps), merged after the pass.
 #include <math.h>
 
 #include <algorithm>
@@ -51,8 +58,57 @@ __device__ __forceinline__ uint32_t ordered_key(float z) {
   return u == 0x7FFFFFFFu ? 0x80000000u : u;
 }
 
+// exp(z - m) with the difference rounded on its own (no contraction into the
+// exponent's scaling), so that the row's maximum contributes exactly 1.
+__device__ __forceinline__ float rel_exp(float z, float m) { return __expf(__fsub_rn(z, m)); }
+
 __device__ __forceinline__ unsigned long long mass_of(float z, float m) {
-  return static_cast<unsigned long long>(static_cast<double>(__expf(z - m)) * kMassScale);
+  return static_cast<unsigned long long>(static_cast<double>(rel_exp(z, m)) * kMassScale);
+}
+
+// Calls f(v, z_v) for this thread's entries of the row, v ascending: loads
+// are issued in batches of eight (float4 when the row is 16-byte aligned)
+// before any of them is used, so each batch costs one memory latency.
+template <typename F>
+__device__ __forceinline__ void for_row(const float *__restrict__ l, int V, float it, F &&f) {
+  constexpr int kBatch = 8;
+  const int t = threadIdx.x;
+  if ((V & 3) == 0) {
+    const float4 *__restrict__ l4 = reinterpret_cast<const float4 *>(l);
+    const int V4 = V >> 2;
+    for (int base = t; base < V4; base += kSelThreads * kBatch) {
+      float4 x[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = base + j * kSelThreads;
+        if (i < V4) x[j] = __ldg(l4 + i);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = base + j * kSelThreads;
+        if (i < V4) {
+          f(4 * i, x[j].x * it);
+          f(4 * i + 1, x[j].y * it);
+          f(4 * i + 2, x[j].z * it);
+          f(4 * i + 3, x[j].w * it);
+        }
+      }
+    }
+  } else {
+    for (int base = t; base < V; base += kSelThreads * kBatch) {
+      float x[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = base + j * kSelThreads;
+        if (i < V) x[j] = __ldg(l + i);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = base + j * kSelThreads;
+        if (i < V) f(i, x[j] * it);
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ float block_max(float v, float *red) {
@@ -118,15 +174,62 @@ __device__ int find_from_top(const unsigned long long *hist, int nb, unsigned lo
   return d;
 }
 
+// Histograms over a whole row go to private copies in shared memory, one per
+// warp for counts and one per pair of warps for masses, so that warps never
+// contend for a bin; priv_merge sums the copies into hist.
+constexpr int kPrivWords = 32768;           // 128 KB
+__device__ __forceinline__ void priv_zero(uint32_t *priv) {
+  for (int i = threadIdx.x; i < kPrivWords; i += kSelThreads) priv[i] = 0u;
+}
+
+__device__ __forceinline__ void priv_merge(const uint32_t *priv, bool mass,
+                                          unsigned long long *hist) {
+  for (int b = threadIdx.x; b < kBins; b += kSelThreads) {
+    unsigned long long s = 0;
+    if (mass) {
+      const unsigned long long *p64 = reinterpret_cast<const unsigned long long *>(priv);
+      for (int c = 0; c < kSelThreads / 64; ++c) s += p64[c * kBins + b];
+    } else {
+      for (int c = 0; c < kSelThreads / 32; ++c) s += priv[c * kBins + b];
+    }
+    hist[b] = s;
+  }
+}
+
+// Total of an nb-bin histogram (every thread gets it).
+__device__ unsigned long long hist_total(const unsigned long long *hist, int nb,
+                                         unsigned long long *scan) {
+  const int t = threadIdx.x;
+  unsigned long long part = 0;
+  for (int b = t; b < nb; b += kSelThreads) part += hist[b];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if ((t & 31) == 0) scan[t >> 5] = part;
+  __syncthreads();
+  unsigned long long total = 0;
+  for (int w = 0; w < kSelThreads / 32; ++w) total += scan[w];
+  __syncthreads();
+  return total;
+}
+
+constexpr int kCand = 4096;                 // entries a row's candidate list can hold
+constexpr size_t kSelDynSmem = (size_t)kCand * 8 + (size_t)kPrivWords * 4;
+
 __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p, const float *logits,
                                                                    int top_k, float top_p) {
   __shared__ unsigned long long hist[kBins];
   __shared__ unsigned long long scan[kSelThreads / 32];
   __shared__ float red[kSelThreads / 32];
-  __shared__ int s_digit;
+  __shared__ int s_digit, s_n;
   __shared__ unsigned long long s_above;
   __shared__ float s_kb[kSelThreads / 32], s_zb[kSelThreads / 32], s_sum[kSelThreads / 32];
   __shared__ int s_idx[kSelThreads / 32];
+  extern __shared__ float cand_z[];           // kCand values, kCand entry ids, private hists
+  int *cand_v = reinterpret_cast<int *>(cand_z + kCand);
+  uint32_t *priv = reinterpret_cast<uint32_t *>(cand_v + kCand);
+  uint32_t *priv_c = priv + (threadIdx.x >> 5) * kBins;       // this warp's count copy
+  unsigned long long *priv_m =
+      reinterpret_cast<unsigned long long *>(priv) + (threadIdx.x >> 6) * kBins;  // mass copy
   const int k = blockIdx.x, t = threadIdx.x;
   const int V = p.vocab;
   pdl_trigger();
@@ -138,142 +241,195 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
   const float it = p.inv_temp;
   constexpr int kShift[3] = {21, 10, 0};
   constexpr int kWidth[3] = {11, 11, 10};
-
-  // max of z and the top-k digits: the first digit pass also finds the max
-  float m = -INFINITY;
-  uint32_t thr = 0;                           // entries with key >= thr are kept
   const bool use_k = top_k > 0 && top_k < V;
-  {
-    uint32_t prefix = 0, pmask = 0;
-    unsigned long long need = (unsigned long long)(use_k ? top_k : 0);
-    const int ndig = use_k ? 3 : 0;
-    for (int v = t; v < kBins; v += kSelThreads) hist[v] = 0;
+
+  // pass over the row: the max, and the counts of the top-k first digit
+  if (use_k) priv_zero(priv);
+  __syncthreads();
+  float m = -INFINITY;
+  for_row(l, V, it, [&](int, float z) {
+    m = fmaxf(m, z);
+    if (use_k) atomicAdd(&priv_c[ordered_key(z) >> kShift[0]], 1u);
+  });
+  m = block_max(m, red);
+  if (use_k) {
+    priv_merge(priv, false, hist);
     __syncthreads();
-    for (int v = t; v < V; v += kSelThreads) {
-      const float z = l[v] * it;
-      m = fmaxf(m, z);
-      if (use_k) atomicAdd(&hist[ordered_key(z) >> kShift[0]], 1ull);
-    }
-    m = block_max(m, red);
-    for (int d = 0; d < ndig; ++d) {
-      const int nb = 1 << kWidth[d];
-      if (d > 0) {
-        for (int v = t; v < kBins; v += kSelThreads) hist[v] = 0;
+  }
+
+  // Entries are visited either straight from the row or, when top-k leaves
+  // few enough candidates (every entry whose first digit is at least the
+  // boundary digit), from a list of them in shared memory.
+  bool use_cand = false;
+  int ncand = 0;
+  uint32_t thr = 0;                           // entries with key >= thr are kept
+  uint32_t prefix = 0, pmask = 0;
+  unsigned long long need = 0;
+  int d_next = 0;                             // next top-k digit to resolve
+  if (use_k) {
+    unsigned long long above;
+    const int d0 = find_from_top(hist, 1 << kWidth[0], (unsigned long long)top_k, above, scan,
+                                 &s_digit, &s_above);
+    if (d0 < 0) {                             // cannot happen for 0 < k < V
+      if (t == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+    } else {
+      prefix = (uint32_t)d0 << kShift[0];
+      pmask = (uint32_t)((1 << kWidth[0]) - 1) << kShift[0];
+      need = (unsigned long long)top_k - above;
+      d_next = 1;
+      if (above + hist[d0] <= (unsigned long long)kCand) {
+        if (t == 0) s_n = 0;
         __syncthreads();
-        for (int v = t; v < V; v += kSelThreads) {
-          const uint32_t key = ordered_key(l[v] * it);
-          if ((key & pmask) == prefix) atomicAdd(&hist[(key >> kShift[d]) & (nb - 1)], 1ull);
+        for_row(l, V, it, [&](int v, float z) {
+          if ((ordered_key(z) >> kShift[0]) >= (uint32_t)d0) {
+            const int i = atomicAdd(&s_n, 1);
+            if (i < kCand) {
+              cand_z[i] = z;
+              cand_v[i] = v;
+            }
+          }
+        });
+        __syncthreads();
+        ncand = min(s_n, kCand);
+        use_cand = true;
+      }
+    }
+  }
+
+  // `row`: the entries come from the row (private histograms), else from the
+  // short candidate list (atomics straight into hist)
+  auto resolve = [&](auto &&visit, bool row) {
+    auto begin_hist = [&]() {
+      if (row) priv_zero(priv);
+      else
+        for (int b = t; b < kBins; b += kSelThreads) hist[b] = 0;
+      __syncthreads();
+    };
+    auto end_hist = [&](bool mass) {
+      __syncthreads();
+      if (row) {
+        priv_merge(priv, mass, hist);
+        __syncthreads();
+      }
+    };
+    // remaining top-k digits
+    if (use_k && d_next > 0) {
+      for (int d = d_next; d < 3; ++d) {
+        const int nb = 1 << kWidth[d], sh = kShift[d];
+        begin_hist();
+        visit([&](int, float z) {
+          const uint32_t key = ordered_key(z);
+          if ((key & pmask) == prefix) {
+            const uint32_t bin = (key >> sh) & (nb - 1);
+            if (row) atomicAdd(&priv_c[bin], 1u);
+            else atomicAdd(&hist[bin], 1ull);
+          }
+        });
+        end_hist(false);
+        unsigned long long above;
+        int dig = find_from_top(hist, nb, need, above, scan, &s_digit, &s_above);
+        if (dig < 0) {
+          if (t == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+          dig = 0;
+          above = 0;
+        }
+        prefix |= (uint32_t)dig << sh;
+        pmask |= (uint32_t)(nb - 1) << sh;
+        need -= above;
+      }
+      thr = prefix;
+    }
+    // top-p digits over the entries top-k kept, by integer mass
+    if (top_p < 1.f) {
+      uint32_t pp = 0, pm = 0;
+      unsigned long long pneed = 0;
+      for (int d = 0; d < 3; ++d) {
+        const int nb = 1 << kWidth[d], sh = kShift[d];
+        begin_hist();
+        visit([&](int, float z) {
+          const uint32_t key = ordered_key(z);
+          if (key >= thr && (key & pm) == pp) {
+            const uint32_t bin = (key >> sh) & (nb - 1);
+            if (row) atomicAdd(&priv_m[bin], mass_of(z, m));
+            else atomicAdd(&hist[bin], mass_of(z, m));
+          }
+        });
+        end_hist(true);
+        if (d == 0) {                         // total kept mass -> the target
+          pneed = (unsigned long long)ceil((double)top_p * (double)hist_total(hist, nb, scan));
+          if (pneed == 0) pneed = 1;
+        }
+        unsigned long long above;
+        int dig = find_from_top(hist, nb, pneed, above, scan, &s_digit, &s_above);
+        if (dig < 0) {                        // rounding put the target past the total
+          if (t == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+          dig = 0;
+          above = 0;
+        }
+        pp |= (uint32_t)dig << sh;
+        pm |= (uint32_t)(nb - 1) << sh;
+        pneed -= above;
+      }
+      thr = max(thr, pp);
+    }
+    // restricted Gumbel-max draw and the kept mass
+    float kb = -INFINITY, zb = -INFINITY, sum = 0.f;
+    int idx = 0x7FFFFFFF;
+    visit([&](int v, float z) {
+      if (ordered_key(z) < thr) return;
+      const float key = z + gumbel_at(v, pos, p.seed, draw);
+      if (key > kb || (key == kb && v < idx)) {
+        kb = key;
+        zb = z;
+        idx = v;
+      }
+      sum += rel_exp(z, m);
+    });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float okb = __shfl_xor_sync(0xffffffffu, kb, o);
+      const float ozb = __shfl_xor_sync(0xffffffffu, zb, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (okb > kb || (okb == kb && oi < idx)) {
+        kb = okb;
+        zb = ozb;
+        idx = oi;
+      }
+    }
+    const int warp = t >> 5;
+    if ((t & 31) == 0) {
+      s_kb[warp] = kb;
+      s_zb[warp] = zb;
+      s_idx[warp] = idx;
+      s_sum[warp] = sum;
+    }
+    __syncthreads();
+    if (t == 0) {
+      float S = 0.f;
+      for (int w = 0; w < kSelThreads / 32; ++w) {
+        S += s_sum[w];
+        if (s_kb[w] > kb || (s_kb[w] == kb && s_idx[w] < idx)) {
+          kb = s_kb[w];
+          zb = s_zb[w];
+          idx = s_idx[w];
         }
       }
-      __syncthreads();
-      unsigned long long above;
-      int dig = find_from_top(hist, nb, need, above, scan, &s_digit, &s_above);
-      if (dig < 0) {                          // cannot happen for 0 < k < V
-        if (t == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
-        dig = 0;
-        above = 0;
-      }
-      prefix |= (uint32_t)dig << kShift[d];
-      pmask |= (uint32_t)(nb - 1) << kShift[d];
-      need -= above;
+      SampleState st;
+      st.m = m;
+      st.s = S;
+      st.kb = kb;
+      st.zb = zb;
+      st.idx = idx < V ? idx : -1;
+      p.ws.spartial[k] = st;                  // the only partial of row k
     }
-    if (use_k) thr = prefix;
-  }
-
-  // top-p digits over the entries top-k kept, by integer mass
-  if (top_p < 1.f) {
-    uint32_t prefix = 0, pmask = 0;
-    unsigned long long need = 0;
-    for (int d = 0; d < 3; ++d) {
-      const int nb = 1 << kWidth[d];
-      for (int v = t; v < kBins; v += kSelThreads) hist[v] = 0;
-      __syncthreads();
-      for (int v = t; v < V; v += kSelThreads) {
-        const float z = l[v] * it;
-        const uint32_t key = ordered_key(z);
-        if (key >= thr && (key & pmask) == prefix)
-          atomicAdd(&hist[(key >> kShift[d]) & (nb - 1)], mass_of(z, m));
-      }
-      __syncthreads();
-      if (d == 0) {                           // total kept mass -> the target
-        unsigned long long part = 0;
-        for (int b = t; b < nb; b += kSelThreads) part += hist[b];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if ((t & 31) == 0) scan[t >> 5] = part;
-        __syncthreads();
-        unsigned long long total = 0;
-        for (int w = 0; w < kSelThreads / 32; ++w) total += scan[w];
-        __syncthreads();
-        need = (unsigned long long)ceil((double)top_p * (double)total);
-        if (need == 0) need = 1;
-      }
-      unsigned long long above;
-      int dig = find_from_top(hist, nb, need, above, scan, &s_digit, &s_above);
-      if (dig < 0) {                          // rounding put the target past the total
-        if (t == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
-        dig = 0;
-        above = 0;
-      }
-      prefix |= (uint32_t)dig << kShift[d];
-      pmask |= (uint32_t)(nb - 1) << kShift[d];
-      need -= above;
-    }
-    thr = max(thr, prefix);
-  }
-
-  // restricted Gumbel-max draw and the kept mass
-  float kb = -INFINITY, zb = -INFINITY, sum = 0.f;
-  int idx = 0x7FFFFFFF;
-  for (int v = t; v < V; v += kSelThreads) {
-    const float z = l[v] * it;
-    if (ordered_key(z) < thr) continue;
-    const float key = z + gumbel_at(v, pos, p.seed, draw);
-    if (key > kb) {                           // v ascending per thread: ties keep the lower
-      kb = key;
-      zb = z;
-      idx = v;
-    }
-    sum += __expf(z - m);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float okb = __shfl_xor_sync(0xffffffffu, kb, o);
-    const float ozb = __shfl_xor_sync(0xffffffffu, zb, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-    sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (okb > kb || (okb == kb && oi < idx)) {
-      kb = okb;
-      zb = ozb;
-      idx = oi;
-    }
-  }
-  const int warp = t >> 5;
-  if ((t & 31) == 0) {
-    s_kb[warp] = kb;
-    s_zb[warp] = zb;
-    s_idx[warp] = idx;
-    s_sum[warp] = sum;
-  }
-  __syncthreads();
-  if (t == 0) {
-    float S = 0.f;
-    for (int w = 0; w < kSelThreads / 32; ++w) {
-      S += s_sum[w];
-      if (s_kb[w] > kb || (s_kb[w] == kb && s_idx[w] < idx)) {
-        kb = s_kb[w];
-        zb = s_zb[w];
-        idx = s_idx[w];
-      }
-    }
-    SampleState st;
-    st.m = m;
-    st.s = S;
-    st.kb = kb;
-    st.zb = zb;
-    st.idx = idx < V ? idx : -1;
-    p.ws.spartial[k] = st;                    // the only partial of row k
-  }
+  };
+  if (use_cand)
+    resolve([&](auto &&f) {
+      for (int i = t; i < ncand; i += kSelThreads) f(cand_v[i], cand_z[i]);
+    }, false);
+  else
+    resolve([&](auto &&f) { for_row(l, V, it, f); }, true);
 }
 
 // out[k][v] = h[row k] . W[v] in fp32, for the masked rows k < count.
@@ -299,7 +455,7 @@ __global__ void __launch_bounds__(256) logits_simt_kernel(ConfParams p, float *o
 }  // namespace
 
 bool preload_truncated() {
-  return preload_kernel(trunc_select_kernel, false) &&
+  return preload_kernel(trunc_select_kernel, true) &&
          preload_kernel(logits_simt_kernel<float>, false) &&
          preload_kernel(logits_simt_kernel<__nv_bfloat16>, false);
 }
@@ -323,8 +479,8 @@ bd_status trunc_logits_and_select(const ConfParams &p, float *logits, int top_k,
     s = e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
   }
   if (s != BD_OK) return s;
-  const cudaError_t e = launch_pdl(trunc_select_kernel, dim3(rows_max), dim3(kSelThreads), 0, st,
-                                   p, (const float *)logits, top_k, top_p);
+  const cudaError_t e = launch_pdl(trunc_select_kernel, dim3(rows_max), dim3(kSelThreads),
+                                   kSelDynSmem, st, p, (const float *)logits, top_k, top_p);
   count_launches(1);
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
