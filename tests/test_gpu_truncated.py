@@ -47,6 +47,16 @@ def test_truncated_block_bf16_ragged_vocab(top_k, top_p):
     lockstep_sampled_block(w, W, h, 0.9, 0.8, seed=5, top_k=top_k, top_p=top_p)
 
 
+@pytest.mark.parametrize("vocab,top_k,top_p", [(997, 30, 0.9), (7, 2, 1.0), (7, 0, 0.6)])
+def test_truncated_vocab_not_a_multiple_of_four(vocab, top_k, top_p):
+    # rows that are not 16-byte aligned take the scalar load path of the
+    # selection kernel; V = 7 also leaves most of the logits tile empty
+    w = SMALL_BF16.with_(vocab=vocab)
+    W = wl.lm_head(w)
+    h, _ = wl.planted_hidden(w, W, 0, a_max=30.0)
+    lockstep_sampled_block(w, W, h, 0.9, 0.8, seed=9, top_k=top_k, top_p=top_p, max_steps=6)
+
+
 def test_truncated_more_rows_than_one_pass():
     w = SMALL_BF16.with_(batch=9)                 # 288 rows: two passes of <= 256
     W = wl.lm_head(w)
