@@ -90,6 +90,25 @@ def _dist():
     return rank, world, local
 
 
+def _max_over_ranks(x: float, device) -> float:
+    """The largest x over the ranks of the process group (x itself without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _whole_job_rate(units_per_rank: float, ms_local: float, world: int, device):
+    """Whole-job throughput of `world` replicas that each processed
+    units_per_rank in ms_local: the slowest rank's time sets the clock.
+    Returns (units per second over all ranks, that time in ms)."""
+    ms = _max_over_ranks(ms_local, device)
+    return units_per_rank * world / (ms / 1e3), ms
+
+
 def _cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -395,11 +414,7 @@ def run_cuda(a):
     recording[0] = False
     eng.step = orig_step
     eng.check_status()
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = tokens_total * world / (ms / 1e3)
+    value, ms = _whole_job_rate(tokens_total, ms, world, "cuda")
 
     # roofline of the dominant call: bd_confidence_commit
     # algorithmic bytes per call: W once, plus the masked rows of h (read) and
