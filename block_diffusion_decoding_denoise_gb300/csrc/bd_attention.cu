@@ -16,6 +16,8 @@
 // attn_combine_kernel.
 #include <math.h>
 
+#include <algorithm>
+
 #include "bd_attention.cuh"
 #include "bd_common.cuh"
 
@@ -202,6 +204,68 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnParams p) {
   for (int j = 0; j < DPL; ++j) out[j] = from_f32<T>(acc[j] * inv);
 }
 
+// The same merge when there are at most 32 partials per row: every load the
+// row needs (the block's tokens, its ctx, the partials' (m, l) pairs and O
+// rows) is issued before any of them is used, so the merge costs about one
+// memory latency instead of one per group of partials.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) attn_combine32_kernel(AttnParams p) {
+  constexpr int DPL = D / 32;
+  constexpr int kMax = 32;
+  const int group = p.hq / p.hkv;
+  const int R = p.block_len * group;
+  const int wid = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
+  if (wid >= p.batch * p.hkv * R) return;
+  const int r = wid % R, g = (wid / R) % p.hkv, b = wid / (R * p.hkv);
+  const int HS = p.seg_heads > 0 ? p.seg_heads : 1;
+  const size_t seg = (size_t)b * (p.hkv / HS) + g / HS;
+  const size_t srows = (size_t)HS * R;
+  const size_t base = seg * p.num_splits * srows + (size_t)(g % HS) * R + r;
+  const int ns = p.num_splits;                // <= kMax (host-checked)
+  const int tok = (p.tokens && lane < p.block_len) ? p.tokens[(size_t)b * p.block_len + lane] : 0;
+  const int ctx = p.ctx_len[b];
+  float2 ml = make_float2(-INFINITY, 0.f);
+  if (lane < ns) ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + (base + lane * srows) * 2));
+  float v[kMax][DPL];
+#pragma unroll
+  for (int s = 0; s < kMax; ++s) {
+    if (s < ns) {
+      const float *src = p.part_o + (base + (size_t)s * srows) * D + lane * DPL;
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) v[s][d] = __ldcg(src + d);
+    }
+  }
+  if (p.tokens && !__any_sync(0xffffffffu, lane < p.block_len && tok == BD_MASK)) return;
+  if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) return;
+  const int used = min(ns, (ctx + p.block_len + p.split_keys - 1) / p.split_keys);
+  float m = lane < used ? ml.x : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float w_l = lane < used ? __expf(ml.x - m) : 0.f;
+  float l = lane < used ? ml.y * w_l : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  float acc[DPL];
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
+#pragma unroll
+  for (int s = 0; s < kMax; ++s) {
+    if (s < used) {
+      const float w = __shfl_sync(0xffffffffu, w_l, s);
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) acc[d] = fmaf(v[s][d], w, acc[d]);
+    }
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const int i = r / group, h = g * group + r % group;
+  T *out = static_cast<T *>(p.out) + (((size_t)b * p.block_len + i) * p.hq + h) * D + lane * DPL;
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) out[d] = from_f32<T>(acc[d] * inv);
+}
+
 // Merge the pieces of every segment cut by the tile-range partition of the
 // bf16 mma.sync kernel; same arithmetic as attn_combine_kernel, slots
 // segment + CTA for the CTAs between those holding the segment's first and
@@ -258,6 +322,99 @@ __global__ void __launch_bounds__(256) attn_combine_sk_kernel(AttnParams p) {
   for (int j = 0; j < DPL; ++j) out[j] = from_f32<T>(acc[j] * inv);
 }
 
+// attn_combine_sk_kernel with one memory latency for segments cut into at
+// most 32 pieces: every piece's (m, l) pair and O row are loaded before any
+// is used; a segment with more pieces takes the loop of attn_combine_sk_kernel.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) attn_combine_sk32_kernel(AttnParams p) {
+  constexpr int DPL = D / 32;
+  constexpr int kMax = 32;
+  const int group = p.hq / p.hkv;
+  const int R = p.block_len * group;
+  const int wid = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
+  if (wid >= p.batch * p.hkv * R) return;
+  const int r = wid % R, g = (wid / R) % p.hkv, b = wid / (R * p.hkv);
+  const int HS = p.seg_heads;
+  const int total = p.plan[2 * p.batch];
+  const int tiles = p.plan[2 * b + 1];
+  const int sbase = p.plan[2 * b];
+  if (tiles <= 0 || total <= 0) return;
+  const long long seg0 = (long long)sbase + (long long)(g / HS) * tiles;
+  const int c0 = sk_cta_of(seg0, total, p.grid), c1 = sk_cta_of(seg0 + tiles - 1, total, p.grid);
+  if (c0 == c1) return;
+  const size_t seg = (size_t)b * (p.hkv / HS) + g / HS;
+  const size_t srows = (size_t)HS * R;
+  const size_t rin = (size_t)(g % HS) * R + r;
+  auto holds = [&](int c) {
+    return ((long long)c * total) / p.grid < ((long long)(c + 1) * total) / p.grid;
+  };
+  const int i = r / group, h = g * group + r % group;
+  T *out = static_cast<T *>(p.out) + (((size_t)b * p.block_len + i) * p.hq + h) * D + lane * DPL;
+  if (c1 - c0 + 1 > kMax) {                   // more pieces than lanes: one group at a time
+    float m = -INFINITY;
+    for (int c = c0 + lane; c <= c1; c += 32)
+      if (holds(c)) m = fmaxf(m, __ldcg(&p.sk_ml[((seg + c) * srows + rin) * 2]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float l = 0.f, acc[DPL];
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
+    for (int c = c0; c <= c1; ++c) {
+      if (!holds(c)) continue;
+      const size_t pr = (seg + c) * srows + rin;
+      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.sk_ml + pr * 2));
+      const float w = __expf(ml.x - m);
+      l = fmaf(ml.y, w, l);
+      const float *src = p.sk_o + pr * D + lane * DPL;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) acc[j] = fmaf(__ldcg(src + j), w, acc[j]);
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) out[j] = from_f32<T>(acc[j] * inv);
+    return;
+  }
+  const int n = c1 - c0 + 1;
+  const bool mine = lane < n && holds(c0 + lane);
+  float2 ml = make_float2(-INFINITY, 0.f);
+  if (mine) ml = __ldcg(reinterpret_cast<const float2 *>(p.sk_ml + ((seg + c0 + lane) * srows + rin) * 2));
+  float v[kMax][DPL];
+#pragma unroll
+  for (int s = 0; s < kMax; ++s) {
+    if (s < n) {
+      const float *src = p.sk_o + ((seg + c0 + s) * srows + rin) * D + lane * DPL;
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) v[s][d] = __ldcg(src + d);
+    }
+  }
+  float m = mine ? ml.x : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float w_l = mine ? __expf(ml.x - m) : 0.f;
+  float l = mine ? ml.y * w_l : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  float acc[DPL];
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
+#pragma unroll
+  for (int s = 0; s < kMax; ++s) {
+    if (s < n) {
+      const float w = __shfl_sync(0xffffffffu, w_l, s);
+      if (w != 0.f) {                         // pieces of CTAs with an empty range weigh 0
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[d] = fmaf(v[s][d], w, acc[d]);
+      }
+    }
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+  for (int d = 0; d < DPL; ++d) out[d] = from_f32<T>(acc[d] * inv);
+}
+
 bd_status attention_combine(const AttnParams &p, cudaStream_t st);
 
 template <typename T, int D>
@@ -265,8 +422,13 @@ static bd_status launch_combine_sk(const AttnParams &p, cudaStream_t st) {
   const int R = p.block_len * (p.hq / p.hkv);
   const size_t warps = (size_t)p.batch * p.hkv * R;
   const int blocks = (int)((warps + 7) / 8);
+  // the one-latency merge holds 32 partial rows per lane (about 150
+  // registers): it wins while the rows fit in one wave of CTAs and latency
+  // decides; with more rows the leaner loop keeps more warps per SM busy
+  const bool one_wave = blocks <= std::max(1, dev_info().sms);
   const cudaError_t e =
-      launch_pdl(attn_combine_sk_kernel<T, D>, dim3(blocks), dim3(256), 0, st, p);
+      one_wave ? launch_pdl(attn_combine_sk32_kernel<T, D>, dim3(blocks), dim3(256), 0, st, p)
+               : launch_pdl(attn_combine_sk_kernel<T, D>, dim3(blocks), dim3(256), 0, st, p);
   count_launches(1);
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
@@ -294,7 +456,12 @@ static bd_status launch_combine(const AttnParams &p, cudaStream_t st) {
   const int R = p.block_len * (p.hq / p.hkv);
   const size_t warps = (size_t)p.batch * p.hkv * R;
   const int blocks = (int)((warps + 7) / 8);
-  const cudaError_t e = launch_pdl(attn_combine_kernel<T, D>, dim3(blocks), dim3(256), 0, st, p);
+  // one-latency merge while it fits (see launch_combine_sk)
+  const bool one_wave = blocks <= std::max(1, dev_info().sms);
+  const cudaError_t e =
+      p.num_splits <= 32 && one_wave
+          ? launch_pdl(attn_combine32_kernel<T, D>, dim3(blocks), dim3(256), 0, st, p)
+          : launch_pdl(attn_combine_kernel<T, D>, dim3(blocks), dim3(256), 0, st, p);
   count_launches(1);
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
@@ -315,8 +482,14 @@ bool preload_attention_simt() {
          preload_kernel(attn_combine_kernel<float, 128>, false) &&
          preload_kernel(attn_combine_kernel<__nv_bfloat16, 64>, false) &&
          preload_kernel(attn_combine_kernel<__nv_bfloat16, 128>, false) &&
+         preload_kernel(attn_combine32_kernel<float, 64>, false) &&
+         preload_kernel(attn_combine32_kernel<float, 128>, false) &&
+         preload_kernel(attn_combine32_kernel<__nv_bfloat16, 64>, false) &&
+         preload_kernel(attn_combine32_kernel<__nv_bfloat16, 128>, false) &&
          preload_kernel(attn_combine_sk_kernel<__nv_bfloat16, 64>, false) &&
-         preload_kernel(attn_combine_sk_kernel<__nv_bfloat16, 128>, false);
+         preload_kernel(attn_combine_sk_kernel<__nv_bfloat16, 128>, false) &&
+         preload_kernel(attn_combine_sk32_kernel<__nv_bfloat16, 64>, false) &&
+         preload_kernel(attn_combine_sk32_kernel<__nv_bfloat16, 128>, false);
 }
 
 bd_status attention_simt(const AttnParams &p, cudaStream_t st) {
