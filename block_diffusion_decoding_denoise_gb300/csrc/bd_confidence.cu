@@ -235,13 +235,17 @@ bd_status lmhead_simt(const ConfParams &p, cudaStream_t st) {
 
 // ---------------------------------------------------------------------------
 // commit: one CTA per sequence; warp i merges the partial states of position
-// i (lanes stride over the producers), warp 0 then takes the decision
+// i (lanes stride over the producers, eight loads in flight per lane before
+// any is merged; the merge order is the producers' order), warp 0 then takes
+// the decision
 // ---------------------------------------------------------------------------
 template <bool kSample>
 __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
   using St = typename ConfState<kSample>::type;
+  constexpr int kInFlight = 8;
   __shared__ float s_pm[32];
   __shared__ int s_am[32];
+  __shared__ int s_masked[32];
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = p.block_len;
   pdl_trigger();
@@ -252,17 +256,32 @@ __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
     if (b == 0 && threadIdx.x == 0) *p.offset += 1;
   if (warp < L) {
     const int pos = b * L + warp;
+    const int tok = p.tokens[pos];            // both loads issued together
+    const int k = p.direct ? pos : p.ws.row_of[pos];
+    const size_t stride = (size_t)p.batch * L;
     float pm = -1.f;
     int am = -1;
-    if (p.tokens[pos] == BD_MASK) {
-      const int k = p.ws.row_of[pos];
-      const size_t stride = (size_t)p.batch * L;
+    const bool masked = tok == BD_MASK;
+    if (masked && (k < 0 || (size_t)k >= stride)) {
+      if (lane == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+    } else if (masked) {
       St st;
       set_empty(st);
       const St *part;
       if constexpr (kSample) part = p.ws.spartial;
       else part = p.ws.partial;
-      for (int c = lane; c < p.ws.num_partials; c += 32) st = merge(st, part[c * stride + k]);
+      const int np = p.ws.num_partials;
+      for (int c0 = 0; c0 < np; c0 += 32 * kInFlight) {
+        St v[kInFlight];
+#pragma unroll
+        for (int j = 0; j < kInFlight; ++j) {
+          const int c = c0 + lane + 32 * j;
+          if (c < np) v[j] = part[c * stride + k];
+          else set_empty(v[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < kInFlight; ++j) st = merge(st, v[j]);
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) st = merge(st, shfl_xor_state(st, o));
       if (lane == 0) {
@@ -273,11 +292,12 @@ __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
     if (lane == 0) {
       s_pm[warp] = pm;
       s_am[warp] = am;
+      s_masked[warp] = masked ? 1 : 0;
     }
   }
   __syncthreads();
   if (warp != 0) return;
-  const bool masked = lane < L && p.tokens[b * L + lane] == BD_MASK;
+  const bool masked = lane < L && s_masked[lane] != 0;
   commit_sequence_warp(p, b, masked, masked ? s_pm[lane] : -1.f, masked ? s_am[lane] : -1);
 }
 
@@ -353,6 +373,9 @@ static size_t conf_workspace(bd_dtype dtype, int32_t batch, int32_t block_len, i
   return carve(p, nullptr, nullptr);
 }
 
+// At most this many positions per call: the LM head reads h in place.
+constexpr int kDirectRows = 64;
+
 // Truncation of a sampled call: logits buffer after the carved workspace.
 struct TruncArgs {
   int top_k;
@@ -390,16 +413,24 @@ static bd_status conf_run(ConfParams &p, const void *hidden_states, const void *
     trunc = &tr;
   }
 
-  // the tensor-core paths read the masked rows from a contiguous copy
+  // the tensor-core paths read the masked rows from a contiguous copy, except
+  // with few positions (at most kDirectRows), where the LM head reads all rows
+  // in place: at that width it is bound by the W stream either way, and the
+  // compaction kernel and its launch drop out of the step
   const bool tc = trunc ? p.dtype == BD_BF16 : lmhead_tc_supported(p);
   const int nrows = p.batch * p.block_len;
-  const int prep_ctas = tc ? std::max(1, std::min(std::max(dev_info().sms, 1), (nrows + 7) / 8)) : 1;
-  const int32_t *tok_in = p.tokens;
-  const char *src = tc ? static_cast<const char *>(hidden_states) : nullptr;
-  cudaError_t e = launch_pdl(conf_prep_kernel, dim3(prep_ctas), dim3(1024), 0, st, tok_in, nrows,
-                             p.ws, src, p.hidden * 2);
-  count_launches(1);
-  if (e != cudaSuccess) return BD_ERR_CUDA;
+  p.direct = (!trunc && tc && nrows <= kDirectRows) ? 1 : 0;
+  cudaError_t e;
+  if (!p.direct) {
+    const int prep_ctas =
+        tc ? std::max(1, std::min(std::max(dev_info().sms, 1), (nrows + 7) / 8)) : 1;
+    const int32_t *tok_in = p.tokens;
+    const char *src = tc ? static_cast<const char *>(hidden_states) : nullptr;
+    e = launch_pdl(conf_prep_kernel, dim3(prep_ctas), dim3(1024), 0, st, tok_in, nrows, p.ws, src,
+                   p.hidden * 2);
+    count_launches(1);
+    if (e != cudaSuccess) return BD_ERR_CUDA;
+  }
   bd_status s;
   if (trunc) {
     s = trunc_logits_and_select(p, trunc->logits, trunc->top_k, trunc->top_p, st);

@@ -41,6 +41,10 @@ struct ConfParams {
   float inv_temp;
   uint64_t seed;
   uint64_t *offset;
+  // direct rows (few positions, tensor-core path): the LM head reads all
+  // batch * block_len rows of h in place, row k being position k, and no
+  // compaction runs; masked or not, every row gets its partial states
+  int direct;
   ConfWorkspace ws;
 };
 

@@ -299,7 +299,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // set-up above overlaps the previous kernel; the row list is read after it
   pdl_trigger();
   pdl_wait();
-  const int count = *p.ws.count;
+  int count;
+  if (p.direct) {
+    // all rows, or none once every position of the call is committed (each
+    // warp reads the <= 64 tokens itself)
+    const int n = p.batch * p.block_len;
+    const bool m0 = lane < n && p.tokens[lane] == BD_MASK;
+    const bool m1 = lane + 32 < n && p.tokens[lane + 32] == BD_MASK;
+    count = __ballot_sync(0xffffffffu, m0 || m1) ? n : 0;
+  } else {
+    count = *p.ws.count;
+  }
   const int npass = count > 0 ? (count + kMaxN - 1) / kMaxN : 0;   // 0: nothing masked
 
   if (warp == 0) {
@@ -418,7 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kSample) {
         // position ids of this pass's rows (the previous pass's readers have
         // all passed the per-tile barrier below)
-        for (int i = tid_e; i < npad; i += kEpiThreads) spos[i] = i < n ? p.ws.rows[r0 + i] : 0;
+        for (int i = tid_e; i < npad; i += kEpiThreads)
+          spos[i] = i < n ? (p.direct ? r0 + i : p.ws.rows[r0 + i]) : 0;
         named_barrier(2, kEpiThreads);
       }
       for (int t = 0; t < my_tiles; ++t, ++tg) {
@@ -528,11 +539,12 @@ bd_status lmhead_tc(const ConfParams &p, cudaStream_t st) {
   CUtensorMap mw, mh, mh64;
   const uint64_t rows = (uint64_t)p.batch * p.block_len;
   if (!make_map(&mw, p.w, p.hidden, p.vocab, kKChunk, kTileV)) return BD_ERR_CUDA;
-  if (!make_map(&mh, p.ws.hc, p.hidden, rows, kKChunk, kBoxRows)) return BD_ERR_CUDA;
+  const void *hsrc = p.direct ? p.h : p.ws.hc;   // rows in place, or the compact copy
+  if (!make_map(&mh, hsrc, p.hidden, rows, kKChunk, kBoxRows)) return BD_ERR_CUDA;
   // the large-box map only when a whole 64-row group can exist
   a.big_boxes = rows >= (uint64_t)kBigBoxRows ? 1 : 0;
   if (a.big_boxes) {
-    if (!make_map(&mh64, p.ws.hc, p.hidden, rows, kKChunk, kBigBoxRows)) return BD_ERR_CUDA;
+    if (!make_map(&mh64, hsrc, p.hidden, rows, kKChunk, kBigBoxRows)) return BD_ERR_CUDA;
   } else {
     mh64 = mh;
   }

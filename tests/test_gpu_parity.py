@@ -182,6 +182,19 @@ def test_decode_threshold_extremes(T, steps):
     assert st.steps_gpu.tolist() == [steps] * w.batch
 
 
+@pytest.mark.parametrize("batch", [1, 2])
+def test_decode_few_positions_read_in_place(batch):
+    # <= 64 positions per call: the LM head reads every row of h in place, no
+    # compaction; the commit must still use only the masked rows
+    w = SMALL_BF16.with_(batch=batch)
+    W = wl.lm_head(w)
+    h, _ = wl.planted_hidden(w, W, 0, a_max=30.0)
+    tok0 = np.full((w.batch, w.block_len), -1)
+    tok0[0, ::3] = 5                              # some positions already committed
+    st = lockstep_block(w, W, h, 0.9, tokens0=tok0)
+    assert st.rows_checked > 0
+
+
 def test_decode_region_thresholds():
     # per-position thresholds (bd_confidence_commit_regions): three regions per
     # sequence at different offsets, one sequence with a NaN region (never

@@ -60,6 +60,16 @@ def test_sampled_sparse_masked_positions():
     lockstep_sampled_block(w, W, h, 0.95, 1.0, seed=123456789012345, tokens0=tok0)
 
 
+def test_sampled_few_positions_read_in_place():
+    # 64 positions: direct rows in the LM head, positions = row indices
+    w = SMALL_BF16.with_(batch=2)
+    W = wl.lm_head(w)
+    h, _ = wl.planted_hidden(w, W, 0, a_max=30.0)
+    tok0 = np.full((w.batch, w.block_len), -1)
+    tok0[1, 4:20] = 3
+    lockstep_sampled_block(w, W, h, 0.9, 1.0, seed=21, tokens0=tok0)
+
+
 def test_sampled_two_lmhead_passes():
     w = SMALL_BF16.with_(batch=9)                 # 288 rows: two passes of <= 256
     W = wl.lm_head(w)
