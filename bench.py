@@ -33,11 +33,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "committed tokens/sec per denoise loop"
-# DRAM bytes (read + write) of one lmhead_tc_kernel launch with 32 masked rows
-# (the first denoise step of this workload), from an ncu capture of the current
-# kernel (eight epilogue warps): dram__bytes_read.sum 622.53 MB +
-# dram__bytes_write.sum 3.26 MB.  Later steps have fewer rows and the same W.
-LMHEAD_TRAFFIC_BYTES = 622_532_864 + 3_257_600
+# DRAM bytes (read + write) of one lmhead_tc_kernel launch at this workload
+# (32 positions, h read in place), the mean over 20 launches of an ncu capture
+# of the current kernel: dram__bytes_read.sum 622.54 MB + dram__bytes_write.sum
+# 0.25 MB.
+LMHEAD_TRAFFIC_BYTES = 622_543_040 + 253_197
 UNIT = "tokens/s"
 WORKLOAD = "sdar_b1"
 
