@@ -304,14 +304,15 @@ __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-int conf_num_partials(bd_dtype dtype, int batch, int block_len, int hidden, int vocab) {
+int conf_num_partials(bd_dtype dtype, int batch, int block_len, int hidden, int vocab,
+                      bool sample) {
   ConfParams probe{};
   probe.dtype = dtype;
   probe.batch = batch;
   probe.block_len = block_len;
   probe.hidden = hidden;
   probe.vocab = vocab;
-  if (lmhead_tc_supported(probe)) return lmhead_tc_num_partials(vocab);
+  if (lmhead_tc_supported(probe)) return lmhead_tc_num_partials(vocab, batch * block_len, sample);
   return (vocab + kSimtChunk - 1) / kSimtChunk;
 }
 
@@ -327,7 +328,7 @@ bool preload_confidence() {
 
 static size_t carve(const ConfParams &p, char *base, ConfWorkspace *ws) {
   const size_t n = (size_t)p.batch * p.block_len;
-  const int np = conf_num_partials(p.dtype, p.batch, p.block_len, p.hidden, p.vocab);
+  const int np = conf_num_partials(p.dtype, p.batch, p.block_len, p.hidden, p.vocab, p.sample != 0);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     char *ptr = base ? base + off : nullptr;

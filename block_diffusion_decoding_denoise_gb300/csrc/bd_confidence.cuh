@@ -116,11 +116,12 @@ __device__ __forceinline__ void commit_sequence_warp(const ConfParams &p, int b,
 }
 
 // Number of partial states the LM-head kernel of `dtype` produces per row.
-int conf_num_partials(bd_dtype dtype, int batch, int block_len, int hidden, int vocab);
+int conf_num_partials(bd_dtype dtype, int batch, int block_len, int hidden, int vocab,
+                      bool sample);
 
 bd_status lmhead_simt(const ConfParams &p, cudaStream_t st);
 bool lmhead_tc_supported(const ConfParams &p);
-int lmhead_tc_num_partials(int vocab);
+int lmhead_tc_num_partials(int vocab, int rows, bool sample);
 bd_status lmhead_tc(const ConfParams &p, cudaStream_t st);
 
 // Truncated sampling (bd_sample_commit_truncated): logits of the masked rows

@@ -56,12 +56,13 @@ constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTileV = 128;                 // vocabulary entries per tile (MMA M)
 constexpr int kKChunk = 64;                 // K elements per stage (128 bytes of bf16)
-constexpr int kMaxN = 256;                  // masked rows per pass (MMA N)
+constexpr int kMaxN = 256;                  // masked rows per pass (MMA N), at most
+constexpr int kNarrowN = 128;               // ... in the two-CTAs-per-SM configuration
+constexpr int kNarrowSmem = 112 * 1024;     // shared memory per CTA there
 constexpr int kBoxRows = 16;                // rows of the compact h copy per small TMA box
 constexpr int kBigBoxRows = 64;             // ... per large box (whole 64-row groups)
 constexpr int kABytes = kTileV * 128;       // 16 KB of W per stage
 constexpr int kMaxStages = 12;
-constexpr uint32_t kTmemCols = 2 * kMaxN;   // two accumulators (all 512 columns)
 constexpr int kSmemLimit = 227 * 1024;
 
 struct Ctrl {
@@ -80,6 +81,7 @@ struct LmTcArgs {
   int stage_bytes;
   int num_tiles;
   int nmax;       // masked rows per pass this launch can hold (multiple of 16)
+  int maxn;       // rows per pass: kMaxN, or kNarrowN with two CTAs per SM
   int big_boxes;  // 1: tmap_h64 (64-row boxes) is valid
   int red_off;    // smem offsets of the merge buffer, the row positions
   int pos_off;    // (sampling only) and Ctrl
@@ -289,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (a.big_boxes) tma_prefetch_desc(&tmap_h64);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctrl->tmem_base), kTmemCols);
+    tmem_alloc(smem_u32(&ctrl->tmem_base), 2u * a.maxn);   // two accumulators
     tmem_relinquish();
   }
   tc_fence_before();
@@ -310,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     count = *p.ws.count;
   }
-  const int npass = count > 0 ? (count + kMaxN - 1) / kMaxN : 0;   // 0: nothing masked
+  const int MN = a.maxn;
+  const int npass = count > 0 ? (count + MN - 1) / MN : 0;   // 0: nothing masked
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -318,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0;
     bool stop = false;
     for (int pass = 0; pass < npass && !stop; ++pass) {
-      const int r0 = pass * kMaxN;
-      const int n = min(kMaxN, count - r0);
+      const int r0 = pass * MN;
+      const int n = min(MN, count - r0);
       const int npad = (n + 15) & ~15;
       const uint32_t tx = kABytes + npad * 128;
       for (int t = 0; t < my_tiles && !stop; ++t) {
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, tg = 0;
       bool stop = false;
       for (int pass = 0; pass < npass && !stop; ++pass) {
-        const int n = min(kMaxN, count - pass * kMaxN);
+        const int n = min(MN, count - pass * MN);
         const int npad = (n + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(kTileV, npad);
         for (int t = 0; t < my_tiles && !stop; ++t, ++tg) {
@@ -381,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem + acc * kMaxN;
+          const uint32_t d = tmem + acc * MN;
           for (int kc = 0; kc < KC; ++kc, ++it) {
             const uint32_t s = it % S, round = it / S;
             if (ctrl->abort || !mbar_wait(smem_u32(&ctrl->full[s]), round & 1)) {
@@ -421,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tg = 0;
     bool stop = false;
     for (int pass = 0; pass < npass && !stop; ++pass) {
-      const int r0 = pass * kMaxN;
-      const int n = min(kMaxN, count - r0);
+      const int r0 = pass * MN;
+      const int n = min(MN, count - r0);
       const int npad = (n + 15) & ~15;
       St run = empty_state<St>();
       if constexpr (kSample) {
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool valid = vbase + lane < p.vocab;
           for (int c0 = 16 * half; c0 < npad; c0 += 32) {
             uint32_t r[16];
-            tmem_ld_32x32b_x16(tmem + ((uint32_t)(32 * q) << 16) + acc * kMaxN + c0, r);
+            tmem_ld_32x32b_x16(tmem + ((uint32_t)(32 * q) << 16) + acc * MN + c0, r);
             tmem_ld_wait();
             St *dst = red + ((tg & 1) * 4 + slot) * a.nmax + c0;
             if constexpr (kSample)
@@ -479,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, 2u * a.maxn);
   }
 }
 
@@ -494,16 +497,28 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, 
 
 int num_tiles(int vocab) { return (vocab + kTileV - 1) / kTileV; }
 
+// Calls with at most kNarrowN positions run two CTAs per SM (half the TMEM
+// and at most kNarrowSmem of shared memory each): one CTA's epilogue and tile
+// hand-offs overlap the other's stream, and the smaller CTAs become resident
+// while the previous kernel drains.  Measured at 32 rows: 134.8 -> 130.7 us
+// per call alone and 6740 -> 7690 committed tokens/s in the step graphs.
+// (Greedy only: the sampling epilogue needs about 127 registers a thread, so
+// two of its CTAs do not fit an SM's register file.)
+bool narrow(int rows, bool sample) { return rows <= kNarrowN && !sample; }
+
 void plan(const ConfParams &p, LmTcArgs &a, size_t *smem) {
   const int rows = p.batch * p.block_len;
-  const int nmax = std::min(kMaxN, (rows + 15) & ~15);
+  const bool nar = narrow(rows, p.sample != 0);
+  a.maxn = nar ? kNarrowN : kMaxN;
+  const int nmax = std::min(a.maxn, (rows + 15) & ~15);
   a.nmax = nmax;
   a.stage_bytes = (kABytes + nmax * 128 + 1023) & ~1023;
   const int state = p.sample ? (int)sizeof(SampleState) : (int)sizeof(MaxSumArg);
   const int red = (2 * 4 * nmax * state + 1023) & ~1023;
   const int pos = p.sample ? ((nmax * 4 + 127) & ~127) : 0;
   const int fixed = red + pos + (int)sizeof(Ctrl) + 1024;
-  a.stages = std::max(2, std::min(kMaxStages, (kSmemLimit - fixed) / a.stage_bytes));
+  const int budget = nar ? kNarrowSmem : kSmemLimit;
+  a.stages = std::max(2, std::min(kMaxStages, (budget - fixed) / a.stage_bytes));
   a.red_off = a.stages * a.stage_bytes;
   a.pos_off = a.red_off + red;
   a.ctrl_off = a.pos_off + pos;
@@ -524,9 +539,10 @@ bool lmhead_tc_supported(const ConfParams &p) {
   return tma_available();
 }
 
-int lmhead_tc_num_partials(int vocab) {
+int lmhead_tc_num_partials(int vocab, int rows, bool sample) {
   const DevInfo d = dev_info();
-  return std::max(1, std::min(d.sms, num_tiles(vocab)));
+  const int ctas = narrow(rows, sample) ? 2 * d.sms : d.sms;
+  return std::max(1, std::min(ctas, num_tiles(vocab)));
 }
 
 bd_status lmhead_tc(const ConfParams &p, cudaStream_t st) {
