@@ -235,14 +235,17 @@ bd_status lmhead_simt(const ConfParams &p, cudaStream_t st) {
 
 // ---------------------------------------------------------------------------
 // commit: one CTA per sequence; warp i merges the partial states of position
-// i (lanes stride over the producers, eight loads in flight per lane before
-// any is merged; the merge order is the producers' order), warp 0 then takes
-// the decision
+// i (lanes stride over the producers, up to twelve loads in flight per lane
+// before any is merged; the merge order is the producers' order), warp 0 then
+// takes the decision
 // ---------------------------------------------------------------------------
 template <bool kSample>
 __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
   using St = typename ConfState<kSample>::type;
-  constexpr int kInFlight = 8;
+  // loads in flight per lane: 12 greedy states cover the 304 partials of a
+  // two-CTAs-per-SM LM head in one round (1024 threads leave 64 registers a
+  // thread, which the larger sampling states fit at 8)
+  constexpr int kInFlight = kSample ? 8 : 12;
   __shared__ float s_pm[32];
   __shared__ int s_am[32];
   __shared__ int s_masked[32];
