@@ -34,10 +34,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "committed tokens/sec per denoise loop"
 # DRAM bytes (read + write) of one lmhead_tc_kernel launch at this workload
-# (32 positions, h read in place), the mean over 20 launches of an ncu capture
-# of the current kernel: dram__bytes_read.sum 622.54 MB + dram__bytes_write.sum
-# 0.25 MB.
-LMHEAD_TRAFFIC_BYTES = 622_543_040 + 253_197
+# (32 positions, h read in place, two CTAs per SM), from an ncu capture of the
+# current kernel: dram__bytes_read.sum 622.54 MB + dram__bytes_write.sum
+# 2.88 MB.
+LMHEAD_TRAFFIC_BYTES = 622_538_752 + 2_876_928
 UNIT = "tokens/s"
 WORKLOAD = "sdar_b1"
 
