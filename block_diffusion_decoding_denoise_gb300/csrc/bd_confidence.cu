@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(256) lmhead_simt_kernel(ConfParams p) {
     St *part;
     if constexpr (kSample) part = p.ws.spartial;
     else part = p.ws.partial;
-    if (r < count) part[(size_t)blockIdx.x * (p.batch * p.block_len) + r] = state[threadIdx.x];
+    if (r < count) part[(size_t)r * gridDim.x + blockIdx.x] = state[threadIdx.x];   // [row][CTA]
   }
 }
 
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
 #pragma unroll
         for (int j = 0; j < kInFlight; ++j) {
           const int c = c0 + lane + 32 * j;
-          if (c < np) v[j] = part[c * stride + k];
+          if (c < np) v[j] = part[(size_t)k * np + c];   // a row's partials are contiguous
           else set_empty(v[j]);
         }
 #pragma unroll

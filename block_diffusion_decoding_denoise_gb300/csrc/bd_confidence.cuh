@@ -13,8 +13,9 @@ namespace bd {
 //   rows     [B*L] int32   compact list of masked positions (b*L + i)
 //   row_of   [B*L] int32   position -> compact row (-1 if not masked)
 //   count    [1]   int32   number of masked rows
-//   partial  [P][B*L] MaxSumArg   one online-softmax state per producer and row
-//                                 (SampleState when sampling)
+//   partial  [B*L][P] MaxSumArg   one online-softmax state per row and producer
+//                                 (SampleState when sampling); a row's P states
+//                                 are contiguous, so the commit reads them coalesced
 //   hc       [B*L][H] bf16        masked rows of h, compacted (bf16 only)
 struct ConfWorkspace {
   int32_t *rows, *row_of, *count;

@@ -270,7 +270,6 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
   const int my_tiles = (a.num_tiles - cta + G - 1) / G;
   const int KC = p.hidden / kKChunk;
   const int S = a.stages;
-  const size_t stride = (size_t)p.batch * p.block_len;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -474,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
       St *part;
       if constexpr (kSample) part = p.ws.spartial;
       else part = p.ws.partial;
-      if (!stop && tid_e < n) part[(size_t)cta * stride + r0 + tid_e] = run;
+      if (!stop && tid_e < n) part[(size_t)(r0 + tid_e) * G + cta] = run;   // [row][CTA]
     }
   }
 
