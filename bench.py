@@ -1,14 +1,19 @@
 """Benchmark: committed tokens/sec of the block-diffusion denoise loop.
 
-Workload (one GPU): SDAR-1.7B-shaped decoder layer in bf16, batch 1, prefix
-4096 (visual + prompt tokens) in a paged KV cache (64-token pages, randomly
-permuted), one block of L'=32 masked tokens, LM head 151936 x 2048 ~ N(0,0.02),
-planted hidden states h = a W[t]/|W[t]| + N(0,1) with a ~ U(0,12) redrawn per
-step, threshold T = 0.95.
+Default workload (one GPU, the largest single-GPU configuration): the
+long-context decode in bf16, batch 8, prefix 16384 (visual + prompt tokens)
+in a paged KV cache (64-token pages, randomly permuted), 16 successive
+blocks of L'=32 masked tokens through a 28-layer random-init decoder of
+SDAR-1.7B shapes (hidden 2048, 16 query / 8 KV heads, head_dim 128), LM head
+151936 x 2048 ~ N(0,0.02); the commit reads planted hidden states
+h = a W[t]/|W[t]| + N(0,1) with a ~ U(0,12) redrawn per step; T = 0.95.
+`--workload sdar_b1` (and the other names) select the single-layer cases.
 
-One bench step = one full pass of the hot path over the block: denoise steps
-(block attention + LM head/confidence/commit) until no position is masked,
-then the append of the block's K/V.  value = committed tokens / second.
+One bench step = one full pass of the hot path over one block: denoise steps
+(every layer's projections and block attention, then the LM head /
+confidence / commit) until no position is masked, then the pass over the
+committed tokens that appends every layer's K/V.  value = committed tokens /
+second.
 
 Arms:
   default            the CUDA library (libbd.so) through its C ABI
@@ -39,7 +44,7 @@ METRIC = "committed tokens/sec per denoise loop"
 # 2.88 MB.
 LMHEAD_TRAFFIC_BYTES = 622_538_752 + 2_876_928
 UNIT = "tokens/s"
-WORKLOAD = "sdar_b1"
+WORKLOAD = "longctx_b8"
 
 
 def _args():
@@ -74,7 +79,7 @@ def _args():
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every kernel from the host instead of replaying CUDA graphs")
     ap.add_argument("--workload", default=WORKLOAD,
-                    help="workload name (the headline line uses sdar_b1)")
+                    help="workload name (the headline line uses longctx_b8)")
     ap.add_argument("--kernel", default=None, choices=["lmhead", "attention", "proj"],
                     help="time one call alone (per-call us, GB/s, TFLOP/s) instead of decoding")
     ap.add_argument("--rows", type=int, default=None,
@@ -126,19 +131,29 @@ def _inputs(w, seed=0):
     return W, plen, kv, q, kb, vb, h
 
 
-def _config(w, extra=None):
+def _config(w, a):
+    """The workload this line measures.  Both arms print exactly this dict for
+    the same flags; what is specific to one run goes to the line's "run"."""
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
     shape = "layer" if w.num_layers == 1 else f"{w.num_layers}-layer decoder"
     c = {"workload": f"{w.name}: SDAR-1.7B-shaped {shape}, batch {w.batch}, prefix {w.prefix}, "
                      f"block {w.block_len}, Hq {w.num_q_heads}/Hkv {w.num_kv_heads}, "
                      f"D {w.head_dim}, LM head {w.vocab}x{w.hidden}, T={w.threshold}, "
                      f"planted a~U(0,{w.a_max:g})",
-         "batch": w.batch, "prefix": w.prefix, "block_len": w.block_len,
-         "vocab": w.vocab, "hidden": w.hidden, "threshold": w.threshold,
+         "batch": w.batch, "prefix": w.prefix, "prefix_min": w.prefix_min,
+         "block_len": w.block_len, "vocab": w.vocab, "hidden": w.hidden,
+         "threshold": w.threshold, "a_max": w.a_max,
          "paged_kv": "64-token pages, permuted page table",
-         "l2": "inputs larger than L2: the 622 MB LM head is streamed every denoise step "
-               "(evicting the 17 MB KV cache between steps)"}
-    if extra:
-        c.update(extra)
+         "decoding": _decoding(a)}
+    if w.num_layers > 1:
+        c.update({"layers": w.num_layers, "blocks": w.num_blocks,
+                  "mlp": (f"SwiGLU, intermediate {wl.MLP_INTER}" if getattr(a, "mlp", False)
+                          else "none (the plainest reading)"),
+                  "l2": "inputs larger than L2: 15.5 GB of per-layer KV cache streamed by "
+                        "every denoise step"})
+    else:
+        c["l2"] = ("inputs larger than L2: the 622 MB LM head is streamed every denoise step "
+                   "(evicting the KV cache between steps)")
     return c
 
 
@@ -191,14 +206,77 @@ def cpu_baseline(w, W, kv, q, kb, vb, h, budget_s=25.0):
                       f"{tokens_done} committed tokens) in {dt:.1f} s, numpy fp64"}
 
 
-def run_reference(a):
-    rank, world, _ = _dist()
-    if rank != 0:
-        return
-    from block_diffusion_decoding_denoise_gb300 import workload as wl
-    w = wl.WORKLOADS[a.workload]
-    if a.a_max is not None:
-        w = w.with_(a_max=a.a_max)
+class DecoderOracle:
+    """The oracle's decode of one sequence of the decoder workload, one denoise
+    step at a time: every step runs the layer stack over the block's current
+    tokens, then the confidence and commit of that sequence's planted hidden
+    states; a finished block is run through the stack once more with its
+    committed tokens and every layer's K/V is appended before the next block
+    (after the last block the decode starts over from the prefix)."""
+
+    def __init__(self, w, b=0, keep=None, mlp=False, temperature=None, seed=1,
+                 top_k=0, top_p=1.0):
+        from block_diffusion_decoding_denoise_gb300 import workload as wl
+        self.w, self.b, self.wl = w, b, wl
+        plen = wl.prefix_lengths(w)
+        self.prefix = (keep if keep is not None else
+                       [wl.prefix_kv(w, b, int(plen[b]), 0, l) for l in range(w.num_layers)])
+        W = wl.lm_head(w)
+        self.W, self.W64 = W, W.astype(np.float64)
+        self.E, self.em = wl.embed_table(w), wl.mask_embedding(w)
+        lw = [wl.layer_weights(w, l) for l in range(w.num_layers)]
+        if mlp:
+            lw = [t + wl.mlp_weights(w, l) for l, t in enumerate(lw)]
+        self.layers = lw
+        self.temperature, self.seed, self.top_k, self.top_p = temperature, seed, top_k, top_p
+        self.draws = 0
+        self._start(0)
+
+    def _start(self, blk):
+        if blk == 0:
+            self.caches = [(k, v) for k, v in self.prefix]
+        self.blk = blk
+        self.h = self.wl.planted_hidden(self.w, self.W, blk)[0][:, self.b:self.b + 1]
+        self.tokens = np.full((1, self.w.block_len), -1, np.int64)
+        self.s = 0
+
+    def step(self):
+        """One denoise step (preceded by the append pass when the previous block
+        finished); returns the number of tokens it committed."""
+        import oracle
+        w = self.w
+        if not (self.tokens == -1).any():
+            _, ks, vs = oracle.decoder_forward(self.tokens[0], self.E, self.em, self.layers,
+                                               self.caches, w.num_q_heads, w.num_kv_heads)
+            self.caches = [(np.concatenate([kc, k.astype(np.float32)]),
+                            np.concatenate([vc, v.astype(np.float32)]))
+                           for (kc, vc), k, v in zip(self.caches, ks, vs)]
+            self._start((self.blk + 1) % w.num_blocks)
+        oracle.decoder_forward(self.tokens[0], self.E, self.em, self.layers, self.caches,
+                               w.num_q_heads, w.num_kv_heads)
+        h = self.h[self.s].astype(np.float64)
+        if self.temperature is None:
+            new, *_ = oracle.denoise_step(self.tokens, h, self.W64, w.threshold)
+        else:
+            new, *_ = oracle.denoise_step_sampled(self.tokens, h, self.W64, w.threshold,
+                                                  self.temperature, self.seed, self.draws,
+                                                  top_k=self.top_k, top_p=self.top_p)
+            self.draws += 1
+        c = int((new != self.tokens).sum())
+        self.tokens = new
+        self.s += 1
+        return c
+
+
+def _reference_steps(a, w):
+    """(one reference step, its description) for workload w."""
+    if w.num_layers > 1:
+        ref = DecoderOracle(w, 0, mlp=a.mlp, temperature=a.temperature, top_k=a.top_k,
+                            top_p=a.top_p)
+        return ref.step, (f"each step = one denoise step of sequence 0 of {w.name} on the fp64 "
+                          f"oracle: the {w.num_layers}-layer stack over the block, confidence "
+                          f"over the full vocabulary and commit (the append pass when a block "
+                          f"finishes)")
     W, plen, kv, q, kb, vb, h = _inputs(w)
     W64 = W.astype(np.float64)
     chunk = 8                       # one reference step = 8 denoise steps of the block
@@ -211,22 +289,34 @@ def run_reference(a):
                                  state["tokens"])
         state["tokens"], state["s"] = tok, state["s"] + n
         return c
+    return ref_step, (f"each step = {chunk} denoise steps of one {w.name} block (all "
+                      f"{w.batch} sequences) on the fp64 oracle: attention, full-logit "
+                      f"confidence, commit, append at block end")
 
+
+def run_reference(a):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    w = wl.WORKLOADS[a.workload]
+    if a.a_max is not None:
+        w = w.with_(a_max=a.a_max)
+    ref_step, sample = _reference_steps(a, w)
     for _ in range(a.warmup):
         ref_step()
     t0 = time.perf_counter()
     committed = sum(ref_step() for _ in range(a.steps))
     dt = time.perf_counter() - t0
     value = committed / dt
-    sample = (f"each step = {chunk} denoise steps of one {w.name} block on the fp64 oracle "
-              f"(attention, full-logit confidence, commit, append at block end)")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt * 1e3 / a.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": _config(w),
+        "data": "synthetic", "config": _config(w, a),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
-                         "sample": sample},
+                         "sample": f"{sample}; {a.steps} steps, {committed} committed tokens "
+                                   f"in {dt:.1f} s"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
@@ -433,7 +523,7 @@ def run_cuda(a):
     achieved = sum(b for b, _ in active) / (sum(t for _, t in active) / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak,
-                "traffic": LMHEAD_TRAFFIC_BYTES if a.workload == WORKLOAD else None,
+                "traffic": LMHEAD_TRAFFIC_BYTES if a.workload == "sdar_b1" else None,
                 "kernel": "bd_confidence_commit (masked-row compaction + LM head with online "
                           "max/sum-exp/argmax + commit)",
                 "peak_source": f"{peak_kind} hbm_gbs"}
@@ -461,14 +551,14 @@ def run_cuda(a):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": max(3, a.warmup), "ms_per_step": ms / a.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": _config(w, {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                              "denoise_steps_per_block": [int(x) for x in steps_per_seq],
-                              "denoise_steps_issued": steps_issued // a.steps,
-                              "check_every": a.check_every, "cuda_graphs": use_graphs,
-                              "decoding": _decoding(a),
-                              "per_call_timing": f"CUDA events around every call in "
-                                                 f"{min(a.steps, 20)} further blocks after the "
-                                                 f"timed region (event nodes slow the graphs)"}),
+        "config": _config(w, a),
+        "run": {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                "denoise_steps_per_block": [int(x) for x in steps_per_seq],
+                "denoise_steps_issued": steps_issued // a.steps,
+                "check_every": a.check_every, "cuda_graphs": use_graphs,
+                "per_call_timing": f"CUDA events around every call in {min(a.steps, 20)} "
+                                   f"further blocks after the timed region (event nodes "
+                                   f"slow the graphs)"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches), "clocks": clk.summary(),
         "conf_call_us_mean": 1e3 * statistics.mean(conf_ms) if conf_ms else None,
@@ -593,8 +683,8 @@ def run_sweep(a):
             "denoise_steps_per_block_mean": float(st.mean()),
             "denoise_steps_per_block_min": int(st.min()),
             "denoise_steps_per_block_max": int(st.max()),
-            "config": _config(w, {"a_max": a_max, "blocks": nblk,
-                                  "prefix_after": int(eng.ctx_len.max().item())})}),
+            "config": _config(w.with_(a_max=a_max), a),
+            "run": {"blocks": nblk, "prefix_after": int(eng.ctx_len.max().item())}}),
               flush=True)
 
 
@@ -710,7 +800,7 @@ def run_ar_compare(a):
                             "denoise_steps_per_block": res[w.block_len][1]},
         "autoregressive": {"block_len": 1, "value": res[1][0]},
         "speedup": res[w.block_len][0] / res[1][0],
-        "config": _config(w, {"a_max": a_max})}))
+        "config": _config(w.with_(a_max=a_max), a)}))
 
 
 # ---------------------------------------------------------------------------
@@ -729,27 +819,6 @@ def _decoder_inputs(w, plen, seed=0, keep_seq=None):
                 yield l, b, k, v
 
 
-def _decoder_oracle_sample(w, W, E, em, lw, host_kv, h_blk, budget_s):
-    """The oracle's denoise steps for sequence 0 of the first block: the
-    28-layer stack over the current tokens, then confidence and commit."""
-    import oracle
-    W64 = W.astype(np.float64)
-    tokens = np.full((1, w.block_len), -1, np.int64)
-    t0 = time.perf_counter()
-    steps = committed = 0
-    while True:
-        oracle.decoder_forward(tokens[0], E, em, lw, host_kv, w.num_q_heads, w.num_kv_heads)
-        new, *_ = oracle.denoise_step(tokens, h_blk[steps][:1].astype(np.float64), W64,
-                                      w.threshold)
-        committed += int((new != tokens).sum())
-        tokens = new
-        steps += 1
-        if time.perf_counter() - t0 > budget_s or steps >= w.block_len:
-            break
-    dt = time.perf_counter() - t0
-    return committed / dt, steps, committed, dt
-
-
 def run_decoder(a):
     """The long-context workload: a 28-layer decoder stack in front of every
     denoise step's commit, successive blocks of one decode (each finished
@@ -760,6 +829,9 @@ def run_decoder(a):
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device (the CUDA arm has no CPU fallback)")
     torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
     from block_diffusion_decoding_denoise_gb300 import bd, build
     from block_diffusion_decoding_denoise_gb300 import workload as wl
     from block_diffusion_decoding_denoise_gb300.engine import (DecoderStack, DenoiseEngine,
@@ -798,6 +870,7 @@ def run_decoder(a):
                         temperature=a.temperature, seed=1, decoder=stack,
                         top_k=a.top_k, top_p=a.top_p)
     h_host = [wl.planted_hidden(w, W, blk)[0] for blk in range(nb)]
+    del W, E, em, lw
     h_dev = [dev(h) for h in h_host]
     h_cur = torch.empty_like(h_dev[0])
     dummy = torch.empty(1, dtype=bf, device="cuda")
@@ -812,19 +885,21 @@ def run_decoder(a):
         except TypeError:
             use_graphs = False
 
-    # per-layer attention events inside every denoise step (captured into the
-    # step graphs as event nodes, read after each chunk)
+    # per-call events (attention of every layer, the commit) inside every
+    # denoise step, captured into the step graphs as event nodes and read
+    # after each chunk; these graphs run only after the timed region
     orig_forward = stack.forward
+    orig_commit = eng.commit
     events = {}
-    attn_ms = []
+    attn_ms, conf_ms = [], []
     stride = eng.n_committed.stride(0) * eng.n_committed.element_size()
     cur_step = [None]
 
     def timed_forward(tokens, attn_tokens=None):
         if attn_tokens is None:
             return orig_forward(tokens, None)
-        s = cur_step[0]
-        evs = []
+        evs = events.setdefault(cur_step[0], {"attn": [], "conf": None})
+        evs["attn"] = []
         stack_attn = bd.bd_block_attention
 
         def attn_wrap(*args, **kw):
@@ -832,30 +907,46 @@ def run_decoder(a):
             e0.record(torch.cuda.current_stream())
             stack_attn(*args, **kw)
             e1.record(torch.cuda.current_stream())
-            evs.append((e0, e1))
+            evs["attn"].append((e0, e1))
         bd.bd_block_attention = attn_wrap
         try:
             orig_forward(tokens, attn_tokens)
         finally:
             bd.bd_block_attention = stack_attn
-        events[s] = evs
+
+    def timed_commit(h, ncom):
+        cur = (ncom.data_ptr() - eng.n_committed.data_ptr()) // stride
+        e0, e1 = torch.cuda.Event(**ev_kw), torch.cuda.Event(**ev_kw)
+        e0.record(torch.cuda.current_stream())
+        orig_commit(h, ncom)
+        e1.record(torch.cuda.current_stream())
+        events.setdefault(cur, {"attn": [], "conf": None})["conf"] = (e0, e1)
 
     orig_step = eng.step
 
-    def step(hh, qq, kk, vv, ncom=None, layer=0):
+    def timed_step(hh, qq, kk, vv, ncom=None, layer=0):
         cur_step[0] = (ncom.data_ptr() - eng.n_committed.data_ptr()) // stride
-        orig_step(hh, qq, kk, vv, ncom, layer)
+        stack.forward = timed_forward
+        eng.commit = timed_commit
+        try:
+            orig_step(hh, qq, kk, vv, ncom, layer)
+        finally:
+            stack.forward = orig_forward
+            eng.commit = orig_commit
 
     recording = [False]
 
     def on_chunk(s0, s1):
         if recording[0]:
             for s in range(s0, s1):
-                for e0, e1 in events.get(s, ()):
+                ev = events.get(s)
+                if ev is None:
+                    continue
+                for e0, e1 in ev["attn"]:
                     attn_ms.append(e0.elapsed_time(e1))
+                if ev["conf"] is not None:
+                    conf_ms.append(ev["conf"][0].elapsed_time(ev["conf"][1]))
 
-    stack.forward = timed_forward
-    eng.step = step
     blk_ctr = [0]
 
     def block():
@@ -867,16 +958,23 @@ def run_decoder(a):
         return eng.decode_block(h_cur, dummy, dummy, dummy, check_every=a.check_every,
                                 graphs=use_graphs, on_chunk=on_chunk)
 
+    # warm-up of both step variants (the first block of each captures its
+    # graphs): the plain step, timed for `value`, then the step with events
     warm = max(3, a.warmup)
-    for _ in range(warm):
-        block()
+    for variant in (timed_step, orig_step):
+        eng.step = variant
+        blk_ctr[0] = 0
+        for _ in range(warm):
+            block()
     torch.cuda.synchronize()
     eng.check_status()
-    ctx_at = ctx.clone()
-    recording[0] = True
+    blk_ctr[0] = 0
+    ctx_at = ctx0.clone()
     steps_issued = committed = 0
     l0 = bd.bd_kernel_launches()
     g0 = eng.graph_kernel_launches
+    if world > 1:
+        torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t0 = torch.cuda.Event(enable_timing=True)
@@ -887,14 +985,29 @@ def run_decoder(a):
             committed += w.batch * L
         t1.record()
         torch.cuda.synchronize()
-    recording[0] = False
+    if world > 1:
+        torch.distributed.barrier()
     ms = t0.elapsed_time(t1)
     eng.check_status()
     launches = (bd.bd_kernel_launches() - l0) + (eng.graph_kernel_launches - g0)
-    value = committed / (ms / 1e3)
-    # attention roofline: K/V of the cache + block once per KV head, Q read, O written;
-    # the context grows by one block per step, so use the mean context of the timed blocks
-    ctx_mean = float(ctx_at.float().mean().item()) + L * (a.steps - 1) / 2.0
+    value, ms = _whole_job_rate(committed, ms, world, "cuda")
+
+    # per-call durations: the same blocks again (from block 0) with events
+    eng.step = timed_step
+    blk_ctr[0] = 0
+    recording[0] = True
+    for _ in range(min(a.steps, nb)):
+        block()
+    torch.cuda.synchronize()
+    recording[0] = False
+    eng.step = orig_step
+    eng.check_status()
+
+    # attention roofline: K/V of the cache + block once per KV head, Q read, O
+    # written; the context grows by one block per block, so take the mean
+    # context of the blocks timed per call
+    nper = min(a.steps, nb)
+    ctx_mean = float(ctx_at.float().mean().item()) + L * (nper - 1) / 2.0
     attn_bytes = (2 * w.batch * (ctx_mean + L) * w.num_kv_heads * w.head_dim * 2
                   + 2 * w.batch * L * w.num_q_heads * w.head_dim * 2)
     peak, peak_kind = _peaks()
@@ -902,11 +1015,18 @@ def run_decoder(a):
     achieved = attn_bytes / (attn_us / 1e6) / 1e9 if attn_us else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak if achieved else None, "traffic": None,
-                "kernel": "bd_block_attention (per layer, 28 per denoise step)",
+                "kernel": f"bd_block_attention (one call per layer, {w.num_layers} per "
+                          f"denoise step)",
                 "bytes_per_call": attn_bytes, "us_per_call": attn_us,
-                "peak_source": f"{peak_kind} hbm_gbs"}
-    stack.forward = orig_forward
-    eng.step = orig_step
+                "calls_timed": len(attn_ms), "peak_source": f"{peak_kind} hbm_gbs"}
+    breakdown = {
+        "denoise_steps_per_block": steps_issued / a.steps,
+        "ms_per_denoise_step": ms / steps_issued if steps_issued else None,
+        "attention_us_per_layer_call": attn_us,
+        "attention_share_of_step": (attn_us * w.num_layers / 1e3) / (ms / steps_issued)
+                                   if attn_us and steps_issued else None,
+        "commit_us_per_call": 1e3 * statistics.mean(conf_ms) if conf_ms else None,
+    }
 
     # e2e: the same blocks through the public API, planted h copied from pinned
     # host memory per block and the committed tokens read back
@@ -915,7 +1035,6 @@ def run_decoder(a):
         hp = [torch.from_numpy(h).to(bf).pin_memory() for h in h_host]
         tok_host = torch.empty(w.batch, L, dtype=torch.int32).pin_memory()
         ctx.copy_(ctx0)
-        blk_ctr[0] = 0
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
@@ -929,32 +1048,44 @@ def run_decoder(a):
             tok_host.copy_(eng.tokens, non_blocking=True)
         e1.record()
         torch.cuda.synchronize()
-        e2e = {"value": committed / (e0.elapsed_time(e1) / 1e3), "unit": UNIT,
+        eng.check_status()
+        e2e_ms = _max_over_ranks(e0.elapsed_time(e1), "cuda")
+        e2e = {"value": committed * world / (e2e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": hp[0].numel() * hp[0].element_size(),
                "d2h_bytes_per_step": tok_host.numel() * 4}
     if rank != 0:
         return
     cpu = None
     if keep is not None:
-        v, st, c, dt = _decoder_oracle_sample(w, W, E, em, lw, keep, h_host[0], 20.0)
-        cpu = {"value": v, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+        ref = DecoderOracle(w, 0, keep=keep, mlp=a.mlp, temperature=a.temperature,
+                            top_k=a.top_k, top_p=a.top_p)
+        t0c = time.perf_counter()
+        st = c = 0
+        while True:
+            c += ref.step()
+            st += 1
+            if time.perf_counter() - t0c > 20.0 or st >= w.block_len:
+                break
+        dt = time.perf_counter() - t0c
+        cpu = {"value": c / dt, "unit": UNIT, "cores": _cores(), "kind": "oracle",
                "sample": f"sequence 0 of block 0: {st} denoise step(s) of the {w.num_layers}-"
-                         f"layer stack + commit ({c} committed tokens) in {dt:.1f} s, numpy fp64"}
+                         f"layer stack + confidence + commit ({c} committed tokens) in "
+                         f"{dt:.1f} s, numpy fp64"}
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": a.steps,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": warm, "ms_per_step": ms / a.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": _config(w, {"parallelism": "single GPU", "layers": w.num_layers,
-                              "mlp": (f"SwiGLU, intermediate {wl.MLP_INTER}" if a.mlp
-                                      else "none (the plainest reading)"),
-                              "blocks_timed": a.steps,
-                              "denoise_steps_issued": steps_issued // a.steps,
-                              "check_every": a.check_every, "cuda_graphs": use_graphs,
-                              "input_generation_s": gen_s,
-                              "l2": "inputs larger than L2: 15.5 GB of per-layer KV cache",
-                              "decoding": _decoding(a)}),
+        "config": _config(w, a),
+        "run": {"parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                "blocks_timed": a.steps, "denoise_steps_issued": steps_issued // a.steps,
+                "check_every": a.check_every, "cuda_graphs": use_graphs,
+                "input_generation_s": gen_s,
+                "per_call_timing": f"CUDA events around every attention and commit call in "
+                                   f"{nper} further blocks after the timed region (event "
+                                   f"nodes slow the graphs)"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches), "clocks": clk.summary(),
+        "step_breakdown": breakdown,
     }
     print(json.dumps(line))
 

@@ -33,7 +33,10 @@ EXPORTS = ("bd_block_attention_workspace", "bd_block_attention",
            "bd_out_projection_workspace", "bd_out_projection_residual",
            "bd_append_block_kv_layers", "bd_confidence_commit_regions",
            "bd_sample_commit_truncated_workspace", "bd_sample_commit_truncated",
-           "bd_mlp_workspace", "bd_mlp_residual")
+           "bd_mlp_workspace", "bd_mlp_residual", "bd_debug_force_attention_kernel", "bd_debug_wait_timeout_selftest")
+
+# bd_attention_kernel values of bd_debug_force_attention_kernel (test hook)
+BD_ATTN = {"auto": 0, "pair": 1, "pair_plan": 2, "mma": 3, "simt": 4}
 
 
 class BDError(RuntimeError):
@@ -82,6 +85,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "bd_status_string": (ctypes.c_char_p, [c_int32]),
             "bd_version": (c_int32, []),
             "bd_kernel_launches": (ctypes.c_uint64, []),
+            "bd_debug_force_attention_kernel": (c_int32, [c_int32]),
+            "bd_debug_wait_timeout_selftest": (c_int32, [c_void_p, c_void_p]),
             "bd_confidence_commit_noalloc": (c_int32, [c_int32, c_int32, c_int32, c_int32,
                                                        c_int32, c_void_p, c_void_p, c_float,
                                                        c_void_p, c_void_p, c_void_p, c_void_p,
@@ -313,6 +318,19 @@ def bd_version() -> int:
 
 def bd_kernel_launches() -> int:
     return int(load().bd_kernel_launches())
+
+
+def bd_debug_wait_timeout_selftest(dev_status, stream=None):
+    """Test hook: one CTA whose bounded wait runs out (BD_ERR_TIMEOUT in dev_status)."""
+    _check("bd_debug_wait_timeout_selftest",
+           load().bd_debug_wait_timeout_selftest(_ptr(dev_status, torch.int32, "dev_status"),
+                                                 _stream(stream)))
+
+
+def bd_debug_force_attention_kernel(which: str):
+    """Test hook: force one attention kernel ("auto" restores the choice by shape)."""
+    _check("bd_debug_force_attention_kernel",
+           load().bd_debug_force_attention_kernel(BD_ATTN[which]))
 
 
 # --- decoder layer stack --------------------------------------------------------

@@ -13,6 +13,8 @@
 namespace bd {
 
 static std::atomic<uint64_t> g_launches{0};
+// kernel forced by bd_debug_force_attention_kernel (BD_ATTN_AUTO: by shape)
+static std::atomic<int> g_forced_attention{BD_ATTN_AUTO};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 __global__ void append_kv_kernel(bd_paged_kv kv, int block_len, size_t elem_bytes,
@@ -30,7 +32,7 @@ bool preload_all() {
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return true;
   const bool ok = preload_kernel(append_kv_kernel, false) && preload_attention_simt() &&
-                  preload_attention_tc() && preload_attention_tc5() && preload_confidence() &&
+                  preload_attention_tc() && preload_confidence() &&
                   preload_lmhead_tc() && preload_decoder() && preload_attention_pair() &&
                   preload_truncated();
   if (!ok) {
@@ -235,15 +237,13 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
   size_t off_ml, sk_o, sk_ml;
   p.grid = num_sms();
   p.seg_heads = 1;
-  // Kernel choice: BD_ATTENTION (pair | pair_plan | tc5 | mma | simt) forces
-  // one kernel, for testing and measurement; pair_plan runs the head-pair
-  // kernel with the tile-range partition even on small problems
-  const char *env = getenv("BD_ATTENTION");
-  const bool force5 = env && !strcmp(env, "tc5");
-  const bool force_simt = env && !strcmp(env, "simt");
-  const bool force_pair_plan = env && !strcmp(env, "pair_plan");
-  const bool force_pair = (env && !strcmp(env, "pair")) || force_pair_plan;
-  const bool force_mma = env && !strcmp(env, "mma");
+  // Kernel choice: by shape (below), unless a test forced one kernel with
+  // bd_debug_force_attention_kernel
+  const int forced = g_forced_attention.load(std::memory_order_relaxed);
+  const bool force_simt = forced == BD_ATTN_SIMT;
+  const bool force_pair_plan = forced == BD_ATTN_PAIR_PLAN;
+  const bool force_pair = forced == BD_ATTN_PAIR || force_pair_plan;
+  const bool force_mma = forced == BD_ATTN_MMA;
   const bool small = attn_small(batch, p.hkv, block_len, max_ctx) && !force_pair_plan;
   // fixed splits of the head-pair kernel: split per head pair
   const bool pair_split = small && force_pair && p.hkv % 2 == 0;
@@ -273,7 +273,7 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
   // kernel with fixed splits on small ones (a few pages per SM, where its
   // shorter start wins); the mma.sync kernel for other bf16 shapes; SIMT for
   // fp32.
-  if (pair_split || ((force_pair || (!force5 && !force_simt && !force_mma)) && p.plan)) {
+  if (pair_split || ((force_pair || (!force_simt && !force_mma)) && p.plan)) {
     if (attention_pair_supported(p)) return attention_pair(p, st);
     if (pair_split) {            // shape not supported: the default kernel, default splits
       if (ws_bytes < attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx, 1,
@@ -282,11 +282,6 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
       p.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + off_ml);
       p.sk_ml = p.part_ml;
     }
-  }
-  if (force5 && attention_tc5_supported(p)) {
-    const bd_status s = attention_tc5(p, st);
-    if (s != BD_OK || p.num_splits == 1) return s;
-    return attention_combine(p, st);
   }
   if (!force_simt) {
     const bd_status s = attention_tc(p, st);
@@ -326,6 +321,12 @@ BD_API const char *bd_status_string(bd_status s) {
   return "BD_ERR_UNKNOWN";
 }
 
-BD_API int32_t bd_version(void) { return 100; }
+BD_API int32_t bd_version(void) { return 200; }
+
+BD_API bd_status bd_debug_force_attention_kernel(int32_t which) {
+  if (which < BD_ATTN_AUTO || which > BD_ATTN_SIMT) return BD_ERR_INVALID_ARG;
+  g_forced_attention.store(which, std::memory_order_relaxed);
+  return BD_OK;
+}
 
 BD_API uint64_t bd_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }

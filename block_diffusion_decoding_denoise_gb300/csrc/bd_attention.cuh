@@ -42,10 +42,8 @@ bd_status attention_simt(const AttnParams &p, cudaStream_t st);
 bd_status attention_tc(const AttnParams &p, cudaStream_t st);
 bd_status attention_combine(const AttnParams &p, cudaStream_t st);
 bd_status attention_combine_sk(const AttnParams &p, cudaStream_t st);
-bool attention_tc5_supported(const AttnParams &p);
 bool attention_pair_supported(const AttnParams &p);
 bd_status attention_pair(const AttnParams &p, cudaStream_t st);
 cudaError_t attention_plan_launch(const AttnParams &p, cudaStream_t st);
-bd_status attention_tc5(const AttnParams &p, cudaStream_t st);
 
 }  // namespace bd

@@ -215,7 +215,6 @@ inline bool preload_kernel(void (*kernel)(KArgs...), bool dyn_smem) {
 bool preload_all();
 bool preload_attention_simt();
 bool preload_attention_tc();
-bool preload_attention_tc5();
 bool preload_confidence();
 bool preload_lmhead_tc();
 bool preload_decoder();

@@ -2,11 +2,11 @@
 // workspace taken from a fixed device array instead of the caller.
 //
 // Why it exists: some callers cannot allocate device memory at the point
-// where they run a denoise step.  Code recorded inside a CUDA-graph capture
-// may not call cudaMalloc; serving runtimes often forbid allocation while a
-// request is in flight (cudaMalloc can synchronise the device and break the
-// server's memory budget); plugins hosted by another framework get no handle
-// to that framework's allocator.  Such callers still own the inputs and the
+// where they run a denoise step.  Serving runtimes often forbid allocation
+// while a request is in flight (cudaMalloc can synchronise the device and
+// break the server's fixed memory budget); plugins hosted by another
+// framework get no handle to that framework's allocator; embedded callers
+// may run with every byte of device memory already handed out at start-up.  Such callers still own the inputs and the
 // outputs, but they have nowhere to put the scratch space that
 // bd_confidence_commit needs (masked-row list, compact copy of the masked
 // rows, per-CTA partial softmax states).  This file gives them one: a
@@ -16,7 +16,10 @@
 // Rules of use (also stated in bd.h):
 //  - The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress while that device is current; make that first call
-//    before any stream capture begins.  Later calls reuse the cached address.
+//    before any stream capture begins.  Later calls reuse the cached address,
+//    so every call must run in the device's primary context (the one the
+//    runtime API uses), and the process must not call cudaDeviceReset after
+//    the first call: the array, and its address, belong to that context.
 //  - Every call on a device shares the one array and leaves its contents
 //    behind.  Nothing in it has to start at zero (each call writes every
 //    scratch value it later reads), but two calls whose executions overlap

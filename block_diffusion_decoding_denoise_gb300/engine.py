@@ -20,6 +20,8 @@ arithmetic runs in libbd's kernels; torch provides memory and streams.
 """
 from __future__ import annotations
 
+import gc
+
 import numpy as np
 import torch
 
@@ -181,11 +183,20 @@ class DenoiseEngine:
                self.step)
         entry = self._graphs.get(key)
         if entry is None:
-            g = torch.cuda.CUDAGraph()
-            n0 = bd.bd_kernel_launches()
-            with torch.cuda.graph(g):
-                for s in range(s0, s1):
-                    self.step(h_steps[s], q, k_blk, v_blk, self.n_committed[s])
+            # Python's cyclic garbage collector must not run inside the capture:
+            # freeing another object's CUDA graphs or memory there invalidates it
+            gc.collect()
+            was_enabled = gc.isenabled()
+            gc.disable()
+            try:
+                g = torch.cuda.CUDAGraph()
+                n0 = bd.bd_kernel_launches()
+                with torch.cuda.graph(g):
+                    for s in range(s0, s1):
+                        self.step(h_steps[s], q, k_blk, v_blk, self.n_committed[s])
+            finally:
+                if was_enabled:
+                    gc.enable()
             entry = (g, bd.bd_kernel_launches() - n0)
             self._graphs[key] = entry
         return entry

@@ -172,9 +172,10 @@ bd_status bd_confidence_commit_regions(bd_dtype dtype, int32_t batch, int32_t bl
 /* ------------------------------------------------------------------------
  * bd_confidence_commit_noalloc -- bd_confidence_commit without a caller
  * workspace.  The paper has no counterpart to this call: it exists for
- * callers that cannot allocate device memory when they run a step (code
- * recorded into a CUDA graph, serving runtimes that forbid allocation while a
- * request is in flight, plugins with no access to their host's allocator).
+ * callers that cannot allocate device memory when they run a step (serving
+ * runtimes that forbid allocation while a request is in flight, plugins with
+ * no access to their host's allocator, embedded callers whose device memory
+ * is all handed out at start-up).
  *
  * Same arguments, results and limits as bd_confidence_commit, minus ws and
  * ws_bytes.  The scratch space comes from one 8 MiB array in device memory
@@ -183,7 +184,10 @@ bd_status bd_confidence_commit_regions(bd_dtype dtype, int32_t batch, int32_t bl
  * rejected with BD_ERR_WORKSPACE before any launch (at hidden 2048 and vocab
  * 151936 on a 152-SM GPU this allows batch * block_len up to about 1400).
  * The first call on a device looks up the array's address while that device
- * is current; make that first call before any stream capture starts.  All
+ * is current; make that first call before any stream capture starts.  The
+ * address is cached per device, so every call must run in that device's
+ * primary context (the runtime API's), and the process must not call
+ * cudaDeviceReset after the first call.  All
  * calls on a device share the array and leave its contents behind: nothing in
  * it needs to start at zero, but calls whose executions overlap on the GPU
  * (unordered streams) race on it.  It allocates and frees nothing.
@@ -380,6 +384,40 @@ int32_t bd_version(void);
 /* Diagnostic: number of kernels this process has launched through the
  * library so far (all devices, all threads).  Reading it never synchronises. */
 uint64_t bd_kernel_launches(void);
+
+/* ------------------------------------------------------------------------
+ * bd_debug_force_attention_kernel -- TEST HOOK, not part of the method.
+ * bd_block_attention picks its kernel from the call's shape and dtype alone
+ * (BD_ATTN_AUTO, the default).  A test that wants to check each kernel on the
+ * same inputs forces one of them for every later bd_block_attention call in
+ * this process; a kernel that cannot serve a shape falls back to the one the
+ * shape would pick.  Returns BD_ERR_INVALID_ARG for an unknown value.
+ * Process-wide and not synchronised with calls in flight: set it only
+ * between calls, and set BD_ATTN_AUTO again afterwards.
+ * ------------------------------------------------------------------------ */
+typedef enum {
+  BD_ATTN_AUTO = 0,      /* by shape                                        */
+  BD_ATTN_PAIR = 1,      /* tcgen05 head-pair kernel                        */
+  BD_ATTN_PAIR_PLAN = 2, /* head-pair kernel with the tile-range partition
+                            even on small problems                          */
+  BD_ATTN_MMA = 3,       /* mma.sync kernel (bf16)                          */
+  BD_ATTN_SIMT = 4       /* SIMT kernel                                     */
+} bd_attention_kernel;
+
+bd_status bd_debug_force_attention_kernel(int32_t which);
+
+/* ------------------------------------------------------------------------
+ * bd_debug_wait_timeout_selftest -- TEST HOOK, not part of the method.
+ * Every device-side wait of the library (mbarrier waits of the tcgen05/TMA
+ * kernels) gives up after one second of wall time; the kernel then writes
+ * BD_ERR_TIMEOUT into *dev_status, stops issuing work, frees its tensor
+ * memory and returns, leaving the context usable.  This call launches one
+ * CTA that takes exactly that path: it allocates tensor memory, waits on a
+ * barrier nothing arrives at, and unwinds.  After about one second the
+ * caller's *dev_status holds BD_ERR_TIMEOUT (if it held 0 before).  No copy
+ * or MMA is in flight at the wait.  Asynchronous on `stream`.
+ * ------------------------------------------------------------------------ */
+bd_status bd_debug_wait_timeout_selftest(int32_t *dev_status, void *stream);
 
 #ifdef __cplusplus
 }

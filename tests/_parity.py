@@ -92,6 +92,8 @@ class StepStats:
     exempt_positions: int = 0
     lockstep_adoptions: int = 0
     max_pmax_err: float = 0.0
+    max_rel_pmax_err: float = 0.0
+    argmax_compared: int = 0
     argmax_mismatch_nonexempt: int = 0
     commit_mismatch_nonexempt: int = 0
     rows_checked: int = 0
@@ -149,6 +151,7 @@ def lockstep_block(w: wl.Workload, W: np.ndarray, h_steps: np.ndarray, threshold
     tokens = np.full((B, L), -1, np.int64) if tokens0 is None else tokens0.astype(np.int64)
     run.set_tokens(tokens)
     Wd = W.astype(np.float64)
+    wmax = float(np.sqrt((Wd ** 2).sum(axis=1)).max())
     steps_gpu = np.zeros(B, np.int64)
     stats = StepStats(steps_gpu, None, None, None)
     s = 0
@@ -164,12 +167,21 @@ def lockstep_block(w: wl.Workload, W: np.ndarray, h_steps: np.ndarray, threshold
         err = np.abs(g_p[bi, ii] - o_p[bi, ii])
         stats.max_pmax_err = max(stats.max_pmax_err, float(err.max()))
         assert err.max() <= tol, f"p_max error {err.max()} > {tol} at step {s}"
+        # relative bound of fp32 logits (tests/_engine_parity.py states it)
+        K = Wd.shape[1]
+        gam = K * 2.0 ** -24 / (1 - K * 2.0 ** -24)
+        eps = 2 * gam * np.sqrt((h_steps[s][bi, ii].astype(np.float64) ** 2).sum(axis=1)) * wmax
+        rel = err / o_p[bi, ii]
+        stats.max_rel_pmax_err = max(stats.max_rel_pmax_err, float(rel.max()))
+        assert (rel <= np.expm1(2 * eps) + (Wd.shape[0] + 3) * 2.0 ** -24).all(), \
+            f"relative p_max error {rel.max():.3e} above its bound at step {s}"
         unmasked = tokens != -1
         assert (g_p[unmasked] == -1).all() and (g_a[unmasked] == -1).all()
         margin = conf["top2_prob_margin"]
         near_t = np.abs(conf["p_max"] - T[bi, ii]) < EXEMPT
         am_exempt = margin < EXEMPT
         bad_am = (g_a[bi, ii] != o_a[bi, ii]) & ~am_exempt
+        stats.argmax_compared += int((~am_exempt).sum())
         stats.argmax_mismatch_nonexempt += int(bad_am.sum())
         assert not bad_am.any(), f"argmax mismatch at non-exempt rows, step {s}"
         # commit decisions

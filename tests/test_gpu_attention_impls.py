@@ -2,15 +2,13 @@
 
 bd_block_attention runs the tcgen05 head-pair kernel for large bf16 problems
 at the SDAR shapes, the mma.sync kernel for the other bf16 cases and the SIMT
-kernel for fp32; each (and the older per-head tcgen05 kernel) is selectable.
-BD_ATTENTION forces one kernel so that each is checked on small, ragged and
-full-size inputs (a kernel that does not support a shape falls back to the
-default one).  "pair" runs the head-pair kernel with fixed KV splits on small
+kernel for fp32, chosen by shape alone.  The library's test hook
+bd_debug_force_attention_kernel forces one kernel so that each is checked on
+small, ragged and full-size inputs (a kernel that does not support a shape
+falls back to the one the shape picks).  "pair" runs the head-pair kernel with fixed KV splits on small
 problems and the tile-range partition on large ones; "pair_plan" runs the
 partition on every problem, which covers more CTAs than tiles.
 """
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -35,15 +33,11 @@ def _lib():
     bd.load()
 
 
-@pytest.fixture(params=["pair", "pair_plan", "tc5", "mma", "simt"])
+@pytest.fixture(params=["auto", "pair", "pair_plan", "mma", "simt"])
 def impl(request):
-    old = os.environ.get("BD_ATTENTION")
-    os.environ["BD_ATTENTION"] = request.param
+    bd.bd_debug_force_attention_kernel(request.param)
     yield request.param
-    if old is None:
-        del os.environ["BD_ATTENTION"]
-    else:
-        os.environ["BD_ATTENTION"] = old
+    bd.bd_debug_force_attention_kernel("auto")
 
 
 def _check(w, plen, impl, blk=0):

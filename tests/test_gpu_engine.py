@@ -1,0 +1,294 @@
+"""The product decode loop against the oracle on all five workloads.
+
+DenoiseEngine.decode_block is the loop bench.py times: 8-step chunks replayed
+as CUDA graphs, the masked count read back only between chunks (steps past a
+block's end are issued speculatively), per-sequence step counts from the
+per-step commit counts, and the finished block's K/V appended before the next
+block ("Rethinking Document OCR as Inverse Rendering via Diffusion Decoding",
+paper.rainbus.top summary, method steps 2-4: blocks decoded in order, each
+step confirming the confident positions; novelty paragraph: the K/V of
+finished blocks reused by later ones).  Every test decodes two successive
+blocks through it and checks every step against the oracle (see
+tests/_engine_parity.py for the comparison rules and the bound that decides
+near-ties), then decodes the same blocks with an engine that records nothing
+and requires the same tokens and step counts.
+
+Each workload runs at the literal planted recipe, a ~ U(0, 12), where no
+position ever reaches the threshold and every step commits through the
+fallback (so step counts are 32 by construction), and at a ~ U(0, 32), where
+confident positions exist, blocks finish in a few steps and the speculative
+steps of the last chunk must change nothing.  The oracle's cost grows with
+the masked rows it must evaluate at the full 151936-entry vocabulary: where a
+workload has more sequences than the oracle covers in seconds, the GPU still
+decodes all of them and the oracle checks the sequences listed (spread over
+the batch), and every sequence's step count is still checked against its
+recorded trajectory.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import functools
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_diffusion_decoding_denoise_gb300 import bd
+from block_diffusion_decoding_denoise_gb300 import workload as wl
+from block_diffusion_decoding_denoise_gb300.engine import DecoderStack, DenoiseEngine, PagedCache
+
+from _engine_parity import (ConfMemo, Counts, Recorder, check_block, dev, run_blocks,
+                            single_layer_setup, torch_dtype)
+
+pytestmark = pytest.mark.gpu
+
+SWEEP = (0.5, 0.7, 0.9, 0.95, 0.99)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_diffusion_decoding_denoise_gb300 import build
+    build.build()
+    bd.load()
+
+
+@functools.lru_cache(maxsize=1)
+def _lm_head(name):
+    w = wl.WORKLOADS[name]
+    W = wl.lm_head(w)
+    return W, dev(W, w.dtype), ConfMemo(W)
+
+
+def _report(name, a_max, T, c: Counts):
+    print(f"\n{name} a_max {a_max:g} T {T}: rows {c.rows}, argmax compared {c.argmax_ns} "
+          f"(by margin) / {c.argmax_rig} (by the bound), commit outcomes compared "
+          f"{c.decisions_ns} / {c.decisions_rig} of {c.decisions}, commits {c.commits_ns}, "
+          f"adopted {c.adoptions}, speculative {c.speculative_steps}, max |dp| "
+          f"{c.max_abs_pmax:.2e}, max rel dp {c.max_rel_pmax:.2e} "
+          f"({c.max_rel_over_bound:.2e} of its bound)")
+
+
+def _attention_check(w, pre, blocks_host, recs, attn_seqs):
+    """Attention output of each block (the last step that ran it) against the
+    oracle over the prefix and every earlier block's K/V."""
+    tol = 1e-4 if w.dtype == "f32" else 2e-2
+    for b in attn_seqs:
+        kc, vc = pre[b]
+        for j, r in enumerate(recs):
+            q, kb, vb = blocks_host[j][1:]
+            ref = oracle.current_block_attention(q[b], kc, vc, kb[b], vb[b])
+            err = float(np.abs(r.attn[b] - ref).max())
+            assert err <= tol, f"block {j} seq {b}: attention error {err}"
+            kc = np.concatenate([kc, kb[b]])
+            vc = np.concatenate([vc, vb[b]])
+
+
+def _pool_check(w, cache, plen, pre, blocks_host, b):
+    """The pages of sequence b hold its prefix followed by every block's K/V
+    (byte-exact), read back through the page table."""
+    n = int(plen[b]) + len(blocks_host) * w.block_len
+    row = cache.page_table_np[b]
+    pages = torch.from_numpy(row[:(n + 63) // 64].astype(np.int64)).cuda()
+    kp = cache.k[pages].float().cpu().numpy()          # [pages, Hkv, 64, D]
+    got = oracle.paged_read(kp, np.arange(len(pages)), n, 64)
+    exp = np.concatenate([pre[b][0]] + [blk[2][b] for blk in blocks_host])
+    assert np.array_equal(got, exp.astype(np.float32)), f"seq {b}: cache pages differ"
+
+
+def _single_layer(name, a_max, seqs, attn_seqs, Ts=None, nblk=2, eager=False):
+    w = wl.WORKLOADS[name]
+    Ts = (w.threshold,) if Ts is None else Ts
+    W, Wd, memo = _lm_head(name)
+    plen, cap, cache, pre = single_layer_setup(w, nblk)
+    blocks_host, blocks_dev = [], []
+    for j in range(nblk):
+        q, kb, vb = wl.block_qkv(w, j)
+        h, _ = wl.planted_hidden(w, W, j, a_max=a_max)
+        blocks_host.append((h, q, kb, vb))
+        blocks_dev.append(tuple(dev(x, w.dtype) for x in (h, q, kb, vb)))
+    ctx0 = torch.from_numpy(plen.astype(np.int32)).cuda()
+    total = Counts()
+    steps_by_T = {}
+    for T in Ts:
+        def engine():
+            return DenoiseEngine(Wd, cache, plen, batch=w.batch, block_len=w.block_len,
+                                 num_q_heads=w.num_q_heads, threshold=T, max_ctx=int(cap.max()))
+        eng = engine()
+        rec = Recorder(eng)
+        recs = run_blocks(eng, blocks_dev, ctx0, rec, graphs=True)
+        plain = run_blocks(engine(), blocks_dev, ctx0, None, graphs=True)
+        variants = [plain]
+        if eager:
+            variants.append(run_blocks(engine(), blocks_dev, ctx0, None, graphs=False))
+        for other in variants:
+            for r, o in zip(recs, other):
+                assert np.array_equal(r.final, o.final) and np.array_equal(r.steps, o.steps)
+        c = Counts()
+        for j, r in enumerate(recs):
+            assert np.array_equal(r.ctx, plen + (j + 1) * w.block_len)
+            check_block(w, memo, (a_max, j), blocks_host[j][0], r, T, seqs, c)
+        _report(name, a_max, T, c)
+        total.add(c)
+        steps_by_T[T] = np.array([r.steps for r in recs])
+        _attention_check(w, pre, blocks_host, recs, attn_seqs)
+    _pool_check(w, cache, plen, pre, blocks_host, attn_seqs[0])
+    return total, steps_by_T
+
+
+def _assert_counts(c: Counts, strong: bool):
+    assert c.argmax_ns > 0 and c.argmax_rig > 0
+    assert c.decisions_ns > 0 and c.decisions_rig > 0
+    if strong:
+        assert c.commits_ns > c.steps_checked      # some steps commit several positions
+        assert c.speculative_steps > 0             # finished sequences saw issued steps
+
+
+# --- tiny_fp32 (fp32, SIMT path) --------------------------------------------
+@pytest.mark.parametrize("a_max", [12.0, 40.0])
+def test_engine_tiny_fp32(a_max):
+    c, st = _single_layer("tiny_fp32", a_max, [0], [0], eager=True)
+    _assert_counts(c, a_max > 12)
+    if a_max == 12.0:
+        assert (st[0.95] == 32).all()
+    else:
+        assert (st[0.95] < 32).all()
+
+
+# --- sdar_b1 (bf16, batch 1, full size) -------------------------------------
+@pytest.mark.parametrize("a_max", [12.0, 32.0])
+def test_engine_sdar_b1(a_max):
+    c, st = _single_layer("sdar_b1", a_max, [0], [0], eager=True)
+    _assert_counts(c, a_max > 12)
+    assert ((st[0.95] == 32).all() if a_max == 12.0 else (st[0.95] < 32).all())
+
+
+# --- serving_b64 (batch 64, ragged prefixes, paged) -------------------------
+def test_engine_serving_b64_strong_all_sequences():
+    c, st = _single_layer("serving_b64", 32.0, list(range(64)), [0, 31, 63])
+    _assert_counts(c, True)
+    assert (st[0.95] < 32).all()
+
+
+def test_engine_serving_b64_literal_sampled_sequences():
+    seqs = list(range(0, 64, 16))
+    c, st = _single_layer("serving_b64", 12.0, seqs, [seqs[1]])
+    _assert_counts(c, False)
+    assert (st[0.95] == 32).all()
+
+
+# --- tsweep_b32 (batch 32, the threshold sweep) -----------------------------
+@pytest.mark.parametrize("a_max", [12.0, 32.0])
+def test_engine_tsweep_b32_all_thresholds(a_max):
+    seqs = list(range(0, 32, 4)) if a_max > 12 else [0, 13, 26]
+    c, st = _single_layer("tsweep_b32", a_max, seqs, [seqs[-1]], Ts=SWEEP)
+    _assert_counts(c, a_max > 12)
+    means = [float(st[T].mean()) for T in SWEEP]
+    print(f"\ntsweep_b32 a_max {a_max:g}: steps per block by T {dict(zip(SWEEP, means))}")
+    if a_max == 12.0:
+        assert all(m == 32.0 for m in means)         # no position ever reaches 0.5
+    else:
+        assert means[0] < means[-1]                  # a lower threshold takes fewer steps
+        assert all(x <= y for x, y in zip(means, means[1:]))
+
+
+# --- longctx_b8 (28-layer decoder stack) ------------------------------------
+@functools.lru_cache(maxsize=1)
+def _longctx_inputs(stack_seqs):
+    """Device state of the 28-layer workload (prefix K/V of every layer for
+    all 8 sequences) and the host copies the oracle needs."""
+    w = wl.WORKLOADS["longctx_b8"]
+    plen = wl.prefix_lengths(w)
+    nblk = 2
+    cap = plen + nblk * w.block_len
+    table, npg = wl.page_tables(w, cap)
+    caches = [PagedCache(npg, w.num_kv_heads, w.head_dim, torch.bfloat16, table)
+              for _ in range(w.num_layers)]
+    keep = {b: [] for b in stack_seqs}
+    with cf.ThreadPoolExecutor(min(w.batch, os.cpu_count() or 1)) as ex:
+        for l in range(w.num_layers):
+            futs = [ex.submit(wl.prefix_kv, w, b, int(plen[b]), 0, l) for b in range(w.batch)]
+            for b, f in enumerate(futs):
+                k, v = f.result()
+                caches[l].load_prefix(b, torch.from_numpy(k), torch.from_numpy(v))
+                if b in keep:
+                    keep[b].append((k, v))
+    E, em = wl.embed_table(w), wl.mask_embedding(w)
+    lw = [wl.layer_weights(w, l) for l in range(w.num_layers)]
+    return w, plen, cap, caches, keep, E, em, lw
+
+
+@pytest.mark.parametrize("a_max", [12.0, 32.0])
+def test_engine_longctx_b8_decoder(a_max):
+    stack_seqs = (0, 5)
+    w, plen, cap, caches, keep, E, em, lw = _longctx_inputs(stack_seqs)
+    W, Wd, memo = _lm_head("longctx_b8")
+    bf = lambda x: dev(x, "bf16")
+    nblk = 2
+    ctx = torch.from_numpy(plen.astype(np.int32)).cuda()
+    stack = DecoderStack(bf(E), bf(em), [(bf(a), bf(b)) for a, b in lw], caches, ctx,
+                         batch=w.batch, block_len=w.block_len, num_q_heads=w.num_q_heads,
+                         max_ctx=int(cap.max()))
+    hs = [wl.planted_hidden(w, W, j, a_max=a_max)[0] for j in range(nblk)]
+    dummy = torch.empty(1, dtype=torch.bfloat16, device="cuda")
+    blocks = [(bf(h), dummy, dummy, dummy) for h in hs]
+    ctx0 = ctx.clone()
+
+    def engine():
+        return DenoiseEngine(Wd, caches, plen, batch=w.batch, block_len=w.block_len,
+                             num_q_heads=w.num_q_heads, threshold=w.threshold,
+                             max_ctx=int(cap.max()), decoder=stack)
+    eng = engine()
+    rec = Recorder(eng)
+    recs = run_blocks(eng, blocks, ctx0, rec, graphs=True)
+    plain = run_blocks(engine(), blocks, ctx0, None, graphs=True)
+    for r, o in zip(recs, plain):
+        assert np.array_equal(r.final, o.final) and np.array_equal(r.steps, o.steps)
+        assert np.array_equal(r.x_app, o.x_app)
+    # the confidence/commit loop on every sequence (literal: four of them)
+    seqs = list(range(w.batch)) if a_max > 12 else [0, 3, 5, 7]
+    c = Counts()
+    for j, r in enumerate(recs):
+        assert np.array_equal(r.ctx, plen + (j + 1) * w.block_len)
+        check_block(w, memo, (a_max, j), hs[j], r, w.threshold, seqs, c)
+    _report("longctx_b8", a_max, w.threshold, c)
+    _assert_counts(c, a_max > 12)
+    # the 28-layer stack for two sequences over both blocks: the residual stream
+    # of the first denoise step (all positions masked) and, after the block,
+    # the append pass over the committed tokens (its stream and every layer's
+    # K/V, which the next block's attention reads from the cache)
+    L = w.block_len
+    for b in stack_seqs:
+        kv = [(k, v) for k, v in keep[b]]
+        for j, r in enumerate(recs):
+            x0, _, _ = oracle.decoder_forward(np.full(L, -1), E, em, lw, kv, w.num_q_heads,
+                                              w.num_kv_heads)
+            got0 = r.x0.reshape(w.batch, L, -1)[b]
+            scale = max(1.0, float(np.abs(x0).max()))
+            assert float(np.abs(got0 - x0).max()) <= 2e-2 * scale, f"block {j} seq {b}: x step 0"
+            xa, ks, vs = oracle.decoder_forward(r.final[b], E, em, lw, kv, w.num_q_heads,
+                                                w.num_kv_heads)
+            gota = r.x_app.reshape(w.batch, L, -1)[b]
+            scale = max(1.0, float(np.abs(xa).max()))
+            err = float(np.abs(gota - xa).max())
+            print(f"\nlongctx seq {b} block {j}: append pass max |dx| {err:.2e} (|x| {scale:.1f})")
+            assert err <= 2e-2 * scale
+            for l in range(w.num_layers):
+                for got, ref in ((r.k_app[l, b], ks[l]), (r.v_app[l, b], vs[l])):
+                    sc = max(1.0, float(np.abs(ref).max()))
+                    assert float(np.abs(got - ref).max()) <= 2e-2 * sc, f"layer {l} K/V"
+            kv = [(np.concatenate([kc, k.astype(np.float32)]),
+                   np.concatenate([vc, v.astype(np.float32)]))
+                  for (kc, vc), k, v in zip(kv, ks, vs)]
+    # the cache holds what the append pass produced (byte-exact, last layer)
+    b = stack_seqs[0]
+    n = int(plen[b]) + nblk * L
+    row = caches[-1].page_table_np[b]
+    pages = torch.from_numpy(row[:(n + 63) // 64].astype(np.int64)).cuda()
+    got = oracle.paged_read(caches[-1].k[pages].float().cpu().numpy(), np.arange(len(pages)),
+                            n, 64)[int(plen[b]):]
+    exp = np.concatenate([r.k_app[-1, b] for r in recs])
+    assert np.array_equal(got, exp)

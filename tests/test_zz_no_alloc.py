@@ -1,10 +1,10 @@
 """The allocation-free confidence/commit entry point.
 
 bd_confidence_commit_noalloc serves callers that cannot allocate device
-memory when they run a step (graph-captured code, serving runtimes that
-forbid allocation mid-request, plugins without access to their host's
-allocator): it takes its scratch space from a fixed array the library keeps
-on the device.  This test drives it through the C ABI for two consecutive
+memory when they run a step (serving runtimes that forbid allocation
+mid-request, plugins without access to their host's allocator, embedded
+callers whose device memory is all handed out at start-up): it takes its
+scratch space from a fixed array the library keeps on the device.  This test drives it through the C ABI for two consecutive
 denoise steps and checks every output against bd_confidence_commit, which
 uses a caller workspace.  It lives in a file of its own that pytest collects
 last, and passes both alone and after the other tests.
