@@ -1176,7 +1176,7 @@ def run_kernel(a):
         vb = torch.randn(kb.shape, device="cuda", generator=g).to(torch.bfloat16)
         out = torch.empty_like(q)
         mc = int(plen.max()) + L
-        ws = torch.empty(max(1, bd.bd_block_attention_workspace(
+        ws = torch.zeros(max(1, bd.bd_block_attention_workspace(
             w.batch, L, w.num_q_heads, w.num_kv_heads, w.head_dim, mc)), dtype=torch.uint8,
             device="cuda")
 

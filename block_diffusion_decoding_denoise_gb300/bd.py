@@ -36,7 +36,7 @@ EXPORTS = ("bd_block_attention_workspace", "bd_block_attention",
            "bd_mlp_workspace", "bd_mlp_residual", "bd_debug_force_attention_kernel", "bd_debug_wait_timeout_selftest")
 
 # bd_attention_kernel values of bd_debug_force_attention_kernel (test hook)
-BD_ATTN = {"auto": 0, "pair": 1, "pair_plan": 2, "mma": 3, "simt": 4}
+BD_ATTN = {"auto": 0, "pair": 1, "mma": 2, "simt": 3}
 
 
 class BDError(RuntimeError):

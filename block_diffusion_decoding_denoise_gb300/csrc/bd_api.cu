@@ -101,29 +101,38 @@ static bool attn_shape_ok(int32_t batch, int32_t block_len, int32_t hq, int32_t 
   return true;
 }
 
-// Workspace of the tile-range partition (bf16 mma.sync kernel): the plan,
-// then partial O and (m, l) for batch * hkv + grid slots.
+// Every attention workspace starts with the head-pair kernel's merge
+// counters (one int per (sequence, KV-head pair)); they must be zero before a
+// call and every call that completes leaves them zero.  The other buffers of
+// a call follow them.
+static size_t attn_counter_bytes(int batch, int hkv) {
+  return align_up((size_t)batch * std::max(1, hkv / 2) * sizeof(int), 256);
+}
+
+// Workspace of the tile-range partition: the plan (mma.sync kernel), then
+// partial O and (m, l) for batch * hkv + 2 grid slots of R rows (the
+// head-pair kernel needs batch * hkv / 2 + grid slots of 2R rows, fewer).
 static size_t attn_sk_bytes(int batch, int block_len, int hq, int hkv, int d, int grid,
-                            size_t *off_o, size_t *off_ml) {
-  // slots: batch * hkv + grid of R rows (one KV head per segment); the
-  // head-pair kernel needs batch * hkv / 2 + grid slots of 2R rows, fewer
+                            size_t *off_plan, size_t *off_o, size_t *off_ml) {
   const size_t rows = ((size_t)batch * hkv + 2 * (size_t)grid) * block_len * (hq / hkv);
-  *off_o = align_up((2 * (size_t)batch + 1) * sizeof(int), 256);
+  *off_plan = attn_counter_bytes(batch, hkv);
+  *off_o = *off_plan + align_up((2 * (size_t)batch + 1) * sizeof(int), 256);
   *off_ml = *off_o + align_up(rows * d * sizeof(float), 256);
   return *off_ml + align_up(rows * 2 * sizeof(float), 256);
 }
 
-// Workspace of the fixed KV splits: partial O and (m, l) per (segment, split,
-// query row); a segment is `seg_heads` KV heads of one sequence.
+// Workspace of the fixed KV splits: partial O and (m, l) per (KV head, split,
+// query row) of every sequence.
 static size_t attn_ws_bytes(int batch, int block_len, int hq, int hkv, int d, int max_ctx,
-                            int seg_heads, int *num_splits, int *split_keys, size_t *off_ml) {
-  choose_split(batch * (hkv / seg_heads), block_len, max_ctx, num_splits, split_keys);
-  if (*num_splits == 1) {
-    *off_ml = 0;
-    return 0;
-  }
+                            int *num_splits, int *split_keys, size_t *off_o, size_t *off_ml) {
+  choose_split(batch * hkv, block_len, max_ctx, num_splits, split_keys);
   const size_t rows = (size_t)batch * hkv * (*num_splits) * block_len * (hq / hkv);
-  *off_ml = align_up(rows * d * sizeof(float), 256);
+  *off_o = attn_counter_bytes(batch, hkv);
+  if (*num_splits == 1) {
+    *off_ml = *off_o;
+    return *off_o;
+  }
+  *off_ml = *off_o + align_up(rows * d * sizeof(float), 256);
   return *off_ml + align_up(rows * 2 * sizeof(float), 256);
 }
 
@@ -190,15 +199,11 @@ BD_API size_t bd_block_attention_workspace(int32_t batch, int32_t block_len, int
   if (!attn_shape_ok(batch, block_len, num_q_heads, num_kv_heads, head_dim, max_ctx)) return 0;
   preload_all();
   int ns, sk;
-  size_t off_ml, so, sm;
-  size_t need = std::max(attn_ws_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim,
-                                       max_ctx, 1, &ns, &sk, &off_ml),
-                         attn_sk_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim,
-                                       num_sms(), &so, &sm));
-  if (num_kv_heads % 2 == 0)
-    need = std::max(need, attn_ws_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim,
-                                        max_ctx, 2, &ns, &sk, &off_ml));
-  return need;
+  size_t a, b, c;
+  return std::max(attn_ws_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim, max_ctx,
+                                &ns, &sk, &a, &b),
+                  attn_sk_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim, num_sms(),
+                                &a, &b, &c));
 }
 
 BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_len,
@@ -234,56 +239,45 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
   p.tokens = tokens;
   p.out = out;
   p.dev_status = dev_status;
-  size_t off_ml, sk_o, sk_ml;
   p.grid = num_sms();
   p.seg_heads = 1;
-  // Kernel choice: by shape (below), unless a test forced one kernel with
-  // bd_debug_force_attention_kernel
+  // Kernel choice, by shape: for bf16 at head_dim 128 and 64 query rows per
+  // KV head (the SDAR shapes), the tcgen05 head-pair kernel on large problems
+  // and the mma.sync kernel with fixed splits on small ones (a few pages per
+  // SM, where its shorter start wins); the mma.sync kernel for other bf16
+  // shapes; SIMT for fp32.  A test may force one kernel with
+  // bd_debug_force_attention_kernel.
   const int forced = g_forced_attention.load(std::memory_order_relaxed);
-  const bool force_simt = forced == BD_ATTN_SIMT;
-  const bool force_pair_plan = forced == BD_ATTN_PAIR_PLAN;
-  const bool force_pair = forced == BD_ATTN_PAIR || force_pair_plan;
-  const bool force_mma = forced == BD_ATTN_MMA;
-  const bool small = attn_small(batch, p.hkv, block_len, max_ctx) && !force_pair_plan;
-  // fixed splits of the head-pair kernel: split per head pair
-  const bool pair_split = small && force_pair && p.hkv % 2 == 0;
+  const bool small = attn_small(batch, p.hkv, block_len, max_ctx);
+  size_t fs_o, fs_ml, off_plan, sk_o, sk_ml;
   const size_t need = std::max(
-      attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx,
-                    pair_split ? 2 : 1, &p.num_splits, &p.split_keys, &off_ml),
-      attn_sk_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, p.grid, &sk_o, &sk_ml));
+      attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx, &p.num_splits,
+                    &p.split_keys, &fs_o, &fs_ml),
+      attn_sk_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, p.grid, &off_plan, &sk_o,
+                    &sk_ml));
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return BD_ERR_WORKSPACE;
-  // the split partials and the partition's buffers share the workspace (one
-  // scheme runs per call)
-  p.part_o = static_cast<float *>(ws);
-  p.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + off_ml);
+  char *w = static_cast<char *>(ws);
+  p.counters = reinterpret_cast<int *>(w);
+  p.part_o = reinterpret_cast<float *>(w + fs_o);
+  p.part_ml = reinterpret_cast<float *>(w + fs_ml);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (forced == BD_ATTN_PAIR || (forced == BD_ATTN_AUTO && !small)) {
+    AttnParams pp = p;
+    pp.sk_o = reinterpret_cast<float *>(w + sk_o);
+    pp.sk_ml = reinterpret_cast<float *>(w + sk_ml);
+    if (attention_pair_supported(pp)) return attention_pair(pp, st);
+  }
   if (small) {
-    // fixed splits: the mma.sync kernel writes its partials where the
-    // split combine reads them
+    // fixed splits: the kernel writes its partials where the split combine reads them
     p.plan = nullptr;
     p.sk_o = p.part_o;
     p.sk_ml = p.part_ml;
   } else {
-    p.plan = static_cast<int *>(ws);
-    p.sk_o = reinterpret_cast<float *>(static_cast<char *>(ws) + sk_o);
-    p.sk_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + sk_ml);
+    p.plan = reinterpret_cast<int *>(w + off_plan);
+    p.sk_o = reinterpret_cast<float *>(w + sk_o);
+    p.sk_ml = reinterpret_cast<float *>(w + sk_ml);
   }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // Default: for bf16 at head_dim 128 and 64 query rows per KV head (the SDAR
-  // shapes), the tcgen05 head-pair kernel on large problems and the mma.sync
-  // kernel with fixed splits on small ones (a few pages per SM, where its
-  // shorter start wins); the mma.sync kernel for other bf16 shapes; SIMT for
-  // fp32.
-  if (pair_split || ((force_pair || (!force_simt && !force_mma)) && p.plan)) {
-    if (attention_pair_supported(p)) return attention_pair(p, st);
-    if (pair_split) {            // shape not supported: the default kernel, default splits
-      if (ws_bytes < attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx, 1,
-                                   &p.num_splits, &p.split_keys, &off_ml))
-        return BD_ERR_WORKSPACE;
-      p.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + off_ml);
-      p.sk_ml = p.part_ml;
-    }
-  }
-  if (!force_simt) {
+  if (forced != BD_ATTN_SIMT) {
     const bd_status s = attention_tc(p, st);
     if (s != BD_ERR_UNSUPPORTED) return s;
   }

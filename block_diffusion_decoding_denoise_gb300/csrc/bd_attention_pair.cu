@@ -22,16 +22,30 @@
 // The off-diagonal halves of MMA1 and MMA2 are wasted work; the tensor pipe
 // has several times the throughput this HBM-bound loop needs.
 //
-// Work partition: the tile-range plan of attn_plan_kernel over (sequence,
-// KV-head pair) segments; a segment inside one CTA's range is written as the
-// final output, a cut one leaves a partial per piece in slot segment + CTA
-// (merged by attn_combine_sk_kernel).
+// One launch does the whole call.
+//   Plan: the tiles of (sequence, KV-head pair) segments are laid end to end
+//   (a sequence with no masked position has none); CTA c of the persistent
+//   grid takes the equal range [c T / G, (c + 1) T / G).  Warp 0 of every
+//   CTA finds its range with a warp-wide scan of the sequences' tile counts.
+//   Merge: a segment inside one CTA's range is written as the final output.
+//   A segment cut by range boundaries leaves one partial per piece (O, and
+//   the running max and sum per row) in slot segment + CTA.  After its last
+//   tile each CTA counts its cut pieces in per-segment counters; the CTA
+//   whose count completes a segment merges that segment's partials: it
+//   bulk-copies them through shared memory (the K/V ring is free by then)
+//   and writes the output.  It also sets the counter back to zero, so the
+//   counters (at the start of the workspace) must be zero before the first
+//   call and stay zero between calls.
+//   L2 prefetch: the producer also asks L2 for the pages a few tiles ahead of
+//   the shared-memory ring, so more of the stream is in flight than the ring
+//   holds.
 //
 // Warp roles (192 threads, one CTA per SM):
 //   warp 0     TMA producer: Q of each piece, K and V of each tile (three stages)
 //   warp 1     TMEM allocator and MMA issuer: MMA1 of tile t, then MMA2 of
 //              tile t - 1 (the softmax of t overlaps MMA2 of t - 1)
 //   warps 2-5  softmax, O rescale and the output of each piece
+//   all        the merges of the segments this CTA completes
 // Every wait is bounded; on expiry the kernel records BD_ERR_TIMEOUT, stops
 // issuing, waits (bounded) for its copies and MMAs, frees TMEM and returns.
 #include <math.h>
@@ -60,6 +74,9 @@ constexpr uint32_t kColO = 256;
 constexpr uint32_t kColP = 384;             // P buffer b at kColP + 64 b: 128 keys as bf16 pairs
 constexpr float kLazy = 8.f;                // max moves only beyond 2^8
 constexpr int kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8;
+constexpr int kPrefetchDist = kStages + 2;  // tiles ahead of the issue point asked of L2
+constexpr int kPieceBytes = kRows * D * 4;  // partial O of one piece: 64 KB
+constexpr int kMaxCut = 2;                  // cut pieces per CTA range (its first and last)
 
 struct Meta {
   int item, lo, hi, flags, slot;
@@ -75,8 +92,14 @@ struct Smem {
   uint64_t s_full[2], s_empty[2], p_full[2];
   uint64_t o_done, o_empty;
   uint64_t mma_done;
+  uint64_t merge_full[3];
   uint32_t tmem_base;
   volatile int abort_flag;
+  int ncut, nmerge;                         // cut pieces written; segments to merge
+  int plan_T;                               // tiles of the whole call
+  int cut_seg[kMaxCut], cut_c0[kMaxCut], cut_c1[kMaxCut];
+  int mrg_seg[kMaxCut], mrg_c0[kMaxCut], mrg_c1[kMaxCut], mrg_b[kMaxCut], mrg_hp[kMaxCut];
+  int cut_b[kMaxCut], cut_hp[kMaxCut];
 };
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, int32_t c0,
@@ -90,6 +113,33 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, 
 
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Ask L2 for one box of a 4-D map (no shared memory, no completion signal).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *m, int32_t c0, int32_t c1,
+                                                int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+// Contiguous global -> shared copy of `bytes` (a multiple of 16, both
+// addresses 16-byte aligned), completion as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// CTA of the tile-range partition that holds tile t, and whether CTA c's
+// range is non-empty (T tiles over G CTAs).
+__device__ __forceinline__ bool range_nonempty(int c, long long T, long long G) {
+  return ((long long)c * T) / G < ((long long)(c + 1) * T) / G;
 }
 
 // MN-major operand in the 128-byte-swizzled layout a TMA load of [key][64 d]
@@ -171,7 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm.o_done), 1);
     mbar_init(smem_u32(&sm.o_empty), 4);
     mbar_init(smem_u32(&sm.mma_done), 1);
+    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&sm.merge_full[i]), 1);
     sm.abort_flag = 0;
+    sm.ncut = 0;
+    sm.nmerge = 0;
+    sm.plan_T = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -207,6 +261,60 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // tiles of sequence b: its cached pages + the block's own keys, or none
+    // when it has no masked position (or an invalid context)
+    auto seq_tiles = [&](int b) -> int {
+      bool active = true;
+      if (p.tokens) {
+        active = false;
+        const int32_t *tk = p.tokens + (size_t)b * L;
+        for (int i = 0; i < L; ++i) active |= tk[i] == BD_MASK;
+      }
+      const int ctx = p.ctx_len[b];
+      if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) {
+        if (active) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+        return 0;
+      }
+      return active ? (ctx + kPage - 1) / kPage + 1 : 0;
+    };
+    // the plan: T = all tiles; this CTA's range [t_begin, t_end) and the
+    // sequence holding t_begin (warp-wide passes over the sequences)
+    const int c = blockIdx.x, G = gridDim.x;
+    int T = 0;
+    for (int b0 = 0; b0 < p.batch; b0 += 32) {
+      int v = (b0 + lane < p.batch) ? npairs * seq_tiles(b0 + lane) : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      T += v;
+    }
+    if (lane == 0) sm.plan_T = T;
+    const int t_begin = (int)(((long long)c * T) / G);
+    const int t_end = (int)(((long long)(c + 1) * T) / G);
+    int b_first = -1, base_first = 0, tiles_first = 0;
+    if (t_begin < t_end) {
+      int carry = 0;
+      for (int b0 = 0; b0 < p.batch && b_first < 0; b0 += 32) {
+        const int b = b0 + lane;
+        const int tl = b < p.batch ? seq_tiles(b) : 0;
+        const int v = npairs * tl;
+        int inc = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += u;
+        }
+        const int excl = carry + inc - v;
+        const unsigned hit = __ballot_sync(0xffffffffu, v > 0 && excl <= t_begin &&
+                                                            t_begin < excl + v);
+        if (hit) {
+          const int src = __ffs(hit) - 1;
+          b_first = __shfl_sync(0xffffffffu, b, src);
+          base_first = __shfl_sync(0xffffffffu, excl, src);
+          tiles_first = __shfl_sync(0xffffffffu, tl, src);
+        }
+        carry += __shfl_sync(0xffffffffu, inc, 31);
+      }
+    }
     uint32_t it = 0, pc = 0;
     bool stop = false;
     if (lane == 0) {
@@ -215,6 +323,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // [blo, bhi)); false once stopped
       auto emit = [&](int b, int hp, int ctx, int npg, int u_first, int u_last, int blo,
                       int bhi, int seg, int slot) -> bool {
+        const int32_t *prow = p.page_table + (size_t)b * p.max_pages;
+        auto prefetch = [&](int pg) {
+          if (pg < 0 || pg >= p.num_pages) return;
+          for (int hs = 0; hs < 2; ++hs)
+            for (int h = 0; h < 2; ++h) {
+              tma_prefetch_4d(&mk_pool, 64 * h, 0, 2 * hp + hs, pg);
+              tma_prefetch_4d(&mv_pool, 64 * h, 0, 2 * hp + hs, pg);
+            }
+        };
+        for (int u = u_first; u < min(u_first + kPrefetchDist, min(u_last, npg)); ++u)
+          prefetch(prow[u]);
         if (pc > 0 && !mbar_wait(smem_u32(&sm.q_empty), (pc - 1) & 1)) {
           fail();
           return false;
@@ -230,6 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++pc;
         for (int u = u_first; u < u_last; ++u, ++it) {
           const uint32_t s = it % kStages, round = it / kStages;
+          // page ids are read before the wait, so the wait covers their latency
+          const int pg = u < npg ? prow[u] : -1;
+          const int upf = u + kPrefetchDist;
+          const int pgpf = (upf < u_last && upf < npg) ? prow[upf] : -1;
           if (sm.abort_flag) return false;
           if (round > 0 && !mbar_wait(smem_u32(&sm.kv_empty[s]), (round - 1) & 1)) {
             fail();
@@ -242,7 +365,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           m.lo = 0;
           m.flags = (u == u_first ? kFirst : 0) | (u == u_last - 1 ? kLast : 0);
           if (u < npg) {
-            const int pg = p.page_table[(size_t)b * p.max_pages + u];
             m.hi = min(kPage, ctx - u * kPage);
             if (pg >= 0 && pg < p.num_pages) {
               sm.meta[s] = m;
@@ -276,28 +398,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             2 * hp + hs, 0, b, bar);
               }
           }
+          if (pgpf >= 0) prefetch(pgpf);
         }
         return true;
       };
-      if (p.plan) {
-        // tile-range partition: this CTA's tiles [t_begin, t_end) of the plan's T
-        const int T = p.plan[2 * p.batch];
-        const int c = blockIdx.x, G = gridDim.x;
-        const int t_begin = (int)(((long long)c * T) / G);
-        const int t_end = (int)(((long long)(c + 1) * T) / G);
-        int b = 0;
-        {                                      // last sequence with base <= t_begin
-          int lo = 0, hi = p.batch - 1;
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.plan[2 * mid] <= t_begin) lo = mid;
-            else hi = mid - 1;
-          }
-          b = lo;
-        }
+      if (b_first >= 0) {
+        int b = b_first, base = base_first, tiles = tiles_first;
         for (int t = t_begin; t < t_end && !stop;) {
-          while (b < p.batch - 1 && t >= p.plan[2 * b] + npairs * p.plan[2 * b + 1]) ++b;
-          const int base = p.plan[2 * b], tiles = p.plan[2 * b + 1];
+          while (b < p.batch - 1 && t >= base + npairs * tiles) {
+            base += npairs * tiles;
+            ++b;
+            tiles = seq_tiles(b);
+          }
           if (tiles <= 0 || t < base || t >= base + npairs * tiles) {
             flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
             break;
@@ -306,39 +418,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int seg0 = base + hp * tiles;
           const int u1 = min(seg0 + tiles, t_end) - seg0;
           const int seg = b * npairs + hp;
-          const int slot = (u0 == 0 && u1 == tiles) ? -1 : seg + c;
-          stop = !emit(b, hp, p.ctx_len[b], tiles - 1, u0, u1, 0, L, seg, slot);
+          const bool whole = u0 == 0 && u1 == tiles;
+          if (!whole) {
+            if (sm.ncut >= kMaxCut) {                // cannot happen: a range cuts at
+              flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);   // most its two ends
+              break;
+            }
+            const int k = sm.ncut++;
+            sm.cut_seg[k] = seg;
+            sm.cut_b[k] = b;
+            sm.cut_hp[k] = hp;
+            sm.cut_c0[k] = sk_cta_of(seg0, T, G);
+            sm.cut_c1[k] = sk_cta_of(seg0 + tiles - 1, T, G);
+          }
+          stop = !emit(b, hp, p.ctx_len[b], tiles - 1, u0, u1, 0, L, seg, whole ? -1 : seg + c);
           t = seg0 + u1;
-        }
-      } else {
-        // fixed KV splits (small problems): items (sequence, head pair, split)
-        // dealt round-robin; split s covers keys [s * split_keys, + split_keys)
-        const int nitems = p.batch * npairs * p.num_splits;
-        for (int item = blockIdx.x; item < nitems && !stop; item += gridDim.x) {
-          const int split = item % p.num_splits;
-          const int hp = (item / p.num_splits) % npairs;
-          const int b = item / (p.num_splits * npairs);
-          if (p.tokens) {
-            bool masked = false;
-            for (int i = 0; i < L; ++i) masked |= p.tokens[(size_t)b * L + i] == BD_MASK;
-            if (!masked) continue;
-          }
-          const int ctx = p.ctx_len[b];
-          if (ctx < 0 || ctx > p.max_ctx || ctx > p.max_pages * p.page_size) {
-            if (split == 0 && hp == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
-            continue;
-          }
-          const int kbeg = split * p.split_keys;
-          const int kend = min(ctx + L, kbeg + p.split_keys);
-          if (kbeg >= kend) continue;            // no key of this sequence in this split
-          const int npg = (ctx + kPage - 1) / kPage;
-          const int p_first = kbeg / kPage;
-          const int p_end = kbeg < ctx ? (min(kend, ctx) + kPage - 1) / kPage : p_first;
-          const int u_last = kend > ctx ? npg + 1 : p_end;   // the block tile follows page npg - 1
-          const int seg = b * npairs + hp;
-          const int slot = p.num_splits == 1 ? -1 : seg * p.num_splits + split;
-          stop = !emit(b, hp, ctx, npg, p_first, u_last, max(kbeg, ctx) - ctx, kend - ctx, seg,
-                       slot);
         }
       }
       if (!stop) {                             // sentinel stage: no more work
@@ -619,11 +713,147 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) fail();
   }
 
+  // every partial this CTA wrote is visible device-wide before it is counted
+  __threadfence();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+
+  // ------------------------------------------------------------ merges
+  // count this CTA's cut pieces; the CTA that completes a segment merges it
+  if (threadIdx.x == 0 && !sm.abort_flag) {
+    for (int k = 0; k < sm.ncut; ++k) {
+      const int seg = sm.cut_seg[k], c0 = sm.cut_c0[k], c1 = sm.cut_c1[k];
+      int n = 0;
+      for (int cc = c0; cc <= c1; ++cc) n += range_nonempty(cc, sm.plan_T, gridDim.x) ? 1 : 0;
+      const int old = atomicAdd(&p.counters[seg], 1);
+      if (old >= n - 1) {
+        if (old != n - 1) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);   // stale counter
+        atomicExch(&p.counters[seg], 0);
+        const int j = sm.nmerge++;
+        sm.mrg_seg[j] = seg;
+        sm.mrg_c0[j] = c0;
+        sm.mrg_c1[j] = c1;
+        sm.mrg_b[j] = sm.cut_b[k];
+        sm.mrg_hp[j] = sm.cut_hp[k];
+      }
+    }
+    __threadfence();                           // the other pieces' partials, before reading
+  }
+  __syncthreads();
+  const int nmerge = sm.nmerge;
+  if (nmerge == 0) return;
+  float *wt = reinterpret_cast<float *>(&sm.q[0][0]);        // [128 rows][64 pieces]
+  float *acc = reinterpret_cast<float *>(&sm.k[0][0][0]);    // 64 KB: piece 0, then the sum
+  const int tid = threadIdx.x;
+  uint32_t uses[3] = {0, 0, 0};                              // phases of merge_full[i]
+  uint32_t issued[3] = {0, 0, 0};                            // copies issued (thread 0)
+  for (int j = 0; j < nmerge; ++j) {
+    const int seg = sm.mrg_seg[j], c0 = sm.mrg_c0[j], c1 = sm.mrg_c1[j];
+    const int b = sm.mrg_b[j], hp = sm.mrg_hp[j];
+    const long long Tm = sm.plan_T;
+    // slot of the k-th piece: segment + the k-th CTA of [c0, c1] with tiles
+    auto slot_of = [&](int k) -> int {
+      for (int cc = c0; cc <= c1; ++cc)
+        if (range_nonempty(cc, Tm, gridDim.x) && k-- == 0) return seg + cc;
+      return -1;
+    };
+    int P = 0;
+    for (int cc = c0; cc <= c1; ++cc) P += range_nonempty(cc, Tm, gridDim.x) ? 1 : 0;
+    // row statistics (one thread per row): M = max_k m_k, L = sum_k l_k e^(m_k - M)
+    float Mr = -INFINITY, Linv = 0.f;
+    if (tid < kRows) {
+      for (int k = 0; k < P; ++k) Mr = fmaxf(Mr, __ldcg(&p.sk_ml[((size_t)slot_of(k) * kRows + tid) * 2]));
+      float Lr = 0.f;
+      for (int k = 0; k < P; ++k) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
+            p.sk_ml + ((size_t)slot_of(k) * kRows + tid) * 2));
+        Lr += ml.y * __expf(ml.x - Mr);
+      }
+      Linv = Lr > 0.f ? 1.f / Lr : 0.f;
+    }
+    auto fill_weights = [&](int k0) {         // weights of pieces [k0, k0 + 64)
+      if (tid < kRows)
+        for (int k = k0; k < min(P, k0 + 64); ++k) {
+          const float m = __ldcg(&p.sk_ml[((size_t)slot_of(k) * kRows + tid) * 2]);
+          wt[tid * 64 + (k - k0)] = __expf(m - Mr) * Linv;
+        }
+    };
+    auto issue = [&](int k) {                 // piece k into its buffer (thread 0)
+      const int bi = k == 0 ? 0 : 1 + ((k - 1) & 1);
+      const uint32_t bar = smem_u32(&sm.merge_full[bi]);
+      fence_proxy_async();
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      mbar_arrive_expect_tx(bar, kPieceBytes);
+      bulk_load(smem_u32(acc + (size_t)bi * (kPieceBytes / 4)),
+                p.sk_o + (size_t)slot_of(k) * kRows * D, kPieceBytes, bar);
+      ++issued[bi];
+    };
+    if (tid == 0)
+      for (int k = 0; k < min(P, 3); ++k) issue(k);
+    fill_weights(0);
+    __syncthreads();
+    bool failed = false;
+    for (int k = 0; k < P && !failed; ++k) {
+      const int bi = k == 0 ? 0 : 1 + ((k - 1) & 1);
+      if (k > 0 && k % 64 == 0) {
+        __syncthreads();
+        fill_weights(k);
+        __syncthreads();
+      }
+      const bool ok = mbar_wait(smem_u32(&sm.merge_full[bi]), uses[bi] & 1);
+      ++uses[bi];
+      if (__syncthreads_or(!ok)) {
+        failed = true;
+        break;
+      }
+      const float4 *src = reinterpret_cast<const float4 *>(acc + (size_t)bi * (kPieceBytes / 4));
+      float4 *dst = reinterpret_cast<float4 *>(acc);
+      const int kw = k % 64;
+      for (int e = tid; e < kRows * D / 4; e += kThreads) {
+        const float w = wt[(e >> 5) * 64 + kw];
+        const float4 x = src[e];
+        if (k == 0) {
+          dst[e] = make_float4(x.x * w, x.y * w, x.z * w, x.w * w);
+        } else {
+          float4 a = dst[e];
+          a.x = fmaf(x.x, w, a.x);
+          a.y = fmaf(x.y, w, a.y);
+          a.z = fmaf(x.z, w, a.z);
+          a.w = fmaf(x.w, w, a.w);
+          dst[e] = a;
+        }
+      }
+      fence_proxy_async();                     // generic reads of buffer bi before the
+      __syncthreads();                         // next bulk copy rewrites it
+      if (tid == 0 && k > 0 && k + 2 < P) issue(k + 2);
+    }
+    if (failed) {
+      if (tid == 0) {                          // wait (bounded) for copies in flight
+        flag_error(p.dev_status, BD_ERR_TIMEOUT);
+        for (int i = 0; i < 3; ++i)
+          for (; uses[i] < issued[i]; ++uses[i]) mbar_wait(smem_u32(&sm.merge_full[i]), uses[i] & 1);
+      }
+      __syncthreads();
+      return;
+    }
+    // the merged rows to the output: row r of the pair is head 2 hp + r / 64,
+    // query row r % 64 = i * group + j of that head
+    const float4 *res = reinterpret_cast<const float4 *>(acc);
+    for (int e = tid; e < kRows * D / 4; e += kThreads) {
+      const int r = e >> 5, d4 = e & 31;
+      const int g = 2 * hp + (r >> 6), rr = r & 63;
+      const int qi = rr / group, h = g * group + rr % group;
+      const float4 x = res[e];
+      __nv_bfloat16 *out =
+          static_cast<__nv_bfloat16 *>(p.out) + (((size_t)b * L + qi) * p.hq + h) * D + 4 * d4;
+      *reinterpret_cast<uint2 *>(out) = make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+    }
+    fence_proxy_async();
+    __syncthreads();                           // acc and wt are reused by the next merge
   }
 }
 
@@ -635,7 +865,7 @@ bool attention_pair_supported(const AttnParams &p) {
   if (p.dtype != BD_BF16 || p.head_dim != D || p.page_size != kPage) return false;
   if (p.hkv % 2 != 0 || p.hq % p.hkv != 0) return false;
   if (p.block_len * (p.hq / p.hkv) != 64) return false;
-  if (p.grid < 1 || ((p.plan || p.num_splits > 1) && (!p.sk_o || !p.sk_ml))) return false;
+  if (p.grid < 1 || !p.sk_o || !p.sk_ml || !p.counters) return false;
   if ((long long)p.batch * (p.hkv / 2) * (p.max_pages + 1) >= (1LL << 30)) return false;
   const DevInfo d = dev_info();
   return d.major >= 10 && tma_available();
@@ -670,18 +900,10 @@ bd_status attention_pair(const AttnParams &p0, cudaStream_t st) {
       !tma_encode_bf16(&mq, 4, p.q, qdims, qstr, qbox))
     return BD_ERR_CUDA;
   const size_t smem = sizeof(Smem) + 1024;
-  int grid = p.grid;
-  if (p.plan) {
-    if (attention_plan_launch(p, st) != cudaSuccess) return BD_ERR_CUDA;
-  } else {
-    grid = std::max(1, std::min(p.batch * (p.hkv / 2) * p.num_splits, p.grid));
-  }
-  const cudaError_t e =
-      launch_pdl(attn_pair_kernel, dim3(grid), dim3(kThreads), smem, st, mkp, mvp, mkb, mvb, mq, p);
+  const cudaError_t e = launch_pdl(attn_pair_kernel, dim3(p.grid), dim3(kThreads), smem, st, mkp,
+                                   mvp, mkb, mvb, mq, p);
   count_launches(1);
-  if (e != cudaSuccess) return BD_ERR_CUDA;
-  if (p.plan) return attention_combine_sk(p, st);
-  return p.num_splits > 1 ? attention_combine(p, st) : BD_OK;
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
 
 }  // namespace bd

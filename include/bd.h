@@ -99,7 +99,13 @@ typedef struct {
  *   out       [batch][block_len][num_q_heads][head_dim], dtype
  *   max_ctx   host-side upper bound on ctx_len (sizes the KV split).
  *   ws        device workspace of at least bd_block_attention_workspace() bytes,
- *             256-byte aligned; its contents need no initialisation.
+ *             256-byte aligned.  Zero-fill it once before its first call (e.g.
+ *             cudaMemsetAsync): its first bytes count the pieces of key
+ *             segments that several CTAs share, and every call that completes
+ *             without a device error leaves them zero again.  After a call
+ *             that reported BD_ERR_TIMEOUT or BD_ERR_DEVICE_CHECK, zero it
+ *             again before reusing it.  Calls that share a workspace must be
+ *             ordered on the GPU (one stream).
  * Limits: head_dim 64 or 128; block_len 1..32; num_q_heads % num_kv_heads == 0;
  *         block_len * (num_q_heads / num_kv_heads) <= 128.
  * ------------------------------------------------------------------------ */
@@ -397,11 +403,9 @@ uint64_t bd_kernel_launches(void);
  * ------------------------------------------------------------------------ */
 typedef enum {
   BD_ATTN_AUTO = 0,      /* by shape                                        */
-  BD_ATTN_PAIR = 1,      /* tcgen05 head-pair kernel                        */
-  BD_ATTN_PAIR_PLAN = 2, /* head-pair kernel with the tile-range partition
-                            even on small problems                          */
-  BD_ATTN_MMA = 3,       /* mma.sync kernel (bf16)                          */
-  BD_ATTN_SIMT = 4       /* SIMT kernel                                     */
+  BD_ATTN_PAIR = 1,      /* tcgen05 head-pair kernel, also on small problems */
+  BD_ATTN_MMA = 2,       /* mma.sync kernel (bf16)                          */
+  BD_ATTN_SIMT = 3       /* SIMT kernel                                     */
 } bd_attention_kernel;
 
 bd_status bd_debug_force_attention_kernel(int32_t which);

@@ -70,7 +70,7 @@ def gpu_attention(s: Setup, q, k_blk, v_blk, tokens=None):
                      dtype=torch_dtype(w.dtype), device="cuda")
     nws = bd.bd_block_attention_workspace(w.batch, w.block_len, w.num_q_heads, w.num_kv_heads,
                                           w.head_dim, s.max_ctx)
-    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(nws, 1), dtype=torch.uint8, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     bd.bd_block_attention(s.cache.kv, s.ctx_len, tokens, dev(q, w.dtype), dev(k_blk, w.dtype),
                           dev(v_blk, w.dtype), out, ws, s.max_ctx, dev_status=st)

@@ -5,9 +5,9 @@ at the SDAR shapes, the mma.sync kernel for the other bf16 cases and the SIMT
 kernel for fp32, chosen by shape alone.  The library's test hook
 bd_debug_force_attention_kernel forces one kernel so that each is checked on
 small, ragged and full-size inputs (a kernel that does not support a shape
-falls back to the one the shape picks).  "pair" runs the head-pair kernel with fixed KV splits on small
-problems and the tile-range partition on large ones; "pair_plan" runs the
-partition on every problem, which covers more CTAs than tiles.
+falls back to the one the shape picks).  "pair" runs the head-pair kernel
+on every problem: on small ones its tile ranges give more CTAs than tiles and
+many pieces per segment, all merged inside the launch.
 """
 import numpy as np
 import pytest
@@ -33,7 +33,7 @@ def _lib():
     bd.load()
 
 
-@pytest.fixture(params=["auto", "pair", "pair_plan", "mma", "simt"])
+@pytest.fixture(params=["auto", "pair", "mma", "simt"])
 def impl(request):
     bd.bd_debug_force_attention_kernel(request.param)
     yield request.param

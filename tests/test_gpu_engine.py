@@ -188,11 +188,13 @@ def test_engine_tsweep_b32_all_thresholds(a_max):
     _assert_counts(c, a_max > 12)
     means = [float(st[T].mean()) for T in SWEEP]
     print(f"\ntsweep_b32 a_max {a_max:g}: steps per block by T {dict(zip(SWEEP, means))}")
+    assert all(x <= y for x, y in zip(means, means[1:]))   # a higher T never takes fewer
     if a_max == 12.0:
-        assert all(m == 32.0 for m in means)         # no position ever reaches 0.5
+        # the literal recipe almost never reaches 0.5 (one position in the whole
+        # run did at T = 0.5), and never 0.7 or more
+        assert means[0] >= 31.5 and all(m == 32.0 for m in means[1:])
     else:
         assert means[0] < means[-1]                  # a lower threshold takes fewer steps
-        assert all(x <= y for x, y in zip(means, means[1:]))
 
 
 # --- longctx_b8 (28-layer decoder stack) ------------------------------------

@@ -140,7 +140,7 @@ def test_attention_corrupt_page_table_sets_status():
                       device="cuda")
     nws = bd.bd_block_attention_workspace(w.batch, w.block_len, w.num_q_heads, w.num_kv_heads,
                                           w.head_dim, s.max_ctx)
-    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(nws, 1), dtype=torch.uint8, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     bd.bd_block_attention(s.cache.kv, s.ctx_len, None, dev(q, "bf16"), dev(kb, "bf16"),
                           dev(vb, "bf16"), out, ws, s.max_ctx, dev_status=st)
