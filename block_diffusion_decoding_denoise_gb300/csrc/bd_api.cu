@@ -101,13 +101,10 @@ static bool attn_shape_ok(int32_t batch, int32_t block_len, int32_t hq, int32_t 
   return true;
 }
 
-// Every attention workspace starts with the head-pair kernel's merge
-// counters (one int per (sequence, KV-head pair)); they must be zero before a
-// call and every call that completes leaves them zero.  The other buffers of
-// a call follow them.
-static size_t attn_counter_bytes(int batch, int hkv) {
-  return align_up((size_t)batch * std::max(1, hkv / 2) * sizeof(int), 256);
-}
+// Every attention workspace starts with the head-pair kernel's merge jobs
+// (eight ints per CTA of the persistent grid, rewritten by every call); the
+// other buffers of a call follow them.
+static size_t attn_job_bytes(int grid) { return align_up((size_t)grid * 8 * sizeof(int), 256); }
 
 // Workspace of the tile-range partition: the plan (mma.sync kernel), then
 // partial O and (m, l) for batch * hkv + 2 grid slots of R rows (the
@@ -115,7 +112,7 @@ static size_t attn_counter_bytes(int batch, int hkv) {
 static size_t attn_sk_bytes(int batch, int block_len, int hq, int hkv, int d, int grid,
                             size_t *off_plan, size_t *off_o, size_t *off_ml) {
   const size_t rows = ((size_t)batch * hkv + 2 * (size_t)grid) * block_len * (hq / hkv);
-  *off_plan = attn_counter_bytes(batch, hkv);
+  *off_plan = attn_job_bytes(grid);
   *off_o = *off_plan + align_up((2 * (size_t)batch + 1) * sizeof(int), 256);
   *off_ml = *off_o + align_up(rows * d * sizeof(float), 256);
   return *off_ml + align_up(rows * 2 * sizeof(float), 256);
@@ -124,10 +121,11 @@ static size_t attn_sk_bytes(int batch, int block_len, int hq, int hkv, int d, in
 // Workspace of the fixed KV splits: partial O and (m, l) per (KV head, split,
 // query row) of every sequence.
 static size_t attn_ws_bytes(int batch, int block_len, int hq, int hkv, int d, int max_ctx,
-                            int *num_splits, int *split_keys, size_t *off_o, size_t *off_ml) {
+                            int grid, int *num_splits, int *split_keys, size_t *off_o,
+                            size_t *off_ml) {
   choose_split(batch * hkv, block_len, max_ctx, num_splits, split_keys);
   const size_t rows = (size_t)batch * hkv * (*num_splits) * block_len * (hq / hkv);
-  *off_o = attn_counter_bytes(batch, hkv);
+  *off_o = attn_job_bytes(grid);
   if (*num_splits == 1) {
     *off_ml = *off_o;
     return *off_o;
@@ -201,7 +199,7 @@ BD_API size_t bd_block_attention_workspace(int32_t batch, int32_t block_len, int
   int ns, sk;
   size_t a, b, c;
   return std::max(attn_ws_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim, max_ctx,
-                                &ns, &sk, &a, &b),
+                                num_sms(), &ns, &sk, &a, &b),
                   attn_sk_bytes(batch, block_len, num_q_heads, num_kv_heads, head_dim, num_sms(),
                                 &a, &b, &c));
 }
@@ -251,13 +249,13 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
   const bool small = attn_small(batch, p.hkv, block_len, max_ctx);
   size_t fs_o, fs_ml, off_plan, sk_o, sk_ml;
   const size_t need = std::max(
-      attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx, &p.num_splits,
-                    &p.split_keys, &fs_o, &fs_ml),
+      attn_ws_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, max_ctx, p.grid,
+                    &p.num_splits, &p.split_keys, &fs_o, &fs_ml),
       attn_sk_bytes(batch, block_len, num_q_heads, p.hkv, p.head_dim, p.grid, &off_plan, &sk_o,
                     &sk_ml));
   if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)) return BD_ERR_WORKSPACE;
   char *w = static_cast<char *>(ws);
-  p.counters = reinterpret_cast<int *>(w);
+  p.jobs = reinterpret_cast<int *>(w);
   p.part_o = reinterpret_cast<float *>(w + fs_o);
   p.part_ml = reinterpret_cast<float *>(w + fs_ml);
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -29,8 +29,7 @@ struct AttnParams {
   int grid;
   int seg_heads;   // KV heads per segment: 1 (mma.sync kernel) or 2 (head-pair kernel)
   int *plan;       // [2 batch + 1]: base_b, tiles_b per sequence, then T
-  int *counters;   // [batch * hkv / 2] pieces counted per head-pair segment (head-pair
-                   // kernel); zero between calls
+  int *jobs;       // [grid][8] merge jobs of the head-pair kernel (one per CTA)
   float *sk_o;     // [batch * hkv + grid][R][head_dim]
   float *sk_ml;    // [batch * hkv + grid][R][2]
 };

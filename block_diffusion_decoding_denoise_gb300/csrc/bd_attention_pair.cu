@@ -22,30 +22,23 @@
 // The off-diagonal halves of MMA1 and MMA2 are wasted work; the tensor pipe
 // has several times the throughput this HBM-bound loop needs.
 //
-// One launch does the whole call.
-//   Plan: the tiles of (sequence, KV-head pair) segments are laid end to end
-//   (a sequence with no masked position has none); CTA c of the persistent
-//   grid takes the equal range [c T / G, (c + 1) T / G).  Warp 0 of every
-//   CTA finds its range with a warp-wide scan of the sequences' tile counts.
-//   Merge: a segment inside one CTA's range is written as the final output.
-//   A segment cut by range boundaries leaves one partial per piece (O, and
-//   the running max and sum per row) in slot segment + CTA.  After its last
-//   tile each CTA counts its cut pieces in per-segment counters; the CTA
-//   whose count completes a segment merges that segment's partials: it
-//   bulk-copies them through shared memory (the K/V ring is free by then)
-//   and writes the output.  It also sets the counter back to zero, so the
-//   counters (at the start of the workspace) must be zero before the first
-//   call and stay zero between calls.
-//   L2 prefetch: the producer also asks L2 for the pages a few tiles ahead of
-//   the shared-memory ring, so more of the stream is in flight than the ring
-//   holds.
+// Work partition: the tiles of (sequence, KV-head pair) segments are laid
+// end to end (a sequence with no masked position has none); CTA c of the
+// persistent grid takes the equal range [c T / G, (c + 1) T / G).  Warp 0 of
+// every CTA finds its range with a warp-wide scan of the sequences' tile
+// counts, so no separate plan launch precedes the kernel.  A segment inside
+// one CTA's range is written as the final output.  A segment cut by range
+// boundaries leaves one partial per piece (O, and the running max and sum
+// per row) in slot segment + CTA, and the CTA holding the segment's first
+// tile records a merge job; attn_pair_merge_kernel, launched right after,
+// merges each job's pieces, 32 rows per CTA with all loads of a row block in
+// flight at once.
 //
 // Warp roles (192 threads, one CTA per SM):
 //   warp 0     TMA producer: Q of each piece, K and V of each tile (three stages)
 //   warp 1     TMEM allocator and MMA issuer: MMA1 of tile t, then MMA2 of
 //              tile t - 1 (the softmax of t overlaps MMA2 of t - 1)
 //   warps 2-5  softmax, O rescale and the output of each piece
-//   all        the merges of the segments this CTA completes
 // Every wait is bounded; on expiry the kernel records BD_ERR_TIMEOUT, stops
 // issuing, waits (bounded) for its copies and MMAs, frees TMEM and returns.
 #include <math.h>
@@ -74,9 +67,7 @@ constexpr uint32_t kColO = 256;
 constexpr uint32_t kColP = 384;             // P buffer b at kColP + 64 b: 128 keys as bf16 pairs
 constexpr float kLazy = 8.f;                // max moves only beyond 2^8
 constexpr int kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8;
-constexpr int kPrefetchDist = kStages + 2;  // tiles ahead of the issue point asked of L2
-constexpr int kPieceBytes = kRows * D * 4;  // partial O of one piece: 64 KB
-constexpr int kMaxCut = 2;                  // cut pieces per CTA range (its first and last)
+constexpr int kJobInts = 8;                 // merge job: seg (-1: none), c1, b, hp, T
 
 struct Meta {
   int item, lo, hi, flags, slot;
@@ -92,14 +83,8 @@ struct Smem {
   uint64_t s_full[2], s_empty[2], p_full[2];
   uint64_t o_done, o_empty;
   uint64_t mma_done;
-  uint64_t merge_full[3];
   uint32_t tmem_base;
   volatile int abort_flag;
-  int ncut, nmerge;                         // cut pieces written; segments to merge
-  int plan_T;                               // tiles of the whole call
-  int cut_seg[kMaxCut], cut_c0[kMaxCut], cut_c1[kMaxCut];
-  int mrg_seg[kMaxCut], mrg_c0[kMaxCut], mrg_c1[kMaxCut], mrg_b[kMaxCut], mrg_hp[kMaxCut];
-  int cut_b[kMaxCut], cut_hp[kMaxCut];
 };
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, int32_t c0,
@@ -115,29 +100,7 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Ask L2 for one box of a 4-D map (no shared memory, no completion signal).
-__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *m, int32_t c0, int32_t c1,
-                                                int32_t c2, int32_t c3) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-          reinterpret_cast<uint64_t>(m)),
-      "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-      : "memory");
-}
-
-// Contiguous global -> shared copy of `bytes` (a multiple of 16, both
-// addresses 16-byte aligned), completion as transaction bytes on `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// CTA of the tile-range partition that holds tile t, and whether CTA c's
-// range is non-empty (T tiles over G CTAs).
+// Whether CTA c's tile range is non-empty (T tiles over G CTAs).
 __device__ __forceinline__ bool range_nonempty(int c, long long T, long long G) {
   return ((long long)c * T) / G < ((long long)(c + 1) * T) / G;
 }
@@ -221,11 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm.o_done), 1);
     mbar_init(smem_u32(&sm.o_empty), 4);
     mbar_init(smem_u32(&sm.mma_done), 1);
-    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&sm.merge_full[i]), 1);
     sm.abort_flag = 0;
-    sm.ncut = 0;
-    sm.nmerge = 0;
-    sm.plan_T = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -287,7 +246,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       T += v;
     }
-    if (lane == 0) sm.plan_T = T;
     const int t_begin = (int)(((long long)c * T) / G);
     const int t_end = (int)(((long long)(c + 1) * T) / G);
     int b_first = -1, base_first = 0, tiles_first = 0;
@@ -324,16 +282,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto emit = [&](int b, int hp, int ctx, int npg, int u_first, int u_last, int blo,
                       int bhi, int seg, int slot) -> bool {
         const int32_t *prow = p.page_table + (size_t)b * p.max_pages;
-        auto prefetch = [&](int pg) {
-          if (pg < 0 || pg >= p.num_pages) return;
-          for (int hs = 0; hs < 2; ++hs)
-            for (int h = 0; h < 2; ++h) {
-              tma_prefetch_4d(&mk_pool, 64 * h, 0, 2 * hp + hs, pg);
-              tma_prefetch_4d(&mv_pool, 64 * h, 0, 2 * hp + hs, pg);
-            }
-        };
-        for (int u = u_first; u < min(u_first + kPrefetchDist, min(u_last, npg)); ++u)
-          prefetch(prow[u]);
         if (pc > 0 && !mbar_wait(smem_u32(&sm.q_empty), (pc - 1) & 1)) {
           fail();
           return false;
@@ -349,10 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++pc;
         for (int u = u_first; u < u_last; ++u, ++it) {
           const uint32_t s = it % kStages, round = it / kStages;
-          // page ids are read before the wait, so the wait covers their latency
+          // the page id is read before the wait, so the wait covers its latency
           const int pg = u < npg ? prow[u] : -1;
-          const int upf = u + kPrefetchDist;
-          const int pgpf = (upf < u_last && upf < npg) ? prow[upf] : -1;
           if (sm.abort_flag) return false;
           if (round > 0 && !mbar_wait(smem_u32(&sm.kv_empty[s]), (round - 1) & 1)) {
             fail();
@@ -398,10 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             2 * hp + hs, 0, b, bar);
               }
           }
-          if (pgpf >= 0) prefetch(pgpf);
         }
         return true;
       };
+      int job[4] = {-1, 0, 0, 0};
       if (b_first >= 0) {
         int b = b_first, base = base_first, tiles = tiles_first;
         for (int t = t_begin; t < t_end && !stop;) {
@@ -419,21 +365,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int u1 = min(seg0 + tiles, t_end) - seg0;
           const int seg = b * npairs + hp;
           const bool whole = u0 == 0 && u1 == tiles;
-          if (!whole) {
-            if (sm.ncut >= kMaxCut) {                // cannot happen: a range cuts at
-              flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);   // most its two ends
-              break;
-            }
-            const int k = sm.ncut++;
-            sm.cut_seg[k] = seg;
-            sm.cut_b[k] = b;
-            sm.cut_hp[k] = hp;
-            sm.cut_c0[k] = sk_cta_of(seg0, T, G);
-            sm.cut_c1[k] = sk_cta_of(seg0 + tiles - 1, T, G);
+          if (!whole && u0 == 0) {               // this CTA holds the cut segment's first
+            job[0] = seg;                        // tile: it records the merge job
+            job[1] = sk_cta_of(seg0 + tiles - 1, T, G);
+            job[2] = b;
+            job[3] = hp;
           }
           stop = !emit(b, hp, p.ctx_len[b], tiles - 1, u0, u1, 0, L, seg, whole ? -1 : seg + c);
           t = seg0 + u1;
         }
+      }
+      {                                        // every CTA writes its entry
+        int *jd = p.jobs + (size_t)c * kJobInts;
+        jd[0] = job[0];
+        jd[1] = job[1];
+        jd[2] = job[2];
+        jd[3] = job[3];
+        jd[4] = T;
       }
       if (!stop) {                             // sentinel stage: no more work
         const uint32_t s = it % kStages, round = it / kStages;
@@ -713,159 +661,147 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) fail();
   }
 
-  // every partial this CTA wrote is visible device-wide before it is counted
-  __threadfence();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
 
-  // ------------------------------------------------------------ merges
-  // count this CTA's cut pieces; the CTA that completes a segment merges it
-  if (threadIdx.x == 0 && !sm.abort_flag) {
-    for (int k = 0; k < sm.ncut; ++k) {
-      const int seg = sm.cut_seg[k], c0 = sm.cut_c0[k], c1 = sm.cut_c1[k];
-      int n = 0;
-      for (int cc = c0; cc <= c1; ++cc) n += range_nonempty(cc, sm.plan_T, gridDim.x) ? 1 : 0;
-      const int old = atomicAdd(&p.counters[seg], 1);
-      if (old >= n - 1) {
-        if (old != n - 1) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);   // stale counter
-        atomicExch(&p.counters[seg], 0);
-        const int j = sm.nmerge++;
-        sm.mrg_seg[j] = seg;
-        sm.mrg_c0[j] = c0;
-        sm.mrg_c1[j] = c1;
-        sm.mrg_b[j] = sm.cut_b[k];
-        sm.mrg_hp[j] = sm.cut_hp[k];
-      }
-    }
-    __threadfence();                           // the other pieces' partials, before reading
+// Merge of the cut segments, one wave of CTAs.  Every CTA reads the whole
+// job table (one entry per attention CTA) and compacts the active jobs; work
+// item (job, r) covers rows [16 r, 16 r + 16) of the job's head pair, and CTA
+// i takes items i, i + gridDim.x, ...  The pieces k of a job are the partials
+// of CTAs c0 .. c1 with non-empty ranges, each an unnormalised O_k with its
+// running max m_k and sum l_k per row:
+//   M = max_k m_k,  S = sum_k l_k e^(m_k - M),  out = sum_k e^(m_k - M) O_k / S.
+// All pieces' (m, l) and the first eight pieces' O rows are loaded before any
+// is used; further pieces follow eight at a time.
+constexpr int kMergeRows = 16;
+constexpr int kMergeThreads = 256;
+constexpr int kMergeGroup = 8;
+constexpr int kMergeEpt = kMergeRows * (D / 4) / kMergeThreads;   // float4 per thread
+constexpr int kMergeMaxPieces = 160;        // pieces of one segment (at most the grid)
+
+__global__ void __launch_bounds__(kMergeThreads) attn_pair_merge_kernel(const AttnParams p) {
+  __shared__ int slots[kMergeMaxPieces];
+  __shared__ int active[kMergeMaxPieces];
+  __shared__ int warp_off[kMergeThreads / 32 + 1];
+  __shared__ int npieces;
+  __shared__ float ml_m[kMergeMaxPieces][kMergeRows], ml_l[kMergeMaxPieces][kMergeRows];
+  __shared__ float wts[kMergeMaxPieces][kMergeRows];
+  pdl_trigger();
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int group = p.hq / p.hkv, L = p.block_len;
+  const long long G = p.grid;                  // CTAs of the attention kernel (<= 160)
+  // the active jobs in CTA order (the same list in every CTA)
+  const bool has = tid < G && p.jobs[(size_t)tid * kJobInts] >= 0;
+  const unsigned bal = __ballot_sync(0xffffffffu, has);
+  if (lane == 0) warp_off[warp + 1] = __popc(bal);
+  __syncthreads();
+  if (tid == 0) {
+    warp_off[0] = 0;
+    for (int w = 0; w < kMergeThreads / 32; ++w) warp_off[w + 1] += warp_off[w];
   }
   __syncthreads();
-  const int nmerge = sm.nmerge;
-  if (nmerge == 0) return;
-  float *wt = reinterpret_cast<float *>(&sm.q[0][0]);        // [128 rows][64 pieces]
-  float *acc = reinterpret_cast<float *>(&sm.k[0][0][0]);    // 64 KB: piece 0, then the sum
-  const int tid = threadIdx.x;
-  uint32_t uses[3] = {0, 0, 0};                              // phases of merge_full[i]
-  uint32_t issued[3] = {0, 0, 0};                            // copies issued (thread 0)
-  for (int j = 0; j < nmerge; ++j) {
-    const int seg = sm.mrg_seg[j], c0 = sm.mrg_c0[j], c1 = sm.mrg_c1[j];
-    const int b = sm.mrg_b[j], hp = sm.mrg_hp[j];
-    const long long Tm = sm.plan_T;
-    // slot of the k-th piece: segment + the k-th CTA of [c0, c1] with tiles
-    auto slot_of = [&](int k) -> int {
-      for (int cc = c0; cc <= c1; ++cc)
-        if (range_nonempty(cc, Tm, gridDim.x) && k-- == 0) return seg + cc;
-      return -1;
-    };
-    int P = 0;
-    for (int cc = c0; cc <= c1; ++cc) P += range_nonempty(cc, Tm, gridDim.x) ? 1 : 0;
-    // row statistics (one thread per row): M = max_k m_k, L = sum_k l_k e^(m_k - M)
-    float Mr = -INFINITY, Linv = 0.f;
-    if (tid < kRows) {
-      for (int k = 0; k < P; ++k) Mr = fmaxf(Mr, __ldcg(&p.sk_ml[((size_t)slot_of(k) * kRows + tid) * 2]));
-      float Lr = 0.f;
-      for (int k = 0; k < P; ++k) {
-        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
-            p.sk_ml + ((size_t)slot_of(k) * kRows + tid) * 2));
-        Lr += ml.y * __expf(ml.x - Mr);
-      }
-      Linv = Lr > 0.f ? 1.f / Lr : 0.f;
+  if (has) active[warp_off[warp] + __popc(bal & ((1u << lane) - 1))] = tid;
+  const int nactive = warp_off[kMergeThreads / 32];
+  const int items = nactive * (kRows / kMergeRows);
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    __syncthreads();                           // active[] written; last item's data used
+    const int j = active[item / (kRows / kMergeRows)];
+    const int r0 = (item % (kRows / kMergeRows)) * kMergeRows;
+    const int *jd = p.jobs + (size_t)j * kJobInts;
+    const int4 job = *reinterpret_cast<const int4 *>(jd);   // seg, c1, b, hp
+    const int seg = job.x, c1 = job.y, b = job.z, hp = job.w;
+    const long long T = jd[4];
+    if (tid == 0) {                            // the pieces: CTAs j..c1 with tiles
+      int n = 0;
+      for (int cc = j; cc <= c1 && n < kMergeMaxPieces; ++cc)
+        if (range_nonempty(cc, T, G)) slots[n++] = seg + cc;
+      npieces = n;
     }
-    auto fill_weights = [&](int k0) {         // weights of pieces [k0, k0 + 64)
-      if (tid < kRows)
-        for (int k = k0; k < min(P, k0 + 64); ++k) {
-          const float m = __ldcg(&p.sk_ml[((size_t)slot_of(k) * kRows + tid) * 2]);
-          wt[tid * 64 + (k - k0)] = __expf(m - Mr) * Linv;
-        }
-    };
-    auto issue = [&](int k) {                 // piece k into its buffer (thread 0)
-      const int bi = k == 0 ? 0 : 1 + ((k - 1) & 1);
-      const uint32_t bar = smem_u32(&sm.merge_full[bi]);
-      fence_proxy_async();
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      mbar_arrive_expect_tx(bar, kPieceBytes);
-      bulk_load(smem_u32(acc + (size_t)bi * (kPieceBytes / 4)),
-                p.sk_o + (size_t)slot_of(k) * kRows * D, kPieceBytes, bar);
-      ++issued[bi];
-    };
-    if (tid == 0)
-      for (int k = 0; k < min(P, 3); ++k) issue(k);
-    fill_weights(0);
     __syncthreads();
-    bool failed = false;
-    for (int k = 0; k < P && !failed; ++k) {
-      const int bi = k == 0 ? 0 : 1 + ((k - 1) & 1);
-      if (k > 0 && k % 64 == 0) {
-        __syncthreads();
-        fill_weights(k);
-        __syncthreads();
+    const int P = npieces;
+    // every (piece, row) pair's running max and sum, one load each, all at once
+    for (int i = tid; i < P * kMergeRows; i += kMergeThreads) {
+      const int k = i / kMergeRows, rr = i % kMergeRows;
+      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
+          p.sk_ml + ((size_t)slots[k] * kRows + r0 + rr) * 2));
+      ml_m[k][rr] = ml.x;
+      ml_l[k][rr] = ml.y;
+    }
+    // the first group of pieces' O, issued before the statistics are used
+    float4 acc[kMergeEpt];
+#pragma unroll
+    for (int i = 0; i < kMergeEpt; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 v[kMergeGroup][kMergeEpt];
+    auto load_group = [&](int k0) {
+#pragma unroll
+      for (int k = 0; k < kMergeGroup; ++k)
+#pragma unroll
+        for (int i = 0; i < kMergeEpt; ++i)
+          v[k][i] = k0 + k < P ? __ldcg(reinterpret_cast<const float4 *>(
+                                     p.sk_o + ((size_t)slots[k0 + k] * kRows + r0) * D) +
+                                 tid + kMergeThreads * i)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    load_group(0);
+    __syncthreads();
+    // weights w_k = e^(m_k - M) / S per row (one thread per row)
+    if (tid < kMergeRows) {
+      float M = -INFINITY;
+      for (int k = 0; k < P; ++k) M = fmaxf(M, ml_m[k][tid]);
+      float S = 0.f;
+      for (int k = 0; k < P; ++k) {
+        const float e = __expf(ml_m[k][tid] - M);
+        wts[k][tid] = e;
+        S = fmaf(ml_l[k][tid], e, S);
       }
-      const bool ok = mbar_wait(smem_u32(&sm.merge_full[bi]), uses[bi] & 1);
-      ++uses[bi];
-      if (__syncthreads_or(!ok)) {
-        failed = true;
-        break;
-      }
-      const float4 *src = reinterpret_cast<const float4 *>(acc + (size_t)bi * (kPieceBytes / 4));
-      float4 *dst = reinterpret_cast<float4 *>(acc);
-      const int kw = k % 64;
-      for (int e = tid; e < kRows * D / 4; e += kThreads) {
-        const float w = wt[(e >> 5) * 64 + kw];
-        const float4 x = src[e];
-        if (k == 0) {
-          dst[e] = make_float4(x.x * w, x.y * w, x.z * w, x.w * w);
-        } else {
-          float4 a = dst[e];
-          a.x = fmaf(x.x, w, a.x);
-          a.y = fmaf(x.y, w, a.y);
-          a.z = fmaf(x.z, w, a.z);
-          a.w = fmaf(x.w, w, a.w);
-          dst[e] = a;
+      const float inv = S > 0.f ? 1.f / S : 0.f;
+      for (int k = 0; k < P; ++k) wts[k][tid] *= inv;
+    }
+    __syncthreads();
+    for (int k0 = 0; k0 < P; k0 += kMergeGroup) {
+      if (k0 > 0) load_group(k0);
+#pragma unroll
+      for (int k = 0; k < kMergeGroup; ++k)
+#pragma unroll
+        for (int i = 0; i < kMergeEpt; ++i) {
+          const float w = k0 + k < P ? wts[k0 + k][(tid + kMergeThreads * i) >> 5] : 0.f;
+          acc[i].x = fmaf(v[k][i].x, w, acc[i].x);
+          acc[i].y = fmaf(v[k][i].y, w, acc[i].y);
+          acc[i].z = fmaf(v[k][i].z, w, acc[i].z);
+          acc[i].w = fmaf(v[k][i].w, w, acc[i].w);
         }
-      }
-      fence_proxy_async();                     // generic reads of buffer bi before the
-      __syncthreads();                         // next bulk copy rewrites it
-      if (tid == 0 && k > 0 && k + 2 < P) issue(k + 2);
     }
-    if (failed) {
-      if (tid == 0) {                          // wait (bounded) for copies in flight
-        flag_error(p.dev_status, BD_ERR_TIMEOUT);
-        for (int i = 0; i < 3; ++i)
-          for (; uses[i] < issued[i]; ++uses[i]) mbar_wait(smem_u32(&sm.merge_full[i]), uses[i] & 1);
-      }
-      __syncthreads();
-      return;
-    }
-    // the merged rows to the output: row r of the pair is head 2 hp + r / 64,
-    // query row r % 64 = i * group + j of that head
-    const float4 *res = reinterpret_cast<const float4 *>(acc);
-    for (int e = tid; e < kRows * D / 4; e += kThreads) {
-      const int r = e >> 5, d4 = e & 31;
+#pragma unroll
+    for (int i = 0; i < kMergeEpt; ++i) {
+      const int e = tid + kMergeThreads * i;
+      const int r = r0 + (e >> 5), d4 = e & 31;
       const int g = 2 * hp + (r >> 6), rr = r & 63;
       const int qi = rr / group, h = g * group + rr % group;
-      const float4 x = res[e];
       __nv_bfloat16 *out =
           static_cast<__nv_bfloat16 *>(p.out) + (((size_t)b * L + qi) * p.hq + h) * D + 4 * d4;
-      *reinterpret_cast<uint2 *>(out) = make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+      *reinterpret_cast<uint2 *>(out) =
+          make_uint2(pack_bf16(acc[i].x, acc[i].y), pack_bf16(acc[i].z, acc[i].w));
     }
-    fence_proxy_async();
-    __syncthreads();                           // acc and wt are reused by the next merge
   }
 }
 
 }  // namespace
 
-bool preload_attention_pair() { return preload_kernel(attn_pair_kernel, true); }
+bool preload_attention_pair() {
+  return preload_kernel(attn_pair_kernel, true) && preload_kernel(attn_pair_merge_kernel, false);
+}
 
 bool attention_pair_supported(const AttnParams &p) {
   if (p.dtype != BD_BF16 || p.head_dim != D || p.page_size != kPage) return false;
   if (p.hkv % 2 != 0 || p.hq % p.hkv != 0) return false;
   if (p.block_len * (p.hq / p.hkv) != 64) return false;
-  if (p.grid < 1 || !p.sk_o || !p.sk_ml || !p.counters) return false;
+  if (p.grid < 1 || p.grid > kMergeMaxPieces || !p.sk_o || !p.sk_ml || !p.jobs) return false;
   if ((long long)p.batch * (p.hkv / 2) * (p.max_pages + 1) >= (1LL << 30)) return false;
   const DevInfo d = dev_info();
   return d.major >= 10 && tma_available();
@@ -900,8 +836,11 @@ bd_status attention_pair(const AttnParams &p0, cudaStream_t st) {
       !tma_encode_bf16(&mq, 4, p.q, qdims, qstr, qbox))
     return BD_ERR_CUDA;
   const size_t smem = sizeof(Smem) + 1024;
-  const cudaError_t e = launch_pdl(attn_pair_kernel, dim3(p.grid), dim3(kThreads), smem, st, mkp,
-                                   mvp, mkb, mvb, mq, p);
+  cudaError_t e = launch_pdl(attn_pair_kernel, dim3(p.grid), dim3(kThreads), smem, st, mkp, mvp,
+                             mkb, mvb, mq, p);
+  count_launches(1);
+  if (e != cudaSuccess) return BD_ERR_CUDA;
+  e = launch_pdl(attn_pair_merge_kernel, dim3(2 * p.grid), dim3(kMergeThreads), 0, st, p);
   count_launches(1);
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }

@@ -126,7 +126,7 @@ class DenoiseEngine:
         cws = query(code, batch, block_len, self.H, self.V)
         if cws == 0:
             raise ValueError("unsupported confidence-commit shape")
-        self.attn_ws = torch.zeros(max(aws, 1), dtype=torch.uint8, device=dev)   # zeroed once
+        self.attn_ws = torch.empty(max(aws, 1), dtype=torch.uint8, device=dev)
         self.conf_ws = torch.empty(cws, dtype=torch.uint8, device=dev)
         self._host_masked = torch.empty(batch, dtype=torch.int32, pin_memory=True)
         self._graphs = {}
@@ -294,7 +294,7 @@ class DecoderStack:
                 if mws == 0:
                     raise ValueError("unsupported MLP shape")
         self.ws = torch.empty(max(qws, ows, mws, 1), dtype=torch.uint8, device=dev)
-        self.attn_ws = torch.zeros(max(aws, 1), dtype=torch.uint8, device=dev)   # zeroed once
+        self.attn_ws = torch.empty(max(aws, 1), dtype=torch.uint8, device=dev)
         # every layer addresses its pool through one shared page table
         for c in self.caches[1:]:
             if not np.array_equal(c.page_table_np, c0.page_table_np):

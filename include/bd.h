@@ -99,13 +99,8 @@ typedef struct {
  *   out       [batch][block_len][num_q_heads][head_dim], dtype
  *   max_ctx   host-side upper bound on ctx_len (sizes the KV split).
  *   ws        device workspace of at least bd_block_attention_workspace() bytes,
- *             256-byte aligned.  Zero-fill it once before its first call (e.g.
- *             cudaMemsetAsync): its first bytes count the pieces of key
- *             segments that several CTAs share, and every call that completes
- *             without a device error leaves them zero again.  After a call
- *             that reported BD_ERR_TIMEOUT or BD_ERR_DEVICE_CHECK, zero it
- *             again before reusing it.  Calls that share a workspace must be
- *             ordered on the GPU (one stream).
+ *             256-byte aligned; its contents need no initialisation.  Calls
+ *             that share a workspace must be ordered on the GPU (one stream).
  * Limits: head_dim 64 or 128; block_len 1..32; num_q_heads % num_kv_heads == 0;
  *         block_len * (num_q_heads / num_kv_heads) <= 128.
  * ------------------------------------------------------------------------ */
