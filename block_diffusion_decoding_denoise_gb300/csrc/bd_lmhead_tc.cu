@@ -80,8 +80,10 @@ struct LmTcArgs {
   int stages;
   int stage_bytes;
   int num_tiles;
-  int nmax;       // masked rows per pass this launch can hold (multiple of 16)
+  int nmax;       // masked rows per pass this launch can hold (multiple of 16; of 32
+                  // for a CTA pair)
   int maxn;       // rows per pass: kMaxN, or kNarrowN with two CTAs per SM
+  int brows;      // rows of h per stage in this CTA: nmax, or nmax / 2 for a CTA pair
   int big_boxes;  // 1: tmap_h64 (64-row boxes) is valid
   int red_off;    // smem offsets of the merge buffer, the row positions
   int pos_off;    // (sampling only) and Ctrl
@@ -251,8 +253,13 @@ template <> __device__ __forceinline__ SampleState empty_state<SampleState>() {
   return SampleState{-INFINITY, 0.f, -INFINITY, -INFINITY, 0x7fffffff};
 }
 
-template <bool kSample>
-__global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow calls)
+// kPair: the CTAs of a two-CTA cluster share each tile of 256 vocabulary
+// entries (128 per CTA) through tcgen05.mma.cta_group::2 (M = 256): each CTA
+// stages its 128 rows of W and half of the pass's rows of h, so each SM
+// brings in a third less operand data per FLOP; the even CTA issues the MMAs
+// and the odd CTA's copies and epilogue report to the even CTA's barriers.
+template <bool kSample, bool kPair>
+__global__ void __launch_bounds__(kThreads, kPair ? 1 : 2)   // narrow calls: two CTAs per SM
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                      const __grid_constant__ CUtensorMap tmap_h,
                      const __grid_constant__ CUtensorMap tmap_h64, const LmTcArgs a) {
@@ -267,7 +274,13 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
   const ConfParams &p = a.p;
 
   const int G = gridDim.x, cta = blockIdx.x;
-  const int my_tiles = (a.num_tiles - cta + G - 1) / G;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;   // 0: issues the pair's MMAs
+  // vocabulary tiles of 128 entries: a CTA takes tiles unit + t * units; a
+  // pair takes pair tiles of two (tile 2 pt + rank for this CTA)
+  const int unit = kPair ? cta >> 1 : cta, units = kPair ? G >> 1 : G;
+  const int unit_tiles = kPair ? (a.num_tiles + 1) >> 1 : a.num_tiles;
+  const int my_tiles = max(0, (unit_tiles - unit + units - 1) / units);
+  auto tile_of = [&](int t) { return kPair ? 2 * (unit + t * units) + (int)rank : unit + t * units; };
   const int KC = p.hidden / kKChunk;
   const int S = a.stages;
 
@@ -278,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&ctrl->tfull[i]), 1);
-      mbar_init(smem_u32(&ctrl->tempty[i]), kEpiWarps);
+      mbar_init(smem_u32(&ctrl->tempty[i]), kPair ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(smem_u32(&ctrl->mma_done), 1);
     ctrl->abort = 0;
@@ -290,11 +303,18 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
     if (a.big_boxes) tma_prefetch_desc(&tmap_h64);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctrl->tmem_base), 2u * a.maxn);   // two accumulators
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(smem_u32(&ctrl->tmem_base), 2u * a.maxn);   // two accumulators
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&ctrl->tmem_base), 2u * a.maxn);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // a pair: both CTAs' barriers exist before either CTA's copies or MMAs signal them
+  if (kPair) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
   // set-up above overlaps the previous kernel; the row list is read after it
@@ -322,34 +342,54 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
     for (int pass = 0; pass < npass && !stop; ++pass) {
       const int r0 = pass * MN;
       const int n = min(MN, count - r0);
-      const int npad = (n + 15) & ~15;
-      const uint32_t tx = kABytes + npad * 128;
+      const int npad = kPair ? (n + 31) & ~31 : (n + 15) & ~15;
+      const int nmine = kPair ? npad >> 1 : npad;          // rows of h this CTA stages
+      const int rfirst = r0 + (int)rank * nmine;
+      const uint32_t tx = kABytes + nmine * 128;
       for (int t = 0; t < my_tiles && !stop; ++t) {
-        const int vt = cta + t * G;
+        const int vt = tile_of(t);
         for (int kc = 0; kc < KC; ++kc, ++it) {
           const uint32_t s = it % S, round = it / S;
           uint8_t *st = smem + (size_t)s * a.stage_bytes;
           int ok = 1;
           if (lane == 0) {
             if (ctrl->abort) ok = 0;
-            else if (round > 0 && !mbar_wait(smem_u32(&ctrl->empty[s]), (round - 1) & 1)) {
+            else if (round > 0 && !mbar_wait_cluster(smem_u32(&ctrl->empty[s]), (round - 1) & 1)) {
               ok = 0;
               ctrl->abort = 1;
               flag_error(p.dev_status, BD_ERR_TIMEOUT);
             }
             if (ok) {
-              const uint32_t bar = smem_u32(&ctrl->full[s]);
-              mbar_arrive_expect_tx(bar, tx);
-              tma_load_2d_hint(smem_u32(st), &tmap_w, kc * kKChunk, vt * kTileV, bar, w_policy);
+              // a pair's copies all count on the even CTA's barrier, which
+              // expects both CTAs' bytes
+              const uint32_t bar = kPair ? map_shared(smem_u32(&ctrl->full[s]), 0)
+                                         : smem_u32(&ctrl->full[s]);
+              if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctrl->full[s]), kPair ? 2 * tx : tx);
+              if (kPair)
+                tma_load_2d_pair_hint(smem_u32(st), &tmap_w, kc * kKChunk, vt * kTileV, bar,
+                                      w_policy);
+              else
+                tma_load_2d_hint(smem_u32(st), &tmap_w, kc * kKChunk, vt * kTileV, bar, w_policy);
               // whole 64-row groups in one box each (fewer, larger copies), the
               // rest of the pass in 16-row boxes
               int r = 0;
               if (a.big_boxes)
-                for (; r + kBigBoxRows <= npad; r += kBigBoxRows)
-                  tma_load_2d(smem_u32(st + kABytes + r * 128), &tmap_h64, kc * kKChunk, r0 + r,
+                for (; r + kBigBoxRows <= nmine; r += kBigBoxRows) {
+                  if (kPair)
+                    tma_load_2d_pair(smem_u32(st + kABytes + r * 128), &tmap_h64, kc * kKChunk,
+                                     rfirst + r, bar);
+                  else
+                    tma_load_2d(smem_u32(st + kABytes + r * 128), &tmap_h64, kc * kKChunk,
+                                rfirst + r, bar);
+                }
+              for (; r < nmine; r += kBoxRows) {
+                if (kPair)
+                  tma_load_2d_pair(smem_u32(st + kABytes + r * 128), &tmap_h, kc * kKChunk,
+                                   rfirst + r, bar);
+                else
+                  tma_load_2d(smem_u32(st + kABytes + r * 128), &tmap_h, kc * kKChunk, rfirst + r,
                               bar);
-              for (; r < npad; r += kBoxRows)
-                tma_load_2d(smem_u32(st + kABytes + r * 128), &tmap_h, kc * kKChunk, r0 + r, bar);
+              }
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -360,25 +400,33 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
         }
       }
     }
-    // on an abort, wait (bounded) for the copies this warp may still have in flight
+    // on an abort, wait (bounded) for the copies this warp may still have in
+    // flight; the odd CTA of a pair cannot observe its copies (they count on
+    // the even CTA's barrier), so it waits a fixed 200 us, far beyond any copy
     if (stop && lane == 0) {
-      const uint32_t first = it > (uint32_t)S ? it - S : 0;
-      for (uint32_t i = first; i < it; ++i)
-        mbar_wait(smem_u32(&ctrl->full[i % S]), (i / S) & 1);
+      if (rank == 0) {
+        const uint32_t first = it > (uint32_t)S ? it - S : 0;
+        for (uint32_t i = first; i < it; ++i)
+          mbar_wait_cluster(smem_u32(&ctrl->full[i % S]), (i / S) & 1);
+      } else {
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 200000ull) {
+        }
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       uint32_t it = 0, tg = 0;
       bool stop = false;
       for (int pass = 0; pass < npass && !stop; ++pass) {
         const int n = min(MN, count - pass * MN);
-        const int npad = (n + 15) & ~15;
-        const uint32_t idesc = idesc_bf16_f32(kTileV, npad);
+        const int npad = kPair ? (n + 31) & ~31 : (n + 15) & ~15;
+        const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kTileV : kTileV, npad);
         for (int t = 0; t < my_tiles && !stop; ++t, ++tg) {
           const uint32_t acc = tg & 1, use = tg >> 1;
           if (ctrl->abort ||
-              (use > 0 && !mbar_wait(smem_u32(&ctrl->tempty[acc]), (use - 1) & 1))) {
+              (use > 0 && !mbar_wait_cluster(smem_u32(&ctrl->tempty[acc]), (use - 1) & 1))) {
             stop = true;
             break;
           }
@@ -386,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
           const uint32_t d = tmem + acc * MN;
           for (int kc = 0; kc < KC; ++kc, ++it) {
             const uint32_t s = it % S, round = it / S;
-            if (ctrl->abort || !mbar_wait(smem_u32(&ctrl->full[s]), round & 1)) {
+            if (ctrl->abort || !mbar_wait_cluster(smem_u32(&ctrl->full[s]), round & 1)) {
               stop = true;
               break;
             }
@@ -394,13 +442,20 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
             const uint32_t a_base = smem_u32(smem + (size_t)s * a.stage_bytes);
             const uint32_t b_base = a_base + kABytes;
 #pragma unroll
-            for (int k = 0; k < kKChunk / 16; ++k)
-              mma_bf16(d, sw128_kmajor_desc(a_base + k * 32), sw128_kmajor_desc(b_base + k * 32),
-                       idesc, (kc | k) != 0);
-            mma_commit(smem_u32(&ctrl->empty[s]));
+            for (int k = 0; k < kKChunk / 16; ++k) {
+              if (kPair)
+                mma_bf16_pair(d, sw128_kmajor_desc(a_base + k * 32),
+                              sw128_kmajor_desc(b_base + k * 32), idesc, (kc | k) != 0);
+              else
+                mma_bf16(d, sw128_kmajor_desc(a_base + k * 32), sw128_kmajor_desc(b_base + k * 32),
+                         idesc, (kc | k) != 0);
+            }
+            if (kPair) mma_commit_pair(smem_u32(&ctrl->empty[s]), 0x3);   // both CTAs' stage
+            else mma_commit(smem_u32(&ctrl->empty[s]));
           }
           if (stop) break;
-          mma_commit(smem_u32(&ctrl->tfull[acc]));
+          if (kPair) mma_commit_pair(smem_u32(&ctrl->tfull[acc]), 0x3);
+          else mma_commit(smem_u32(&ctrl->tfull[acc]));
         }
       }
       if (stop) {
@@ -408,7 +463,8 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
         flag_error(p.dev_status, BD_ERR_TIMEOUT);
       }
       // every MMA this thread issued has completed once mma_done fires
-      mma_commit(smem_u32(&ctrl->mma_done));
+      if (kPair) mma_commit_pair(smem_u32(&ctrl->mma_done), 0x1);
+      else mma_commit(smem_u32(&ctrl->mma_done));
       mbar_wait(smem_u32(&ctrl->mma_done), 0);
     }
   } else {
@@ -435,10 +491,10 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
         named_barrier(2, kEpiThreads);
       }
       for (int t = 0; t < my_tiles; ++t, ++tg) {
-        const int vt = cta + t * G;
+        const int vt = tile_of(t);
         const uint32_t acc = tg & 1, use = tg >> 1;
         int ok = 1;
-        if (lane == 0) ok = mbar_wait(smem_u32(&ctrl->tfull[acc]), use & 1) ? 1 : 0;
+        if (lane == 0) ok = mbar_wait_cluster(smem_u32(&ctrl->tfull[acc]), use & 1) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok) {
           tc_fence_after();
@@ -456,7 +512,10 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctrl->tempty[acc]));
+          if (lane == 0) {                     // the pair's MMAs wait on the even CTA's barrier
+            if (kPair) mbar_arrive_cluster(map_shared(smem_u32(&ctrl->tempty[acc]), 0));
+            else mbar_arrive(smem_u32(&ctrl->tempty[acc]));
+          }
         } else {
           ctrl->abort = 1;
           if (lane == 0) flag_error(p.dev_status, BD_ERR_TIMEOUT);
@@ -479,9 +538,13 @@ __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM fit (narrow 
 
   tc_fence_before();
   __syncthreads();
+  // a pair: the even CTA's MMAs (which read the odd CTA's shared memory and
+  // write its tensor memory) and all cross-CTA arrivals are done
+  if (kPair) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 2u * a.maxn);
+    if (kPair) tmem_dealloc_pair(tmem, 2u * a.maxn);
+    else tmem_dealloc(tmem, 2u * a.maxn);
   }
 }
 
@@ -505,13 +568,18 @@ int num_tiles(int vocab) { return (vocab + kTileV - 1) / kTileV; }
 // the sampling epilogue fits in 96 without spills.)
 bool narrow(int rows, bool) { return rows <= kNarrowN; }
 
+// Wider calls run as CTA pairs (cta_group::2, one CTA per SM).
+bool paired(int rows, bool sample) { return !narrow(rows, sample); }
+
 void plan(const ConfParams &p, LmTcArgs &a, size_t *smem) {
   const int rows = p.batch * p.block_len;
   const bool nar = narrow(rows, p.sample != 0);
+  const bool pair = paired(rows, p.sample != 0);
   a.maxn = nar ? kNarrowN : kMaxN;
-  const int nmax = std::min(a.maxn, (rows + 15) & ~15);
+  const int nmax = std::min(a.maxn, pair ? (rows + 31) & ~31 : (rows + 15) & ~15);
   a.nmax = nmax;
-  a.stage_bytes = (kABytes + nmax * 128 + 1023) & ~1023;
+  a.brows = pair ? nmax / 2 : nmax;
+  a.stage_bytes = (kABytes + a.brows * 128 + 1023) & ~1023;
   const int state = p.sample ? (int)sizeof(SampleState) : (int)sizeof(MaxSumArg);
   const int red = (2 * 4 * nmax * state + 1023) & ~1023;
   const int pos = p.sample ? ((nmax * 4 + 127) & ~127) : 0;
@@ -527,7 +595,10 @@ void plan(const ConfParams &p, LmTcArgs &a, size_t *smem) {
 }  // namespace
 
 bool preload_lmhead_tc() {
-  return preload_kernel(lmhead_tc_kernel<false>, true) && preload_kernel(lmhead_tc_kernel<true>, true);
+  return preload_kernel(lmhead_tc_kernel<false, false>, true) &&
+         preload_kernel(lmhead_tc_kernel<true, false>, true) &&
+         preload_kernel(lmhead_tc_kernel<false, true>, true) &&
+         preload_kernel(lmhead_tc_kernel<true, true>, true);
 }
 
 bool lmhead_tc_supported(const ConfParams &p) {
@@ -540,6 +611,8 @@ bool lmhead_tc_supported(const ConfParams &p) {
 
 int lmhead_tc_num_partials(int vocab, int rows, bool sample) {
   const DevInfo d = dev_info();
+  if (paired(rows, sample))   // an even number of CTAs, at most one pair per pair tile
+    return std::max(2, std::min(d.sms & ~1, 2 * ((num_tiles(vocab) + 1) / 2)));
   const int ctas = narrow(rows, sample) ? 2 * d.sms : d.sms;
   return std::max(1, std::min(ctas, num_tiles(vocab)));
 }
@@ -564,12 +637,20 @@ bd_status lmhead_tc(const ConfParams &p, cudaStream_t st) {
     mh64 = mh;
   }
   const int grid = p.ws.num_partials;
-  if (grid < 1 || grid > a.num_tiles) return BD_ERR_INVALID_ARG;
-  const cudaError_t e =
-      p.sample
-          ? launch_pdl(lmhead_tc_kernel<true>, dim3(grid), dim3(kThreads), smem, st, mw, mh, mh64, a)
-          : launch_pdl(lmhead_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, st, mw, mh, mh64,
-                       a);
+  cudaError_t e;
+  if (paired((int)rows, p.sample != 0)) {
+    if (grid < 2 || grid % 2 || grid > 2 * ((a.num_tiles + 1) / 2)) return BD_ERR_INVALID_ARG;
+    e = p.sample ? launch_pdl_cluster(lmhead_tc_kernel<true, true>, dim3(grid), dim3(kThreads),
+                                      smem, st, dim3(2, 1, 1), mw, mh, mh64, a)
+                 : launch_pdl_cluster(lmhead_tc_kernel<false, true>, dim3(grid), dim3(kThreads),
+                                      smem, st, dim3(2, 1, 1), mw, mh, mh64, a);
+  } else {
+    if (grid < 1 || grid > a.num_tiles) return BD_ERR_INVALID_ARG;
+    e = p.sample ? launch_pdl(lmhead_tc_kernel<true, false>, dim3(grid), dim3(kThreads), smem, st,
+                              mw, mh, mh64, a)
+                 : launch_pdl(lmhead_tc_kernel<false, false>, dim3(grid), dim3(kThreads), smem, st,
+                              mw, mh, mh64, a);
+  }
   count_launches(1);
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
