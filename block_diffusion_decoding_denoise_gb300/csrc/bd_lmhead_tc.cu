@@ -14,8 +14,13 @@
 // B operand), so a step with only a handful of masked rows still fills the
 // 128-lane tensor-core tile and the kernel streams W at HBM speed.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over vocabulary tiles
-// vt = blockIdx.x + i * gridDim.x):
+// Work: units of (pass over up to 256 masked rows, tile of 128 vocabulary
+// entries), laid out pass by pass and dealt round-robin to the persistent
+// CTAs, so the shares differ by at most one unit over the whole call.  Calls
+// of at most 128 positions run two CTAs per SM; wider calls run CTA pairs
+// (clusters of two, tcgen05.mma.cta_group::2 with M = 256: each CTA stages its
+// 128 rows of W and half of the pass's rows, the even CTA issues the MMAs).
+// Warp roles (320 threads):
 //   warp 0     TMA producer: per 64-wide K chunk, one 128x64 box of W and
 //              16x64 boxes of the compacted masked rows of h (conf_prep_kernel
 //              gathers them) into a ring of smem stages (128-byte swizzle),
@@ -275,12 +280,12 @@ __global__ void __launch_bounds__(kThreads, kPair ? 1 : 2)   // narrow calls: tw
 
   const int G = gridDim.x, cta = blockIdx.x;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;   // 0: issues the pair's MMAs
-  // vocabulary tiles of 128 entries: a CTA takes tiles unit + t * units; a
-  // pair takes pair tiles of two (tile 2 pt + rank for this CTA)
+  // Work units: (pass over the rows, vocabulary tile) pairs laid out pass by
+  // pass; a CTA (or a pair) takes units unit + i * units, so every CTA's share
+  // differs by at most one unit over the whole call, not one per pass.  A
+  // pair's tiles are pair tiles of two 128-entry tiles (2 pt + rank here).
   const int unit = kPair ? cta >> 1 : cta, units = kPair ? G >> 1 : G;
   const int unit_tiles = kPair ? (a.num_tiles + 1) >> 1 : a.num_tiles;
-  const int my_tiles = max(0, (unit_tiles - unit + units - 1) / units);
-  auto tile_of = [&](int t) { return kPair ? 2 * (unit + t * units) + (int)rank : unit + t * units; };
   const int KC = p.hidden / kKChunk;
   const int S = a.stages;
 
@@ -333,21 +338,28 @@ __global__ void __launch_bounds__(kThreads, kPair ? 1 : 2)   // narrow calls: tw
   }
   const int MN = a.maxn;
   const int npass = count > 0 ? (count + MN - 1) / MN : 0;   // 0: nothing masked
+  const int total_units = npass * unit_tiles;
+  const int my_units = total_units > unit ? (total_units - unit + units - 1) / units : 0;
+  auto unit_pass = [&](int i) { return (unit + i * units) / unit_tiles; };
+  auto unit_tile = [&](int i) {
+    const int tp = (unit + i * units) % unit_tiles;
+    return kPair ? 2 * tp + (int)rank : tp;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t w_policy = l2_policy_evict_first();   // W is read once per step
     uint32_t it = 0;
     bool stop = false;
-    for (int pass = 0; pass < npass && !stop; ++pass) {
-      const int r0 = pass * MN;
+    for (int i = 0; i < my_units && !stop; ++i) {
+      const int r0 = unit_pass(i) * MN;
       const int n = min(MN, count - r0);
       const int npad = kPair ? (n + 31) & ~31 : (n + 15) & ~15;
       const int nmine = kPair ? npad >> 1 : npad;          // rows of h this CTA stages
       const int rfirst = r0 + (int)rank * nmine;
       const uint32_t tx = kABytes + nmine * 128;
-      for (int t = 0; t < my_tiles && !stop; ++t) {
-        const int vt = tile_of(t);
+      {
+        const int vt = unit_tile(i);
         for (int kc = 0; kc < KC; ++kc, ++it) {
           const uint32_t s = it % S, round = it / S;
           uint8_t *st = smem + (size_t)s * a.stage_bytes;
@@ -419,11 +431,11 @@ __global__ void __launch_bounds__(kThreads, kPair ? 1 : 2)   // narrow calls: tw
     if (lane == 0 && rank == 0) {
       uint32_t it = 0, tg = 0;
       bool stop = false;
-      for (int pass = 0; pass < npass && !stop; ++pass) {
-        const int n = min(MN, count - pass * MN);
+      for (int i = 0; i < my_units && !stop; ++i, ++tg) {
+        const int n = min(MN, count - unit_pass(i) * MN);
         const int npad = kPair ? (n + 31) & ~31 : (n + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kTileV : kTileV, npad);
-        for (int t = 0; t < my_tiles && !stop; ++t, ++tg) {
+        {
           const uint32_t acc = tg & 1, use = tg >> 1;
           if (ctrl->abort ||
               (use > 0 && !mbar_wait_cluster(smem_u32(&ctrl->tempty[acc]), (use - 1) & 1))) {
@@ -476,22 +488,39 @@ __global__ void __launch_bounds__(kThreads, kPair ? 1 : 2)   // narrow calls: tw
     const int tid_e = threadIdx.x - 64;      // 0..255: row tid_e of the pass
     uint64_t draw = 0;                       // the step's draw counter (sampling)
     if constexpr (kSample) draw = *p.offset;
-    uint32_t tg = 0;
+    St *part;
+    if constexpr (kSample) part = p.ws.spartial;
+    else part = p.ws.partial;
+    // this CTA's state of every row of pass q: `run`, or an empty state for a
+    // pass it has no tile of
+    auto write_pass = [&](int q, const St &st) {
+      const int n = min(MN, count - q * MN);
+      if (tid_e < n) part[(size_t)(q * MN + tid_e) * G + cta] = st;   // [row][CTA]
+    };
     bool stop = false;
-    for (int pass = 0; pass < npass && !stop; ++pass) {
+    int cur = -1;                            // pass of the running state
+    St run = empty_state<St>();
+    for (int i = 0; i < my_units; ++i) {
+      const int pass = unit_pass(i);
+      const uint32_t tg = (uint32_t)i;
       const int r0 = pass * MN;
       const int n = min(MN, count - r0);
       const int npad = (n + 15) & ~15;
-      St run = empty_state<St>();
-      if constexpr (kSample) {
-        // position ids of this pass's rows (the previous pass's readers have
-        // all passed the per-tile barrier below)
-        for (int i = tid_e; i < npad; i += kEpiThreads)
-          spos[i] = i < n ? (p.direct ? r0 + i : p.ws.rows[r0 + i]) : 0;
-        named_barrier(2, kEpiThreads);
+      if (pass != cur) {
+        if (cur >= 0) write_pass(cur, run);
+        for (int q = cur + 1; q < pass; ++q) write_pass(q, empty_state<St>());
+        cur = pass;
+        run = empty_state<St>();
+        if constexpr (kSample) {
+          // position ids of this pass's rows (the previous pass's readers have
+          // all passed the per-tile barrier below)
+          for (int j = tid_e; j < npad; j += kEpiThreads)
+            spos[j] = j < n ? (p.direct ? r0 + j : p.ws.rows[r0 + j]) : 0;
+          named_barrier(2, kEpiThreads);
+        }
       }
-      for (int t = 0; t < my_tiles; ++t, ++tg) {
-        const int vt = tile_of(t);
+      {
+        const int vt = unit_tile(i);
         const uint32_t acc = tg & 1, use = tg >> 1;
         int ok = 1;
         if (lane == 0) ok = mbar_wait_cluster(smem_u32(&ctrl->tfull[acc]), use & 1) ? 1 : 0;
@@ -529,10 +558,10 @@ __global__ void __launch_bounds__(kThreads, kPair ? 1 : 2)   // narrow calls: tw
           for (int w = 0; w < 4; ++w) run = merge(run, red[((tg & 1) * 4 + w) * a.nmax + tid_e]);
         }
       }
-      St *part;
-      if constexpr (kSample) part = p.ws.spartial;
-      else part = p.ws.partial;
-      if (!stop && tid_e < n) part[(size_t)(r0 + tid_e) * G + cta] = run;   // [row][CTA]
+    }
+    if (!stop) {
+      if (cur >= 0) write_pass(cur, run);
+      for (int q = cur + 1; q < npass; ++q) write_pass(q, empty_state<St>());
     }
   }
 
