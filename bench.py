@@ -43,6 +43,13 @@ METRIC = "committed tokens/sec per denoise loop"
 # current kernel: dram__bytes_read.sum 622.54 MB + dram__bytes_write.sum
 # 2.88 MB.
 LMHEAD_TRAFFIC_BYTES = 622_538_752 + 2_876_928
+# DRAM bytes (read + write) of one attn_pair_kernel launch at longctx_b8 (8
+# sequences x 16384 cached tokens, one layer), from an ncu capture of the
+# current kernel: dram__bytes_read.sum 539.89 MB + dram__bytes_write.sum
+# 4.80 MB, against 540.02 MB of algorithmic bytes for that launch; the decode
+# line scales it by its calls' algorithmic bytes (the context grows by one
+# block per block).
+LONGCTX_ATTN_TRAFFIC = (539_888_640 + 4_795_392, 540_016_640)
 UNIT = "tokens/s"
 WORKLOAD = "longctx_b8"
 
@@ -80,8 +87,10 @@ def _args():
                     help="launch every kernel from the host instead of replaying CUDA graphs")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="workload name (the headline line uses longctx_b8)")
-    ap.add_argument("--kernel", default=None, choices=["lmhead", "attention", "proj"],
-                    help="time one call alone (per-call us, GB/s, TFLOP/s) instead of decoding")
+    ap.add_argument("--kernel", default=None, choices=["lmhead", "attention", "proj", "step"],
+                    help="time one call alone (per-call us, GB/s, TFLOP/s) instead of decoding; "
+                         "'step': one eager denoise step of the decoder workload (for a launch "
+                         "list of exactly one step)")
     ap.add_argument("--rows", type=int, default=None,
                     help="--kernel lmhead: masked rows of the call (default: all of the workload's)")
     ap.add_argument("--iters", type=int, default=20, help="--kernel: timed calls")
@@ -1013,10 +1022,13 @@ def run_decoder(a):
     peak, peak_kind = _peaks()
     attn_us = 1e3 * statistics.mean(attn_ms) if attn_ms else None
     achieved = attn_bytes / (attn_us / 1e6) / 1e9 if attn_us else None
+    traffic = None
+    if a.workload == "longctx_b8":
+        traffic = LONGCTX_ATTN_TRAFFIC[0] * attn_bytes / LONGCTX_ATTN_TRAFFIC[1]
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak if achieved else None, "traffic": None,
+                "frac": achieved / peak if achieved else None, "traffic": traffic,
                 "kernel": f"bd_block_attention (one call per layer, {w.num_layers} per "
-                          f"denoise step)",
+                          f"denoise step: attn_pair_kernel + attn_pair_merge_kernel)",
                 "bytes_per_call": attn_bytes, "us_per_call": attn_us,
                 "calls_timed": len(attn_ms), "peak_source": f"{peak_kind} hbm_gbs"}
     breakdown = {
@@ -1209,8 +1221,61 @@ def run_kernel(a):
                       "peak_source": f"{kind} hbm_gbs"}))
 
 
+def run_step(a):
+    """One denoise step of the decoder workload launched eagerly, after one
+    warm-up step: every layer's projections and block attention, then the
+    confidence/commit.  Prints the step's duration; under a profiler the
+    second step's launches are exactly one step."""
+    import torch
+    from block_diffusion_decoding_denoise_gb300 import bd, build
+    from block_diffusion_decoding_denoise_gb300 import workload as wl
+    from block_diffusion_decoding_denoise_gb300.engine import (DecoderStack, DenoiseEngine,
+                                                               PagedCache)
+    if not os.path.exists(bd.LIB_PATH):
+        build.build()
+    bd.load()
+    w = wl.WORKLOADS[a.workload]
+    if w.num_layers == 1:
+        raise SystemExit("--kernel step needs a decoder workload (longctx_b8)")
+    L = w.block_len
+    plen = wl.prefix_lengths(w)
+    cap = plen + L
+    table, npg = wl.page_tables(w, cap)
+    bf = torch.bfloat16
+    caches = [PagedCache(npg, w.num_kv_heads, w.head_dim, bf, table) for _ in range(w.num_layers)]
+    for l, b, k, v in _decoder_inputs(w, plen):
+        caches[l].load_prefix(b, torch.from_numpy(k), torch.from_numpy(v))
+    dev = lambda x: torch.from_numpy(x).to("cuda", bf)
+    W = wl.lm_head(w)
+    lw = [tuple(dev(x) for x in wl.layer_weights(w, l)) for l in range(w.num_layers)]
+    ctx = torch.from_numpy(plen.astype(np.int32)).cuda()
+    stack = DecoderStack(dev(wl.embed_table(w)), dev(wl.mask_embedding(w)), lw, caches, ctx,
+                         batch=w.batch, block_len=L, num_q_heads=w.num_q_heads,
+                         max_ctx=int(cap.max()))
+    eng = DenoiseEngine(dev(W), caches, plen, batch=w.batch, block_len=L,
+                        num_q_heads=w.num_q_heads, threshold=w.threshold, max_ctx=int(cap.max()),
+                        decoder=stack)
+    h = dev(wl.planted_hidden(w, W, 0, steps=2)[0])
+    dummy = torch.empty(1, dtype=bf, device="cuda")
+    ts = []
+    for s in range(2):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push(f"step{s}")
+        e0.record()
+        eng.step(h[s], dummy, dummy, dummy, eng.n_committed[s])
+        e1.record()
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    eng.check_status()
+    print(json.dumps({"kernel": "step", "workload": w.name, "us": ts}))
+
+
 def main():
     a = _args()
+    if a.kernel == "step":
+        run_step(a)
+        return
     if a.kernel:
         run_kernel(a)
         return
