@@ -33,7 +33,10 @@ EXPORTS = ("bd_block_attention_workspace", "bd_block_attention",
            "bd_out_projection_workspace", "bd_out_projection_residual",
            "bd_append_block_kv_layers", "bd_confidence_commit_regions",
            "bd_sample_commit_truncated_workspace", "bd_sample_commit_truncated",
-           "bd_mlp_workspace", "bd_mlp_residual", "bd_debug_force_attention_kernel", "bd_debug_wait_timeout_selftest")
+           "bd_mlp_workspace", "bd_mlp_residual", "bd_debug_force_attention_kernel", "bd_debug_wait_timeout_selftest",
+           "bd_confidence_shard_workspace", "bd_confidence_shard", "bd_commit_shards",
+           "bd_merge_conf_records_host", "bd_merge_attention_partials_host",
+           "bd_merge_attention_partials")
 
 # bd_attention_kernel values of bd_debug_force_attention_kernel (test hook)
 BD_ATTN = {"auto": 0, "pair": 1, "mma": 2, "simt": 3}
@@ -87,6 +90,16 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "bd_kernel_launches": (ctypes.c_uint64, []),
             "bd_debug_force_attention_kernel": (c_int32, [c_int32]),
             "bd_debug_wait_timeout_selftest": (c_int32, [c_void_p, c_void_p]),
+            "bd_confidence_shard_workspace": (c_size_t, [c_int32] * 5),
+            "bd_confidence_shard": (c_int32, [c_int32] * 6 + [c_void_p] * 5 + [c_size_t, c_void_p,
+                                                                            c_void_p]),
+            "bd_commit_shards": (c_int32, [c_int32] * 4 + [c_void_p, c_float] + [c_void_p] * 7),
+            "bd_merge_conf_records_host": (c_int32, [c_int32, ctypes.c_int64, c_void_p, c_void_p]),
+            "bd_merge_attention_partials_host": (c_int32, [c_int32, ctypes.c_int64, c_int32,
+                                                           c_void_p, c_void_p, c_void_p, c_void_p]),
+            "bd_merge_attention_partials": (c_int32, [c_int32, ctypes.c_int64, c_int32, c_void_p,
+                                                      c_void_p, c_void_p, c_int32, c_void_p,
+                                                      c_void_p]),
             "bd_confidence_commit_noalloc": (c_int32, [c_int32, c_int32, c_int32, c_int32,
                                                        c_int32, c_void_p, c_void_p, c_float,
                                                        c_void_p, c_void_p, c_void_p, c_void_p,
@@ -412,3 +425,78 @@ def bd_append_block_kv_layers(kvs, k_blk, v_blk, ctx_len, n_masked=None, dev_sta
         _ptr(ctx_len, torch.int32, "ctx_len"), _ptr(n_masked, torch.int32, "n_masked"),
         _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check("bd_append_block_kv_layers", st)
+
+
+# --- one sequence split across GPUs (vocabulary slices, key slices) ------------
+RECORD_INTS = 3          # bd_conf_record: float m, float s, int32 idx
+
+
+def bd_confidence_shard_workspace(batch, block_len, hidden, vocab_shard) -> int:
+    return int(load().bd_confidence_shard_workspace(BD_BF16, batch, block_len, hidden,
+                                                    vocab_shard))
+
+
+def bd_confidence_shard(h, w_shard, vocab_offset, tokens, records, ws, dev_status=None,
+                        stream=None):
+    """records: int32 CUDA tensor [batch * block_len, 3] (bd_conf_record)."""
+    B, L, H = h.shape
+    Vs = w_shard.shape[0]
+    if records.dtype != torch.int32 or records.numel() != B * L * RECORD_INTS:
+        raise TypeError("records must be int32 [batch * block_len, 3]")
+    st = load().bd_confidence_shard(
+        BD_BF16, B, L, H, Vs, int(vocab_offset), _ptr(h, torch.bfloat16, "h"),
+        _ptr(w_shard, torch.bfloat16, "w_shard"), _ptr(tokens, torch.int32, "tokens"),
+        _ptr(records, torch.int32, "records"), _ptr(ws, name="ws"), ws.numel(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check("bd_confidence_shard", st)
+
+
+def bd_commit_shards(records, vocab, threshold, tokens, p_max, argmax, n_committed, n_masked,
+                     dev_status=None, stream=None):
+    """records: int32 CUDA tensor [num_shards, batch * block_len, 3]."""
+    B, L = tokens.shape
+    S = records.shape[0]
+    if records.dtype != torch.int32 or records.numel() != S * B * L * RECORD_INTS:
+        raise TypeError("records must be int32 [num_shards, batch * block_len, 3]")
+    st = load().bd_commit_shards(
+        B, L, int(vocab), S, _ptr(records, torch.int32, "records"), float(threshold),
+        _ptr(tokens, torch.int32, "tokens"), _ptr(p_max, torch.float32, "p_max"),
+        _ptr(argmax, torch.int32, "argmax"), _ptr(n_committed, torch.int32, "n_committed"),
+        _ptr(n_masked, torch.int32, "n_masked"), _ptr(dev_status, torch.int32, "dev_status"),
+        _stream(stream))
+    _check("bd_commit_shards", st)
+
+
+def bd_merge_conf_records_host(records):
+    """records: numpy structured array [num_shards, n] of (m f4, s f4, idx i4),
+    C-contiguous; returns the merged [n] array."""
+    import numpy as np
+    rec = np.ascontiguousarray(records)
+    S, n = rec.shape
+    out = np.empty(n, dtype=rec.dtype)
+    st = load().bd_merge_conf_records_host(S, n, rec.ctypes.data, out.ctypes.data)
+    _check("bd_merge_conf_records_host", st)
+    return out
+
+
+def bd_merge_attention_partials_host(m, l, o):
+    """m, l: float32 [num_shards, rows]; o: float32 [num_shards, rows, D] (host)."""
+    import numpy as np
+    m = np.ascontiguousarray(m, np.float32)
+    l = np.ascontiguousarray(l, np.float32)
+    o = np.ascontiguousarray(o, np.float32)
+    S, R, D = o.shape
+    out = np.empty((R, D), np.float32)
+    st = load().bd_merge_attention_partials_host(S, R, D, m.ctypes.data, l.ctypes.data,
+                                                 o.ctypes.data, out.ctypes.data)
+    _check("bd_merge_attention_partials_host", st)
+    return out
+
+
+def bd_merge_attention_partials(m, l, o, out, stream=None):
+    """Device merge: m, l [S, rows], o [S, rows, D] fp32 CUDA; out [rows, D] fp32/bf16."""
+    S, R, D = o.shape
+    st = load().bd_merge_attention_partials(
+        S, R, D, _ptr(m, torch.float32, "m"), _ptr(l, torch.float32, "l"),
+        _ptr(o, torch.float32, "o"), _dtype_code(out), _ptr(out, name="out"), _stream(stream))
+    _check("bd_merge_attention_partials", st)

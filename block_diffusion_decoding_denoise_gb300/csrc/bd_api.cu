@@ -34,7 +34,7 @@ bool preload_all() {
   const bool ok = preload_kernel(append_kv_kernel, false) && preload_attention_simt() &&
                   preload_attention_tc() && preload_confidence() &&
                   preload_lmhead_tc() && preload_decoder() && preload_attention_pair() &&
-                  preload_truncated();
+                  preload_truncated() && preload_parallel();
   if (!ok) {
     cudaGetLastError();
     return false;

@@ -241,6 +241,7 @@ bool preload_lmhead_tc();
 bool preload_decoder();
 bool preload_attention_pair();
 bool preload_truncated();
+bool preload_parallel();
 
 inline bd_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? BD_OK : BD_ERR_CUDA;

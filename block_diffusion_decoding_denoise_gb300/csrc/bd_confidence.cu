@@ -274,12 +274,15 @@ __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
       if constexpr (kSample) part = p.ws.spartial;
       else part = p.ws.partial;
       const int np = p.ws.num_partials;
+      const int64_t rs = p.ws.row_stride ? p.ws.row_stride : np;
+      const int64_t cs = p.ws.row_stride ? p.ws.col_stride : 1;
       for (int c0 = 0; c0 < np; c0 += 32 * kInFlight) {
         St v[kInFlight];
 #pragma unroll
         for (int j = 0; j < kInFlight; ++j) {
           const int c = c0 + lane + 32 * j;
-          if (c < np) v[j] = part[(size_t)k * np + c];   // a row's partials are contiguous
+          // by default a row's partials are contiguous (coalesced)
+          if (c < np) v[j] = part[(size_t)k * rs + (size_t)c * cs];
           else set_empty(v[j]);
         }
 #pragma unroll
@@ -304,6 +307,47 @@ __global__ void __launch_bounds__(1024) conf_commit_kernel(ConfParams p) {
   commit_sequence_warp(p, b, masked, masked ? s_pm[lane] : -1.f, masked ? s_am[lane] : -1);
 }
 
+// Vocabulary-parallel LM head: the merged (max, sum-exp, argmax) state of
+// every position over this call's vocabulary slice, the argmax shifted by the
+// slice's first entry, in position order; positions already committed get
+// the empty state.  One warp per position, partial loads as in the commit.
+__global__ void __launch_bounds__(1024) conf_records_kernel(ConfParams p, MaxSumArg *records,
+                                                            int vocab_offset) {
+  constexpr int kInFlight = 12;
+  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int L = p.block_len;
+  pdl_trigger();
+  pdl_wait();
+  if (warp >= L) return;
+  const int pos = b * L + warp;
+  const int tok = p.tokens[pos];
+  const int k = p.direct ? pos : p.ws.row_of[pos];
+  MaxSumArg st;
+  set_empty(st);
+  if (tok == BD_MASK) {
+    if (k < 0 || k >= p.batch * L) {
+      if (lane == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+    } else {
+      const int np = p.ws.num_partials;
+      for (int c0 = 0; c0 < np; c0 += 32 * kInFlight) {
+        MaxSumArg v[kInFlight];
+#pragma unroll
+        for (int j = 0; j < kInFlight; ++j) {
+          const int c = c0 + lane + 32 * j;
+          if (c < np) v[j] = p.ws.partial[(size_t)k * np + c];
+          else set_empty(v[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < kInFlight; ++j) st = merge(st, v[j]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) st = merge(st, shfl_xor_state(st, o));
+      if (st.idx >= 0 && st.idx < p.vocab) st.idx += vocab_offset;
+    }
+  }
+  if (lane == 0) records[pos] = st;
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -322,6 +366,7 @@ int conf_num_partials(bd_dtype dtype, int batch, int block_len, int hidden, int 
 bool preload_confidence() {
   return preload_kernel(conf_prep_kernel, false) &&
          preload_kernel(conf_commit_kernel<false>, false) &&
+         preload_kernel(conf_records_kernel, false) &&
          preload_kernel(conf_commit_kernel<true>, false) &&
          preload_kernel(lmhead_simt_kernel<float, false>, false) &&
          preload_kernel(lmhead_simt_kernel<__nv_bfloat16, false>, false) &&
@@ -390,12 +435,15 @@ struct TruncArgs {
 // Shared body of bd_confidence_commit, bd_sample_commit and
 // bd_sample_commit_truncated: argument checks, workspace carve, then
 // prep -> LM head (or logits + truncated selection) -> commit on one stream.
+// `records` (vocabulary-parallel LM head, greedy only): write every
+// position's merged state over this vocabulary slice instead of committing.
 static bd_status conf_run(ConfParams &p, const void *hidden_states, const void *lm_head,
                           void *ws, size_t ws_bytes, void *stream,
-                          const TruncArgs *trunc_in = nullptr) {
+                          const TruncArgs *trunc_in = nullptr, MaxSumArg *records = nullptr,
+                          int vocab_offset = 0) {
   if (!conf_args_ok(p.dtype, p.batch, p.block_len, p.hidden, p.vocab)) return BD_ERR_INVALID_ARG;
-  if (!hidden_states || !lm_head || !p.tokens || !p.p_max || !p.argmax || !p.n_committed ||
-      !p.n_masked)
+  if (!hidden_states || !lm_head || !p.tokens ||
+      (!records && (!p.p_max || !p.argmax || !p.n_committed || !p.n_masked)))
     return BD_ERR_INVALID_ARG;
   if (!preload_all()) return BD_ERR_CUDA;
   if (isnan(p.threshold)) return BD_ERR_INVALID_ARG;
@@ -443,6 +491,12 @@ static bd_status conf_run(ConfParams &p, const void *hidden_states, const void *
     s = tc ? lmhead_tc(p, st) : lmhead_simt(p, st);
   }
   if (s != BD_OK) return s;
+  if (records) {
+    e = launch_pdl(conf_records_kernel, dim3(p.batch), dim3(32 * p.block_len), 0, st, p, records,
+                   vocab_offset);
+    count_launches(1);
+    return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+  }
   e = p.sample ? launch_pdl(conf_commit_kernel<true>, dim3(p.batch), dim3(32 * p.block_len), 0,
                             st, p)
                : launch_pdl(conf_commit_kernel<false>, dim3(p.batch), dim3(32 * p.block_len), 0,
@@ -579,4 +633,71 @@ BD_API bd_status bd_sample_commit(bd_dtype dtype, int32_t batch, int32_t block_l
   p.seed = seed;
   p.offset = offset;
   return conf_run(p, hidden_states, lm_head, ws, ws_bytes, stream);
+}
+
+// ---------------------------------------------------------------------------
+// vocabulary-parallel LM head (one vocabulary slice per GPU)
+// ---------------------------------------------------------------------------
+static_assert(sizeof(bd_conf_record) == sizeof(MaxSumArg), "record layout");
+
+BD_API size_t bd_confidence_shard_workspace(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                            int32_t hidden, int32_t vocab_shard) {
+  if (dtype != BD_BF16) return 0;
+  return conf_workspace(dtype, batch, block_len, hidden, vocab_shard, false);
+}
+
+BD_API bd_status bd_confidence_shard(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                     int32_t hidden, int32_t vocab_shard, int32_t vocab_offset,
+                                     const void *hidden_states, const void *lm_head_shard,
+                                     const int32_t *tokens, bd_conf_record *records, void *ws,
+                                     size_t ws_bytes, int32_t *dev_status, void *stream) {
+  if (dtype != BD_BF16 || !records || vocab_offset < 0 ||
+      (int64_t)vocab_offset + vocab_shard > (int64_t)1 << 31)
+    return BD_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(records) & 3) return BD_ERR_INVALID_ARG;
+  ConfParams p{};
+  p.dtype = dtype;
+  p.batch = batch;
+  p.block_len = block_len;
+  p.hidden = hidden;
+  p.vocab = vocab_shard;
+  p.tokens = const_cast<int32_t *>(tokens);
+  p.dev_status = dev_status;
+  return conf_run(p, hidden_states, lm_head_shard, ws, ws_bytes, stream, nullptr,
+                  reinterpret_cast<MaxSumArg *>(records), vocab_offset);
+}
+
+BD_API bd_status bd_commit_shards(int32_t batch, int32_t block_len, int32_t vocab,
+                                  int32_t num_shards, const bd_conf_record *records,
+                                  float threshold, int32_t *tokens, float *p_max, int32_t *argmax,
+                                  int32_t *n_committed, int32_t *n_masked, int32_t *dev_status,
+                                  void *stream) {
+  if (batch < 1 || block_len < 1 || block_len > 32 || vocab < 1 || num_shards < 1 ||
+      (int64_t)batch * block_len > (1 << 20))
+    return BD_ERR_INVALID_ARG;
+  if (!records || !tokens || !p_max || !argmax || !n_committed || !n_masked || isnan(threshold))
+    return BD_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(records) & 3) return BD_ERR_INVALID_ARG;
+  if (!preload_all()) return BD_ERR_CUDA;
+  ConfParams p{};
+  p.dtype = BD_BF16;
+  p.batch = batch;
+  p.block_len = block_len;
+  p.vocab = vocab;
+  p.threshold = threshold;
+  p.tokens = tokens;
+  p.p_max = p_max;
+  p.argmax = argmax;
+  p.n_committed = n_committed;
+  p.n_masked = n_masked;
+  p.dev_status = dev_status;
+  p.direct = 1;                               // records are in position order
+  p.ws.partial = const_cast<MaxSumArg *>(reinterpret_cast<const MaxSumArg *>(records));
+  p.ws.num_partials = num_shards;
+  p.ws.row_stride = 1;                        // [shard][position]
+  p.ws.col_stride = (int64_t)batch * block_len;
+  const cudaError_t e = launch_pdl(conf_commit_kernel<false>, dim3(batch), dim3(32 * block_len),
+                                   0, static_cast<cudaStream_t>(stream), p);
+  count_launches(1);
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }

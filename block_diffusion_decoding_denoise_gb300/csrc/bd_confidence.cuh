@@ -22,6 +22,9 @@ struct ConfWorkspace {
   MaxSumArg *partial;
   SampleState *spartial;  // the same memory, typed for the sampling mode
   int num_partials;
+  // partial (row k, producer c) at k * row_stride + c * col_stride; 0 means the
+  // default [row][producer] layout (row_stride = num_partials, col_stride = 1)
+  int64_t row_stride, col_stride;
   char *hc;
 };
 

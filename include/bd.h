@@ -376,6 +376,67 @@ bd_status bd_append_block_kv_layers(const bd_paged_kv *kv, int32_t num_layers, i
                                     int32_t *ctx_len, const int32_t *n_masked,
                                     int32_t *dev_status, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Splitting one sequence across GPUs (the path otherwise shards by sequence
+ * with no exchange).  Each split needs one exchange, done by the caller with
+ * its collective library; these calls produce what is exchanged and combine
+ * what was gathered (method steps 3-4: the block's attention and each masked
+ * position's confidence are the quantities split).
+ *
+ * bd_conf_record: the online-softmax state of one position over a slice of
+ * the vocabulary: m = max logit, s = sum of exp(l - m) over the slice, idx =
+ * lowest vocabulary id (whole-vocabulary numbering) attaining m.  A position
+ * that is not masked holds m = -inf, s = 0, idx = INT32_MAX.  12 bytes.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  float m;
+  float s;
+  int32_t idx;
+} bd_conf_record;
+
+/* Vocabulary-parallel LM head: this GPU's slice lm_head_shard = rows
+ * [vocab_offset, vocab_offset + vocab_shard) of W ([vocab_shard][hidden],
+ * bf16).  For every position of tokens (BD_MASK = masked) writes
+ * records[b * block_len + i] over the slice; no logit reaches memory and
+ * nothing is committed.  Workspace from bd_confidence_shard_workspace()
+ * (256-byte aligned).  bf16 only. */
+size_t bd_confidence_shard_workspace(bd_dtype dtype, int32_t batch, int32_t block_len,
+                                     int32_t hidden, int32_t vocab_shard);
+bd_status bd_confidence_shard(bd_dtype dtype, int32_t batch, int32_t block_len, int32_t hidden,
+                              int32_t vocab_shard, int32_t vocab_offset,
+                              const void *hidden_states, const void *lm_head_shard,
+                              const int32_t *tokens, bd_conf_record *records, void *ws,
+                              size_t ws_bytes, int32_t *dev_status, void *stream);
+
+/* The commit of bd_confidence_commit from gathered records: records is
+ * DEVICE memory [num_shards][batch * block_len] (the concatenation of every
+ * slice's records, in any shard order); vocab is the whole vocabulary size.
+ * Merges each position's states (p_max = 1 / s, argmax = idx) and applies the
+ * commit rule; outputs as bd_confidence_commit. */
+bd_status bd_commit_shards(int32_t batch, int32_t block_len, int32_t vocab, int32_t num_shards,
+                           const bd_conf_record *records, float threshold, int32_t *tokens,
+                           float *p_max, int32_t *argmax, int32_t *n_committed,
+                           int32_t *n_masked, int32_t *dev_status, void *stream);
+
+/* Host-side merge of gathered records (HOST memory [num_shards][n] -> [n]),
+ * the same rule as the device merge.  No CUDA call. */
+bd_status bd_merge_conf_records_host(int32_t num_shards, int64_t n,
+                                     const bd_conf_record *records, bd_conf_record *out);
+
+/* KV-split attention: merge per-row partials of num_shards key slices,
+ * m and l [num_shards][rows] (max in natural-log units, sum of exp(s - m)),
+ * o [num_shards][rows][head_dim] unnormalised: out[r] = sum_s e^(m_s - M)
+ * o_s[r] / sum_s e^(m_s - M) l_s[r].  A slice with no key of a row holds
+ * m = -inf, l = 0.  The host version takes HOST pointers and calls no CUDA
+ * function; the device version takes DEVICE pointers and writes out
+ * [rows][head_dim] as fp32 or bf16 (head_dim <= 256), async on stream. */
+bd_status bd_merge_attention_partials_host(int32_t num_shards, int64_t rows, int32_t head_dim,
+                                           const float *m, const float *l, const float *o,
+                                           float *out);
+bd_status bd_merge_attention_partials(int32_t num_shards, int64_t rows, int32_t head_dim,
+                                      const float *m, const float *l, const float *o,
+                                      bd_dtype out_dtype, void *out, void *stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *bd_status_string(bd_status status);
 
