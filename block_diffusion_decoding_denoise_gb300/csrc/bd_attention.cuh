@@ -41,6 +41,7 @@ __host__ __device__ inline int sk_cta_of(long long t, long long T, long long G) 
 
 bd_status attention_simt(const AttnParams &p, cudaStream_t st);
 bd_status attention_tc(const AttnParams &p, cudaStream_t st);
+bd_status attention_cluster(const AttnParams &p, cudaStream_t st);
 bd_status attention_combine(const AttnParams &p, cudaStream_t st);
 bd_status attention_combine_sk(const AttnParams &p, cudaStream_t st);
 bool attention_pair_supported(const AttnParams &p);

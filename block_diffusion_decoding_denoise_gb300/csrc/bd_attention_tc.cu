@@ -32,6 +32,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "bd_attention.cuh"
 #include "bd_common.cuh"
@@ -169,6 +170,161 @@ __global__ void __launch_bounds__(1024) attn_plan_kernel(AttnParams p) {
   }
   if (threadIdx.x == 0) p.plan[2 * p.batch] = carry;
 }
+// One tile of a consumer warp: S = Q K^T over the warp's keys [max(lo, key0),
+// min(hi, key0 + 8 KJ)) of the stage at bk (K, then V TILE bytes later), the
+// online-softmax update of (m_run, l_run, o) and O += P V.
+template <int D, int KJ>
+__device__ __forceinline__ void attend_tile(uint8_t *bk, int lo, int hi, int key0, int lane,
+                                            float sl2, const uint32_t (&qa)[D / 16][4],
+                                            float (&o)[D / 8][4], float (&m_run)[2],
+                                            float (&l_run)[2]) {
+  constexpr int NH = D / 64;
+  constexpr int TILE = NH * kHalfBytes;
+  constexpr int KSTEPS = D / 16;
+  constexpr int DN = D / 8;
+  const int tig = lane & 3;
+  const int w_lo = max(lo, key0), w_hi = min(hi, key0 + 8 * KJ);
+  if (w_lo >= w_hi) return;
+  uint8_t *bv = bk + TILE;
+  const uint32_t kbase = smem_u32(bk), vbase = smem_u32(bv);
+  const int hi16 = (w_hi + 15) & ~15;
+  const bool zeroed = (w_hi & 15) != 0;
+  if (zeroed) {                          // rows past the valid ones feed P = 0: make them finite
+    for (int e = lane; e < (hi16 - w_hi) * NH * 8; e += 32) {
+      const int row = w_hi + e / (NH * 8), chunk = e % (NH * 8);
+      *reinterpret_cast<int4 *>(bv + swz(row, chunk)) = make_int4(0, 0, 0, 0);
+    }
+    __syncwarp();
+  }
+  // S = Q K^T for this warp's 16 rows x 8 KJ keys
+  float sc[KJ][4];
+#pragma unroll
+  for (int j = 0; j < KJ; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < KSTEPS; ++kk) {
+#pragma unroll
+    for (int jp = 0; jp < KJ / 2; ++jp) {
+      if (key0 + 16 * jp < w_hi) {
+        const int key = key0 + 16 * jp + (lane & 7) + ((lane >> 4) << 3);
+        const int chunk = 2 * kk + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + swz(key, chunk), b0, b1, b2, b3);
+        mma_16816(sc[2 * jp], qa[kk], b0, b1);
+        mma_16816(sc[2 * jp + 1], qa[kk], b2, b3);
+      }
+    }
+  }
+  float mt[2] = {-INFINITY, -INFINITY};
+  if (w_lo != key0 || w_hi != key0 + 8 * KJ) {   // partial tile: mask the invalid keys
+#pragma unroll
+    for (int j = 0; j < KJ; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = key0 + 8 * j + tig * 2 + (e & 1);
+        if (key < w_lo || key >= w_hi) sc[j][e] = -INFINITY;
+      }
+  }
+#pragma unroll
+  for (int j = 0; j < KJ; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mt[e >> 1] = fmaxf(mt[e >> 1], sc[j][e]);
+  float corr[2], mneg[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], 1));
+    mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], 2));
+    const float mnew = fmaxf(m_run[i], mt[i]);
+    corr[i] = fast_exp2((m_run[i] - mnew) * sl2);
+    m_run[i] = mnew;
+    mneg[i] = -mnew * sl2;
+    l_run[i] *= corr[i];
+  }
+  // rescale only when some running max of the warp moved (a factor of
+  // exactly 1 changes nothing, and after the first tiles most do not move)
+  if (!__all_sync(0xffffffffu, corr[0] == 1.f && corr[1] == 1.f)) {
+#pragma unroll
+    for (int j = 0; j < DN; ++j) {
+      o[j][0] *= corr[0];
+      o[j][1] *= corr[0];
+      o[j][2] *= corr[1];
+      o[j][3] *= corr[1];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < KJ; ++j) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      sc[j][e] = fast_exp2(fmaf(sc[j][e], sl2, mneg[e >> 1]));
+      l_run[e >> 1] += sc[j][e];
+    }
+  }
+  uint32_t pa[KJ / 2][4];
+#pragma unroll
+  for (int kk = 0; kk < KJ / 2; ++kk) {
+    pa[kk][0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
+    pa[kk][1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
+    pa[kk][2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+    pa[kk][3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+  }
+#pragma unroll
+  for (int kk = 0; kk < KJ / 2; ++kk) {
+    if (key0 + 16 * kk < hi16) {
+#pragma unroll
+      for (int dp = 0; dp < DN / 2; ++dp) {
+        const int key = key0 + 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int chunk = 2 * dp + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vbase + swz(key, chunk), b0, b1, b2, b3);
+        mma_16816(o[2 * dp], pa[kk], b0, b1);
+        mma_16816(o[2 * dp + 1], pa[kk], b2, b3);
+      }
+    }
+  }
+  if (zeroed) fence_proxy_async();       // our generic writes precede the next TMA fill
+}
+
+// Merge the two key halves of a row group (KH = 2): half 1 hands its state
+// over through the exchange slot, half 0 folds it into its own.  Both warps
+// of the row group call this once.
+template <int D>
+__device__ __forceinline__ void merge_key_halves(float *xchg, int rg, int kh, int lane, float sl2,
+                                                 float (&o)[D / 8][4], float (&m_run)[2],
+                                                 float (&l_run)[2]) {
+  constexpr int DN = D / 8;
+  // merge the two key halves of the row group: half 1 hands over, half 0 writes
+  constexpr int F = 4 * DN + 4;        // floats per lane: o[DN][4] + m[2], l[2]
+  float *xw = xchg + (size_t)rg * F * 32;
+  if (kh == 1) {
+#pragma unroll
+    for (int j = 0; j < DN; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) xw[(j * 4 + e) * 32 + lane] = o[j][e];
+    xw[(4 * DN + 0) * 32 + lane] = m_run[0];
+    xw[(4 * DN + 1) * 32 + lane] = m_run[1];
+    xw[(4 * DN + 2) * 32 + lane] = l_run[0];
+    xw[(4 * DN + 3) * 32 + lane] = l_run[1];
+  }
+  named_barrier(1 + rg, 64);
+  if (kh == 0) {
+    float w0[2], w1[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float mo = xw[(4 * DN + i) * 32 + lane];
+      const float mnew = fmaxf(m_run[i], mo);
+      w0[i] = m_run[i] == -INFINITY ? 0.f : exp2f((m_run[i] - mnew) * sl2);
+      w1[i] = mo == -INFINITY ? 0.f : exp2f((mo - mnew) * sl2);
+      l_run[i] = l_run[i] * w0[i] + xw[(4 * DN + 2 + i) * 32 + lane] * w1[i];
+      m_run[i] = mnew;
+    }
+#pragma unroll
+    for (int j = 0; j < DN; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        o[j][e] = o[j][e] * w0[e >> 1] + xw[(j * 4 + e) * 32 + lane] * w1[e >> 1];
+  }
+  named_barrier(1 + rg, 64);           // exchange slot free for the next item
+}
+
 constexpr int kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8;
 constexpr int kMaxStages = 12;
 
@@ -434,144 +590,13 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
         m_run[0] = m_run[1] = -INFINITY;
         l_run[0] = l_run[1] = 0.f;
       }
-      // this warp's valid keys of the tile: [max(lo, key0), min(hi, key0 + 8 KJ))
-      const int lo = m.lo, hi = m.hi;
-      const int w_lo = max(lo, key0), w_hi = min(hi, key0 + 8 * KJ);
-      if (!(m.flags & kSkip) && w_lo < w_hi) {
-        uint8_t *bk = smem + (size_t)s * 2 * TILE, *bv = bk + TILE;
-        const uint32_t kbase = smem_u32(bk), vbase = smem_u32(bv);
-        const int hi16 = (w_hi + 15) & ~15;
-        const bool zeroed = (w_hi & 15) != 0;
-        if (zeroed) {                          // rows past the valid ones feed P = 0: make them finite
-          for (int e = lane; e < (hi16 - w_hi) * NH * 8; e += 32) {
-            const int row = w_hi + e / (NH * 8), chunk = e % (NH * 8);
-            *reinterpret_cast<int4 *>(bv + swz(row, chunk)) = make_int4(0, 0, 0, 0);
-          }
-          __syncwarp();
-        }
-        // S = Q K^T for this warp's 16 rows x 8 KJ keys
-        float sc[KJ][4];
-#pragma unroll
-        for (int j = 0; j < KJ; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < KSTEPS; ++kk) {
-#pragma unroll
-          for (int jp = 0; jp < KJ / 2; ++jp) {
-            if (key0 + 16 * jp < w_hi) {
-              const int key = key0 + 16 * jp + (lane & 7) + ((lane >> 4) << 3);
-              const int chunk = 2 * kk + ((lane >> 3) & 1);
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4(kbase + swz(key, chunk), b0, b1, b2, b3);
-              mma_16816(sc[2 * jp], qa[kk], b0, b1);
-              mma_16816(sc[2 * jp + 1], qa[kk], b2, b3);
-            }
-          }
-        }
-        float mt[2] = {-INFINITY, -INFINITY};
-        if (w_lo != key0 || w_hi != key0 + 8 * KJ) {   // partial tile: mask the invalid keys
-#pragma unroll
-          for (int j = 0; j < KJ; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int key = key0 + 8 * j + tig * 2 + (e & 1);
-              if (key < w_lo || key >= w_hi) sc[j][e] = -INFINITY;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < KJ; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) mt[e >> 1] = fmaxf(mt[e >> 1], sc[j][e]);
-        float corr[2], mneg[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], 1));
-          mt[i] = fmaxf(mt[i], __shfl_xor_sync(0xffffffffu, mt[i], 2));
-          const float mnew = fmaxf(m_run[i], mt[i]);
-          corr[i] = fast_exp2((m_run[i] - mnew) * sl2);
-          m_run[i] = mnew;
-          mneg[i] = -mnew * sl2;
-          l_run[i] *= corr[i];
-        }
-        // rescale only when some running max of the warp moved (a factor of
-        // exactly 1 changes nothing, and after the first tiles most do not move)
-        if (!__all_sync(0xffffffffu, corr[0] == 1.f && corr[1] == 1.f)) {
-#pragma unroll
-          for (int j = 0; j < DN; ++j) {
-            o[j][0] *= corr[0];
-            o[j][1] *= corr[0];
-            o[j][2] *= corr[1];
-            o[j][3] *= corr[1];
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < KJ; ++j) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            sc[j][e] = fast_exp2(fmaf(sc[j][e], sl2, mneg[e >> 1]));
-            l_run[e >> 1] += sc[j][e];
-          }
-        }
-        uint32_t pa[KJ / 2][4];
-#pragma unroll
-        for (int kk = 0; kk < KJ / 2; ++kk) {
-          pa[kk][0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-          pa[kk][1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-          pa[kk][2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-          pa[kk][3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-        }
-#pragma unroll
-        for (int kk = 0; kk < KJ / 2; ++kk) {
-          if (key0 + 16 * kk < hi16) {
-#pragma unroll
-            for (int dp = 0; dp < DN / 2; ++dp) {
-              const int key = key0 + 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
-              const int chunk = 2 * dp + (lane >> 4);
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4_t(vbase + swz(key, chunk), b0, b1, b2, b3);
-              mma_16816(o[2 * dp], pa[kk], b0, b1);
-              mma_16816(o[2 * dp + 1], pa[kk], b2, b3);
-            }
-          }
-        }
-        if (zeroed) fence_proxy_async();       // our generic writes precede the next TMA fill
-      }
+      if (!(m.flags & kSkip))
+        attend_tile<D, KJ>(smem + (size_t)s * 2 * TILE, m.lo, m.hi, key0, lane, sl2, qa, o, m_run,
+                           l_run);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
       if (m.flags & kLast) {
-        if (KH == 2) {
-          // merge the two key halves of the row group: half 1 hands over, half 0 writes
-          constexpr int F = 4 * DN + 4;        // floats per lane: o[DN][4] + m[2], l[2]
-          float *xw = xchg + (size_t)rg * F * 32;
-          if (kh == 1) {
-#pragma unroll
-            for (int j = 0; j < DN; ++j)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) xw[(j * 4 + e) * 32 + lane] = o[j][e];
-            xw[(4 * DN + 0) * 32 + lane] = m_run[0];
-            xw[(4 * DN + 1) * 32 + lane] = m_run[1];
-            xw[(4 * DN + 2) * 32 + lane] = l_run[0];
-            xw[(4 * DN + 3) * 32 + lane] = l_run[1];
-          }
-          named_barrier(1 + rg, 64);
-          if (kh == 0) {
-            float w0[2], w1[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const float mo = xw[(4 * DN + i) * 32 + lane];
-              const float mnew = fmaxf(m_run[i], mo);
-              w0[i] = m_run[i] == -INFINITY ? 0.f : exp2f((m_run[i] - mnew) * sl2);
-              w1[i] = mo == -INFINITY ? 0.f : exp2f((mo - mnew) * sl2);
-              l_run[i] = l_run[i] * w0[i] + xw[(4 * DN + 2 + i) * 32 + lane] * w1[i];
-              m_run[i] = mnew;
-            }
-#pragma unroll
-            for (int j = 0; j < DN; ++j)
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                o[j][e] = o[j][e] * w0[e >> 1] + xw[(j * 4 + e) * 32 + lane] * w1[e >> 1];
-          }
-          named_barrier(1 + rg, 64);           // exchange slot free for the next item
-        }
+        if (KH == 2) merge_key_halves<D>(xchg, rg, kh, lane, sl2, o, m_run, l_run);
         if (kh == 0) {
           float lsum[2];
 #pragma unroll
@@ -611,14 +636,323 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
   __syncthreads();
 }
 
+// Block attention for small problems, one launch, no partials in global memory.
+//
+// A cluster of C CTAs works on one segment (sequence b, KV head g).  The
+// segment's tiles are numbered on a grid fixed by max_ctx: u = 0 .. Tm - 1
+// with Tm = ceil(max_ctx / 64) + 1; tile u < npg = ceil(ctx / 64) is cached
+// page u, tile npg is the block's own keys and later tiles are empty.  CTA
+// rank r takes tiles [r Tm / C, (r + 1) Tm / C).  That range does not depend
+// on ctx, so the producer issues its loads of the block's tokens, of ctx and
+// of the range's page ids together (one memory latency before the first TMA),
+// and the consumers load their Q rows before the first tile lands.  At the
+// end every CTA leaves its piece's state (m in base-2 units, l, O) in its own
+// shared memory; after a cluster barrier CTA r merges rows [r R / C,
+// (r + 1) R / C) of all C pieces through distributed shared memory,
+//   out = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k,
+// and writes them as bf16.  A second cluster barrier keeps every CTA's pieces
+// alive until the other CTAs have read them.
+constexpr int kMaxCluster = 16;
+
 template <int D, int RG, int KH>
-bd_status launch(const AttnParams &p, cudaStream_t st) {
-  constexpr int NW = RG * KH;
-  constexpr size_t kXchgBytes = KH == 2 ? (size_t)RG * (4 * (D / 8) + 4) * 32 * 4 : 0;
+__global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
+    attn_cluster_kernel(const __grid_constant__ CUtensorMap mk_pool,
+                        const __grid_constant__ CUtensorMap mv_pool,
+                        const __grid_constant__ CUtensorMap mk_blk,
+                        const __grid_constant__ CUtensorMap mv_blk, const AttnParams p, int S,
+                        int C, int Tm) {
   constexpr int NH = D / 64;
   constexpr int TILE = NH * kHalfBytes;
+  constexpr int KSTEPS = D / 16;
+  constexpr int DN = D / 8;
+  constexpr int DPL = D / 32;                 // merged columns per lane
+  constexpr int NW = RG * KH;
+  constexpr int KJ = 8 / KH;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * 2 * TILE);
+  uint64_t *empty = full + kMaxStages;
+  TileMeta *meta = reinterpret_cast<TileMeta *>(empty + kMaxStages);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(meta + kMaxStages);
+  volatile int *active_flag = abort_flag + 1;
+
+  const int group = p.hq / p.hkv;
+  const int R = p.block_len * group;
+  const int L = p.block_len;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cluster_ctarank();
+  const int seg = blockIdx.x / C;
+  const int b = seg / p.hkv, g = seg % p.hkv;
+  const float sl2 = p.scale * 1.4426950408889634f;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), NW);
+    }
+    *abort_flag = 0;
+    *active_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mk_pool);
+    tma_prefetch_desc(&mv_pool);
+    tma_prefetch_desc(&mk_blk);
+    tma_prefetch_desc(&mv_blk);
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+
+  // consumer state (warps 1..NW); warp cw owns rows [16 rg, 16 rg + 16) and,
+  // when KH == 2, one half of the keys of every tile
+  const int cw = warp - 1;
+  const int rg = cw % RG, kh = cw / RG;
+  const int key0 = kh * 8 * KJ;
+  const int gid = lane >> 2, tig = lane & 3;
+  uint32_t qa[KSTEPS][4];
+  float o[DN][4];
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < DN; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const int u0 = (int)((long long)rank * Tm / C), u1 = (int)((long long)(rank + 1) * Tm / C);
+    const int32_t *tok = p.tokens ? p.tokens + (size_t)b * L : nullptr;
+    const int32_t *ptab = p.page_table + (size_t)b * p.max_pages;
+    // one memory latency: the block's tokens, ctx and the first 32 page ids
+    const int t = (tok && lane < L) ? tok[lane] : 0;
+    const int ctx = p.ctx_len[b];
+    int pid = -1;
+    if (u0 + lane < u1 && u0 + lane < p.max_pages) pid = ptab[u0 + lane];
+    const bool has = !tok || __any_sync(0xffffffffu, lane < L && t == BD_MASK);
+    const bool ctx_ok = ctx >= 0 && ctx <= p.max_ctx && ctx <= p.max_pages * p.page_size;
+    if (has && !ctx_ok && rank == 0 && lane == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+    const bool active = has && ctx_ok;
+    if (lane == 0) *active_flag = active ? 1 : 0;
+    uint32_t it = 0;
+    bool stop = false;
+    auto acquire = [&](uint32_t &s_out) -> bool {
+      const uint32_t s = it % S, round = it / S;
+      int ok = 1;
+      if (lane == 0) {
+        if (*abort_flag) ok = 0;
+        else if (round > 0 && !mbar_wait(smem_u32(&empty[s]), (round - 1) & 1)) {
+          ok = 0;
+          *abort_flag = 1;
+          flag_error(p.dev_status, BD_ERR_TIMEOUT);
+        }
+      }
+      s_out = s;
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
+    if (active) {
+      const int npg = (ctx + kPageRows - 1) / kPageRows;
+      const int last = min(u1, npg + 1);
+      for (int c0 = u0; c0 < last && !stop; c0 += 32) {
+        if (c0 != u0) {
+          pid = -1;
+          if (c0 + lane < last && c0 + lane < npg) pid = ptab[c0 + lane];
+        }
+        const int cend = min(c0 + 32, last);
+        for (int u = c0; u < cend && !stop; ++u) {
+          const int pg = __shfl_sync(0xffffffffu, pid, u - c0);
+          uint32_t s;
+          if (!acquire(s)) {
+            stop = true;
+            break;
+          }
+          if (lane == 0) {
+            const uint32_t bar = smem_u32(&full[s]);
+            uint8_t *bk = smem + (size_t)s * 2 * TILE, *bv = bk + TILE;
+            TileMeta m;
+            m.item = seg;
+            m.slot = -1;
+            m.flags = 0;
+            m.lo = 0;
+            if (u < npg) {
+              m.hi = min(kPageRows, ctx - u * kPageRows);
+              if (pg >= 0 && pg < p.num_pages) {
+                meta[s] = m;
+                fence_proxy_async();
+                mbar_arrive_expect_tx(bar, 2 * TILE);
+#pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                  tma_load_4d(smem_u32(bk + h * kHalfBytes), &mk_pool, 64 * h, 0, g, pg, bar);
+                  tma_load_4d(smem_u32(bv + h * kHalfBytes), &mv_pool, 64 * h, 0, g, pg, bar);
+                }
+              } else {
+                flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+                m.flags = kSkip;
+                meta[s] = m;
+                mbar_arrive(bar);
+              }
+            } else {                               // u == npg: the block's own keys
+              m.hi = L;
+              meta[s] = m;
+              fence_proxy_async();
+              mbar_arrive_expect_tx(bar, 2 * NH * L * 128);
+#pragma unroll
+              for (int h = 0; h < NH; ++h) {
+                tma_load_4d(smem_u32(bk + h * kHalfBytes), &mk_blk, 64 * h, g, 0, b, bar);
+                tma_load_4d(smem_u32(bv + h * kHalfBytes), &mv_blk, 64 * h, g, 0, b, bar);
+              }
+            }
+          }
+          __syncwarp();
+          ++it;
+        }
+      }
+    }
+    if (!stop) {
+      uint32_t s;
+      if (acquire(s)) {
+        if (lane == 0) {
+          meta[s] = TileMeta{-1, 0, 0, kEnd, -1};
+          mbar_arrive(smem_u32(&full[s]));
+        }
+        ++it;
+      }
+    }
+    // Wait for every copy this CTA issued (each stage's last use), so that
+    // the stage memory is free for the merge below; on the normal path the
+    // consumers have already seen all of them land.
+    if (lane == 0) {
+      const uint32_t first = it > (uint32_t)S ? it - S : 0;
+      for (uint32_t i = first; i < it; ++i) mbar_wait(smem_u32(&full[i % S]), (i / S) & 1);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ consumers
+    {
+      const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q);
+      const int r_lo = rg * 16 + gid, r_hi = r_lo + 8;
+      const __nv_bfloat16 *q_lo = nullptr, *q_hi = nullptr;
+      if (r_lo < R)
+        q_lo = q + (((size_t)b * L + r_lo / group) * p.hq + g * group + r_lo % group) * D;
+      if (r_hi < R)
+        q_hi = q + (((size_t)b * L + r_hi / group) * p.hq + g * group + r_hi % group) * D;
+#pragma unroll
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        const int c = kk * 16 + tig * 2;
+        qa[kk][0] = q_lo ? *reinterpret_cast<const uint32_t *>(q_lo + c) : 0u;
+        qa[kk][1] = q_hi ? *reinterpret_cast<const uint32_t *>(q_hi + c) : 0u;
+        qa[kk][2] = q_lo ? *reinterpret_cast<const uint32_t *>(q_lo + c + 8) : 0u;
+        qa[kk][3] = q_hi ? *reinterpret_cast<const uint32_t *>(q_hi + c + 8) : 0u;
+      }
+    }
+    for (uint32_t it = 0;; ++it) {
+      const uint32_t s = it % S;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(smem_u32(&full[s]), (it / S) & 1) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          flag_error(p.dev_status, BD_ERR_TIMEOUT);
+        }
+        break;
+      }
+      const volatile int *mv = reinterpret_cast<const volatile int *>(&meta[s]);
+      const int lo = mv[1], hi = mv[2], flags = mv[3];
+      if (flags & kEnd) break;
+      if (!(flags & kSkip))
+        attend_tile<D, KJ>(smem + (size_t)s * 2 * TILE, lo, hi, key0, lane, sl2, qa, o, m_run,
+                           l_run);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    }
+  }
+  __syncthreads();                             // stage memory free: pieces and exchange go there
+
+  // this CTA's piece: O [R][D] fp32, then (m in base-2 units, l) [R][2]
+  float *c_o = reinterpret_cast<float *>(smem);
+  float *c_ml = c_o + (size_t)R * D;
+  float *xchg = c_ml + 2 * (size_t)R;
+  if (warp > 0) {
+    if (KH == 2) merge_key_halves<D>(xchg, rg, kh, lane, sl2, o, m_run, l_run);
+    if (kh == 0) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        float ls = l_run[i] + __shfl_xor_sync(0xffffffffu, l_run[i], 1);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+        const int r = rg * 16 + gid + 8 * i;
+        if (r < R) {
+#pragma unroll
+          for (int j = 0; j < DN; ++j)
+            *reinterpret_cast<float2 *>(c_o + (size_t)r * D + 8 * j + tig * 2) =
+                make_float2(o[j][2 * i], o[j][2 * i + 1]);
+          if (tig == 0)
+            *reinterpret_cast<float2 *>(c_ml + 2 * r) = make_float2(m_run[i] * sl2, ls);
+        }
+      }
+    }
+  }
+  cluster_sync();                              // every piece of the cluster is written
+
+  if (*active_flag) {
+    const int r_begin = (int)((long long)rank * R / C), r_end = (int)((long long)(rank + 1) * R / C);
+    for (int r = r_begin + warp; r < r_end; r += NW + 1) {
+      float2 ml = make_float2(-INFINITY, 0.f);
+      if (lane < C) ml = ld_cluster_f2(map_shared(smem_u32(c_ml + 2 * r), lane));
+      float v[kMaxCluster][DPL];
+      const uint32_t src = smem_u32(c_o + (size_t)r * D + lane * DPL);
+#pragma unroll
+      for (int k = 0; k < kMaxCluster; ++k) {
+        if (k < C) {
+          if constexpr (DPL == 4) {
+            const float4 x = ld_cluster_f4(map_shared(src, k));
+            v[k][0] = x.x;
+            v[k][1] = x.y;
+            v[k][2] = x.z;
+            v[k][3] = x.w;
+          } else {
+            const float2 x = ld_cluster_f2(map_shared(src, k));
+            v[k][0] = x.x;
+            v[k][1] = x.y;
+          }
+        }
+      }
+      float mx = ml.x;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float w = (lane < C && ml.x != -INFINITY) ? exp2f(ml.x - mx) : 0.f;
+      float l = w * ml.y;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+      float acc[DPL];
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
+#pragma unroll
+      for (int k = 0; k < kMaxCluster; ++k) {
+        if (k < C) {
+          const float wk = __shfl_sync(0xffffffffu, w, k);
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) acc[d] = fmaf(wk, v[k][d], acc[d]);
+        }
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int qi = r / group, h = g * group + r % group;
+      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) +
+                           (((size_t)b * L + qi) * p.hq + h) * D + lane * DPL;
+      if constexpr (DPL == 4) {
+        *reinterpret_cast<uint2 *>(out) =
+            make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv));
+      } else {
+        *reinterpret_cast<uint32_t *>(out) = pack_bf16(acc[0] * inv, acc[1] * inv);
+      }
+    }
+  }
+  cluster_sync();                              // no CTA leaves while its piece is being read
+}
+
+// TMA maps of one call: the pool as [page][Hkv][64][D] and the block's keys
+// as [B][L'][Hkv][D], each read in [64 keys][64 columns] boxes.
+template <int D>
+bool encode_maps(const AttnParams &p, CUtensorMap &mkp, CUtensorMap &mvp, CUtensorMap &mkb,
+                 CUtensorMap &mvb) {
   const uint64_t eb = 2;
-  CUtensorMap mkp, mvp, mkb, mvb;
   const uint64_t pdims[4] = {(uint64_t)D, (uint64_t)p.page_size, (uint64_t)p.hkv,
                              (uint64_t)p.num_pages};
   const uint64_t pstr[3] = {D * eb, (uint64_t)p.page_size * D * eb,
@@ -633,7 +967,18 @@ bd_status launch(const AttnParams &p, cudaStream_t st) {
       !tma_encode_bf16(&mvp, 4, p.v_pool, pdims, pstr, pbox) ||
       !tma_encode_bf16(&mkb, 4, p.k_blk, bdims, bstr, bbox) ||
       !tma_encode_bf16(&mvb, 4, p.v_blk, bdims, bstr, bbox))
-    return BD_ERR_CUDA;
+    return false;
+  return true;
+}
+
+template <int D, int RG, int KH>
+bd_status launch(const AttnParams &p, cudaStream_t st) {
+  constexpr int NW = RG * KH;
+  constexpr size_t kXchgBytes = KH == 2 ? (size_t)RG * (4 * (D / 8) + 4) * 32 * 4 : 0;
+  constexpr int NH = D / 64;
+  constexpr int TILE = NH * kHalfBytes;
+  CUtensorMap mkp, mvp, mkb, mvb;
+  if (!encode_maps<D>(p, mkp, mvp, mkb, mvb)) return BD_ERR_CUDA;
   const size_t ctrl = kMaxStages * (2 * sizeof(uint64_t) + sizeof(TileMeta)) + 16;
   const int S = (int)std::min<size_t>(kMaxStages,
                                       (200 * 1024 - ctrl - kXchgBytes) / (2 * TILE));
@@ -651,6 +996,85 @@ bd_status launch(const AttnParams &p, cudaStream_t st) {
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
 
+
+// Shared memory of attn_cluster_kernel: S stages of K and V, the control
+// block, and the alignment slack; the stages must also hold the piece and the
+// key-half exchange at the end.
+template <int D, int RG, int KH>
+bool cluster_layout(int R, int *S_out, size_t *smem_out) {
+  constexpr int TILE = (D / 64) * kHalfBytes;
+  constexpr size_t kXchgBytes = KH == 2 ? (size_t)RG * (4 * (D / 8) + 4) * 32 * 4 : 0;
+  constexpr size_t kOptin = 227 * 1024;
+  const size_t ctrl = kMaxStages * (2 * sizeof(uint64_t) + sizeof(TileMeta)) + 16;
+  const int S = (int)std::min<size_t>(kMaxStages, (kOptin - 1024 - ctrl) / (2 * TILE));
+  const size_t piece = (size_t)R * D * 4 + (size_t)R * 2 * 4 + kXchgBytes;
+  if (S < 2 || piece > (size_t)S * 2 * TILE) return false;
+  *S_out = S;
+  *smem_out = (size_t)S * 2 * TILE + ctrl + 1024;
+  return true;
+}
+
+// Clusters of C CTAs of attn_cluster_kernel that the device holds at once
+// (cached per device and C; 0 when the size cannot be launched).
+template <int D, int RG, int KH>
+int active_clusters(int C, size_t smem) {
+  static std::atomic<int> cache[64][kMaxCluster + 1];
+  static std::atomic<bool> init{false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (!init.exchange(true))
+    for (auto &row : cache)
+      for (auto &c : row) c.store(-1);
+  const int hit = cache[dev][C].load();
+  if (hit >= 0) return hit;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C);
+  cfg.blockDim = dim3((RG * KH + 1) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<D, RG, KH>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[dev][C].store(n);
+  return n;
+}
+
+// One cluster per segment; C as large as the SMs allow (each CTA then streams
+// a few pages), reduced until all clusters of the call fit on the device at once.
+template <int D, int RG, int KH>
+bd_status launch_cluster(const AttnParams &p, cudaStream_t st) {
+  constexpr int NW = RG * KH;
+  const int R = p.block_len * (p.hq / p.hkv);
+  int S;
+  size_t smem;
+  if (!cluster_layout<D, RG, KH>(R, &S, &smem)) return BD_ERR_UNSUPPORTED;
+  const long long segs = (long long)p.batch * p.hkv;
+  if (segs > (1LL << 24)) return BD_ERR_UNSUPPORTED;
+  const int sms = std::max(1, dev_info().sms);
+  const int Tm = (p.max_ctx + kPageRows - 1) / kPageRows + 1;
+  int C = (int)std::min<long long>(std::min(kMaxCluster, Tm), std::max(1LL, sms / segs));
+  while (C > 1 && active_clusters<D, RG, KH>(C, smem) < std::min<long long>(segs, sms / C)) --C;
+  if (active_clusters<D, RG, KH>(C, smem) < 1) return BD_ERR_UNSUPPORTED;
+  CUtensorMap mkp, mvp, mkb, mvb;
+  if (!encode_maps<D>(p, mkp, mvp, mkb, mvb)) return BD_ERR_CUDA;
+  const cudaError_t e =
+      launch_pdl_cluster(attn_cluster_kernel<D, RG, KH>, dim3((unsigned)(segs * C)),
+                         dim3((NW + 1) * 32), smem, st, dim3(C, 1, 1), mkp, mvp, mkb, mvb, p, S,
+                         C, Tm);
+  count_launches(1);
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
 }  // namespace
 
 cudaError_t attention_plan_launch(const AttnParams &p, cudaStream_t st) {
@@ -659,24 +1083,47 @@ cudaError_t attention_plan_launch(const AttnParams &p, cudaStream_t st) {
   return e;
 }
 
+// The cluster kernel may run clusters of up to 16 CTAs (beyond the portable 8).
+template <int D, int RG, int KH>
+static bool preload_cluster() {
+  auto k = attn_cluster_kernel<D, RG, KH>;
+  return preload_kernel(k, true) &&
+         cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+}
+
 bool preload_attention_tc() {
-  return preload_kernel(attn_plan_kernel, false) && preload_kernel(attn_tc_kernel<64, 4, 2>, true) &&
+  return preload_cluster<64, 4, 2>() && preload_cluster<64, 8, 1>() &&
+         preload_cluster<128, 4, 2>() && preload_cluster<128, 8, 1>() &&
+         preload_kernel(attn_plan_kernel, false) && preload_kernel(attn_tc_kernel<64, 4, 2>, true) &&
          preload_kernel(attn_tc_kernel<64, 8, 1>, true) &&
          preload_kernel(attn_tc_kernel<128, 4, 2>, true) &&
          preload_kernel(attn_tc_kernel<128, 8, 1>, true);
 }
 
+// Shapes both bf16 tensor-core kernels take.
+static bool tc_shape_ok(const AttnParams &p) {
+  if (p.dtype != BD_BF16 || (p.head_dim != 64 && p.head_dim != 128)) return false;
+  if (p.page_size != kPageRows || p.block_len > 32) return false;
+  if (p.block_len * (p.hq / p.hkv) > 128) return false;
+  if ((reinterpret_cast<uintptr_t>(p.q) & 3) != 0) return false;
+  const DevInfo d = dev_info();
+  return d.major >= 10 && tma_available();
+}
+
+bd_status attention_cluster(const AttnParams &p, cudaStream_t st) {
+  if (!tc_shape_ok(p) || (reinterpret_cast<uintptr_t>(p.out) & 7) != 0) return BD_ERR_UNSUPPORTED;
+  const int R = p.block_len * (p.hq / p.hkv);
+  if (p.head_dim == 64)
+    return R <= 64 ? launch_cluster<64, 4, 2>(p, st) : launch_cluster<64, 8, 1>(p, st);
+  return R <= 64 ? launch_cluster<128, 4, 2>(p, st) : launch_cluster<128, 8, 1>(p, st);
+}
+
 bd_status attention_tc(const AttnParams &p, cudaStream_t st) {
-  if (p.dtype != BD_BF16 || (p.head_dim != 64 && p.head_dim != 128)) return BD_ERR_UNSUPPORTED;
-  if (p.page_size != kPageRows || p.block_len > 32) return BD_ERR_UNSUPPORTED;
-  if (p.block_len * (p.hq / p.hkv) > 128) return BD_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(p.q) & 3) != 0) return BD_ERR_UNSUPPORTED;
+  if (!tc_shape_ok(p)) return BD_ERR_UNSUPPORTED;
   if (p.grid < 1 || ((p.plan || p.num_splits > 1) && (!p.sk_o || !p.sk_ml)))
     return BD_ERR_UNSUPPORTED;
   if (p.plan && (long long)p.batch * p.hkv * (p.max_pages + 1) >= (1LL << 30))
     return BD_ERR_UNSUPPORTED;
-  const DevInfo d = dev_info();
-  if (d.major < 10 || !tma_available()) return BD_ERR_UNSUPPORTED;
   const int R = p.block_len * (p.hq / p.hkv);
   bd_status s;
   // up to 64 rows: 4 row groups x 2 key halves; up to 128 rows: 8 row groups

@@ -203,6 +203,26 @@ __device__ __forceinline__ uint32_t map_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
+// Loads from another CTA's shared memory (an address from map_shared).  The
+// caller orders them after the writer's stores with a cluster barrier.
+__device__ __forceinline__ float2 ld_cluster_f2(uint32_t cluster_addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+               : "=f"(v.x), "=f"(v.y)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
 // Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)

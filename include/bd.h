@@ -460,8 +460,10 @@ uint64_t bd_kernel_launches(void);
 typedef enum {
   BD_ATTN_AUTO = 0,      /* by shape                                        */
   BD_ATTN_PAIR = 1,      /* tcgen05 head-pair kernel, also on small problems */
-  BD_ATTN_MMA = 2,       /* mma.sync kernel (bf16)                          */
-  BD_ATTN_SIMT = 3       /* SIMT kernel                                     */
+  BD_ATTN_MMA = 2,       /* mma.sync kernel (bf16), tile ranges or splits   */
+  BD_ATTN_SIMT = 3,      /* SIMT kernel                                     */
+  BD_ATTN_CLUSTER = 4    /* cluster-per-segment kernel (bf16), also on      *
+                          * large problems                                  */
 } bd_attention_kernel;
 
 bd_status bd_debug_force_attention_kernel(int32_t which);

@@ -1,13 +1,17 @@
 """Each attention kernel of the library against the oracle on the same cases.
 
-bd_block_attention runs the tcgen05 head-pair kernel for large bf16 problems
-at the SDAR shapes, the mma.sync kernel for the other bf16 cases and the SIMT
-kernel for fp32, chosen by shape alone.  The library's test hook
-bd_debug_force_attention_kernel forces one kernel so that each is checked on
-small, ragged and full-size inputs (a kernel that does not support a shape
-falls back to the one the shape picks).  "pair" runs the head-pair kernel
-on every problem: on small ones its tile ranges give more CTAs than tiles and
-many pieces per segment, all merged inside the launch.
+bd_block_attention runs, for bf16, the cluster-per-segment kernel on small
+problems and the tcgen05 head-pair kernel (SDAR shapes) or the mma.sync kernel
+(other shapes) on large ones; the SIMT kernel for fp32.  The choice is by shape
+alone.  The library's test hook bd_debug_force_attention_kernel forces one
+kernel so that each is checked on small, ragged and full-size inputs (a kernel
+that does not support a shape falls back to the one the shape picks).
+- "pair" runs the head-pair kernel on every problem.  On small ones its tile
+  ranges give more CTAs than tiles and many pieces per segment, all merged
+  inside the launch.
+- "cluster" runs the cluster kernel on every problem.  On sdar_b1 it runs 16-CTA
+  clusters.  On serving_b64 it runs one CTA per segment, with up to 193 tiles,
+  so its page ids arrive in several 32-tile chunks.
 """
 import numpy as np
 import pytest
@@ -33,7 +37,7 @@ def _lib():
     bd.load()
 
 
-@pytest.fixture(params=["auto", "pair", "mma", "simt"])
+@pytest.fixture(params=["auto", "pair", "mma", "simt", "cluster"])
 def impl(request):
     bd.bd_debug_force_attention_kernel(request.param)
     yield request.param
@@ -78,5 +82,20 @@ def test_serving_shapes_sampled(impl):
     q, kb, vb = wl.block_qkv(w, 0)
     got = gpu_attention(s, q, kb, vb)
     for b in (0, 31, 63):
+        err = float(np.abs(got[b] - oracle_attention(s, b, q, kb, vb)).max())
+        assert err <= 2e-2, f"{impl}: sequence {b} max-abs error {err}"
+
+
+def test_sequence_without_mask_is_skipped(impl):
+    # sequence 1 has no masked position: its output rows stay untouched
+    w = SMALL
+    s = make_cache(w, 0, [300, 140, 65])
+    q, kb, vb = wl.block_qkv(w, 0)
+    tokens = np.full((w.batch, w.block_len), bd.BD_MASK, dtype=np.int32)
+    tokens[1] = 7
+    tokens[2, ::2] = 11                            # half committed: still attended
+    got = gpu_attention(s, q, kb, vb, tokens=torch.from_numpy(tokens).cuda())
+    assert np.isnan(got[1]).all()
+    for b in (0, 2):
         err = float(np.abs(got[b] - oracle_attention(s, b, q, kb, vb)).max())
         assert err <= 2e-2, f"{impl}: sequence {b} max-abs error {err}"
