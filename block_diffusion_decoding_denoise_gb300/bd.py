@@ -39,7 +39,7 @@ EXPORTS = ("bd_block_attention_workspace", "bd_block_attention",
            "bd_merge_attention_partials")
 
 # bd_attention_kernel values of bd_debug_force_attention_kernel (test hook)
-BD_ATTN = {"auto": 0, "pair": 1, "mma": 2, "simt": 3, "cluster": 4}
+BD_ATTN = {"auto": 0, "pair": 1, "mma": 2, "simt": 3, "cluster": 4, "pair_cluster": 5}
 
 
 class BDError(RuntimeError):

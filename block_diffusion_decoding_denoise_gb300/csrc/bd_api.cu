@@ -239,12 +239,13 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
   p.dev_status = dev_status;
   p.grid = num_sms();
   p.seg_heads = 1;
-  // Kernel choice, by shape: for bf16, the cluster-per-segment kernel on
-  // small problems (a few pages per SM in all: one launch, pieces merged in
-  // distributed shared memory); on large ones the tcgen05 head-pair kernel at
-  // head_dim 128 and 64 query rows per KV head (the SDAR shapes) and the
-  // mma.sync kernel for other shapes; SIMT for fp32.  A test may force one
-  // kernel with bd_debug_force_attention_kernel.
+  // Kernel choice, by shape, for bf16: the tcgen05 head-pair kernel at
+  // head_dim 128 and 64 query rows per KV head (the SDAR shapes), the
+  // mma.sync kernel for other shapes; each in its cluster form on small
+  // problems (a few pages per SM in all: one cluster of CTAs per segment, one
+  // launch, pieces merged through L2) and in its tile-range
+  // form on large ones.  SIMT for fp32.  A test may force one kernel with
+  // bd_debug_force_attention_kernel.
   const int forced = g_forced_attention.load(std::memory_order_relaxed);
   const bool small = attn_small(batch, p.hkv, block_len, max_ctx);
   size_t fs_o, fs_ml, off_plan, sk_o, sk_ml;
@@ -259,15 +260,20 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
   p.part_o = reinterpret_cast<float *>(w + fs_o);
   p.part_ml = reinterpret_cast<float *>(w + fs_ml);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // tile-range partials of the mma.sync and head-pair kernels; the cluster
+  // forms keep one piece slot per CTA there
+  p.sk_o = reinterpret_cast<float *>(w + sk_o);
+  p.sk_ml = reinterpret_cast<float *>(w + sk_ml);
+  if (forced == BD_ATTN_PAIR_CLUSTER || (forced == BD_ATTN_AUTO && small)) {
+    const bd_status s = attention_pair_cluster(p, st);
+    if (s != BD_ERR_UNSUPPORTED) return s;
+  }
   if (forced == BD_ATTN_CLUSTER || (forced == BD_ATTN_AUTO && small)) {
     const bd_status s = attention_cluster(p, st);
     if (s != BD_ERR_UNSUPPORTED) return s;
   }
   if (forced == BD_ATTN_PAIR || (forced == BD_ATTN_AUTO && !small)) {
-    AttnParams pp = p;
-    pp.sk_o = reinterpret_cast<float *>(w + sk_o);
-    pp.sk_ml = reinterpret_cast<float *>(w + sk_ml);
-    if (attention_pair_supported(pp)) return attention_pair(pp, st);
+    if (attention_pair_supported(p)) return attention_pair(p, st);
   }
   if (small) {
     // fixed splits: the kernel writes its partials where the split combine reads them
@@ -276,8 +282,6 @@ BD_API bd_status bd_block_attention(const bd_paged_kv *kv, const int32_t *ctx_le
     p.sk_ml = p.part_ml;
   } else {
     p.plan = reinterpret_cast<int *>(w + off_plan);
-    p.sk_o = reinterpret_cast<float *>(w + sk_o);
-    p.sk_ml = reinterpret_cast<float *>(w + sk_ml);
   }
   if (forced != BD_ATTN_SIMT) {
     const bd_status s = attention_tc(p, st);
@@ -320,7 +324,7 @@ BD_API const char *bd_status_string(bd_status s) {
 BD_API int32_t bd_version(void) { return 200; }
 
 BD_API bd_status bd_debug_force_attention_kernel(int32_t which) {
-  if (which < BD_ATTN_AUTO || which > BD_ATTN_CLUSTER) return BD_ERR_INVALID_ARG;
+  if (which < BD_ATTN_AUTO || which > BD_ATTN_PAIR_CLUSTER) return BD_ERR_INVALID_ARG;
   g_forced_attention.store(which, std::memory_order_relaxed);
   return BD_OK;
 }

@@ -46,6 +46,8 @@ bd_status attention_combine(const AttnParams &p, cudaStream_t st);
 bd_status attention_combine_sk(const AttnParams &p, cudaStream_t st);
 bool attention_pair_supported(const AttnParams &p);
 bd_status attention_pair(const AttnParams &p, cudaStream_t st);
+bool attention_pair_cluster_supported(const AttnParams &p);
+bd_status attention_pair_cluster(const AttnParams &p, cudaStream_t st);
 cudaError_t attention_plan_launch(const AttnParams &p, cudaStream_t st);
 
 }  // namespace bd

@@ -44,6 +44,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "bd_attention.cuh"
 #include "bd_common.cuh"
@@ -68,6 +69,10 @@ constexpr uint32_t kColP = 384;             // P buffer b at kColP + 64 b: 128 k
 constexpr float kLazy = 8.f;                // max moves only beyond 2^8
 constexpr int kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8;
 constexpr int kJobInts = 8;                 // merge job: seg (-1: none), c1, b, hp, T
+constexpr int kMaxCluster = 16;             // cluster form: CTAs per segment
+constexpr int kPieceStride = D + 4;         // cluster form: floats per piece row in shared
+                                            // memory (a thread writing its own row has no
+                                            // bank conflicts)
 
 struct Meta {
   int item, lo, hi, flags, slot;
@@ -85,6 +90,8 @@ struct Smem {
   uint64_t mma_done;
   uint32_t tmem_base;
   volatile int abort_flag;
+  int pid[32];                              // cluster form: page ids of the first 32 tiles
+  volatile int active;                      // cluster form: the segment has output to write
 };
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, int32_t c0,
@@ -155,12 +162,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+template <bool kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap mk_pool,
                      const __grid_constant__ CUtensorMap mv_pool,
                      const __grid_constant__ CUtensorMap mk_blk,
                      const __grid_constant__ CUtensorMap mv_blk,
-                     const __grid_constant__ CUtensorMap mq, const AttnParams p) {
+                     const __grid_constant__ CUtensorMap mq, const AttnParams p, int C, int Tm) {
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -217,6 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.abort_flag = 1;
     flag_error(p.dev_status, BD_ERR_TIMEOUT);
   };
+  // cluster form: this CTA's piece (a softmax thread's row keeps its O in TMEM)
+  bool have_piece = false;
+  float piece_m2 = -INFINITY, piece_l = 0.f;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -236,19 +247,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return active ? (ctx + kPage - 1) / kPage + 1 : 0;
     };
+    const int c = blockIdx.x, G = gridDim.x;
+    int T = 0, t_begin = 0, t_end = 0, b_first = -1, base_first = 0, tiles_first = 0;
+    // cluster form: segment (b, hp) of this cluster, this CTA's tiles
+    // [cu0, clast) of it, and the page ids of the first 32 of them in sm.pid
+    int cb = 0, chp = 0, cctx = 0, cnpg = 0, cu0 = 0, clast = 0;
+    if constexpr (kCluster) {
+      const int rank = (int)cluster_ctarank();
+      const int seg = blockIdx.x / C;
+      cb = seg / npairs;
+      chp = seg % npairs;
+      cu0 = (int)((long long)rank * Tm / C);
+      const int cu1 = (int)((long long)(rank + 1) * Tm / C);
+      // one memory latency: the block's tokens, ctx and the range's page ids
+      const int32_t *tk = p.tokens ? p.tokens + (size_t)cb * L : nullptr;
+      const int32_t *prow = p.page_table + (size_t)cb * p.max_pages;
+      const int tv = (tk && lane < L) ? tk[lane] : 0;
+      cctx = p.ctx_len[cb];
+      const int pid = (cu0 + lane < cu1 && cu0 + lane < p.max_pages) ? prow[cu0 + lane] : -1;
+      const bool has = !tk || __any_sync(0xffffffffu, lane < L && tv == BD_MASK);
+      const bool ctx_ok = cctx >= 0 && cctx <= p.max_ctx && cctx <= p.max_pages * p.page_size;
+      if (has && !ctx_ok && rank == 0 && chp == 0 && lane == 0)
+        flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
+      const bool active = has && ctx_ok;
+      cnpg = active ? (cctx + kPage - 1) / kPage : 0;
+      clast = active ? min(cu1, cnpg + 1) : cu0;
+      sm.pid[lane] = pid;
+      if (lane == 0) sm.active = active ? 1 : 0;
+      __syncwarp();
+    }
     // the plan: T = all tiles; this CTA's range [t_begin, t_end) and the
     // sequence holding t_begin (warp-wide passes over the sequences)
-    const int c = blockIdx.x, G = gridDim.x;
-    int T = 0;
+    if constexpr (!kCluster) {
     for (int b0 = 0; b0 < p.batch; b0 += 32) {
       int v = (b0 + lane < p.batch) ? npairs * seq_tiles(b0 + lane) : 0;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       T += v;
     }
-    const int t_begin = (int)(((long long)c * T) / G);
-    const int t_end = (int)(((long long)(c + 1) * T) / G);
-    int b_first = -1, base_first = 0, tiles_first = 0;
+    t_begin = (int)(((long long)c * T) / G);
+    t_end = (int)(((long long)(c + 1) * T) / G);
     if (t_begin < t_end) {
       int carry = 0;
       for (int b0 = 0; b0 < p.batch && b_first < 0; b0 += 32) {
@@ -272,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         carry += __shfl_sync(0xffffffffu, inc, 31);
       }
+    }
     }
     uint32_t it = 0, pc = 0;
     bool stop = false;
@@ -298,7 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = u_first; u < u_last; ++u, ++it) {
           const uint32_t s = it % kStages, round = it / kStages;
           // the page id is read before the wait, so the wait covers its latency
-          const int pg = u < npg ? prow[u] : -1;
+          // (cluster form: the first 32 were loaded together up front)
+          const int pg =
+              u < npg ? ((kCluster && u - cu0 < 32) ? sm.pid[u - cu0] : prow[u]) : -1;
           if (sm.abort_flag) return false;
           if (round > 0 && !mbar_wait(smem_u32(&sm.kv_empty[s]), (round - 1) & 1)) {
             fail();
@@ -347,6 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
+      if constexpr (kCluster) {
+        if (cu0 < clast)
+          stop = !emit(cb, chp, cctx, cnpg, cu0, clast, 0, L, cb * npairs + chp, -1);
+      } else {
       int job[4] = {-1, 0, 0, 0};
       if (b_first >= 0) {
         int b = b_first, base = base_first, tiles = tiles_first;
@@ -382,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         jd[2] = job[2];
         jd[3] = job[3];
         jd[4] = T;
+      }
       }
       if (!stop) {                             // sentinel stage: no more work
         const uint32_t s = it % kStages, round = it / kStages;
@@ -549,10 +595,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.s_empty[s]));
       const int lo = m.lo, hi = (m.flags & kSkip) ? 0 : m.hi;
-      float mt = -INFINITY;
+      const bool none = hi <= lo;              // no valid key in the tile: P = 0
+      if (lo > 0 || hi < 64) {                 // partial tile: masked keys score -inf
 #pragma unroll
-      for (int j = 0; j < 64; ++j)
-        if (j >= lo && j < hi) mt = fmaxf(mt, sc[j]);
+        for (int j = 0; j < 64; ++j)
+          if (j < lo || j >= hi) sc[j] = -INFINITY;
+      }
+      float mt4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four short chains
+#pragma unroll
+      for (int j = 0; j < 64; ++j) mt4[j & 3] = fmaxf(mt4[j & 3], sc[j]);
+      const float mt = fmaxf(fmaxf(mt4[0], mt4[1]), fmaxf(mt4[2], mt4[3]));
       float factor = 1.f;
       if (mt > m2) {
         if (m2 == -INFINITY) {
@@ -565,17 +617,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // P row as bf16 pairs (its own head's 64 keys = 32 TMEM columns)
       uint32_t pw[32];
-      {
-        float sum = 0.f;
+      if (none) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pw[e] = 0u;
+      } else {                                 // exp2(-inf - m2) = 0 for the masked keys
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int j0 = 2 * e, j1 = j0 + 1;
-          const float p0 = (j0 >= lo && j0 < hi) ? fast_exp2(sc[j0] - m2) : 0.f;
-          const float p1 = (j1 >= lo && j1 < hi) ? fast_exp2(sc[j1] - m2) : 0.f;
-          sum += p0 + p1;
+          const float p0 = fast_exp2(sc[2 * e] - m2);
+          const float p1 = fast_exp2(sc[2 * e + 1] - m2);
+          sum4[e & 3] += p0 + p1;
           pw[e] = pack_bf16(p0, p1);
         }
-        l += sum;
+        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       }
       // MMA2 of the previous tile has to be complete before O is rescaled and
       // before this tile's P overwrites the buffer MMA2 of tile t - 2 read
@@ -618,6 +672,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         o_seen = t + 1;
         tc_fence_after();
+        if (kCluster && C > 1) {               // O stays in TMEM for the cluster merge
+          have_piece = true;
+          piece_m2 = m2;
+          piece_l = l;
+        } else {
         const int b = m.item / npairs, hp = m.item % npairs;
         const int g = 2 * hp + hs;
         const int qi = rr / group, h = g * group + rr % group;
@@ -653,6 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.sk_ml[prow * 2 + 0] = m2 * 0.6931471805599453f;   // natural-log units
           p.sk_ml[prow * 2 + 1] = l;
         }
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm.o_empty));
@@ -663,6 +723,104 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (kCluster && C > 1) {
+    // Every CTA publishes its piece in its own slot of the workspace: O
+    // [128][D] fp32 at sk_o and (m in base-2 units, l) [128][2] at sk_ml (a
+    // CTA without tiles publishes m = -inf, l = 0 and O = 0).  The softmax
+    // threads stage their rows in the K stages (free now: every copy has
+    // landed and every MMA has completed), and all threads copy the piece out
+    // in coalesced 16-byte stores.  After a cluster barrier (release/acquire
+    // at cluster scope) CTA rank r merges rows [r 128 / C, (r + 1) 128 / C) of
+    // the C pieces from L2, one item (row, 8 columns) per thread with every
+    // load of the item issued before any is used.
+    float *c_o = reinterpret_cast<float *>(&sm.k[0][0][0]);
+    float *c_ml = c_o + kRows * kPieceStride;
+    if (warp >= 2) {
+      const int row = 32 * (warp & 3) + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+      float4 *dst = reinterpret_cast<float4 *>(c_o + row * kPieceStride);
+      if (__any_sync(0xffffffffu, have_piece)) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(lane_base + kColO + c * 16, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[4 * c + e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                                         __uint_as_float(r[4 * e + 2]),
+                                         __uint_as_float(r[4 * e + 3]));
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < D / 4; ++e) dst[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      *reinterpret_cast<float2 *>(c_ml + 2 * row) =
+          have_piece ? make_float2(piece_m2, piece_l) : make_float2(-INFINITY, 0.f);
+    }
+    __syncthreads();
+    {
+      float4 *go = reinterpret_cast<float4 *>(p.sk_o + (size_t)blockIdx.x * kRows * D);
+      for (int i = threadIdx.x; i < kRows * D / 4; i += kThreads)
+        go[i] = *reinterpret_cast<const float4 *>(c_o + (i / (D / 4)) * kPieceStride +
+                                                  4 * (i % (D / 4)));
+      float2 *gml = reinterpret_cast<float2 *>(p.sk_ml + (size_t)blockIdx.x * kRows * 2);
+      for (int i = threadIdx.x; i < kRows; i += kThreads)
+        gml[i] = *reinterpret_cast<const float2 *>(c_ml + 2 * i);
+    }
+    cluster_sync();                            // every piece of the cluster is published
+    if (sm.active) {
+      const int rank = (int)cluster_ctarank();
+      const int seg = blockIdx.x / C, b = seg / npairs, hp = seg % npairs;
+      const size_t first = (size_t)blockIdx.x - rank;   // CTA of rank 0
+      const int r_begin = rank * kRows / C, r_end = (rank + 1) * kRows / C;
+      for (int item = threadIdx.x; item < (r_end - r_begin) * (D / 8); item += kThreads) {
+        const int r = r_begin + item / (D / 8), q = item % (D / 8);
+        float2 ml[kMaxCluster];
+        float4 va[kMaxCluster], vb[kMaxCluster];
+#pragma unroll
+        for (int k = 0; k < kMaxCluster; ++k) {
+          if (k < C) {
+            const size_t prow = (first + k) * kRows + r;
+            ml[k] = __ldcg(reinterpret_cast<const float2 *>(p.sk_ml + prow * 2));
+            const float4 *src = reinterpret_cast<const float4 *>(p.sk_o + prow * D + 8 * q);
+            va[k] = __ldcg(src);
+            vb[k] = __ldcg(src + 1);
+          }
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kMaxCluster; ++k)
+          if (k < C) mx = fmaxf(mx, ml[k].x);
+        float lsum = 0.f;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < kMaxCluster; ++k) {
+          if (k < C && ml[k].x != -INFINITY) {
+            const float w = exp2f(ml[k].x - mx);
+            lsum = fmaf(w, ml[k].y, lsum);
+            acc[0] = fmaf(w, va[k].x, acc[0]);
+            acc[1] = fmaf(w, va[k].y, acc[1]);
+            acc[2] = fmaf(w, va[k].z, acc[2]);
+            acc[3] = fmaf(w, va[k].w, acc[3]);
+            acc[4] = fmaf(w, vb[k].x, acc[4]);
+            acc[5] = fmaf(w, vb[k].y, acc[5]);
+            acc[6] = fmaf(w, vb[k].z, acc[6]);
+            acc[7] = fmaf(w, vb[k].w, acc[7]);
+          }
+        }
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const int g = 2 * hp + (r >> 6), rr = r & 63;
+        const int qi = rr / group, h = g * group + rr % group;
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) +
+                             (((size_t)b * L + qi) * p.hq + h) * D + 8 * q;
+        *reinterpret_cast<uint4 *>(out) =
+            make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                       pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+      }
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -794,26 +952,36 @@ __global__ void __launch_bounds__(kMergeThreads) attn_pair_merge_kernel(const At
 }  // namespace
 
 bool preload_attention_pair() {
-  return preload_kernel(attn_pair_kernel, true) && preload_kernel(attn_pair_merge_kernel, false);
+  return preload_kernel(attn_pair_kernel<false>, true) &&
+         preload_kernel(attn_pair_kernel<true>, true) &&
+         cudaFuncSetAttribute(attn_pair_kernel<true>,
+                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+         preload_kernel(attn_pair_merge_kernel, false);
 }
 
-bool attention_pair_supported(const AttnParams &p) {
+// Shapes the head-pair kernel takes (both forms).
+static bool pair_shape_ok(const AttnParams &p) {
   if (p.dtype != BD_BF16 || p.head_dim != D || p.page_size != kPage) return false;
   if (p.hkv % 2 != 0 || p.hq % p.hkv != 0) return false;
   if (p.block_len * (p.hq / p.hkv) != 64) return false;
-  if (p.grid < 1 || p.grid > kMergeMaxPieces || !p.sk_o || !p.sk_ml || !p.jobs) return false;
-  if ((long long)p.batch * (p.hkv / 2) * (p.max_pages + 1) >= (1LL << 30)) return false;
+  if ((reinterpret_cast<uintptr_t>(p.out) & 7) != 0) return false;
   const DevInfo d = dev_info();
   return d.major >= 10 && tma_available();
 }
 
-bd_status attention_pair(const AttnParams &p0, cudaStream_t st) {
-  if (!attention_pair_supported(p0)) return BD_ERR_UNSUPPORTED;
-  AttnParams p = p0;
-  p.seg_heads = 2;
+bool attention_pair_supported(const AttnParams &p) {
+  if (!pair_shape_ok(p)) return false;
+  if (p.grid < 1 || p.grid > kMergeMaxPieces || !p.sk_o || !p.sk_ml || !p.jobs) return false;
+  return (long long)p.batch * (p.hkv / 2) * (p.max_pages + 1) < (1LL << 30);
+}
+
+// TMA maps of one call: the pool as [page][Hkv][64][D], the block's keys as
+// [B][L'][Hkv][D] (both in [64 keys][64 d] boxes) and Q as [B][L'][Hq][D]
+// (boxes of the group's query heads for all L' positions).
+static bool pair_maps(const AttnParams &p, CUtensorMap &mkp, CUtensorMap &mvp, CUtensorMap &mkb,
+                      CUtensorMap &mvb, CUtensorMap &mq) {
   const uint64_t eb = 2;
   const int group = p.hq / p.hkv;
-  CUtensorMap mkp, mvp, mkb, mvb, mq;
   const uint64_t pdims[4] = {(uint64_t)D, (uint64_t)p.page_size, (uint64_t)p.hkv,
                              (uint64_t)p.num_pages};
   const uint64_t pstr[3] = {D * eb, (uint64_t)p.page_size * D * eb,
@@ -829,18 +997,89 @@ bd_status attention_pair(const AttnParams &p0, cudaStream_t st) {
   const uint64_t qstr[3] = {D * eb, (uint64_t)p.hq * D * eb,
                             (uint64_t)p.block_len * p.hq * D * eb};
   const uint32_t qbox[4] = {64, (uint32_t)group, (uint32_t)p.block_len, 1};
-  if (!tma_encode_bf16(&mkp, 4, p.k_pool, pdims, pstr, pbox) ||
-      !tma_encode_bf16(&mvp, 4, p.v_pool, pdims, pstr, pbox) ||
-      !tma_encode_bf16(&mkb, 4, p.k_blk, bdims, bstr, bbox) ||
-      !tma_encode_bf16(&mvb, 4, p.v_blk, bdims, bstr, bbox) ||
-      !tma_encode_bf16(&mq, 4, p.q, qdims, qstr, qbox))
-    return BD_ERR_CUDA;
+  return tma_encode_bf16(&mkp, 4, p.k_pool, pdims, pstr, pbox) &&
+         tma_encode_bf16(&mvp, 4, p.v_pool, pdims, pstr, pbox) &&
+         tma_encode_bf16(&mkb, 4, p.k_blk, bdims, bstr, bbox) &&
+         tma_encode_bf16(&mvb, 4, p.v_blk, bdims, bstr, bbox) &&
+         tma_encode_bf16(&mq, 4, p.q, qdims, qstr, qbox);
+}
+
+bd_status attention_pair(const AttnParams &p0, cudaStream_t st) {
+  if (!attention_pair_supported(p0)) return BD_ERR_UNSUPPORTED;
+  AttnParams p = p0;
+  p.seg_heads = 2;
+  CUtensorMap mkp, mvp, mkb, mvb, mq;
+  if (!pair_maps(p, mkp, mvp, mkb, mvb, mq)) return BD_ERR_CUDA;
   const size_t smem = sizeof(Smem) + 1024;
-  cudaError_t e = launch_pdl(attn_pair_kernel, dim3(p.grid), dim3(kThreads), smem, st, mkp, mvp,
-                             mkb, mvb, mq, p);
+  cudaError_t e = launch_pdl(attn_pair_kernel<false>, dim3(p.grid), dim3(kThreads), smem, st, mkp,
+                             mvp, mkb, mvb, mq, p, 1, 0);
   count_launches(1);
   if (e != cudaSuccess) return BD_ERR_CUDA;
   e = launch_pdl(attn_pair_merge_kernel, dim3(2 * p.grid), dim3(kMergeThreads), 0, st, p);
+  count_launches(1);
+  return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+}
+
+// Clusters of C CTAs of the cluster form that the device holds at once
+// (cached per device and C; 0 when that size cannot be launched).
+static int pair_active_clusters(int C, size_t smem) {
+  static std::atomic<int> cache[64][kMaxCluster + 1];
+  static std::atomic<bool> init{false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (!init.exchange(true))
+    for (auto &row : cache)
+      for (auto &c : row) c.store(-1);
+  const int hit = cache[dev][C].load();
+  if (hit >= 0) return hit;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_pair_kernel<true>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[dev][C].store(n);
+  return n;
+}
+
+bool attention_pair_cluster_supported(const AttnParams &p) {
+  return pair_shape_ok(p) && (long long)p.batch * (p.hkv / 2) <= (1LL << 24) && p.sk_o &&
+         p.sk_ml && p.grid >= 1;
+}
+
+// Cluster form: one cluster of C CTAs per (sequence, KV-head pair) segment,
+// C as large as the SMs allow, reduced until all clusters fit at once.
+bd_status attention_pair_cluster(const AttnParams &p0, cudaStream_t st) {
+  if (!attention_pair_cluster_supported(p0)) return BD_ERR_UNSUPPORTED;
+  AttnParams p = p0;
+  p.seg_heads = 2;
+  const size_t smem = sizeof(Smem) + 1024;
+  const long long segs = (long long)p.batch * (p.hkv / 2);
+  const int sms = std::max(1, dev_info().sms);
+  const int Tm = (p.max_ctx + kPage - 1) / kPage + 1;
+  // pieces (C > 1) take one 128-row slot of sk_o / sk_ml per CTA: segs * C <= grid
+  int C = (int)std::min<long long>(std::min(kMaxCluster, Tm),
+                                   std::max(1LL, std::min<long long>(sms, p.grid) / segs));
+  while (C > 1 && pair_active_clusters(C, smem) < std::min<long long>(segs, sms / C)) --C;
+  if (pair_active_clusters(C, smem) < 1) return BD_ERR_UNSUPPORTED;
+  CUtensorMap mkp, mvp, mkb, mvb, mq;
+  if (!pair_maps(p, mkp, mvp, mkb, mvb, mq)) return BD_ERR_CUDA;
+  const cudaError_t e =
+      launch_pdl_cluster(attn_pair_kernel<true>, dim3((unsigned)(segs * C)), dim3(kThreads), smem,
+                         st, dim3(C, 1, 1), mkp, mvp, mkb, mvb, mq, p, C, Tm);
   count_launches(1);
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }

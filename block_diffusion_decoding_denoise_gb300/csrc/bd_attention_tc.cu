@@ -636,7 +636,7 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
   __syncthreads();
 }
 
-// Block attention for small problems, one launch, no partials in global memory.
+// Block attention for small problems, one launch (cluster form).
 //
 // A cluster of C CTAs works on one segment (sequence b, KV head g).  The
 // segment's tiles are numbered on a grid fixed by max_ctx: u = 0 .. Tm - 1
@@ -646,12 +646,14 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
 // on ctx, so the producer issues its loads of the block's tokens, of ctx and
 // of the range's page ids together (one memory latency before the first TMA),
 // and the consumers load their Q rows before the first tile lands.  At the
-// end every CTA leaves its piece's state (m in base-2 units, l, O) in its own
-// shared memory; after a cluster barrier CTA r merges rows [r R / C,
-// (r + 1) R / C) of all C pieces through distributed shared memory,
+// end every CTA writes its piece's state (m in base-2 units, l, O) to its
+// slot of the workspace; after a cluster barrier CTA r merges rows
+// [r R / C, (r + 1) R / C) of the C pieces from L2,
 //   out = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k,
-// and writes them as bf16.  A second cluster barrier keeps every CTA's pieces
-// alive until the other CTAs have read them.
+// and writes them as bf16.  (Reading the pieces straight from the other CTAs'
+// shared memory was measured slower: about 2 us per row group of 12 to 16
+// remote loads per lane.)  With C == 1 the piece is the segment and is
+// written as the output.
 constexpr int kMaxCluster = 16;
 
 template <int D, int RG, int KH>
@@ -864,12 +866,15 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
       if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
     }
   }
-  __syncthreads();                             // stage memory free: pieces and exchange go there
+  __syncthreads();                             // stage memory free: the key-half exchange goes there
 
-  // this CTA's piece: O [R][D] fp32, then (m in base-2 units, l) [R][2]
-  float *c_o = reinterpret_cast<float *>(smem);
-  float *c_ml = c_o + (size_t)R * D;
-  float *xchg = c_ml + 2 * (size_t)R;
+  // This CTA's piece: with C == 1 it is the whole segment and is written as
+  // the output; otherwise O [R][D] fp32 goes to slot blockIdx.x of sk_o and
+  // (m in base-2 units, l) [R][2] to sk_ml, and after a cluster barrier
+  // (release/acquire at cluster scope) CTA rank r merges rows [r R / C,
+  // (r + 1) R / C) of the C pieces of its cluster.
+  float *xchg = reinterpret_cast<float *>(smem);
+  const bool active = *active_flag != 0;
   if (warp > 0) {
     if (KH == 2) merge_key_halves<D>(xchg, rg, kh, lane, sl2, o, m_run, l_run);
     if (kh == 0) {
@@ -878,73 +883,90 @@ __global__ void __launch_bounds__((RG * KH + 1) * 32, 1)
         float ls = l_run[i] + __shfl_xor_sync(0xffffffffu, l_run[i], 1);
         ls += __shfl_xor_sync(0xffffffffu, ls, 2);
         const int r = rg * 16 + gid + 8 * i;
-        if (r < R) {
+        if (r >= R) continue;
+        if (C == 1) {
+          if (!active) continue;
+          const float inv = ls > 0.f ? 1.f / ls : 0.f;
+          const int qi = r / group, h = g * group + r % group;
+          __nv_bfloat16 *out =
+              static_cast<__nv_bfloat16 *>(p.out) + (((size_t)b * L + qi) * p.hq + h) * D;
 #pragma unroll
           for (int j = 0; j < DN; ++j)
-            *reinterpret_cast<float2 *>(c_o + (size_t)r * D + 8 * j + tig * 2) =
-                make_float2(o[j][2 * i], o[j][2 * i + 1]);
+            *reinterpret_cast<uint32_t *>(out + 8 * j + tig * 2) =
+                pack_bf16(o[j][2 * i] * inv, o[j][2 * i + 1] * inv);
+        } else {
+          const size_t prow = (size_t)blockIdx.x * R + r;
+          if (m_run[i] != -INFINITY) {
+#pragma unroll
+            for (int j = 0; j < DN; ++j)
+              *reinterpret_cast<float2 *>(p.sk_o + prow * D + 8 * j + tig * 2) =
+                  make_float2(o[j][2 * i], o[j][2 * i + 1]);
+          }
           if (tig == 0)
-            *reinterpret_cast<float2 *>(c_ml + 2 * r) = make_float2(m_run[i] * sl2, ls);
+            *reinterpret_cast<float2 *>(p.sk_ml + prow * 2) = make_float2(m_run[i] * sl2, ls);
         }
       }
     }
   }
-  cluster_sync();                              // every piece of the cluster is written
-
-  if (*active_flag) {
-    const int r_begin = (int)((long long)rank * R / C), r_end = (int)((long long)(rank + 1) * R / C);
-    for (int r = r_begin + warp; r < r_end; r += NW + 1) {
-      float2 ml = make_float2(-INFINITY, 0.f);
-      if (lane < C) ml = ld_cluster_f2(map_shared(smem_u32(c_ml + 2 * r), lane));
-      float v[kMaxCluster][DPL];
-      const uint32_t src = smem_u32(c_o + (size_t)r * D + lane * DPL);
+  if (C > 1) {
+    cluster_sync();                            // every piece of the cluster is written
+    if (active) {
+      const size_t first = (size_t)blockIdx.x - rank;   // CTA of rank 0
+      const int r_begin = (int)((long long)rank * R / C), r_end = (int)((long long)(rank + 1) * R / C);
+      for (int r = r_begin + warp; r < r_end; r += NW + 1) {
+        float2 ml = make_float2(-INFINITY, 0.f);
+        if (lane < C)
+          ml = __ldcg(reinterpret_cast<const float2 *>(p.sk_ml + ((first + lane) * R + r) * 2));
+        float mx = ml.x;
 #pragma unroll
-      for (int k = 0; k < kMaxCluster; ++k) {
-        if (k < C) {
-          if constexpr (DPL == 4) {
-            const float4 x = ld_cluster_f4(map_shared(src, k));
-            v[k][0] = x.x;
-            v[k][1] = x.y;
-            v[k][2] = x.z;
-            v[k][3] = x.w;
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float w = (lane < C && ml.x != -INFINITY) ? exp2f(ml.x - mx) : 0.f;
+        float l = w * ml.y;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+        float v[kMaxCluster][DPL];
+        float wk[kMaxCluster];
+#pragma unroll
+        for (int k = 0; k < kMaxCluster; ++k) {
+          wk[k] = __shfl_sync(0xffffffffu, w, k & 31);
+          const float *src = p.sk_o + ((first + k) * R + r) * D + lane * DPL;
+          if (k < C && wk[k] > 0.f) {
+            if constexpr (DPL == 4) {
+              const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
+              v[k][0] = x.x;
+              v[k][1] = x.y;
+              v[k][2] = x.z;
+              v[k][3] = x.w;
+            } else {
+              const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
+              v[k][0] = x.x;
+              v[k][1] = x.y;
+            }
           } else {
-            const float2 x = ld_cluster_f2(map_shared(src, k));
-            v[k][0] = x.x;
-            v[k][1] = x.y;
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) v[k][d] = 0.f;
           }
         }
-      }
-      float mx = ml.x;
+        float acc[DPL];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float w = (lane < C && ml.x != -INFINITY) ? exp2f(ml.x - mx) : 0.f;
-      float l = w * ml.y;
+        for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-      float acc[DPL];
+        for (int k = 0; k < kMaxCluster; ++k)
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
-#pragma unroll
-      for (int k = 0; k < kMaxCluster; ++k) {
-        if (k < C) {
-          const float wk = __shfl_sync(0xffffffffu, w, k);
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) acc[d] = fmaf(wk, v[k][d], acc[d]);
+          for (int d = 0; d < DPL; ++d) acc[d] = fmaf(wk[k], v[k][d], acc[d]);
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int qi = r / group, h = g * group + r % group;
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) +
+                             (((size_t)b * L + qi) * p.hq + h) * D + lane * DPL;
+        if constexpr (DPL == 4) {
+          *reinterpret_cast<uint2 *>(out) =
+              make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv));
+        } else {
+          *reinterpret_cast<uint32_t *>(out) = pack_bf16(acc[0] * inv, acc[1] * inv);
         }
-      }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int qi = r / group, h = g * group + r % group;
-      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) +
-                           (((size_t)b * L + qi) * p.hq + h) * D + lane * DPL;
-      if constexpr (DPL == 4) {
-        *reinterpret_cast<uint2 *>(out) =
-            make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv));
-      } else {
-        *reinterpret_cast<uint32_t *>(out) = pack_bf16(acc[0] * inv, acc[1] * inv);
       }
     }
   }
-  cluster_sync();                              // no CTA leaves while its piece is being read
 }
 
 // TMA maps of one call: the pool as [page][Hkv][64][D] and the block's keys
@@ -998,8 +1020,8 @@ bd_status launch(const AttnParams &p, cudaStream_t st) {
 
 
 // Shared memory of attn_cluster_kernel: S stages of K and V, the control
-// block, and the alignment slack; the stages must also hold the piece and the
-// key-half exchange at the end.
+// block, and the alignment slack; the stages also hold the key-half exchange
+// at the end.
 template <int D, int RG, int KH>
 bool cluster_layout(int R, int *S_out, size_t *smem_out) {
   constexpr int TILE = (D / 64) * kHalfBytes;
@@ -1007,8 +1029,7 @@ bool cluster_layout(int R, int *S_out, size_t *smem_out) {
   constexpr size_t kOptin = 227 * 1024;
   const size_t ctrl = kMaxStages * (2 * sizeof(uint64_t) + sizeof(TileMeta)) + 16;
   const int S = (int)std::min<size_t>(kMaxStages, (kOptin - 1024 - ctrl) / (2 * TILE));
-  const size_t piece = (size_t)R * D * 4 + (size_t)R * 2 * 4 + kXchgBytes;
-  if (S < 2 || piece > (size_t)S * 2 * TILE) return false;
+  if (S < 2 || kXchgBytes > (size_t)S * 2 * TILE) return false;
   *S_out = S;
   *smem_out = (size_t)S * 2 * TILE + ctrl + 1024;
   return true;
@@ -1060,10 +1081,12 @@ bd_status launch_cluster(const AttnParams &p, cudaStream_t st) {
   size_t smem;
   if (!cluster_layout<D, RG, KH>(R, &S, &smem)) return BD_ERR_UNSUPPORTED;
   const long long segs = (long long)p.batch * p.hkv;
-  if (segs > (1LL << 24)) return BD_ERR_UNSUPPORTED;
+  if (segs > (1LL << 24) || !p.sk_o || !p.sk_ml || p.grid < 1) return BD_ERR_UNSUPPORTED;
   const int sms = std::max(1, dev_info().sms);
   const int Tm = (p.max_ctx + kPageRows - 1) / kPageRows + 1;
-  int C = (int)std::min<long long>(std::min(kMaxCluster, Tm), std::max(1LL, sms / segs));
+  // pieces (C > 1) take one R-row slot of sk_o / sk_ml per CTA: segs * C <= grid
+  int C = (int)std::min<long long>(std::min(kMaxCluster, Tm),
+                                   std::max(1LL, std::min<long long>(sms, p.grid) / segs));
   while (C > 1 && active_clusters<D, RG, KH>(C, smem) < std::min<long long>(segs, sms / C)) --C;
   if (active_clusters<D, RG, KH>(C, smem) < 1) return BD_ERR_UNSUPPORTED;
   CUtensorMap mkp, mvp, mkb, mvb;

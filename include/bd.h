@@ -462,8 +462,10 @@ typedef enum {
   BD_ATTN_PAIR = 1,      /* tcgen05 head-pair kernel, also on small problems */
   BD_ATTN_MMA = 2,       /* mma.sync kernel (bf16), tile ranges or splits   */
   BD_ATTN_SIMT = 3,      /* SIMT kernel                                     */
-  BD_ATTN_CLUSTER = 4    /* cluster-per-segment kernel (bf16), also on      *
-                          * large problems                                  */
+  BD_ATTN_CLUSTER = 4,   /* mma.sync kernel, one cluster per segment (bf16), *
+                          * also on large problems                          */
+  BD_ATTN_PAIR_CLUSTER = 5 /* tcgen05 head-pair kernel, one cluster per head  *
+                            * pair, also on large problems                   */
 } bd_attention_kernel;
 
 bd_status bd_debug_force_attention_kernel(int32_t which);

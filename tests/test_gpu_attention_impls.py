@@ -9,9 +9,11 @@ that does not support a shape falls back to the one the shape picks).
 - "pair" runs the head-pair kernel on every problem.  On small ones its tile
   ranges give more CTAs than tiles and many pieces per segment, all merged
   inside the launch.
-- "cluster" runs the cluster kernel on every problem.  On sdar_b1 it runs 16-CTA
-  clusters.  On serving_b64 it runs one CTA per segment, with up to 193 tiles,
-  so its page ids arrive in several 32-tile chunks.
+- "cluster" and "pair_cluster" run the cluster forms of the mma.sync and
+  head-pair kernels on every problem.  On sdar_b1 they run clusters of up to
+  16 CTAs per segment.  On serving_b64 they run one CTA per segment, with up to
+  193 tiles, so the page ids past the first 32 come from the page table one by
+  one.
 """
 import numpy as np
 import pytest
@@ -37,7 +39,7 @@ def _lib():
     bd.load()
 
 
-@pytest.fixture(params=["auto", "pair", "mma", "simt", "cluster"])
+@pytest.fixture(params=["auto", "pair", "mma", "simt", "cluster", "pair_cluster"])
 def impl(request):
     bd.bd_debug_force_attention_kernel(request.param)
     yield request.param
