@@ -87,6 +87,33 @@ __device__ __forceinline__ float4 load_bf16x4(const __nv_bfloat16 *src) {
 // (4 * kMaxVec values per thread, elements f = 4 * (threadIdx.x + i * 256)).
 constexpr int kMaxVec = 4;   // hidden <= 4 * 4 * 256 = 4096
 
+// The finishing kernels sum the split-K partials in split order, loading up to
+// kSplitGroup of them at once so that the sum costs one memory latency per
+// group instead of one per split.
+constexpr int kSplitGroup = 8;
+
+__device__ __forceinline__ void add4(float4 &a, const float4 &b) {
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+}
+
+// acc += partial[s][off] for s = 0 .. splits - 1 (stride sstride floats), in order.
+__device__ __forceinline__ void sum_splits(float4 &acc, const float *partial, size_t off,
+                                           size_t sstride, int splits) {
+  for (int s0 = 0; s0 < splits; s0 += kSplitGroup) {
+    float4 pv[kSplitGroup];
+#pragma unroll
+    for (int j = 0; j < kSplitGroup; ++j)
+      if (s0 + j < splits)
+        pv[j] = *reinterpret_cast<const float4 *>(partial + (size_t)(s0 + j) * sstride + off);
+#pragma unroll
+    for (int j = 0; j < kSplitGroup; ++j)
+      if (s0 + j < splits) add4(acc, pv[j]);
+  }
+}
+
 __device__ __forceinline__ void write_norm(const float4 (&vals)[kMaxVec], int nvec, int hidden,
                                            float eps, __nv_bfloat16 *xn_row, float *red) {
   float ss = 0.f;
@@ -154,19 +181,18 @@ __global__ void __launch_bounds__(kRowThreads) out_finish_kernel(const float *pa
   for (int i = 0; i < kMaxVec; ++i) {
     const int f = 4 * (threadIdx.x + i * kRowThreads);
     vals[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i < nvec && f < hidden) {
-      float4 acc = *reinterpret_cast<const float4 *>(x + (size_t)row * hidden + f);
-      for (int s = 0; s < splits; ++s) {
-        const float4 p =
-            *reinterpret_cast<const float4 *>(partial + ((size_t)s * rows + row) * hidden + f);
-        acc.x += p.x;
-        acc.y += p.y;
-        acc.z += p.z;
-        acc.w += p.w;
-      }
-      vals[i] = acc;
-      *reinterpret_cast<float4 *>(x + (size_t)row * hidden + f) = acc;
-    }
+    if (i < nvec && f < hidden) vals[i] = *reinterpret_cast<const float4 *>(x + (size_t)row * hidden + f);
+  }
+  const size_t sstride = (size_t)rows * hidden;
+#pragma unroll
+  for (int i = 0; i < kMaxVec; ++i) {
+    const int f = 4 * (threadIdx.x + i * kRowThreads);
+    if (i < nvec && f < hidden) sum_splits(vals[i], partial, (size_t)row * hidden + f, sstride, splits);
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxVec; ++i) {
+    const int f = 4 * (threadIdx.x + i * kRowThreads);
+    if (i < nvec && f < hidden) *reinterpret_cast<float4 *>(x + (size_t)row * hidden + f) = vals[i];
   }
   write_norm(vals, nvec, hidden, eps, xn + (size_t)row * hidden, red);
 }
@@ -181,13 +207,7 @@ __global__ void __launch_bounds__(256) qkv_finish_kernel(const float *partial, i
   if (e >= (size_t)rows * F) return;
   const int row = (int)(e / F), f = (int)(e % F);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < splits; ++s) {
-    const float4 p = *reinterpret_cast<const float4 *>(partial + ((size_t)s * rows + row) * F + f);
-    acc.x += p.x;
-    acc.y += p.y;
-    acc.z += p.z;
-    acc.w += p.w;
-  }
+  sum_splits(acc, partial, (size_t)row * F + f, (size_t)rows * F, splits);
   __nv_bfloat16 *dst;
   if (f < fq) dst = q + (size_t)row * fq + f;
   else if (f < fq + fk) dst = k + (size_t)row * fk + (f - fq);
@@ -207,19 +227,8 @@ __global__ void __launch_bounds__(256) swiglu_finish_kernel(const float *partial
   const int row = (int)(e / inter), j = (int)(e % inter);
   const size_t F = 2 * (size_t)inter;
   float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
-  for (int s = 0; s < splits; ++s) {
-    const float *base = partial + ((size_t)s * rows + row) * F;
-    const float4 pg = *reinterpret_cast<const float4 *>(base + j);
-    const float4 pu = *reinterpret_cast<const float4 *>(base + inter + j);
-    g.x += pg.x;
-    g.y += pg.y;
-    g.z += pg.z;
-    g.w += pg.w;
-    u.x += pu.x;
-    u.y += pu.y;
-    u.z += pu.z;
-    u.w += pu.w;
-  }
+  sum_splits(g, partial, (size_t)row * F + j, (size_t)rows * F, splits);
+  sum_splits(u, partial, (size_t)row * F + inter + j, (size_t)rows * F, splits);
   const auto silu = [](float x) { return x / (1.f + __expf(-x)); };
   store_bf16x4(act + (size_t)row * inter + j,
                make_float4(silu(g.x) * u.x, silu(g.y) * u.y, silu(g.z) * u.z, silu(g.w) * u.w));
