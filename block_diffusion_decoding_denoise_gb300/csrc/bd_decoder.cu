@@ -301,13 +301,32 @@ __global__ void __launch_bounds__(kPThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctrl->tmem_base;
   pdl_trigger();
+  // The weights do not depend on earlier work on the stream: the first stages'
+  // weight tiles are requested before the dependency wait (their transaction
+  // bytes registered without an arrival, so no stage can complete before its
+  // activation tile, requested after the wait, has landed too).
+  const int pre = min(S, KC);
+  if (warp == 0 && lane == 0) {
+    for (int kc = 0; kc < pre; ++kc) {
+      const uint32_t bar = smem_u32(&ctrl->full[kc]);
+      mbar_expect_tx(bar, kPABytes);
+      tma_load_2d(smem_u32(smem + (size_t)kc * a.stage_bytes), &tmap_w, k0 + kc * kPK,
+                  ft * kPTileF, bar);
+    }
+  }
   pdl_wait();   // x (and the row count) are written by the previous kernel on the stream
   const int rows = a.dev_rows ? min(a.rows, max(0, *a.dev_rows)) : a.rows;
   const int n = min(kPMaxN, rows - r0);     // rows of this pass; none: nothing to do
   const int npad = (n + 15) & ~15;
 
   if (n <= 0) {
-    // pass beyond the row count
+    // pass beyond the row count: let the early weight copies land before leaving
+    if (warp == 0 && lane == 0) {
+      for (int kc = 0; kc < pre; ++kc) {
+        mbar_arrive(smem_u32(&ctrl->full[kc]));
+        mbar_wait(smem_u32(&ctrl->full[kc]), 0);
+      }
+    }
   } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -322,13 +341,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         uint8_t *st = smem + (size_t)s * a.stage_bytes;
         const uint32_t bar = smem_u32(&ctrl->full[s]);
-        mbar_arrive_expect_tx(bar, tx);
-        tma_load_2d(smem_u32(st), &tmap_w, k0 + kc * kPK, ft * kPTileF, bar);
+        if (kc < pre) {                       // weights already requested
+          mbar_arrive_expect_tx(bar, tx - kPABytes);
+        } else {
+          mbar_arrive_expect_tx(bar, tx);
+          tma_load_2d(smem_u32(st), &tmap_w, k0 + kc * kPK, ft * kPTileF, bar);
+        }
         tma_load_2d(smem_u32(st + kPABytes), &tmap_x, k0 + kc * kPK, r0, bar);
       }
       if (kc < KC) {   // aborted: wait (bounded) for the copies still in flight
+        for (int i = kc; i < pre; ++i) mbar_arrive(smem_u32(&ctrl->full[i]));   // weights only
         const int first = kc > S ? kc - S : 0;
-        for (int i = first; i < kc; ++i) mbar_wait(smem_u32(&ctrl->full[i % S]), (i / S) & 1);
+        for (int i = first; i < max(kc, pre); ++i)
+          mbar_wait(smem_u32(&ctrl->full[i % S]), (i / S) & 1);
       }
     }
   } else if (warp == 1) {
