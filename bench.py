@@ -38,18 +38,18 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "committed tokens/sec per denoise loop"
-# DRAM bytes (read + write) of one lmhead_tc_kernel launch at this workload
-# (32 positions, h read in place, two CTAs per SM), from an ncu capture of the
-# current kernel: dram__bytes_read.sum 622.54 MB + dram__bytes_write.sum
-# 2.88 MB.
-LMHEAD_TRAFFIC_BYTES = 622_538_752 + 2_876_928
+# DRAM bytes (read + write) of one lmhead_tc_kernel launch at sdar_b1
+# (32 positions, h read in place, two CTAs per SM): the mean over 26 launches
+# of an ncu launch list of the current kernel, dram__bytes_read.sum 622.55 MB
+# + dram__bytes_write.sum 0.23 MB.
+LMHEAD_TRAFFIC_BYTES = 622_550_725 + 225_526
 # DRAM bytes (read + write) of one attn_pair_kernel launch at longctx_b8 (8
 # sequences x 16384 cached tokens, one layer), from an ncu capture of the
-# current kernel: dram__bytes_read.sum 539.89 MB + dram__bytes_write.sum
-# 4.80 MB, against 540.02 MB of algorithmic bytes for that launch; the decode
+# current kernel: dram__bytes_read.sum 539.88 MB + dram__bytes_write.sum
+# 4.63 MB, against 540.02 MB of algorithmic bytes for that launch; the decode
 # line scales it by its calls' algorithmic bytes (the context grows by one
 # block per block).
-LONGCTX_ATTN_TRAFFIC = (539_888_640 + 4_795_392, 540_016_640)
+LONGCTX_ATTN_TRAFFIC = (539_881_216 + 4_632_576, 540_016_640)
 UNIT = "tokens/s"
 WORKLOAD = "longctx_b8"
 
