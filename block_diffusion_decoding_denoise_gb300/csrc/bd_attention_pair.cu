@@ -90,7 +90,7 @@ struct Smem {
   uint64_t mma_done;
   uint32_t tmem_base;
   volatile int abort_flag;
-  int pid[32];                              // cluster form: page ids of the first 32 tiles
+  int pid[32];                              // page ids of the first piece's first 32 pages
   volatile int active;                      // cluster form: the segment has output to write
 };
 
@@ -252,6 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // cluster form: segment (b, hp) of this cluster, this CTA's tiles
     // [cu0, clast) of it, and the page ids of the first 32 of them in sm.pid
     int cb = 0, chp = 0, cctx = 0, cnpg = 0, cu0 = 0, clast = 0;
+    // page ids of sequence pid_b's pages [pid_u0, pid_u0 + 32), loaded by the
+    // whole warp in one latency (the first piece's pages)
+    int pid_b = -1, pid_u0 = 0;
     if constexpr (kCluster) {
       const int rank = (int)cluster_ctarank();
       const int seg = blockIdx.x / C;
@@ -273,6 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       cnpg = active ? (cctx + kPage - 1) / kPage : 0;
       clast = active ? min(cu1, cnpg + 1) : cu0;
       sm.pid[lane] = pid;
+      pid_b = cb;
+      pid_u0 = cu0;
       if (lane == 0) sm.active = active ? 1 : 0;
       __syncwarp();
     }
@@ -311,6 +316,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         carry += __shfl_sync(0xffffffffu, inc, 31);
       }
     }
+    if (b_first >= 0) {
+      const int u0 = (t_begin - base_first) % tiles_first, u = u0 + lane;
+      sm.pid[lane] = u < tiles_first - 1 ? p.page_table[(size_t)b_first * p.max_pages + u] : -1;
+      pid_b = b_first;
+      pid_u0 = u0;
+      __syncwarp();
+    }
     }
     uint32_t it = 0, pc = 0;
     bool stop = false;
@@ -337,9 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = u_first; u < u_last; ++u, ++it) {
           const uint32_t s = it % kStages, round = it / kStages;
           // the page id is read before the wait, so the wait covers its latency
-          // (cluster form: the first 32 were loaded together up front)
-          const int pg =
-              u < npg ? ((kCluster && u - cu0 < 32) ? sm.pid[u - cu0] : prow[u]) : -1;
+          // (the first piece's first 32 were loaded together up front)
+          const int pg = u < npg ? ((b == pid_b && u >= pid_u0 && u - pid_u0 < 32)
+                                        ? sm.pid[u - pid_u0]
+                                        : prow[u])
+                                 : -1;
           if (sm.abort_flag) return false;
           if (round > 0 && !mbar_wait(smem_u32(&sm.kv_empty[s]), (round - 1) & 1)) {
             fail();
