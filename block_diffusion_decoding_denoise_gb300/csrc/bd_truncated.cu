@@ -41,6 +41,7 @@
 #include <algorithm>
 
 #include "bd_confidence.cuh"
+#include "bd_sm100.cuh"
 
 namespace bd {
 
@@ -66,17 +67,20 @@ __device__ __forceinline__ unsigned long long mass_of(float z, float m) {
   return static_cast<unsigned long long>(static_cast<double>(rel_exp(z, m)) * kMassScale);
 }
 
-// Calls f(v, z_v) for this thread's entries of the row, v ascending: loads
-// are issued in batches of eight (float4 when the row is 16-byte aligned)
-// before any of them is used, so each batch costs one memory latency.
+// Calls f(v, z_v) for this thread's entries of slice `part` of `parts` of the
+// row, v ascending: loads are issued in batches of eight (float4 when the row
+// is 16-byte aligned) before any of them is used, so each batch costs one
+// memory latency.
 template <typename F>
-__device__ __forceinline__ void for_row(const float *__restrict__ l, int V, float it, F &&f) {
+__device__ __forceinline__ void for_row(const float *__restrict__ l, int V, float it, int part,
+                                        int parts, F &&f) {
   constexpr int kBatch = 8;
   const int t = threadIdx.x;
   if ((V & 3) == 0) {
     const float4 *__restrict__ l4 = reinterpret_cast<const float4 *>(l);
-    const int V4 = V >> 2;
-    for (int base = t; base < V4; base += kSelThreads * kBatch) {
+    const int lo4 = (int)((long long)part * (V >> 2) / parts);
+    const int V4 = (int)((long long)(part + 1) * (V >> 2) / parts);
+    for (int base = lo4 + t; base < V4; base += kSelThreads * kBatch) {
       float4 x[kBatch];
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
@@ -95,17 +99,19 @@ __device__ __forceinline__ void for_row(const float *__restrict__ l, int V, floa
       }
     }
   } else {
-    for (int base = t; base < V; base += kSelThreads * kBatch) {
+    const int lo = (int)((long long)part * V / parts);
+    const int hi = (int)((long long)(part + 1) * V / parts);
+    for (int base = lo + t; base < hi; base += kSelThreads * kBatch) {
       float x[kBatch];
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const int i = base + j * kSelThreads;
-        if (i < V) x[j] = __ldg(l + i);
+        if (i < hi) x[j] = __ldg(l + i);
       }
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const int i = base + j * kSelThreads;
-        if (i < V) f(i, x[j] * it);
+        if (i < hi) f(i, x[j] * it);
       }
     }
   }
@@ -212,12 +218,57 @@ __device__ unsigned long long hist_total(const unsigned long long *hist, int nb,
   return total;
 }
 
+// A row is split over a cluster of kSelCluster CTAs, each taking a slice.
+// After every histogram pass each CTA adds up all slices' histograms from
+// the cluster's shared memory into its own copy of the row's histogram
+// (integer sums, so every CTA gets the same values and takes the same
+// digit), and the cluster barriers on both sides keep a CTA from starting the
+// next pass, which overwrites its histogram, while others still read it.
+constexpr int kSelCluster = 4;
+
+__device__ __forceinline__ unsigned long long ld_cluster_u64(uint32_t cluster_addr) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_cluster_s32(uint32_t cluster_addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+__device__ void cluster_sum_hist(const unsigned long long *hist, unsigned long long *ghist, int nb) {
+  sm100::cluster_sync();                      // every slice's histogram is complete
+  for (int b = threadIdx.x; b < nb; b += kSelThreads) {
+    unsigned long long v[kSelCluster];
+    const uint32_t a = sm100::smem_u32(&hist[b]);
+#pragma unroll
+    for (int q = 0; q < kSelCluster; ++q) v[q] = ld_cluster_u64(sm100::map_shared(a, q));
+    unsigned long long sum = 0;
+#pragma unroll
+    for (int q = 0; q < kSelCluster; ++q) sum += v[q];
+    ghist[b] = sum;
+  }
+  sm100::cluster_sync();                      // every CTA has read the others' histograms
+}
+
 constexpr int kCand = 4096;                 // entries a row's candidate list can hold
 constexpr size_t kSelDynSmem = (size_t)kCand * 8 + (size_t)kPrivWords * 4;
 
 __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p, const float *logits,
                                                                    int top_k, float top_p) {
-  __shared__ unsigned long long hist[kBins];
+  __shared__ unsigned long long hist[kBins];    // this slice's histogram
+  __shared__ unsigned long long ghist[kBins];   // the row's (all slices of the cluster)
+  __shared__ float s_max;
+  __shared__ float s_fkb, s_fzb, s_fsum;
+  __shared__ int s_fidx;
   __shared__ unsigned long long scan[kSelThreads / 32];
   __shared__ float red[kSelThreads / 32];
   __shared__ int s_digit, s_n;
@@ -230,7 +281,8 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
   uint32_t *priv_c = priv + (threadIdx.x >> 5) * kBins;       // this warp's count copy
   unsigned long long *priv_m =
       reinterpret_cast<unsigned long long *>(priv) + (threadIdx.x >> 6) * kBins;  // mass copy
-  const int k = blockIdx.x, t = threadIdx.x;
+  const int k = blockIdx.x / kSelCluster, t = threadIdx.x;
+  const int part = (int)sm100::cluster_ctarank();
   const int V = p.vocab;
   pdl_trigger();
   pdl_wait();
@@ -247,14 +299,24 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
   if (use_k) priv_zero(priv);
   __syncthreads();
   float m = -INFINITY;
-  for_row(l, V, it, [&](int, float z) {
+  for_row(l, V, it, part, kSelCluster, [&](int, float z) {
     m = fmaxf(m, z);
     if (use_k) atomicAdd(&priv_c[ordered_key(z) >> kShift[0]], 1u);
   });
   m = block_max(m, red);
+  if (t == 0) s_max = m;
   if (use_k) {
     priv_merge(priv, false, hist);
-    __syncthreads();
+    cluster_sum_hist(hist, ghist, 1 << kWidth[0]);   // also publishes s_max
+  } else {
+    sm100::cluster_sync();
+  }
+  {                                           // the row's max over the slices
+    float gm = -INFINITY;
+    const uint32_t a = sm100::smem_u32(&s_max);
+#pragma unroll
+    for (int q = 0; q < kSelCluster; ++q) gm = fmaxf(gm, ld_cluster_f32(sm100::map_shared(a, q)));
+    m = gm;
   }
 
   // Entries are visited either straight from the row or, when top-k leaves
@@ -268,7 +330,7 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
   int d_next = 0;                             // next top-k digit to resolve
   if (use_k) {
     unsigned long long above;
-    const int d0 = find_from_top(hist, 1 << kWidth[0], (unsigned long long)top_k, above, scan,
+    const int d0 = find_from_top(ghist, 1 << kWidth[0], (unsigned long long)top_k, above, scan,
                                  &s_digit, &s_above);
     if (d0 < 0) {                             // cannot happen for 0 < k < V
       if (t == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
@@ -277,10 +339,10 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
       pmask = (uint32_t)((1 << kWidth[0]) - 1) << kShift[0];
       need = (unsigned long long)top_k - above;
       d_next = 1;
-      if (above + hist[d0] <= (unsigned long long)kCand) {
+      if (above + ghist[d0] <= (unsigned long long)kCand) {
         if (t == 0) s_n = 0;
         __syncthreads();
-        for_row(l, V, it, [&](int v, float z) {
+        for_row(l, V, it, part, kSelCluster, [&](int v, float z) {
           if ((ordered_key(z) >> kShift[0]) >= (uint32_t)d0) {
             const int i = atomicAdd(&s_n, 1);
             if (i < kCand) {
@@ -305,12 +367,10 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
         for (int b = t; b < kBins; b += kSelThreads) hist[b] = 0;
       __syncthreads();
     };
-    auto end_hist = [&](bool mass) {
+    auto end_hist = [&](bool mass, int nb) {
       __syncthreads();
-      if (row) {
-        priv_merge(priv, mass, hist);
-        __syncthreads();
-      }
+      if (row) priv_merge(priv, mass, hist);
+      cluster_sum_hist(hist, ghist, nb);
     };
     // remaining top-k digits
     if (use_k && d_next > 0) {
@@ -325,9 +385,9 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
             else atomicAdd(&hist[bin], 1ull);
           }
         });
-        end_hist(false);
+        end_hist(false, nb);
         unsigned long long above;
-        int dig = find_from_top(hist, nb, need, above, scan, &s_digit, &s_above);
+        int dig = find_from_top(ghist, nb, need, above, scan, &s_digit, &s_above);
         if (dig < 0) {
           if (t == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
           dig = 0;
@@ -354,13 +414,13 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
             else atomicAdd(&hist[bin], mass_of(z, m));
           }
         });
-        end_hist(true);
+        end_hist(true, nb);
         if (d == 0) {                         // total kept mass -> the target
-          pneed = (unsigned long long)ceil((double)top_p * (double)hist_total(hist, nb, scan));
+          pneed = (unsigned long long)ceil((double)top_p * (double)hist_total(ghist, nb, scan));
           if (pneed == 0) pneed = 1;
         }
         unsigned long long above;
-        int dig = find_from_top(hist, nb, pneed, above, scan, &s_digit, &s_above);
+        int dig = find_from_top(ghist, nb, pneed, above, scan, &s_digit, &s_above);
         if (dig < 0) {                        // rounding put the target past the total
           if (t == 0) flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
           dig = 0;
@@ -405,7 +465,7 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
       s_sum[warp] = sum;
     }
     __syncthreads();
-    if (t == 0) {
+    if (t == 0) {                             // this slice's draw and kept mass
       float S = 0.f;
       for (int w = 0; w < kSelThreads / 32; ++w) {
         S += s_sum[w];
@@ -413,6 +473,28 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
           kb = s_kb[w];
           zb = s_zb[w];
           idx = s_idx[w];
+        }
+      }
+      s_fkb = kb;
+      s_fzb = zb;
+      s_fidx = idx;
+      s_fsum = S;
+    }
+    sm100::cluster_sync();
+    if (part == 0 && t == 0) {                // the row's: slices merged in order
+      float S = 0.f;
+      kb = -INFINITY;
+      zb = -INFINITY;
+      idx = 0x7FFFFFFF;
+      for (int q = 0; q < kSelCluster; ++q) {
+        const float qkb = ld_cluster_f32(sm100::map_shared(sm100::smem_u32(&s_fkb), q));
+        const float qzb = ld_cluster_f32(sm100::map_shared(sm100::smem_u32(&s_fzb), q));
+        const int qi = ld_cluster_s32(sm100::map_shared(sm100::smem_u32(&s_fidx), q));
+        S += ld_cluster_f32(sm100::map_shared(sm100::smem_u32(&s_fsum), q));
+        if (qkb > kb || (qkb == kb && qi < idx)) {
+          kb = qkb;
+          zb = qzb;
+          idx = qi;
         }
       }
       SampleState st;
@@ -423,13 +505,14 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
       st.idx = idx < V ? idx : -1;
       p.ws.spartial[k] = st;                  // the only partial of row k
     }
+    sm100::cluster_sync();                    // the slices' results stay until read
   };
   if (use_cand)
     resolve([&](auto &&f) {
       for (int i = t; i < ncand; i += kSelThreads) f(cand_v[i], cand_z[i]);
     }, false);
   else
-    resolve([&](auto &&f) { for_row(l, V, it, f); }, true);
+    resolve([&](auto &&f) { for_row(l, V, it, part, kSelCluster, f); }, true);
 }
 
 // out[k][v] = h[row k] . W[v] in fp32, for the masked rows k < count.
@@ -479,8 +562,10 @@ bd_status trunc_logits_and_select(const ConfParams &p, float *logits, int top_k,
     s = e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
   }
   if (s != BD_OK) return s;
-  const cudaError_t e = launch_pdl(trunc_select_kernel, dim3(rows_max), dim3(kSelThreads),
-                                   kSelDynSmem, st, p, (const float *)logits, top_k, top_p);
+  const cudaError_t e =
+      launch_pdl_cluster(trunc_select_kernel, dim3(rows_max * kSelCluster), dim3(kSelThreads),
+                         kSelDynSmem, st, dim3(kSelCluster, 1, 1), p, (const float *)logits,
+                         top_k, top_p);
   count_launches(1);
   return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
 }
