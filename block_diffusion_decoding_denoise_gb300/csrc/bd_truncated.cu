@@ -25,7 +25,10 @@
 // Kernels:
 //   logits_simt_kernel   one CTA per (masked row, 256 entries): fp32 dot
 //                        products against the row of h staged in smem
-//   trunc_select_kernel  one CTA per masked row: max and the top-k digits,
+//   trunc_select_kernel  one cluster of four CTAs per masked row, each on a
+//                        quarter of the row, their histograms summed through
+//                        the cluster's shared memory after every pass: max and
+//                        the top-k digits,
 //                        the top-p digits, then the restricted Gumbel-max draw
 //                        and the kept mass; writes one sampling state per row
 //                        for conf_commit_kernel.  With top-k, once the first
