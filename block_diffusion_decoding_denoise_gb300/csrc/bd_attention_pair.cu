@@ -859,8 +859,10 @@ constexpr int kMergeMaxPieces = 160;        // pieces of one segment (at most th
 __global__ void __launch_bounds__(kMergeThreads) attn_pair_merge_kernel(const AttnParams p) {
   __shared__ int slots[kMergeMaxPieces];
   __shared__ int active[kMergeMaxPieces];
+  __shared__ int4 active_job[kMergeMaxPieces];
   __shared__ int warp_off[kMergeThreads / 32 + 1];
   __shared__ int npieces;
+  __shared__ long long s_T;
   __shared__ float ml_m[kMergeMaxPieces][kMergeRows], ml_l[kMergeMaxPieces][kMergeRows];
   __shared__ float wts[kMergeMaxPieces][kMergeRows];
   pdl_trigger();
@@ -868,8 +870,16 @@ __global__ void __launch_bounds__(kMergeThreads) attn_pair_merge_kernel(const At
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int group = p.hq / p.hkv, L = p.block_len;
   const long long G = p.grid;                  // CTAs of the attention kernel (<= 160)
-  // the active jobs in CTA order (the same list in every CTA)
-  const bool has = tid < G && p.jobs[(size_t)tid * kJobInts] >= 0;
+  // the active jobs in CTA order (the same list in every CTA); each entry is
+  // read whole in this one pass
+  int4 myjob = make_int4(-1, 0, 0, 0);
+  int myT = 0;
+  if (tid < G) {
+    myjob = *reinterpret_cast<const int4 *>(p.jobs + (size_t)tid * kJobInts);   // seg, c1, b, hp
+    myT = p.jobs[(size_t)tid * kJobInts + 4];
+  }
+  const bool has = tid < G && myjob.x >= 0;
+  if (tid == 0) s_T = myT;                     // every entry holds the same T
   const unsigned bal = __ballot_sync(0xffffffffu, has);
   if (lane == 0) warp_off[warp + 1] = __popc(bal);
   __syncthreads();
@@ -878,17 +888,20 @@ __global__ void __launch_bounds__(kMergeThreads) attn_pair_merge_kernel(const At
     for (int w = 0; w < kMergeThreads / 32; ++w) warp_off[w + 1] += warp_off[w];
   }
   __syncthreads();
-  if (has) active[warp_off[warp] + __popc(bal & ((1u << lane) - 1))] = tid;
+  if (has) {
+    const int pos = warp_off[warp] + __popc(bal & ((1u << lane) - 1));
+    active[pos] = tid;
+    active_job[pos] = myjob;
+  }
   const int nactive = warp_off[kMergeThreads / 32];
   const int items = nactive * (kRows / kMergeRows);
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     __syncthreads();                           // active[] written; last item's data used
     const int j = active[item / (kRows / kMergeRows)];
     const int r0 = (item % (kRows / kMergeRows)) * kMergeRows;
-    const int *jd = p.jobs + (size_t)j * kJobInts;
-    const int4 job = *reinterpret_cast<const int4 *>(jd);   // seg, c1, b, hp
+    const int4 job = active_job[item / (kRows / kMergeRows)];   // seg, c1, b, hp
     const int seg = job.x, c1 = job.y, b = job.z, hp = job.w;
-    const long long T = jd[4];
+    const long long T = s_T;
     if (tid == 0) {                            // the pieces: CTAs j..c1 with tiles
       int n = 0;
       for (int cc = j; cc <= c1 && n < kMergeMaxPieces; ++cc)
