@@ -101,3 +101,10 @@ def test_sequence_without_mask_is_skipped(impl):
     for b in (0, 2):
         err = float(np.abs(got[b] - oracle_attention(s, b, q, kb, vb)).max())
         assert err <= 2e-2, f"{impl}: sequence {b} max-abs error {err}"
+
+
+def test_head_dim_64(impl):
+    # D = 64: the head-pair kernel does not take it (it falls back by shape);
+    # the mma.sync kernels run their 64-column instantiations
+    w = SMALL.with_(head_dim=64)
+    _check(w, [0, 77, 300], impl)
