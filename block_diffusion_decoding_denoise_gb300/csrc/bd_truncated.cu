@@ -229,31 +229,13 @@ __device__ unsigned long long hist_total(const unsigned long long *hist, int nb,
 // next pass, which overwrites its histogram, while others still read it.
 constexpr int kSelCluster = 4;
 
-__device__ __forceinline__ unsigned long long ld_cluster_u64(uint32_t cluster_addr) {
-  unsigned long long v;
-  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(cluster_addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ int ld_cluster_s32(uint32_t cluster_addr) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-  return v;
-}
-
 __device__ void cluster_sum_hist(const unsigned long long *hist, unsigned long long *ghist, int nb) {
   sm100::cluster_sync();                      // every slice's histogram is complete
   for (int b = threadIdx.x; b < nb; b += kSelThreads) {
     unsigned long long v[kSelCluster];
     const uint32_t a = sm100::smem_u32(&hist[b]);
 #pragma unroll
-    for (int q = 0; q < kSelCluster; ++q) v[q] = ld_cluster_u64(sm100::map_shared(a, q));
+    for (int q = 0; q < kSelCluster; ++q) v[q] = sm100::ld_cluster_u64(sm100::map_shared(a, q));
     unsigned long long sum = 0;
 #pragma unroll
     for (int q = 0; q < kSelCluster; ++q) sum += v[q];
@@ -318,7 +300,7 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
     float gm = -INFINITY;
     const uint32_t a = sm100::smem_u32(&s_max);
 #pragma unroll
-    for (int q = 0; q < kSelCluster; ++q) gm = fmaxf(gm, ld_cluster_f32(sm100::map_shared(a, q)));
+    for (int q = 0; q < kSelCluster; ++q) gm = fmaxf(gm, sm100::ld_cluster_f32(sm100::map_shared(a, q)));
     m = gm;
   }
 
@@ -490,10 +472,10 @@ __global__ void __launch_bounds__(kSelThreads) trunc_select_kernel(ConfParams p,
       zb = -INFINITY;
       idx = 0x7FFFFFFF;
       for (int q = 0; q < kSelCluster; ++q) {
-        const float qkb = ld_cluster_f32(sm100::map_shared(sm100::smem_u32(&s_fkb), q));
-        const float qzb = ld_cluster_f32(sm100::map_shared(sm100::smem_u32(&s_fzb), q));
-        const int qi = ld_cluster_s32(sm100::map_shared(sm100::smem_u32(&s_fidx), q));
-        S += ld_cluster_f32(sm100::map_shared(sm100::smem_u32(&s_fsum), q));
+        const float qkb = sm100::ld_cluster_f32(sm100::map_shared(sm100::smem_u32(&s_fkb), q));
+        const float qzb = sm100::ld_cluster_f32(sm100::map_shared(sm100::smem_u32(&s_fzb), q));
+        const int qi = sm100::ld_cluster_s32(sm100::map_shared(sm100::smem_u32(&s_fidx), q));
+        S += sm100::ld_cluster_f32(sm100::map_shared(sm100::smem_u32(&s_fsum), q));
         if (qkb > kb || (qkb == kb && qi < idx)) {
           kb = qkb;
           zb = qzb;
