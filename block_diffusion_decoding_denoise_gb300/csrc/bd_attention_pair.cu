@@ -103,6 +103,19 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, 
       : "memory");
 }
 
+// Whether the phase with the given parity has completed (never suspends).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -462,81 +475,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // MMA1 of tile t needs the tile's K/V stage, MMA2 of tile t the softmax's P
+    // of t.  Each is issued as soon as its inputs are ready (MMA1 first when
+    // both are), so a stage is released once its own MMA2 is done, without
+    // waiting for the next tile to land.
     if (lane == 0) {
       const uint32_t idesc1 = idesc_bf16_f32(kRows, kRows);
       const uint32_t idesc2 = idesc_bf16_f32(kRows, D) | (1u << 16);   // B (V) MN-major
       uint32_t pc = 0;                         // pieces whose Q was consumed
-      // pending MMA2: tile index, its meta, whether it starts a piece, piece index
-      bool have_prev = false, prev_first = false, prev_skip = false, o_init = false;
-      uint32_t prev_t = 0, prev_piece = 0;
-      auto mma2 = [&](uint32_t tp, bool first, bool skip, uint32_t piece) -> bool {
-        if (!mbar_wait(smem_u32(&sm.p_full[tp & 1]), (tp >> 1) & 1)) return false;
-        if (first) {
-          if (piece > 0 && !mbar_wait(smem_u32(&sm.o_empty), (piece - 1) & 1)) return false;
-          o_init = false;
-        }
-        tc_fence_after();
-        if (!skip) {
-          const uint32_t pt = tmem + kColP + 64 * (tp & 1);
-          const uint32_t vb = smem_u32(sm.v[tp % kStages][0]);
+      uint32_t t1 = 0, t2 = 0;                 // next tile of MMA1, of MMA2 (t2 <= t1)
+      // tiles t2..t1-1 awaiting MMA2, 8 bits each at bit 8 (t % 4): the meta
+      // flags (bits 0-3), piece > 0 (bit 4), parity of piece - 1 (bit 5)
+      uint32_t pend = 0;
+      bool ended = false, o_init = false, ok = true;
+      uint32_t idle = 0;
+      uint64_t idle_t0 = 0;
+      while (true) {
+        bool progressed = false;
+        if (!ended && t1 - t2 < 4) {
+          const uint32_t st = t1 % kStages, s = t1 & 1;
+          if (mbar_test_wait(smem_u32(&sm.kv_full[st]), (t1 / kStages) & 1)) {
+            const volatile int *mv = reinterpret_cast<const volatile int *>(&sm.meta[st]);
+            const int flags = mv[3];
+            const bool first = (flags & kFirst) != 0;
+            if (flags & kEnd) {
+              ended = true;
+              progressed = true;
+            } else if ((!first || mbar_test_wait(smem_u32(&sm.q_full), pc & 1)) &&
+                       (t1 < 2 || mbar_test_wait(smem_u32(&sm.s_empty[s]), ((t1 >> 1) - 1) & 1))) {
+              tc_fence_after();
+              if (!(flags & kSkip)) {
+                const uint32_t qa = smem_u32(sm.q[0]);
+                const uint32_t kb = smem_u32(sm.k[st][0]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)           // 16 keys = 8 TMEM columns per step
-            mma_bf16_ts(tmem + kColO, pt + 8 * j, sw128_mnmajor_desc(vb + j * 2048), idesc2,
-                        (o_init || j > 0) ? 1u : 0u);
-          o_init = true;
+                for (int j = 0; j < 8; ++j)
+                  mma_bf16(tmem + s * 128,
+                           sw128_kmajor_desc(qa + (j >> 2) * kHalf + (j & 3) * 32),
+                           sw128_kmajor_desc(kb + (j >> 2) * kHalf + (j & 3) * 32), idesc1,
+                           j > 0 ? 1u : 0u);
+              }
+              mma_commit(smem_u32(&sm.s_full[s]));
+              if (flags & kLast) mma_commit(smem_u32(&sm.q_empty));   // Q free after this MMA1
+              {
+                const uint32_t piece = first ? pc : (pc > 0 ? pc - 1 : 0);
+                const uint32_t e = (uint32_t)(flags & 15) | (piece > 0 ? 16u : 0u) |
+                                   (((piece - 1) & 1u) << 5);
+                const uint32_t sh = 8 * (t1 & 3);
+                pend = (pend & ~(0xFFu << sh)) | (e << sh);
+              }
+              if (first) ++pc;
+              ++t1;
+              progressed = true;
+            }
+          }
         }
-        mma_commit(smem_u32(&sm.kv_empty[tp % kStages]));
-        mma_commit(smem_u32(&sm.o_done));
-        return true;
-      };
-      bool ok = true;
-      for (uint32_t t = 0; ok; ++t) {
-        const uint32_t st = t % kStages, s = t & 1;   // K/V stage, S buffer
-        if (sm.abort_flag || !mbar_wait(smem_u32(&sm.kv_full[st]), (t / kStages) & 1)) {
-          ok = false;
-          break;
-        }
-        const volatile int *mv = reinterpret_cast<const volatile int *>(&sm.meta[st]);
-        const int flags = mv[3];
-        if (flags & kEnd) {
-          if (have_prev && !mma2(prev_t, prev_first, prev_skip, prev_piece)) ok = false;
-          mma_commit(smem_u32(&sm.s_full[s]));   // tells the softmax warps to stop
-          break;
-        }
-        const bool first = (flags & kFirst) != 0, skip = (flags & kSkip) != 0;
-        if (first && !mbar_wait(smem_u32(&sm.q_full), pc & 1)) {
-          ok = false;
-          break;
-        }
-        if (t >= 2 && !mbar_wait(smem_u32(&sm.s_empty[s]), ((t >> 1) - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (!skip) {
-          const uint32_t qa = smem_u32(sm.q[0]);
-          const uint32_t kb = smem_u32(sm.k[st][0]);
+        if (t2 < t1) {
+          const uint32_t e = (pend >> (8 * (t2 & 3))) & 0xFFu;
+          const int flags = (int)(e & 15);
+          const bool first = (flags & kFirst) != 0;
+          if (mbar_test_wait(smem_u32(&sm.p_full[t2 & 1]), (t2 >> 1) & 1) &&
+              (!first || !(e & 16) || mbar_test_wait(smem_u32(&sm.o_empty), (e >> 5) & 1))) {
+            if (first) o_init = false;
+            tc_fence_after();
+            if (!(flags & kSkip)) {
+              const uint32_t pt = tmem + kColP + 64 * (t2 & 1);
+              const uint32_t vb = smem_u32(sm.v[t2 % kStages][0]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            mma_bf16(tmem + s * 128, sw128_kmajor_desc(qa + (j >> 2) * kHalf + (j & 3) * 32),
-                     sw128_kmajor_desc(kb + (j >> 2) * kHalf + (j & 3) * 32), idesc1,
-                     j > 0 ? 1u : 0u);
+              for (int j = 0; j < 8; ++j)         // 16 keys = 8 TMEM columns per step
+                mma_bf16_ts(tmem + kColO, pt + 8 * j, sw128_mnmajor_desc(vb + j * 2048),
+                            idesc2, (o_init || j > 0) ? 1u : 0u);
+              o_init = true;
+            }
+            mma_commit(smem_u32(&sm.kv_empty[t2 % kStages]));
+            mma_commit(smem_u32(&sm.o_done));
+            ++t2;
+            progressed = true;
+          }
         }
-        mma_commit(smem_u32(&sm.s_full[s]));
-        const uint32_t piece = first ? pc : (pc > 0 ? pc - 1 : 0);
-        if (flags & kLast) {
-          mma_commit(smem_u32(&sm.q_empty));     // Q free once this MMA1 is done
-        }
-        if (first) ++pc;
-        if (have_prev && !mma2(prev_t, prev_first, prev_skip, prev_piece)) {
-          ok = false;
+        if (ended && t2 == t1) {
+          mma_commit(smem_u32(&sm.s_full[t1 & 1]));   // tells the softmax warps to stop
           break;
         }
-        have_prev = true;
-        prev_t = t;
-        prev_first = first;
-        prev_skip = skip;
-        prev_piece = piece;
+        if (progressed) {
+          idle = 0;
+        } else if ((++idle & 63) == 0) {       // bounded: no progress for the wait limit
+          const uint64_t now = globaltimer();
+          if (idle == 64) {
+            idle_t0 = now;
+          } else if (sm.abort_flag || now - idle_t0 > kWaitLimitNs) {
+            ok = false;
+            break;
+          }
+        }
       }
       if (!ok) fail();
       // every MMA issued above has completed once mma_done fires
