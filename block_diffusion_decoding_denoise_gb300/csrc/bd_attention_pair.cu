@@ -36,8 +36,11 @@
 //
 // Warp roles (192 threads, one CTA per SM):
 //   warp 0     TMA producer: Q of each piece, K and V of each tile (three stages)
-//   warp 1     TMEM allocator and MMA issuer: MMA1 of tile t, then MMA2 of
-//              tile t - 1 (the softmax of t overlaps MMA2 of t - 1)
+//   warp 1     TMEM allocator and MMA issuer: MMA1 of a tile once its K/V
+//              stage has landed, MMA2 of a tile once the softmax has written
+//              its P, each as soon as it is ready (the softmax of t overlaps
+//              MMA2 of t - 1, and a stage is freed without waiting for the
+//              next tile)
 //   warps 2-5  softmax, O rescale and the output of each piece
 // Every wait is bounded; on expiry the kernel records BD_ERR_TIMEOUT, stops
 // issuing, waits (bounded) for its copies and MMAs, frees TMEM and returns.
