@@ -23,8 +23,10 @@
 // has several times the throughput this HBM-bound loop needs.
 //
 // Work partition: the tiles of (sequence, KV-head pair) segments are laid
-// end to end (a sequence with no masked position has none); CTA c of the
-// persistent grid takes the equal range [c T / G, (c + 1) T / G).  Warp 0 of
+// end to end (a sequence with no masked position has none), each segment
+// preceded by kPieceCost places that hold no tile (the cost of starting a
+// piece); CTA c of the persistent grid takes the equal range
+// [c T / G, (c + 1) T / G) of the T places.  Warp 0 of
 // every CTA finds its range with a warp-wide scan of the sequences' tile
 // counts, so no separate plan launch precedes the kernel.  A segment inside
 // one CTA's range is written as the final output.  A segment cut by range
@@ -73,6 +75,10 @@ constexpr float kLazy = 8.f;                // max moves only beyond 2^8
 constexpr int kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8;
 constexpr int kJobInts = 8;                 // merge job: seg (-1: none), c1, b, hp, T
 constexpr int kMaxCluster = 16;             // cluster form: CTAs per segment
+constexpr int kPieceCost = 3;               // tile-range form: tiles of budget a segment
+                                            // start costs the CTA that takes it (a second
+                                            // piece: its Q, the drain of O, a partial);
+                                            // 0-4 measured, 3 best at 8 x 16384 keys
 constexpr int kPieceStride = D + 4;         // cluster form: floats per piece row in shared
                                             // memory (a thread writing its own row has no
                                             // bank conflicts)
@@ -297,11 +303,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) sm.active = active ? 1 : 0;
       __syncwarp();
     }
-    // the plan: T = all tiles; this CTA's range [t_begin, t_end) and the
-    // sequence holding t_begin (warp-wide passes over the sequences)
+    // the plan: every segment of tl tiles takes tl + kPieceCost places on the
+    // tile line (its first kPieceCost places hold no tile), T = all places;
+    // this CTA's range [t_begin, t_end) of places and the sequence holding
+    // t_begin (warp-wide passes over the sequences)
+    auto vlen = [](int tl) { return tl > 0 ? tl + kPieceCost : 0; };
     if constexpr (!kCluster) {
     for (int b0 = 0; b0 < p.batch; b0 += 32) {
-      int v = (b0 + lane < p.batch) ? npairs * seq_tiles(b0 + lane) : 0;
+      int v = (b0 + lane < p.batch) ? npairs * vlen(seq_tiles(b0 + lane)) : 0;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       T += v;
@@ -313,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int b0 = 0; b0 < p.batch && b_first < 0; b0 += 32) {
         const int b = b0 + lane;
         const int tl = b < p.batch ? seq_tiles(b) : 0;
-        const int v = npairs * tl;
+        const int v = npairs * vlen(tl);
         int inc = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -333,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (b_first >= 0) {
-      const int u0 = (t_begin - base_first) % tiles_first, u = u0 + lane;
+      const int u0 = max(0, (t_begin - base_first) % vlen(tiles_first) - kPieceCost);
+      const int u = u0 + lane;
       sm.pid[lane] = u < tiles_first - 1 ? p.page_table[(size_t)b_first * p.max_pages + u] : -1;
       pid_b = b_first;
       pid_u0 = u0;
@@ -426,28 +436,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (b_first >= 0) {
         int b = b_first, base = base_first, tiles = tiles_first;
         for (int t = t_begin; t < t_end && !stop;) {
-          while (b < p.batch - 1 && t >= base + npairs * tiles) {
-            base += npairs * tiles;
+          while (b < p.batch - 1 && t >= base + npairs * vlen(tiles)) {
+            base += npairs * vlen(tiles);
             ++b;
             tiles = seq_tiles(b);
           }
-          if (tiles <= 0 || t < base || t >= base + npairs * tiles) {
+          if (tiles <= 0 || t < base || t >= base + npairs * vlen(tiles)) {
             flag_error(p.dev_status, BD_ERR_DEVICE_CHECK);
             break;
           }
-          const int hp = (t - base) / tiles, u0 = (t - base) % tiles;
-          const int seg0 = base + hp * tiles;
-          const int u1 = min(seg0 + tiles, t_end) - seg0;
-          const int seg = b * npairs + hp;
-          const bool whole = u0 == 0 && u1 == tiles;
-          if (!whole && u0 == 0) {               // this CTA holds the cut segment's first
-            job[0] = seg;                        // tile: it records the merge job
-            job[1] = sk_cta_of(seg0 + tiles - 1, T, G);
-            job[2] = b;
-            job[3] = hp;
+          const int vl = vlen(tiles);
+          const int hp = (t - base) / vl;
+          const int seg0 = base + hp * vl;        // the segment's first place
+          const int vend = min(seg0 + vl, t_end);
+          const int u0 = max(0, t - seg0 - kPieceCost), u1 = vend - seg0 - kPieceCost;
+          if (u1 > u0) {                         // the range holds tiles [u0, u1) of it
+            const int seg = b * npairs + hp;
+            const bool whole = u0 == 0 && u1 == tiles;
+            if (!whole && u0 == 0) {             // this CTA holds the cut segment's first
+              job[0] = seg;                      // tile: it records the merge job
+              job[1] = sk_cta_of(seg0 + kPieceCost + tiles - 1, T, G);
+              job[2] = b;
+              job[3] = hp;
+            }
+            stop = !emit(b, hp, p.ctx_len[b], tiles - 1, u0, u1, 0, L, seg, whole ? -1 : seg + c);
           }
-          stop = !emit(b, hp, p.ctx_len[b], tiles - 1, u0, u1, 0, L, seg, whole ? -1 : seg + c);
-          t = seg0 + u1;
+          t = vend;
         }
       }
       {                                        // every CTA writes its entry
