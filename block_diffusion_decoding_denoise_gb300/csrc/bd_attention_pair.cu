@@ -949,7 +949,11 @@ __global__ void __launch_bounds__(kMergeThreads) attn_pair_merge_kernel(const At
     const int4 job = active_job[item / (kRows / kMergeRows)];   // seg, c1, b, hp
     const int seg = job.x, c1 = job.y, b = job.z, hp = job.w;
     const long long T = s_T;
-    if (tid == 0) {                            // the pieces: CTAs j..c1 with tiles
+    if (T >= G) {                              // the pieces: CTAs j..c1, every range
+      const int n = min(c1 - j + 1, kMergeMaxPieces);   // non-empty
+      for (int k = tid; k < n; k += kMergeThreads) slots[k] = seg + j + k;
+      if (tid == 0) npieces = n;
+    } else if (tid == 0) {                     // the CTAs j..c1 with tiles
       int n = 0;
       for (int cc = j; cc <= c1 && n < kMergeMaxPieces; ++cc)
         if (range_nonempty(cc, T, G)) slots[n++] = seg + cc;
