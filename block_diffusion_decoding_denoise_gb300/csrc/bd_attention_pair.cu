@@ -228,14 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  // finite contents everywhere a masked key can reach MMA2 (P = 0 times a V
-  // row that no TMA load has written yet must not be 0 * NaN)
-  {
-    int4 *z = reinterpret_cast<int4 *>(&sm.k[0][0][0]);
-    const int n = (int)((sizeof(sm.k) + sizeof(sm.v)) / sizeof(int4));
-    for (int i = threadIdx.x; i < n; i += blockDim.x) z[i] = make_int4(0, 0, 0, 0);
-  }
-  fence_proxy_async();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -721,6 +713,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * factor);
           tmem_st_32x32b_x16(lane_base + kColO + c * 16, r);
         }
+      }
+      if (!(m.flags & kSkip) && (m.lo > 0 || m.hi < 64)) {
+        // A masked key has P = 0, but 0 * NaN is NaN: the V rows of the tile's
+        // keys outside [lo, hi) (pool rows past the context, the rows of the
+        // block tile's stage that its copy did not write) are zeroed, both
+        // heads and both halves of D, before MMA2 reads the stage.
+        uint8_t *vs = &sm.v[t % kStages][0][0];
+        for (int i = threadIdx.x - 64; i < 64 * 32; i += 128) {
+          const int r = i >> 5, c = i & 31;      // key, 16-byte chunk of its 512 bytes
+          if (r < m.lo || r >= m.hi)
+            *reinterpret_cast<int4 *>(vs + (c >> 4) * kHalf + ((c >> 3) & 1) * kHeadOff +
+                                      r * 128 + (c & 7) * 16) = make_int4(0, 0, 0, 0);
+        }
+        fence_proxy_async();                   // before MMA2 (async proxy) reads the rows
       }
       tmem_st_wait();
       tc_fence_before();

@@ -91,7 +91,9 @@ typedef struct {
  * later block exists at decode time, so no further mask applies.
  *
  *   ctx_len   [batch] int32, device: cached tokens per sequence (<= max_ctx and
- *             <= max_pages_per_seq * page_size, checked on the device).
+ *             <= max_pages_per_seq * page_size, checked on the device).  Pool
+ *             rows past a sequence's context (the rest of its last page) may
+ *             hold anything, NaN included: they never reach the output.
  *   tokens    [batch][block_len] int32 or NULL.  When given, a sequence with
  *             no BD_MASK position is skipped (its out rows are not written).
  *   q         [batch][block_len][num_q_heads][head_dim]

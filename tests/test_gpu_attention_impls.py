@@ -57,6 +57,37 @@ def _check(w, plen, impl, blk=0):
     assert worst <= 2e-2, f"{impl}: max-abs error {worst}"
 
 
+def _poison_unused_rows(s):
+    """NaN in every pool row that holds no cached token: the rest of each
+    sequence's last page and every page no sequence uses."""
+    cache = s.cache
+    valid = torch.zeros(cache.k.shape[0], cache.k.shape[2], dtype=torch.bool)
+    for b, n in enumerate(s.plen):
+        pos = np.arange(int(n))
+        pages = cache.page_table_np[b][pos // bd.BD_PAGE_SIZE]
+        valid[torch.from_numpy(pages.astype(np.int64)),
+              torch.from_numpy((pos % bd.BD_PAGE_SIZE).astype(np.int64))] = True
+    bad = (~valid).to(cache.k.device)[:, None, :, None].expand_as(cache.k)
+    cache.k.masked_fill_(bad, float("nan"))
+    cache.v.masked_fill_(bad, float("nan"))
+
+
+def test_nan_in_unused_pool_rows(impl):
+    # A masked key has probability zero, and zero times NaN is NaN: no kernel
+    # may let a pool row past a sequence's context reach its output (the
+    # tails of partial last pages: 77, 130 and 1 tokens; the block tile of 32
+    # keys in a 64-row stage)
+    w = SMALL.with_(batch=4)
+    s = make_cache(w, 0, [77, 300, 1, 130])
+    _poison_unused_rows(s)
+    q, kb, vb = wl.block_qkv(w, 0)
+    got = gpu_attention(s, q, kb, vb)
+    assert np.isfinite(got).all(), f"{impl}: non-finite output"
+    worst = max(float(np.abs(got[b] - oracle_attention(s, b, q, kb, vb)).max())
+                for b in range(w.batch))
+    assert worst <= 2e-2, f"{impl}: max-abs error {worst}"
+
+
 def test_ragged_prefixes(impl):
     # 0 (block only), 77 (odd page count, partial page), 300
     _check(SMALL, [0, 77, 300], impl)
