@@ -720,11 +720,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // block tile's stage that its copy did not write) are zeroed, both
         // heads and both halves of D, before MMA2 reads the stage.
         uint8_t *vs = &sm.v[t % kStages][0][0];
-        for (int i = threadIdx.x - 64; i < 64 * 32; i += 128) {
-          const int r = i >> 5, c = i & 31;      // key, 16-byte chunk of its 512 bytes
-          if (r < m.lo || r >= m.hi)
-            *reinterpret_cast<int4 *>(vs + (c >> 4) * kHalf + ((c >> 3) & 1) * kHeadOff +
-                                      r * 128 + (c & 7) * 16) = make_int4(0, 0, 0, 0);
+        const int nlo = max(0, m.lo), hi0 = max(nlo, min(64, m.hi));
+        const int nz = nlo + (64 - hi0);         // keys [0, lo) and [hi, 64)
+        for (int i = threadIdx.x - 64; i < nz * 32; i += 128) {
+          const int j = i >> 5, c = i & 31;      // j-th zeroed key, 16-byte chunk of its 512 bytes
+          const int r = j < nlo ? j : hi0 + (j - nlo);
+          *reinterpret_cast<int4 *>(vs + (c >> 4) * kHalf + ((c >> 3) & 1) * kHeadOff + r * 128 +
+                                    (c & 7) * 16) = make_int4(0, 0, 0, 0);
         }
         fence_proxy_async();                   // before MMA2 (async proxy) reads the rows
       }
