@@ -184,6 +184,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Zero the V rows of keys outside [lo, hi) in one stage (both heads, both
+// halves of D; a key's row is 128 bytes in each of the four 8 KB blocks),
+// shared by the 128 softmax threads (tid 0..127); then order the writes before
+// MMA2 (async proxy) reads the stage.  Kept out of line: it runs for partial
+// tiles only, and the softmax loop keeps its registers.
+__device__ __noinline__ void zero_v_rows(uint8_t *vs, int lo, int hi, int tid) {
+  const int nlo = max(0, lo), hi0 = max(nlo, min(64, hi));
+  const int nz = nlo + (64 - hi0);               // keys [0, lo) and [hi, 64)
+  for (int i = tid; i < nz * 32; i += 128) {
+    const int j = i >> 5, c = i & 31;            // j-th zeroed key, 16-byte chunk of its 512 bytes
+    const int r = j < nlo ? j : hi0 + (j - nlo);
+    *reinterpret_cast<int4 *>(vs + (c >> 4) * kHalf + ((c >> 3) & 1) * kHeadOff + r * 128 +
+                              (c & 7) * 16) = make_int4(0, 0, 0, 0);
+  }
+  fence_proxy_async();
+}
+
 template <bool kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap mk_pool,
@@ -719,16 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // keys outside [lo, hi) (pool rows past the context, the rows of the
         // block tile's stage that its copy did not write) are zeroed, both
         // heads and both halves of D, before MMA2 reads the stage.
-        uint8_t *vs = &sm.v[t % kStages][0][0];
-        const int nlo = max(0, m.lo), hi0 = max(nlo, min(64, m.hi));
-        const int nz = nlo + (64 - hi0);         // keys [0, lo) and [hi, 64)
-        for (int i = threadIdx.x - 64; i < nz * 32; i += 128) {
-          const int j = i >> 5, c = i & 31;      // j-th zeroed key, 16-byte chunk of its 512 bytes
-          const int r = j < nlo ? j : hi0 + (j - nlo);
-          *reinterpret_cast<int4 *>(vs + (c >> 4) * kHalf + ((c >> 3) & 1) * kHeadOff + r * 128 +
-                                    (c & 7) * 16) = make_int4(0, 0, 0, 0);
-        }
-        fence_proxy_async();                   // before MMA2 (async proxy) reads the rows
+        zero_v_rows(&sm.v[t % kStages][0][0], m.lo, m.hi, threadIdx.x - 64);
       }
       tmem_st_wait();
       tc_fence_before();
