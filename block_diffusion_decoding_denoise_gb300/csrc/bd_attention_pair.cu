@@ -15,7 +15,9 @@
 //         own head, running max kept in base-2 units and moved only when a new
 //         maximum exceeds it by more than 8 (then O's row is rescaled in
 //         TMEM), P = exp2(s - m) as bf16 written to TMEM (the thread's own
-//         lane); the other head's 64 keys of P stay zero
+//         lane); the other head's 64 keys of P stay zero.  For a partial
+//         tile the V rows of the keys outside its valid range are zeroed
+//         first (they may hold anything, and 0 * NaN is NaN)
 //   MMA2  O[row][d]   += P[row][key] . V[key][d]    M = 128, N = D, K = 128 keys
 //         (P read from TMEM, V from shared memory MN-major); O stays in TMEM
 //         for the whole piece
